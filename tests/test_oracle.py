@@ -1,0 +1,260 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test is chosen so that a plausible slip in the oracle -- a transposed
+operand, a wrong index or leading dimension, a dropped or repeated k term, a
+sign error, a wrong 16-bit decoder, a wrong |A||B| -- fails at least one of
+them. None of them re-types the oracle's own loop.
+"""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from dense_gemm_14_gb300 import inputs
+
+
+def f32(x):
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+# ----------------------------------------------------------------- decoders
+
+def test_decode_f16_all_patterns_match_numpy(oracle_mod):
+    """Every binary16 pattern, including subnormals, infinities and NaN, decodes
+    like numpy's independent float16 implementation."""
+    bits = np.arange(65536, dtype=np.uint16).reshape(256, 256)
+    got = oracle_mod.decode(bits, "f16")
+    want = bits.view(np.float16).astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    m = ~np.isnan(want)
+    assert np.array_equal(got[m], want[m])
+    assert np.array_equal(np.signbit(got[m]), np.signbit(want[m]))
+
+
+def test_decode_bf16_all_patterns_match_torch(oracle_mod):
+    """Every bfloat16 pattern decodes like torch's bfloat16 -> float32 cast."""
+    bits = np.arange(65536, dtype=np.uint16).reshape(256, 256)
+    got = oracle_mod.decode(bits, "bf16")
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    m = ~np.isnan(want)
+    assert np.array_equal(got[m], want[m])
+
+
+@pytest.mark.parametrize("bits,value", [
+    (0x3C00, 1.0), (0xC000, -2.0), (0x0001, 2.0 ** -24), (0x03FF, 1023 * 2.0 ** -24),
+    (0x0400, 2.0 ** -14), (0x7BFF, 65504.0), (0x3555, 0.333251953125),
+])
+def test_decode_f16_textbook_values(oracle_mod, bits, value):
+    got = oracle_mod.decode(np.array([[bits]], dtype=np.uint16), "f16")[0, 0]
+    assert got == value
+
+
+@pytest.mark.parametrize("bits,value", [
+    (0x3F80, 1.0), (0xC000, -2.0), (0x4049, 3.140625), (0x0001, 2.0 ** -133),
+    (0x7F7F, 3.3895313892515355e38),
+])
+def test_decode_bf16_textbook_values(oracle_mod, bits, value):
+    got = oracle_mod.decode(np.array([[bits]], dtype=np.uint16), "bf16")[0, 0]
+    assert got == value
+
+
+# ----------------------------------------------------------------- structure
+
+def test_identity_right_and_left(oracle_mod):
+    g = np.random.default_rng(1)
+    A = f32(g.uniform(-1, 1, (7, 5)))
+    C, _ = oracle_mod.gemm(A, f32(np.eye(5)))
+    assert np.array_equal(C, A.astype(np.float64))
+    B = f32(g.uniform(-1, 1, (5, 9)))
+    C, _ = oracle_mod.gemm(f32(np.eye(5)), B)
+    assert np.array_equal(C, B.astype(np.float64))
+
+
+def test_permutation_rows_and_columns(oracle_mod):
+    """P @ B permutes the rows of B; A @ Q permutes the columns of A. An operand
+    transposed or an index swapped inside the oracle breaks this."""
+    g = np.random.default_rng(2)
+    perm = g.permutation(6)
+    P = np.zeros((6, 6), np.float32)
+    P[np.arange(6), perm] = 1
+    B = f32(g.uniform(-1, 1, (6, 11)))
+    C, _ = oracle_mod.gemm(P, B)
+    assert np.array_equal(C, B[perm].astype(np.float64))
+    A = f32(g.uniform(-1, 1, (4, 6)))
+    Q = np.zeros((6, 6), np.float32)
+    Q[perm, np.arange(6)] = 1
+    C, _ = oracle_mod.gemm(A, Q)
+    assert np.array_equal(C, A[:, perm].astype(np.float64))
+
+
+def test_selection_non_square(oracle_mod):
+    """A @ S with S picking column sel[j] of A into column j (K != N)."""
+    g = np.random.default_rng(3)
+    A = f32(g.uniform(-1, 1, (5, 8)))
+    sel = np.array([7, 0, 3, 3, 1])
+    S = np.zeros((8, 5), np.float32)
+    S[sel, np.arange(5)] = 1
+    C, _ = oracle_mod.gemm(A, S)
+    assert np.array_equal(C, A[:, sel].astype(np.float64))
+
+
+def test_diagonal_scaling_is_one_product(oracle_mod):
+    g = np.random.default_rng(4)
+    d = f32(g.uniform(-2, 2, 6))
+    B = f32(g.uniform(-1, 1, (6, 7)))
+    C, _ = oracle_mod.gemm(f32(np.diag(d)), B)
+    assert np.array_equal(C, d.astype(np.float64)[:, None] * B.astype(np.float64))
+
+
+# ----------------------------------------------------------------- exact sums
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_integer_matrices_exact(oracle_mod, dtype):
+    """Integer entries in [-4, 4]: the exact product is the int64 matmul."""
+    A_t, B_t = inputs.make_integer(37, 29, 53, 4, dtype=dtype, seed=5)
+    A_i = A_t.to(torch.int64).numpy()
+    B_i = B_t.to(torch.int64).numpy()
+    C, Cabs = oracle_mod.gemm(inputs.host_view(A_t), inputs.host_view(B_t), dtype)
+    assert np.array_equal(C, (A_i @ B_i).astype(np.float64))
+    assert np.array_equal(Cabs, (np.abs(A_i) @ np.abs(B_i)).astype(np.float64))
+
+
+def test_closed_forms(oracle_mod):
+    M, N, K = 9, 13, 17
+    C, Cabs = oracle_mod.gemm(np.ones((M, K), np.float32), np.ones((K, N), np.float32))
+    assert np.all(C == K) and np.all(Cabs == K)
+    a = (np.arange(M) % 7 + 1).astype(np.float32)
+    b = (np.arange(N) % 5 + 1).astype(np.float32)
+    A = np.repeat(a[:, None], K, axis=1)
+    B = np.repeat(b[None, :], K, axis=0)
+    C, _ = oracle_mod.gemm(f32(A), f32(B))
+    assert np.array_equal(C, K * np.outer(a, b).astype(np.float64))
+    # alternating signs cancel exactly: row i of A = (-1)^k, B = ones
+    A = f32(np.tile((-1.0) ** np.arange(16), (3, 1)))
+    C, Cabs = oracle_mod.gemm(A, np.ones((16, 4), np.float32))
+    assert np.all(C == 0) and np.all(Cabs == 16)
+
+
+def test_brute_force_tiny_shapes_fraction(oracle_mod):
+    """All shapes in {1..4}^3 with dyadic entries k/8: compared with exact
+    rational sums (fractions.Fraction), so any rounding, missing term or
+    mis-indexing shows."""
+    g = np.random.default_rng(6)
+    for M, N, K in itertools.product(range(1, 5), repeat=3):
+        A = g.integers(-16, 17, (M, K)) / 8.0
+        B = g.integers(-16, 17, (K, N)) / 8.0
+        C, Cabs = oracle_mod.gemm(f32(A), f32(B))
+        for i in range(M):
+            for j in range(N):
+                exact = sum(Fraction(A[i, k]) * Fraction(B[k, j]) for k in range(K))
+                exact_abs = sum(abs(Fraction(A[i, k]) * Fraction(B[k, j])) for k in range(K))
+                assert C[i, j] == float(exact)
+                assert Cabs[i, j] == float(exact_abs)
+
+
+def test_empty_inner_dimension_is_zero(oracle_mod):
+    C, Cabs = oracle_mod.gemm(np.zeros((3, 0), np.float32), np.zeros((0, 4), np.float32))
+    assert C.shape == (3, 4) and np.all(C == 0) and np.all(Cabs == 0)
+    C, _ = oracle_mod.gemm(np.zeros((0, 5), np.float32), np.zeros((5, 4), np.float32))
+    assert C.shape == (0, 4)
+
+
+def test_leading_dimension_views(oracle_mod):
+    """Strided views (lda > K, ldb > N) give the same result as compact copies."""
+    g = np.random.default_rng(7)
+    Abig = f32(g.uniform(-1, 1, (10, 20)))
+    Bbig = f32(g.uniform(-1, 1, (12, 30)))
+    A, B = Abig[:, :12], Bbig[:, 5:19]
+    C1, _ = oracle_mod.gemm(A, B)
+    C2, _ = oracle_mod.gemm(np.ascontiguousarray(A), np.ascontiguousarray(B))
+    assert np.array_equal(C1, C2)
+
+
+# ----------------------------------------------------------------- library cross-check
+
+@pytest.mark.parametrize("shape", [(64, 96, 128), (257, 129, 300), (512, 64, 513)])
+def test_matches_numpy_float64(oracle_mod, shape):
+    """numpy's float64 matmul is an independent evaluation of the same sum;
+    the two agree to within fp64 rounding of a length-K sum."""
+    M, N, K = shape
+    A_t, B_t = inputs.make(M, N, K, "f32", "normal", 1.0, seed=8)
+    A, B = A_t.numpy(), B_t.numpy()
+    C, Cabs = oracle_mod.gemm(A, B)
+    ref = A.astype(np.float64) @ B.astype(np.float64)
+    assert np.all(np.abs(C - ref) <= 1e-12 * Cabs)
+    assert np.array_equal(Cabs, np.abs(A.astype(np.float64)) @ np.abs(B.astype(np.float64))) or \
+        np.all(np.abs(Cabs - np.abs(A.astype(np.float64)) @ np.abs(B.astype(np.float64))) <= 1e-12 * Cabs)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_16bit_matches_numpy_on_decoded_values(oracle_mod, dtype):
+    A_t, B_t = inputs.make(96, 80, 257, dtype, "normal", 1.0 / 16, seed=9)
+    A64 = A_t.to(torch.float64).numpy()
+    B64 = B_t.to(torch.float64).numpy()
+    C, Cabs = oracle_mod.gemm(inputs.host_view(A_t), inputs.host_view(B_t), dtype)
+    assert np.all(np.abs(C - A64 @ B64) <= 1e-12 * Cabs)
+
+
+def test_entries_agree_with_full_product(oracle_mod):
+    A_t, B_t = inputs.make(70, 90, 110, "f32", "uniform", 1.0, seed=10)
+    A, B = A_t.numpy(), B_t.numpy()
+    C, Cabs = oracle_mod.gemm(A, B)
+    g = np.random.default_rng(11)
+    rows, cols = g.integers(0, 70, 200), g.integers(0, 90, 200)
+    e, ea = oracle_mod.gemm_entries(A, B, rows, cols)
+    assert np.array_equal(e, C[rows, cols]) and np.array_equal(ea, Cabs[rows, cols])
+
+
+def test_thread_count_does_not_change_results(oracle_mod):
+    A_t, B_t = inputs.make(65, 33, 129, "f32", "normal", 1.0, seed=12)
+    C1, _ = oracle_mod.gemm(A_t.numpy(), B_t.numpy(), threads=1)
+    C4, _ = oracle_mod.gemm(A_t.numpy(), B_t.numpy(), threads=4)
+    assert np.array_equal(C1, C4)
+
+
+# ----------------------------------------------------------------- the acceptance check
+
+def test_within_bound_accepts_rounded_oracle_and_rejects_perturbation(oracle_mod):
+    A_t, B_t = inputs.make(40, 50, 300, "f32", "uniform", 1.0, seed=13)
+    C, Cabs = oracle_mod.gemm(A_t.numpy(), B_t.numpy())
+    ok, worst = oracle_mod.within_bound(C.astype(np.float32), C, Cabs, 1e-5)
+    assert ok and worst < 1e-7
+    bad = C.astype(np.float32).astype(np.float64)
+    bad[3, 4] += 2e-5 * Cabs[3, 4]
+    ok, _ = oracle_mod.within_bound(bad, C, Cabs, 1e-5)
+    assert not ok
+    nan = C.copy()
+    nan[0, 0] = np.nan
+    ok, _ = oracle_mod.within_bound(nan, C, Cabs, 1e-5)
+    assert not ok
+
+
+def test_sequential_fp32_sum_fits_the_fp32_bound(oracle_mod):
+    """The fp32 bound 1e-5 * (|A||B|)_ij leaves room for any plain fp32
+    summation order: a sequential float32 sum (the worst common order) over
+    K = 3072 stays well inside it."""
+    A_t, B_t = inputs.make(16, 16, 3072, "f32", "uniform", 1.0, seed=14)
+    A, B = A_t.numpy(), B_t.numpy()
+    C, Cabs = oracle_mod.gemm(A, B)
+    seq = np.zeros((16, 16), np.float32)
+    for k in range(3072):
+        seq = (seq + np.outer(A[:, k], B[k, :]).astype(np.float32)).astype(np.float32)
+    ok, worst = oracle_mod.within_bound(seq, C, Cabs, 1e-5)
+    assert ok and worst < 1e-6
+
+
+def test_inputs_are_seeded_and_shaped():
+    A1, B1 = inputs.make_workload("f32_ragged", M=33, N=17, K=9)
+    A2, B2 = inputs.make_workload("f32_ragged", M=33, N=17, K=9)
+    assert torch.equal(A1, A2) and torch.equal(B1, B2)
+    assert A1.shape == (33, 9) and B1.shape == (9, 17) and A1.dtype == torch.float32
+    A, B = inputs.make_workload("bf16_8192", M=8, N=8, K=8)
+    assert A.dtype == torch.bfloat16
+    A16, _ = inputs.make_workload("f16_8192", M=8, N=8, K=8)
+    assert torch.equal(A.float().half().float() - A16.float(), A.float().half().float() - A16.float())
+    w = inputs.WORKLOADS["bf16_8192"]
+    assert math.isclose(w.sigma, 1 / math.sqrt(8192))
