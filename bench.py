@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""Benchmark: dense GEMM throughput (TFLOP/s = 2MNK / t) on one GB300.
+
+One step is one pass of the whole hot path: an fp32 product at n = 3072 on the
+SIMT kernel (gemm_f32) and a bf16-input / fp32-accumulate product at
+8192^3 on the tcgen05 kernel (gemm_bf16_f32acc), on seeded synthetic inputs
+already resident in HBM. `value` = total FLOPs of the K timed steps / their
+device time (CUDA events on the launching stream). Each kernel's own time is
+taken with events around it and reported in `parts` with its roofline.
+
+Inputs rotate over several copies whose total size exceeds the 129 MB L2, so
+no timed launch finds its operands in L2 from the previous step.
+
+`e2e` is the same metric through the public tensor API with HOST tensors: the
+host->device copy of A and B and the device->host copy of C are inside the
+timed region.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same step on its own GPU
+(replicas); value = FLOPs of all ranks / max time over ranks.
+`--impl reference` times the CPU oracle on the host cores on a bounded sample
+of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (2MNK/t) fp32 n=3072 and bf16 8192³; % of GB300 peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+WORKLOAD_NAME = "fp32 3072^3 (gemm_f32) + bf16->fp32 8192^3 (gemm_bf16_f32acc), one of each per step"
+
+# (workload name, kernel, roofline bound, C-ABI entry name, kernel source file)
+PARTS = [
+    ("f32_3072", "sgemm_simt_kernel", "alu", "gemm_f32", "sgemm_simt.cu"),
+    ("bf16_8192", "hgemm_tc_kernel", "tensor", "gemm_bf16_f32acc", "hgemm_tc.cu"),
+]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="target oracle seconds per part for cpu_baseline")
+    ap.add_argument("--only", choices=[p[0] for p in PARTS], default=None,
+                    help="time one part only (for profiling; not a bench line)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+class Dist:
+    def __init__(self, n_gpus: int):
+        import torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.n_gpus = n_gpus
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in a child process during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(self._path(), "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _path(self):
+        d = os.path.join(ROOT, "gpurun_out")
+        os.makedirs(d, exist_ok=True)
+        return os.path.join(d, f"clocks_rank{self.dev}.csv")
+
+    def stop(self) -> dict:
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self._path()) as f:
+            for line in f:
+                cols = [c.strip() for c in line.split(",")]
+                if len(cols) < 9:
+                    continue
+                try:
+                    sm.append(float(cols[1]))
+                    smax.append(float(cols[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, cols[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def source_sha(fname: str) -> str:
+    h = hashlib.sha256()
+    for f in (fname, "ptx.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "dense_gemm_14_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, src: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, only if it was taken
+    on the current source of the kernel (else null)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel)
+    if not e or e.get("source_sha") != source_sha(src) or e.get("workload") != workload:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def workload_info(name):
+    from dense_gemm_14_gb300 import inputs, roofline
+    w = inputs.WORKLOADS[name]
+    in_b = 4 if w.dtype == "f32" else 2
+    return w, roofline.flops(w.M, w.N, w.K), roofline.ideal_bytes(w.M, w.N, w.K, in_b, 4)
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def time_oracle_sample(name: str, target_s: float, A=None, B=None):
+    """Times the oracle on the first R rows of the named product, R sized so
+    the call takes about target_s seconds. Returns (flops, seconds, rows, threads)."""
+    import oracle
+    from dense_gemm_14_gb300 import inputs, roofline
+    w = inputs.WORKLOADS[name]
+    if A is None:
+        A, B = inputs.make_workload(name)
+    Ah, Bh = inputs.host_view(A), inputs.host_view(B)
+    rows = 8
+    t0 = time.perf_counter()
+    oracle.gemm(Ah[:rows], Bh, w.dtype, with_abs=False)
+    probe = time.perf_counter() - t0
+    rows = int(max(8, min(w.M, rows * target_s / max(probe, 1e-6))))
+    t0 = time.perf_counter()
+    oracle.gemm(Ah[:rows], Bh, w.dtype, with_abs=False)
+    dt = time.perf_counter() - t0
+    return roofline.flops(rows, w.N, w.K), dt, rows, oracle.max_threads()
+
+
+def run_reference(args, dist: Dist):
+    """The oracle arm: the CPU oracle on host cores, a bounded sample per step."""
+    if dist.rank != 0:
+        return
+    import oracle
+    from dense_gemm_14_gb300 import inputs
+    oracle.build()
+    data = {name: inputs.make_workload(name) for name, *_ in PARTS}
+    per_step_s = max(0.5, 120.0 / max(1, args.steps + args.warmup)) / len(PARTS)
+    # calibrate rows per part once
+    rows = {}
+    for name, *_ in PARTS:
+        _, dt, r, _ = time_oracle_sample(name, per_step_s, *data[name])
+        rows[name] = r
+    tot_f, tot_t = 0.0, 0.0
+    for step in range(args.warmup + args.steps):
+        for name, *_ in PARTS:
+            w = inputs.WORKLOADS[name]
+            A, B = data[name]
+            r = rows[name]
+            t0 = time.perf_counter()
+            oracle.gemm(inputs.host_view(A)[:r], inputs.host_view(B), w.dtype, with_abs=False)
+            dt = time.perf_counter() - t0
+            if step >= args.warmup:
+                tot_f += 2.0 * r * w.N * w.K
+                tot_t += dt
+    value = tot_f / tot_t / 1e12
+    sample = ", ".join(f"first {rows[n]} rows of {n}" for n, *_ in PARTS) + " per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, dist: Dist):
+    import torch
+
+    import dense_gemm_14_gb300 as g14
+    from dense_gemm_14_gb300 import inputs, roofline
+
+    g14.load()
+    dev = torch.device("cuda", dist.local_rank if dist.world > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks = roofline.measured_peaks()
+
+    entries = {"gemm_f32": g14.gemm_f32, "gemm_bf16_f32acc": g14.gemm_bf16_f32acc}
+    parts = []
+    host = {}
+    for name, kernel, bound, entry, src in PARTS:
+        if args.only and name != args.only:
+            continue
+        w, fl, ib = workload_info(name)
+        A, B = inputs.make_workload(name)
+        host[name] = (A, B)
+        per_set = A.numel() * A.element_size() + B.numel() * B.element_size() + w.M * w.N * 4
+        nsets = max(2, -(-2 * L2_BYTES // per_set))
+        a0, b0 = A.to(dev), B.to(dev)
+        sets = [(a0, b0, torch.empty(w.M, w.N, device=dev))]
+        for _ in range(nsets - 1):
+            sets.append((a0.clone(), b0.clone(), torch.empty(w.M, w.N, device=dev)))
+        parts.append(dict(name=name, kernel=kernel, bound=bound, fn=entries[entry], src=src,
+                          w=w, flops=fl, ideal_bytes=ib, sets=sets))
+
+    def launch(p, step):
+        a, b, c = p["sets"][step % len(p["sets"])]
+        w = p["w"]
+        p["fn"](w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N,
+                stream.cuda_stream)
+
+    # warm-up (also configures the kernels' shared-memory attributes)
+    for step in range(args.warmup):
+        for p in parts:
+            launch(p, step)
+    st = g14.check_device_error(stream.cuda_stream)
+    if st:
+        raise RuntimeError(f"device error during warm-up: {g14.status_string(st)}")
+
+    K = args.steps
+    ev = {p["name"]: ([torch.cuda.Event(enable_timing=True) for _ in range(K)],
+                      [torch.cuda.Event(enable_timing=True) for _ in range(K)]) for p in parts}
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index)
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    start.record(stream)
+    for step in range(K):
+        for p in parts:
+            s_ev, e_ev = ev[p["name"]]
+            s_ev[step].record(stream)
+            launch(p, step)
+            e_ev[step].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    st = g14.check_device_error(stream.cuda_stream)
+    if st:
+        raise RuntimeError(f"device error in the timed region: {g14.status_string(st)}")
+    elapsed_s = start.elapsed_time(end) / 1e3
+    elapsed_max = dist.max(elapsed_s)
+    flops_step = sum(p["flops"] for p in parts)
+    value = flops_step * K * dist.world / elapsed_max / 1e12
+
+    part_out = []
+    for p in parts:
+        s_ev, e_ev = ev[p["name"]]
+        ms = [s_ev[i].elapsed_time(e_ev[i]) for i in range(K)]
+        avg_s = statistics.mean(ms) / 1e3
+        tflops = p["flops"] / avg_s / 1e12
+        if p["bound"] == "tensor":
+            peak = peaks["bf16_tflops_sustained"]
+            peak_note = f"bf16 dense, sustained ({peaks['source']})"
+        else:
+            peak = roofline.fp32_alu_peak_tflops()
+            peak_note = "FFMA: 152 SMs x 128 lanes x 2 FLOP x 2070 MHz (unit counts)"
+        part_out.append({
+            "workload": p["name"], "kernel": p["kernel"], "M": p["w"].M, "N": p["w"].N,
+            "K": p["w"].K, "ms_mean": statistics.mean(ms), "ms_min": min(ms),
+            "tflops": tflops,
+            "roofline": {"bound": p["bound"], "achieved": tflops, "peak": peak, "unit": UNIT,
+                         "frac": tflops / peak, "peak_kind": peak_note,
+                         "traffic": traffic_for(p["kernel"], p["src"], p["name"]),
+                         "ideal_bytes": p["ideal_bytes"],
+                         "hbm_floor_ms": p["ideal_bytes"] / (peaks["hbm_gbs"] * 1e9) * 1e3},
+        })
+    dominant = max(part_out, key=lambda x: x["ms_mean"])
+
+    # ---- end to end through the public API with host tensors
+    e2e = None
+    if not args.no_e2e:
+        pinned = {n: (a.pin_memory(), b.pin_memory()) for n, (a, b) in host.items()}
+        h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size()
+                  for a, b in pinned.values())
+        d2h = sum(p["w"].M * p["w"].N * 4 for p in parts)
+        e2e_steps = max(1, min(K, 5))
+        for _ in range(2):
+            for n, (a, b) in pinned.items():
+                g14.gemm(a, b)
+        dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            for n, (a, b) in pinned.items():
+                g14.gemm(a, b)
+        torch.cuda.synchronize()
+        t_e2e = dist.max(time.perf_counter() - t0)
+        e2e = {"value": flops_step * e2e_steps * dist.world / t_e2e / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+    # ---- CPU oracle baseline (rank 0, one GPU only)
+    cpu = None
+    if dist.world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        tf, tt, desc, threads = 0.0, 0.0, [], 1
+        for p in parts:
+            f, t, r, threads = time_oracle_sample(p["name"], args.cpu_seconds, *host[p["name"]])
+            tf += f
+            tt += t
+            desc.append(f"first {r} rows of {p['name']}")
+        cpu = {"value": tf / tt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": "; ".join(desc) + " (fp64 oracle, product only)", "seconds": tt}
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": elapsed_max / K * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32 (FFMA) + bf16xbf16->f32 (tcgen05)", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME,
+                       "l2": "inputs rotate over copies totalling > 2x L2 (no flush)",
+                       "parallelism": f"replicas x{dist.world}"},
+            "roofline": {k: dominant["roofline"][k] for k in
+                         ("bound", "achieved", "peak", "unit", "frac", "traffic")},
+            "dominant_kernel": dominant["kernel"],
+            "parts": part_out,
+            "gpu_launches": len(parts) * K,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    dist = Dist(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

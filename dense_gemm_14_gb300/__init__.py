@@ -1,0 +1,24 @@
+"""GB300 (sm_103a) dense GEMM: C = A @ B on row-major matrices.
+
+A thin binding over the C ABI of ``libgemm14.so`` (``include/gemm14.h``). The
+three entry points keep their C names and arguments -- sizes, raw device
+pointers, leading dimensions and a stream handle -- and only marshal them;
+every step of the product runs in the library's CUDA kernels. There is no CPU
+fallback: if the library is missing or the GPU is unsupported, calls raise.
+
+``gemm(a, b)`` is the convenience call on torch tensors: CUDA tensors run on
+the current stream; CPU tensors are copied through pinned host memory to the
+GPU and the result is copied back (the end-to-end path).
+"""
+from __future__ import annotations
+
+from ._lib import (GEMM14_DTYPE_BF16, GEMM14_DTYPE_F16, GEMM14_DTYPE_F32, Gemm14Error, Plan,
+                   check_device_error, gemm_bf16_f32acc, gemm_f16_f32acc, gemm_f32, lib_path,
+                   load, plan, status_string, version)
+from .api import gemm, gemm_into
+
+__all__ = [
+    "gemm", "gemm_into", "gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "plan", "Plan",
+    "check_device_error", "status_string", "version", "load", "lib_path", "Gemm14Error",
+    "GEMM14_DTYPE_F32", "GEMM14_DTYPE_BF16", "GEMM14_DTYPE_F16",
+]

@@ -1,0 +1,143 @@
+"""ctypes binding of libgemm14.so: the C ABI of include/gemm14.h, argument
+marshalling only."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_DEFAULT_LIB = os.path.join(_HERE, "_build", "libgemm14.so")
+
+GEMM14_OK = 0
+GEMM14_ERR_INVALID_ARG = 1
+GEMM14_ERR_UNSUPPORTED_DEVICE = 2
+GEMM14_ERR_CUDA = 3
+GEMM14_ERR_TIMEOUT = 4
+
+GEMM14_DTYPE_F32 = 0
+GEMM14_DTYPE_BF16 = 1
+GEMM14_DTYPE_F16 = 2
+
+# Every function the header declares, with (restype, argtypes).
+_i64, _vp, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+_GEMM_ARGS = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [("kernel", _int), ("loader", _int), ("bm", _int), ("bn", _int), ("bk", _int),
+                ("stages", _int), ("threads", _int), ("smem_bytes", _int),
+                ("vec_store", _int), ("tiles", _i64), ("grid", _int)]
+
+
+SIGNATURES = {
+    "gemm_f32": (_int, _GEMM_ARGS),
+    "gemm_bf16_f32acc": (_int, _GEMM_ARGS),
+    "gemm_f16_f32acc": (_int, _GEMM_ARGS),
+    "gemm14_status_string": (ctypes.c_char_p, [_int]),
+    "gemm14_last_error_string": (ctypes.c_char_p, []),
+    "gemm14_check_device_error": (_int, [_vp]),
+    "gemm14_plan_gemm": (_int, [_int, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int,
+                                ctypes.POINTER(_Plan)]),
+    "gemm14_version": (_int, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class Gemm14Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        detail = ""
+        if status == GEMM14_ERR_CUDA and _lib is not None:
+            detail = ": " + _lib.gemm14_last_error_string().decode(errors="replace")
+        super().__init__(f"{where} failed: {status_string(status)} ({status}){detail}")
+
+
+def lib_path() -> str:
+    return os.environ.get("GEMM14_LIB", _DEFAULT_LIB)
+
+
+def load():
+    """Loads libgemm14.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with `python -m dense_gemm_14_gb300.build` "
+                    "(there is no fallback implementation)")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().gemm14_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(load().gemm14_version())
+
+
+def _call(name: str, M, N, K, A, lda, B, ldb, C, ldc, stream) -> int:
+    return int(getattr(load(), name)(M, N, K, A, lda, B, ldb, C, ldc, stream))
+
+
+def gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream=None, check=True) -> int:
+    """C ABI gemm_f32 on raw device pointers (ints); raises on a non-OK status if check."""
+    st = _call("gemm_f32", M, N, K, A, lda, B, ldb, C, ldc, stream)
+    if check and st:
+        raise Gemm14Error(st, "gemm_f32")
+    return st
+
+
+def gemm_bf16_f32acc(M, N, K, A, lda, B, ldb, C, ldc, stream=None, check=True) -> int:
+    """C ABI gemm_bf16_f32acc on raw device pointers (ints)."""
+    st = _call("gemm_bf16_f32acc", M, N, K, A, lda, B, ldb, C, ldc, stream)
+    if check and st:
+        raise Gemm14Error(st, "gemm_bf16_f32acc")
+    return st
+
+
+def gemm_f16_f32acc(M, N, K, A, lda, B, ldb, C, ldc, stream=None, check=True) -> int:
+    """C ABI gemm_f16_f32acc on raw device pointers (ints)."""
+    st = _call("gemm_f16_f32acc", M, N, K, A, lda, B, ldb, C, ldc, stream)
+    if check and st:
+        raise Gemm14Error(st, "gemm_f16_f32acc")
+    return st
+
+
+def check_device_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error status."""
+    return int(load().gemm14_check_device_error(stream))
+
+
+@dataclass
+class Plan:
+    kernel: int
+    loader: int
+    bm: int
+    bn: int
+    bk: int
+    stages: int
+    threads: int
+    smem_bytes: int
+    vec_store: int
+    tiles: int
+    grid: int
+
+
+def plan(dtype: int, M, N, K, A, lda, B, ldb, C, ldc, sm_count: int):
+    """Host-only launch plan (no CUDA call). Returns (status, Plan)."""
+    p = _Plan()
+    st = int(load().gemm14_plan_gemm(dtype, M, N, K, A, lda, B, ldb, C, ldc, sm_count,
+                                     ctypes.byref(p)))
+    return st, Plan(**{f: getattr(p, f) for f, _ in _Plan._fields_})

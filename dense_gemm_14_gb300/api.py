@@ -1,0 +1,72 @@
+"""Tensor-level calls on top of the C ABI (argument marshalling only)."""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+_ENTRY = {
+    torch.float32: _lib.gemm_f32,
+    torch.bfloat16: _lib.gemm_bf16_f32acc,
+    torch.float16: _lib.gemm_f16_f32acc,
+}
+
+
+def _check_matrix(x: torch.Tensor, name: str) -> None:
+    if x.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(x.shape)}")
+    if x.size(1) > 1 and x.stride(1) != 1:
+        raise ValueError(f"{name} must have unit stride along its rows (row-major)")
+
+
+def gemm_into(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """out = a @ b on the GPU through the C ABI; a, b, out are CUDA tensors.
+
+    a: (M, K), b: (K, N) in float32, bfloat16 or float16 (same dtype);
+    out: (M, N) float32. Row pitches come from the tensors' strides. Runs on
+    `stream` (default: torch's current stream) without synchronising.
+    """
+    if a.dtype != b.dtype or a.dtype not in _ENTRY:
+        raise TypeError(f"unsupported dtypes {a.dtype}, {b.dtype}")
+    if out.dtype != torch.float32:
+        raise TypeError("out must be float32")
+    for x, n in ((a, "a"), (b, "b"), (out, "out")):
+        _check_matrix(x, n)
+        if not x.is_cuda:
+            raise ValueError(f"{n} must be a CUDA tensor")
+    M, K = a.shape
+    K2, N = b.shape
+    if K != K2 or tuple(out.shape) != (M, N):
+        raise ValueError(f"shape mismatch: {tuple(a.shape)} @ {tuple(b.shape)} -> {tuple(out.shape)}")
+    if stream is None:
+        stream = torch.cuda.current_stream(a.device).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    with torch.cuda.device(a.device):
+        _ENTRY[a.dtype](M, N, K, a.data_ptr(), max(a.stride(0), 1), b.data_ptr(),
+                        max(b.stride(0), 1), out.data_ptr(), max(out.stride(0), 1), stream)
+    return out
+
+
+def gemm(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """C = a @ b with fp32 accumulation and output.
+
+    CUDA inputs: computed on the current stream, returned on the GPU.
+    CPU inputs: staged through pinned host memory to the current CUDA device,
+    computed there, and the result is copied back to (pinned) host memory; the
+    call returns once the result is on the host.
+    """
+    if a.is_cuda:
+        if out is None:
+            out = torch.empty((a.shape[0], b.shape[1]), dtype=torch.float32, device=a.device)
+        return gemm_into(a, b, out)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    a_d = a.pin_memory().to(dev, non_blocking=True) if not a.is_pinned() else a.to(dev, non_blocking=True)
+    b_d = b.pin_memory().to(dev, non_blocking=True) if not b.is_pinned() else b.to(dev, non_blocking=True)
+    c_d = torch.empty((a.shape[0], b.shape[1]), dtype=torch.float32, device=dev)
+    gemm_into(a_d.contiguous(), b_d.contiguous(), c_d)
+    if out is None:
+        out = torch.empty((a.shape[0], b.shape[1]), dtype=torch.float32, pin_memory=True)
+    out.copy_(c_d, non_blocking=True)
+    torch.cuda.current_stream(dev).synchronize()
+    return out

@@ -1,0 +1,94 @@
+"""Builds libgemm14.so in-tree (dense_gemm_14_gb300/_build/) with nvcc for sm_103a.
+
+The translation units are compiled in parallel, then linked into one shared
+library with the CUDA runtime linked statically, so the library depends on
+nothing but the driver (libcuda, reached at run time) and libc/libstdc++.
+
+    python -m dense_gemm_14_gb300.build [--force] [--verbose]
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import shutil
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+BUILD_DIR = os.path.join(HERE, "_build")
+LIB_NAME = "libgemm14.so"
+LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
+
+SOURCES = ["api.cu", "sgemm_simt.cu", "hgemm_tc.cu"]
+HEADERS = ["ptx.cuh", "kernels.h"]
+
+NVCC_FLAGS = [
+    "-gencode", "arch=compute_103a,code=sm_103a",
+    "-lineinfo", "-O3", "-std=c++17",
+    "-Xcompiler", "-fPIC",
+    "-Xptxas", "-v",
+    "--expt-relaxed-constexpr",
+]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found (set NVCC or put it on PATH)")
+
+
+def _stale(lib: str, inputs) -> bool:
+    if not os.path.exists(lib):
+        return True
+    t = os.path.getmtime(lib)
+    return any(os.path.getmtime(p) > t for p in inputs)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compiles every .cu and links libgemm14.so; returns its path."""
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    inputs = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
+    inputs.append(os.path.join(INCLUDE, "gemm14.h"))
+    inputs.append(os.path.abspath(__file__))
+    if not force and not _stale(LIB_PATH, inputs):
+        return LIB_PATH
+    cc = nvcc()
+    procs = []
+    for src in SOURCES:
+        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        log = os.path.join(BUILD_DIR, src.replace(".cu", ".ptxas.log"))
+        cmd = [cc, *NVCC_FLAGS, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+        fh = open(log, "w")
+        procs.append((src, obj, log, fh, subprocess.Popen(cmd, stdout=fh, stderr=subprocess.STDOUT)))
+    failed = []
+    for src, obj, log, fh, p in procs:
+        rc = p.wait()
+        fh.close()
+        if rc != 0:
+            failed.append((src, log))
+        elif verbose:
+            sys.stdout.write(open(log).read())
+    if failed:
+        msgs = "\n".join(f"--- {s} ---\n{open(l).read()}" for s, l in failed)
+        raise RuntimeError(f"nvcc failed for {[s for s, _ in failed]}:\n{msgs}")
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    objs = [o for _, o, _, _, _ in procs]
+    subprocess.run([cc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a",
+                    "-o", tmp, *objs], check=True)
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--force", action="store_true")
+    ap.add_argument("--verbose", action="store_true")
+    a = ap.parse_args()
+    print(build(force=a.force, verbose=a.verbose))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,321 @@
+// api.cu -- the C ABI of libgemm14.so: argument validation, launch planning,
+// TMA tensor-map encoding, device checks and error reporting.
+// The contract of each entry point is documented in include/gemm14.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm14.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gemm14 {
+namespace {
+
+// The library's device error word: kernels OR kDevErr* bits into it when a
+// bounded wait expires. Host code reaches it through the address cached per
+// device below (a symbol's host-side name is not a device address).
+__device__ unsigned g_device_error;
+
+thread_local char t_last_error[256] = "";
+
+void set_cuda_error(const char* what, cudaError_t e) {
+  std::snprintf(t_last_error, sizeof t_last_error, "%s: %s (%d)", what, cudaGetErrorString(e),
+                static_cast<int>(e));
+}
+
+void set_driver_error(const char* what, CUresult r) {
+  std::snprintf(t_last_error, sizeof t_last_error, "%s: CUresult %d", what, static_cast<int>(r));
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+  unsigned* err_word = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mutex;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode_tiled = nullptr;
+std::once_flag g_encode_once;
+
+// Looks up the current device once: compute capability, SM count and the
+// device address of the error word. Returns a gemm14_status.
+int current_device(const DeviceInfo** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_cuda_error("cudaGetDevice", e);
+    return GEMM14_ERR_UNSUPPORTED_DEVICE;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return GEMM14_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_devices_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) {
+      set_cuda_error("cudaDeviceGetAttribute", e);
+      return GEMM14_ERR_CUDA;
+    }
+    d.supported = (major == 10 && minor == 3);
+    d.sm_count = sms;
+    if (d.supported) {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_device_error)) != cudaSuccess) {
+        set_cuda_error("cudaGetSymbolAddress(error word)", e);
+        return GEMM14_ERR_CUDA;
+      }
+      d.err_word = static_cast<unsigned*>(p);
+    }
+    d.ready = true;
+  }
+  if (!d.supported) return GEMM14_ERR_UNSUPPORTED_DEVICE;
+  *out = &d;
+  return GEMM14_OK;
+}
+
+int encoder(EncodeTiledFn* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode_tiled = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!g_encode_tiled) {
+    std::snprintf(t_last_error, sizeof t_last_error, "cuTensorMapEncodeTiled not available");
+    return GEMM14_ERR_CUDA;
+  }
+  *fn = g_encode_tiled;
+  return GEMM14_OK;
+}
+
+// 2-D row-major tensor map: `rows` x `cols` elements, row pitch ld elements,
+// box = box_cols (inner) x box_rows, zero fill out of range.
+int make_map(CUtensorMap* map, CUtensorMapDataType type, int elem_bytes, const void* base,
+             int64_t rows, int64_t cols, int64_t ld, int box_cols, int box_rows,
+             CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = nullptr;
+  int st = encoder(&fn);
+  if (st != GEMM14_OK) return st;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * elem_bytes};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_driver_error("cuTensorMapEncodeTiled", r);
+    return GEMM14_ERR_CUDA;
+  }
+  return GEMM14_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elem_bytes_of(int dtype) { return dtype == GEMM14_DTYPE_F32 ? 4 : 2; }
+
+// Argument validation shared by the entry points and the planner.
+int validate(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+             const void* B, int64_t ldb, const void* C, int64_t ldc) {
+  if (dtype != GEMM14_DTYPE_F32 && dtype != GEMM14_DTYPE_BF16 && dtype != GEMM14_DTYPE_F16)
+    return GEMM14_ERR_INVALID_ARG;
+  const int64_t kMax = INT32_MAX;
+  if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax) return GEMM14_ERR_INVALID_ARG;
+  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    return GEMM14_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM14_OK;
+  if (!C || !aligned(C, 4)) return GEMM14_ERR_INVALID_ARG;
+  if (K == 0) return GEMM14_OK;
+  const int eb = elem_bytes_of(dtype);
+  if (!A || !B || !aligned(A, eb) || !aligned(B, eb)) return GEMM14_ERR_INVALID_ARG;
+  // TMA strides must stay below 2^40 bytes.
+  if (lda > (int64_t(1) << 36) || ldb > (int64_t(1) << 36)) return GEMM14_ERR_INVALID_ARG;
+  return GEMM14_OK;
+}
+
+int hgemm_bn_for(int64_t N) { return N <= 64 ? 64 : N <= 128 ? 128 : 256; }
+
+void plan_for(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+              const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
+              gemm14_plan* p) {
+  std::memset(p, 0, sizeof *p);
+  if (M == 0 || N == 0 || K == 0) return;  // nothing launched (K == 0: a memset)
+  p->vec_store = aligned(C, 16) && (ldc % 4 == 0);
+  if (dtype == GEMM14_DTYPE_F32) {
+    using S = SgemmShape;
+    p->kernel = 1;
+    p->loader = (aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 && ldb % 4 == 0) ? 1 : 2;
+    p->bm = S::BM;
+    p->bn = S::BN;
+    p->bk = S::BK;
+    p->stages = S::STAGES;
+    p->threads = S::THREADS;
+    p->smem_bytes = S::SMEM_BYTES;
+  } else {
+    const int bn = hgemm_bn_for(N);
+    p->kernel = 2;
+    p->loader = (aligned(A, 16) && aligned(B, 16) && lda % 8 == 0 && ldb % 8 == 0) ? 1 : 2;
+    p->bm = HgemmShape::BM;
+    p->bn = bn;
+    p->bk = HgemmShape::BK;
+    p->stages = HgemmShape::stages(bn);
+    p->threads = HgemmShape::THREADS;
+    p->smem_bytes = HgemmShape::smem_bytes(bn);
+  }
+  p->tiles = ((M + p->bm - 1) / p->bm) * ((N + p->bn - 1) / p->bn);
+  const int64_t sms = sm_count > 0 ? sm_count : 1;
+  p->grid = static_cast<int>(p->tiles < sms ? p->tiles : sms);
+}
+
+bool debug_checks() {
+  static const bool on = [] {
+    const char* v = std::getenv("GEMM14_DEBUG");
+    return v && v[0] && v[0] != '0';
+  }();
+  return on;
+}
+
+int finish(cudaError_t e, const char* what, cudaStream_t stream) {
+  if (e != cudaSuccess) {
+    set_cuda_error(what, e);
+    return GEMM14_ERR_CUDA;
+  }
+  if (debug_checks()) return gemm14_check_device_error(stream);
+  return GEMM14_OK;
+}
+
+int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+             const void* B, int64_t ldb, float* C, int64_t ldc, void* stream_ptr) {
+  int st = validate(dtype, M, N, K, A, lda, B, ldb, C, ldc);
+  if (st != GEMM14_OK) return st;
+  if (M == 0 || N == 0) return GEMM14_OK;
+  const DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev)) != GEMM14_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+  if (K == 0) {
+    cudaError_t e = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 4, 0,
+                                      static_cast<size_t>(N) * 4, static_cast<size_t>(M), stream);
+    return finish(e, "cudaMemset2DAsync", stream);
+  }
+
+  gemm14_plan plan;
+  plan_for(dtype, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+  GemmArgs args{static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                A, lda, B, ldb, C, ldc, plan.vec_store, dev->err_word};
+
+  if (dtype == GEMM14_DTYPE_F32) {
+    if (plan.loader == 2)
+      return finish(launch_sgemm_cpasync(args, plan.grid, stream), "sgemm launch", stream);
+    CUtensorMap ma, mb;
+    if ((st = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A, M, K, lda, SgemmShape::BK,
+                       SgemmShape::BM, CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
+      return st;
+    if ((st = make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, K, N, ldb, SgemmShape::BN,
+                       SgemmShape::BK, CU_TENSOR_MAP_SWIZZLE_NONE)) != GEMM14_OK)
+      return st;
+    return finish(launch_sgemm_tma(ma, mb, args, plan.grid, stream), "sgemm launch", stream);
+  }
+
+  const bool bf16 = dtype == GEMM14_DTYPE_BF16;
+  const uint32_t idesc = idesc_f16_f32acc(bf16, HgemmShape::BM, plan.bn);
+  if (plan.loader == 2)
+    return finish(launch_hgemm_tc_soft(plan.bn, args, idesc, plan.grid, stream), "hgemm launch",
+                  stream);
+  const CUtensorMapDataType tt =
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap ma, mb;
+  if ((st = make_map(&ma, tt, 2, A, M, K, lda, HgemmShape::BK, HgemmShape::BM,
+                     CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
+    return st;
+  if ((st = make_map(&mb, tt, 2, B, K, N, ldb, 64, HgemmShape::BK, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+      GEMM14_OK)
+    return st;
+  return finish(launch_hgemm_tc(plan.bn, ma, mb, args, idesc, plan.grid, stream), "hgemm launch",
+                stream);
+}
+
+}  // namespace
+}  // namespace gemm14
+
+using namespace gemm14;
+
+extern "C" {
+
+int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
+             int64_t ldb, float* C, int64_t ldc, void* stream) {
+  return run_gemm(GEMM14_DTYPE_F32, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+int gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                     const void* B, int64_t ldb, float* C, int64_t ldc, void* stream) {
+  return run_gemm(GEMM14_DTYPE_BF16, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+int gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                    int64_t ldb, float* C, int64_t ldc, void* stream) {
+  return run_gemm(GEMM14_DTYPE_F16, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+const char* gemm14_status_string(int status) {
+  switch (status) {
+    case GEMM14_OK: return "ok";
+    case GEMM14_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM14_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case GEMM14_ERR_CUDA: return "CUDA error";
+    case GEMM14_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* gemm14_last_error_string(void) { return t_last_error; }
+
+int gemm14_check_device_error(void* stream_ptr) {
+  const DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GEMM14_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    set_cuda_error("cudaStreamSynchronize", e);
+    return GEMM14_ERR_CUDA;
+  }
+  unsigned word = 0;
+  if ((e = cudaMemcpy(&word, dev->err_word, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+      (e = cudaMemset(dev->err_word, 0, sizeof word)) != cudaSuccess) {
+    set_cuda_error("reading the device error word", e);
+    return GEMM14_ERR_CUDA;
+  }
+  return word ? GEMM14_ERR_TIMEOUT : GEMM14_OK;
+}
+
+int gemm14_plan_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                     const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
+                     gemm14_plan* plan) {
+  if (!plan) return GEMM14_ERR_INVALID_ARG;
+  int st = validate(dtype, M, N, K, A, lda, B, ldb, C, ldc);
+  if (st != GEMM14_OK) return st;
+  plan_for(dtype, M, N, K, A, lda, B, ldb, C, ldc, sm_count, plan);
+  return GEMM14_OK;
+}
+
+int gemm14_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,336 @@
+// hgemm_tc.cu -- bf16 / fp16 inputs, fp32 accumulate and output, on the
+// 5th-generation tensor cores (tcgen05), C = A * B, all row-major.
+//
+// The pages' tensor-core kernel (WMMA 16x16x16 with half inputs and a float
+// accumulator, "Kernel 优化指南", "Level 4: Tensor Cores (WMMA)") and their
+// account of wgmma (gpu-hpc-book ch.06 "高级 cuda 特性 —— 从矩阵乘法(gemm)说起",
+// "Tensor Cores" / "wgmma": asynchronous D = A*B + D with operands in shared
+// memory fed by TMA) are the prior art; on sm_103a the same product is one
+// tcgen05.mma issued by a single thread with the accumulator in tensor memory.
+//
+// Structure (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0      producer: TMA loads of A (128 m x 64 k, K-major, 128-byte
+//               swizzle) and B (BN/64 boxes of 64 n x 64 k, N-major, 128-byte
+//               swizzle) into an S-stage ring (full/empty mbarriers); for
+//               operands TMA cannot address, the whole warp fills the same
+//               layout with plain loads and stores;
+//   warp 1      allocates 2*BN TMEM columns (two accumulators) and one lane
+//               issues 4 x tcgen05.mma (K = 16 each) per 64-deep k-block;
+//               tcgen05.commit frees the smem stage and, at the end of a
+//               tile, publishes the accumulator;
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, fp32
+//               stores to C (16-byte vectors when C allows, guarded edges);
+//               while they drain accumulator b the MMA warp fills 1-b.
+// Tiles are visited in groups of 16 row-tiles so that the CTAs running at the
+// same time share A and B panels in L2.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gemm14 {
+namespace {
+
+using H = HgemmShape;
+constexpr int kGroupM = 16;
+
+template <int BN>
+struct TcSmem {
+  static constexpr int STAGES = H::stages(BN);
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Grouped raster: tile t -> (tm, tn), row-tiles in groups of kGroupM.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
+  const int per_group = kGroupM * tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * kGroupM;
+  const int gm = min(tiles_m - first_m, kGroupM);
+  const int r = t - g * per_group;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
+// Software loader for operands that break TMA's 16-byte rules (any 2-byte
+// aligned base and pitch): the producer warp reads element pairs with 2-byte
+// loads (zero outside the matrix) and writes them into the same 128-byte
+// swizzled layout TMA would produce, then fences them into the async proxy.
+__device__ __forceinline__ uint32_t ld_pair(const uint16_t* base, int64_t row_off, int col,
+                                            int ncols, bool row_ok) {
+  uint32_t lo = 0, hi = 0;
+  if (row_ok && col < ncols) lo = __ldg(base + row_off + col);
+  if (row_ok && col + 1 < ncols) hi = __ldg(base + row_off + col + 1);
+  return lo | (hi << 16);
+}
+
+template <int BN>
+__device__ __forceinline__ void soft_load_stage(uint8_t* a_st, const GemmArgs& args, int tm,
+                                                int tn, int kb, int lane) {
+  const uint16_t* A = static_cast<const uint16_t*>(args.A);
+  const uint16_t* B = static_cast<const uint16_t*>(args.B);
+  uint8_t* b_st = a_st + H::BM * H::BK * 2;
+  // Lane l holds columns 2l, 2l+1 of a 64-wide, 128-byte row; its 4-byte word
+  // sits in 16-byte chunk (l / 4) XOR (row % 8), at byte 4 (l % 4) of the chunk.
+  const uint32_t word = static_cast<uint32_t>((lane & 3) << 2);
+  const int k0 = kb * H::BK + 2 * lane;
+#pragma unroll 4
+  for (int r = 0; r < H::BM; ++r) {
+    const int m = tm * H::BM + r;
+    const uint32_t v = ld_pair(A, static_cast<int64_t>(m) * args.lda, k0, args.K, m < args.M);
+    *reinterpret_cast<uint32_t*>(a_st + r * 128 + ((((lane >> 2) ^ (r & 7)) & 7) << 4) + word) = v;
+  }
+#pragma unroll 1
+  for (int c = 0; c < BN / 64; ++c) {
+    const int n0 = tn * BN + c * 64 + 2 * lane;
+#pragma unroll 4
+    for (int kr = 0; kr < H::BK; ++kr) {
+      const int k = kb * H::BK + kr;
+      const uint32_t v = ld_pair(B, static_cast<int64_t>(k) * args.ldb, n0, args.N, k < args.K);
+      *reinterpret_cast<uint32_t*>(b_st + c * (64 * H::BK * 2) + kr * 128 +
+                                   ((((lane >> 2) ^ (kr & 7)) & 7) << 4) + word) = v;
+    }
+  }
+}
+
+template <int BN, bool kTma>
+__global__ void __launch_bounds__(H::THREADS, 1)
+    hgemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_b, const GemmArgs args,
+                    const uint32_t idesc) {
+  constexpr int STAGES = H::stages(BN);
+  constexpr int A_BYTES = H::BM * H::BK * 2;   // 16 KB
+  constexpr int B_BYTES = H::BK * BN * 2;      // BN/64 boxes of 8 KB
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles = align1024(smem_raw);
+  TcSmem<BN>& sm = *reinterpret_cast<TcSmem<BN>*>(tiles + STAGES * STAGE_BYTES);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int M = args.M, N = args.N, K = args.K;
+  const int tiles_m = (M + H::BM - 1) / H::BM;
+  const int tiles_n = (N + BN - 1) / BN;
+  const int num_tiles = tiles_m * tiles_n;
+  const int kblocks = (K + H::BK - 1) / H::BK;
+  volatile int* abort_flag = &sm.abort_flag;
+  uint32_t prod_it = 0;
+  bool mma_issued = false;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sm.full[s], kTma ? 1 : 32);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_empty[b], 4);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+    if (kTma) {
+      tma_prefetch_desc(&map_a);
+      tma_prefetch_desc(&map_b);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (!kTma) {
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, tiles_m, tiles_n, tm, tn);
+        for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
+          const uint32_t s = prod_it % STAGES, ph = (prod_it / STAGES) & 1;
+          int got = 1;
+          if (lane == 0) got = mbar_wait(&sm.empty[s], ph ^ 1, args.err, abort_flag) ? 1 : 0;
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) { ok = false; break; }
+          soft_load_stage<BN>(tiles + s * STAGE_BYTES, args, tm, tn, kb, lane);
+          fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
+          mbar_arrive(&sm.full[s]);
+        }
+      }
+    } else if (lane == 0) {
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, tiles_m, tiles_n, tm, tn);
+        for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
+          const uint32_t s = prod_it % STAGES, ph = (prod_it / STAGES) & 1;
+          if (!mbar_wait(&sm.empty[s], ph ^ 1, args.err, abort_flag)) { ok = false; break; }
+          uint8_t* a_st = tiles + s * STAGE_BYTES;
+          uint8_t* b_st = a_st + A_BYTES;
+          mbar_arrive_expect_tx(&sm.full[s], STAGE_BYTES);
+          tma_load_2d(a_st, &map_a, kb * H::BK, tm * H::BM, &sm.full[s]);
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c)
+            tma_load_2d(b_st + c * (64 * H::BK * 2), &map_b, tn * BN + c * 64, kb * H::BK,
+                        &sm.full[s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t it = 0;
+      int local = 0;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+        const int b = local & 1;
+        const uint32_t aph = (local >> 1) & 1;
+        if (!mbar_wait(&sm.acc_empty[b], aph ^ 1, args.err, abort_flag)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+          if (!mbar_wait(&sm.full[s], ph, args.err, abort_flag)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t a_addr = smem_u32(tiles + s * STAGE_BYTES);
+          const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < H::BK / 16; ++kk) {
+            // A: K-major, 128-byte rows, 8-row groups 1024 B apart; a K = 16
+            // slice starts 32 bytes further along the row.
+            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            // B: N-major, 64-column boxes 8 KB apart (leading offset), 8-k
+            // groups 1024 B apart (stride offset); a K = 16 slice is 16 rows.
+            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * 2048, 64 * H::BK * 2, 1024);
+            tc_mma_f16(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0);
+          }
+          mma_issued = true;
+          tc_commit(&sm.empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(&sm.acc_full[b]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int local = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+      int tm, tn;
+      tile_coords(t, tiles_m, tiles_n, tm, tn);
+      const int b = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      // One lane waits; the warp then proceeds converged (tcgen05.ld is .sync.aligned).
+      int got = 1;
+      if (lane == 0) got = mbar_wait(&sm.acc_full[b], aph, args.err, abort_flag) ? 1 : 0;
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) break;
+      tc_fence_after_sync();
+      const int row = tm * H::BM + q * 32 + lane;
+      float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(b * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, r);
+        tc_wait_ld();
+        const int col0 = tn * BN + c * 32;
+        if (row < M) {
+          if (args.vec_store && col0 + 32 <= N) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              *reinterpret_cast<float4*>(crow + col0 + 4 * v) =
+                  make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < N) crow[col0 + j] = __uint_as_float(r[j]);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
+    }
+  }
+
+  // On abort: let issued MMAs and TMA loads finish (bounded) before TMEM is
+  // freed and the CTA's shared memory is released.
+  __syncthreads();
+  if (sm.abort_flag) {
+    if (warp == 1 && lane == 0 && mma_issued) {
+      tc_commit(&sm.drain);
+      mbar_wait_timed(&sm.drain, 0, 100000000ull);
+    }
+    if (kTma && warp == 0 && lane == 0) {
+      const uint32_t first = prod_it > STAGES ? prod_it - STAGES : 0;
+      for (uint32_t j = first; j < prod_it; ++j)
+        mbar_wait_timed(&sm.full[j % STAGES], (j / STAGES) & 1, 100000000ull);
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int BN, bool kTma>
+cudaError_t launch_bn(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
+                      uint32_t idesc, int grid, cudaStream_t stream) {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(hgemm_tc_kernel<BN, kTma>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, H::smem_bytes(BN));
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  CUtensorMap dummy{};
+  hgemm_tc_kernel<BN, kTma><<<grid, H::THREADS, H::smem_bytes(BN), stream>>>(
+      map_a ? *map_a : dummy, map_b ? *map_b : dummy, args, idesc);
+  return cudaGetLastError();
+}
+
+template <bool kTma>
+cudaError_t launch_any(int bn, const CUtensorMap* map_a, const CUtensorMap* map_b,
+                       const GemmArgs& args, uint32_t idesc, int grid, cudaStream_t stream) {
+  switch (bn) {
+    case 64: return launch_bn<64, kTma>(map_a, map_b, args, idesc, grid, stream);
+    case 128: return launch_bn<128, kTma>(map_a, map_b, args, idesc, grid, stream);
+    case 256: return launch_bn<256, kTma>(map_a, map_b, args, idesc, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_hgemm_tc(int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const GemmArgs& args, uint32_t idesc, int grid, cudaStream_t stream) {
+  return launch_any<true>(bn, &map_a, &map_b, args, idesc, grid, stream);
+}
+
+cudaError_t launch_hgemm_tc_soft(int bn, const GemmArgs& args, uint32_t idesc, int grid,
+                                 cudaStream_t stream) {
+  return launch_any<false>(bn, nullptr, nullptr, args, idesc, grid, stream);
+}
+
+}  // namespace gemm14

@@ -1,0 +1,59 @@
+// kernels.h -- internal interface between the C-ABI layer (api.cu) and the
+// kernel translation units. Nothing here crosses the library boundary.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gemm14 {
+
+// Arguments shared by every kernel: sizes, operand pointers and the library's
+// device error word (a plain device pointer, see api.cu).
+struct GemmArgs {
+  int M, N, K;
+  const void* A;
+  int64_t lda;
+  const void* B;
+  int64_t ldb;
+  float* C;
+  int64_t ldc;
+  int vec_store;  // C rows may take 16-byte stores (C 16-B aligned, ldc % 4 == 0)
+  unsigned* err;
+};
+
+// ---- fp32 SIMT kernel (sgemm_simt.cu)
+struct SgemmShape {
+  static constexpr int BM = 128, BN = 256, BK = 32, STAGES = 4;
+  static constexpr int WARPS = 8;  // all compute; thread 0 also issues the TMA loads
+  static constexpr int THREADS = WARPS * 32;
+  static constexpr int A_STAGE_BYTES = BM * BK * 4;
+  static constexpr int B_STAGE_BYTES = BK * BN * 4;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;  // + barriers + align slack
+};
+
+// Loader: TMA tensor maps (A box 32 x 128 with 128-byte swizzle, B box
+// 256 x 32) or, when the operands break TMA's 16-byte rules, cp.async.
+cudaError_t launch_sgemm_tma(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                             const GemmArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_sgemm_cpasync(const GemmArgs& args, int grid, cudaStream_t stream);
+
+// ---- bf16 / fp16 tcgen05 kernel (hgemm_tc.cu)
+struct HgemmShape {
+  static constexpr int BM = 128, BK = 64;
+  static constexpr int THREADS = 6 * 32;  // producer, MMA, 4 epilogue warps
+  static constexpr int stages(int bn) { return bn == 256 ? 4 : bn == 128 ? 6 : 8; }
+  static constexpr int stage_bytes(int bn) { return BM * BK * 2 + BK * bn * 2; }
+  static constexpr int smem_bytes(int bn) { return stages(bn) * stage_bytes(bn) + 256 + 1024; }
+};
+
+// bn in {64, 128, 256}; idesc is the tcgen05 instruction descriptor
+// (operand format and shape); map_b boxes are 64 (n) x 64 (k).
+cudaError_t launch_hgemm_tc(int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const GemmArgs& args, uint32_t idesc, int grid, cudaStream_t stream);
+// Same kernel with the software loader (operands TMA cannot address).
+cudaError_t launch_hgemm_tc_soft(int bn, const GemmArgs& args, uint32_t idesc, int grid,
+                                 cudaStream_t stream);
+
+}  // namespace gemm14

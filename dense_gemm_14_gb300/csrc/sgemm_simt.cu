@@ -1,0 +1,303 @@
+// sgemm_simt.cu -- fp32 GEMM on the CUDA cores (FFMA), C = A * B, row-major.
+//
+// Design (sm_103a):
+//  * Persistent grid: one CTA (8 warps) per SM walks output tiles blockIdx.x,
+//    +gridDim.x, ... Its work is one flat list of (tile, k-block) iterations,
+//    so the loads of the next tile start while the current tile is still
+//    being computed and stored.
+//  * Multistage ring: 4 shared-memory stages guarded by full/empty mbarriers.
+//    Loads for iteration j + 3 are issued as soon as every warp has finished
+//    iteration j - 1, overlapping transfer and compute -- the double-buffering
+//    of "Kernel 优化指南" (cuda-kernel-academy module 02), "Level 3: Double
+//    Buffering", and of gpu-hpc-book ch.06 "高级 cuda 特性 —— 从矩阵乘法(gemm)说起",
+//    "调度优化" (batching loads along k, asynchronous copies), with a deeper ring.
+//  * Loads: thread 0 issues TMA boxes (A: 32 k x 128 m with the 128-byte
+//    swizzle; B: 256 n x 32 k). When an operand breaks TMA's 16-byte rules all
+//    256 threads fill the very same shared-memory layout with 4-byte cp.async
+//    copies instead. Either way out-of-range elements are zero-filled: the
+//    guarded zero-fill of the pages' tiled kernels ("矩阵乘法中的分块与数据复用",
+//    matmul_l1 and matmul_l1_reg).
+//  * Register tiling: each thread owns an 8 x 16 block of C and per k does
+//    8 x 16 FFMAs from 8 A values and 16 B values -- the outer product of the
+//    pages' matmul_l1_reg ("Register Tiling"), grown to a 128 x 256 block tile
+//    and an 8 x 16 microtile so that there are ~21 FFMAs per shared-memory
+//    load instruction.
+//  * Conflict-free shared memory: A rows are 128 bytes with the 16-byte chunk
+//    index XOR-ed by (row % 8); a warp's A loads touch rows r .. r+3 (distinct
+//    mod 8), so its four distinct 16-byte chunks land in distinct banks. B
+//    rows are read as 8 contiguous float4 per warp (128 bytes). This is the
+//    bank-conflict avoidance of "Kernel 优化指南", "Bank Conflict 避免", done by
+//    swizzling instead of padding.
+//  * Epilogue: 16-byte stores when C permits ("向量化加载"), guarded scalar
+//    stores otherwise; each warp store covers 4 rows x 128 contiguous bytes.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gemm14 {
+namespace {
+
+using S = SgemmShape;
+
+struct SgemmSmem {
+  uint64_t full[S::STAGES];
+  uint64_t empty[S::STAGES];
+  int abort_flag;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Byte offset of A element (m, k) inside an A stage: 128-byte rows, 16-byte
+// chunks XOR-swizzled by (m % 8) -- the layout TMA's 128-byte swizzle writes.
+__device__ __forceinline__ uint32_t a_tile_offset(int m, int k) {
+  return static_cast<uint32_t>(m * 128 + ((((k >> 2) ^ (m & 7)) & 7) << 4) + (k & 3) * 4);
+}
+
+struct TileWalk {
+  int tiles_m, num_tiles, kblocks;
+  // Flat iteration j of this CTA -> output tile (tm, tn) and k-block kb.
+  __device__ __forceinline__ void at(uint32_t j, int& tm, int& tn, int& kb) const {
+    const int local_tile = static_cast<int>(j / static_cast<uint32_t>(kblocks));
+    kb = static_cast<int>(j - static_cast<uint32_t>(local_tile) * kblocks);
+    const int tile = blockIdx.x + local_tile * gridDim.x;
+    tm = tile % tiles_m;
+    tn = tile / tiles_m;
+  }
+};
+
+// Loads of flat iteration j into stage j % STAGES.
+template <bool kTma>
+__device__ __forceinline__ void issue_stage(uint32_t j, const TileWalk& w, uint8_t* tiles,
+                                            SgemmSmem& sm, const CUtensorMap* map_a,
+                                            const CUtensorMap* map_b, const GemmArgs& args) {
+  int tm, tn, kb;
+  w.at(j, tm, tn, kb);
+  const uint32_t s = j % S::STAGES;
+  uint8_t* a_st = tiles + s * S::STAGE_BYTES;
+  if (kTma) {
+    // called by thread 0 only
+    mbar_arrive_expect_tx(&sm.full[s], S::STAGE_BYTES);
+    tma_load_2d(a_st, map_a, kb * S::BK, tm * S::BM, &sm.full[s]);
+    tma_load_2d(a_st + S::A_STAGE_BYTES, map_b, tn * S::BN, kb * S::BK, &sm.full[s]);
+  } else {
+    // called by all threads: 4096 A + 8192 B elements, 48 per thread
+    const float* A = static_cast<const float*>(args.A);
+    const float* B = static_cast<const float*>(args.B);
+    const uint32_t a_sm = smem_u32(a_st);
+    const uint32_t b_sm = a_sm + S::A_STAGE_BYTES;
+    const int t = threadIdx.x;
+    {
+      const int kl = t & 31;           // k within the block: a warp reads 128 contiguous bytes
+      const int k = kb * S::BK + kl;
+      const bool k_ok = k < args.K;
+#pragma unroll 4
+      for (int r = t >> 5; r < S::BM; r += S::THREADS / 32) {
+        const int m = tm * S::BM + r;
+        const bool in = k_ok && m < args.M;
+        cp_async_4(a_sm + a_tile_offset(r, kl),
+                   in ? A + static_cast<int64_t>(m) * args.lda + k : A, in ? 4u : 0u);
+      }
+    }
+    {
+      const int nl = t;                // 256 threads = 256 columns of one k row
+      const int n = tn * S::BN + nl;
+      const bool n_ok = n < args.N;
+#pragma unroll 4
+      for (int kr = 0; kr < S::BK; ++kr) {
+        const int k = kb * S::BK + kr;
+        const bool in = n_ok && k < args.K;
+        cp_async_4(b_sm + static_cast<uint32_t>(kr * S::BN + nl) * 4,
+                   in ? B + static_cast<int64_t>(k) * args.ldb + n : B, in ? 4u : 0u);
+      }
+    }
+    cp_async_mbar_arrive_noinc(&sm.full[s]);
+  }
+}
+
+template <bool kTma>
+__global__ void __launch_bounds__(S::THREADS, 1)
+    sgemm_simt_kernel(const __grid_constant__ CUtensorMap map_a,
+                      const __grid_constant__ CUtensorMap map_b, const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles = align1024(smem_raw);
+  SgemmSmem& sm = *reinterpret_cast<SgemmSmem*>(tiles + S::STAGES * S::STAGE_BYTES);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int M = args.M, N = args.N;
+  TileWalk walk;
+  walk.tiles_m = (M + S::BM - 1) / S::BM;
+  walk.num_tiles = walk.tiles_m * ((N + S::BN - 1) / S::BN);
+  walk.kblocks = (args.K + S::BK - 1) / S::BK;
+  const int my_tiles = blockIdx.x < walk.num_tiles
+                           ? (walk.num_tiles - 1 - blockIdx.x) / gridDim.x + 1
+                           : 0;
+  const uint32_t n_iter = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(walk.kblocks);
+  volatile int* abort_flag = &sm.abort_flag;
+  const bool producer = kTma ? threadIdx.x == 0 : true;
+  uint32_t issued = 0;  // iterations whose loads this thread has issued
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::STAGES; ++s) {
+      mbar_init(&sm.full[s], kTma ? 1 : S::THREADS);
+      mbar_init(&sm.empty[s], S::WARPS);
+    }
+    sm.abort_flag = 0;
+    fence_barrier_init();
+    if (kTma) {
+      tma_prefetch_desc(&map_a);
+      tma_prefetch_desc(&map_b);
+    }
+  }
+  __syncthreads();
+
+  // Prologue: fill the ring (fresh stages need no empty-wait).
+  if (producer) {
+    for (; issued < n_iter && issued < static_cast<uint32_t>(S::STAGES); ++issued)
+      issue_stage<kTma>(issued, walk, tiles, sm, &map_a, &map_b, args);
+  }
+
+  // This thread's rows: warp_m*32 + tr + 4*i (i < 8); columns:
+  // warp_n*128 + tc*4 + 32*jj + q (jj, q < 4).
+  const int warp_m = warp & 3;  // 4 warps along m (32 rows each)
+  const int warp_n = warp >> 2; // 2 warps along n (128 columns each)
+  const int tr = lane >> 3;     // 4 thread rows per warp
+  const int tc = lane & 7;      // 8 thread columns per warp
+  const uint32_t a_thread = static_cast<uint32_t>((warp_m * 32 + tr) * 128);
+  const uint32_t b_thread = static_cast<uint32_t>((warp_n * 128 + tc * 4) * 4);
+
+  uint32_t it = 0;
+  bool ok = true;
+  for (int lt = 0; lt < my_tiles && ok; ++lt) {
+    const int tile = blockIdx.x + lt * gridDim.x;
+    const int tm = tile % walk.tiles_m, tn = tile / walk.tiles_m;
+    float acc[8][16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[i][j] = 0.f;
+
+    for (int kb = 0; kb < walk.kblocks; ++kb, ++it) {
+      const uint32_t s = it % S::STAGES, ph = (it / S::STAGES) & 1;
+      if (!mbar_wait(&sm.full[s], ph, args.err, abort_flag)) { ok = false; break; }
+      const uint8_t* a_st = tiles + s * S::STAGE_BYTES + a_thread;
+      const uint8_t* b_st = tiles + s * S::STAGE_BYTES + S::A_STAGE_BYTES + b_thread;
+#pragma unroll
+      for (int kg = 0; kg < S::BK / 4; ++kg) {
+        // A values for k = 4kg .. 4kg+3 of this thread's 8 rows.
+        const uint32_t x0 = static_cast<uint32_t>((kg ^ tr) << 4);
+        const uint32_t x1 = x0 ^ 64u;  // rows with (row % 8) >= 4
+        float4 a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          a[i] = *reinterpret_cast<const float4*>(a_st + 512 * i + ((i & 1) ? x1 : x0));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          float4 b[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            b[jj] = *reinterpret_cast<const float4*>(b_st + (kg * 4 + kk) * (S::BN * 4) +
+                                                     128 * jj);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              acc[i][jj * 4 + 0] = fmaf(av, b[jj].x, acc[i][jj * 4 + 0]);
+              acc[i][jj * 4 + 1] = fmaf(av, b[jj].y, acc[i][jj * 4 + 1]);
+              acc[i][jj * 4 + 2] = fmaf(av, b[jj].z, acc[i][jj * 4 + 2]);
+              acc[i][jj * 4 + 3] = fmaf(av, b[jj].w, acc[i][jj * 4 + 3]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[s]);
+
+      // Refill: once every warp is done with iteration it-1, its stage takes
+      // iteration it-1+STAGES (one iteration of slack keeps warp 0 from
+      // waiting on the slowest warp of the current iteration).
+      if (producer && it >= 1 && issued < n_iter && issued == it - 1 + S::STAGES) {
+        const uint32_t j = it - 1;
+        if (!mbar_wait(&sm.empty[j % S::STAGES], (j / S::STAGES) & 1, args.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        issue_stage<kTma>(issued, walk, tiles, sm, &map_a, &map_b, args);
+        ++issued;
+      }
+    }
+    if (!ok) break;
+
+    // Epilogue: rows beyond M and columns beyond N are not written.
+    const int row0 = tm * S::BM + warp_m * 32 + tr;
+    const int col0 = tn * S::BN + warp_n * 128 + tc * 4;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = row0 + 4 * i;
+      if (row >= M) continue;
+      float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int col = col0 + 32 * jj;
+        if (args.vec_store && col + 3 < N) {
+          *reinterpret_cast<float4*>(crow + col) =
+              make_float4(acc[i][jj * 4 + 0], acc[i][jj * 4 + 1], acc[i][jj * 4 + 2],
+                          acc[i][jj * 4 + 3]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (col + q < N) crow[col + q] = acc[i][jj * 4 + q];
+        }
+      }
+    }
+  }
+
+  // A CTA that gave up on a wait may still have copies in flight into its own
+  // shared memory: drain them (bounded) before the CTA exits.
+  __syncthreads();
+  if (sm.abort_flag) {
+    if (kTma) {
+      if (threadIdx.x == 0) {
+        const uint32_t first = issued > S::STAGES ? issued - S::STAGES : 0;
+        for (uint32_t j = first; j < issued; ++j)
+          mbar_wait_timed(&sm.full[j % S::STAGES], (j / S::STAGES) & 1, 100000000ull);
+      }
+    } else {
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+  }
+}
+
+template <bool kTma>
+cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
+                   int grid, cudaStream_t stream) {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(sgemm_simt_kernel<kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             S::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  CUtensorMap dummy{};
+  sgemm_simt_kernel<kTma><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(
+      map_a ? *map_a : dummy, map_b ? *map_b : dummy, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sgemm_tma(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                             const GemmArgs& args, int grid, cudaStream_t stream) {
+  return launch<true>(&map_a, &map_b, args, grid, stream);
+}
+
+cudaError_t launch_sgemm_cpasync(const GemmArgs& args, int grid, cudaStream_t stream) {
+  return launch<false>(nullptr, nullptr, args, grid, stream);
+}
+
+}  // namespace gemm14

@@ -1,0 +1,132 @@
+/*
+ * gemm14.h -- C ABI of the GB300 (sm_103a) dense GEMM library libgemm14.so.
+ *
+ * Operation (all entry points): C = A * B with
+ *     C[i][j] = sum_{k < K} A[i][k] * B[k][j],   0 <= i < M, 0 <= j < N,
+ * the matrix product of gpu-hpc-book ch.06 "高级 cuda 特性 —— 从矩阵乘法(gemm)说起"
+ * (Advanced CUDA features, starting from GEMM; opening section and
+ * "缓存缺失与带宽约束分析" item (4)) and of "Kernel 优化指南" (cuda-kernel-academy
+ * module 02), "GEMM 优化路径", Level 1, whose kernels take (M, N, K) and
+ * row-major pointers; this interface adds leading dimensions and a stream.
+ *
+ * Layout: A, B and C are row-major. Element (i, k) of A is A[i * lda + k];
+ * (k, j) of B is B[k * ldb + j]; (i, j) of C is C[i * ldc + j]. Leading
+ * dimensions are counted in elements: lda >= K, ldb >= N, ldc >= N (each at
+ * least 1). C is overwritten (no alpha/beta); A and B are only read. C must
+ * not overlap A or B.
+ *
+ * Pointers are DEVICE pointers in the current CUDA device's address space
+ * (e.g. torch CUDA tensors' data_ptr()). `stream` is a cudaStream_t (NULL =
+ * legacy default stream). Calls are asynchronous: the work is enqueued on
+ * `stream` and the function returns without synchronising. The caller owns
+ * every buffer; the library allocates and frees no device memory and keeps no
+ * pointer after it returns.
+ *
+ * Degenerate sizes: M == 0 or N == 0 returns GEMM14_OK and launches nothing;
+ * K == 0 sets the M x N block of C to zero (the empty sum).
+ *
+ * Errors: every entry point returns a gemm14_status and never aborts, prints
+ * or exits. Invalid arguments are detected on the host before any CUDA call.
+ * A device-side failure (a bounded wait inside a kernel that expired) is
+ * recorded in a device error word and reported by gemm14_check_device_error.
+ *
+ * Only compute capability 10.3 (GB300) is supported; any other device gives
+ * GEMM14_ERR_UNSUPPORTED_DEVICE. Sizes up to 2^31 - 1 per dimension.
+ * Thread safety: all entry points are reentrant.
+ */
+#ifndef GEMM14_H
+#define GEMM14_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gemm14_status {
+  GEMM14_OK = 0,
+  GEMM14_ERR_INVALID_ARG = 1,        /* negative or too large size, ld too small, NULL
+                                        pointer with a non-empty extent, misaligned
+                                        element pointer, bad dtype */
+  GEMM14_ERR_UNSUPPORTED_DEVICE = 2, /* no CUDA device, or it is not compute capability 10.3 */
+  GEMM14_ERR_CUDA = 3,               /* a CUDA runtime/driver call failed; see
+                                        gemm14_last_error_string() */
+  GEMM14_ERR_TIMEOUT = 4             /* a kernel's bounded wait expired (device-side) */
+} gemm14_status;
+
+/* Element types for the planning query. */
+enum { GEMM14_DTYPE_F32 = 0, GEMM14_DTYPE_BF16 = 1, GEMM14_DTYPE_F16 = 2 };
+
+/*
+ * fp32 inputs, fp32 FFMA accumulation on the CUDA cores, fp32 output.
+ * A, B, C: 4-byte aligned. The fast loader (TMA) is used when A and B are
+ * 16-byte aligned and lda, ldb are multiples of 4; otherwise an equivalent
+ * cp.async loader is used (same results). 16-byte stores are used for C when
+ * C is 16-byte aligned and ldc is a multiple of 4.
+ * Follows the register-tiled, shared-memory-tiled kernels of gpu-hpc-book
+ * ch.06, "矩阵乘法中的分块与数据复用" (Shared Memory Tiling, Register Tiling).
+ */
+int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
+             int64_t ldb, float* C, int64_t ldc, void* stream);
+
+/*
+ * bf16 inputs (raw bfloat16 bit patterns), fp32 accumulation on the tensor
+ * cores (tcgen05), fp32 output. Inputs are rounded to bf16 by the caller.
+ * A, B: 2-byte aligned; C: 4-byte aligned. The fast loader (TMA) is used when
+ * A and B are 16-byte aligned and lda, ldb are multiples of 8; otherwise a
+ * software loader fills the same shared-memory tiles (same results, slower).
+ * The tensor-core path of "Kernel 优化指南", "Level 4: Tensor Cores (WMMA)"
+ * (half-precision inputs, float accumulator), and of gpu-hpc-book ch.06,
+ * "Tensor Cores".
+ */
+int gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                     const void* B, int64_t ldb, float* C, int64_t ldc, void* stream);
+
+/* As gemm_bf16_f32acc with IEEE binary16 (fp16) inputs. */
+int gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                    int64_t ldb, float* C, int64_t ldc, void* stream);
+
+/* Static text for a status code (never NULL). */
+const char* gemm14_status_string(int status);
+
+/* Text of the last CUDA failure seen by this thread ("" if none). */
+const char* gemm14_last_error_string(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word. Returns GEMM14_ERR_TIMEOUT if a kernel recorded an expired wait since
+ * the last check, GEMM14_ERR_CUDA if the synchronisation failed, else OK.
+ */
+int gemm14_check_device_error(void* stream);
+
+/* Launch plan chosen for a call (host-side only; no CUDA call is made). */
+typedef struct gemm14_plan {
+  int kernel;     /* 1 = fp32 SIMT (FFMA), 2 = tcgen05 tensor core, 0 = no launch */
+  int loader;     /* 1 = TMA, 2 = software loader (cp.async for fp32), 0 = none */
+  int bm, bn, bk; /* output tile rows x columns, k-block depth */
+  int stages;     /* shared-memory ring depth */
+  int threads;    /* threads per CTA */
+  int smem_bytes; /* dynamic shared memory per CTA */
+  int vec_store;  /* 1 if C takes 16-byte stores */
+  int64_t tiles;  /* output tiles */
+  int grid;       /* CTAs launched (persistent: min(tiles, sm_count)) */
+} gemm14_plan;
+
+/*
+ * Fills *plan with what the matching gemm_* call would launch on a GPU with
+ * `sm_count` SMs. Validates arguments exactly like the entry points (pointers
+ * are only inspected for NULL and alignment, never dereferenced). Returns a
+ * gemm14_status; makes no CUDA call.
+ */
+int gemm14_plan_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                     const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
+                     gemm14_plan* plan);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gemm14_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM14_H */

@@ -1,0 +1,76 @@
+"""Helpers for the GPU tests: run the library through its C ABI on buffers
+with chosen leading dimensions and offsets, and compare with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import dense_gemm_14_gb300 as g14
+from dense_gemm_14_gb300 import inputs
+
+# Element-wise bounds |C - C_ref| <= tol * (|A||B|)_ij (inputs as rounded).
+TOL = {"f32": 1e-5, "bf16": 4e-3, "f16": 4e-3}
+ENTRY = {"f32": g14.gemm_f32, "bf16": g14.gemm_bf16_f32acc, "f16": g14.gemm_f16_f32acc}
+
+
+def dtype_name(t: torch.Tensor) -> str:
+    return {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}[t.dtype]
+
+
+def to_device_padded(x: torch.Tensor, ld: int, offset_elems: int = 0) -> tuple[torch.Tensor, torch.Tensor]:
+    """Copies a (rows, cols) CPU matrix into a device buffer with row pitch ld,
+    starting offset_elems into the buffer. Returns (buffer, view)."""
+    rows, cols = x.shape
+    buf = torch.zeros(offset_elems + max(rows, 1) * ld + 16, dtype=x.dtype, device="cuda")
+    view = buf[offset_elems:offset_elems + rows * ld].view(rows, ld)[:, :cols] if rows else \
+        buf[offset_elems:offset_elems].view(0, ld)[:, :cols]
+    view.copy_(x.to("cuda"))
+    return buf, view
+
+
+def run_abi(A: torch.Tensor, B: torch.Tensor, lda=None, ldb=None, ldc=None, a_off=0, b_off=0,
+            c_off=0, stream=None, poison=True, check_err=True):
+    """C = A @ B through the C ABI entry point for A's dtype. Returns C (CPU fp32)."""
+    M, K = A.shape
+    _, N = B.shape
+    lda = lda or max(K, 1)
+    ldb = ldb or max(N, 1)
+    ldc = ldc or max(N, 1)
+    _abuf, a = to_device_padded(A, lda, a_off)
+    _bbuf, b = to_device_padded(B, ldb, b_off)
+    cbuf = torch.full((c_off + max(M, 1) * ldc + 16,), float("nan") if poison else 0.0,
+                      dtype=torch.float32, device="cuda")
+    c_ptr = cbuf.data_ptr() + 4 * c_off
+    s = stream if stream is not None else torch.cuda.current_stream()
+    ENTRY[dtype_name(A)](M, N, K, a.data_ptr() if M and K else 0, lda,
+                         b.data_ptr() if K and N else 0, ldb, c_ptr, ldc, s.cuda_stream)
+    if check_err:
+        st = g14.check_device_error(s.cuda_stream)
+        assert st == 0, g14.status_string(st)
+    torch.cuda.synchronize()
+    if M == 0:
+        return torch.empty((0, N))
+    C = cbuf[c_off:c_off + M * ldc].view(M, ldc)[:, :N].cpu()
+    return C
+
+
+def oracle_check(oracle_mod, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, rows=None):
+    """Element-wise comparison with the oracle on all rows (or the given rows)."""
+    dt = dtype_name(A)
+    Ah = inputs.host_view(A)
+    Bh = inputs.host_view(B)
+    if rows is not None:
+        Ah = np.ascontiguousarray(Ah[rows])
+        Cg = C.numpy()[rows]
+    else:
+        Cg = C.numpy()
+    ref, refabs = oracle_mod.gemm(Ah, Bh, dt)
+    ok, worst = oracle_mod.within_bound(Cg, ref, refabs, TOL[dt])
+    if not ok:
+        diff = np.abs(Cg.astype(np.float64) - ref) - TOL[dt] * refabs
+        bad = np.argwhere(~(diff <= 0))
+        i, j = bad[0]
+        raise AssertionError(
+            f"{dt} {tuple(A.shape)}x{tuple(B.shape)}: {len(bad)} elements out of bound; "
+            f"first at ({i},{j}) gpu={Cg[i, j]!r} ref={ref[i, j]!r} abs={refabs[i, j]!r}; worst={worst:.3g}")
+    return worst

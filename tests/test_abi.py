@@ -1,0 +1,139 @@
+"""The C ABI on the host: the library loads, exports every symbol the header
+declares, validates arguments before touching CUDA, and plans launches.
+No GPU needed (nothing here enqueues work)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_gemm_14_gb300 as g14
+from dense_gemm_14_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm14.h")
+
+F32, BF16, F16 = g14.GEMM14_DTYPE_F32, g14.GEMM14_DTYPE_BF16, g14.GEMM14_DTYPE_F16
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dense_gemm_14_gb300 import build
+    build.build()
+    return g14.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_three_entry_points():
+    names = declared_functions()
+    for n in ("gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _lib.SIGNATURES, f"binding lacks {n}"
+
+
+def test_status_strings(lib):
+    assert g14.status_string(0) == "ok"
+    for s in range(1, 5):
+        assert g14.status_string(s) and g14.status_string(s) != "unknown status"
+    assert g14.status_string(99) == "unknown status"
+    assert g14.version() >= 100
+
+
+P = 0x10000  # a 64 KiB-aligned fake device address (never dereferenced)
+
+
+@pytest.mark.parametrize("fn", [g14.gemm_f32, g14.gemm_bf16_f32acc, g14.gemm_f16_f32acc])
+@pytest.mark.parametrize("args", [
+    (-1, 4, 4, P, 4, P, 4, P, 4),        # negative M
+    (4, -1, 4, P, 4, P, 4, P, 4),        # negative N
+    (4, 4, -2, P, 4, P, 4, P, 4),        # negative K
+    (1 << 31, 4, 4, P, 4, P, 4, P, 4),   # M beyond int32
+    (4, 4, 8, P, 4, P, 4, P, 4),         # lda < K
+    (4, 8, 4, P, 8, P, 4, P, 8),         # ldb < N
+    (4, 8, 4, P, 8, P, 8, P, 4),         # ldc < N
+    (4, 4, 4, 0, 8, P, 8, P, 8),         # A NULL
+    (4, 4, 4, P, 8, 0, 8, P, 8),         # B NULL
+    (4, 4, 4, P, 8, P, 8, 0, 8),         # C NULL
+    (4, 4, 4, P, 8, P, 8, P + 2, 8),     # C misaligned
+])
+def test_invalid_arguments_rejected_before_cuda(lib, fn, args):
+    assert fn(*args, None, check=False) == _lib.GEMM14_ERR_INVALID_ARG
+
+
+def test_loader_choice_follows_tma_rules(lib):
+    # 16-bit operands: TMA needs 16-byte bases and pitches (multiples of 8 elements)
+    st, p = g14.plan(BF16, 4, 8, 4, P, 8, P, 8, P, 8, 152)
+    assert st == 0 and p.loader == 1
+    st, p = g14.plan(BF16, 4, 8, 4, P, 12, P, 8, P, 8, 152)
+    assert st == 0 and p.loader == 2
+    st, p = g14.plan(F16, 4, 8, 4, P + 8, 8, P, 8, P, 8, 152)
+    assert st == 0 and p.loader == 2
+    # an odd byte address is not an element address
+    assert g14.gemm_bf16_f32acc(4, 8, 4, P + 1, 8, P, 8, P, 8, None, check=False) == 1
+    # fp32: any 4-byte aligned pointer/pitch (cp.async loader)
+    st, p = g14.plan(F32, 4, 8, 5, P + 4, 5, P + 4, 9, P, 8, 152)
+    assert st == 0 and p.loader == 2
+    assert g14.gemm_f32(4, 8, 4, P + 2, 8, P, 8, P, 8, None, check=False) == 1
+
+
+def test_empty_product_is_a_no_op(lib):
+    # M == 0 or N == 0: OK without any CUDA call (works without a GPU)
+    assert g14.gemm_f32(0, 4, 4, 0, 4, 0, 4, 0, 4, None, check=False) == 0
+    assert g14.gemm_bf16_f32acc(4, 0, 4, 0, 8, 0, 8, 0, 1, None, check=False) == 0
+
+
+def test_plan_fp32_tma_and_fallback(lib):
+    st, p = g14.plan(F32, 3072, 3072, 3072, P, 3072, P, 3072, P, 3072, 152)
+    assert st == 0
+    assert (p.kernel, p.loader, p.bm, p.bn, p.bk) == (1, 1, 128, 256, 32)
+    assert p.tiles == 24 * 12 and p.grid == 152 and p.vec_store == 1
+    assert p.smem_bytes <= 227 * 1024 and p.threads == 256
+    # the ragged workload breaks TMA's 16-byte pitch rule -> cp.async loader, scalar stores
+    st, p = g14.plan(F32, 4097, 3001, 513, P, 513, P, 3001, P, 3001, 152)
+    assert st == 0 and p.loader == 2 and p.vec_store == 0
+    assert p.tiles == 33 * 12
+    # few tiles -> grid = tiles
+    st, p = g14.plan(F32, 256, 256, 256, P, 256, P, 256, P, 256, 152)
+    assert p.tiles == 2 and p.grid == 2
+
+
+@pytest.mark.parametrize("N,bn", [(1, 64), (64, 64), (65, 128), (128, 128), (129, 256), (11008, 256)])
+def test_plan_tensor_core_tile_width(lib, N, bn):
+    st, p = g14.plan(BF16, 16384, N, 4096, P, 4096, P, ((N + 7) // 8) * 8, P, N, 152)
+    assert st == 0 and p.kernel == 2 and p.bn == bn and p.bm == 128 and p.bk == 64
+    assert p.smem_bytes <= 227 * 1024
+    assert p.tiles == 128 * ((N + bn - 1) // bn)
+
+
+def test_plan_k_zero_launches_nothing(lib):
+    st, p = g14.plan(F16, 10, 10, 0, 0, 1, 0, 16, P, 16, 152)
+    assert st == 0 and p.kernel == 0
+
+
+def test_no_gpu_gives_a_status_not_a_crash(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = g14.gemm_f32(4, 4, 4, P, 4, P, 4, P, 4, None, check=False)
+    assert st in (_lib.GEMM14_ERR_UNSUPPORTED_DEVICE, _lib.GEMM14_ERR_CUDA)
+    with pytest.raises(g14.Gemm14Error):
+        g14.gemm_f32(4, 4, 4, P, 4, P, 4, P, 4, None)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setenv("GEMM14_LIB", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _lib.load()

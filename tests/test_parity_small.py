@@ -1,0 +1,183 @@
+"""GPU parity at sizes the oracle checks element by element: several tiles,
+ragged tails, both fp32 loaders, every tensor-core tile width, exact
+integer sums, structured matrices that expose layout bugs, and the
+degenerate sizes. All calls go through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_14_gb300 as g14
+from dense_gemm_14_gb300 import inputs
+
+from gpu_util import oracle_check, run_abi
+
+pytestmark = pytest.mark.gpu
+
+
+def rup(x, m):
+    return (x + m - 1) // m * m
+
+
+F32_SHAPES = [(1, 1, 1), (3, 5, 7), (17, 33, 5), (128, 256, 32), (129, 257, 33),
+              (300, 520, 200), (64, 1000, 96), (1000, 70, 513), (513, 769, 1025)]
+
+
+@pytest.mark.parametrize("M,N,K", F32_SHAPES)
+def test_f32_tma_loader(oracle_mod, M, N, K):
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=M * 7 + N * 3 + K)
+    # pitches rounded to 4 elements -> TMA loader and vector stores
+    C = run_abi(A, B, lda=rup(K, 4), ldb=rup(N, 4), ldc=rup(N, 4))
+    oracle_check(oracle_mod, A, B, C)
+
+
+@pytest.mark.parametrize("M,N,K", F32_SHAPES)
+def test_f32_cpasync_loader(oracle_mod, M, N, K):
+    A, B = inputs.make(M, N, K, "f32", "normal", 1.0, seed=M + N + K)
+    # odd pitches and 4-byte offsets break TMA's rules -> cp.async loader, scalar stores
+    C = run_abi(A, B, lda=K + 1 if (K + 1) % 4 else K + 2, ldb=N + 1 if (N + 1) % 4 else N + 2,
+                ldc=N + 1, a_off=1, b_off=3, c_off=1)
+    oracle_check(oracle_mod, A, B, C)
+
+
+TC_SHAPES = [(1, 1, 1), (5, 7, 3), (128, 64, 64), (128, 128, 64), (128, 256, 64),
+             (200, 300, 100), (257, 129, 1000), (129, 65, 130), (512, 512, 512), (384, 1000, 200)]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", TC_SHAPES)
+def test_tensor_core(oracle_mod, dt, M, N, K):
+    A, B = inputs.make(M, N, K, dt, "normal", 1.0 / max(K, 1) ** 0.5, seed=M * 5 + N + K)
+    C = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), ldc=N)
+    oracle_check(oracle_mod, A, B, C)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_tensor_core_padded_pitches(oracle_mod, dt):
+    A, B = inputs.make(300, 200, 150, dt, "uniform", 1.0, seed=3)
+    C = run_abi(A, B, lda=160, ldb=264, ldc=203, a_off=8, b_off=16, c_off=3)
+    oracle_check(oracle_mod, A, B, C)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (190, 300, 257), (128, 64, 130), (300, 129, 77)])
+def test_tensor_core_software_loader(oracle_mod, dt, M, N, K):
+    """Pitches that are not multiples of 8 elements and 2-byte offsets: the
+    software loader must give the same results as the TMA path."""
+    A, B = inputs.make(M, N, K, dt, "normal", 0.25, seed=M + 2 * N + 3 * K)
+    C = run_abi(A, B, lda=K + 1, ldb=N + 3, ldc=N + 1, a_off=1, b_off=5, c_off=2)
+    oracle_check(oracle_mod, A, B, C)
+    C_tma = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), ldc=N)
+    assert torch.equal(C, C_tma)
+
+
+# ------------------------------------------------------------------ exact results
+
+def test_f32_integer_exact():
+    """Entries in [-3, 3], K = 3072: every partial sum is an integer below 2^24,
+    so any summation order gives the exact result bit for bit."""
+    A, B = inputs.make_integer(300, 520, 3072, 3, "f32", seed=21)
+    C = run_abi(A, B)
+    assert torch.equal(C, (A.double() @ B.double()).float())
+    C = run_abi(A, B, lda=3073, ldb=521, ldc=521)  # cp.async loader
+    assert torch.equal(C, (A.double() @ B.double()).float())
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_tensor_core_integer_exact(dt):
+    """Entries in [-4, 4], K = 8192: partial sums stay below 2^24 -> exact."""
+    A, B = inputs.make_integer(256, 320, 8192, 4, dt, seed=22)
+    C = run_abi(A, B)
+    assert torch.equal(C, (A.double() @ B.double()).float())
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+def test_permutation_and_identity(dt):
+    """P @ B must return the rows of B permuted and A @ I must return A, bit
+    for bit: a wrong tile index, swizzle or descriptor shows here."""
+    td = inputs.torch_dtype(dt)
+    g = torch.Generator().manual_seed(23)
+    K = 320
+    perm = torch.randperm(K, generator=g)
+    P = torch.zeros(K, K)
+    P[torch.arange(K), perm] = 1
+    B = (torch.rand(K, 264, generator=g) * 2 - 1).to(td)
+    C = run_abi(P.to(td), B)
+    assert torch.equal(C, B.float()[perm])
+    A = (torch.rand(200, K, generator=g) * 2 - 1).to(td)
+    C = run_abi(A, torch.eye(K).to(td))
+    assert torch.equal(C, A.float())
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_rank_one_closed_form(dt):
+    td = inputs.torch_dtype(dt)
+    M, N, K = 260, 300, 96
+    a = (torch.arange(M) % 7 + 1).float()
+    b = (torch.arange(N) % 5 + 1).float()
+    A = a[:, None].expand(M, K).contiguous().to(td)
+    B = b[None, :].expand(K, N).contiguous().to(td)
+    C = run_abi(A, B)
+    assert torch.equal(C, K * torch.outer(a, b))
+
+
+def test_f16_subnormal_inputs(oracle_mod):
+    """fp16 subnormals are values, not zeros, on the tensor-core path."""
+    g = torch.Generator().manual_seed(24)
+    A = (torch.randint(1, 1024, (128, 64), generator=g) * 2.0 ** -24).half()  # all subnormal
+    B = torch.randint(-8, 9, (64, 128), generator=g).float().half()
+    C = run_abi(A, B)
+    assert torch.equal(C, (A.double() @ B.double()).float())
+    oracle_check(oracle_mod, A, B, C)
+
+
+# ------------------------------------------------------------------ degenerate sizes
+
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+def test_k_zero_zeroes_c(dt):
+    td = inputs.torch_dtype(dt)
+    A = torch.zeros(7, 0, dtype=td)
+    B = torch.zeros(0, 9, dtype=td)
+    C = run_abi(A, B, lda=8, ldb=16, ldc=11)
+    assert C.shape == (7, 9) and torch.all(C == 0)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_empty_m_or_n(dt):
+    td = inputs.torch_dtype(dt)
+    assert run_abi(torch.zeros(0, 8, dtype=td), torch.zeros(8, 8, dtype=td)).shape == (0, 8)
+    C = run_abi(torch.ones(8, 8, dtype=td), torch.zeros(8, 0, dtype=td), ldb=8, ldc=8)
+    assert C.shape == (8, 0)
+
+
+def test_nan_propagates_along_its_row():
+    A, B = inputs.make(130, 260, 64, "f32", "uniform", 1.0, seed=25)
+    A[5, 10] = float("nan")
+    C = run_abi(A, B)
+    assert torch.isnan(C[5]).all()
+    assert not torch.isnan(C[torch.arange(130) != 5]).any()
+
+
+# ------------------------------------------------------------------ streams, API, determinism
+
+def test_non_default_stream_and_repeatability():
+    A, B = inputs.make(700, 900, 333, "f32", "normal", 1.0, seed=26)
+    s = torch.cuda.Stream()
+    C1 = run_abi(A, B, stream=s)
+    C2 = run_abi(A, B)
+    assert torch.equal(C1, C2)  # run-to-run deterministic (no atomics)
+
+
+def test_tensor_api_cuda_and_host():
+    A, B = inputs.make(257, 300, 190, "bf16", "normal", 0.1, seed=27)
+    want = run_abi(A, B)
+    got_dev = g14.gemm(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(got_dev.cpu(), want)
+    got_host = g14.gemm(A, B)  # host tensors: copied in, computed, copied back
+    assert got_host.device.type == "cpu" and torch.equal(got_host, want)
+
+
+def test_device_error_word_is_clear_after_good_calls():
+    A, B = inputs.make(256, 256, 256, "f32", "uniform", 1.0, seed=28)
+    run_abi(A, B, check_err=False)
+    assert g14.check_device_error(None) == 0
