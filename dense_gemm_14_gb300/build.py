@@ -47,20 +47,27 @@ def _stale(lib: str, inputs) -> bool:
     return any(os.path.getmtime(p) > t for p in inputs)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compiles every .cu and links libgemm14.so; returns its path."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str | None = None) -> str:
+    """Compiles every .cu and links libgemm14.so; returns its path.
+
+    extra_flags (e.g. schedule macros such as -DSGEMM_UNROLL=2) and out_dir
+    allow building variants side by side; the default build is the product.
+    """
+    build_dir = out_dir or BUILD_DIR
+    lib_path = os.path.join(build_dir, LIB_NAME)
+    os.makedirs(build_dir, exist_ok=True)
     inputs = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
     inputs.append(os.path.join(INCLUDE, "gemm14.h"))
     inputs.append(os.path.abspath(__file__))
-    if not force and not _stale(LIB_PATH, inputs):
-        return LIB_PATH
+    if not force and not extra_flags and not _stale(lib_path, inputs):
+        return lib_path
     cc = nvcc()
     procs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        log = os.path.join(BUILD_DIR, src.replace(".cu", ".ptxas.log"))
-        cmd = [cc, *NVCC_FLAGS, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
+        log = os.path.join(build_dir, src.replace(".cu", ".ptxas.log"))
+        cmd = [cc, *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-c", os.path.join(CSRC, src),
+               "-o", obj]
         fh = open(log, "w")
         procs.append((src, obj, log, fh, subprocess.Popen(cmd, stdout=fh, stderr=subprocess.STDOUT)))
     failed = []
@@ -74,12 +81,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if failed:
         msgs = "\n".join(f"--- {s} ---\n{open(l).read()}" for s, l in failed)
         raise RuntimeError(f"nvcc failed for {[s for s, _ in failed]}:\n{msgs}")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     objs = [o for _, o, _, _, _ in procs]
     subprocess.run([cc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a",
                     "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 def main() -> None:

@@ -33,10 +33,64 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+// Schedule parameters of the inner loop (defaults are the measured best):
+//   SGEMM_AK      k values per A-fragment load: 4 (float4) or 2 (float2)
+//   SGEMM_UNROLL  unroll factor of the loop over A fragments in a k-block
+//   SGEMM_B_OUTER 0: FFMAs ordered row-major over the 8 x 16 block (A value
+//                 reused across 16 FFMAs); 1: column-major (B value reused)
+#ifndef SGEMM_AK
+#define SGEMM_AK 4
+#endif
+#ifndef SGEMM_UNROLL
+#define SGEMM_UNROLL 8
+#endif
+#ifndef SGEMM_B_OUTER
+#define SGEMM_B_OUTER 0
+#endif
+//   SGEMM_FFMA2   1: packed fp32x2 FMAs (fma.rn.f32x2, two IEEE fp32 FMAs per
+//                 instruction, same rounding as fmaf); 0: scalar fmaf
+#ifndef SGEMM_FFMA2
+#define SGEMM_FFMA2 1
+#endif
+#define GEMM14_PRAGMA(x) _Pragma(#x)
+#define GEMM14_UNROLL(n) GEMM14_PRAGMA(unroll n)
+
 namespace gemm14 {
 namespace {
 
 using S = SgemmShape;
+constexpr int kAK = SGEMM_AK;
+static_assert(kAK == 2 || kAK == 4, "A fragments are float2 or float4");
+
+template <int AK> struct AFrag;
+template <> struct AFrag<4> {
+  using T = float4;
+  static __device__ __forceinline__ float get(const float4& v, int kk) {
+    return kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w;
+  }
+};
+template <> struct AFrag<2> {
+  using T = float2;
+  static __device__ __forceinline__ float get(const float2& v, int kk) {
+    return kk == 0 ? v.x : v.y;
+  }
+};
+
+// Two fp32 values in one 64-bit register (low half = first value).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+// d = a * b + d on both halves, each an IEEE fp32 fma (round to nearest).
+__device__ __forceinline__ void fma2(uint64_t& d, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
 
 struct SgemmSmem {
   uint64_t full[S::STAGES];
@@ -172,36 +226,79 @@ __global__ void __launch_bounds__(S::THREADS, 1)
   for (int lt = 0; lt < my_tiles && ok; ++lt) {
     const int tile = blockIdx.x + lt * gridDim.x;
     const int tm = tile % walk.tiles_m, tn = tile / walk.tiles_m;
+#if SGEMM_FFMA2
+    // acc2[i][2*jj + h] holds columns 4*jj + 2*h and 4*jj + 2*h + 1 of row i.
+    uint64_t acc2[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc2[i][j] = 0ull;
+#else
     float acc[8][16];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[i][j] = 0.f;
+#endif
 
     for (int kb = 0; kb < walk.kblocks; ++kb, ++it) {
       const uint32_t s = it % S::STAGES, ph = (it / S::STAGES) & 1;
       if (!mbar_wait(&sm.full[s], ph, args.err, abort_flag)) { ok = false; break; }
       const uint8_t* a_st = tiles + s * S::STAGE_BYTES + a_thread;
       const uint8_t* b_st = tiles + s * S::STAGE_BYTES + S::A_STAGE_BYTES + b_thread;
-#pragma unroll
-      for (int kg = 0; kg < S::BK / 4; ++kg) {
-        // A values for k = 4kg .. 4kg+3 of this thread's 8 rows.
-        const uint32_t x0 = static_cast<uint32_t>((kg ^ tr) << 4);
+      GEMM14_UNROLL(SGEMM_UNROLL)
+      for (int kg = 0; kg < S::BK / kAK; ++kg) {
+        // A values for k = kAK*kg .. kAK*kg + kAK-1 of this thread's 8 rows:
+        // 16-byte chunk (kAK*kg)/4, XOR-swizzled by (row % 8) = tr + 4*(i % 2).
+        const int k0 = kg * kAK;
+        const uint32_t x0 = static_cast<uint32_t>((((k0 >> 2) ^ tr) << 4) + (k0 & 3) * 4);
         const uint32_t x1 = x0 ^ 64u;  // rows with (row % 8) >= 4
-        float4 a[8];
+        typename AFrag<kAK>::T a[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          a[i] = *reinterpret_cast<const float4*>(a_st + 512 * i + ((i & 1) ? x1 : x0));
+          a[i] = *reinterpret_cast<const typename AFrag<kAK>::T*>(a_st + 512 * i +
+                                                                 ((i & 1) ? x1 : x0));
+#if SGEMM_FFMA2
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
+        for (int kk = 0; kk < kAK; ++kk) {
+          ulonglong2 b[4];  // (cols 4jj, 4jj+1), (cols 4jj+2, 4jj+3)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            b[jj] = *reinterpret_cast<const ulonglong2*>(b_st + (k0 + kk) * (S::BN * 4) +
+                                                         128 * jj);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float av = AFrag<kAK>::get(a[i], kk);
+            const uint64_t a2 = pack2(av, av);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              fma2(acc2[i][2 * jj + 0], a2, b[jj].x);
+              fma2(acc2[i][2 * jj + 1], a2, b[jj].y);
+            }
+          }
+        }
+#else
+#pragma unroll
+        for (int kk = 0; kk < kAK; ++kk) {
           float4 b[4];
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj)
-            b[jj] = *reinterpret_cast<const float4*>(b_st + (kg * 4 + kk) * (S::BN * 4) +
-                                                     128 * jj);
+            b[jj] = *reinterpret_cast<const float4*>(b_st + (k0 + kk) * (S::BN * 4) + 128 * jj);
+#if SGEMM_B_OUTER
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float bv = q == 0 ? b[jj].x : q == 1 ? b[jj].y : q == 2 ? b[jj].z : b[jj].w;
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                acc[i][jj * 4 + q] = fmaf(AFrag<kAK>::get(a[i], kk), bv, acc[i][jj * 4 + q]);
+            }
+          }
+#else
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+            const float av = AFrag<kAK>::get(a[i], kk);
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
               acc[i][jj * 4 + 0] = fmaf(av, b[jj].x, acc[i][jj * 4 + 0]);
@@ -210,7 +307,9 @@ __global__ void __launch_bounds__(S::THREADS, 1)
               acc[i][jj * 4 + 3] = fmaf(av, b[jj].w, acc[i][jj * 4 + 3]);
             }
           }
+#endif
         }
+#endif
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[s]);
@@ -238,17 +337,28 @@ __global__ void __launch_bounds__(S::THREADS, 1)
       const int row = row0 + 4 * i;
       if (row >= M) continue;
       float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
+#if SGEMM_FFMA2
+      float acc_row[16];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 v = unpack2(acc2[i][j]);
+        acc_row[2 * j] = v.x;
+        acc_row[2 * j + 1] = v.y;
+      }
+#else
+      const float* acc_row = acc[i];
+#endif
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         const int col = col0 + 32 * jj;
         if (args.vec_store && col + 3 < N) {
           *reinterpret_cast<float4*>(crow + col) =
-              make_float4(acc[i][jj * 4 + 0], acc[i][jj * 4 + 1], acc[i][jj * 4 + 2],
-                          acc[i][jj * 4 + 3]);
+              make_float4(acc_row[jj * 4 + 0], acc_row[jj * 4 + 1], acc_row[jj * 4 + 2],
+                          acc_row[jj * 4 + 3]);
         } else {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            if (col + q < N) crow[col + q] = acc[i][jj * 4 + q];
+            if (col + q < N) crow[col + q] = acc_row[jj * 4 + q];
         }
       }
     }
