@@ -61,6 +61,9 @@ def parse_args():
                     help="target oracle seconds per part for cpu_baseline")
     ap.add_argument("--only", choices=[p[0] for p in PARTS], default=None,
                     help="time one part only (for profiling; not a bench line)")
+    ap.add_argument("--table", action="store_true",
+                    help="time every named workload alone and print one JSON line per workload "
+                         "(the parity workloads' speeds; not the bench line)")
     return ap.parse_args()
 
 
@@ -201,25 +204,28 @@ def time_oracle_sample(name: str, target_s: float, A=None, B=None):
     if A is None:
         A, B = inputs.make_workload(name)
     Ah, Bh = inputs.host_view(A), inputs.host_view(B)
-    rows = 8
+    M, (K, N) = Ah.shape[0], Bh.shape
+    rows = min(M, 32)
     t0 = time.perf_counter()
     oracle.gemm(Ah[:rows], Bh, w.dtype, with_abs=False)
     probe = time.perf_counter() - t0
-    rows = int(max(8, min(w.M, rows * target_s / max(probe, 1e-6))))
+    rows = int(max(1, min(M, rows * target_s / max(probe, 1e-6))))
     t0 = time.perf_counter()
     oracle.gemm(Ah[:rows], Bh, w.dtype, with_abs=False)
     dt = time.perf_counter() - t0
-    return roofline.flops(rows, w.N, w.K), dt, rows, oracle.max_threads()
+    return roofline.flops(rows, N, K), dt, rows, oracle.max_threads()
 
 
-def run_reference(args, dist: Dist):
-    """The oracle arm: the CPU oracle on host cores, a bounded sample per step."""
+def run_reference(args, dist: Dist, data=None):
+    """The oracle arm: the CPU oracle on host cores, a bounded sample per step.
+    Under torchrun only rank 0 works and prints; `data` overrides the inputs."""
     if dist.rank != 0:
-        return
+        return None
     import oracle
     from dense_gemm_14_gb300 import inputs
     oracle.build()
-    data = {name: inputs.make_workload(name) for name, *_ in PARTS}
+    if data is None:
+        data = {name: inputs.make_workload(name) for name, *_ in PARTS}
     per_step_s = max(0.5, 120.0 / max(1, args.steps + args.warmup)) / len(PARTS)
     # calibrate rows per part once
     rows = {}
@@ -236,7 +242,7 @@ def run_reference(args, dist: Dist):
             oracle.gemm(inputs.host_view(A)[:r], inputs.host_view(B), w.dtype, with_abs=False)
             dt = time.perf_counter() - t0
             if step >= args.warmup:
-                tot_f += 2.0 * r * w.N * w.K
+                tot_f += 2.0 * r * B.shape[1] * B.shape[0]
                 tot_t += dt
     value = tot_f / tot_t / 1e12
     sample = ", ".join(f"first {rows[n]} rows of {n}" for n, *_ in PARTS) + " per step"
@@ -251,6 +257,7 @@ def run_reference(args, dist: Dist):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+    return line
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -408,8 +415,65 @@ def run_ours(args, dist: Dist):
         print(json.dumps(line), flush=True)
 
 
+def run_table(args):
+    """Every named workload timed alone (CUDA events per launch, operand copies
+    rotating over > 2x L2), with its roofline fraction. One JSON line each."""
+    import torch
+
+    import dense_gemm_14_gb300 as g14
+    from dense_gemm_14_gb300 import inputs, roofline
+
+    g14.load()
+    peaks = roofline.measured_peaks()
+    entry = {"f32": g14.gemm_f32, "bf16": g14.gemm_bf16_f32acc, "f16": g14.gemm_f16_f32acc}
+    stream = torch.cuda.current_stream()
+    for name, w in inputs.WORKLOADS.items():
+        _, fl, ib = workload_info(name)
+        A, B = inputs.make_workload(name)
+        per_set = A.numel() * A.element_size() + B.numel() * B.element_size() + w.M * w.N * 4
+        nsets = max(2, -(-2 * L2_BYTES // per_set))
+        sets = [(A.cuda(), B.cuda(), torch.empty(w.M, w.N, device="cuda")) for _ in range(nsets)]
+        fn = entry[w.dtype]
+
+        def launch(i):
+            a, b, c = sets[i % nsets]
+            fn(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N,
+               stream.cuda_stream)
+
+        for i in range(args.warmup):
+            launch(i)
+        reps = max(args.steps, 5)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        for i, (e0, e1) in enumerate(evs):
+            e0.record(stream)
+            launch(i)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if g14.check_device_error(stream.cuda_stream):
+            raise RuntimeError(f"device error in {name}")
+        ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+        mean = statistics.mean(ms)
+        tf = fl / (mean / 1e3) / 1e12
+        if w.dtype == "f32":
+            peak, kind = roofline.fp32_alu_peak_tflops(), "alu"
+        else:
+            peak, kind = peaks["bf16_tflops_sustained"], "tensor"
+        gbs = ib / (mean / 1e3) / 1e9
+        print(json.dumps({"workload": name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype,
+                          "ms_mean": mean, "ms_min": min(ms), "tflops": tf,
+                          "bound": kind, "peak_tflops": peak, "frac_compute": tf / peak,
+                          "algorithmic_bytes": ib, "gbs": gbs,
+                          "frac_hbm": gbs / peaks["hbm_gbs"]}), flush=True)
+        del sets
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
+    if args.table:
+        run_table(args)
+        return
     dist = Dist(args.gpus)
     try:
         if args.impl == "reference":

@@ -41,6 +41,7 @@ SIGNATURES = {
     "gemm14_plan_gemm": (_int, [_int, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int,
                                 ctypes.POINTER(_Plan)]),
     "gemm14_version": (_int, []),
+    "gemm14_debug_inject": (_int, [_int, ctypes.c_uint64]),
 }
 
 _lib = None
@@ -113,6 +114,12 @@ def gemm_f16_f32acc(M, N, K, A, lda, B, ldb, C, ldc, stream=None, check=True) ->
     if check and st:
         raise Gemm14Error(st, "gemm_f16_f32acc")
     return st
+
+
+def debug_inject(fault: int, wait_limit_ns: int = 0) -> int:
+    """Failure-detection hook: the next call on this thread runs with `fault`
+    (1 = the producer never loads its first stage) and the given wait limit."""
+    return int(load().gemm14_debug_inject(fault, wait_limit_ns))
 
 
 def check_device_error(stream=None) -> int:

@@ -24,6 +24,10 @@ __device__ unsigned g_device_error;
 
 thread_local char t_last_error[256] = "";
 
+// One-shot request from gemm14_debug_inject for the next call on this thread.
+thread_local int t_fault = kFaultNone;
+thread_local unsigned long long t_wait_limit_ns = 0;
+
 void set_cuda_error(const char* what, cudaError_t e) {
   std::snprintf(t_last_error, sizeof t_last_error, "%s: %s (%d)", what, cudaGetErrorString(e),
                 static_cast<int>(e));
@@ -203,6 +207,11 @@ int finish(cudaError_t e, const char* what, cudaStream_t stream) {
 
 int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
              const void* B, int64_t ldb, float* C, int64_t ldc, void* stream_ptr) {
+  // A pending test request applies to this call only, whatever its outcome.
+  const int fault = t_fault;
+  const unsigned long long wait_limit_ns = t_wait_limit_ns ? t_wait_limit_ns : kWaitTimeoutNs;
+  t_fault = kFaultNone;
+  t_wait_limit_ns = 0;
   int st = validate(dtype, M, N, K, A, lda, B, ldb, C, ldc);
   if (st != GEMM14_OK) return st;
   if (M == 0 || N == 0) return GEMM14_OK;
@@ -219,7 +228,7 @@ int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   gemm14_plan plan;
   plan_for(dtype, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
   GemmArgs args{static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                A, lda, B, ldb, C, ldc, plan.vec_store, dev->err_word};
+                A, lda, B, ldb, C, ldc, plan.vec_store, dev->err_word, wait_limit_ns, fault};
 
   if (dtype == GEMM14_DTYPE_F32) {
     if (plan.loader == 2)
@@ -313,6 +322,13 @@ int gemm14_plan_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, 
   int st = validate(dtype, M, N, K, A, lda, B, ldb, C, ldc);
   if (st != GEMM14_OK) return st;
   plan_for(dtype, M, N, K, A, lda, B, ldb, C, ldc, sm_count, plan);
+  return GEMM14_OK;
+}
+
+int gemm14_debug_inject(int fault, uint64_t wait_limit_ns) {
+  if (fault != kFaultNone && fault != kFaultSkipFirstStage) return GEMM14_ERR_INVALID_ARG;
+  t_fault = fault;
+  t_wait_limit_ns = wait_limit_ns;
   return GEMM14_OK;
 }
 

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(H::THREADS, 1)
   const int tiles_n = (N + BN - 1) / BN;
   const int num_tiles = tiles_m * tiles_n;
   const int kblocks = (K + H::BK - 1) / H::BK;
-  volatile int* abort_flag = &sm.abort_flag;
+  const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns};
   uint32_t prod_it = 0;
   bool mma_issued = false;
 
@@ -162,9 +162,11 @@ __global__ void __launch_bounds__(H::THREADS, 1)
         for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
           const uint32_t s = prod_it % STAGES, ph = (prod_it / STAGES) & 1;
           int got = 1;
-          if (lane == 0) got = mbar_wait(&sm.empty[s], ph ^ 1, args.err, abort_flag) ? 1 : 0;
+          if (lane == 0) got = mbar_wait(&sm.empty[s], ph ^ 1, wc) ? 1 : 0;
           got = __shfl_sync(0xffffffffu, got, 0);
           if (!got) { ok = false; break; }
+          // Failure-detection tests: the first stage is never loaded.
+          if (args.fault == kFaultSkipFirstStage && prod_it == 0) continue;
           soft_load_stage<BN>(tiles + s * STAGE_BYTES, args, tm, tn, kb, lane);
           fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
           mbar_arrive(&sm.full[s]);
@@ -177,7 +179,9 @@ __global__ void __launch_bounds__(H::THREADS, 1)
         tile_coords(t, tiles_m, tiles_n, tm, tn);
         for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
           const uint32_t s = prod_it % STAGES, ph = (prod_it / STAGES) & 1;
-          if (!mbar_wait(&sm.empty[s], ph ^ 1, args.err, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&sm.empty[s], ph ^ 1, wc)) { ok = false; break; }
+          // Failure-detection tests: the first stage is never loaded.
+          if (args.fault == kFaultSkipFirstStage && prod_it == 0) continue;
           uint8_t* a_st = tiles + s * STAGE_BYTES;
           uint8_t* b_st = a_st + A_BYTES;
           mbar_arrive_expect_tx(&sm.full[s], STAGE_BYTES);
@@ -198,12 +202,12 @@ __global__ void __launch_bounds__(H::THREADS, 1)
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
         const int b = local & 1;
         const uint32_t aph = (local >> 1) & 1;
-        if (!mbar_wait(&sm.acc_empty[b], aph ^ 1, args.err, abort_flag)) break;
+        if (!mbar_wait(&sm.acc_empty[b], aph ^ 1, wc)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-          if (!mbar_wait(&sm.full[s], ph, args.err, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&sm.full[s], ph, wc)) { ok = false; break; }
           tc_fence_after_sync();
           const uint32_t a_addr = smem_u32(tiles + s * STAGE_BYTES);
           const uint32_t b_addr = a_addr + A_BYTES;
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(H::THREADS, 1)
       const uint32_t aph = (local >> 1) & 1;
       // One lane waits; the warp then proceeds converged (tcgen05.ld is .sync.aligned).
       int got = 1;
-      if (lane == 0) got = mbar_wait(&sm.acc_full[b], aph, args.err, abort_flag) ? 1 : 0;
+      if (lane == 0) got = mbar_wait(&sm.acc_full[b], aph, wc) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
       tc_fence_after_sync();
@@ -280,7 +284,8 @@ __global__ void __launch_bounds__(H::THREADS, 1)
     if (kTma && warp == 0 && lane == 0) {
       const uint32_t first = prod_it > STAGES ? prod_it - STAGES : 0;
       for (uint32_t j = first; j < prod_it; ++j)
-        mbar_wait_timed(&sm.full[j % STAGES], (j / STAGES) & 1, 100000000ull);
+        if (!(args.fault == kFaultSkipFirstStage && j == 0))
+          mbar_wait_timed(&sm.full[j % STAGES], (j / STAGES) & 1, 100000000ull);
     }
     __syncthreads();
   }

@@ -20,7 +20,12 @@ struct GemmArgs {
   int64_t ldc;
   int vec_store;  // C rows may take 16-byte stores (C 16-B aligned, ldc % 4 == 0)
   unsigned* err;
+  unsigned long long wait_limit_ns;  // time limit of one mbarrier wait
+  int fault;  // kFaultNone, or kFaultSkipFirstStage (failure-detection tests only)
 };
+
+// Fault modes a test may request for one call (see gemm14_debug_inject).
+enum : int { kFaultNone = 0, kFaultSkipFirstStage = 1 };
 
 // ---- fp32 SIMT kernel (sgemm_simt.cu)
 struct SgemmShape {

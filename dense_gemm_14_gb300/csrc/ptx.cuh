@@ -2,10 +2,10 @@
 // use: mbarriers (with bounded waits), TMA tile loads, cp.async with zero fill,
 // and the tcgen05 tensor-core family (TMEM alloc, MMA, commit, TMEM loads).
 //
-// Every wait here is bounded: a wait that does not finish within
-// kWaitTimeoutNs (or that sees the CTA's abort flag) returns false instead of
-// spinning forever, so a protocol bug ends the kernel with an error status
-// instead of hanging the GPU.
+// Every wait here is bounded: a wait that does not finish within its limit
+// (kWaitTimeoutNs unless the call set another) or that sees the CTA's abort
+// flag returns false instead of spinning forever, so a protocol bug ends the
+// kernel with an error status instead of hanging the GPU.
 #pragma once
 
 #include <cstdint>
@@ -16,7 +16,7 @@ namespace gemm14 {
 // Bits OR-ed into the library's device error word.
 enum : unsigned { kDevErrTimeout = 1u, kDevErrBadConfig = 2u };
 
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // default limit of one wait: 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -68,19 +68,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// How a kernel waits: where to report an expired wait, the CTA's abort flag,
+// and the time limit of one wait.
+struct WaitCtx {
+  unsigned* err;
+  volatile int* abort_flag;
+  unsigned long long limit_ns;
+};
+
 // Slow path of mbar_wait: spins with a time limit. On expiry it records
 // kDevErrTimeout in *err and raises the CTA-wide abort flag so the other roles
 // of the CTA stop waiting too.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, unsigned* err,
-                                            volatile int* abort_flag) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                                   const WaitCtx& w) {
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-        atomicOr(err, kDevErrTimeout);
-        *abort_flag = 1;
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.limit_ns) {
+        atomicOr(w.err, kDevErrTimeout);
+        *w.abort_flag = 1;
         return false;
       }
     }
@@ -98,10 +106,9 @@ static __device__ __noinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t pari
 }
 
 // Waits until the barrier phase with the given parity has completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err,
-                                          volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, err, abort_flag);
+  return mbar_wait_slow(bar, parity, w);
 }
 
 // ---------------------------------------------------------------- TMA

@@ -125,6 +125,9 @@ template <bool kTma>
 __device__ __forceinline__ void issue_stage(uint32_t j, const TileWalk& w, uint8_t* tiles,
                                             SgemmSmem& sm, const CUtensorMap* map_a,
                                             const CUtensorMap* map_b, const GemmArgs& args) {
+  // Failure-detection tests: the first stage is never loaded, so every wait
+  // for it must expire and report a timeout.
+  if (args.fault == kFaultSkipFirstStage && j == 0) return;
   int tm, tn, kb;
   w.at(j, tm, tn, kb);
   const uint32_t s = j % S::STAGES;
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(S::THREADS, 1)
                            ? (walk.num_tiles - 1 - blockIdx.x) / gridDim.x + 1
                            : 0;
   const uint32_t n_iter = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(walk.kblocks);
-  volatile int* abort_flag = &sm.abort_flag;
+  const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns};
   const bool producer = kTma ? threadIdx.x == 0 : true;
   uint32_t issued = 0;  // iterations whose loads this thread has issued
 
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(S::THREADS, 1)
 
     for (int kb = 0; kb < walk.kblocks; ++kb, ++it) {
       const uint32_t s = it % S::STAGES, ph = (it / S::STAGES) & 1;
-      if (!mbar_wait(&sm.full[s], ph, args.err, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(&sm.full[s], ph, wc)) { ok = false; break; }
       const uint8_t* a_st = tiles + s * S::STAGE_BYTES + a_thread;
       const uint8_t* b_st = tiles + s * S::STAGE_BYTES + S::A_STAGE_BYTES + b_thread;
       GEMM14_UNROLL(SGEMM_UNROLL)
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(S::THREADS, 1)
       // waiting on the slowest warp of the current iteration).
       if (producer && it >= 1 && issued < n_iter && issued == it - 1 + S::STAGES) {
         const uint32_t j = it - 1;
-        if (!mbar_wait(&sm.empty[j % S::STAGES], (j / S::STAGES) & 1, args.err, abort_flag)) {
+        if (!mbar_wait(&sm.empty[j % S::STAGES], (j / S::STAGES) & 1, wc)) {
           ok = false;
           break;
         }
@@ -372,7 +375,8 @@ __global__ void __launch_bounds__(S::THREADS, 1)
       if (threadIdx.x == 0) {
         const uint32_t first = issued > S::STAGES ? issued - S::STAGES : 0;
         for (uint32_t j = first; j < issued; ++j)
-          mbar_wait_timed(&sm.full[j % S::STAGES], (j / S::STAGES) & 1, 100000000ull);
+          if (!(args.fault == kFaultSkipFirstStage && j == 0))
+            mbar_wait_timed(&sm.full[j % S::STAGES], (j / S::STAGES) & 1, 100000000ull);
       }
     } else {
       asm volatile("cp.async.wait_all;" ::: "memory");

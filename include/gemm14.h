@@ -122,6 +122,20 @@ int gemm14_plan_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, 
                      const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
                      gemm14_plan* plan);
 
+/*
+ * Failure-detection hook for tests. The NEXT gemm_* call made by this thread
+ * runs with the given fault mode and per-wait time limit, then both reset:
+ *   fault 0 = none; 1 = the kernel's producer never loads its first shared-
+ *   memory stage, so every wait for that stage expires after wait_limit_ns,
+ *   the kernel records GEMM14_ERR_TIMEOUT in the device error word, drains
+ *   its in-flight copies and exits; C is left incomplete.
+ *   wait_limit_ns = 0 keeps the default limit (2 s).
+ * No fault makes the GPU fault, trap or hang: waits are bounded, the context
+ * stays usable, and gemm14_check_device_error reports the timeout.
+ * Returns GEMM14_ERR_INVALID_ARG for an unknown mode.
+ */
+int gemm14_debug_inject(int fault, uint64_t wait_limit_ns);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int gemm14_version(void);
 

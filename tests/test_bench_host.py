@@ -1,0 +1,77 @@
+"""Host-side logic of bench.py on the CPU: max-over-ranks timing with two
+gloo ranks, and the oracle (reference) arm on a small sample."""
+import json
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    d = bench.Dist(world)
+    d.barrier()
+    got = d.max(1.5 + rank)
+    with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
+        json.dump({"rank": d.rank, "world": d.world, "max": got}, f)
+    d.close()
+
+
+def test_max_over_ranks_with_gloo(tmp_path):
+    if torch.cuda.is_available():
+        pytest.skip("exercises the CPU (gloo) path")
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+                       start_method="spawn")
+    res = [json.load(open(tmp_path / f"r{r}.json")) for r in range(world)]
+    assert [r["rank"] for r in res] == [0, 1]
+    assert all(r["world"] == 2 and r["max"] == 2.5 for r in res)
+
+
+class _FakeDist:
+    def __init__(self, rank):
+        self.rank, self.world = rank, 2
+
+
+def test_reference_arm_only_rank0_prints(capsys):
+    ns = type("A", (), {"steps": 2, "warmup": 1, "gpus": 2})()
+    assert bench.run_reference(ns, _FakeDist(1)) is None
+    assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_on_small_inputs(capsys):
+    from dense_gemm_14_gb300 import inputs
+    data = {"f32_3072": inputs.make(64, 48, 40, "f32", "uniform", 1.0, 1),
+            "bf16_8192": inputs.make(32, 40, 48, "bf16", "normal", 0.1, 2)}
+    ns = type("A", (), {"steps": 2, "warmup": 1, "gpus": 1})()
+    line = bench.run_reference(ns, _FakeDist(0), data=data)
+    printed = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert printed == json.loads(json.dumps(line))
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["higher_is_better"] is True
+    assert line["metric"] == bench.METRIC
+
+
+def test_source_hash_and_traffic_gate(tmp_path, monkeypatch):
+    sha = bench.source_sha("sgemm_simt.cu")
+    assert len(sha) == 16
+    t = bench.traffic_for("sgemm_simt_kernel", "sgemm_simt.cu", "f32_3072")
+    assert t is None or t > 0
+    assert bench.traffic_for("sgemm_simt_kernel", "sgemm_simt.cu", "other_workload") is None

@@ -1,0 +1,55 @@
+"""Failure detection without a GPU fault.
+
+Every mbarrier wait in the kernels has a time limit. gemm14_debug_inject makes
+the next call's producer skip its first shared-memory stage -- a barrier that
+nothing will ever complete -- and shortens the wait limit. The kernel must
+then report GEMM14_ERR_TIMEOUT through the device error word, end on its own
+well within a few seconds, and leave the CUDA context usable.
+"""
+import time
+
+import pytest
+import torch
+
+import dense_gemm_14_gb300 as g14
+from dense_gemm_14_gb300 import _lib, inputs
+
+from gpu_util import oracle_check, run_abi
+
+
+def test_inject_rejects_unknown_modes():
+    g14.load()
+    assert g14.debug_inject(7) == _lib.GEMM14_ERR_INVALID_ARG
+    assert g14.debug_inject(0) == _lib.GEMM14_OK
+
+
+def test_injection_is_consumed_by_the_next_call_even_if_invalid():
+    g14.load()
+    assert g14.debug_inject(1, 1000) == 0
+    # an invalid call consumes the request without touching CUDA
+    assert g14.gemm_f32(-1, 1, 1, 0, 1, 0, 1, 0, 1, None, check=False) == 1
+    # M == 0: a valid no-op that would have carried a leftover request
+    assert g14.gemm_f32(0, 4, 4, 0, 4, 0, 4, 0, 4, None, check=False) == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dt,soft", [("f32", False), ("f32", True), ("bf16", False),
+                                     ("bf16", True), ("f16", False)])
+def test_expired_wait_reports_timeout_and_context_survives(oracle_mod, dt, soft):
+    M, N, K = 300, 520, 200
+    A, B = inputs.make(M, N, K, dt, "uniform", 1.0, seed=31)
+    lda = K + 1 if soft else (K + 7) // 8 * 8
+    ldb = N + 1 if soft else (N + 7) // 8 * 8
+    s = torch.cuda.current_stream()
+    assert g14.check_device_error(s.cuda_stream) == 0
+    assert g14.debug_inject(1, 20_000_000) == 0  # 20 ms per wait
+    t0 = time.perf_counter()
+    run_abi(A, B, lda=lda, ldb=ldb, check_err=False)
+    st = g14.check_device_error(s.cuda_stream)
+    elapsed = time.perf_counter() - t0
+    assert st == _lib.GEMM14_ERR_TIMEOUT, g14.status_string(st)
+    assert elapsed < 10.0
+    # the error word was read and cleared; the context still computes correctly
+    assert g14.check_device_error(s.cuda_stream) == 0
+    C = run_abi(A, B, lda=lda, ldb=ldb)
+    oracle_check(oracle_mod, A, B, C)
