@@ -341,8 +341,14 @@ def run_ours(args, dist: Dist):
         avg_s = statistics.mean(ms) / 1e3
         tflops = p["flops"] / avg_s / 1e12
         if p["bound"] == "tensor":
-            peak = peaks["bf16_tflops_sustained"]
-            peak_note = f"bf16 dense, sustained ({peaks['source']})"
+            # a short back-to-back region runs at burst clocks; seconds of
+            # load settle at the power-capped sustained rate
+            if elapsed_s >= 1.0:
+                peak = peaks["bf16_tflops_sustained"]
+                peak_note = f"bf16 dense, sustained ({peaks['source']}; timed region >= 1 s)"
+            else:
+                peak = peaks["bf16_tflops"]
+                peak_note = f"bf16 dense, burst ({peaks['source']}; timed region < 1 s)"
         else:
             peak = roofline.fp32_alu_peak_tflops()
             peak_note = "FFMA: 152 SMs x 128 lanes x 2 FLOP x 2070 MHz (unit counts)"
@@ -458,7 +464,7 @@ def run_table(args):
         if w.dtype == "f32":
             peak, kind = roofline.fp32_alu_peak_tflops(), "alu"
         else:
-            peak, kind = peaks["bf16_tflops_sustained"], "tensor"
+            peak, kind = peaks["bf16_tflops"], "tensor"  # each workload is timed alone: burst
         gbs = ib / (mean / 1e3) / 1e9
         print(json.dumps({"workload": name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype,
                           "ms_mean": mean, "ms_min": min(ms), "tflops": tf,

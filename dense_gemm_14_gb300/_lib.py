@@ -42,6 +42,7 @@ SIGNATURES = {
                                 ctypes.POINTER(_Plan)]),
     "gemm14_version": (_int, []),
     "gemm14_debug_inject": (_int, [_int, ctypes.c_uint64]),
+    "gemm14_set_pair_kernel": (_int, [_int]),
 }
 
 _lib = None
@@ -120,6 +121,12 @@ def debug_inject(fault: int, wait_limit_ns: int = 0) -> int:
     """Failure-detection hook: the next call on this thread runs with `fault`
     (1 = the producer never loads its first stage) and the given wait limit."""
     return int(load().gemm14_debug_inject(fault, wait_limit_ns))
+
+
+def set_pair_kernel(enable: bool) -> bool:
+    """Allows (default) or forbids the CTA-pair tensor-core kernel; returns the
+    previous setting. Results are identical either way."""
+    return bool(load().gemm14_set_pair_kernel(1 if enable else 0))
 
 
 def check_device_error(stream=None) -> int:

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -23,6 +24,9 @@ namespace {
 __device__ unsigned g_device_error;
 
 thread_local char t_last_error[256] = "";
+
+// Whether 16-bit products may use the CTA-pair kernel (gemm14_set_pair_kernel).
+std::atomic<int> g_pair_enabled{1};
 
 // One-shot request from gemm14_debug_inject for the next call on this thread.
 thread_local int t_fault = kFaultNone;
@@ -174,8 +178,23 @@ void plan_for(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t
     p->smem_bytes = S::SMEM_BYTES;
   } else {
     const int bn = hgemm_bn_for(N);
-    p->kernel = 2;
     p->loader = (aligned(A, 16) && aligned(B, 16) && lda % 8 == 0 && ldb % 8 == 0) ? 1 : 2;
+    if (p->loader == 1 && M > 128 && N > 128 && g_pair_enabled.load() && sm_count >= 2) {
+      // 256 x 256 tiles on CTA pairs; grid = 2 x clusters
+      using P = PairShape;
+      p->kernel = 3;
+      p->bm = P::BM;
+      p->bn = P::BN;
+      p->bk = P::BK;
+      p->stages = P::STAGES;
+      p->threads = P::THREADS;
+      p->smem_bytes = P::SMEM_BYTES;
+      p->tiles = ((M + P::BM - 1) / P::BM) * ((N + P::BN - 1) / P::BN);
+      const int64_t clusters = sm_count / 2;
+      p->grid = static_cast<int>(2 * (p->tiles < clusters ? p->tiles : clusters));
+      return;
+    }
+    p->kernel = 2;
     p->bm = HgemmShape::BM;
     p->bn = bn;
     p->bk = HgemmShape::BK;
@@ -244,6 +263,30 @@ int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   }
 
   const bool bf16 = dtype == GEMM14_DTYPE_BF16;
+  int pair_clusters = 0;
+  if (plan.kernel == 3) {
+    pair_clusters = pair_max_clusters();
+    if (pair_clusters <= 0) {
+      // clusters of two do not fit: the one-SM kernel computes the same product
+      g_pair_enabled.store(0);
+    }
+  }
+  if (plan.kernel == 3 && pair_clusters > 0) {
+    const CUtensorMapDataType tt =
+        bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap ma, mb;
+    if ((st = make_map(&ma, tt, 2, A, M, K, lda, PairShape::BK, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
+      return st;
+    if ((st = make_map(&mb, tt, 2, B, K, N, ldb, 64, PairShape::BK,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
+      return st;
+    const int64_t clusters = plan.tiles < pair_clusters ? plan.tiles : pair_clusters;
+    const uint32_t idesc2 = idesc_f16_f32acc(bf16, PairShape::BM, PairShape::BN);
+    return finish(launch_hgemm_tc_pair(ma, mb, args, idesc2, static_cast<int>(clusters), stream),
+                  "hgemm pair launch", stream);
+  }
+  if (plan.kernel == 3) plan_for(dtype, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
   const uint32_t idesc = idesc_f16_f32acc(bf16, HgemmShape::BM, plan.bn);
   if (plan.loader == 2)
     return finish(launch_hgemm_tc_soft(plan.bn, args, idesc, plan.grid, stream), "hgemm launch",
@@ -323,6 +366,12 @@ int gemm14_plan_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, 
   if (st != GEMM14_OK) return st;
   plan_for(dtype, M, N, K, A, lda, B, ldb, C, ldc, sm_count, plan);
   return GEMM14_OK;
+}
+
+int gemm14_set_pair_kernel(int enable) {
+  const int previous = g_pair_enabled.load();
+  g_pair_enabled.store(enable ? 1 : 0);
+  return previous;
 }
 
 int gemm14_debug_inject(int fault, uint64_t wait_limit_ns) {

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(H::THREADS, 1)
   const int tiles_n = (N + BN - 1) / BN;
   const int num_tiles = tiles_m * tiles_n;
   const int kblocks = (K + H::BK - 1) / H::BK;
-  const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns};
+  const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns, 0u};
   uint32_t prod_it = 0;
   bool mma_issued = false;
 

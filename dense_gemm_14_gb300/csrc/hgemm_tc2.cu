@@ -1,0 +1,273 @@
+// hgemm_tc2.cu -- bf16 / fp16 inputs, fp32 accumulate and output, on CTA
+// pairs: tcgen05.mma.cta_group::2 computes a 256 x 256 output tile on two SMs.
+//
+// Why pairs: a one-SM 128 x 256 MMA reads 96 B/clk of operands from shared
+// memory while TMA writes another 96 B/clk into it, more than one SM's shared
+// memory serves; on a pair each SM holds its 128 rows of A and HALF of B
+// (128 columns), the tensor cores exchange the B halves, and per SM the
+// traffic drops to 64 + 64 B/clk. L2 -> SM traffic per output element drops
+// by a third as well. (The pages' wgmma discussion, gpu-hpc-book ch.06
+// "高级 cuda 特性 —— 从矩阵乘法(gemm)说起", "Tensor Cores" / "wgmma", is the
+// prior art: asynchronous D = A*B + D with TMA-fed shared-memory operands.)
+//
+// Roles per CTA (192 threads, cluster of 2, persistent over pair tiles):
+//   warp 0      producer: TMA loads of this CTA's A rows (128 m x 64 k) and
+//               B columns (2 boxes of 64 n x 64 k) into a 6-stage ring; the
+//               completion of BOTH CTAs' loads is counted on the leader's
+//               full barrier (cta_group::2 TMA);
+//   warp 1      both CTAs allocate the pair's TMEM (2 x 256 columns); in the
+//               leader one lane issues the pair MMAs (M 256, N 256, K 16) and
+//               commits to both CTAs' empty / accumulator barriers;
+//   warps 2..5  epilogue in each CTA: its 128 rows of the accumulator from
+//               its own TMEM to C; all eight epilogue warps release the
+//               accumulator on the leader's barrier.
+// Every wait is bounded; a CTA that gives up also raises its peer's abort
+// flag. Both CTAs meet at a cluster barrier before TMEM is freed, so neither
+// exits while the pair MMAs may still read its shared memory.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gemm14 {
+namespace {
+
+using P = PairShape;
+
+struct PairSmem {
+  uint64_t full[P::STAGES];   // leader: both CTAs' bytes of a stage have landed
+  uint64_t empty[P::STAGES];  // each CTA: the pair MMAs finished reading the stage
+  uint64_t acc_full[2];       // each CTA: accumulator b holds a finished tile
+  uint64_t acc_empty[2];      // leader: all 8 epilogue warps drained accumulator b
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Grouped raster over pair tiles: groups of kGroupM row-tiles.
+__device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n, int& tm,
+                                                 int& tn) {
+  constexpr int kGroupM = 8;
+  const int per_group = kGroupM * tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * kGroupM;
+  const int gm = min(tiles_m - first_m, kGroupM);
+  const int r = t - g * per_group;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
+    hgemm_tc2_kernel(const __grid_constant__ CUtensorMap map_a,
+                     const __grid_constant__ CUtensorMap map_b, const GemmArgs args,
+                     const uint32_t idesc) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles = align1024(smem_raw);
+  PairSmem& sm = *reinterpret_cast<PairSmem*>(tiles + P::STAGES * P::STAGE_BYTES + P::GUARD_BYTES);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(cluster_count_x());
+  const int M = args.M, N = args.N, K = args.K;
+  const int tiles_m = (M + P::BM - 1) / P::BM;
+  const int tiles_n = (N + P::BN - 1) / P::BN;
+  const int num_tiles = tiles_m * tiles_n;
+  const int kblocks = (K + P::BK - 1) / P::BK;
+  const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns,
+                   mapa_shared(smem_u32(&sm.abort_flag), rank ^ 1u)};
+  uint32_t prod_it = 0;
+  bool mma_issued = false;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P::STAGES; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_empty[b], 8);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b);
+  }
+  // Both CTAs' barriers exist before either CTA signals the other's.
+  cluster_sync();
+  if (warp == 1) {
+    tmem_alloc_pair(&sm.tmem_base, P::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = true;
+      for (int t = cid; t < num_tiles && ok; t += ncl) {
+        int tm, tn;
+        pair_tile_coords(t, tiles_m, tiles_n, tm, tn);
+        for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
+          const uint32_t s = prod_it % P::STAGES, ph = (prod_it / P::STAGES) & 1;
+          if (!mbar_wait(&sm.empty[s], ph ^ 1, wc)) { ok = false; break; }
+          // Failure-detection tests: the first stage is never loaded.
+          if (args.fault == kFaultSkipFirstStage && prod_it == 0) continue;
+          uint8_t* a_st = tiles + s * P::STAGE_BYTES;
+          uint8_t* b_st = a_st + P::A_BYTES;
+          const uint32_t full_leader = mapa_shared(smem_u32(&sm.full[s]), 0);
+          if (leader) mbar_arrive_expect_tx(&sm.full[s], 2 * P::STAGE_BYTES);
+          tma_load_2d_pair(a_st, &map_a, kb * P::BK, tm * P::BM + static_cast<int>(rank) * 128,
+                           full_leader);
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d_pair(b_st + c * (64 * P::BK * 2), &map_b,
+                             tn * P::BN + static_cast<int>(rank) * 128 + c * 64, kb * P::BK,
+                             full_leader);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (leader && lane == 0) {
+      bool ok = true;
+      uint32_t it = 0;
+      int local = 0;
+      for (int t = cid; t < num_tiles && ok; t += ncl, ++local) {
+        const int b = local & 1;
+        const uint32_t aph = (local >> 1) & 1;
+        if (!mbar_wait_cluster(&sm.acc_empty[b], aph ^ 1, wc)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * P::BN);
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const uint32_t s = it % P::STAGES, ph = (it / P::STAGES) & 1;
+          if (!mbar_wait(&sm.full[s], ph, wc)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t a_addr = smem_u32(tiles + s * P::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + P::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < P::BK / 16; ++kk) {
+            // A (each CTA's 128 rows): K-major, 128-byte rows, 8-row groups
+            // 1024 B apart; a K = 16 slice starts 32 bytes further along.
+            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            // B (each CTA's 128 columns): N-major, two 64-column boxes 8 KB
+            // apart, 8-k groups 1024 B apart; a K = 16 slice is 16 rows.
+            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * 2048, 64 * P::BK * 2, 1024);
+            tc_mma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0);
+          }
+          mma_issued = true;
+          tc_commit_pair_multicast(&sm.empty[s], 0x3);
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(&sm.acc_full[b], 0x3);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&sm.acc_empty[0]), 0);
+    const uint32_t acc_empty_leader1 = mapa_shared(smem_u32(&sm.acc_empty[1]), 0);
+    int local = 0;
+    for (int t = cid; t < num_tiles; t += ncl, ++local) {
+      int tm, tn;
+      pair_tile_coords(t, tiles_m, tiles_n, tm, tn);
+      const int b = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      int got = 1;
+      if (lane == 0) got = mbar_wait(&sm.acc_full[b], aph, wc) ? 1 : 0;
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) break;
+      tc_fence_after_sync();
+      const int row = tm * P::BM + static_cast<int>(rank) * 128 + q * 32 + lane;
+      float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(b * P::BN);
+#pragma unroll 1
+      for (int c = 0; c < P::BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, r);
+        tc_wait_ld();
+        const int col0 = tn * P::BN + c * 32;
+        if (row < M) {
+          if (args.vec_store && col0 + 32 <= N) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              *reinterpret_cast<float4*>(crow + col0 + 4 * v) =
+                  make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < N) crow[col0 + j] = __uint_as_float(r[j]);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(b ? acc_empty_leader1 : acc_empty_leader0);
+    }
+  }
+
+  // Teardown. On abort, the leader lets its issued MMAs and both CTAs' loads
+  // (counted on its full barriers) finish, bounded, before the pair meets.
+  __syncthreads();
+  if (sm.abort_flag && leader) {
+    if (warp == 1 && lane == 0 && mma_issued) {
+      tc_commit_pair_multicast(&sm.drain, 0x1);
+      mbar_wait_timed(&sm.drain, 0, 100000000ull);
+    }
+    if (warp == 0 && lane == 0) {
+      const uint32_t first = prod_it > P::STAGES ? prod_it - P::STAGES : 0;
+      for (uint32_t j = first; j < prod_it; ++j)
+        if (!(args.fault == kFaultSkipFirstStage && j == 0))
+          mbar_wait_timed(&sm.full[j % P::STAGES], (j / P::STAGES) & 1, 100000000ull);
+    }
+  }
+  // Neither CTA frees TMEM or exits while the pair may still use it.
+  cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, P::TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+int pair_max_clusters() {
+  static int cached[64];
+  static bool have[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (have[dev]) return cached[dev];
+  if (cudaFuncSetAttribute(hgemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           P::SMEM_BYTES) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(P::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = P::SMEM_BYTES;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2_kernel, &cfg) != cudaSuccess) n = 0;
+  cached[dev] = n;
+  have[dev] = true;
+  return n;
+}
+
+cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                                 const GemmArgs& args, uint32_t idesc, int clusters,
+                                 cudaStream_t stream) {
+  hgemm_tc2_kernel<<<2 * clusters, P::THREADS, P::SMEM_BYTES, stream>>>(map_a, map_b, args,
+                                                                        idesc);
+  return cudaGetLastError();
+}
+
+}  // namespace gemm14

@@ -57,6 +57,25 @@ struct HgemmShape {
 // (operand format and shape); map_b boxes are 64 (n) x 64 (k).
 cudaError_t launch_hgemm_tc(int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
                             const GemmArgs& args, uint32_t idesc, int grid, cudaStream_t stream);
+// ---- bf16 / fp16 tcgen05 kernel on CTA pairs (hgemm_tc2.cu): 256 x 256 tiles
+struct PairShape {
+  static constexpr int BM = 256, BN = 256, BK = 64, STAGES = 6;
+  static constexpr int THREADS = 6 * 32;
+  static constexpr int A_BYTES = 128 * BK * 2;      // this CTA's 128 rows of A
+  static constexpr int B_BYTES = BK * 128 * 2;      // this CTA's 128 columns of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int GUARD_BYTES = 16384;         // slack past the last stage
+  static constexpr int TMEM_COLS = 512;             // two 128-lane x 256-column accumulators
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + GUARD_BYTES + 256 + 1024;
+};
+
+// Clusters of two that fit at once on the current device (0: the pair kernel
+// cannot run). The first call per device also sets the kernel's smem limit.
+int pair_max_clusters();
+cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                                 const GemmArgs& args, uint32_t idesc, int clusters,
+                                 cudaStream_t stream);
+
 // Same kernel with the software loader (operands TMA cannot address).
 cudaError_t launch_hgemm_tc_soft(int bn, const GemmArgs& args, uint32_t idesc, int grid,
                                  cudaStream_t stream);

@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(S::THREADS, 1)
                            ? (walk.num_tiles - 1 - blockIdx.x) / gridDim.x + 1
                            : 0;
   const uint32_t n_iter = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(walk.kblocks);
-  const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns};
+  const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns, 0u};
   const bool producer = kTma ? threadIdx.x == 0 : true;
   uint32_t issued = 0;  // iterations whose loads this thread has issued
 

@@ -101,7 +101,8 @@ int gemm14_check_device_error(void* stream);
 
 /* Launch plan chosen for a call (host-side only; no CUDA call is made). */
 typedef struct gemm14_plan {
-  int kernel;     /* 1 = fp32 SIMT (FFMA), 2 = tcgen05 tensor core, 0 = no launch */
+  int kernel;     /* 1 = fp32 SIMT (FFMA), 2 = tcgen05 on one SM per tile,
+                     3 = tcgen05 on CTA pairs (two SMs per 256 x 256 tile), 0 = no launch */
   int loader;     /* 1 = TMA, 2 = software loader (cp.async for fp32), 0 = none */
   int bm, bn, bk; /* output tile rows x columns, k-block depth */
   int stages;     /* shared-memory ring depth */
@@ -109,7 +110,8 @@ typedef struct gemm14_plan {
   int smem_bytes; /* dynamic shared memory per CTA */
   int vec_store;  /* 1 if C takes 16-byte stores */
   int64_t tiles;  /* output tiles */
-  int grid;       /* CTAs launched (persistent: min(tiles, sm_count)) */
+  int grid;       /* CTAs launched (persistent: min(tiles, sm_count); for kernel 3,
+                     2 x min(tiles, sm_count / 2)) */
 } gemm14_plan;
 
 /*
@@ -121,6 +123,18 @@ typedef struct gemm14_plan {
 int gemm14_plan_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                      const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
                      gemm14_plan* plan);
+
+/*
+ * The 16-bit entry points compute 256 x 256 output tiles on pairs of SMs
+ * (a cluster of two CTAs sharing each tile's B operand) when the operands are
+ * TMA-addressable and M, N > 128; otherwise 128-row tiles on one SM. Both
+ * kernels accumulate in the same order and give bit-identical results.
+ * gemm14_set_pair_kernel(0) restricts all later calls in the process to the
+ * one-SM kernel, (1) allows pairs again (the default); returns the previous
+ * setting. If pairs cannot be launched on the device the library falls back
+ * to the one-SM kernel by itself.
+ */
+int gemm14_set_pair_kernel(int enable);
 
 /*
  * Failure-detection hook for tests. The NEXT gemm_* call made by this thread

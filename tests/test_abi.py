@@ -109,12 +109,31 @@ def test_plan_fp32_tma_and_fallback(lib):
     assert p.tiles == 2 and p.grid == 2
 
 
-@pytest.mark.parametrize("N,bn", [(1, 64), (64, 64), (65, 128), (128, 128), (129, 256), (11008, 256)])
+@pytest.mark.parametrize("N,bn", [(1, 64), (64, 64), (65, 128), (128, 128)])
 def test_plan_tensor_core_tile_width(lib, N, bn):
     st, p = g14.plan(BF16, 16384, N, 4096, P, 4096, P, ((N + 7) // 8) * 8, P, N, 152)
     assert st == 0 and p.kernel == 2 and p.bn == bn and p.bm == 128 and p.bk == 64
     assert p.smem_bytes <= 227 * 1024
     assert p.tiles == 128 * ((N + bn - 1) // bn)
+
+
+@pytest.mark.parametrize("M,N", [(16384, 129), (16384, 11008), (8192, 8192), (129, 300)])
+def test_plan_pair_kernel_for_wide_products(lib, M, N):
+    ldb = ((N + 7) // 8) * 8
+    st, p = g14.plan(BF16, M, N, 4096, P, 4096, P, ldb, P, N, 152)
+    assert st == 0 and p.kernel == 3 and (p.bm, p.bn, p.bk) == (256, 256, 64)
+    tiles = ((M + 255) // 256) * ((N + 255) // 256)
+    assert p.tiles == tiles and p.grid == 2 * min(tiles, 76) and p.grid % 2 == 0
+    assert p.smem_bytes <= 227 * 1024 and p.threads == 192
+    prev = g14.set_pair_kernel(False)
+    try:
+        st, p1 = g14.plan(BF16, M, N, 4096, P, 4096, P, ldb, P, N, 152)
+        assert p1.kernel == 2 and p1.bm == 128
+    finally:
+        g14.set_pair_kernel(prev)
+    # operands TMA cannot address stay on the one-SM kernel with the software loader
+    st, p2 = g14.plan(BF16, M, N, 4096, P, 4097, P, ldb, P, N, 152)
+    assert p2.kernel == 2 and p2.loader == 2
 
 
 def test_plan_k_zero_launches_nothing(lib):

@@ -181,3 +181,26 @@ def test_device_error_word_is_clear_after_good_calls():
     A, B = inputs.make(256, 256, 256, "f32", "uniform", 1.0, seed=28)
     run_abi(A, B, check_err=False)
     assert g14.check_device_error(None) == 0
+
+
+# ------------------------------------------------------------------ CTA-pair vs one-SM kernel
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", [(129, 129, 64), (256, 256, 64), (300, 520, 200),
+                                   (1000, 777, 1000), (2048, 1536, 640)])
+def test_pair_kernel_matches_single_sm_kernel(oracle_mod, dt, M, N, K):
+    """The 256 x 256 CTA-pair kernel and the 128-row one-SM kernel accumulate in
+    the same order: bit-identical results, both within the oracle's bound."""
+    A, B = inputs.make(M, N, K, dt, "normal", 1.0 / K ** 0.5, seed=M + N + K)
+    ldb = rup(N, 8)
+    st, plan = g14.plan(g14.GEMM14_DTYPE_BF16, M, N, K, 1 << 16, rup(K, 8), 1 << 16, ldb,
+                        1 << 16, N, 152)
+    assert plan.kernel == 3
+    C_pair = run_abi(A, B, lda=rup(K, 8), ldb=ldb, ldc=N)
+    prev = g14.set_pair_kernel(False)
+    try:
+        C_one = run_abi(A, B, lda=rup(K, 8), ldb=ldb, ldc=N)
+    finally:
+        g14.set_pair_kernel(prev)
+    oracle_check(oracle_mod, A, B, C_pair)
+    assert torch.equal(C_pair, C_one)
