@@ -45,7 +45,7 @@ WORKLOAD_NAME = "fp32 3072^3 (gemm_f32) + bf16->fp32 8192^3 (gemm_bf16_f32acc), 
 # (workload name, kernel, roofline bound, C-ABI entry name, kernel source file)
 PARTS = [
     ("f32_3072", "sgemm_simt_kernel", "alu", "gemm_f32", "sgemm_simt.cu"),
-    ("bf16_8192", "hgemm_tc_kernel", "tensor", "gemm_bf16_f32acc", "hgemm_tc.cu"),
+    ("bf16_8192", "hgemm_tc2_kernel", "tensor", "gemm_bf16_f32acc", "hgemm_tc2.cu"),
 ]
 
 
