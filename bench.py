@@ -42,10 +42,12 @@ UNIT = "TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
 WORKLOAD_NAME = "fp32 3072^3 (gemm_f32) + bf16->fp32 8192^3 (gemm_bf16_f32acc), one of each per step"
 
-# (workload name, kernel, roofline bound, C-ABI entry name, kernel source file)
+# (workload name, kernel, roofline bound, C-ABI entry name, kernel source file).
+# The entry points are the workspace (stream-K) variants; a workspace is
+# allocated once, outside the timed region, where the product uses one.
 PARTS = [
-    ("f32_3072", "sgemm_simt_kernel", "alu", "gemm_f32", "sgemm_simt.cu"),
-    ("bf16_8192", "hgemm_tc2_kernel", "tensor", "gemm_bf16_f32acc", "hgemm_tc2.cu"),
+    ("f32_3072", "sgemm_simt_kernel", "alu", "gemm_f32_ws", "sgemm_simt.cu"),
+    ("bf16_8192", "hgemm_tc2_kernel", "tensor", "gemm_bf16_f32acc_ws", "hgemm_tc2.cu"),
 ]
 
 
@@ -274,7 +276,8 @@ def run_ours(args, dist: Dist):
     stream = torch.cuda.current_stream(dev)
     peaks = roofline.measured_peaks()
 
-    entries = {"gemm_f32": g14.gemm_f32, "gemm_bf16_f32acc": g14.gemm_bf16_f32acc}
+    entries = {"gemm_f32_ws": g14.gemm_f32_ws, "gemm_bf16_f32acc_ws": g14.gemm_bf16_f32acc_ws}
+    codes = {"f32": g14.GEMM14_DTYPE_F32, "bf16": g14.GEMM14_DTYPE_BF16}
     parts = []
     host = {}
     for name, kernel, bound, entry, src in PARTS:
@@ -289,14 +292,17 @@ def run_ours(args, dist: Dist):
         sets = [(a0, b0, torch.empty(w.M, w.N, device=dev))]
         for _ in range(nsets - 1):
             sets.append((a0.clone(), b0.clone(), torch.empty(w.M, w.N, device=dev)))
+        ws_bytes = g14.workspace_bytes(codes[w.dtype], w.M, w.N, w.K, 0)
+        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
         parts.append(dict(name=name, kernel=kernel, bound=bound, fn=entries[entry], src=src,
-                          w=w, flops=fl, ideal_bytes=ib, sets=sets))
+                          w=w, flops=fl, ideal_bytes=ib, sets=sets, ws=ws, ws_bytes=ws_bytes,
+                          entry=entry))
 
     def launch(p, step):
         a, b, c = p["sets"][step % len(p["sets"])]
         w = p["w"]
         p["fn"](w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N,
-                stream.cuda_stream)
+                p["ws"].data_ptr(), p["ws_bytes"], stream.cuda_stream)
 
     # warm-up (also configures the kernels' shared-memory attributes)
     for step in range(args.warmup):
@@ -353,7 +359,9 @@ def run_ours(args, dist: Dist):
             peak = roofline.fp32_alu_peak_tflops()
             peak_note = "FFMA: 152 SMs x 128 lanes x 2 FLOP x 2070 MHz (unit counts)"
         part_out.append({
-            "workload": p["name"], "kernel": p["kernel"], "M": p["w"].M, "N": p["w"].N,
+            "workload": p["name"], "kernel": p["kernel"], "entry": p["entry"],
+            "schedule": "stream-K" if p["ws_bytes"] else "data-parallel",
+            "workspace_bytes": p["ws_bytes"], "M": p["w"].M, "N": p["w"].N,
             "K": p["w"].K, "ms_mean": statistics.mean(ms), "ms_min": min(ms),
             "tflops": tflops,
             "roofline": {"bound": p["bound"], "achieved": tflops, "peak": peak, "unit": UNIT,
@@ -432,6 +440,10 @@ def run_table(args):
     g14.load()
     peaks = roofline.measured_peaks()
     entry = {"f32": g14.gemm_f32, "bf16": g14.gemm_bf16_f32acc, "f16": g14.gemm_f16_f32acc}
+    entry_ws = {"f32": g14.gemm_f32_ws, "bf16": g14.gemm_bf16_f32acc_ws,
+                "f16": g14.gemm_f16_f32acc_ws}
+    code = {"f32": g14.GEMM14_DTYPE_F32, "bf16": g14.GEMM14_DTYPE_BF16,
+            "f16": g14.GEMM14_DTYPE_F16}
     stream = torch.cuda.current_stream()
     for name, w in inputs.WORKLOADS.items():
         _, fl, ib = workload_info(name)
@@ -439,40 +451,55 @@ def run_table(args):
         per_set = A.numel() * A.element_size() + B.numel() * B.element_size() + w.M * w.N * 4
         nsets = max(2, -(-2 * L2_BYTES // per_set))
         sets = [(A.cuda(), B.cuda(), torch.empty(w.M, w.N, device="cuda")) for _ in range(nsets)]
-        fn = entry[w.dtype]
+        ws_bytes = g14.workspace_bytes(code[w.dtype], w.M, w.N, w.K, 0)
+        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+        for schedule in ("data-parallel", "stream-K"):
+            if schedule == "stream-K" and ws_bytes == 0:
+                continue
+            time_one(args, name, w, fl, ib, sets, nsets, stream, peaks, roofline, g14, schedule,
+                     entry[w.dtype], entry_ws[w.dtype], ws, ws_bytes)
+        del sets
+        torch.cuda.empty_cache()
 
-        def launch(i):
-            a, b, c = sets[i % nsets]
+
+def time_one(args, name, w, fl, ib, sets, nsets, stream, peaks, roofline, g14, schedule, fn,
+             fn_ws, ws, ws_bytes):
+    """One --table line: `schedule` selects the plain or the workspace entry point."""
+    import torch
+    def launch(i):
+        a, b, c = sets[i % nsets]
+        if schedule == "stream-K":
+            fn_ws(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N,
+                  ws.data_ptr(), ws_bytes, stream.cuda_stream)
+        else:
             fn(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N,
                stream.cuda_stream)
 
-        for i in range(args.warmup):
-            launch(i)
-        reps = max(args.steps, 5)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(reps)]
-        for i, (e0, e1) in enumerate(evs):
-            e0.record(stream)
-            launch(i)
-            e1.record(stream)
-        torch.cuda.synchronize()
-        if g14.check_device_error(stream.cuda_stream):
-            raise RuntimeError(f"device error in {name}")
-        ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-        mean = statistics.mean(ms)
-        tf = fl / (mean / 1e3) / 1e12
-        if w.dtype == "f32":
-            peak, kind = roofline.fp32_alu_peak_tflops(), "alu"
-        else:
-            peak, kind = peaks["bf16_tflops"], "tensor"  # each workload is timed alone: burst
-        gbs = ib / (mean / 1e3) / 1e9
-        print(json.dumps({"workload": name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype,
-                          "ms_mean": mean, "ms_min": min(ms), "tflops": tf,
-                          "bound": kind, "peak_tflops": peak, "frac_compute": tf / peak,
-                          "algorithmic_bytes": ib, "gbs": gbs,
-                          "frac_hbm": gbs / peaks["hbm_gbs"]}), flush=True)
-        del sets
-        torch.cuda.empty_cache()
+    for i in range(args.warmup):
+        launch(i)
+    reps = max(args.steps, 5)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for i, (e0, e1) in enumerate(evs):
+        e0.record(stream)
+        launch(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if g14.check_device_error(stream.cuda_stream):
+        raise RuntimeError(f"device error in {name}")
+    ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    mean = statistics.mean(ms)
+    tf = fl / (mean / 1e3) / 1e12
+    if w.dtype == "f32":
+        peak, kind = roofline.fp32_alu_peak_tflops(), "alu"
+    else:
+        peak, kind = peaks["bf16_tflops"], "tensor"  # each workload is timed alone: burst
+    gbs = ib / (mean / 1e3) / 1e9
+    print(json.dumps({"workload": name, "schedule": schedule, "M": w.M, "N": w.N, "K": w.K,
+                      "dtype": w.dtype, "ms_mean": mean, "ms_min": min(ms), "tflops": tf,
+                      "bound": kind, "peak_tflops": peak, "frac_compute": tf / peak,
+                      "algorithmic_bytes": ib, "gbs": gbs,
+                      "frac_hbm": gbs / peaks["hbm_gbs"]}), flush=True)
 
 
 def main():

@@ -13,12 +13,14 @@ GPU and the result is copied back (the end-to-end path).
 from __future__ import annotations
 
 from ._lib import (GEMM14_DTYPE_BF16, GEMM14_DTYPE_F16, GEMM14_DTYPE_F32, Gemm14Error, Plan,
-                   check_device_error, debug_inject, gemm_bf16_f32acc, gemm_f16_f32acc, gemm_f32, lib_path,
-                   load, plan, set_pair_kernel, status_string, version)
+                   check_device_error, debug_inject, gemm_bf16_f32acc, gemm_bf16_f32acc_ws,
+                   gemm_f16_f32acc, gemm_f16_f32acc_ws, gemm_f32, gemm_f32_ws, lib_path, load,
+                   plan, set_pair_kernel, status_string, version, workspace_bytes)
 from .api import gemm, gemm_into
 
 __all__ = [
-    "gemm", "gemm_into", "gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "plan", "Plan",
+    "gemm", "gemm_into", "gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "gemm_f32_ws",
+    "gemm_bf16_f32acc_ws", "gemm_f16_f32acc_ws", "workspace_bytes", "plan", "Plan",
     "check_device_error", "debug_inject", "set_pair_kernel", "status_string", "version", "load", "lib_path", "Gemm14Error",
     "GEMM14_DTYPE_F32", "GEMM14_DTYPE_BF16", "GEMM14_DTYPE_F16",
 ]

@@ -43,6 +43,10 @@ SIGNATURES = {
     "gemm14_version": (_int, []),
     "gemm14_debug_inject": (_int, [_int, ctypes.c_uint64]),
     "gemm14_set_pair_kernel": (_int, [_int]),
+    "gemm_f32_ws": (_int, _GEMM_ARGS[:9] + [_vp, ctypes.c_size_t, _vp]),
+    "gemm_bf16_f32acc_ws": (_int, _GEMM_ARGS[:9] + [_vp, ctypes.c_size_t, _vp]),
+    "gemm_f16_f32acc_ws": (_int, _GEMM_ARGS[:9] + [_vp, ctypes.c_size_t, _vp]),
+    "gemm14_workspace_bytes": (ctypes.c_size_t, [_int, _i64, _i64, _i64, _int]),
 }
 
 _lib = None
@@ -115,6 +119,39 @@ def gemm_f16_f32acc(M, N, K, A, lda, B, ldb, C, ldc, stream=None, check=True) ->
     if check and st:
         raise Gemm14Error(st, "gemm_f16_f32acc")
     return st
+
+
+def _call_ws(name, M, N, K, A, lda, B, ldb, C, ldc, ws, ws_bytes, stream, check):
+    st = int(getattr(load(), name)(M, N, K, A, lda, B, ldb, C, ldc, ws, ws_bytes, stream))
+    if check and st:
+        raise Gemm14Error(st, name)
+    return st
+
+
+def gemm_f32_ws(M, N, K, A, lda, B, ldb, C, ldc, workspace, workspace_bytes, stream=None,
+                check=True) -> int:
+    """C ABI gemm_f32_ws: gemm_f32 with a device workspace (stream-K schedule)."""
+    return _call_ws("gemm_f32_ws", M, N, K, A, lda, B, ldb, C, ldc, workspace,
+                    workspace_bytes, stream, check)
+
+
+def gemm_bf16_f32acc_ws(M, N, K, A, lda, B, ldb, C, ldc, workspace, workspace_bytes,
+                        stream=None, check=True) -> int:
+    """C ABI gemm_bf16_f32acc_ws."""
+    return _call_ws("gemm_bf16_f32acc_ws", M, N, K, A, lda, B, ldb, C, ldc, workspace,
+                    workspace_bytes, stream, check)
+
+
+def gemm_f16_f32acc_ws(M, N, K, A, lda, B, ldb, C, ldc, workspace, workspace_bytes,
+                       stream=None, check=True) -> int:
+    """C ABI gemm_f16_f32acc_ws."""
+    return _call_ws("gemm_f16_f32acc_ws", M, N, K, A, lda, B, ldb, C, ldc, workspace,
+                    workspace_bytes, stream, check)
+
+
+def workspace_bytes(dtype: int, M, N, K, sm_count: int = 0) -> int:
+    """Workspace the *_ws call needs for the stream-K schedule (0: none)."""
+    return int(load().gemm14_workspace_bytes(dtype, M, N, K, sm_count))
 
 
 def debug_inject(fault: int, wait_limit_ns: int = 0) -> int:

@@ -5,11 +5,27 @@ import torch
 
 from . import _lib
 
-_ENTRY = {
-    torch.float32: _lib.gemm_f32,
-    torch.bfloat16: _lib.gemm_bf16_f32acc,
-    torch.float16: _lib.gemm_f16_f32acc,
+_ENTRY_WS = {
+    torch.float32: _lib.gemm_f32_ws,
+    torch.bfloat16: _lib.gemm_bf16_f32acc_ws,
+    torch.float16: _lib.gemm_f16_f32acc_ws,
 }
+_CODE = {torch.float32: _lib.GEMM14_DTYPE_F32, torch.bfloat16: _lib.GEMM14_DTYPE_BF16,
+         torch.float16: _lib.GEMM14_DTYPE_F16}
+
+# Stream-K workspaces, one per (device, stream): calls on one stream run in
+# order, so they may share it; calls on different streams must not.
+_workspaces: dict = {}
+
+
+def _workspace(device: torch.device, stream_handle: int, nbytes: int) -> torch.Tensor:
+    key = (device.index, stream_handle)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        # zero-filled once: the library leaves only epochs of finished calls in it
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
 
 
 def _check_matrix(x: torch.Tensor, name: str) -> None:
@@ -22,11 +38,14 @@ def _check_matrix(x: torch.Tensor, name: str) -> None:
 def gemm_into(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
     """out = a @ b on the GPU through the C ABI; a, b, out are CUDA tensors.
 
+    Uses the stream-K entry point with a workspace cached per (device,
+    stream) when the product benefits from it.
+
     a: (M, K), b: (K, N) in float32, bfloat16 or float16 (same dtype);
     out: (M, N) float32. Row pitches come from the tensors' strides. Runs on
     `stream` (default: torch's current stream) without synchronising.
     """
-    if a.dtype != b.dtype or a.dtype not in _ENTRY:
+    if a.dtype != b.dtype or a.dtype not in _ENTRY_WS:
         raise TypeError(f"unsupported dtypes {a.dtype}, {b.dtype}")
     if out.dtype != torch.float32:
         raise TypeError("out must be float32")
@@ -43,8 +62,11 @@ def gemm_into(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor, stream=None) 
     elif isinstance(stream, torch.cuda.Stream):
         stream = stream.cuda_stream
     with torch.cuda.device(a.device):
-        _ENTRY[a.dtype](M, N, K, a.data_ptr(), max(a.stride(0), 1), b.data_ptr(),
-                        max(b.stride(0), 1), out.data_ptr(), max(out.stride(0), 1), stream)
+        nbytes = _lib.workspace_bytes(_CODE[a.dtype], M, N, K, 0) if M and N and K else 0
+        ws = _workspace(a.device, int(stream or 0), nbytes) if nbytes else None
+        _ENTRY_WS[a.dtype](M, N, K, a.data_ptr(), max(a.stride(0), 1), b.data_ptr(),
+                           max(b.stride(0), 1), out.data_ptr(), max(out.stride(0), 1),
+                           ws.data_ptr() if ws is not None else None, nbytes, stream)
     return out
 
 

@@ -28,6 +28,15 @@ thread_local char t_last_error[256] = "";
 // Whether 16-bit products may use the CTA-pair kernel (gemm14_set_pair_kernel).
 std::atomic<int> g_pair_enabled{1};
 
+// Stream-K publication flags hold the epoch of the call that wrote them; a
+// call's epoch is never 0 and differs from the previous 2^32 - 1 calls'.
+std::atomic<unsigned> g_epoch{0};
+unsigned next_epoch() {
+  unsigned e;
+  do { e = ++g_epoch; } while (e == 0);
+  return e;
+}
+
 // One-shot request from gemm14_debug_inject for the next call on this thread.
 thread_local int t_fault = kFaultNone;
 thread_local unsigned long long t_wait_limit_ns = 0;
@@ -224,8 +233,46 @@ int finish(cudaError_t e, const char* what, cudaStream_t stream) {
   return GEMM14_OK;
 }
 
+// Stream-K workspace the call would use with a workspace (0: it uses none).
+// Tile slots per worker: the fp32 kernel's HEAD keeps its own sums in a
+// second slot; the tensor-core kernel's HEAD adds straight from TMEM.
+int slots_per_worker(const gemm14_plan& plan) { return plan.kernel == 1 ? 2 : 1; }
+
+size_t workspace_need(const gemm14_plan& plan, int sm_count) {
+  if (plan.kernel != 1 && plan.kernel != 2) return 0;
+  if (plan.tiles > INT32_MAX || !stream_k_pays(static_cast<int>(plan.tiles), sm_count)) return 0;
+  return streamk_workspace_bytes(sm_count, plan.bm, plan.bn, slots_per_worker(plan));
+}
+
+// The schedule of a one-SM-per-tile launch: data-parallel over min(tiles, SMs)
+// CTAs, or, with a large enough workspace, stream-K over all SMs.
+void schedule(const gemm14_plan& plan, int64_t K, int sm_count, void* workspace,
+              size_t workspace_bytes, GemmArgs& args, int& grid) {
+  const int tiles = static_cast<int>(plan.tiles);
+  const int L = static_cast<int>((K + plan.bk - 1) / plan.bk);
+  const size_t need = workspace_need(plan, sm_count);
+  const bool sk = workspace && need && workspace_bytes >= need;
+  if (sk) {
+    args.sk = make_stream_k(tiles, L, sm_count, true);
+    // Slots are laid out for the uncapped worker count; sk.G <= sm_count.
+    args.partials = static_cast<float*>(workspace);
+    args.flags = reinterpret_cast<unsigned*>(
+        static_cast<char*>(workspace) +
+        streamk_slot_bytes(sm_count, plan.bm, plan.bn, slots_per_worker(plan)));
+    args.epoch = next_epoch();
+    grid = args.sk.G;
+  } else {
+    grid = tiles < sm_count ? tiles : sm_count;
+    args.sk = make_stream_k(tiles, L, grid, false);
+    args.partials = nullptr;
+    args.flags = nullptr;
+    args.epoch = 0;
+  }
+}
+
 int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-             const void* B, int64_t ldb, float* C, int64_t ldc, void* stream_ptr) {
+             const void* B, int64_t ldb, float* C, int64_t ldc, void* workspace,
+             size_t workspace_bytes, void* stream_ptr) {
   // A pending test request applies to this call only, whatever its outcome.
   const int fault = t_fault;
   const unsigned long long wait_limit_ns = t_wait_limit_ns ? t_wait_limit_ns : kWaitTimeoutNs;
@@ -233,6 +280,7 @@ int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   t_wait_limit_ns = 0;
   int st = validate(dtype, M, N, K, A, lda, B, ldb, C, ldc);
   if (st != GEMM14_OK) return st;
+  if (workspace && !aligned(workspace, 16)) return GEMM14_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return GEMM14_OK;
   const DeviceInfo* dev = nullptr;
   if ((st = current_device(&dev)) != GEMM14_OK) return st;
@@ -247,11 +295,14 @@ int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   gemm14_plan plan;
   plan_for(dtype, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
   GemmArgs args{static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                A, lda, B, ldb, C, ldc, plan.vec_store, dev->err_word, wait_limit_ns, fault};
+                A, lda, B, ldb, C, ldc, plan.vec_store, dev->err_word, wait_limit_ns, fault,
+                StreamK{}, nullptr, nullptr, 0u};
+  int grid = plan.grid;
 
   if (dtype == GEMM14_DTYPE_F32) {
+    schedule(plan, K, dev->sm_count, workspace, workspace_bytes, args, grid);
     if (plan.loader == 2)
-      return finish(launch_sgemm_cpasync(args, plan.grid, stream), "sgemm launch", stream);
+      return finish(launch_sgemm_cpasync(args, grid, stream), "sgemm launch", stream);
     CUtensorMap ma, mb;
     if ((st = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A, M, K, lda, SgemmShape::BK,
                        SgemmShape::BM, CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
@@ -259,7 +310,7 @@ int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
     if ((st = make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, K, N, ldb, SgemmShape::BN,
                        SgemmShape::BK, CU_TENSOR_MAP_SWIZZLE_NONE)) != GEMM14_OK)
       return st;
-    return finish(launch_sgemm_tma(ma, mb, args, plan.grid, stream), "sgemm launch", stream);
+    return finish(launch_sgemm_tma(ma, mb, args, grid, stream), "sgemm launch", stream);
   }
 
   const bool bf16 = dtype == GEMM14_DTYPE_BF16;
@@ -287,9 +338,10 @@ int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
                   "hgemm pair launch", stream);
   }
   if (plan.kernel == 3) plan_for(dtype, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+  schedule(plan, K, dev->sm_count, workspace, workspace_bytes, args, grid);
   const uint32_t idesc = idesc_f16_f32acc(bf16, HgemmShape::BM, plan.bn);
   if (plan.loader == 2)
-    return finish(launch_hgemm_tc_soft(plan.bn, args, idesc, plan.grid, stream), "hgemm launch",
+    return finish(launch_hgemm_tc_soft(plan.bn, args, idesc, grid, stream), "hgemm launch",
                   stream);
   const CUtensorMapDataType tt =
       bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -300,7 +352,7 @@ int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   if ((st = make_map(&mb, tt, 2, B, K, N, ldb, 64, HgemmShape::BK, CU_TENSOR_MAP_SWIZZLE_128B)) !=
       GEMM14_OK)
     return st;
-  return finish(launch_hgemm_tc(plan.bn, ma, mb, args, idesc, plan.grid, stream), "hgemm launch",
+  return finish(launch_hgemm_tc(plan.bn, ma, mb, args, idesc, grid, stream), "hgemm launch",
                 stream);
 }
 
@@ -313,17 +365,55 @@ extern "C" {
 
 int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
              int64_t ldb, float* C, int64_t ldc, void* stream) {
-  return run_gemm(GEMM14_DTYPE_F32, M, N, K, A, lda, B, ldb, C, ldc, stream);
+  return run_gemm(GEMM14_DTYPE_F32, M, N, K, A, lda, B, ldb, C, ldc, nullptr, 0, stream);
 }
 
 int gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                      const void* B, int64_t ldb, float* C, int64_t ldc, void* stream) {
-  return run_gemm(GEMM14_DTYPE_BF16, M, N, K, A, lda, B, ldb, C, ldc, stream);
+  return run_gemm(GEMM14_DTYPE_BF16, M, N, K, A, lda, B, ldb, C, ldc, nullptr, 0, stream);
 }
 
 int gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, float* C, int64_t ldc, void* stream) {
-  return run_gemm(GEMM14_DTYPE_F16, M, N, K, A, lda, B, ldb, C, ldc, stream);
+  return run_gemm(GEMM14_DTYPE_F16, M, N, K, A, lda, B, ldb, C, ldc, nullptr, 0, stream);
+}
+
+int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
+                int64_t ldb, float* C, int64_t ldc, void* workspace, size_t workspace_bytes,
+                void* stream) {
+  return run_gemm(GEMM14_DTYPE_F32, M, N, K, A, lda, B, ldb, C, ldc, workspace, workspace_bytes,
+                  stream);
+}
+
+int gemm_bf16_f32acc_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                        const void* B, int64_t ldb, float* C, int64_t ldc, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  return run_gemm(GEMM14_DTYPE_BF16, M, N, K, A, lda, B, ldb, C, ldc, workspace,
+                  workspace_bytes, stream);
+}
+
+int gemm_f16_f32acc_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                       const void* B, int64_t ldb, float* C, int64_t ldc, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return run_gemm(GEMM14_DTYPE_F16, M, N, K, A, lda, B, ldb, C, ldc, workspace, workspace_bytes,
+                  stream);
+}
+
+size_t gemm14_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int sm_count) {
+  if (sm_count <= 0) {
+    const DeviceInfo* dev = nullptr;
+    if (current_device(&dev) != GEMM14_OK) return 0;
+    sm_count = dev->sm_count;
+  }
+  // Pointers only matter for the loader choice; assume TMA-addressable operands.
+  const void* p = reinterpret_cast<const void*>(uintptr_t(1) << 16);
+  const int64_t lda = ((K + 7) / 8) * 8, ldb = ((N + 7) / 8) * 8;
+  if (validate(dtype, M, N, K, p, lda > 0 ? lda : 1, p, ldb > 0 ? ldb : 1, p,
+               N > 0 ? ldb : 1) != GEMM14_OK)
+    return 0;
+  gemm14_plan plan;
+  plan_for(dtype, M, N, K, p, lda, p, ldb, p, ldb, sm_count, &plan);
+  return workspace_need(plan, sm_count);
 }
 
 const char* gemm14_status_string(int status) {

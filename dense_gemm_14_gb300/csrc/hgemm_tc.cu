@@ -40,8 +40,11 @@ struct TcSmem {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
+  uint64_t partial_stored;  // stream-K: the 4 epilogue warps stored this CTA's partial
+  uint64_t flags_ready;     // stream-K: the later workers' partials are published
   uint32_t tmem_base;
   int abort_flag;
+  SkTable sched;  // this CTA's segments, decoded once
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -100,7 +103,9 @@ __device__ __forceinline__ void soft_load_stage(uint8_t* a_st, const GemmArgs& a
   }
 }
 
-template <int BN, bool kTma>
+// kSK: the stream-K schedule (segments, workspace partials); without it the
+// schedule is plain data-parallel and none of the stream-K code is compiled in.
+template <int BN, bool kTma, bool kSK>
 __global__ void __launch_bounds__(H::THREADS, 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b, const GemmArgs args,
@@ -117,11 +122,10 @@ __global__ void __launch_bounds__(H::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int M = args.M, N = args.N, K = args.K;
+  const int M = args.M, N = args.N;
   const int tiles_m = (M + H::BM - 1) / H::BM;
   const int tiles_n = (N + BN - 1) / BN;
-  const int num_tiles = tiles_m * tiles_n;
-  const int kblocks = (K + H::BK - 1) / H::BK;
+  const int w = blockIdx.x;  // this CTA's worker index in the schedule
   const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns, 0u};
   uint32_t prod_it = 0;
   bool mma_issued = false;
@@ -136,7 +140,16 @@ __global__ void __launch_bounds__(H::THREADS, 1)
       mbar_init(&sm.acc_empty[b], 4);
     }
     mbar_init(&sm.drain, 1);
+    mbar_init(&sm.partial_stored, 4);
+    mbar_init(&sm.flags_ready, 1);
     sm.abort_flag = 0;
+    if (kSK) {
+      sm.sched.fill(args.sk, w);
+      if (sm.sched.n_sk > kMaxSk) {  // cannot happen for schedules make_stream_k builds
+        atomicOr(args.err, kDevErrBadConfig);
+        sm.abort_flag = 1;
+      }
+    }
     fence_barrier_init();
     if (kTma) {
       tma_prefetch_desc(&map_a);
@@ -151,15 +164,30 @@ __global__ void __launch_bounds__(H::THREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = sm.tmem_base;
+  const int G = args.sk.G, L = args.sk.L;
+  const int n_seg = kSK ? (sm.abort_flag ? 0 : sm.sched.segments()) : args.sk.dp_count(w);
+  // Segment i: data-parallel tile w + i * G whole, or the decoded stream-K table.
+  auto segment = [&](int i, int& tile, int& kb0, int& kb1, int& kind) {
+    if (kSK) {
+      sm.sched.get(i, tile, kb0, kb1, kind);
+    } else {
+      tile = w + i * G;
+      kb0 = 0;
+      kb1 = L;
+      kind = kSegFull;
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Segment by segment; a segment's tile coordinates are computed once.
     if (!kTma) {
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        int tm, tn;
-        tile_coords(t, tiles_m, tiles_n, tm, tn);
-        for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
+      for (int seg = 0; seg < n_seg && ok; ++seg) {
+        int tile, kb0, kb1, kind, tm, tn;
+        segment(seg, tile, kb0, kb1, kind);
+        tile_coords(tile, tiles_m, tiles_n, tm, tn);
+        for (int kb = kb0; kb < kb1; ++kb, ++prod_it) {
           const uint32_t s = prod_it % STAGES, ph = (prod_it / STAGES) & 1;
           int got = 1;
           if (lane == 0) got = mbar_wait(&sm.empty[s], ph ^ 1, wc) ? 1 : 0;
@@ -174,10 +202,11 @@ __global__ void __launch_bounds__(H::THREADS, 1)
       }
     } else if (lane == 0) {
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        int tm, tn;
-        tile_coords(t, tiles_m, tiles_n, tm, tn);
-        for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
+      for (int seg = 0; seg < n_seg && ok; ++seg) {
+        int tile, kb0, kb1, kind, tm, tn;
+        segment(seg, tile, kb0, kb1, kind);
+        tile_coords(tile, tiles_m, tiles_n, tm, tn);
+        for (int kb = kb0; kb < kb1; ++kb, ++prod_it) {
           const uint32_t s = prod_it % STAGES, ph = (prod_it / STAGES) & 1;
           if (!mbar_wait(&sm.empty[s], ph ^ 1, wc)) { ok = false; break; }
           // Failure-detection tests: the first stage is never loaded.
@@ -198,14 +227,15 @@ __global__ void __launch_bounds__(H::THREADS, 1)
     if (lane == 0) {
       bool ok = true;
       uint32_t it = 0;
-      int local = 0;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
-        const int b = local & 1;
-        const uint32_t aph = (local >> 1) & 1;
+      for (int seg = 0; seg < n_seg && ok; ++seg) {
+        int tile, kb0, kb1, kind;
+        segment(seg, tile, kb0, kb1, kind);
+        const int b = seg & 1;
+        const uint32_t aph = (seg >> 1) & 1;
         if (!mbar_wait(&sm.acc_empty[b], aph ^ 1, wc)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait(&sm.full[s], ph, wc)) { ok = false; break; }
           tc_fence_after_sync();
@@ -219,7 +249,7 @@ __global__ void __launch_bounds__(H::THREADS, 1)
             // B: N-major, 64-column boxes 8 KB apart (leading offset), 8-k
             // groups 1024 B apart (stride offset); a K = 16 slice is 16 rows.
             const uint64_t b_desc = smem_desc_sw128(b_addr + kk * 2048, 64 * H::BK * 2, 1024);
-            tc_mma_f16(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0);
+            tc_mma_f16(d_tmem, a_desc, b_desc, idesc, kb > kb0 || kk != 0);
           }
           mma_issued = true;
           tc_commit(&sm.empty[s]);
@@ -231,27 +261,75 @@ __global__ void __launch_bounds__(H::THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    int local = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-      int tm, tn;
-      tile_coords(t, tiles_m, tiles_n, tm, tn);
-      const int b = local & 1;
-      const uint32_t aph = (local >> 1) & 1;
+    const int r_loc = q * 32 + lane;  // this thread's row within the tile
+    for (int seg = 0; seg < n_seg; ++seg) {
+      int tile, kb0, kb1, kind, tm, tn;
+      segment(seg, tile, kb0, kb1, kind);
+      tile_coords(tile, tiles_m, tiles_n, tm, tn);
+      const int b = seg & 1;
+      const uint32_t aph = (seg >> 1) & 1;
       // One lane waits; the warp then proceeds converged (tcgen05.ld is .sync.aligned).
       int got = 1;
       if (lane == 0) got = mbar_wait(&sm.acc_full[b], aph, wc) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
+      if (kSK && kind == kSegHead) {
+        // Wait for every later worker holding part of this tile (one lane of
+        // warp 2 polls their flags; the other warps wait on flags_ready).
+        // A worker has at most one HEAD segment: the barrier's first phase.
+        if (warp == 2 && lane == 0) {
+          bool all = true;
+          for (int c = w + 1; c <= sm.sched.head_last && all; ++c)
+            all = flag_wait(args.flags + c, args.epoch, wc);
+          if (all) mbar_arrive(&sm.flags_ready);
+        }
+        if (lane == 0) got = mbar_wait(&sm.flags_ready, 0, wc) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) break;
+      }
       tc_fence_after_sync();
-      const int row = tm * H::BM + q * 32 + lane;
+      const int row = tm * H::BM + r_loc;
       float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
+      float* prow = args.partials + (static_cast<size_t>(w) * H::BM + r_loc) * BN;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(b * BN);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
+        // HEAD: fetch the first contributor's partial of this chunk before the
+        // TMEM read so that the two latencies overlap.
+        float4 pre[8];
+        if (kSK && kind == kSegHead && sm.sched.head_last > w) {
+          const float* src = args.partials + (static_cast<size_t>(w + 1) * H::BM + r_loc) * BN + c * 32;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) pre[v] = __ldcg(reinterpret_cast<const float4*>(src + 4 * v));
+        }
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tc_wait_ld();
+        if (kSK && kind == kSegPartial) {
+          // Stream-K: partial sums of this tile go to workspace slot w.
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            __stcg(reinterpret_cast<float4*>(prow + c * 32 + 4 * v),
+                   make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                               __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+          continue;
+        }
+        if (kSK && kind == kSegHead) {
+          // Add the later workers' partial sums, in worker order.
+          for (int cw = w + 1; cw <= sm.sched.head_last; ++cw) {
+            const float* src = args.partials + (static_cast<size_t>(cw) * H::BM + r_loc) * BN + c * 32;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const float4 p =
+                  cw == w + 1 ? pre[v] : __ldcg(reinterpret_cast<const float4*>(src + 4 * v));
+              r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + p.x);
+              r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + p.y);
+              r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + p.z);
+              r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + p.w);
+            }
+          }
+        }
         const int col0 = tn * BN + c * 32;
         if (row < M) {
           if (args.vec_store && col0 + 32 <= N) {
@@ -270,6 +348,13 @@ __global__ void __launch_bounds__(H::THREADS, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
+      if (kSK && kind == kSegPartial) {
+        // All four warps' partial stores precede the flag. A worker has at
+        // most one PARTIAL segment: the barrier's first phase.
+        if (lane == 0) mbar_arrive(&sm.partial_stored);
+        if (warp == 2 && lane == 0 && mbar_wait(&sm.partial_stored, 0, wc))
+          flag_publish(args.flags + w, args.epoch);
+      }
     }
   }
 
@@ -296,23 +381,31 @@ __global__ void __launch_bounds__(H::THREADS, 1)
   }
 }
 
-template <int BN, bool kTma>
-cudaError_t launch_bn(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
-                      uint32_t idesc, int grid, cudaStream_t stream) {
+template <int BN, bool kTma, bool kSK>
+cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
+                           const GemmArgs& args, uint32_t idesc, int grid, cudaStream_t stream) {
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(hgemm_tc_kernel<BN, kTma>,
+    e = cudaFuncSetAttribute(hgemm_tc_kernel<BN, kTma, kSK>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, H::smem_bytes(BN));
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   CUtensorMap dummy{};
-  hgemm_tc_kernel<BN, kTma><<<grid, H::THREADS, H::smem_bytes(BN), stream>>>(
+  hgemm_tc_kernel<BN, kTma, kSK><<<grid, H::THREADS, H::smem_bytes(BN), stream>>>(
       map_a ? *map_a : dummy, map_b ? *map_b : dummy, args, idesc);
   return cudaGetLastError();
+}
+
+template <int BN, bool kTma>
+cudaError_t launch_bn(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
+                      uint32_t idesc, int grid, cudaStream_t stream) {
+  if (args.sk.dp_tiles < args.sk.tiles)
+    return launch_variant<BN, kTma, true>(map_a, map_b, args, idesc, grid, stream);
+  return launch_variant<BN, kTma, false>(map_a, map_b, args, idesc, grid, stream);
 }
 
 template <bool kTma>

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "streamk.cuh"
+
 namespace gemm14 {
 
 // Arguments shared by every kernel: sizes, operand pointers and the library's
@@ -22,7 +24,23 @@ struct GemmArgs {
   unsigned* err;
   unsigned long long wait_limit_ns;  // time limit of one mbarrier wait
   int fault;  // kFaultNone, or kFaultSkipFirstStage (failure-detection tests only)
+  StreamK sk;          // work schedule; sk.G == number of workers launched
+  float* partials;     // stream-K: tile-sized fp32 slots (see streamk_slot_bytes), or null
+  unsigned* flags;     // stream-K: G publication flags (hold the call's epoch)
+  unsigned epoch;      // this call's nonzero epoch
 };
+
+// Bytes of stream-K workspace for G workers, bm x bn tiles and `spw` tile
+// slots per worker (slot w: a worker's PARTIAL; slot G + w, fp32 kernel
+// only: its HEAD's own sums), then the G flags, each part 256-byte aligned.
+inline size_t streamk_slot_bytes(int G, int bm, int bn, int spw) {
+  const size_t b = static_cast<size_t>(spw) * G * bm * bn * sizeof(float);
+  return ((b + 255) / 256) * 256;
+}
+inline size_t streamk_workspace_bytes(int G, int bm, int bn, int spw) {
+  const size_t flags = static_cast<size_t>(G) * sizeof(unsigned);
+  return streamk_slot_bytes(G, bm, bn, spw) + ((flags + 255) / 256) * 256;
+}
 
 // Fault modes a test may request for one call (see gemm14_debug_inject).
 enum : int { kFaultNone = 0, kFaultSkipFirstStage = 1 };
@@ -35,7 +53,8 @@ struct SgemmShape {
   static constexpr int A_STAGE_BYTES = BM * BK * 4;
   static constexpr int B_STAGE_BYTES = BK * BN * 4;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;  // + barriers + align slack
+  // + barriers, schedule table and the loaders' cursors (20 B per thread) + align slack
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 512 + 20 * THREADS + 1024;
 };
 
 // Loader: TMA tensor maps (A box 32 x 128 with 128-byte swizzle, B box

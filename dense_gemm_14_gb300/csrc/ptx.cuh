@@ -173,6 +173,34 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return done != 0;
 }
 
+// ---------------------------------------------------------------- global flags
+// Publishes `value` at `flag` after every write this thread (and, through a
+// preceding CTA barrier, its CTA) made before it (release, GPU scope).
+__device__ __forceinline__ void flag_publish(unsigned* flag, unsigned value) {
+  __threadfence();
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(value) : "memory");
+}
+
+// Waits until *flag == value (acquire, GPU scope), bounded like mbar_wait.
+static __device__ __noinline__ bool flag_wait(const unsigned* flag, unsigned value,
+                                              const WaitCtx& w) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v == value) return true;
+    if ((i & 15u) == 15u) {
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.limit_ns) {
+        atomicOr(w.err, kDevErrTimeout);
+        *w.abort_flag = 1;
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

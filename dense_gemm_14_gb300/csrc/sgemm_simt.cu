@@ -52,6 +52,11 @@
 #ifndef SGEMM_FFMA2
 #define SGEMM_FFMA2 1
 #endif
+//   SGEMM_PACK_FIRST 1: duplicate all 8 A values of a k step into pairs
+//                 before its packed FMAs; 0: each just before its 8 FMAs
+#ifndef SGEMM_PACK_FIRST
+#define SGEMM_PACK_FIRST 0
+#endif
 #define GEMM14_PRAGMA(x) _Pragma(#x)
 #define GEMM14_UNROLL(n) GEMM14_PRAGMA(unroll n)
 
@@ -96,7 +101,13 @@ struct SgemmSmem {
   uint64_t full[S::STAGES];
   uint64_t empty[S::STAGES];
   int abort_flag;
+  SkTable sched;  // this CTA's segments, decoded once
+  // The loaders' position in the schedule (touched once per k-block, kept out
+  // of registers): slot 0 for the TMA thread, one per thread for cp.async.
+  SegmentCursor cursor[S::THREADS];
 };
+
+static_assert(sizeof(SgemmSmem) <= 512 + 20 * S::THREADS, "smem reserve for barriers and cursors");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -108,28 +119,27 @@ __device__ __forceinline__ uint32_t a_tile_offset(int m, int k) {
   return static_cast<uint32_t>(m * 128 + ((((k >> 2) ^ (m & 7)) & 7) << 4) + (k & 3) * 4);
 }
 
-struct TileWalk {
-  int tiles_m, num_tiles, kblocks;
-  // Flat iteration j of this CTA -> output tile (tm, tn) and k-block kb.
-  __device__ __forceinline__ void at(uint32_t j, int& tm, int& tn, int& kb) const {
-    const int local_tile = static_cast<int>(j / static_cast<uint32_t>(kblocks));
-    kb = static_cast<int>(j - static_cast<uint32_t>(local_tile) * kblocks);
-    const int tile = blockIdx.x + local_tile * gridDim.x;
+// Output tile index -> (row tile, column tile): row tiles vary fastest, so
+// CTAs working at the same time share B panels.
+struct TileGrid {
+  int tiles_m;
+  __device__ __forceinline__ void coords(int tile, int& tm, int& tn) const {
     tm = tile % tiles_m;
     tn = tile / tiles_m;
   }
 };
 
-// Loads of flat iteration j into stage j % STAGES.
+// Loads of flat iteration j (output tile `tile`, k-block kb) into stage j % STAGES.
 template <bool kTma>
-__device__ __forceinline__ void issue_stage(uint32_t j, const TileWalk& w, uint8_t* tiles,
-                                            SgemmSmem& sm, const CUtensorMap* map_a,
-                                            const CUtensorMap* map_b, const GemmArgs& args) {
+__device__ __forceinline__ void issue_stage(uint32_t j, int tile, int kb, const TileGrid& grid,
+                                            uint8_t* tiles, SgemmSmem& sm,
+                                            const CUtensorMap* map_a, const CUtensorMap* map_b,
+                                            const GemmArgs& args) {
   // Failure-detection tests: the first stage is never loaded, so every wait
   // for it must expire and report a timeout.
   if (args.fault == kFaultSkipFirstStage && j == 0) return;
-  int tm, tn, kb;
-  w.at(j, tm, tn, kb);
+  int tm, tn;
+  grid.coords(tile, tm, tn);
   const uint32_t s = j % S::STAGES;
   uint8_t* a_st = tiles + s * S::STAGE_BYTES;
   if (kTma) {
@@ -172,7 +182,10 @@ __device__ __forceinline__ void issue_stage(uint32_t j, const TileWalk& w, uint8
   }
 }
 
-template <bool kTma>
+// kSK: the stream-K schedule (segments, workspace partials); without it the
+// schedule is plain data-parallel (tiles w, w+G, ... whole) and none of the
+// stream-K machinery is compiled in.
+template <bool kTma, bool kSK>
 __global__ void __launch_bounds__(S::THREADS, 1)
     sgemm_simt_kernel(const __grid_constant__ CUtensorMap map_a,
                       const __grid_constant__ CUtensorMap map_b, const GemmArgs args) {
@@ -183,14 +196,9 @@ __global__ void __launch_bounds__(S::THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int M = args.M, N = args.N;
-  TileWalk walk;
-  walk.tiles_m = (M + S::BM - 1) / S::BM;
-  walk.num_tiles = walk.tiles_m * ((N + S::BN - 1) / S::BN);
-  walk.kblocks = (args.K + S::BK - 1) / S::BK;
-  const int my_tiles = blockIdx.x < walk.num_tiles
-                           ? (walk.num_tiles - 1 - blockIdx.x) / gridDim.x + 1
-                           : 0;
-  const uint32_t n_iter = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(walk.kblocks);
+  const int w = blockIdx.x;  // this CTA's worker index in the schedule
+  const TileGrid tgrid{(M + S::BM - 1) / S::BM};
+  const uint32_t n_iter = static_cast<uint32_t>(args.sk.iterations(w));
   const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns, 0u};
   const bool producer = kTma ? threadIdx.x == 0 : true;
   uint32_t issued = 0;  // iterations whose loads this thread has issued
@@ -201,6 +209,13 @@ __global__ void __launch_bounds__(S::THREADS, 1)
       mbar_init(&sm.empty[s], S::WARPS);
     }
     sm.abort_flag = 0;
+    if (kSK) {
+      sm.sched.fill(args.sk, w);
+      if (sm.sched.n_sk > kMaxSk) {  // cannot happen for schedules make_stream_k builds
+        atomicOr(args.err, kDevErrBadConfig);
+        sm.abort_flag = 1;
+      }
+    }
     fence_barrier_init();
     if (kTma) {
       tma_prefetch_desc(&map_a);
@@ -208,11 +223,33 @@ __global__ void __launch_bounds__(S::THREADS, 1)
     }
   }
   __syncthreads();
+  const int G = args.sk.G, L = args.sk.L;
+  const int n_seg = kSK ? (sm.abort_flag ? 0 : sm.sched.segments()) : args.sk.dp_count(w);
+
+  // The loaders walk the iterations in order. Data-parallel: iteration j is
+  // k-block j % L of tile w + (j / L) * G. Stream-K: a cursor over the
+  // decoded segments, kept in shared memory (touched once per k-block).
+  // Data-parallel: two registers (tile, k-block). Stream-K: a cursor over the
+  // decoded segments in shared memory (it would cost registers in the loop).
+  SegmentCursor& pcur = sm.cursor[kTma ? 0 : threadIdx.x];
+  int dp_tile = w, dp_kb = 0;
+  auto load = [&](uint32_t j) {
+    if (kSK) {
+      issue_stage<kTma>(j, pcur.tile, pcur.kb, tgrid, tiles, sm, &map_a, &map_b, args);
+      pcur.next<true>(sm.sched, G);
+    } else {
+      issue_stage<kTma>(j, dp_tile, dp_kb, tgrid, tiles, sm, &map_a, &map_b, args);
+      if (++dp_kb == L) {
+        dp_kb = 0;
+        dp_tile += G;
+      }
+    }
+  };
 
   // Prologue: fill the ring (fresh stages need no empty-wait).
-  if (producer) {
-    for (; issued < n_iter && issued < static_cast<uint32_t>(S::STAGES); ++issued)
-      issue_stage<kTma>(issued, walk, tiles, sm, &map_a, &map_b, args);
+  if (producer && n_seg > 0) {
+    if (kSK) pcur.start<true>(sm.sched, w, n_seg, L);
+    for (; issued < n_iter && issued < static_cast<uint32_t>(S::STAGES); ++issued) load(issued);
   }
 
   // This thread's rows: warp_m*32 + tr + 4*i (i < 8); columns:
@@ -226,9 +263,17 @@ __global__ void __launch_bounds__(S::THREADS, 1)
 
   uint32_t it = 0;
   bool ok = true;
-  for (int lt = 0; lt < my_tiles && ok; ++lt) {
-    const int tile = blockIdx.x + lt * gridDim.x;
-    const int tm = tile % walk.tiles_m, tn = tile / walk.tiles_m;
+  for (int seg = 0; seg < n_seg && ok; ++seg) {
+    int tile, kb0, kb1, kind, tm, tn;
+    if (kSK) {
+      sm.sched.get(seg, tile, kb0, kb1, kind);
+    } else {
+      tile = w + seg * G;
+      kb0 = 0;
+      kb1 = L;
+      kind = kSegFull;
+    }
+    tgrid.coords(tile, tm, tn);
 #if SGEMM_FFMA2
     // acc2[i][2*jj + h] holds columns 4*jj + 2*h and 4*jj + 2*h + 1 of row i.
     uint64_t acc2[8][8];
@@ -244,7 +289,7 @@ __global__ void __launch_bounds__(S::THREADS, 1)
       for (int j = 0; j < 16; ++j) acc[i][j] = 0.f;
 #endif
 
-    for (int kb = 0; kb < walk.kblocks; ++kb, ++it) {
+    for (int kb = kb0; kb < kb1; ++kb, ++it) {
       const uint32_t s = it % S::STAGES, ph = (it / S::STAGES) & 1;
       if (!mbar_wait(&sm.full[s], ph, wc)) { ok = false; break; }
       const uint8_t* a_st = tiles + s * S::STAGE_BYTES + a_thread;
@@ -269,6 +314,30 @@ __global__ void __launch_bounds__(S::THREADS, 1)
           for (int jj = 0; jj < 4; ++jj)
             b[jj] = *reinterpret_cast<const ulonglong2*>(b_st + (k0 + kk) * (S::BN * 4) +
                                                          128 * jj);
+#if SGEMM_PACK_FIRST || SGEMM_B_OUTER
+          uint64_t a2[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float av = AFrag<kAK>::get(a[i], kk);
+            a2[i] = pack2(av, av);
+          }
+#if SGEMM_B_OUTER
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) fma2(acc2[i][2 * jj + h], a2[i], h ? b[jj].y : b[jj].x);
+#else
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              fma2(acc2[i][2 * jj + 0], a2[i], b[jj].x);
+              fma2(acc2[i][2 * jj + 1], a2[i], b[jj].y);
+            }
+#endif
+#else
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float av = AFrag<kAK>::get(a[i], kk);
@@ -279,6 +348,7 @@ __global__ void __launch_bounds__(S::THREADS, 1)
               fma2(acc2[i][2 * jj + 1], a2, b[jj].y);
             }
           }
+#endif
         }
 #else
 #pragma unroll
@@ -326,15 +396,100 @@ __global__ void __launch_bounds__(S::THREADS, 1)
           ok = false;
           break;
         }
-        issue_stage<kTma>(issued, walk, tiles, sm, &map_a, &map_b, args);
+        load(issued);
         ++issued;
       }
     }
+    if (kSK) {
+      // Stream-K segments end at a CTA barrier: a thread whose wait failed
+      // has raised the abort flag and left the k loop, and all threads take
+      // the decision to stop at the same point before the epilogues' barriers.
+      __syncthreads();
+      if (sm.abort_flag) ok = false;
+    }
     if (!ok) break;
 
+    // Stream-K: PARTIAL and HEAD segments leave their sums in workspace slot
+    // w (tile-local element (r, c) at r * BN + c). A PARTIAL then publishes
+    // flag w. A HEAD waits for the later workers' flags and reduces the slots
+    // w, w+1, ..., head_last in that order into C, a plain loop over the tile
+    // with the accumulators no longer live.
+    const int r_loc = warp_m * 32 + tr;   // + 4 i
+    const int c_loc = warp_n * 128 + tc * 4;  // + 32 jj
+    if (kSK && kind != kSegFull) {
+      // PARTIAL -> slot w; HEAD -> slot G + w (a worker may hold both, and a
+      // PARTIAL must survive until its owner has read it).
+      float* slot = args.partials +
+                    static_cast<size_t>(kind == kSegHead ? args.sk.G + w : w) * (S::BM * S::BN);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          float4 v;
+#if SGEMM_FFMA2
+          const float2 lo = unpack2(acc2[i][2 * jj]), hi = unpack2(acc2[i][2 * jj + 1]);
+          v = make_float4(lo.x, lo.y, hi.x, hi.y);
+#else
+          v = make_float4(acc[i][jj * 4], acc[i][jj * 4 + 1], acc[i][jj * 4 + 2], acc[i][jj * 4 + 3]);
+#endif
+          __stcg(reinterpret_cast<float4*>(slot + (r_loc + 4 * i) * S::BN + c_loc + 32 * jj), v);
+        }
+      if (kind == kSegPartial) {
+        __syncthreads();
+        if (threadIdx.x == 0) flag_publish(args.flags + w, args.epoch);
+        continue;
+      }
+      const int last = sm.sched.head_last;
+      if (threadIdx.x == 0)
+        for (int c = w + 1; c <= last; ++c)
+          if (!flag_wait(args.flags + c, args.epoch, wc)) break;  // raises abort on expiry
+      __syncthreads();  // also orders this CTA's own slot stores before the reads
+      if (sm.abort_flag) { ok = false; break; }
+      // float4 q of the tile (q = thread + 256 u): row q / 64, columns
+      // 4 (q % 64) .. +3 -- a warp covers 512 contiguous bytes of a row.
+      // Eight float4 per thread are in flight per slot to hide L2 latency.
+      constexpr int kPer = S::BM * S::BN / 4 / S::THREADS;  // 32
+#pragma unroll 1
+      for (int u0 = 0; u0 < kPer; u0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          v[u] = __ldcg(reinterpret_cast<const float4*>(slot) + threadIdx.x + (u0 + u) * S::THREADS);
+#pragma unroll 1
+        for (int c = w + 1; c <= last; ++c) {
+          const float4* src = reinterpret_cast<const float4*>(
+              args.partials + static_cast<size_t>(c) * (S::BM * S::BN));
+          float4 p[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) p[u] = __ldcg(src + threadIdx.x + (u0 + u) * S::THREADS);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            v[u].x += p[u].x; v[u].y += p[u].y; v[u].z += p[u].z; v[u].w += p[u].w;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int q = threadIdx.x + (u0 + u) * S::THREADS;
+          const int r = q / (S::BN / 4), c4 = (q % (S::BN / 4)) * 4;
+          const int row = tm * S::BM + r, col = tn * S::BN + c4;
+          if (row >= M) continue;
+          float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
+          if (args.vec_store && col + 3 < N) {
+            *reinterpret_cast<float4*>(crow + col) = v[u];
+          } else {
+            if (col < N) crow[col] = v[u].x;
+            if (col + 1 < N) crow[col + 1] = v[u].y;
+            if (col + 2 < N) crow[col + 2] = v[u].z;
+            if (col + 3 < N) crow[col + 3] = v[u].w;
+          }
+        }
+      }
+      continue;
+    }
+
     // Epilogue: rows beyond M and columns beyond N are not written.
-    const int row0 = tm * S::BM + warp_m * 32 + tr;
-    const int col0 = tn * S::BN + warp_n * 128 + tc * 4;
+    const int row0 = tm * S::BM + r_loc;
+    const int col0 = tn * S::BN + c_loc;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int row = row0 + 4 * i;
@@ -384,23 +539,31 @@ __global__ void __launch_bounds__(S::THREADS, 1)
   }
 }
 
-template <bool kTma>
-cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
-                   int grid, cudaStream_t stream) {
+template <bool kTma, bool kSK>
+cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
+                           const GemmArgs& args, int grid, cudaStream_t stream) {
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(sgemm_simt_kernel<kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             S::SMEM_BYTES);
+    e = cudaFuncSetAttribute(sgemm_simt_kernel<kTma, kSK>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   CUtensorMap dummy{};
-  sgemm_simt_kernel<kTma><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(
+  sgemm_simt_kernel<kTma, kSK><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(
       map_a ? *map_a : dummy, map_b ? *map_b : dummy, args);
   return cudaGetLastError();
+}
+
+template <bool kTma>
+cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
+                   int grid, cudaStream_t stream) {
+  if (args.sk.dp_tiles < args.sk.tiles)
+    return launch_variant<kTma, true>(map_a, map_b, args, grid, stream);
+  return launch_variant<kTma, false>(map_a, map_b, args, grid, stream);
 }
 
 }  // namespace

@@ -37,6 +37,7 @@
 #ifndef GEMM14_H
 #define GEMM14_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -85,6 +86,46 @@ int gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
 /* As gemm_bf16_f32acc with IEEE binary16 (fp16) inputs. */
 int gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, float* C, int64_t ldc, void* stream);
+
+/*
+ * Stream-K variants. Same operation and arguments as gemm_f32 /
+ * gemm_bf16_f32acc / gemm_f16_f32acc, plus a caller-owned DEVICE workspace.
+ * With a workspace of at least gemm14_workspace_bytes(...) bytes, the one-SM
+ * kernels split the k-blocks of the last wave and a half of output tiles
+ * evenly over all SMs instead of leaving SMs idle in a partial last wave, or,
+ * for products of fewer tiles than half the SMs, spread all their k-blocks
+ * over the SMs (the "stream-K" schedule): a tile shared by several SMs is finished by the
+ * SM holding its first k-blocks, which adds the others' partial sums from the
+ * workspace in a fixed order, so results are deterministic run to run (they
+ * may differ in the last bits from the data-parallel schedule, which sums a
+ * tile's k-blocks in one run). With workspace == NULL, a smaller workspace, a
+ * product whose tiles fill whole waves, or one with between half and all of
+ * a wave of tiles (where splitting measured slower), the call is exactly the
+ * plain entry point. The CTA-pair kernel (wide 16-bit products) does not use
+ * a workspace.
+ * workspace: 16-byte aligned (else GEMM14_ERR_INVALID_ARG), zero-filled
+ * before its first use (calls leave only nonzero epochs of finished calls in
+ * it); it must not be used by two calls that may run at the same time.
+ */
+int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
+                int64_t ldb, float* C, int64_t ldc, void* workspace, size_t workspace_bytes,
+                void* stream);
+int gemm_bf16_f32acc_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                        const void* B, int64_t ldb, float* C, int64_t ldc, void* workspace,
+                        size_t workspace_bytes, void* stream);
+int gemm_f16_f32acc_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                       const void* B, int64_t ldb, float* C, int64_t ldc, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes that let the *_ws call of this dtype and shape use the
+ * stream-K schedule on a GPU with sm_count SMs (sm_count <= 0: the current
+ * device's). 0 means the call would not split tiles (whole waves, between
+ * half and one wave of tiles, or the CTA-pair kernel) or the arguments are
+ * invalid. Assumes operands
+ * TMA can address (16-byte aligned, pitches multiple of 16 bytes).
+ */
+size_t gemm14_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int sm_count);
 
 /* Static text for a status code (never NULL). */
 const char* gemm14_status_string(int status);

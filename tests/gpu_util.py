@@ -28,9 +28,14 @@ def to_device_padded(x: torch.Tensor, ld: int, offset_elems: int = 0) -> tuple[t
     return buf, view
 
 
+ENTRY_WS = {"f32": g14.gemm_f32_ws, "bf16": g14.gemm_bf16_f32acc_ws,
+            "f16": g14.gemm_f16_f32acc_ws}
+
+
 def run_abi(A: torch.Tensor, B: torch.Tensor, lda=None, ldb=None, ldc=None, a_off=0, b_off=0,
-            c_off=0, stream=None, poison=True, check_err=True):
-    """C = A @ B through the C ABI entry point for A's dtype. Returns C (CPU fp32)."""
+            c_off=0, stream=None, poison=True, check_err=True, workspace=None):
+    """C = A @ B through the C ABI entry point for A's dtype (the *_ws entry
+    point when a workspace tensor is given). Returns C (CPU fp32)."""
     M, K = A.shape
     _, N = B.shape
     lda = lda or max(K, 1)
@@ -42,8 +47,13 @@ def run_abi(A: torch.Tensor, B: torch.Tensor, lda=None, ldb=None, ldc=None, a_of
                       dtype=torch.float32, device="cuda")
     c_ptr = cbuf.data_ptr() + 4 * c_off
     s = stream if stream is not None else torch.cuda.current_stream()
-    ENTRY[dtype_name(A)](M, N, K, a.data_ptr() if M and K else 0, lda,
-                         b.data_ptr() if K and N else 0, ldb, c_ptr, ldc, s.cuda_stream)
+    if workspace is None:
+        ENTRY[dtype_name(A)](M, N, K, a.data_ptr() if M and K else 0, lda,
+                             b.data_ptr() if K and N else 0, ldb, c_ptr, ldc, s.cuda_stream)
+    else:
+        ENTRY_WS[dtype_name(A)](M, N, K, a.data_ptr() if M and K else 0, lda,
+                                b.data_ptr() if K and N else 0, ldb, c_ptr, ldc,
+                                workspace.data_ptr(), workspace.numel(), s.cuda_stream)
     if check_err:
         st = g14.check_device_error(s.cuda_stream)
         assert st == 0, g14.status_string(st)
@@ -74,3 +84,11 @@ def oracle_check(oracle_mod, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, 
             f"{dt} {tuple(A.shape)}x{tuple(B.shape)}: {len(bad)} elements out of bound; "
             f"first at ({i},{j}) gpu={Cg[i, j]!r} ref={ref[i, j]!r} abs={refabs[i, j]!r}; worst={worst:.3g}")
     return worst
+
+
+def make_workspace(dtype: str, M: int, N: int, K: int) -> torch.Tensor:
+    """A zero-filled device workspace large enough for the stream-K schedule."""
+    code = {"f32": g14.GEMM14_DTYPE_F32, "bf16": g14.GEMM14_DTYPE_BF16,
+            "f16": g14.GEMM14_DTYPE_F16}[dtype]
+    n = g14.workspace_bytes(code, M, N, K, 0)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device="cuda")

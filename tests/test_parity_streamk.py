@@ -1,0 +1,90 @@
+"""GPU parity of the stream-K schedule (the *_ws entry points): tiles split
+over several SMs, partial sums combined in a fixed order through the
+workspace. Checked against the oracle, for run-to-run bit equality, and
+against the data-parallel schedule within the bound."""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_14_gb300 as g14
+from dense_gemm_14_gb300 import _lib, inputs
+
+from gpu_util import make_workspace, oracle_check, run_abi
+
+pytestmark = pytest.mark.gpu
+
+
+def rup(x, m):
+    return (x + m - 1) // m * m
+
+
+# (M, N, K): few tiles over all SMs (a tile shared by many SMs), about two
+# waves (each tile split in two), a ragged tail, and tiny products.
+F32_CASES = [(1000, 1000, 777), (3072, 3072, 3072), (4097, 3001, 513), (129, 257, 4000),
+             (256, 256, 256), (1, 1, 1), (7, 300, 35)]
+
+
+@pytest.mark.parametrize("M,N,K", F32_CASES)
+@pytest.mark.parametrize("soft", [False, True])
+def test_f32_streamk(oracle_mod, M, N, K, soft):
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=M + 3 * N + 7 * K)
+    lda = K + 1 if soft else rup(K, 4)
+    ldb = N + 1 if soft else rup(N, 4)
+    ws = make_workspace("f32", M, N, K)
+    C1 = run_abi(A, B, lda=lda, ldb=ldb, ldc=N, workspace=ws)
+    big = M * N * K > 2e9
+    oracle_check(oracle_mod, A, B, C1, rows=np.arange(0, M, 97) if big else None)
+    C2 = run_abi(A, B, lda=lda, ldb=ldb, ldc=N, workspace=ws)  # same workspace, next epoch
+    assert torch.equal(C1, C2)
+
+
+TC_CASES = [(16384, 64, 4096), (300, 100, 5000), (2000, 128, 777), (129, 65, 3000),
+            (1, 8, 8), (500, 64, 64)]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", TC_CASES)
+def test_tensor_core_streamk(oracle_mod, dt, M, N, K):
+    A, B = inputs.make(M, N, K, dt, "normal", 1.0 / K ** 0.5, seed=M + N + K)
+    ws = make_workspace(dt, M, N, K)
+    C1 = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), ldc=N, workspace=ws)
+    oracle_check(oracle_mod, A, B, C1,
+                 rows=np.arange(0, M, 61) if M * N * K > 2e9 else None)
+    C2 = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), ldc=N, workspace=ws)
+    assert torch.equal(C1, C2)
+    # software loader + stream-K
+    C3 = run_abi(A, B, lda=K + 1, ldb=N + 1, ldc=N, a_off=1, workspace=ws)
+    assert torch.equal(C1, C3)
+
+
+def test_streamk_vs_data_parallel_within_bound(oracle_mod):
+    A, B = inputs.make(1000, 1000, 777, "f32", "normal", 1.0, seed=5)
+    ws = make_workspace("f32", 1000, 1000, 777)
+    C_sk = run_abi(A, B, workspace=ws)
+    C_dp = run_abi(A, B)
+    oracle_check(oracle_mod, A, B, C_sk)
+    oracle_check(oracle_mod, A, B, C_dp)
+    # exact on integer inputs, whatever the split
+    Ai, Bi = inputs.make_integer(1000, 1000, 777, 3, "f32", seed=6)
+    want = (Ai.double() @ Bi.double()).float()
+    assert torch.equal(run_abi(Ai, Bi, workspace=ws), want)
+
+
+def test_small_workspace_falls_back_to_data_parallel():
+    A, B = inputs.make(1000, 1000, 777, "f32", "normal", 1.0, seed=7)
+    small = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    assert torch.equal(run_abi(A, B, workspace=small), run_abi(A, B))
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_streamk_expired_wait_reports_timeout(oracle_mod, dt):
+    M, N, K = (1000, 1000, 777) if dt == "f32" else (300, 100, 5000)
+    A, B = inputs.make(M, N, K, dt, "uniform", 1.0, seed=8)
+    ws = make_workspace(dt, M, N, K)
+    s = torch.cuda.current_stream()
+    assert g14.check_device_error(s.cuda_stream) == 0
+    g14.debug_inject(1, 20_000_000)
+    run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), workspace=ws, check_err=False)
+    assert g14.check_device_error(s.cuda_stream) == _lib.GEMM14_ERR_TIMEOUT
+    C = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), workspace=ws)
+    oracle_check(oracle_mod, A, B, C)

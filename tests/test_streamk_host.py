@@ -1,0 +1,53 @@
+"""Host-side checks of the stream-K schedule and the workspace entry points."""
+import os
+import subprocess
+
+import pytest
+
+import dense_gemm_14_gb300 as g14
+from dense_gemm_14_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "dense_gemm_14_gb300", "csrc")
+
+
+def test_schedule_covers_every_k_block_once(tmp_path):
+    exe = tmp_path / "sk_check"
+    subprocess.run(["g++", "-std=c++17", "-O1", "-I", CSRC, "-o", str(exe),
+                    os.path.join(ROOT, "tests", "streamk_schedule_check.cpp")], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout[-2000:]
+    assert "bad = 0" in out.stdout
+
+
+def test_workspace_bytes():
+    g14.load()
+    F32, BF16 = g14.GEMM14_DTYPE_F32, g14.GEMM14_DTYPE_BF16
+    # fp32: two 128 x 256 slots per worker (PARTIAL and HEAD), then the flags
+    slots = 2 * 152 * 128 * 256 * 4
+    want = (slots + 255) // 256 * 256 + (152 * 4 + 255) // 256 * 256
+    assert g14.workspace_bytes(F32, 3072, 3072, 3072, 152) == want
+    assert g14.workspace_bytes(F32, 4097, 3001, 513, 152) == want
+    # skinny bf16: 128 tiles of 128 x 64 -- between half and one wave: not split
+    assert g14.workspace_bytes(BF16, 16384, 64, 4096, 152) == 0
+    # few tiles (fewer than half a wave): split, one 128 x 64 slot per worker
+    assert g14.workspace_bytes(BF16, 1024, 64, 4096, 152) == \
+        (152 * 128 * 64 * 4 + 255) // 256 * 256 + 768
+    # the CTA-pair kernel uses none; whole waves use none; invalid args -> 0
+    assert g14.workspace_bytes(BF16, 8192, 8192, 8192, 152) == 0
+    assert g14.workspace_bytes(F32, 128 * 152, 256, 64, 152) == 0
+    assert g14.workspace_bytes(F32, -1, 4, 4, 152) == 0
+
+
+def test_ws_entry_points_validate_workspace():
+    g14.load()
+    P = 1 << 16
+    for fn in (g14.gemm_f32_ws, g14.gemm_bf16_f32acc_ws, g14.gemm_f16_f32acc_ws):
+        # misaligned workspace
+        assert fn(4, 8, 8, P, 8, P, 8, P, 8, P + 4, 1 << 20, None, check=False) == \
+            _lib.GEMM14_ERR_INVALID_ARG
+        # the usual argument checks still apply
+        assert fn(-1, 8, 8, P, 8, P, 8, P, 8, P, 1 << 20, None, check=False) == \
+            _lib.GEMM14_ERR_INVALID_ARG
+        # empty products need nothing
+        assert fn(0, 8, 8, P, 8, P, 8, P, 8, 0, 0, None, check=False) == 0
