@@ -254,11 +254,10 @@ void schedule(const gemm14_plan& plan, int64_t K, int sm_count, void* workspace,
   const bool sk = workspace && need && workspace_bytes >= need;
   if (sk) {
     args.sk = make_stream_k(tiles, L, sm_count, true);
-    // Slots are laid out for the uncapped worker count; sk.G <= sm_count.
-    args.partials = static_cast<float*>(workspace);
-    args.flags = reinterpret_cast<unsigned*>(
-        static_cast<char*>(workspace) +
-        streamk_slot_bytes(sm_count, plan.bm, plan.bn, slots_per_worker(plan)));
+    // Flags first (a fixed region), then the slots; sk.G <= sm_count.
+    args.flags = static_cast<unsigned*>(workspace);
+    args.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             streamk_flag_bytes(sm_count));
     args.epoch = next_epoch();
     grid = args.sk.G;
   } else {

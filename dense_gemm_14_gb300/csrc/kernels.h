@@ -25,21 +25,21 @@ struct GemmArgs {
   unsigned long long wait_limit_ns;  // time limit of one mbarrier wait
   int fault;  // kFaultNone, or kFaultSkipFirstStage (failure-detection tests only)
   StreamK sk;          // work schedule; sk.G == number of workers launched
-  float* partials;     // stream-K: tile-sized fp32 slots (see streamk_slot_bytes), or null
+  float* partials;     // stream-K: tile-sized fp32 slots (see streamk_workspace_bytes), or null
   unsigned* flags;     // stream-K: G publication flags (hold the call's epoch)
   unsigned epoch;      // this call's nonzero epoch
 };
 
-// Bytes of stream-K workspace for G workers, bm x bn tiles and `spw` tile
-// slots per worker (slot w: a worker's PARTIAL; slot G + w, fp32 kernel
-// only: its HEAD's own sums), then the G flags, each part 256-byte aligned.
-inline size_t streamk_slot_bytes(int G, int bm, int bn, int spw) {
-  const size_t b = static_cast<size_t>(spw) * G * bm * bn * sizeof(float);
-  return ((b + 255) / 256) * 256;
+// Stream-K workspace layout on a GPU with `sms` SMs: first one flag word
+// per SM (a region whose place and size never depend on the product, so a
+// workspace reused for another shape never finds partial sums where a flag
+// is expected), then `spw` tile slots of bm x bn floats per worker (slot w: a
+// worker's PARTIAL; slot G + w, fp32 kernel only: its HEAD's own sums).
+inline size_t streamk_flag_bytes(int sms) {
+  return ((static_cast<size_t>(sms) * sizeof(unsigned) + 255) / 256) * 256;
 }
-inline size_t streamk_workspace_bytes(int G, int bm, int bn, int spw) {
-  const size_t flags = static_cast<size_t>(G) * sizeof(unsigned);
-  return streamk_slot_bytes(G, bm, bn, spw) + ((flags + 255) / 256) * 256;
+inline size_t streamk_workspace_bytes(int sms, int bm, int bn, int spw) {
+  return streamk_flag_bytes(sms) + static_cast<size_t>(spw) * sms * bm * bn * sizeof(float);
 }
 
 // Fault modes a test may request for one call (see gemm14_debug_inject).

@@ -104,8 +104,11 @@ int gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  * plain entry point. The CTA-pair kernel (wide 16-bit products) does not use
  * a workspace.
  * workspace: 16-byte aligned (else GEMM14_ERR_INVALID_ARG), zero-filled
- * before its first use (calls leave only nonzero epochs of finished calls in
- * it); it must not be used by two calls that may run at the same time.
+ * before its first use. Its first bytes (one 4-byte word per SM, rounded up
+ * to 256 bytes) hold publication flags that only ever contain zero or the
+ * number of a finished call, so a workspace may be reused by any later call,
+ * of any shape, without clearing; it must not be used by two calls that may
+ * run at the same time.
  */
 int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
                 int64_t ldb, float* C, int64_t ldc, void* workspace, size_t workspace_bytes,

@@ -88,3 +88,17 @@ def test_streamk_expired_wait_reports_timeout(oracle_mod, dt):
     assert g14.check_device_error(s.cuda_stream) == _lib.GEMM14_ERR_TIMEOUT
     C = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), workspace=ws)
     oracle_check(oracle_mod, A, B, C)
+
+
+def test_workspace_reused_across_shapes(oracle_mod):
+    """One workspace, products of different shapes and dtypes in turn: the
+    flag words sit at a fixed place, so stale partial sums never pose as flags."""
+    need = max(g14.workspace_bytes(g14.GEMM14_DTYPE_F32, 1000, 1000, 777, 0),
+               g14.workspace_bytes(g14.GEMM14_DTYPE_BF16, 300, 100, 5000, 0))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    cases = [("f32", 1000, 1000, 777), ("bf16", 300, 100, 5000), ("f32", 256, 256, 256),
+             ("bf16", 500, 64, 64), ("f32", 1000, 1000, 777)]
+    for i, (dt, M, N, K) in enumerate(cases):
+        A, B = inputs.make(M, N, K, dt, "uniform", 1.0, seed=40 + i)
+        C = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), workspace=ws)
+        oracle_check(oracle_mod, A, B, C)

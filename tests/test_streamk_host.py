@@ -23,16 +23,15 @@ def test_schedule_covers_every_k_block_once(tmp_path):
 def test_workspace_bytes():
     g14.load()
     F32, BF16 = g14.GEMM14_DTYPE_F32, g14.GEMM14_DTYPE_BF16
-    # fp32: two 128 x 256 slots per worker (PARTIAL and HEAD), then the flags
-    slots = 2 * 152 * 128 * 256 * 4
-    want = (slots + 255) // 256 * 256 + (152 * 4 + 255) // 256 * 256
+    # fp32: the flags (one word per SM, 256-byte aligned), then two 128 x 256
+    # slots per worker (PARTIAL and HEAD)
+    want = 768 + 2 * 152 * 128 * 256 * 4
     assert g14.workspace_bytes(F32, 3072, 3072, 3072, 152) == want
     assert g14.workspace_bytes(F32, 4097, 3001, 513, 152) == want
     # skinny bf16: 128 tiles of 128 x 64 -- between half and one wave: not split
     assert g14.workspace_bytes(BF16, 16384, 64, 4096, 152) == 0
     # few tiles (fewer than half a wave): split, one 128 x 64 slot per worker
-    assert g14.workspace_bytes(BF16, 1024, 64, 4096, 152) == \
-        (152 * 128 * 64 * 4 + 255) // 256 * 256 + 768
+    assert g14.workspace_bytes(BF16, 1024, 64, 4096, 152) == 768 + 152 * 128 * 64 * 4
     # the CTA-pair kernel uses none; whole waves use none; invalid args -> 0
     assert g14.workspace_bytes(BF16, 8192, 8192, 8192, 152) == 0
     assert g14.workspace_bytes(F32, 128 * 152, 256, 64, 152) == 0
