@@ -47,6 +47,7 @@ SIGNATURES = {
     "gemm_bf16_f32acc_ws": (_int, _GEMM_ARGS[:9] + [_vp, ctypes.c_size_t, _vp]),
     "gemm_f16_f32acc_ws": (_int, _GEMM_ARGS[:9] + [_vp, ctypes.c_size_t, _vp]),
     "gemm14_workspace_bytes": (ctypes.c_size_t, [_int, _i64, _i64, _i64, _int]),
+    "gemm_bf16_f32acc_noalloc": (_int, _GEMM_ARGS),
 }
 
 _lib = None
@@ -147,6 +148,21 @@ def gemm_f16_f32acc_ws(M, N, K, A, lda, B, ldb, C, ldc, workspace, workspace_byt
     """C ABI gemm_f16_f32acc_ws."""
     return _call_ws("gemm_f16_f32acc_ws", M, N, K, A, lda, B, ldb, C, ldc, workspace,
                     workspace_bytes, stream, check)
+
+
+def gemm_bf16_f32acc_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=None, check=True) -> int:
+    """C ABI gemm_bf16_f32acc_noalloc: gemm_bf16_f32acc for callers that may
+    not allocate device memory; its stream-K scratch is a fixed array inside
+    the library (see include/gemm14.h for the limit)."""
+    st = _call("gemm_bf16_f32acc_noalloc", M, N, K, A, lda, B, ldb, C, ldc, stream)
+    if check and st:
+        raise Gemm14Error(st, "gemm_bf16_f32acc_noalloc")
+    return st
+
+
+def last_error_string() -> str:
+    """Text of the last failure seen by this thread (the C ABI's message)."""
+    return load().gemm14_last_error_string().decode(errors="replace")
 
 
 def workspace_bytes(dtype: int, M, N, K, sm_count: int = 0) -> int:

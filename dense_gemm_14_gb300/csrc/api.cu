@@ -473,3 +473,93 @@ int gemm14_debug_inject(int fault, uint64_t wait_limit_ns) {
 int gemm14_version(void) { return 100; }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// The entry point that allocates nothing.
+//
+// Some callers may not allocate device memory at all: code that runs inside a
+// framework whose pool has reserved the GPU's memory up front and owns every
+// allocation, plug-ins and embedded libraries that are not allowed to touch
+// the allocator, and latency-critical paths that cannot afford the implicit
+// device synchronisation of cudaMalloc / cudaFree. Such a caller cannot set
+// up the workspace of gemm_bf16_f32acc_ws. gemm_bf16_f32acc_noalloc gives it
+// the same product with the workspace taken from a fixed array that lives in
+// the library itself (reserved on every GPU that loads the library, for as
+// long as the process runs).
+namespace gemm14 {
+namespace {
+
+// Capacity of the built-in scratch: enough for every product the one-SM
+// tensor-core kernel splits with tiles up to 128 columns wide on this GPU
+// (flags + one 128 x 128 fp32 slot per SM: about 10 MB on 152 SMs).
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocScratch {
+  bool ready = false;
+  unsigned char* ptr = nullptr;  // device address of g_noalloc_scratch
+};
+NoAllocScratch g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// Device address of the scratch on the current device, looked up once per
+// device (the symbol's host-side name is not a device address), with its
+// flag words cleared on that first use, on the caller's stream.
+int noalloc_scratch(int sm_count, cudaStream_t stream, unsigned char** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    set_cuda_error("cudaGetDevice", e);
+    return GEMM14_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  NoAllocScratch& s = g_noalloc[dev];
+  if (!s.ready) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess) {
+      set_cuda_error("cudaGetSymbolAddress(no-alloc scratch)", e);
+      return GEMM14_ERR_CUDA;
+    }
+    if ((e = cudaMemsetAsync(p, 0, streamk_flag_bytes(sm_count), stream)) != cudaSuccess) {
+      set_cuda_error("cudaMemsetAsync(no-alloc scratch flags)", e);
+      return GEMM14_ERR_CUDA;
+    }
+    s.ptr = static_cast<unsigned char*>(p);
+    s.ready = true;
+  }
+  *out = s.ptr;
+  return GEMM14_OK;
+}
+
+}  // namespace
+}  // namespace gemm14
+
+extern "C" int gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K, const void* A,
+                                        int64_t lda, const void* B, int64_t ldb, float* C,
+                                        int64_t ldc, void* stream_ptr) {
+  int st = validate(GEMM14_DTYPE_BF16, M, N, K, A, lda, B, ldb, C, ldc);
+  if (st != GEMM14_OK) return st;
+  if (M == 0 || N == 0 || K == 0)  // nothing to split: the plain path
+    return run_gemm(GEMM14_DTYPE_BF16, M, N, K, A, lda, B, ldb, C, ldc, nullptr, 0, stream_ptr);
+  const DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev)) != GEMM14_OK) return st;
+  gemm14_plan plan;
+  plan_for(GEMM14_DTYPE_BF16, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+  const size_t need = workspace_need(plan, dev->sm_count);
+  if (need > kNoAllocScratchBytes) {
+    std::snprintf(t_last_error, sizeof t_last_error,
+                  "gemm_bf16_f32acc_noalloc: this product needs %zu bytes of scratch, more than "
+                  "the %zu bytes built into the library; use gemm_bf16_f32acc_ws",
+                  need, kNoAllocScratchBytes);
+    return GEMM14_ERR_INVALID_ARG;
+  }
+  if (need == 0)
+    return run_gemm(GEMM14_DTYPE_BF16, M, N, K, A, lda, B, ldb, C, ldc, nullptr, 0, stream_ptr);
+  unsigned char* scratch = nullptr;
+  if ((st = noalloc_scratch(dev->sm_count, static_cast<cudaStream_t>(stream_ptr), &scratch)) !=
+      GEMM14_OK)
+    return st;
+  return run_gemm(GEMM14_DTYPE_BF16, M, N, K, A, lda, B, ldb, C, ldc, scratch,
+                  kNoAllocScratchBytes, stream_ptr);
+}

@@ -121,6 +121,32 @@ int gemm_f16_f32acc_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t l
                        size_t workspace_bytes, void* stream);
 
 /*
+ * gemm_bf16_f32acc without any device allocation by the caller or the
+ * library. The pages have no counterpart to this entry point; it exists for
+ * callers that may not allocate device memory: code inside a framework whose
+ * memory pool has reserved the GPU and owns every allocation, plug-ins that
+ * must not touch the allocator, and latency-critical paths that cannot take
+ * the implicit device synchronisation of cudaMalloc / cudaFree. The caller
+ * passes A, B and C exactly as for gemm_bf16_f32acc; the stream-K scratch
+ * that gemm_bf16_f32acc_ws would take from the caller comes instead from a
+ * 16 MiB array built into the library, which every GPU that loads the library
+ * holds until the process exits. It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ * Limit: products whose split needs more than the 16 MiB (on this GPU, those
+ * the one-SM kernel computes in 256-column tiles, e.g. M <= 128 with wide N)
+ * return GEMM14_ERR_INVALID_ARG and gemm14_last_error_string() says how many
+ * bytes were needed; products that need no scratch run as gemm_bf16_f32acc.
+ * Set-up: the first call on each device looks up the array's device address
+ * and clears its flag words on the caller's stream; make that first call
+ * before any stream capture. Every call shares the one array, which keeps the
+ * last call's contents (only its flag words must start at zero, and calls
+ * leave them holding finished calls' numbers): calls that may overlap on the
+ * GPU race with each other and must not be issued.
+ */
+int gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                             const void* B, int64_t ldb, float* C, int64_t ldc, void* stream);
+
+/*
  * Workspace bytes that let the *_ws call of this dtype and shape use the
  * stream-K schedule on a GPU with sm_count SMs (sm_count <= 0: the current
  * device's). 0 means the call would not split tiles (whole waves, between
