@@ -67,6 +67,10 @@ def _load():
             lib.oracle_gemm_entries.restype = ctypes.c_int
             lib.oracle_decode_matrix.argtypes = [ctypes.c_int, vp, i64, i64, i64, dp]
             lib.oracle_decode_matrix.restype = ctypes.c_int
+            lib.oracle_gemm_ex.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_double, vp, i64, vp, i64, ctypes.c_double,
+                                           vp, i64, dp, dp, i64, ctypes.c_int]
+            lib.oracle_gemm_ex.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -120,6 +124,36 @@ def gemm(A: np.ndarray, B: np.ndarray, dtype: str = "f32", threads: int = 0,
                              _ptr(C), _ptr(Cabs) if Cabs is not None else 0, N, threads)
     if rc != 0:
         raise RuntimeError(f"oracle_gemm failed with code {rc}")
+    return C, Cabs
+
+
+def gemm_ex(A: np.ndarray, B: np.ndarray, dtype: str = "f32", transa: bool = False,
+            transb: bool = False, alpha: float = 1.0, beta: float = 0.0,
+            C0: np.ndarray | None = None, threads: int = 0):
+    """Returns (C, Cabs) for C = alpha * op(A) @ op(B) + beta * C0 in float64.
+
+    A and B are the STORED arrays: op(A) = A (M x K) or A.T when transa (A is
+    then K x M); likewise for B. C0 is float32 M x N, read only if beta != 0.
+    """
+    code = DTYPE_CODES[dtype]
+    A = _check(A, dtype, "A")
+    B = _check(B, dtype, "B")
+    M, K = (A.shape[1], A.shape[0]) if transa else A.shape
+    K2, N = (B.shape[1], B.shape[0]) if transb else B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: op(A) {M}x{K}, op(B) {K2}x{N}")
+    if beta != 0.0:
+        if C0 is None or C0.shape != (M, N):
+            raise ValueError("C0 of shape (M, N) is needed when beta != 0")
+        C0 = np.ascontiguousarray(C0, dtype=np.float32)
+    C = np.empty((M, N), dtype=np.float64)
+    Cabs = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_ex(M, N, K, code, int(bool(transa)), int(bool(transb)),
+                                float(alpha), _ptr(A), _ld(A), _ptr(B), _ld(B), float(beta),
+                                _ptr(C0) if beta != 0.0 else 0, N, _ptr(C), _ptr(Cabs), N,
+                                threads)
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_ex failed with code {rc}")
     return C, Cabs
 
 

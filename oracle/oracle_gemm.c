@@ -166,6 +166,67 @@ int oracle_gemm_entries(int64_t M, int64_t N, int64_t K, int dtype,
   return 0;
 }
 
+/*
+ * The extended product of the pages' wgmma description (gpu-hpc-book ch.06
+ * "Tensor Cores" / "wgmma": D = A*B + D, with A and B optionally transposed
+ * and negated, and D scaled by 0 or 1), written for general scalars:
+ *     C[i][j] = alpha * sum_k opA[i][k] * opB[k][j] + beta * C0[i][j]
+ * where opA[i][k] = A[i*lda + k] (transa == 0) or A[k*lda + i] (transa != 0),
+ * and   opB[k][j] = B[k*ldb + j] (transb == 0) or B[j*ldb + k] (transb != 0).
+ * C0 is fp32 (ldc0) and is not read when beta == 0. Cabs (if not NULL) is
+ * |alpha| * sum |opA||opB| + |beta| * |C0| (0 for the second term when
+ * beta == 0), the scale of the error bound. The sum runs over k in order, in
+ * double; alpha * sum and beta * C0 are formed in double and added last.
+ */
+int oracle_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, int transa, int transb,
+                   double alpha, const void *A, int64_t lda, const void *B, int64_t ldb,
+                   double beta, const float *C0, int64_t ldc0, double *C, double *Cabs,
+                   int64_t ldc, int nthreads) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
+  if (lda < (transa ? M : K) || ldb < (transb ? K : N) || ldc < N) return -1;
+  if (M == 0 || N == 0) return 0;
+  if (!C || (K > 0 && (!A || !B)) || (beta != 0.0 && (!C0 || ldc0 < N))) return -1;
+
+  /* opB decoded once, K x N row-major */
+  double *Bd = NULL;
+  if (K > 0) {
+    Bd = (double *)malloc((size_t)K * (size_t)N * sizeof(double));
+    if (!Bd) return -2;
+    for (int64_t k = 0; k < K; ++k)
+      for (int64_t j = 0; j < N; ++j)
+        Bd[k * N + j] = decode_one(dtype, B, transb ? j * ldb + k : k * ldb + j);
+  }
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+  for (int64_t i = 0; i < M; ++i) {
+    double *c = C + i * ldc;
+    double *cabs = Cabs ? Cabs + i * ldc : NULL;
+    for (int64_t j = 0; j < N; ++j) {
+      c[j] = 0.0;
+      if (cabs) cabs[j] = 0.0;
+    }
+    for (int64_t k = 0; k < K; ++k) {
+      const double a = decode_one(dtype, A, transa ? k * lda + i : i * lda + k);
+      const double *b = Bd + k * N;
+      for (int64_t j = 0; j < N; ++j) c[j] += a * b[j];
+      if (cabs) {
+        const double aa = fabs(a);
+        for (int64_t j = 0; j < N; ++j) cabs[j] += aa * fabs(b[j]);
+      }
+    }
+    for (int64_t j = 0; j < N; ++j) {
+      const double c0 = beta != 0.0 ? (double)C0[i * ldc0 + j] : 0.0;
+      c[j] = alpha * c[j] + (beta != 0.0 ? beta * c0 : 0.0);
+      if (cabs) cabs[j] = fabs(alpha) * cabs[j] + (beta != 0.0 ? fabs(beta) * fabs(c0) : 0.0);
+    }
+  }
+  free(Bd);
+  return 0;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

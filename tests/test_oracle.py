@@ -258,3 +258,71 @@ def test_inputs_are_seeded_and_shaped():
     assert torch.equal(A.float().half().float() - A16.float(), A.float().half().float() - A16.float())
     w = inputs.WORKLOADS["bf16_8192"]
     assert math.isclose(w.sigma, 1 / math.sqrt(8192))
+
+
+# ----------------------------------------------------------------- the extended product
+# C = alpha * op(A) @ op(B) + beta * C0 (the pages' wgmma: D = A*B + D with
+# transposable, negatable operands and D scaled by 0 or 1; generalised).
+
+@pytest.mark.parametrize("transa,transb", [(False, False), (True, False), (False, True),
+                                           (True, True)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ex_transposes_match_plain_product(oracle_mod, transa, transb, dtype):
+    """Stored transposes (made by numpy) give exactly the plain product."""
+    A_t, B_t = inputs.make(23, 17, 31, dtype, "normal", 1.0, seed=51)
+    A, B = inputs.host_view(A_t), inputs.host_view(B_t)
+    C, Cabs = oracle_mod.gemm(A, B, dtype)
+    As = np.ascontiguousarray(A.T) if transa else A
+    Bs = np.ascontiguousarray(B.T) if transb else B
+    C2, Cabs2 = oracle_mod.gemm_ex(As, Bs, dtype, transa, transb)
+    assert np.array_equal(C, C2) and np.array_equal(Cabs, Cabs2)
+
+
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (1.0, 1.0), (-1.0, 1.0), (2.0, -3.0),
+                                        (0.5, 0.25), (0.0, 1.0), (-1.0, 0.0)])
+def test_ex_alpha_beta_integer_exact(oracle_mod, alpha, beta):
+    """Integer matrices and dyadic scalars: the exact result, computed with
+    Python fractions, including the |alpha||A||B| + |beta||C0| scale."""
+    from fractions import Fraction as F
+    A_t, B_t = inputs.make_integer(9, 11, 13, 4, "f32", seed=52)
+    g = np.random.default_rng(53)
+    C0 = g.integers(-50, 51, (9, 11)).astype(np.float32)
+    A, B = A_t.numpy(), B_t.numpy()
+    C, Cabs = oracle_mod.gemm_ex(A, B, "f32", alpha=alpha, beta=beta, C0=C0)
+    AB = A.astype(np.int64) @ B.astype(np.int64)
+    AbsAB = np.abs(A.astype(np.int64)) @ np.abs(B.astype(np.int64))
+    for i in range(9):
+        for j in range(11):
+            want = F(alpha) * int(AB[i, j]) + F(beta) * F(float(C0[i, j]))
+            want_abs = abs(F(alpha)) * int(AbsAB[i, j]) + abs(F(beta)) * abs(F(float(C0[i, j])))
+            assert C[i, j] == float(want) and Cabs[i, j] == float(want_abs)
+
+
+def test_ex_beta_zero_does_not_read_c0(oracle_mod):
+    A_t, B_t = inputs.make(8, 8, 8, "f32", "uniform", 1.0, seed=54)
+    C0 = np.full((8, 8), np.nan, np.float32)
+    C, Cabs = oracle_mod.gemm_ex(A_t.numpy(), B_t.numpy(), "f32", alpha=2.0, beta=0.0, C0=C0)
+    ref, refabs = oracle_mod.gemm(A_t.numpy(), B_t.numpy())
+    assert not np.isnan(C).any()
+    assert np.array_equal(C, 2.0 * ref) and np.array_equal(Cabs, 2.0 * refabs)
+
+
+def test_ex_brute_force_tiny_fraction(oracle_mod):
+    """All shapes in {1..3}^3, every transpose combination, dyadic entries and
+    scalars: exact rational sums."""
+    from fractions import Fraction as F
+    g = np.random.default_rng(55)
+    for M, N, K in itertools.product(range(1, 4), repeat=3):
+        for ta, tb in itertools.product([False, True], repeat=2):
+            A = (g.integers(-16, 17, (M, K)) / 8.0).astype(np.float32)
+            B = (g.integers(-16, 17, (K, N)) / 8.0).astype(np.float32)
+            C0 = (g.integers(-16, 17, (M, N)) / 4.0).astype(np.float32)
+            alpha, beta = float(g.integers(-4, 5)) / 2, float(g.integers(-4, 5)) / 2
+            As = np.ascontiguousarray(A.T) if ta else A
+            Bs = np.ascontiguousarray(B.T) if tb else B
+            C, _ = oracle_mod.gemm_ex(As, Bs, "f32", ta, tb, alpha, beta, C0)
+            for i in range(M):
+                for j in range(N):
+                    s = sum(F(float(A[i, k])) * F(float(B[k, j])) for k in range(K))
+                    want = F(alpha) * s + (F(beta) * F(float(C0[i, j])) if beta else 0)
+                    assert C[i, j] == float(want)
