@@ -14,15 +14,14 @@ from __future__ import annotations
 
 from ._lib import (GEMM14_DTYPE_BF16, GEMM14_DTYPE_F16, GEMM14_DTYPE_F32, Gemm14Error, Plan,
                    check_device_error, debug_inject, gemm_bf16_f32acc, gemm_bf16_f32acc_ws,
-                   gemm_bf16_f32acc_noalloc, gemm_f16_f32acc, gemm_f16_f32acc_ws, gemm_f32, gemm_f32_ws,
-                   last_error_string, lib_path, load,
-                   plan, set_pair_kernel, status_string, version, workspace_bytes)
+                   gemm_bf16_f32acc_noalloc, gemm_ex, gemm_f16_f32acc, gemm_f16_f32acc_ws, gemm_f32,
+                   gemm_f32_ws, last_error_string, lib_path, load, plan, plan_ex, set_pair_kernel, status_string, version, workspace_bytes)
 from .api import gemm, gemm_into
 
 __all__ = [
     "gemm", "gemm_into", "gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "gemm_f32_ws",
-    "gemm_bf16_f32acc_ws", "gemm_f16_f32acc_ws", "gemm_bf16_f32acc_noalloc", "workspace_bytes",
-    "last_error_string", "plan", "Plan",
+    "gemm_bf16_f32acc_ws", "gemm_f16_f32acc_ws", "gemm_bf16_f32acc_noalloc", "gemm_ex", "workspace_bytes",
+    "last_error_string", "plan", "plan_ex", "Plan",
     "check_device_error", "debug_inject", "set_pair_kernel", "status_string", "version", "load", "lib_path", "Gemm14Error",
     "GEMM14_DTYPE_F32", "GEMM14_DTYPE_BF16", "GEMM14_DTYPE_F16",
 ]

@@ -48,6 +48,10 @@ SIGNATURES = {
     "gemm_f16_f32acc_ws": (_int, _GEMM_ARGS[:9] + [_vp, ctypes.c_size_t, _vp]),
     "gemm14_workspace_bytes": (ctypes.c_size_t, [_int, _i64, _i64, _i64, _int]),
     "gemm_bf16_f32acc_noalloc": (_int, _GEMM_ARGS),
+    "gemm14_gemm_ex": (_int, [_int, _int, _int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64,
+                              _vp, _i64, ctypes.c_float, _vp, _i64, _vp, ctypes.c_size_t, _vp]),
+    "gemm14_plan_gemm_ex": (_int, [_int, _int, _int, _i64, _i64, _i64, _vp, _i64, _vp, _i64,
+                                   _vp, _i64, _int, ctypes.POINTER(_Plan)]),
 }
 
 _lib = None
@@ -160,6 +164,18 @@ def gemm_bf16_f32acc_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=None, check
     return st
 
 
+def gemm_ex(dtype: int, transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+            workspace=None, workspace_bytes=0, stream=None, check=True) -> int:
+    """C ABI gemm14_gemm_ex: C = alpha * op(A) op(B) + beta * C on raw device
+    pointers, op(A) = A stored M x K (transa 0) or its transpose stored K x M
+    (transa 1), likewise B."""
+    st = int(load().gemm14_gemm_ex(dtype, transa, transb, M, N, K, alpha, A, lda, B, ldb, beta,
+                                   C, ldc, workspace, workspace_bytes, stream))
+    if check and st:
+        raise Gemm14Error(st, "gemm14_gemm_ex")
+    return st
+
+
 def last_error_string() -> str:
     """Text of the last failure seen by this thread (the C ABI's message)."""
     return load().gemm14_last_error_string().decode(errors="replace")
@@ -207,4 +223,12 @@ def plan(dtype: int, M, N, K, A, lda, B, ldb, C, ldc, sm_count: int):
     p = _Plan()
     st = int(load().gemm14_plan_gemm(dtype, M, N, K, A, lda, B, ldb, C, ldc, sm_count,
                                      ctypes.byref(p)))
+    return st, Plan(**{f: getattr(p, f) for f, _ in _Plan._fields_})
+
+
+def plan_ex(dtype: int, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, sm_count: int):
+    """Host-only launch plan of a gemm_ex call. Returns (status, Plan)."""
+    p = _Plan()
+    st = int(load().gemm14_plan_gemm_ex(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc,
+                                        sm_count, ctypes.byref(p)))
     return st, Plan(**{f: getattr(p, f) for f, _ in _Plan._fields_})

@@ -5,11 +5,6 @@ import torch
 
 from . import _lib
 
-_ENTRY_WS = {
-    torch.float32: _lib.gemm_f32_ws,
-    torch.bfloat16: _lib.gemm_bf16_f32acc_ws,
-    torch.float16: _lib.gemm_f16_f32acc_ws,
-}
 _CODE = {torch.float32: _lib.GEMM14_DTYPE_F32, torch.bfloat16: _lib.GEMM14_DTYPE_BF16,
          torch.float16: _lib.GEMM14_DTYPE_F16}
 
@@ -35,24 +30,46 @@ def _check_matrix(x: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must have unit stride along its rows (row-major)")
 
 
-def gemm_into(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
-    """out = a @ b on the GPU through the C ABI; a, b, out are CUDA tensors.
+def _operand(x: torch.Tensor, name: str) -> tuple[int, int]:
+    """(trans, ld) of an operand view: trans 0 for a row-major view (unit
+    stride along rows, pitch stride(0)); trans 1 for the transpose of a
+    row-major matrix (unit stride down columns, pitch stride(1))."""
+    if x.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(x.shape)}")
+    rows, cols = x.shape
+    if cols <= 1 or x.stride(1) == 1:
+        if rows > 1 and x.stride(0) < max(cols, 1):
+            raise ValueError(f"{name}: rows overlap (stride {x.stride()})")
+        return 0, max(x.stride(0), cols, 1)
+    if rows <= 1 or x.stride(0) == 1:
+        if x.stride(1) < max(rows, 1):
+            raise ValueError(f"{name}: columns overlap (stride {x.stride()})")
+        return 1, max(x.stride(1), rows, 1)
+    raise ValueError(f"{name} needs unit stride along its rows or its columns, got {x.stride()}")
 
-    Uses the stream-K entry point with a workspace cached per (device,
-    stream) when the product benefits from it.
 
-    a: (M, K), b: (K, N) in float32, bfloat16 or float16 (same dtype);
-    out: (M, N) float32. Row pitches come from the tensors' strides. Runs on
-    `stream` (default: torch's current stream) without synchronising.
+def gemm_into(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor, alpha: float = 1.0,
+              beta: float = 0.0, stream=None) -> torch.Tensor:
+    """out = alpha * a @ b + beta * out on the GPU through the C ABI
+    (gemm14_gemm_ex); a, b, out are CUDA tensors.
+
+    a: (M, K), b: (K, N) in float32, bfloat16 or float16 (same dtype), each
+    either a row-major view or the transpose of one (e.g. ``x.t()``), which
+    becomes the call's transa / transb; out: (M, N) float32, row-major. With
+    beta == 0, out is not read. Uses a stream-K workspace cached per (device,
+    stream) when the product benefits from it. Runs on `stream` (default:
+    torch's current stream) without synchronising.
     """
-    if a.dtype != b.dtype or a.dtype not in _ENTRY_WS:
+    if a.dtype != b.dtype or a.dtype not in _CODE:
         raise TypeError(f"unsupported dtypes {a.dtype}, {b.dtype}")
     if out.dtype != torch.float32:
         raise TypeError("out must be float32")
     for x, n in ((a, "a"), (b, "b"), (out, "out")):
-        _check_matrix(x, n)
         if not x.is_cuda:
             raise ValueError(f"{n} must be a CUDA tensor")
+    _check_matrix(out, "out")
+    ta, lda = _operand(a, "a")
+    tb, ldb = _operand(b, "b")
     M, K = a.shape
     K2, N = b.shape
     if K != K2 or tuple(out.shape) != (M, N):
@@ -64,9 +81,9 @@ def gemm_into(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor, stream=None) 
     with torch.cuda.device(a.device):
         nbytes = _lib.workspace_bytes(_CODE[a.dtype], M, N, K, 0) if M and N and K else 0
         ws = _workspace(a.device, int(stream or 0), nbytes) if nbytes else None
-        _ENTRY_WS[a.dtype](M, N, K, a.data_ptr(), max(a.stride(0), 1), b.data_ptr(),
-                           max(b.stride(0), 1), out.data_ptr(), max(out.stride(0), 1),
-                           ws.data_ptr() if ws is not None else None, nbytes, stream)
+        _lib.gemm_ex(_CODE[a.dtype], ta, tb, M, N, K, float(alpha), a.data_ptr(), lda,
+                     b.data_ptr(), ldb, float(beta), out.data_ptr(), max(out.stride(0), N, 1),
+                     ws.data_ptr() if ws is not None else None, nbytes, stream)
     return out
 
 

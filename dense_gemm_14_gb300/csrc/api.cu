@@ -148,14 +148,19 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int elem_bytes_of(int dtype) { return dtype == GEMM14_DTYPE_F32 ? 4 : 2; }
 
-// Argument validation shared by the entry points and the planner.
-int validate(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-             const void* B, int64_t ldb, const void* C, int64_t ldc) {
+// Argument validation shared by the entry points and the planner. transa /
+// transb select the stored shape of A (M x K, or K x M) and of B (K x N, or
+// N x K); each must be 0 or 1.
+int validate(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K, const void* A,
+             int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc) {
   if (dtype != GEMM14_DTYPE_F32 && dtype != GEMM14_DTYPE_BF16 && dtype != GEMM14_DTYPE_F16)
     return GEMM14_ERR_INVALID_ARG;
+  if ((transa != 0 && transa != 1) || (transb != 0 && transb != 1)) return GEMM14_ERR_INVALID_ARG;
   const int64_t kMax = INT32_MAX;
   if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax) return GEMM14_ERR_INVALID_ARG;
-  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+  const int64_t a_cols = transa ? M : K, b_cols = transb ? K : N;
+  if (lda < (a_cols > 1 ? a_cols : 1) || ldb < (b_cols > 1 ? b_cols : 1) ||
+      ldc < (N > 1 ? N : 1))
     return GEMM14_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return GEMM14_OK;
   if (!C || !aligned(C, 4)) return GEMM14_ERR_INVALID_ARG;
@@ -166,11 +171,18 @@ int validate(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   if (lda > (int64_t(1) << 36) || ldb > (int64_t(1) << 36)) return GEMM14_ERR_INVALID_ARG;
   return GEMM14_OK;
 }
+int validate(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+             const void* B, int64_t ldb, const void* C, int64_t ldc) {
+  return validate(dtype, 0, 0, M, N, K, A, lda, B, ldb, C, ldc);
+}
 
 int hgemm_bn_for(int64_t N) { return N <= 64 ? 64 : N <= 128 ? 128 : 256; }
 
-void plan_for(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-              const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
+// The fp32 kernel's TMA loader serves untransposed operands only; stored
+// transposes go through its cp.async loader. The 16-bit kernels' TMA loaders
+// serve every storage (a transposed operand is an MN-major A or a K-major B).
+void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K, const void* A,
+              int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
               gemm14_plan* p) {
   std::memset(p, 0, sizeof *p);
   if (M == 0 || N == 0 || K == 0) return;  // nothing launched (K == 0: a memset)
@@ -178,7 +190,10 @@ void plan_for(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t
   if (dtype == GEMM14_DTYPE_F32) {
     using S = SgemmShape;
     p->kernel = 1;
-    p->loader = (aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 && ldb % 4 == 0) ? 1 : 2;
+    p->loader = (!transa && !transb && aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 &&
+                 ldb % 4 == 0)
+                    ? 1
+                    : 2;
     p->bm = S::BM;
     p->bn = S::BN;
     p->bk = S::BK;
@@ -214,6 +229,11 @@ void plan_for(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t
   p->tiles = ((M + p->bm - 1) / p->bm) * ((N + p->bn - 1) / p->bn);
   const int64_t sms = sm_count > 0 ? sm_count : 1;
   p->grid = static_cast<int>(p->tiles < sms ? p->tiles : sms);
+}
+void plan_for(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+              const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
+              gemm14_plan* p) {
+  plan_for(dtype, 0, 0, M, N, K, A, lda, B, ldb, C, ldc, sm_count, p);
 }
 
 bool debug_checks() {
@@ -269,15 +289,31 @@ void schedule(const gemm14_plan& plan, int64_t K, int sm_count, void* workspace,
   }
 }
 
-int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-             const void* B, int64_t ldb, float* C, int64_t ldc, void* workspace,
-             size_t workspace_bytes, void* stream_ptr) {
+// Tensor maps of the 16-bit kernels for a tile of bm rows x bn columns:
+// A stored M x K: box 64 k x bm m; stored K x M: box 64 m x 64 k (bm / 64
+// loads per stage). B stored K x N: box 64 n x 64 k (bn / 64 loads); stored
+// N x K: box 64 k x bn n. All with the 128-byte swizzle.
+int make_maps_16(bool bf16, int transa, int transb, int64_t M, int64_t N, int64_t K,
+                 const void* A, int64_t lda, const void* B, int64_t ldb, int bm, int bn,
+                 CUtensorMap* ma, CUtensorMap* mb) {
+  const CUtensorMapDataType tt =
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  int st = transa ? make_map(ma, tt, 2, A, K, M, lda, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
+                  : make_map(ma, tt, 2, A, M, K, lda, 64, bm, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != GEMM14_OK) return st;
+  return transb ? make_map(mb, tt, 2, B, N, K, ldb, 64, bn, CU_TENSOR_MAP_SWIZZLE_128B)
+                : make_map(mb, tt, 2, B, K, N, ldb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K, float alpha,
+             const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
+             int64_t ldc, void* workspace, size_t workspace_bytes, void* stream_ptr) {
   // A pending test request applies to this call only, whatever its outcome.
   const int fault = t_fault;
   const unsigned long long wait_limit_ns = t_wait_limit_ns ? t_wait_limit_ns : kWaitTimeoutNs;
   t_fault = kFaultNone;
   t_wait_limit_ns = 0;
-  int st = validate(dtype, M, N, K, A, lda, B, ldb, C, ldc);
+  int st = validate(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc);
   if (st != GEMM14_OK) return st;
   if (workspace && !aligned(workspace, 16)) return GEMM14_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return GEMM14_OK;
@@ -285,17 +321,26 @@ int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   if ((st = current_device(&dev)) != GEMM14_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
-  if (K == 0) {
-    cudaError_t e = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 4, 0,
-                                      static_cast<size_t>(N) * 4, static_cast<size_t>(M), stream);
-    return finish(e, "cudaMemset2DAsync", stream);
+  if (K == 0 || alpha == 0.0f) {
+    // No product term (A and B are not read): C = beta * C.
+    if (beta == 1.0f) return GEMM14_OK;
+    if (beta == 0.0f) {
+      cudaError_t e = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 4, 0,
+                                        static_cast<size_t>(N) * 4, static_cast<size_t>(M),
+                                        stream);
+      return finish(e, "cudaMemset2DAsync", stream);
+    }
+    return finish(launch_scale_c(C, ldc, static_cast<int>(M), static_cast<int>(N), beta,
+                                 dev->sm_count, stream),
+                  "scale launch", stream);
   }
 
   gemm14_plan plan;
-  plan_for(dtype, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+  plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+  const int epi = beta != 0.0f ? kEpiAccum : alpha != 1.0f ? kEpiScale : kEpiStore;
   GemmArgs args{static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                A, lda, B, ldb, C, ldc, plan.vec_store, dev->err_word, wait_limit_ns, fault,
-                StreamK{}, nullptr, nullptr, 0u};
+                A, lda, B, ldb, C, ldc, plan.vec_store, transa, transb, epi, alpha, beta,
+                dev->err_word, wait_limit_ns, fault, StreamK{}, nullptr, nullptr, 0u};
   int grid = plan.grid;
 
   if (dtype == GEMM14_DTYPE_F32) {
@@ -322,37 +367,38 @@ int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
     }
   }
   if (plan.kernel == 3 && pair_clusters > 0) {
-    const CUtensorMapDataType tt =
-        bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap ma, mb;
-    if ((st = make_map(&ma, tt, 2, A, M, K, lda, PairShape::BK, 128,
-                       CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
-      return st;
-    if ((st = make_map(&mb, tt, 2, B, K, N, ldb, 64, PairShape::BK,
-                       CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
+    // each CTA of a pair loads 128 rows of A and 128 columns of B
+    if ((st = make_maps_16(bf16, transa, transb, M, N, K, A, lda, B, ldb, 128, 128, &ma, &mb)) !=
+        GEMM14_OK)
       return st;
     const int64_t clusters = plan.tiles < pair_clusters ? plan.tiles : pair_clusters;
-    const uint32_t idesc2 = idesc_f16_f32acc(bf16, PairShape::BM, PairShape::BN);
+    const uint32_t idesc2 =
+        idesc_f16_f32acc(bf16, PairShape::BM, PairShape::BN, transa != 0, transb == 0);
     return finish(launch_hgemm_tc_pair(ma, mb, args, idesc2, static_cast<int>(clusters), stream),
                   "hgemm pair launch", stream);
   }
-  if (plan.kernel == 3) plan_for(dtype, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+  if (plan.kernel == 3)
+    plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
   schedule(plan, K, dev->sm_count, workspace, workspace_bytes, args, grid);
-  const uint32_t idesc = idesc_f16_f32acc(bf16, HgemmShape::BM, plan.bn);
+  const uint32_t idesc =
+      idesc_f16_f32acc(bf16, HgemmShape::BM, plan.bn, transa != 0, transb == 0);
   if (plan.loader == 2)
     return finish(launch_hgemm_tc_soft(plan.bn, args, idesc, grid, stream), "hgemm launch",
                   stream);
-  const CUtensorMapDataType tt =
-      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap ma, mb;
-  if ((st = make_map(&ma, tt, 2, A, M, K, lda, HgemmShape::BK, HgemmShape::BM,
-                     CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
-    return st;
-  if ((st = make_map(&mb, tt, 2, B, K, N, ldb, 64, HgemmShape::BK, CU_TENSOR_MAP_SWIZZLE_128B)) !=
-      GEMM14_OK)
+  if ((st = make_maps_16(bf16, transa, transb, M, N, K, A, lda, B, ldb, HgemmShape::BM, plan.bn,
+                         &ma, &mb)) != GEMM14_OK)
     return st;
   return finish(launch_hgemm_tc(plan.bn, ma, mb, args, idesc, grid, stream), "hgemm launch",
                 stream);
+}
+
+int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+             const void* B, int64_t ldb, float* C, int64_t ldc, void* workspace,
+             size_t workspace_bytes, void* stream_ptr) {
+  return run_gemm(dtype, 0, 0, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, workspace,
+                  workspace_bytes, stream_ptr);
 }
 
 }  // namespace
@@ -396,6 +442,14 @@ int gemm_f16_f32acc_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t l
                        size_t workspace_bytes, void* stream) {
   return run_gemm(GEMM14_DTYPE_F16, M, N, K, A, lda, B, ldb, C, ldc, workspace, workspace_bytes,
                   stream);
+}
+
+int gemm14_gemm_ex(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
+                   float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                   float beta, float* C, int64_t ldc, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  return run_gemm(dtype, transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, workspace,
+                  workspace_bytes, stream);
 }
 
 size_t gemm14_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int sm_count) {
@@ -457,6 +511,16 @@ int gemm14_plan_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, 
   return GEMM14_OK;
 }
 
+int gemm14_plan_gemm_ex(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
+                        const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
+                        int64_t ldc, int sm_count, gemm14_plan* plan) {
+  if (!plan) return GEMM14_ERR_INVALID_ARG;
+  int st = validate(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc);
+  if (st != GEMM14_OK) return st;
+  plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, sm_count, plan);
+  return GEMM14_OK;
+}
+
 int gemm14_set_pair_kernel(int enable) {
   const int previous = g_pair_enabled.load();
   g_pair_enabled.store(enable ? 1 : 0);
@@ -470,7 +534,7 @@ int gemm14_debug_inject(int fault, uint64_t wait_limit_ns) {
   return GEMM14_OK;
 }
 
-int gemm14_version(void) { return 100; }
+int gemm14_version(void) { return 200; }
 
 }  // extern "C"
 

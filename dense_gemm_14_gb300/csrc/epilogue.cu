@@ -1,0 +1,42 @@
+// epilogue.cu -- C = beta * C without a product term: what the extended
+// product alpha * op(A) * op(B) + beta * C leaves when K == 0 or alpha == 0
+// (A and B are then not read, so a NaN or infinity in them does not reach C).
+// A memory-bound pass: each C element is read and written once, with
+// 16-byte accesses in rows whose start and pitch allow them.
+#include "kernels.h"
+
+namespace gemm14 {
+namespace {
+
+// Grid-stride over rows; the threads of a block cover a row's columns.
+__global__ void __launch_bounds__(256) scale_c_kernel(float* C, int64_t ldc, int M, int N,
+                                                      float beta, int vec) {
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+    float* c = C + row * ldc;
+    if (vec) {
+      float4* c4 = reinterpret_cast<float4*>(c);
+      const int n4 = N / 4;
+      for (int j = threadIdx.x; j < n4; j += blockDim.x) {
+        float4 v = c4[j];
+        v.x *= beta; v.y *= beta; v.z *= beta; v.w *= beta;
+        c4[j] = v;
+      }
+      for (int j = 4 * n4 + threadIdx.x; j < N; j += blockDim.x) c[j] *= beta;
+    } else {
+      for (int j = threadIdx.x; j < N; j += blockDim.x) c[j] *= beta;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_scale_c(float* C, int64_t ldc, int M, int N, float beta, int sm_count,
+                           cudaStream_t stream) {
+  const int vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
+  const int64_t cap = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 8;
+  const int grid = static_cast<int>(M < cap ? M : cap);
+  scale_c_kernel<<<grid, 256, 0, stream>>>(C, ldc, M, N, beta, vec);
+  return cudaGetLastError();
+}
+
+}  // namespace gemm14

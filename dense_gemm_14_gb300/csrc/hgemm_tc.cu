@@ -74,42 +74,72 @@ __device__ __forceinline__ uint32_t ld_pair(const uint16_t* base, int64_t row_of
   return lo | (hi << 16);
 }
 
+// A K-major operand tile of ROWS rows (matrix rows row0 ..) by 64 k (from
+// k0): 128-byte rows. Lane l holds k pair (2l, 2l+1) of a row; its 4-byte word
+// sits in 16-byte chunk (l / 4) XOR (row % 8), at byte 4 (l % 4) of the chunk.
+template <int ROWS>
+__device__ __forceinline__ void soft_kmajor(uint8_t* dst, const uint16_t* src, int64_t ld,
+                                            int row0, int nrows, int k0, int K, int lane) {
+  const uint32_t word = static_cast<uint32_t>((lane & 3) << 2);
+  const int k = k0 + 2 * lane;
+#pragma unroll 4
+  for (int r = 0; r < ROWS; ++r) {
+    const int m = row0 + r;
+    const uint32_t v = ld_pair(src, static_cast<int64_t>(m) * ld, k, K, m < nrows);
+    *reinterpret_cast<uint32_t*>(dst + r * 128 + ((((lane >> 2) ^ (r & 7)) & 7) << 4) + word) = v;
+  }
+}
+
+// An MN-major operand tile of COLS columns (matrix columns col0 ..) by 64 k:
+// COLS / 64 boxes of 64 columns x 64 k rows (8 KB each, 128-byte rows).
+template <int COLS>
+__device__ __forceinline__ void soft_mnmajor(uint8_t* dst, const uint16_t* src, int64_t ld,
+                                             int col0, int ncols, int k0, int K, int lane) {
+  const uint32_t word = static_cast<uint32_t>((lane & 3) << 2);
+#pragma unroll 1
+  for (int c = 0; c < COLS / 64; ++c) {
+    const int n0 = col0 + c * 64 + 2 * lane;
+#pragma unroll 4
+    for (int kr = 0; kr < H::BK; ++kr) {
+      const int k = k0 + kr;
+      const uint32_t v = ld_pair(src, static_cast<int64_t>(k) * ld, n0, ncols, k < K);
+      *reinterpret_cast<uint32_t*>(dst + c * (64 * H::BK * 2) + kr * 128 +
+                                   ((((lane >> 2) ^ (kr & 7)) & 7) << 4) + word) = v;
+    }
+  }
+}
+
+// One stage by the software loader. A stored M x K is K-major, stored K x M
+// (transa) MN-major; B stored K x N is MN-major, stored N x K (transb) K-major.
 template <int BN>
 __device__ __forceinline__ void soft_load_stage(uint8_t* a_st, const GemmArgs& args, int tm,
                                                 int tn, int kb, int lane) {
   const uint16_t* A = static_cast<const uint16_t*>(args.A);
   const uint16_t* B = static_cast<const uint16_t*>(args.B);
   uint8_t* b_st = a_st + H::BM * H::BK * 2;
-  // Lane l holds columns 2l, 2l+1 of a 64-wide, 128-byte row; its 4-byte word
-  // sits in 16-byte chunk (l / 4) XOR (row % 8), at byte 4 (l % 4) of the chunk.
-  const uint32_t word = static_cast<uint32_t>((lane & 3) << 2);
-  const int k0 = kb * H::BK + 2 * lane;
-#pragma unroll 4
-  for (int r = 0; r < H::BM; ++r) {
-    const int m = tm * H::BM + r;
-    const uint32_t v = ld_pair(A, static_cast<int64_t>(m) * args.lda, k0, args.K, m < args.M);
-    *reinterpret_cast<uint32_t*>(a_st + r * 128 + ((((lane >> 2) ^ (r & 7)) & 7) << 4) + word) = v;
-  }
-#pragma unroll 1
-  for (int c = 0; c < BN / 64; ++c) {
-    const int n0 = tn * BN + c * 64 + 2 * lane;
-#pragma unroll 4
-    for (int kr = 0; kr < H::BK; ++kr) {
-      const int k = kb * H::BK + kr;
-      const uint32_t v = ld_pair(B, static_cast<int64_t>(k) * args.ldb, n0, args.N, k < args.K);
-      *reinterpret_cast<uint32_t*>(b_st + c * (64 * H::BK * 2) + kr * 128 +
-                                   ((((lane >> 2) ^ (kr & 7)) & 7) << 4) + word) = v;
-    }
-  }
+  const int k0 = kb * H::BK;
+  if (args.transa)
+    soft_mnmajor<H::BM>(a_st, A, args.lda, tm * H::BM, args.M, k0, args.K, lane);
+  else
+    soft_kmajor<H::BM>(a_st, A, args.lda, tm * H::BM, args.M, k0, args.K, lane);
+  if (args.transb)
+    soft_kmajor<BN>(b_st, B, args.ldb, tn * BN, args.N, k0, args.K, lane);
+  else
+    soft_mnmajor<BN>(b_st, B, args.ldb, tn * BN, args.N, k0, args.K, lane);
 }
 
 // kSK: the stream-K schedule (segments, workspace partials); without it the
 // schedule is plain data-parallel and none of the stream-K code is compiled in.
-template <int BN, bool kTma, bool kSK>
+// kGeneral: stored transposes and the alpha / beta epilogue are read from
+// args; without it the kernel is compiled for untransposed operands and a
+// plain store of C (the software-loader variants are always general).
+template <int BN, bool kTma, bool kSK, bool kGeneral>
 __global__ void __launch_bounds__(H::THREADS, 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b, const GemmArgs args,
                     const uint32_t idesc) {
+  const int transa = kGeneral ? args.transa : 0;
+  const int transb = kGeneral ? args.transb : 0;
   constexpr int STAGES = H::stages(BN);
   constexpr int A_BYTES = H::BM * H::BK * 2;   // 16 KB
   constexpr int B_BYTES = H::BK * BN * 2;      // BN/64 boxes of 8 KB
@@ -214,17 +244,32 @@ __global__ void __launch_bounds__(H::THREADS, 1)
           uint8_t* a_st = tiles + s * STAGE_BYTES;
           uint8_t* b_st = a_st + A_BYTES;
           mbar_arrive_expect_tx(&sm.full[s], STAGE_BYTES);
-          tma_load_2d(a_st, &map_a, kb * H::BK, tm * H::BM, &sm.full[s]);
+          // A: one box of 64 k x 128 m, or (stored K x M) two boxes of 64 m x 64 k.
+          if (!transa) {
+            tma_load_2d(a_st, &map_a, kb * H::BK, tm * H::BM, &sm.full[s]);
+          } else {
 #pragma unroll
-          for (int c = 0; c < BN / 64; ++c)
-            tma_load_2d(b_st + c * (64 * H::BK * 2), &map_b, tn * BN + c * 64, kb * H::BK,
-                        &sm.full[s]);
+            for (int c = 0; c < H::BM / 64; ++c)
+              tma_load_2d(a_st + c * (64 * H::BK * 2), &map_a, tm * H::BM + c * 64, kb * H::BK,
+                          &sm.full[s]);
+          }
+          // B: BN / 64 boxes of 64 n x 64 k, or (stored N x K) one box of 64 k x BN n.
+          if (!transb) {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              tma_load_2d(b_st + c * (64 * H::BK * 2), &map_b, tn * BN + c * 64, kb * H::BK,
+                          &sm.full[s]);
+          } else {
+            tma_load_2d(b_st, &map_b, kb * H::BK, tn * BN, &sm.full[s]);
+          }
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      const OperandDesc a_op = operand_desc(transa == 0);
+      const OperandDesc b_op = operand_desc(transb != 0);
       bool ok = true;
       uint32_t it = 0;
       for (int seg = 0; seg < n_seg && ok; ++seg) {
@@ -243,12 +288,8 @@ __global__ void __launch_bounds__(H::THREADS, 1)
           const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < H::BK / 16; ++kk) {
-            // A: K-major, 128-byte rows, 8-row groups 1024 B apart; a K = 16
-            // slice starts 32 bytes further along the row.
-            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-            // B: N-major, 64-column boxes 8 KB apart (leading offset), 8-k
-            // groups 1024 B apart (stride offset); a K = 16 slice is 16 rows.
-            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * 2048, 64 * H::BK * 2, 1024);
+            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * a_op.step, a_op.lbo, 1024);
+            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * b_op.step, b_op.lbo, 1024);
             tc_mma_f16(d_tmem, a_desc, b_desc, idesc, kb > kb0 || kk != 0);
           }
           mma_issued = true;
@@ -335,13 +376,13 @@ __global__ void __launch_bounds__(H::THREADS, 1)
           if (args.vec_store && col0 + 32 <= N) {
 #pragma unroll
             for (int v = 0; v < 8; ++v)
-              *reinterpret_cast<float4*>(crow + col0 + 4 * v) =
-                  make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
-                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+              epi_store4<kGeneral>(args, crow + col0 + 4 * v,
+                         make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                                     __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (col0 + j < N) crow[col0 + j] = __uint_as_float(r[j]);
+              if (col0 + j < N) epi_store1<kGeneral>(args, crow + col0 + j, __uint_as_float(r[j]));
           }
         }
       }
@@ -381,7 +422,7 @@ __global__ void __launch_bounds__(H::THREADS, 1)
   }
 }
 
-template <int BN, bool kTma, bool kSK>
+template <int BN, bool kTma, bool kSK, bool kGeneral>
 cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
                            const GemmArgs& args, uint32_t idesc, int grid, cudaStream_t stream) {
   static int configured[64] = {0};
@@ -389,23 +430,32 @@ cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(hgemm_tc_kernel<BN, kTma, kSK>,
+    e = cudaFuncSetAttribute(hgemm_tc_kernel<BN, kTma, kSK, kGeneral>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, H::smem_bytes(BN));
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   CUtensorMap dummy{};
-  hgemm_tc_kernel<BN, kTma, kSK><<<grid, H::THREADS, H::smem_bytes(BN), stream>>>(
+  hgemm_tc_kernel<BN, kTma, kSK, kGeneral><<<grid, H::THREADS, H::smem_bytes(BN), stream>>>(
       map_a ? *map_a : dummy, map_b ? *map_b : dummy, args, idesc);
   return cudaGetLastError();
+}
+
+template <int BN, bool kTma, bool kSK>
+cudaError_t launch_epi(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
+                       uint32_t idesc, int grid, cudaStream_t stream) {
+  if (!kTma || args.transa || args.transb || args.epi != kEpiStore)
+    return launch_variant<BN, kTma, kSK, true>(map_a, map_b, args, idesc, grid, stream);
+  return launch_variant<BN, kTma, kSK, kTma ? false : true>(map_a, map_b, args, idesc, grid,
+                                                             stream);
 }
 
 template <int BN, bool kTma>
 cudaError_t launch_bn(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
                       uint32_t idesc, int grid, cudaStream_t stream) {
   if (args.sk.dp_tiles < args.sk.tiles)
-    return launch_variant<BN, kTma, true>(map_a, map_b, args, idesc, grid, stream);
-  return launch_variant<BN, kTma, false>(map_a, map_b, args, idesc, grid, stream);
+    return launch_epi<BN, kTma, true>(map_a, map_b, args, idesc, grid, stream);
+  return launch_epi<BN, kTma, false>(map_a, map_b, args, idesc, grid, stream);
 }
 
 template <bool kTma>

@@ -59,10 +59,16 @@ __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n
   tn = r / gm;
 }
 
+// kGeneral: stored transposes and the alpha / beta epilogue are read from
+// args; without it the kernel is compiled for untransposed operands and a
+// plain store of C (the common case, with nothing decided at run time).
+template <bool kGeneral>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
     hgemm_tc2_kernel(const __grid_constant__ CUtensorMap map_a,
                      const __grid_constant__ CUtensorMap map_b, const GemmArgs args,
                      const uint32_t idesc) {
+  const int transa = kGeneral ? args.transa : 0;
+  const int transb = kGeneral ? args.transb : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = align1024(smem_raw);
   PairSmem& sm = *reinterpret_cast<PairSmem*>(tiles + P::STAGES * P::STAGE_BYTES + P::GUARD_BYTES);
@@ -125,19 +131,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
           uint8_t* b_st = a_st + P::A_BYTES;
           const uint32_t full_leader = mapa_shared(smem_u32(&sm.full[s]), 0);
           if (leader) mbar_arrive_expect_tx(&sm.full[s], 2 * P::STAGE_BYTES);
-          tma_load_2d_pair(a_st, &map_a, kb * P::BK, tm * P::BM + static_cast<int>(rank) * 128,
-                           full_leader);
+          const int m0 = tm * P::BM + static_cast<int>(rank) * 128;
+          const int n0 = tn * P::BN + static_cast<int>(rank) * 128;
+          // A: one box of 64 k x 128 m, or (stored K x M) two of 64 m x 64 k.
+          if (!transa) {
+            tma_load_2d_pair(a_st, &map_a, kb * P::BK, m0, full_leader);
+          } else {
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-            tma_load_2d_pair(b_st + c * (64 * P::BK * 2), &map_b,
-                             tn * P::BN + static_cast<int>(rank) * 128 + c * 64, kb * P::BK,
-                             full_leader);
+            for (int c = 0; c < 2; ++c)
+              tma_load_2d_pair(a_st + c * (64 * P::BK * 2), &map_a, m0 + c * 64, kb * P::BK,
+                               full_leader);
+          }
+          // B: two boxes of 64 n x 64 k, or (stored N x K) one of 64 k x 128 n.
+          if (!transb) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              tma_load_2d_pair(b_st + c * (64 * P::BK * 2), &map_b, n0 + c * 64, kb * P::BK,
+                               full_leader);
+          } else {
+            tma_load_2d_pair(b_st, &map_b, kb * P::BK, n0, full_leader);
+          }
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader)
     if (leader && lane == 0) {
+      const OperandDesc a_op = operand_desc(transa == 0);
+      const OperandDesc b_op = operand_desc(transb != 0);
       bool ok = true;
       uint32_t it = 0;
       int local = 0;
@@ -155,12 +176,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
           const uint32_t b_addr = a_addr + P::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < P::BK / 16; ++kk) {
-            // A (each CTA's 128 rows): K-major, 128-byte rows, 8-row groups
-            // 1024 B apart; a K = 16 slice starts 32 bytes further along.
-            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-            // B (each CTA's 128 columns): N-major, two 64-column boxes 8 KB
-            // apart, 8-k groups 1024 B apart; a K = 16 slice is 16 rows.
-            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * 2048, 64 * P::BK * 2, 1024);
+            // Each CTA's 128 rows of A and 128 columns of B, in the same
+            // layout in both CTAs.
+            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * a_op.step, a_op.lbo, 1024);
+            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * b_op.step, b_op.lbo, 1024);
             tc_mma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0);
           }
           mma_issued = true;
@@ -200,13 +219,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
           if (args.vec_store && col0 + 32 <= N) {
 #pragma unroll
             for (int v = 0; v < 8; ++v)
-              *reinterpret_cast<float4*>(crow + col0 + 4 * v) =
-                  make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
-                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+              epi_store4<kGeneral>(args, crow + col0 + 4 * v,
+                         make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                                     __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (col0 + j < N) crow[col0 + j] = __uint_as_float(r[j]);
+              if (col0 + j < N) epi_store1<kGeneral>(args, crow + col0 + j, __uint_as_float(r[j]));
           }
         }
       }
@@ -248,7 +267,9 @@ int pair_max_clusters() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (have[dev]) return cached[dev];
-  if (cudaFuncSetAttribute(hgemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(hgemm_tc2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           P::SMEM_BYTES) != cudaSuccess ||
+      cudaFuncSetAttribute(hgemm_tc2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            P::SMEM_BYTES) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
@@ -256,7 +277,7 @@ int pair_max_clusters() {
   cfg.blockDim = dim3(P::THREADS, 1, 1);
   cfg.dynamicSmemBytes = P::SMEM_BYTES;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2_kernel, &cfg) != cudaSuccess) n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2_kernel<false>, &cfg) != cudaSuccess) n = 0;
   cached[dev] = n;
   have[dev] = true;
   return n;
@@ -265,8 +286,12 @@ int pair_max_clusters() {
 cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
                                  const GemmArgs& args, uint32_t idesc, int clusters,
                                  cudaStream_t stream) {
-  hgemm_tc2_kernel<<<2 * clusters, P::THREADS, P::SMEM_BYTES, stream>>>(map_a, map_b, args,
-                                                                        idesc);
+  if (args.transa || args.transb || args.epi != kEpiStore)
+    hgemm_tc2_kernel<true><<<2 * clusters, P::THREADS, P::SMEM_BYTES, stream>>>(map_a, map_b,
+                                                                              args, idesc);
+  else
+    hgemm_tc2_kernel<false><<<2 * clusters, P::THREADS, P::SMEM_BYTES, stream>>>(map_a, map_b,
+                                                                               args, idesc);
   return cudaGetLastError();
 }
 

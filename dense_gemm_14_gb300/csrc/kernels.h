@@ -10,8 +10,18 @@
 
 namespace gemm14 {
 
+// How the epilogue writes an output element from its sum s:
+//   kEpiStore  C = s                     (alpha = 1, beta = 0)
+//   kEpiScale  C = alpha * s             (beta = 0: C is not read)
+//   kEpiAccum  C = alpha * s + beta * C  (one fp32 fma on beta * C)
+enum : int { kEpiStore = 0, kEpiScale = 1, kEpiAccum = 2 };
+
 // Arguments shared by every kernel: sizes, operand pointers and the library's
 // device error word (a plain device pointer, see api.cu).
+// Operand storage: op(A) is M x K and op(B) is K x N. transa == 0: A is a
+// row-major M x K matrix (element (i, k) at A[i * lda + k]); transa == 1: A is
+// stored K x M (element (i, k) at A[k * lda + i]). Likewise transb == 0: B is
+// K x N (B[k * ldb + j]); transb == 1: B is stored N x K (B[j * ldb + k]).
 struct GemmArgs {
   int M, N, K;
   const void* A;
@@ -21,6 +31,9 @@ struct GemmArgs {
   float* C;
   int64_t ldc;
   int vec_store;  // C rows may take 16-byte stores (C 16-B aligned, ldc % 4 == 0)
+  int transa, transb;
+  int epi;              // kEpiStore / kEpiScale / kEpiAccum
+  float alpha, beta;
   unsigned* err;
   unsigned long long wait_limit_ns;  // time limit of one mbarrier wait
   int fault;  // kFaultNone, or kFaultSkipFirstStage (failure-detection tests only)
@@ -29,6 +42,30 @@ struct GemmArgs {
   unsigned* flags;     // stream-K: G publication flags (hold the call's epoch)
   unsigned epoch;      // this call's nonzero epoch
 };
+
+// The epilogue's update of one output element, and of four consecutive ones
+// (p 16-byte aligned). kEpiAccum reads C; the others do not. kGeneral false:
+// a plain store, with args.epi not consulted (kernels compiled for the
+// kEpiStore case only).
+template <bool kGeneral>
+__device__ __forceinline__ void epi_store1(const GemmArgs& a, float* p, float s) {
+  if (!kGeneral || a.epi == kEpiStore) *p = s;
+  else if (a.epi == kEpiScale) *p = a.alpha * s;
+  else *p = fmaf(a.alpha, s, a.beta * *p);
+}
+template <bool kGeneral>
+__device__ __forceinline__ void epi_store4(const GemmArgs& a, float* p, float4 v) {
+  float4* q = reinterpret_cast<float4*>(p);
+  if (!kGeneral || a.epi == kEpiStore) {
+    *q = v;
+  } else if (a.epi == kEpiScale) {
+    *q = make_float4(a.alpha * v.x, a.alpha * v.y, a.alpha * v.z, a.alpha * v.w);
+  } else {
+    const float4 c = *q;
+    *q = make_float4(fmaf(a.alpha, v.x, a.beta * c.x), fmaf(a.alpha, v.y, a.beta * c.y),
+                     fmaf(a.alpha, v.z, a.beta * c.z), fmaf(a.alpha, v.w, a.beta * c.w));
+  }
+}
 
 // Stream-K workspace layout on a GPU with `sms` SMs: first one flag word
 // per SM (a region whose place and size never depend on the product, so a
@@ -98,5 +135,10 @@ cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& ma
 // Same kernel with the software loader (operands TMA cannot address).
 cudaError_t launch_hgemm_tc_soft(int bn, const GemmArgs& args, uint32_t idesc, int grid,
                                  cudaStream_t stream);
+
+// ---- C = beta * C over an M x N block (epilogue.cu): the call when the
+// product term vanishes (K == 0 or alpha == 0) and beta is not 0 or 1.
+cudaError_t launch_scale_c(float* C, int64_t ldc, int M, int N, float beta, int sm_count,
+                           cudaStream_t stream);
 
 }  // namespace gemm14

@@ -373,14 +373,32 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 
 // Instruction descriptor for kind::f16 with fp32 accumulation: A and B both
 // fp16 (is_bf16 = false) or both bf16; A K-major, B MN-major; shape M x N.
-__host__ __device__ constexpr uint32_t idesc_f16_f32acc(bool is_bf16, int M, int N) {
+// a_mn / b_mn: the operand is MN-major in shared memory (M or N contiguous)
+// rather than K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32acc(bool is_bf16, int M, int N, bool a_mn,
+                                                        bool b_mn) {
   return (1u << 4)                                  // D format: f32
          | ((is_bf16 ? 1u : 0u) << 7)               // A format
          | ((is_bf16 ? 1u : 0u) << 10)              // B format
-         | (0u << 15)                               // A: K-major
-         | (1u << 16)                               // B: MN-major
+         | ((a_mn ? 1u : 0u) << 15)                 // A major-ness
+         | ((b_mn ? 1u : 0u) << 16)                 // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Shared-memory layout of one 64-deep k-block of a 16-bit operand with the
+// 128-byte swizzle, as the kernels' loaders write it:
+//  K-major:  128-byte rows of 64 k, 8-row groups 1024 B apart (stride
+//            offset); a K = 16 slice starts 32 B further along the rows.
+//  MN-major: boxes of 64 (m or n) x 64 k rows, 8 KB each, boxes 8 KB apart
+//            (leading offset), 8-k groups 1024 B apart; a K = 16 slice starts
+//            16 rows (2048 B) further.
+struct OperandDesc {
+  uint32_t step;  // bytes from one K = 16 slice to the next
+  uint32_t lbo;   // leading byte offset of the descriptor
+};
+__device__ __forceinline__ OperandDesc operand_desc(bool k_major) {
+  return k_major ? OperandDesc{32u, 16u} : OperandDesc{2048u, 8192u};
 }
 
 }  // namespace gemm14

@@ -130,7 +130,7 @@ struct TileGrid {
 };
 
 // Loads of flat iteration j (output tile `tile`, k-block kb) into stage j % STAGES.
-template <bool kTma>
+template <bool kTma, bool kGeneral>
 __device__ __forceinline__ void issue_stage(uint32_t j, int tile, int kb, const TileGrid& grid,
                                             uint8_t* tiles, SgemmSmem& sm,
                                             const CUtensorMap* map_a, const CUtensorMap* map_b,
@@ -154,7 +154,7 @@ __device__ __forceinline__ void issue_stage(uint32_t j, int tile, int kb, const 
     const uint32_t a_sm = smem_u32(a_st);
     const uint32_t b_sm = a_sm + S::A_STAGE_BYTES;
     const int t = threadIdx.x;
-    {
+    if (!(kGeneral && args.transa)) {
       const int kl = t & 31;           // k within the block: a warp reads 128 contiguous bytes
       const int k = kb * S::BK + kl;
       const bool k_ok = k < args.K;
@@ -165,17 +165,36 @@ __device__ __forceinline__ void issue_stage(uint32_t j, int tile, int kb, const 
         cp_async_4(a_sm + a_tile_offset(r, kl),
                    in ? A + static_cast<int64_t>(m) * args.lda + k : A, in ? 4u : 0u);
       }
+    } else {
+      // A stored K x M: 128 threads read 512 contiguous bytes (128 m) of a k
+      // row; the swizzle spreads their 4-byte stores over 8 banks.
+      const int ml = t & (S::BM - 1);
+      const int m = tm * S::BM + ml;
+      const bool m_ok = m < args.M;
+#pragma unroll 4
+      for (int kr = t / S::BM; kr < S::BK; kr += S::THREADS / S::BM) {
+        const int k = kb * S::BK + kr;
+        const bool in = m_ok && k < args.K;
+        cp_async_4(a_sm + a_tile_offset(ml, kr),
+                   in ? A + static_cast<int64_t>(k) * args.lda + m : A, in ? 4u : 0u);
+      }
     }
     {
-      const int nl = t;                // 256 threads = 256 columns of one k row
+      // 256 threads = 256 columns of one k row. B stored N x K: thread n
+      // reads its row's 32 consecutive k (one 128-byte line, kept in L1
+      // across the loop); the shared-memory stores stay conflict-free.
+      const int nl = t;
       const int n = tn * S::BN + nl;
       const bool n_ok = n < args.N;
+      const bool tb = kGeneral && args.transb;
+      const int64_t k_stride = tb ? 1 : args.ldb;
+      const float* b_col = B + (tb ? static_cast<int64_t>(n) * args.ldb : n);
 #pragma unroll 4
       for (int kr = 0; kr < S::BK; ++kr) {
         const int k = kb * S::BK + kr;
         const bool in = n_ok && k < args.K;
         cp_async_4(b_sm + static_cast<uint32_t>(kr * S::BN + nl) * 4,
-                   in ? B + static_cast<int64_t>(k) * args.ldb + n : B, in ? 4u : 0u);
+                   in ? b_col + static_cast<int64_t>(k) * k_stride : B, in ? 4u : 0u);
       }
     }
     cp_async_mbar_arrive_noinc(&sm.full[s]);
@@ -184,8 +203,10 @@ __device__ __forceinline__ void issue_stage(uint32_t j, int tile, int kb, const 
 
 // kSK: the stream-K schedule (segments, workspace partials); without it the
 // schedule is plain data-parallel (tiles w, w+G, ... whole) and none of the
-// stream-K machinery is compiled in.
-template <bool kTma, bool kSK>
+// stream-K machinery is compiled in. kGeneral: stored transposes (cp.async
+// loader) and the alpha / beta epilogue are read from args; without it the
+// kernel is compiled for untransposed operands and a plain store of C.
+template <bool kTma, bool kSK, bool kGeneral>
 __global__ void __launch_bounds__(S::THREADS, 1)
     sgemm_simt_kernel(const __grid_constant__ CUtensorMap map_a,
                       const __grid_constant__ CUtensorMap map_b, const GemmArgs args) {
@@ -235,10 +256,10 @@ __global__ void __launch_bounds__(S::THREADS, 1)
   int dp_tile = w, dp_kb = 0;
   auto load = [&](uint32_t j) {
     if (kSK) {
-      issue_stage<kTma>(j, pcur.tile, pcur.kb, tgrid, tiles, sm, &map_a, &map_b, args);
+      issue_stage<kTma, kGeneral>(j, pcur.tile, pcur.kb, tgrid, tiles, sm, &map_a, &map_b, args);
       pcur.next<true>(sm.sched, G);
     } else {
-      issue_stage<kTma>(j, dp_tile, dp_kb, tgrid, tiles, sm, &map_a, &map_b, args);
+      issue_stage<kTma, kGeneral>(j, dp_tile, dp_kb, tgrid, tiles, sm, &map_a, &map_b, args);
       if (++dp_kb == L) {
         dp_kb = 0;
         dp_tile += G;
@@ -475,12 +496,12 @@ __global__ void __launch_bounds__(S::THREADS, 1)
           if (row >= M) continue;
           float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
           if (args.vec_store && col + 3 < N) {
-            *reinterpret_cast<float4*>(crow + col) = v[u];
+            epi_store4<kGeneral>(args, crow + col, v[u]);
           } else {
-            if (col < N) crow[col] = v[u].x;
-            if (col + 1 < N) crow[col + 1] = v[u].y;
-            if (col + 2 < N) crow[col + 2] = v[u].z;
-            if (col + 3 < N) crow[col + 3] = v[u].w;
+            if (col < N) epi_store1<kGeneral>(args, crow + col, v[u].x);
+            if (col + 1 < N) epi_store1<kGeneral>(args, crow + col + 1, v[u].y);
+            if (col + 2 < N) epi_store1<kGeneral>(args, crow + col + 2, v[u].z);
+            if (col + 3 < N) epi_store1<kGeneral>(args, crow + col + 3, v[u].w);
           }
         }
       }
@@ -510,13 +531,13 @@ __global__ void __launch_bounds__(S::THREADS, 1)
       for (int jj = 0; jj < 4; ++jj) {
         const int col = col0 + 32 * jj;
         if (args.vec_store && col + 3 < N) {
-          *reinterpret_cast<float4*>(crow + col) =
-              make_float4(acc_row[jj * 4 + 0], acc_row[jj * 4 + 1], acc_row[jj * 4 + 2],
-                          acc_row[jj * 4 + 3]);
+          epi_store4<kGeneral>(args, crow + col,
+                     make_float4(acc_row[jj * 4 + 0], acc_row[jj * 4 + 1], acc_row[jj * 4 + 2],
+                                 acc_row[jj * 4 + 3]));
         } else {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            if (col + q < N) crow[col + q] = acc_row[jj * 4 + q];
+            if (col + q < N) epi_store1<kGeneral>(args, crow + col + q, acc_row[jj * 4 + q]);
         }
       }
     }
@@ -539,7 +560,7 @@ __global__ void __launch_bounds__(S::THREADS, 1)
   }
 }
 
-template <bool kTma, bool kSK>
+template <bool kTma, bool kSK, bool kGeneral>
 cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
                            const GemmArgs& args, int grid, cudaStream_t stream) {
   static int configured[64] = {0};
@@ -547,23 +568,31 @@ cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(sgemm_simt_kernel<kTma, kSK>,
+    e = cudaFuncSetAttribute(sgemm_simt_kernel<kTma, kSK, kGeneral>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   CUtensorMap dummy{};
-  sgemm_simt_kernel<kTma, kSK><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(
+  sgemm_simt_kernel<kTma, kSK, kGeneral><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(
       map_a ? *map_a : dummy, map_b ? *map_b : dummy, args);
   return cudaGetLastError();
+}
+
+template <bool kTma, bool kSK>
+cudaError_t launch_epi(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
+                       int grid, cudaStream_t stream) {
+  if (args.transa || args.transb || args.epi != kEpiStore)
+    return launch_variant<kTma, kSK, true>(map_a, map_b, args, grid, stream);
+  return launch_variant<kTma, kSK, false>(map_a, map_b, args, grid, stream);
 }
 
 template <bool kTma>
 cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
                    int grid, cudaStream_t stream) {
   if (args.sk.dp_tiles < args.sk.tiles)
-    return launch_variant<kTma, true>(map_a, map_b, args, grid, stream);
-  return launch_variant<kTma, false>(map_a, map_b, args, grid, stream);
+    return launch_epi<kTma, true>(map_a, map_b, args, grid, stream);
+  return launch_epi<kTma, false>(map_a, map_b, args, grid, stream);
 }
 
 }  // namespace

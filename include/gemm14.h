@@ -12,8 +12,8 @@
  * Layout: A, B and C are row-major. Element (i, k) of A is A[i * lda + k];
  * (k, j) of B is B[k * ldb + j]; (i, j) of C is C[i * ldc + j]. Leading
  * dimensions are counted in elements: lda >= K, ldb >= N, ldc >= N (each at
- * least 1). C is overwritten (no alpha/beta); A and B are only read. C must
- * not overlap A or B.
+ * least 1). C is overwritten (alpha, beta and stored transposes: see
+ * gemm14_gemm_ex); A and B are only read. C must not overlap A or B.
  *
  * Pointers are DEVICE pointers in the current CUDA device's address space
  * (e.g. torch CUDA tensors' data_ptr()). `stream` is a cudaStream_t (NULL =
@@ -147,6 +147,41 @@ int gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int
                              const void* B, int64_t ldb, float* C, int64_t ldc, void* stream);
 
 /*
+ * The extended product, for all three element types (dtype = GEMM14_DTYPE_*):
+ *     C = alpha * op(A) * op(B) + beta * C,
+ * op(A) an M x K matrix and op(B) a K x N matrix. It generalises the
+ * accumulate form of the pages' asynchronous tensor-core MMA (gpu-hpc-book
+ * ch.06 "高级 cuda 特性 —— 从矩阵乘法(gemm)说起", "Tensor Cores" / "wgmma":
+ * D = A * B + D with either operand optionally transposed and D scaled by
+ * 0 or 1) to any fp32 alpha and beta.
+ * Storage (row-major throughout):
+ *   transa = 0: A is stored M x K, op(A)[i][k] = A[i * lda + k], lda >= K;
+ *   transa = 1: A is stored K x M, op(A)[i][k] = A[k * lda + i], lda >= M;
+ *   transb = 0: B is stored K x N, op(B)[k][j] = B[k * ldb + j], ldb >= N;
+ *   transb = 1: B is stored N x K, op(B)[k][j] = B[j * ldb + k], ldb >= K;
+ *   C is M x N, C[i * ldc + j], ldc >= N. Any other transa / transb value is
+ *   GEMM14_ERR_INVALID_ARG.
+ * Arithmetic: the sum over k is formed exactly as by gemm_f32 /
+ * gemm_bf16_f32acc / gemm_f16_f32acc (bit-identical for alpha = 1,
+ * beta = 0); then each element is written as alpha * sum (beta == 0) or as
+ * fmaf(alpha, sum, beta * C) in fp32.
+ * beta == 0: C is not read (NaN or infinity in C does not propagate).
+ * K == 0 or alpha == 0: A and B are not read; C becomes beta * C (beta == 1
+ * launches nothing, beta == 0 zeroes C).
+ * Loaders: 16-bit operands take TMA under the same alignment rules as
+ * gemm_bf16_f32acc in either storage; fp32 operands take TMA only when
+ * neither is transposed, and the equivalent cp.async loader otherwise.
+ * workspace / workspace_bytes: as for the *_ws calls (NULL, 0 allowed); the
+ * bytes needed do not depend on transa / transb, so
+ * gemm14_workspace_bytes(dtype, M, N, K, ...) applies.
+ * Other rules (device pointers, stream, errors, degenerate sizes) as above.
+ */
+int gemm14_gemm_ex(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
+                   float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                   float beta, float* C, int64_t ldc, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/*
  * Workspace bytes that let the *_ws call of this dtype and shape use the
  * stream-K schedule on a GPU with sm_count SMs (sm_count <= 0: the current
  * device's). 0 means the call would not split tiles (whole waves, between
@@ -193,6 +228,11 @@ typedef struct gemm14_plan {
 int gemm14_plan_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                      const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
                      gemm14_plan* plan);
+
+/* As gemm14_plan_gemm for a gemm14_gemm_ex call with these transposes. */
+int gemm14_plan_gemm_ex(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
+                        const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
+                        int64_t ldc, int sm_count, gemm14_plan* plan);
 
 /*
  * The 16-bit entry points compute 256 x 256 output tiles on pairs of SMs

@@ -92,3 +92,67 @@ def make_workspace(dtype: str, M: int, N: int, K: int) -> torch.Tensor:
             "f16": g14.GEMM14_DTYPE_F16}[dtype]
     n = g14.workspace_bytes(code, M, N, K, 0)
     return torch.zeros(max(n, 256), dtype=torch.uint8, device="cuda")
+
+
+DTYPE_CODE = {"f32": g14.GEMM14_DTYPE_F32, "bf16": g14.GEMM14_DTYPE_BF16,
+              "f16": g14.GEMM14_DTYPE_F16}
+
+
+def stored(X: torch.Tensor, trans: int) -> torch.Tensor:
+    """The matrix as the library reads it: X itself, or X^T stored row-major."""
+    return X.t().contiguous() if trans else X
+
+
+def run_ex(A: torch.Tensor, B: torch.Tensor, transa=0, transb=0, alpha=1.0, beta=0.0,
+           C0: torch.Tensor | None = None, lda=None, ldb=None, ldc=None, a_off=0, b_off=0,
+           c_off=0, workspace=None, stream=None, check_err=True):
+    """C = alpha * A @ B + beta * C0 through gemm14_gemm_ex, with A (M x K) and
+    B (K x N) stored transposed when transa / transb. C0 None: C starts as NaN
+    (which beta == 0 must ignore). Returns C (CPU fp32)."""
+    M, K = A.shape
+    _, N = B.shape
+    As, Bs = stored(A, transa), stored(B, transb)
+    lda = lda or max(As.shape[1], 1)
+    ldb = ldb or max(Bs.shape[1], 1)
+    ldc = ldc or max(N, 1)
+    _abuf, a = to_device_padded(As, lda, a_off)
+    _bbuf, b = to_device_padded(Bs, ldb, b_off)
+    cbuf = torch.full((c_off + max(M, 1) * ldc + 16,), float("nan"), dtype=torch.float32,
+                      device="cuda")
+    if C0 is not None and M:
+        cbuf[c_off:c_off + M * ldc].view(M, ldc)[:, :N].copy_(C0.to("cuda"))
+    c_ptr = cbuf.data_ptr() + 4 * c_off
+    s = stream if stream is not None else torch.cuda.current_stream()
+    g14.gemm_ex(DTYPE_CODE[dtype_name(A)], transa, transb, M, N, K, alpha,
+                a.data_ptr() if As.numel() else 0, lda, b.data_ptr() if Bs.numel() else 0, ldb,
+                beta, c_ptr, ldc, workspace.data_ptr() if workspace is not None else None,
+                workspace.numel() if workspace is not None else 0, s.cuda_stream)
+    if check_err:
+        st = g14.check_device_error(s.cuda_stream)
+        assert st == 0, g14.status_string(st)
+    torch.cuda.synchronize()
+    if M == 0:
+        return torch.empty((0, N))
+    return cbuf[c_off:c_off + M * ldc].view(M, ldc)[:, :N].cpu()
+
+
+def oracle_check_ex(oracle_mod, A, B, C, transa=0, transb=0, alpha=1.0, beta=0.0, C0=None):
+    """Element-wise comparison with the oracle's extended product, which reads
+    the same stored (possibly transposed) matrices."""
+    dt = dtype_name(A)
+    As = inputs.host_view(stored(A, transa))
+    Bs = inputs.host_view(stored(B, transb))
+    c0 = C0.numpy().astype(np.float32) if C0 is not None else None
+    ref, refabs = oracle_mod.gemm_ex(As, Bs, dt, bool(transa), bool(transb), float(alpha),
+                                     float(beta), c0)
+    Cg = C.numpy()
+    ok, worst = oracle_mod.within_bound(Cg, ref, refabs, TOL[dt])
+    if not ok:
+        diff = np.abs(Cg.astype(np.float64) - ref) - TOL[dt] * refabs
+        bad = np.argwhere(~(diff <= 0))
+        i, j = bad[0]
+        raise AssertionError(
+            f"{dt} op(A) {tuple(A.shape)} op(B) {tuple(B.shape)} ta={transa} tb={transb} "
+            f"alpha={alpha} beta={beta}: {len(bad)} elements out of bound; first at ({i},{j}) "
+            f"gpu={Cg[i, j]!r} ref={ref[i, j]!r} abs={refabs[i, j]!r}; worst={worst:.3g}")
+    return worst

@@ -156,3 +156,59 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         _lib.load()
+
+
+# ----------------------------------------------------------------- the extended call
+
+def _ex(dtype, ta, tb, M, N, K, A, lda, B, ldb, C, ldc, alpha=1.0, beta=0.0):
+    return g14.gemm_ex(dtype, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, None, 0,
+                       None, check=False)
+
+
+@pytest.mark.parametrize("dtype", [F32, BF16, F16])
+def test_ex_leading_dimensions_follow_storage(lib, dtype):
+    """lda >= K when A is stored M x K, >= M when stored K x M; likewise ldb."""
+    M, N, K = 8, 16, 24
+    bad = _lib.GEMM14_ERR_INVALID_ARG
+    st, _ = g14.plan_ex(dtype, 1, 0, M, N, K, P, M, P, N, P, N, 152)
+    assert st == 0
+    st, _ = g14.plan_ex(dtype, 1, 0, M, N, K, P, M - 1, P, N, P, N, 152)
+    assert st == bad
+    st, _ = g14.plan_ex(dtype, 0, 1, M, N, K, P, K, P, K, P, N, 152)
+    assert st == 0
+    st, _ = g14.plan_ex(dtype, 0, 1, M, N, K, P, K, P, K - 1, P, N, 152)
+    assert st == bad
+    st, _ = g14.plan_ex(dtype, 0, 0, M, N, K, P, K, P, N - 1, P, N, 152)
+    assert st == bad
+    st, _ = g14.plan_ex(dtype, 0, 0, M, N, K, P, K - 1, P, N, P, N, 152)
+    assert st == bad
+
+
+@pytest.mark.parametrize("ta,tb", [(2, 0), (0, 2), (-1, 0), (0, -1)])
+def test_ex_invalid_transpose_flags(lib, ta, tb):
+    assert _ex(F32, ta, tb, 4, 4, 4, P, 4, P, 4, P, 4) == _lib.GEMM14_ERR_INVALID_ARG
+    st, _ = g14.plan_ex(F32, ta, tb, 4, 4, 4, P, 4, P, 4, P, 4, 152)
+    assert st == _lib.GEMM14_ERR_INVALID_ARG
+
+
+def test_ex_plan_loaders(lib):
+    """fp32: stored transposes take the cp.async loader (same tiles); 16-bit:
+    TMA in every storage, pairs included."""
+    st, nn = g14.plan_ex(F32, 0, 0, 512, 512, 512, P, 512, P, 512, P, 512, 152)
+    assert st == 0 and nn.loader == 1
+    for ta, tb in ((1, 0), (0, 1), (1, 1)):
+        st, p = g14.plan_ex(F32, ta, tb, 512, 512, 512, P, 512, P, 512, P, 512, 152)
+        assert st == 0 and p.loader == 2 and p.tiles == nn.tiles and p.grid == nn.grid
+        st, p = g14.plan_ex(BF16, ta, tb, 512, 512, 512, P, 512, P, 512, P, 512, 152)
+        assert st == 0 and p.loader == 1 and p.kernel == 3
+        st, p = g14.plan_ex(F16, ta, tb, 100, 512, 512, P, 512, P, 512, P, 512, 152)
+        assert st == 0 and p.loader == 1 and p.kernel == 2
+    # the plain planner is the extended one without transposes
+    st, p0 = g14.plan(BF16, 300, 700, 200, P, 200, P, 704, P, 700, 152)
+    st1, p1 = g14.plan_ex(BF16, 0, 0, 300, 700, 200, P, 200, P, 704, P, 700, 152)
+    assert st == st1 == 0 and p0 == p1
+
+
+def test_ex_empty_product_is_a_no_op(lib):
+    assert _ex(BF16, 1, 1, 0, 4, 4, 0, 1, 0, 4, 0, 4, 2.0, 3.0) == 0
+    assert _ex(F32, 0, 1, 4, 0, 4, 0, 4, 0, 4, 0, 1, 2.0, 3.0) == 0
