@@ -66,6 +66,9 @@ def parse_args():
     ap.add_argument("--table", action="store_true",
                     help="time every named workload alone and print one JSON line per workload "
                          "(the parity workloads' speeds; not the bench line)")
+    ap.add_argument("--table-ex", action="store_true",
+                    help="time the extended call (stored transposes, alpha/beta) on the fp32 "
+                         "3072^3 and 16-bit 8192^3 workloads, one JSON line per variant")
     return ap.parse_args()
 
 
@@ -502,10 +505,83 @@ def time_one(args, name, w, fl, ib, sets, nsets, stream, peaks, roofline, g14, s
                       "frac_hbm": gbs / peaks["hbm_gbs"]}), flush=True)
 
 
+# (transa, transb, alpha, beta) variants of the extended call
+EX_VARIANTS = [(0, 0, 1.0, 0.0), (1, 0, 1.0, 0.0), (0, 1, 1.0, 0.0), (1, 1, 1.0, 0.0),
+               (0, 0, -1.5, 0.0), (0, 0, -1.5, 0.5)]
+
+
+def run_table_ex(args):
+    """gemm14_gemm_ex timed alone per variant: the operands stored as the
+    variant says (transposed copies made before timing), C read too when
+    beta != 0 (its bytes added to the algorithmic traffic). Operand copies
+    rotate over > 2x L2; the workspace entry (stream-K where it applies)."""
+    import torch
+
+    import dense_gemm_14_gb300 as g14
+    from dense_gemm_14_gb300 import inputs, roofline
+
+    g14.load()
+    peaks = roofline.measured_peaks()
+    code = {"f32": g14.GEMM14_DTYPE_F32, "bf16": g14.GEMM14_DTYPE_BF16,
+            "f16": g14.GEMM14_DTYPE_F16}
+    stream = torch.cuda.current_stream()
+    for name in ("f32_3072", "bf16_8192", "f16_8192"):
+        w, fl, ib = workload_info(name)
+        A, B = inputs.make_workload(name)
+        ws_bytes = g14.workspace_bytes(code[w.dtype], w.M, w.N, w.K, 0)
+        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+        for ta, tb, alpha, beta in EX_VARIANTS:
+            As = (A.t().contiguous() if ta else A).cuda()
+            Bs = (B.t().contiguous() if tb else B).cuda()
+            per_set = As.numel() * As.element_size() + Bs.numel() * Bs.element_size() + w.M * w.N * 4
+            nsets = max(2, -(-2 * L2_BYTES // per_set))
+            sets = [(As.clone(), Bs.clone(), torch.zeros(w.M, w.N, device="cuda"))
+                    for _ in range(nsets)]
+            lda, ldb = As.shape[1], Bs.shape[1]
+
+            def launch(i):
+                a, b, c = sets[i % nsets]
+                g14.gemm_ex(code[w.dtype], ta, tb, w.M, w.N, w.K, alpha, a.data_ptr(), lda,
+                            b.data_ptr(), ldb, beta, c.data_ptr(), w.N, ws.data_ptr(), ws_bytes,
+                            stream.cuda_stream)
+
+            for i in range(args.warmup):
+                launch(i)
+            reps = max(args.steps, 5)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            for i, (e0, e1) in enumerate(evs):
+                e0.record(stream)
+                launch(i)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            if g14.check_device_error(stream.cuda_stream):
+                raise RuntimeError(f"device error in {name}")
+            ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+            mean = statistics.mean(ms)
+            tf = fl / (mean / 1e3) / 1e12
+            if w.dtype == "f32":
+                peak, kind = roofline.fp32_alu_peak_tflops(), "alu"
+            else:
+                peak, kind = peaks["bf16_tflops"], "tensor"
+            nbytes = ib + (w.M * w.N * 4 if beta != 0.0 else 0)
+            gbs = nbytes / (mean / 1e3) / 1e9
+            print(json.dumps({"workload": name, "transa": ta, "transb": tb, "alpha": alpha,
+                              "beta": beta, "ms_mean": mean, "ms_min": min(ms), "tflops": tf,
+                              "bound": kind, "peak_tflops": peak, "frac_compute": tf / peak,
+                              "algorithmic_bytes": nbytes, "gbs": gbs,
+                              "frac_hbm": gbs / peaks["hbm_gbs"]}), flush=True)
+            del sets, As, Bs
+            torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
     if args.table:
         run_table(args)
+        return
+    if args.table_ex:
+        run_table_ex(args)
         return
     dist = Dist(args.gpus)
     try:
