@@ -66,6 +66,12 @@ def parse_args():
     ap.add_argument("--table", action="store_true",
                     help="time every named workload alone and print one JSON line per workload "
                          "(the parity workloads' speeds; not the bench line)")
+    ap.add_argument("--table-tf32", action="store_true",
+                    help="time fp32 inputs in every arithmetic (FFMA, TF32, 3xTF32) at 3072^3 "
+                         "and 8192^3, one JSON line each")
+    ap.add_argument("--tf32-only", default=None, metavar="SHAPE:MODE",
+                    help="with --table-tf32: one shape (f32_3072 or f32_8192) and one mode "
+                         "(fp32, tf32 or 3xtf32), e.g. f32_3072:3xtf32 (for profiling)")
     ap.add_argument("--table-ex", action="store_true",
                     help="time the extended call (stored transposes, alpha/beta) on the fp32 "
                          "3072^3 and 16-bit 8192^3 workloads, one JSON line per variant")
@@ -575,8 +581,85 @@ def run_table_ex(args):
             torch.cuda.empty_cache()
 
 
+def run_table_tf32(args):
+    """fp32 inputs timed alone in each arithmetic: gemm_f32 (FFMA, workspace
+    entry), gemm_tf32_f32acc and gemm_f32_3xtf32 (tensor cores), at the 3072^3
+    workload and at an 8192^3 product of the same distribution (U[-1,1), seed
+    14007). Operand copies rotate over > 2x L2."""
+    import torch
+
+    import dense_gemm_14_gb300 as g14
+    from dense_gemm_14_gb300 import inputs, roofline
+
+    g14.load()
+    peaks = roofline.measured_peaks()
+    stream = torch.cuda.current_stream()
+    shapes = [("f32_3072", None), ("f32_8192", (8192, 8192, 8192, 14007))]
+    modes = [("fp32 FFMA", g14.GEMM14_DTYPE_F32), ("tf32", g14.GEMM14_DTYPE_TF32),
+             ("3xtf32", g14.GEMM14_DTYPE_F32_3XTF32)]
+    if args.tf32_only:
+        only_shape, only_mode = args.tf32_only.split(":")
+        shapes = [sh for sh in shapes if sh[0] == only_shape]
+        modes = [m for m in modes if m[0].split()[0] == only_mode]
+    for name, spec in shapes:
+        if spec is None:
+            w = inputs.WORKLOADS[name]
+            M, N, K = w.M, w.N, w.K
+            A, B = inputs.make_workload(name)
+        else:
+            M, N, K, seed = spec
+            A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=seed)
+        fl = roofline.flops(M, N, K)
+        ib = roofline.ideal_bytes(M, N, K, 4, 4)
+        per_set = (M * K + K * N + M * N) * 4
+        nsets = max(2, -(-2 * L2_BYTES // per_set))
+        sets = [(A.cuda(), B.cuda(), torch.empty(M, N, device="cuda")) for _ in range(nsets)]
+        ws_bytes = g14.workspace_bytes(g14.GEMM14_DTYPE_F32, M, N, K, 0)
+        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+        for mode, code in modes:
+            def launch(i):
+                a, b, c = sets[i % nsets]
+                g14.gemm_ex(code, 0, 0, M, N, K, 1.0, a.data_ptr(), K, b.data_ptr(), N, 0.0,
+                            c.data_ptr(), N, ws.data_ptr(), ws_bytes, stream.cuda_stream)
+
+            for i in range(args.warmup):
+                launch(i)
+            reps = max(args.steps, 5)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            for i, (e0, e1) in enumerate(evs):
+                e0.record(stream)
+                launch(i)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            if g14.check_device_error(stream.cuda_stream):
+                raise RuntimeError(f"device error in {name} {mode}")
+            ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+            mean = statistics.mean(ms)
+            tf = fl / (mean / 1e3) / 1e12
+            mma_flops = fl * (3 if code == g14.GEMM14_DTYPE_F32_3XTF32 else 1)
+            if code == g14.GEMM14_DTYPE_F32:
+                peak, kind = roofline.fp32_alu_peak_tflops(), "alu"
+            else:
+                # tf32 dense peak: the measured bf16 burst figure x the nominal
+                # tf32 / bf16 ratio (1.1 / 2.25 PFLOP/s)
+                peak, kind = peaks["bf16_tflops"] * 1.1 / 2.25, "tensor (tf32)"
+            print(json.dumps({"workload": name, "mode": mode, "M": M, "N": N, "K": K,
+                              "ms_mean": mean, "ms_min": min(ms), "tflops": tf,
+                              "mma_tflops": mma_flops / (mean / 1e3) / 1e12, "bound": kind,
+                              "peak_tflops": peak,
+                              "frac_compute": mma_flops / (mean / 1e3) / 1e12 / peak,
+                              "vs_ffma_peak": tf / roofline.fp32_alu_peak_tflops(),
+                              "gbs": ib / (mean / 1e3) / 1e9}), flush=True)
+        del sets
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
+    if args.table_tf32:
+        run_table_tf32(args)
+        return
     if args.table:
         run_table(args)
         return

@@ -19,6 +19,8 @@ GEMM14_ERR_TIMEOUT = 4
 GEMM14_DTYPE_F32 = 0
 GEMM14_DTYPE_BF16 = 1
 GEMM14_DTYPE_F16 = 2
+GEMM14_DTYPE_TF32 = 3
+GEMM14_DTYPE_F32_3XTF32 = 4
 
 # Every function the header declares, with (restype, argtypes).
 _i64, _vp, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
@@ -35,6 +37,8 @@ SIGNATURES = {
     "gemm_f32": (_int, _GEMM_ARGS),
     "gemm_bf16_f32acc": (_int, _GEMM_ARGS),
     "gemm_f16_f32acc": (_int, _GEMM_ARGS),
+    "gemm_tf32_f32acc": (_int, _GEMM_ARGS),
+    "gemm_f32_3xtf32": (_int, _GEMM_ARGS),
     "gemm14_status_string": (ctypes.c_char_p, [_int]),
     "gemm14_last_error_string": (ctypes.c_char_p, []),
     "gemm14_check_device_error": (_int, [_vp]),
@@ -123,6 +127,23 @@ def gemm_f16_f32acc(M, N, K, A, lda, B, ldb, C, ldc, stream=None, check=True) ->
     st = _call("gemm_f16_f32acc", M, N, K, A, lda, B, ldb, C, ldc, stream)
     if check and st:
         raise Gemm14Error(st, "gemm_f16_f32acc")
+    return st
+
+
+def gemm_tf32_f32acc(M, N, K, A, lda, B, ldb, C, ldc, stream=None, check=True) -> int:
+    """C ABI gemm_tf32_f32acc: fp32 inputs rounded to tf32 on the tensor cores."""
+    st = _call("gemm_tf32_f32acc", M, N, K, A, lda, B, ldb, C, ldc, stream)
+    if check and st:
+        raise Gemm14Error(st, "gemm_tf32_f32acc")
+    return st
+
+
+def gemm_f32_3xtf32(M, N, K, A, lda, B, ldb, C, ldc, stream=None, check=True) -> int:
+    """C ABI gemm_f32_3xtf32: fp32 inputs, split tf32 arithmetic on the tensor
+    cores within the fp32 bound."""
+    st = _call("gemm_f32_3xtf32", M, N, K, A, lda, B, ldb, C, ldc, stream)
+    if check and st:
+        raise Gemm14Error(st, "gemm_f32_3xtf32")
     return st
 
 

@@ -48,8 +48,12 @@ def _operand(x: torch.Tensor, name: str) -> tuple[int, int]:
     raise ValueError(f"{name} needs unit stride along its rows or its columns, got {x.stride()}")
 
 
+_FP32_MODES = {None: _lib.GEMM14_DTYPE_F32, "fp32": _lib.GEMM14_DTYPE_F32,
+               "tf32": _lib.GEMM14_DTYPE_TF32, "3xtf32": _lib.GEMM14_DTYPE_F32_3XTF32}
+
+
 def gemm_into(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor, alpha: float = 1.0,
-              beta: float = 0.0, stream=None) -> torch.Tensor:
+              beta: float = 0.0, stream=None, fp32_mode: str | None = None) -> torch.Tensor:
     """out = alpha * a @ b + beta * out on the GPU through the C ABI
     (gemm14_gemm_ex); a, b, out are CUDA tensors.
 
@@ -58,7 +62,8 @@ def gemm_into(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor, alpha: float 
     becomes the call's transa / transb; out: (M, N) float32, row-major. With
     beta == 0, out is not read. Uses a stream-K workspace cached per (device,
     stream) when the product benefits from it. Runs on `stream` (default:
-    torch's current stream) without synchronising.
+    torch's current stream) without synchronising. fp32_mode (float32 inputs
+    only): "fp32" (default, FFMA), "tf32" or "3xtf32" (tensor cores).
     """
     if a.dtype != b.dtype or a.dtype not in _CODE:
         raise TypeError(f"unsupported dtypes {a.dtype}, {b.dtype}")
@@ -78,10 +83,13 @@ def gemm_into(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor, alpha: float 
         stream = torch.cuda.current_stream(a.device).cuda_stream
     elif isinstance(stream, torch.cuda.Stream):
         stream = stream.cuda_stream
+    if fp32_mode not in _FP32_MODES or (fp32_mode not in (None, "fp32") and a.dtype != torch.float32):
+        raise ValueError(f"fp32_mode {fp32_mode!r} needs float32 inputs and one of {list(_FP32_MODES)}")
+    code = _FP32_MODES[fp32_mode] if a.dtype == torch.float32 else _CODE[a.dtype]
     with torch.cuda.device(a.device):
-        nbytes = _lib.workspace_bytes(_CODE[a.dtype], M, N, K, 0) if M and N and K else 0
+        nbytes = _lib.workspace_bytes(code, M, N, K, 0) if M and N and K else 0
         ws = _workspace(a.device, int(stream or 0), nbytes) if nbytes else None
-        _lib.gemm_ex(_CODE[a.dtype], ta, tb, M, N, K, float(alpha), a.data_ptr(), lda,
+        _lib.gemm_ex(code, ta, tb, M, N, K, float(alpha), a.data_ptr(), lda,
                      b.data_ptr(), ldb, float(beta), out.data_ptr(), max(out.stride(0), N, 1),
                      ws.data_ptr() if ws is not None else None, nbytes, stream)
     return out

@@ -146,14 +146,20 @@ int make_map(CUtensorMap* map, CUtensorMapDataType type, int elem_bytes, const v
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int elem_bytes_of(int dtype) { return dtype == GEMM14_DTYPE_F32 ? 4 : 2; }
+bool is_tf32_mode(int dtype) {
+  return dtype == GEMM14_DTYPE_TF32 || dtype == GEMM14_DTYPE_F32_3XTF32;
+}
+int elem_bytes_of(int dtype) {
+  return dtype == GEMM14_DTYPE_F32 || is_tf32_mode(dtype) ? 4 : 2;
+}
 
 // Argument validation shared by the entry points and the planner. transa /
 // transb select the stored shape of A (M x K, or K x M) and of B (K x N, or
 // N x K); each must be 0 or 1.
 int validate(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K, const void* A,
              int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc) {
-  if (dtype != GEMM14_DTYPE_F32 && dtype != GEMM14_DTYPE_BF16 && dtype != GEMM14_DTYPE_F16)
+  if (dtype != GEMM14_DTYPE_F32 && dtype != GEMM14_DTYPE_BF16 && dtype != GEMM14_DTYPE_F16 &&
+      !is_tf32_mode(dtype))
     return GEMM14_ERR_INVALID_ARG;
   if ((transa != 0 && transa != 1) || (transb != 0 && transb != 1)) return GEMM14_ERR_INVALID_ARG;
   const int64_t kMax = INT32_MAX;
@@ -187,6 +193,27 @@ void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K
   std::memset(p, 0, sizeof *p);
   if (M == 0 || N == 0 || K == 0) return;  // nothing launched (K == 0: a memset)
   p->vec_store = aligned(C, 16) && (ldc % 4 == 0);
+  if (is_tf32_mode(dtype)) {
+    // fp32 inputs on the tensor cores: TMA-addressable operands on CTA pairs;
+    // anything else on the fp32 SIMT kernel (exact fp32 products, so at least
+    // as accurate as either tensor-core mode).
+    if (aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 && ldb % 4 == 0 && sm_count >= 2) {
+      using T = Tf32Shape;
+      p->kernel = 4;
+      p->loader = 1;
+      p->bm = T::BM;
+      p->bn = T::BN;
+      p->bk = T::BK;
+      p->stages = T::OP_STAGES;
+      p->threads = T::THREADS;
+      p->smem_bytes = T::SMEM_BYTES;
+      p->tiles = ((M + T::BM - 1) / T::BM) * ((N + T::BN - 1) / T::BN);
+      const int64_t clusters = sm_count / 2;
+      p->grid = static_cast<int>(2 * (p->tiles < clusters ? p->tiles : clusters));
+      return;
+    }
+    dtype = GEMM14_DTYPE_F32;
+  }
   if (dtype == GEMM14_DTYPE_F32) {
     using S = SgemmShape;
     p->kernel = 1;
@@ -343,6 +370,34 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
                 dev->err_word, wait_limit_ns, fault, StreamK{}, nullptr, nullptr, 0u};
   int grid = plan.grid;
 
+  if (plan.kernel == 4) {
+    const int clusters_max = tf32_pair_max_clusters();
+    if (clusters_max > 0) {
+      CUtensorMap ma, mb;
+      const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+      st = transa ? make_map(&ma, f32, 4, A, K, M, lda, 128, Tf32Shape::BK,
+                             CU_TENSOR_MAP_SWIZZLE_NONE)
+                  : make_map(&ma, f32, 4, A, M, K, lda, Tf32Shape::BK, 128,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+      if (st != GEMM14_OK) return st;
+      st = transb ? make_map(&mb, f32, 4, B, N, K, ldb, Tf32Shape::BK, 128,
+                             CU_TENSOR_MAP_SWIZZLE_128B)
+                  : make_map(&mb, f32, 4, B, K, N, ldb, 128, Tf32Shape::BK,
+                             CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (st != GEMM14_OK) return st;
+      const int64_t clusters = plan.tiles < clusters_max ? plan.tiles : clusters_max;
+      const int terms = dtype == GEMM14_DTYPE_F32_3XTF32 ? 3 : 1;
+      return finish(launch_sgemm_tf32_pair(ma, mb, args, terms, static_cast<int>(clusters), stream),
+                    "tf32 pair launch", stream);
+    }
+    // clusters of the tf32 kernel do not fit: the fp32 SIMT kernel
+    dtype = GEMM14_DTYPE_F32;
+    plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+    args.vec_store = plan.vec_store;
+    grid = plan.grid;
+  }
+  if (is_tf32_mode(dtype)) dtype = GEMM14_DTYPE_F32;  // planned on the SIMT kernel
+
   if (dtype == GEMM14_DTYPE_F32) {
     schedule(plan, K, dev->sm_count, workspace, workspace_bytes, args, grid);
     if (plan.loader == 2)
@@ -442,6 +497,16 @@ int gemm_f16_f32acc_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t l
                        size_t workspace_bytes, void* stream) {
   return run_gemm(GEMM14_DTYPE_F16, M, N, K, A, lda, B, ldb, C, ldc, workspace, workspace_bytes,
                   stream);
+}
+
+int gemm_tf32_f32acc(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                     const float* B, int64_t ldb, float* C, int64_t ldc, void* stream) {
+  return run_gemm(GEMM14_DTYPE_TF32, M, N, K, A, lda, B, ldb, C, ldc, nullptr, 0, stream);
+}
+
+int gemm_f32_3xtf32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                    const float* B, int64_t ldb, float* C, int64_t ldc, void* stream) {
+  return run_gemm(GEMM14_DTYPE_F32_3XTF32, M, N, K, A, lda, B, ldb, C, ldc, nullptr, 0, stream);
 }
 
 int gemm14_gemm_ex(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,

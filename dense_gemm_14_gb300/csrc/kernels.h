@@ -136,6 +136,32 @@ cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& ma
 cudaError_t launch_hgemm_tc_soft(int bn, const GemmArgs& args, uint32_t idesc, int grid,
                                  cudaStream_t stream);
 
+// ---- fp32 inputs on the tensor cores (sgemm_tc3.cu): tcgen05 kind::tf32 on
+// CTA pairs, 256 x 256 tiles. Each fp32 input x is split into hi = tf32(x)
+// and lo = x - hi by converter warps; terms = 1 computes hi(A) hi(B) (TF32
+// precision), terms = 3 adds hi(A) lo(B) + lo(A) hi(B) ("3xTF32").
+struct Tf32Shape {
+  static constexpr int BM = 256, BN = 256, BK = 32;  // k-block: 32 fp32 = one 128-byte row
+  static constexpr int RAW_STAGES = 3, OP_STAGES = 2;
+  static constexpr int THREADS = 10 * 32;  // producer, MMA, 4 epilogue, 4 converter warps
+  static constexpr int RAW_TILE = 128 * BK * 4;   // one CTA's fp32 A rows or B columns: 16 KB
+  static constexpr int RAW_STAGE = 2 * RAW_TILE;  // A, B as loaded
+  static constexpr int OP_TILE = 128 * BK * 4;    // one K-major tf32 operand tile: 16 KB
+  static constexpr int OP_STAGE = 4 * OP_TILE;    // A hi, A lo, B hi, B lo
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int SMEM_BYTES = RAW_STAGES * RAW_STAGE + OP_STAGES * OP_STAGE + 512 + 1024;
+};
+
+// Clusters of two the tf32 kernel fits at once on the current device (0: it
+// cannot run). The first call per device also sets the kernels' smem limit.
+int tf32_pair_max_clusters();
+// map_a / map_b: A stored M x K: box 32 k x 128 m, 128-byte swizzle; stored
+// K x M (transa): box 128 m x 32 k, no swizzle. B stored K x N: box 128 n x
+// 32 k, no swizzle; stored N x K (transb): box 32 k x 128 n, 128-byte swizzle.
+cudaError_t launch_sgemm_tf32_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                                   const GemmArgs& args, int terms, int clusters,
+                                   cudaStream_t stream);
+
 // ---- C = beta * C over an M x N block (epilogue.cu): the call when the
 // product term vanishes (K == 0 or alpha == 0) and beta is not 0 or 1.
 cudaError_t launch_scale_c(float* C, int64_t ldc, int M, int N, float beta, int sm_count,

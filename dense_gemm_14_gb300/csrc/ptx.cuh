@@ -298,6 +298,18 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
       : "memory");
 }
+// The same pair MMA with tf32 operands (fp32 bit patterns in shared memory,
+// K = 8 per instruction), fp32 accumulation.
+__device__ __forceinline__ void tc_mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
 // Arrives once on the barrier at this shared offset in every CTA of cta_mask
 // when the pair MMAs issued so far by this thread have completed.
 __device__ __forceinline__ void tc_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {
@@ -384,6 +396,24 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32acc(bool is_bf16, int M, int
          | ((b_mn ? 1u : 0u) << 16)                 // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor for kind::tf32 with fp32 accumulation, both
+// operands K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32acc(int M, int N) {
+  return (1u << 4)                                  // D format: f32
+         | (2u << 7)                                // A format: tf32
+         | (2u << 10)                               // B format: tf32
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// x rounded to the nearest tf32 value (10 fraction bits, ties away from
+// zero), returned as an fp32 value whose low 13 bits are zero.
+__device__ __forceinline__ float round_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
 }
 
 // Shared-memory layout of one 64-deep k-block of a 16-bit operand with the

@@ -1,0 +1,423 @@
+// sgemm_tc3.cu -- fp32 inputs on the 5th-generation tensor cores: tcgen05
+// kind::tf32 on CTA pairs, fp32 accumulation in TMEM, C = A * B (and the
+// extended product of the epilogue modes and stored transposes).
+//
+// TF32 is the pages' tensor-core format for fp32 data (gpu-hpc-book ch.06
+// "高级 cuda 特性 —— 从矩阵乘法(gemm)说起", "Tensor Cores": 8 exponent bits as
+// fp32, 10 fraction bits, taking fp32 inputs). One TF32 product carries about
+// 2^-11 relative error per input, too much for the fp32 bound, so the kernel
+// also runs the split-precision scheme known as 3xTF32 (Ootomo and Yokota,
+// "Recovering single precision accuracy from Tensor Cores while surpassing the
+// FP32 theoretical peak performance", 2022): x = hi + lo with hi = tf32(x)
+// and lo = x - hi (exact in fp32), and
+//     A B ~= hi(A) hi(B) + hi(A) lo(B) + lo(A) hi(B),
+// dropping lo(A) lo(B) (below 2^-22 relative) and the tf32 rounding of the lo
+// parts (below 2^-21 relative): about 3 * 2^-21 |A||B| in all.
+//
+// Roles per CTA (320 threads, cluster of two, persistent over 256 x 256 pair
+// tiles; each CTA holds 128 rows of A and 128 columns of B):
+//   warp 0      producer: TMA of this CTA's fp32 A and B tiles of a 32-deep
+//               k-block into a 3-stage raw ring, in the storage's own layout;
+//   warp 1      TMEM (2 x 256 columns per CTA); in the leader one lane issues
+//               per k-block 4 slices x (1 or 3) pair MMAs M 256, N 256, K 8;
+//   warps 2..5  epilogue: each CTA's 128 accumulator rows from TMEM to C;
+//   warps 6..9  converters: split the raw tiles into K-major, 128-byte-
+//               swizzled hi / lo operand tiles (transposing where the stored
+//               operand is MN-major) in a 2-stage operand ring; both CTAs'
+//               converters count on the leader's barrier before its MMAs read
+//               the stage.
+// Every MMA operand is K-major, the one layout every tcgen05 kind takes.
+// Every wait is bounded, a CTA that gives up raises its peer's abort flag,
+// and both CTAs meet at a cluster barrier before TMEM is freed.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gemm14 {
+namespace {
+
+using T = Tf32Shape;
+
+struct Tf32Smem {
+  uint64_t raw_full[T::RAW_STAGES];   // each CTA: its TMA bytes of a raw stage landed
+  uint64_t raw_empty[T::RAW_STAGES];  // each CTA: its converters are done with a raw stage
+  uint64_t op_full[T::OP_STAGES];     // leader: both CTAs' converters wrote an operand stage
+  uint64_t op_empty[T::OP_STAGES];    // each CTA: the pair MMAs finished reading it
+  uint64_t acc_full[2];               // each CTA: accumulator b holds a finished tile
+  uint64_t acc_empty[2];              // leader: all 8 epilogue warps drained accumulator b
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Tf32Smem) <= 512, "barrier block");
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n, int& tm,
+                                                 int& tn) {
+  constexpr int kGroupM = 8;
+  const int per_group = kGroupM * tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * kGroupM;
+  const int gm = min(tiles_m - first_m, kGroupM);
+  const int r = t - g * per_group;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, float4 v) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ float lds32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// hi = tf32(x), lo = x - hi, four values at a time.
+__device__ __forceinline__ void split4(float4 x, float4& hi, float4& lo) {
+  hi = make_float4(round_tf32(x.x), round_tf32(x.y), round_tf32(x.z), round_tf32(x.w));
+  lo = make_float4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
+}
+
+// Byte offset of the 16-byte chunk c (k = 4c .. 4c+3) of row r in a K-major
+// operand tile: 128-byte rows, chunk index XOR-ed with (r % 8) -- the layout
+// TMA's 128-byte swizzle writes and the MMA descriptors below describe.
+__device__ __forceinline__ uint32_t kmajor_chunk(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + (((c ^ r) & 7) << 4));
+}
+
+// Row r of a raw K-major tile (as TMA's 128-byte swizzle wrote it): the 32
+// values of the row, chunk c in v[c].
+__device__ __forceinline__ void load_kmajor(uint32_t raw, int r, float4 (&v)[8]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) v[c] = lds128(raw + kmajor_chunk(r, c));
+}
+
+// Column r of a raw MN-major tile (32 k rows of 128 fp32, unswizzled, as TMA
+// wrote it): a warp reads 32 consecutive floats of one k row per load.
+__device__ __forceinline__ void load_mnmajor(uint32_t raw, int r, float4 (&v)[8]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    v[c].x = lds32(raw + static_cast<uint32_t>(((4 * c + 0) * 128 + r) * 4));
+    v[c].y = lds32(raw + static_cast<uint32_t>(((4 * c + 1) * 128 + r) * 4));
+    v[c].z = lds32(raw + static_cast<uint32_t>(((4 * c + 2) * 128 + r) * 4));
+    v[c].w = lds32(raw + static_cast<uint32_t>(((4 * c + 3) * 128 + r) * 4));
+  }
+}
+
+// The 32 values of row r (k = 4c .. 4c+3 in v[c]) split into row r of the
+// K-major hi and lo operand tiles.
+__device__ __forceinline__ void store_split(uint32_t hi, uint32_t lo, int r,
+                                            const float4 (&v)[8], bool three) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t off = kmajor_chunk(r, c);
+    float4 h, l;
+    split4(v[c], h, l);
+    sts128(hi + off, h);
+    if (three) sts128(lo + off, l);
+  }
+}
+
+// kTA / kTB: A stored K x M / B stored N x K. kGeneral: the alpha / beta
+// epilogue read from args (else a plain store).
+template <bool kTA, bool kTB, bool kGeneral>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
+    sgemm_tf32_pair_kernel(const __grid_constant__ CUtensorMap map_a,
+                           const __grid_constant__ CUtensorMap map_b, const GemmArgs args,
+                           const uint32_t idesc, const int terms) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* raw_ring = base;
+  uint8_t* op_ring = base + T::RAW_STAGES * T::RAW_STAGE;
+  Tf32Smem& sm = *reinterpret_cast<Tf32Smem*>(op_ring + T::OP_STAGES * T::OP_STAGE);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(cluster_count_x());
+  const int M = args.M, N = args.N, K = args.K;
+  const int tiles_m = (M + T::BM - 1) / T::BM;
+  const int tiles_n = (N + T::BN - 1) / T::BN;
+  const int num_tiles = tiles_m * tiles_n;
+  const int kblocks = (K + T::BK - 1) / T::BK;
+  const bool three = terms == 3;
+  const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns,
+                   mapa_shared(smem_u32(&sm.abort_flag), rank ^ 1u)};
+  uint32_t prod_it = 0;
+  bool mma_issued = false;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < T::RAW_STAGES; ++s) {
+      mbar_init(&sm.raw_full[s], 1);
+      mbar_init(&sm.raw_empty[s], 4);
+    }
+    for (int s = 0; s < T::OP_STAGES; ++s) {
+      mbar_init(&sm.op_full[s], 8);
+      mbar_init(&sm.op_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_empty[b], 8);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b);
+  }
+  // Both CTAs' barriers exist before either CTA signals the other's.
+  cluster_sync();
+  if (warp == 1) {
+    tmem_alloc_pair(&sm.tmem_base, T::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = true;
+      for (int t = cid; t < num_tiles && ok; t += ncl) {
+        int tm, tn;
+        pair_tile_coords(t, tiles_m, tiles_n, tm, tn);
+        const int m0 = tm * T::BM + static_cast<int>(rank) * 128;
+        const int n0 = tn * T::BN + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
+          const uint32_t s = prod_it % T::RAW_STAGES, ph = (prod_it / T::RAW_STAGES) & 1;
+          if (!mbar_wait(&sm.raw_empty[s], ph ^ 1, wc)) { ok = false; break; }
+          // Failure-detection tests: the first stage is never loaded.
+          if (args.fault == kFaultSkipFirstStage && prod_it == 0) continue;
+          uint8_t* ra = raw_ring + s * T::RAW_STAGE;
+          uint8_t* rb = ra + T::RAW_TILE;
+          mbar_arrive_expect_tx(&sm.raw_full[s], T::RAW_STAGE);
+          if (kTA) tma_load_2d(ra, &map_a, m0, kb * T::BK, &sm.raw_full[s]);
+          else tma_load_2d(ra, &map_a, kb * T::BK, m0, &sm.raw_full[s]);
+          if (kTB) tma_load_2d(rb, &map_b, kb * T::BK, n0, &sm.raw_full[s]);
+          else tma_load_2d(rb, &map_b, n0, kb * T::BK, &sm.raw_full[s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (leader && lane == 0) {
+      bool ok = true;
+      uint32_t it = 0;
+      int local = 0;
+      for (int t = cid; t < num_tiles && ok; t += ncl, ++local) {
+        const int b = local & 1;
+        const uint32_t aph = (local >> 1) & 1;
+        if (!mbar_wait_cluster(&sm.acc_empty[b], aph ^ 1, wc)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * T::BN);
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const uint32_t s = it % T::OP_STAGES, ph = (it / T::OP_STAGES) & 1;
+          if (!mbar_wait_cluster(&sm.op_full[s], ph, wc)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t a_hi = smem_u32(op_ring + s * T::OP_STAGE);
+          const uint32_t a_lo = a_hi + T::OP_TILE;
+          const uint32_t b_hi = a_hi + 2 * T::OP_TILE;
+          const uint32_t b_lo = a_hi + 3 * T::OP_TILE;
+#pragma unroll
+          for (int kk = 0; kk < T::BK / 8; ++kk) {
+            // K-major, 128-byte rows, 8-row groups 1024 B apart; a K = 8 slice
+            // of tf32 is 32 bytes further along the rows.
+            const uint32_t off = static_cast<uint32_t>(kk * 32);
+            const uint64_t ah = smem_desc_sw128(a_hi + off, 16, 1024);
+            const uint64_t bh = smem_desc_sw128(b_hi + off, 16, 1024);
+            tc_mma_tf32_pair(d_tmem, ah, bh, idesc, (kb | kk) != 0);
+            if (three) {
+              tc_mma_tf32_pair(d_tmem, ah, smem_desc_sw128(b_lo + off, 16, 1024), idesc, true);
+              tc_mma_tf32_pair(d_tmem, smem_desc_sw128(a_lo + off, 16, 1024), bh, idesc, true);
+            }
+          }
+          mma_issued = true;
+          tc_commit_pair_multicast(&sm.op_empty[s], 0x3);
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(&sm.acc_full[b], 0x3);
+      }
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&sm.acc_empty[0]), 0);
+    const uint32_t acc_empty_leader1 = mapa_shared(smem_u32(&sm.acc_empty[1]), 0);
+    int local = 0;
+    for (int t = cid; t < num_tiles; t += ncl, ++local) {
+      int tm, tn;
+      pair_tile_coords(t, tiles_m, tiles_n, tm, tn);
+      const int b = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      int got = 1;
+      if (lane == 0) got = mbar_wait(&sm.acc_full[b], aph, wc) ? 1 : 0;
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) break;
+      tc_fence_after_sync();
+      const int row = tm * T::BM + static_cast<int>(rank) * 128 + q * 32 + lane;
+      float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(b * T::BN);
+#pragma unroll 1
+      for (int c = 0; c < T::BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, r);
+        tc_wait_ld();
+        const int col0 = tn * T::BN + c * 32;
+        if (row < M) {
+          if (args.vec_store && col0 + 32 <= N) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              epi_store4<kGeneral>(
+                  args, crow + col0 + 4 * v,
+                  make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < N) epi_store1<kGeneral>(args, crow + col0 + j, __uint_as_float(r[j]));
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(b ? acc_empty_leader1 : acc_empty_leader0);
+    }
+  } else {
+    // ------------------------------------------------------------ converters
+    // Thread r handles row r of A and row r of B^T. The raw stage is released
+    // only after the split values are stored: the stores consume the loaded
+    // registers, so the loads have read the stage before TMA may refill it
+    // (released straight after the loads, it was refilled under them).
+    const int r = threadIdx.x - 6 * 32;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = cid; t < num_tiles && ok; t += ncl) {
+      for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        const uint32_t s = it % T::RAW_STAGES, ph = (it / T::RAW_STAGES) & 1;
+        const uint32_t o = it % T::OP_STAGES, oph = (it / T::OP_STAGES) & 1;
+        int got = 1;
+        if (lane == 0) got = mbar_wait(&sm.raw_full[s], ph, wc) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) { ok = false; break; }
+        const uint32_t ra = smem_u32(raw_ring + s * T::RAW_STAGE);
+        const uint32_t rb = ra + T::RAW_TILE;
+        float4 va[8], vb[8];
+        if (kTA) load_mnmajor(ra, r, va);
+        else load_kmajor(ra, r, va);
+        if (kTB) load_kmajor(rb, r, vb);
+        else load_mnmajor(rb, r, vb);
+        if (lane == 0) got = mbar_wait(&sm.op_empty[o], oph ^ 1, wc) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) { ok = false; break; }
+        const uint32_t a_hi = smem_u32(op_ring + o * T::OP_STAGE);
+        store_split(a_hi, a_hi + T::OP_TILE, r, va, three);
+        store_split(a_hi + 2 * T::OP_TILE, a_hi + 3 * T::OP_TILE, r, vb, three);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.raw_empty[s]);
+        // This thread's operand writes -> visible to the MMAs (async proxy);
+        // the warp's writes are ordered before lane 0's release arrival.
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm.op_full[o]), 0));
+      }
+    }
+  }
+
+  // Teardown. On abort, the leader lets its issued MMAs finish and every CTA
+  // lets its own raw loads land (bounded) before the pair meets.
+  __syncthreads();
+  if (sm.abort_flag) {
+    if (leader && warp == 1 && lane == 0 && mma_issued) {
+      tc_commit_pair_multicast(&sm.drain, 0x1);
+      mbar_wait_timed(&sm.drain, 0, 100000000ull);
+    }
+    if (warp == 0 && lane == 0) {
+      const uint32_t first = prod_it > T::RAW_STAGES ? prod_it - T::RAW_STAGES : 0;
+      for (uint32_t j = first; j < prod_it; ++j)
+        if (!(args.fault == kFaultSkipFirstStage && j == 0))
+          mbar_wait_timed(&sm.raw_full[j % T::RAW_STAGES], (j / T::RAW_STAGES) & 1,
+                          100000000ull);
+    }
+  }
+  // Neither CTA frees TMEM or exits while the pair may still use it.
+  cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, T::TMEM_COLS);
+  }
+}
+
+template <bool kTA, bool kTB, bool kGeneral>
+cudaError_t set_smem() {
+  return cudaFuncSetAttribute(sgemm_tf32_pair_kernel<kTA, kTB, kGeneral>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+}
+
+template <bool kTA, bool kTB, bool kGeneral>
+void launch_one(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
+                uint32_t idesc, int terms, int clusters, cudaStream_t stream) {
+  sgemm_tf32_pair_kernel<kTA, kTB, kGeneral>
+      <<<2 * clusters, T::THREADS, T::SMEM_BYTES, stream>>>(map_a, map_b, args, idesc, terms);
+}
+
+template <bool kTA, bool kTB>
+void launch_epi(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
+                uint32_t idesc, int terms, int clusters, cudaStream_t stream) {
+  if (args.epi != kEpiStore)
+    launch_one<kTA, kTB, true>(map_a, map_b, args, idesc, terms, clusters, stream);
+  else
+    launch_one<kTA, kTB, false>(map_a, map_b, args, idesc, terms, clusters, stream);
+}
+
+}  // namespace
+
+int tf32_pair_max_clusters() {
+  static int cached[64];
+  static bool have[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (have[dev]) return cached[dev];
+  if (set_smem<false, false, false>() || set_smem<false, false, true>() ||
+      set_smem<true, false, false>() || set_smem<true, false, true>() ||
+      set_smem<false, true, false>() || set_smem<false, true, true>() ||
+      set_smem<true, true, false>() || set_smem<true, true, true>())
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(T::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = T::SMEM_BYTES;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, sgemm_tf32_pair_kernel<false, false, false>, &cfg) !=
+      cudaSuccess)
+    n = 0;
+  cached[dev] = n;
+  have[dev] = true;
+  return n;
+}
+
+cudaError_t launch_sgemm_tf32_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                                   const GemmArgs& args, int terms, int clusters,
+                                   cudaStream_t stream) {
+  const uint32_t idesc = idesc_tf32_f32acc(T::BM, T::BN);
+  if (args.transa) {
+    if (args.transb) launch_epi<true, true>(map_a, map_b, args, idesc, terms, clusters, stream);
+    else launch_epi<true, false>(map_a, map_b, args, idesc, terms, clusters, stream);
+  } else {
+    if (args.transb) launch_epi<false, true>(map_a, map_b, args, idesc, terms, clusters, stream);
+    else launch_epi<false, false>(map_a, map_b, args, idesc, terms, clusters, stream);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gemm14

@@ -55,8 +55,21 @@ typedef enum gemm14_status {
   GEMM14_ERR_TIMEOUT = 4             /* a kernel's bounded wait expired (device-side) */
 } gemm14_status;
 
-/* Element types for the planning query. */
-enum { GEMM14_DTYPE_F32 = 0, GEMM14_DTYPE_BF16 = 1, GEMM14_DTYPE_F16 = 2 };
+/*
+ * Element types and arithmetic, for gemm14_gemm_ex and the planning queries:
+ *   F32        fp32 inputs, fp32 FMAs on the CUDA cores (gemm_f32);
+ *   BF16, F16  16-bit inputs, fp32 accumulation on the tensor cores;
+ *   TF32       fp32 inputs rounded to tf32 on the tensor cores (gemm_tf32_f32acc);
+ *   F32_3XTF32 fp32 inputs, split tf32 arithmetic on the tensor cores that
+ *              meets the fp32 bound (gemm_f32_3xtf32).
+ */
+enum {
+  GEMM14_DTYPE_F32 = 0,
+  GEMM14_DTYPE_BF16 = 1,
+  GEMM14_DTYPE_F16 = 2,
+  GEMM14_DTYPE_TF32 = 3,
+  GEMM14_DTYPE_F32_3XTF32 = 4
+};
 
 /*
  * fp32 inputs, fp32 FFMA accumulation on the CUDA cores, fp32 output.
@@ -86,6 +99,30 @@ int gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
 /* As gemm_bf16_f32acc with IEEE binary16 (fp16) inputs. */
 int gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, float* C, int64_t ldc, void* stream);
+
+/*
+ * fp32 inputs on the tensor cores (tcgen05 kind::tf32, fp32 accumulation in
+ * tensor memory), fp32 output. TF32 is the pages' tensor-core format for fp32
+ * data (gpu-hpc-book ch.06, "Tensor Cores": fp32's 8 exponent bits, 10
+ * fraction bits).
+ *   gemm_tf32_f32acc: every input is rounded to the nearest tf32 value (ties
+ *     away from zero) and the products of the rounded values are summed in
+ *     fp32: |C - A B| <= 2e-3 (|A||B|) element-wise, the tf32 analogue of the
+ *     16-bit bound; against the rounded inputs, the fp32 bound.
+ *   gemm_f32_3xtf32: each input x is split into hi = tf32(x) and lo = x - hi,
+ *     and C = hi(A) hi(B) + hi(A) lo(B) + lo(A) hi(B) summed in fp32 (the
+ *     split-precision scheme known as 3xTF32): within the fp32 bound,
+ *     |C - A B| <= 1e-5 (|A||B|), at tensor-core speed.
+ * Arguments, layout and rules as gemm_f32. A and B 16-byte aligned with lda,
+ * ldb multiples of 4 run on CTA pairs of tensor-core SMs (256 x 256 tiles);
+ * other operands run on gemm_f32's kernel, whose exact fp32 products meet both
+ * bounds. Infinite inputs give NaN where a product would be infinite (lo =
+ * inf - inf); finite inputs whose products overflow behave as in gemm_f32.
+ */
+int gemm_tf32_f32acc(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                     const float* B, int64_t ldb, float* C, int64_t ldc, void* stream);
+int gemm_f32_3xtf32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                    const float* B, int64_t ldb, float* C, int64_t ldc, void* stream);
 
 /*
  * Stream-K variants. Same operation and arguments as gemm_f32 /
@@ -147,7 +184,8 @@ int gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int
                              const void* B, int64_t ldb, float* C, int64_t ldc, void* stream);
 
 /*
- * The extended product, for all three element types (dtype = GEMM14_DTYPE_*):
+ * The extended product, for every element type and arithmetic (dtype =
+ * GEMM14_DTYPE_*):
  *     C = alpha * op(A) * op(B) + beta * C,
  * op(A) an M x K matrix and op(B) a K x N matrix. It generalises the
  * accumulate form of the pages' asynchronous tensor-core MMA (gpu-hpc-book
@@ -207,7 +245,8 @@ int gemm14_check_device_error(void* stream);
 /* Launch plan chosen for a call (host-side only; no CUDA call is made). */
 typedef struct gemm14_plan {
   int kernel;     /* 1 = fp32 SIMT (FFMA), 2 = tcgen05 on one SM per tile,
-                     3 = tcgen05 on CTA pairs (two SMs per 256 x 256 tile), 0 = no launch */
+                     3 = tcgen05 on CTA pairs (two SMs per 256 x 256 tile),
+                     4 = tcgen05 kind::tf32 on CTA pairs (TF32 / 3xTF32), 0 = no launch */
   int loader;     /* 1 = TMA, 2 = software loader (cp.async for fp32), 0 = none */
   int bm, bn, bk; /* output tile rows x columns, k-block depth */
   int stages;     /* shared-memory ring depth */

@@ -212,3 +212,31 @@ def test_ex_plan_loaders(lib):
 def test_ex_empty_product_is_a_no_op(lib):
     assert _ex(BF16, 1, 1, 0, 4, 4, 0, 1, 0, 4, 0, 4, 2.0, 3.0) == 0
     assert _ex(F32, 0, 1, 4, 0, 4, 0, 4, 0, 4, 0, 1, 2.0, 3.0) == 0
+
+
+# ----------------------------------------------------------------- fp32 on the tensor cores
+
+TF32, X3 = g14.GEMM14_DTYPE_TF32, g14.GEMM14_DTYPE_F32_3XTF32
+
+
+@pytest.mark.parametrize("dtype", [TF32, X3])
+def test_plan_tf32_pairs_and_fallback(lib, dtype):
+    st, p = g14.plan(dtype, 3072, 3072, 3072, P, 3072, P, 3072, P, 3072, 152)
+    assert st == 0 and p.kernel == 4 and (p.bm, p.bn, p.bk) == (256, 256, 32)
+    assert p.tiles == 144 and p.grid == 152 and p.threads == 320
+    assert p.smem_bytes <= 227 * 1024
+    for ta, tb in ((1, 0), (0, 1), (1, 1)):
+        st, pt = g14.plan_ex(dtype, ta, tb, 3072, 3072, 3072, P, 3072, P, 3072, P, 3072, 152)
+        assert st == 0 and pt == p
+    # pitches TMA cannot take: the fp32 SIMT kernel (cp.async loader)
+    st, p2 = g14.plan(dtype, 4097, 3001, 513, P, 513, P, 3001, P, 3001, 152)
+    assert st == 0 and p2.kernel == 1 and p2.loader == 2
+    # no workspace: the pair kernel does not split tiles
+    assert g14.workspace_bytes(dtype, 3072, 3072, 3072, 152) == 0
+
+
+def test_tf32_entry_points_validate(lib):
+    for fn in (g14.gemm_tf32_f32acc, g14.gemm_f32_3xtf32):
+        assert fn(4, 4, 8, P, 4, P, 4, P, 4, None, check=False) == _lib.GEMM14_ERR_INVALID_ARG
+        assert fn(0, 4, 4, 0, 4, 0, 4, 0, 4, None, check=False) == 0
+    assert _ex(5, 0, 0, 4, 4, 4, P, 4, P, 4, P, 4) == _lib.GEMM14_ERR_INVALID_ARG  # no dtype 5
