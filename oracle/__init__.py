@@ -73,6 +73,8 @@ def _load():
             lib.oracle_gemm_ex.restype = ctypes.c_int
             lib.oracle_round_tf32.argtypes = [vp, i64]
             lib.oracle_round_tf32.restype = ctypes.c_int
+            lib.oracle_truncate_tf32.argtypes = [vp, i64]
+            lib.oracle_truncate_tf32.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -190,6 +192,16 @@ def round_tf32(X: np.ndarray) -> np.ndarray:
     rc = _load().oracle_round_tf32(_ptr(out) if out.size else 0, out.size)
     if rc != 0:
         raise RuntimeError(f"oracle_round_tf32 failed with code {rc}")
+    return out
+
+
+def truncate_tf32(X: np.ndarray) -> np.ndarray:
+    """A float32 copy of X with every value truncated to tf32 (the 13 low
+    fraction bits cleared: what the tensor cores take from an fp32 input)."""
+    out = np.array(X, dtype=np.float32, copy=True, order="C")
+    rc = _load().oracle_truncate_tf32(_ptr(out) if out.size else 0, out.size)
+    if rc != 0:
+        raise RuntimeError(f"oracle_truncate_tf32 failed with code {rc}")
     return out
 
 

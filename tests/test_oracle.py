@@ -387,3 +387,42 @@ def test_round_tf32_matches_exact_rational_rounding(oracle_mod):
     # every result has its 13 low bits clear (it is a tf32 value)
     fin = np.isfinite(got)
     assert not (got[fin].view(np.uint32) & 0x1FFF).any()
+
+
+def _tf32_trunc_reference(x: float) -> float:
+    """Largest-magnitude value with 11 significant bits not above |x| (fp32's
+    exponent range), sign kept: truncation toward zero, by exact rationals."""
+    if x == 0 or math.isinf(x) or math.isnan(x):
+        return x
+    s = -1 if x < 0 else 1
+    a = Fraction(abs(x))
+    _, e = math.frexp(abs(x))
+    e = max(e, -125)
+    unit = Fraction(2) ** (e - 11)
+    return s * float((a // unit) * unit)
+
+
+@pytest.mark.parametrize("x,want", [
+    (1.0, 1.0), (1 + 2.0 ** -10, 1 + 2.0 ** -10),
+    (1 + 2.0 ** -11, 1.0), (1 + 2.0 ** -10 - 2.0 ** -23, 1.0),    # toward zero, never up
+    (-(1 + 2.0 ** -10 - 2.0 ** -23), -1.0),
+    (2 - 2.0 ** -23, 2 - 2.0 ** -10),                               # no carry
+    (3.4028234663852886e38, (2 - 2.0 ** -10) * 2.0 ** 127),         # stays finite
+    (2.0 ** -149, 0.0), (2.0 ** -136 + 2.0 ** -149, 2.0 ** -136),
+    (math.inf, math.inf), (-math.inf, -math.inf),
+])
+def test_truncate_tf32_textbook_values(oracle_mod, x, want):
+    got = oracle_mod.truncate_tf32(np.array([[x]], np.float32))[0, 0]
+    assert got == np.float32(want) and np.signbit(got) == np.signbit(np.float32(want))
+
+
+def test_truncate_tf32_matches_exact_rational_truncation(oracle_mod):
+    g = np.random.default_rng(61)
+    x = g.integers(0, 2 ** 32, 20000, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    x = x[np.isfinite(x)].reshape(1, -1)
+    got = oracle_mod.truncate_tf32(x)[0]
+    for xi, gi in zip(x[0], got):
+        assert gi == np.float32(_tf32_trunc_reference(float(xi))), (xi, gi)
+    # a quiet NaN stays NaN; truncation never moves a value away from zero
+    assert np.isnan(oracle_mod.truncate_tf32(np.array([[np.nan]], np.float32))[0, 0])
+    assert (np.abs(got) <= np.abs(x[0])).all()
