@@ -137,19 +137,20 @@ cudaError_t launch_hgemm_tc_soft(int bn, const GemmArgs& args, uint32_t idesc, i
                                  cudaStream_t stream);
 
 // ---- fp32 inputs on the tensor cores (sgemm_tc3.cu): tcgen05 kind::tf32 on
-// CTA pairs, 256 x 256 tiles. Each fp32 input x is split into hi = tf32(x)
-// and lo = x - hi by converter warps; terms = 1 computes hi(A) hi(B) (TF32
-// precision), terms = 3 adds hi(A) lo(B) + lo(A) hi(B) ("3xTF32").
+// CTA pairs, 256 x 256 tiles. The tensor cores read an fp32 operand as tf32 by
+// dropping its 13 low fraction bits: hi(x). terms = 1 computes hi(A) hi(B)
+// (TF32); terms = 3 adds hi(A) lo(B) + lo(A) hi(B) with lo(x) = x - hi(x),
+// written by converter warps ("3xTF32").
 struct Tf32Shape {
   static constexpr int BM = 256, BN = 256, BK = 32;  // k-block: 32 fp32 = one 128-byte row
-  static constexpr int RAW_STAGES = 3, OP_STAGES = 2;
+  static constexpr int OP_STAGES = 2;
+  static constexpr int MAX_RAW_STAGES = 5;
   static constexpr int THREADS = 10 * 32;  // producer, MMA, 4 epilogue, 4 converter warps
-  static constexpr int RAW_TILE = 128 * BK * 4;   // one CTA's fp32 A rows or B columns: 16 KB
-  static constexpr int RAW_STAGE = 2 * RAW_TILE;  // A, B as loaded
-  static constexpr int OP_TILE = 128 * BK * 4;    // one K-major tf32 operand tile: 16 KB
-  static constexpr int OP_STAGE = 4 * OP_TILE;    // A hi, A lo, B hi, B lo
+  static constexpr int TILE = 128 * BK * 4;       // one CTA's 128 rows x 32 k of fp32: 16 KB
+  static constexpr int RAW_STAGE = 2 * TILE;      // A, B as loaded
+  static constexpr int RING_BYTES = 224 * 1024;   // raw + operand rings
   static constexpr int TMEM_COLS = 512;
-  static constexpr int SMEM_BYTES = RAW_STAGES * RAW_STAGE + OP_STAGES * OP_STAGE + 512 + 1024;
+  static constexpr int SMEM_BYTES = RING_BYTES + 512 + 1024;
 };
 
 // Clusters of two the tf32 kernel fits at once on the current device (0: it

@@ -408,14 +408,6 @@ __host__ __device__ constexpr uint32_t idesc_tf32_f32acc(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
-// x rounded to the nearest tf32 value (10 fraction bits, ties away from
-// zero), returned as an fp32 value whose low 13 bits are zero.
-__device__ __forceinline__ float round_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
-}
-
 // Shared-memory layout of one 64-deep k-block of a 16-bit operand with the
 // 128-byte swizzle, as the kernels' loaders write it:
 //  K-major:  128-byte rows of 64 k, 8-row groups 1024 B apart (stride

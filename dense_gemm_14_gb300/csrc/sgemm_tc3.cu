@@ -4,29 +4,32 @@
 //
 // TF32 is the pages' tensor-core format for fp32 data (gpu-hpc-book ch.06
 // "高级 cuda 特性 —— 从矩阵乘法(gemm)说起", "Tensor Cores": 8 exponent bits as
-// fp32, 10 fraction bits, taking fp32 inputs). One TF32 product carries about
-// 2^-11 relative error per input, too much for the fp32 bound, so the kernel
-// also runs the split-precision scheme known as 3xTF32 (Ootomo and Yokota,
-// "Recovering single precision accuracy from Tensor Cores while surpassing the
-// FP32 theoretical peak performance", 2022): x = hi + lo with hi = tf32(x)
-// and lo = x - hi (exact in fp32), and
+// fp32, 10 fraction bits, taking fp32 inputs). The tensor cores read an fp32
+// operand as tf32 by dropping its 13 low fraction bits, hi(x); one such
+// product carries up to 2^-9 relative error, too much for the fp32 bound, so
+// the kernel also runs the split-precision scheme known as 3xTF32 (Ootomo and
+// Yokota, "Recovering single precision accuracy from Tensor Cores while
+// surpassing the FP32 theoretical peak performance", 2022): lo(x) = x - hi(x)
+// is exact in fp32, and
 //     A B ~= hi(A) hi(B) + hi(A) lo(B) + lo(A) hi(B),
-// dropping lo(A) lo(B) (below 2^-22 relative) and the tf32 rounding of the lo
-// parts (below 2^-21 relative): about 3 * 2^-21 |A||B| in all.
+// dropping lo(A) lo(B) and the tensor cores' truncation of the lo parts (each
+// below 2^-20 relative): at most 3 * 2^-20 |A||B| in all.
 //
 // Roles per CTA (320 threads, cluster of two, persistent over 256 x 256 pair
 // tiles; each CTA holds 128 rows of A and 128 columns of B):
 //   warp 0      producer: TMA of this CTA's fp32 A and B tiles of a 32-deep
-//               k-block into a 3-stage raw ring, in the storage's own layout;
+//               k-block, in the storage's own layout, into a raw ring;
 //   warp 1      TMEM (2 x 256 columns per CTA); in the leader one lane issues
 //               per k-block 4 slices x (1 or 3) pair MMAs M 256, N 256, K 8;
 //   warps 2..5  epilogue: each CTA's 128 accumulator rows from TMEM to C;
-//   warps 6..9  converters: split the raw tiles into K-major, 128-byte-
-//               swizzled hi / lo operand tiles (transposing where the stored
-//               operand is MN-major) in a 2-stage operand ring; both CTAs'
-//               converters count on the leader's barrier before its MMAs read
-//               the stage.
-// Every MMA operand is K-major, the one layout every tcgen05 kind takes.
+//   warps 6..9  converters: write what the MMAs need beyond the raw tiles into
+//               a 2-stage operand ring: the lo tiles (3xTF32), and a K-major
+//               copy of an operand stored MN-major; both CTAs' converters count
+//               on the leader's barrier before its MMAs read the stage.
+// Every MMA operand is K-major with the 128-byte swizzle, the one layout every
+// tcgen05 kind takes. A raw tile that TMA already wrote K-major (A stored
+// M x K, B stored N x K) is an MMA operand as it stands; its raw stage is then
+// freed by the MMAs' commit as well as by the converters.
 // Every wait is bounded, a CTA that gives up raises its peer's abort flag,
 // and both CTAs meet at a cluster barrier before TMEM is freed.
 #include "kernels.h"
@@ -37,13 +40,33 @@ namespace {
 
 using T = Tf32Shape;
 
+// Shared-memory plan of one storage variant (kTA: A stored K x M; kTB: B
+// stored N x K). The operand stage holds, in this order, a K-major copy of A
+// (if A is stored K x M), lo(A), a K-major copy of B (if B is stored K x N)
+// and lo(B); the raw ring takes what is left of the ring budget.
+template <bool kTA, bool kTB>
+struct Tf32Plan {
+  static constexpr bool A_RAW = !kTA;  // the raw A tile is K-major: the MMAs read it
+  static constexpr bool B_RAW = kTB;
+  static constexpr int A_HI = 0;
+  static constexpr int A_LO = (A_RAW ? 0 : 1) * T::TILE;
+  static constexpr int B_HI = A_LO + T::TILE;
+  static constexpr int B_LO = B_HI + (B_RAW ? 0 : 1) * T::TILE;
+  static constexpr int OP_STAGE = B_LO + T::TILE;
+  static constexpr int RAW_STAGES_FIT = (T::RING_BYTES - T::OP_STAGES * OP_STAGE) / T::RAW_STAGE;
+  static constexpr int RAW_STAGES =
+      RAW_STAGES_FIT < T::MAX_RAW_STAGES ? RAW_STAGES_FIT : T::MAX_RAW_STAGES;
+  static_assert(RAW_STAGES >= 3, "raw ring depth");
+  static_assert(RAW_STAGES * T::RAW_STAGE + T::OP_STAGES * OP_STAGE <= T::RING_BYTES, "rings");
+};
+
 struct Tf32Smem {
-  uint64_t raw_full[T::RAW_STAGES];   // each CTA: its TMA bytes of a raw stage landed
-  uint64_t raw_empty[T::RAW_STAGES];  // each CTA: its converters are done with a raw stage
-  uint64_t op_full[T::OP_STAGES];     // leader: both CTAs' converters wrote an operand stage
-  uint64_t op_empty[T::OP_STAGES];    // each CTA: the pair MMAs finished reading it
-  uint64_t acc_full[2];               // each CTA: accumulator b holds a finished tile
-  uint64_t acc_empty[2];              // leader: all 8 epilogue warps drained accumulator b
+  uint64_t raw_full[T::MAX_RAW_STAGES];   // each CTA: its TMA bytes of a raw stage landed
+  uint64_t raw_empty[T::MAX_RAW_STAGES];  // each CTA: converters (and MMAs) are done with it
+  uint64_t op_full[T::OP_STAGES];         // leader: both CTAs' converters wrote an operand stage
+  uint64_t op_empty[T::OP_STAGES];        // each CTA: the pair MMAs finished reading it
+  uint64_t acc_full[2];                   // each CTA: accumulator b holds a finished tile
+  uint64_t acc_empty[2];                  // leader: all 8 epilogue warps drained accumulator b
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -77,10 +100,9 @@ __device__ __forceinline__ float lds32(uint32_t addr) {
   return v;
 }
 
-// hi = tf32(x), lo = x - hi, four values at a time.
-__device__ __forceinline__ void split4(float4 x, float4& hi, float4& lo) {
-  hi = make_float4(round_tf32(x.x), round_tf32(x.y), round_tf32(x.z), round_tf32(x.w));
-  lo = make_float4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
+// lo(x) = x - hi(x), hi(x) = x with its 13 low fraction bits cleared (exact).
+__device__ __forceinline__ float lo_tf32(float x) {
+  return x - __uint_as_float(__float_as_uint(x) & 0xffffe000u);
 }
 
 // Byte offset of the 16-byte chunk c (k = 4c .. 4c+3) of row r in a K-major
@@ -109,18 +131,17 @@ __device__ __forceinline__ void load_mnmajor(uint32_t raw, int r, float4 (&v)[8]
   }
 }
 
-// The 32 values of row r (k = 4c .. 4c+3 in v[c]) split into row r of the
-// K-major hi and lo operand tiles.
-__device__ __forceinline__ void store_split(uint32_t hi, uint32_t lo, int r,
-                                            const float4 (&v)[8], bool three) {
+// Row r of a K-major operand tile: the values as they are (the tensor cores
+// drop their low bits), or their lo parts.
+__device__ __forceinline__ void store_row(uint32_t tile, int r, const float4 (&v)[8]) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint32_t off = kmajor_chunk(r, c);
-    float4 h, l;
-    split4(v[c], h, l);
-    sts128(hi + off, h);
-    if (three) sts128(lo + off, l);
-  }
+  for (int c = 0; c < 8; ++c) sts128(tile + kmajor_chunk(r, c), v[c]);
+}
+__device__ __forceinline__ void store_lo_row(uint32_t tile, int r, const float4 (&v)[8]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    sts128(tile + kmajor_chunk(r, c),
+           make_float4(lo_tf32(v[c].x), lo_tf32(v[c].y), lo_tf32(v[c].z), lo_tf32(v[c].w)));
 }
 
 // kTA / kTB: A stored K x M / B stored N x K. kGeneral: the alpha / beta
@@ -130,11 +151,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
     sgemm_tf32_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                            const __grid_constant__ CUtensorMap map_b, const GemmArgs args,
                            const uint32_t idesc, const int terms) {
+  using L = Tf32Plan<kTA, kTB>;
+  constexpr int RS = L::RAW_STAGES;
+  constexpr bool kMmaReadsRaw = L::A_RAW || L::B_RAW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint8_t* raw_ring = base;
-  uint8_t* op_ring = base + T::RAW_STAGES * T::RAW_STAGE;
-  Tf32Smem& sm = *reinterpret_cast<Tf32Smem*>(op_ring + T::OP_STAGES * T::OP_STAGE);
+  uint8_t* op_ring = base + RS * T::RAW_STAGE;
+  Tf32Smem& sm = *reinterpret_cast<Tf32Smem*>(base + T::RING_BYTES);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -154,9 +178,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
   bool mma_issued = false;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < T::RAW_STAGES; ++s) {
+    for (int s = 0; s < RS; ++s) {
       mbar_init(&sm.raw_full[s], 1);
-      mbar_init(&sm.raw_empty[s], 4);
+      mbar_init(&sm.raw_empty[s], kMmaReadsRaw ? 5 : 4);
     }
     for (int s = 0; s < T::OP_STAGES; ++s) {
       mbar_init(&sm.op_full[s], 8);
@@ -193,12 +217,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
         const int m0 = tm * T::BM + static_cast<int>(rank) * 128;
         const int n0 = tn * T::BN + static_cast<int>(rank) * 128;
         for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
-          const uint32_t s = prod_it % T::RAW_STAGES, ph = (prod_it / T::RAW_STAGES) & 1;
+          const uint32_t s = prod_it % RS, ph = (prod_it / RS) & 1;
           if (!mbar_wait(&sm.raw_empty[s], ph ^ 1, wc)) { ok = false; break; }
           // Failure-detection tests: the first stage is never loaded.
           if (args.fault == kFaultSkipFirstStage && prod_it == 0) continue;
           uint8_t* ra = raw_ring + s * T::RAW_STAGE;
-          uint8_t* rb = ra + T::RAW_TILE;
+          uint8_t* rb = ra + T::TILE;
           mbar_arrive_expect_tx(&sm.raw_full[s], T::RAW_STAGE);
           if (kTA) tma_load_2d(ra, &map_a, m0, kb * T::BK, &sm.raw_full[s]);
           else tma_load_2d(ra, &map_a, kb * T::BK, m0, &sm.raw_full[s]);
@@ -220,13 +244,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * T::BN);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const uint32_t s = it % T::OP_STAGES, ph = (it / T::OP_STAGES) & 1;
-          if (!mbar_wait_cluster(&sm.op_full[s], ph, wc)) { ok = false; break; }
+          const uint32_t s = it % RS;
+          const uint32_t o = it % T::OP_STAGES, oph = (it / T::OP_STAGES) & 1;
+          // Both CTAs' converters have seen raw stage s full and written
+          // operand stage o.
+          if (!mbar_wait_cluster(&sm.op_full[o], oph, wc)) { ok = false; break; }
           tc_fence_after_sync();
-          const uint32_t a_hi = smem_u32(op_ring + s * T::OP_STAGE);
-          const uint32_t a_lo = a_hi + T::OP_TILE;
-          const uint32_t b_hi = a_hi + 2 * T::OP_TILE;
-          const uint32_t b_lo = a_hi + 3 * T::OP_TILE;
+          const uint32_t raw = smem_u32(raw_ring + s * T::RAW_STAGE);
+          const uint32_t op = smem_u32(op_ring + o * L::OP_STAGE);
+          const uint32_t a_hi = L::A_RAW ? raw : op + L::A_HI;
+          const uint32_t b_hi = L::B_RAW ? raw + T::TILE : op + L::B_HI;
 #pragma unroll
           for (int kk = 0; kk < T::BK / 8; ++kk) {
             // K-major, 128-byte rows, 8-row groups 1024 B apart; a K = 8 slice
@@ -236,12 +263,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
             const uint64_t bh = smem_desc_sw128(b_hi + off, 16, 1024);
             tc_mma_tf32_pair(d_tmem, ah, bh, idesc, (kb | kk) != 0);
             if (three) {
-              tc_mma_tf32_pair(d_tmem, ah, smem_desc_sw128(b_lo + off, 16, 1024), idesc, true);
-              tc_mma_tf32_pair(d_tmem, smem_desc_sw128(a_lo + off, 16, 1024), bh, idesc, true);
+              tc_mma_tf32_pair(d_tmem, ah, smem_desc_sw128(op + L::B_LO + off, 16, 1024), idesc,
+                               true);
+              tc_mma_tf32_pair(d_tmem, smem_desc_sw128(op + L::A_LO + off, 16, 1024), bh, idesc,
+                               true);
             }
           }
           mma_issued = true;
-          tc_commit_pair_multicast(&sm.op_empty[s], 0x3);
+          tc_commit_pair_multicast(&sm.op_empty[o], 0x3);
+          if (kMmaReadsRaw) tc_commit_pair_multicast(&sm.raw_empty[s], 0x3);
         }
         if (!ok) break;
         tc_commit_pair_multicast(&sm.acc_full[b], 0x3);
@@ -294,34 +324,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ converters
-    // Thread r handles row r of A and row r of B^T. The raw stage is released
-    // only after the split values are stored: the stores consume the loaded
-    // registers, so the loads have read the stage before TMA may refill it
-    // (released straight after the loads, it was refilled under them).
+    // Thread r handles row r of A and row r of B^T. A raw stage is released
+    // only after the values loaded from it are stored: the stores consume
+    // the loaded registers, so the loads have read the stage before TMA may
+    // refill it (released straight after the loads, it was refilled under
+    // them).
     const int r = threadIdx.x - 6 * 32;
+    const bool need_a = !L::A_RAW || three;  // a K-major copy of A, or lo(A)
+    const bool need_b = !L::B_RAW || three;
     uint32_t it = 0;
     bool ok = true;
     for (int t = cid; t < num_tiles && ok; t += ncl) {
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
-        const uint32_t s = it % T::RAW_STAGES, ph = (it / T::RAW_STAGES) & 1;
+        const uint32_t s = it % RS, ph = (it / RS) & 1;
         const uint32_t o = it % T::OP_STAGES, oph = (it / T::OP_STAGES) & 1;
         int got = 1;
         if (lane == 0) got = mbar_wait(&sm.raw_full[s], ph, wc) ? 1 : 0;
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) { ok = false; break; }
         const uint32_t ra = smem_u32(raw_ring + s * T::RAW_STAGE);
-        const uint32_t rb = ra + T::RAW_TILE;
+        const uint32_t rb = ra + T::TILE;
         float4 va[8], vb[8];
-        if (kTA) load_mnmajor(ra, r, va);
-        else load_kmajor(ra, r, va);
-        if (kTB) load_kmajor(rb, r, vb);
-        else load_mnmajor(rb, r, vb);
+        if (need_a) {
+          if (kTA) load_mnmajor(ra, r, va);
+          else load_kmajor(ra, r, va);
+        }
+        if (need_b) {
+          if (kTB) load_kmajor(rb, r, vb);
+          else load_mnmajor(rb, r, vb);
+        }
         if (lane == 0) got = mbar_wait(&sm.op_empty[o], oph ^ 1, wc) ? 1 : 0;
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) { ok = false; break; }
-        const uint32_t a_hi = smem_u32(op_ring + o * T::OP_STAGE);
-        store_split(a_hi, a_hi + T::OP_TILE, r, va, three);
-        store_split(a_hi + 2 * T::OP_TILE, a_hi + 3 * T::OP_TILE, r, vb, three);
+        const uint32_t op = smem_u32(op_ring + o * L::OP_STAGE);
+        if (!L::A_RAW) store_row(op + L::A_HI, r, va);
+        if (three) store_lo_row(op + L::A_LO, r, va);
+        if (!L::B_RAW) store_row(op + L::B_HI, r, vb);
+        if (three) store_lo_row(op + L::B_LO, r, vb);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.raw_empty[s]);
         // This thread's operand writes -> visible to the MMAs (async proxy);
@@ -342,11 +381,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
       mbar_wait_timed(&sm.drain, 0, 100000000ull);
     }
     if (warp == 0 && lane == 0) {
-      const uint32_t first = prod_it > T::RAW_STAGES ? prod_it - T::RAW_STAGES : 0;
+      const uint32_t first = prod_it > RS ? prod_it - RS : 0;
       for (uint32_t j = first; j < prod_it; ++j)
         if (!(args.fault == kFaultSkipFirstStage && j == 0))
-          mbar_wait_timed(&sm.raw_full[j % T::RAW_STAGES], (j / T::RAW_STAGES) & 1,
-                          100000000ull);
+          mbar_wait_timed(&sm.raw_full[j % RS], (j / RS) & 1, 100000000ull);
     }
   }
   // Neither CTA frees TMEM or exits while the pair may still use it.

@@ -105,19 +105,22 @@ int gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  * tensor memory), fp32 output. TF32 is the pages' tensor-core format for fp32
  * data (gpu-hpc-book ch.06, "Tensor Cores": fp32's 8 exponent bits, 10
  * fraction bits).
- *   gemm_tf32_f32acc: every input is rounded to the nearest tf32 value (ties
- *     away from zero) and the products of the rounded values are summed in
- *     fp32: |C - A B| <= 2e-3 (|A||B|) element-wise, the tf32 analogue of the
- *     16-bit bound; against the rounded inputs, the fp32 bound.
- *   gemm_f32_3xtf32: each input x is split into hi = tf32(x) and lo = x - hi,
- *     and C = hi(A) hi(B) + hi(A) lo(B) + lo(A) hi(B) summed in fp32 (the
- *     split-precision scheme known as 3xTF32): within the fp32 bound,
+ *   gemm_tf32_f32acc: every input is read as tf32 the way the tensor cores
+ *     read an fp32 operand, tf32(x) = x with its 13 low fraction bits
+ *     cleared (truncation toward zero), and the products of those values are
+ *     summed in fp32: against the truncated inputs, the fp32 bound; against
+ *     the fp32 inputs |C - A B| <= 4e-3 (|A||B|) element-wise.
+ *   gemm_f32_3xtf32: each input x is split into hi = tf32(x) and lo = x - hi
+ *     (exact), and C = hi(A) hi(B) + hi(A) lo(B) + lo(A) hi(B) summed in fp32
+ *     (the split-precision scheme known as 3xTF32): within the fp32 bound,
  *     |C - A B| <= 1e-5 (|A||B|), at tensor-core speed.
  * Arguments, layout and rules as gemm_f32. A and B 16-byte aligned with lda,
  * ldb multiples of 4 run on CTA pairs of tensor-core SMs (256 x 256 tiles);
  * other operands run on gemm_f32's kernel, whose exact fp32 products meet both
  * bounds. Infinite inputs give NaN where a product would be infinite (lo =
- * inf - inf); finite inputs whose products overflow behave as in gemm_f32.
+ * inf - inf), and a NaN whose payload lies only in the 13 low fraction bits
+ * is read as an infinity; finite inputs whose products overflow behave as in
+ * gemm_f32.
  */
 int gemm_tf32_f32acc(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                      const float* B, int64_t ldb, float* C, int64_t ldc, void* stream);

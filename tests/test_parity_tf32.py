@@ -3,9 +3,10 @@ pairs) against the oracle:
 
 - gemm_f32_3xtf32 (split hi/lo tf32 arithmetic): within the fp32 bound
   1e-5 (|A||B|) of the exact product of the fp32 inputs;
-- gemm_tf32_f32acc (inputs rounded to tf32): within the fp32 bound of the
-  exact product of the oracle-rounded inputs, and within 2e-3 (|A||B|) of the
-  exact product of the unrounded ones (two roundings of 2^-11 per product).
+- gemm_tf32_f32acc (inputs read as tf32 by the tensor cores, i.e. with their
+  13 low fraction bits dropped): within the fp32 bound of the exact product of
+  the oracle-truncated inputs, and within 4e-3 (|A||B|) of the exact product
+  of the fp32 ones (two truncations of under 2^-10 per product, doubled).
 
 TF32 is the pages' tensor-core format for fp32 data (gpu-hpc-book ch.06,
 "Tensor Cores")."""
@@ -21,7 +22,7 @@ from gpu_util import TOL, oracle_check_ex, run_abi, run_ex, stored, to_device_pa
 pytestmark = pytest.mark.gpu
 
 X3, TF32 = g14.GEMM14_DTYPE_F32_3XTF32, g14.GEMM14_DTYPE_TF32
-TOL_TF32 = 2e-3
+TOL_TF32 = 4e-3
 TRANS = [(0, 0), (1, 0), (0, 1), (1, 1)]
 
 
@@ -55,12 +56,12 @@ def run_mode(code, A, B, transa=0, transb=0, alpha=1.0, beta=0.0, C0=None, lda=N
 
 def check(oracle_mod, A, B, C, tol, transa=0, transb=0, alpha=1.0, beta=0.0, C0=None,
           rounded=False):
-    """C against the oracle's extended product of the stored (optionally
-    oracle-rounded to tf32) fp32 matrices."""
+    """C against the oracle's extended product of the stored fp32 matrices,
+    or (rounded) of their tf32 values, the oracle's truncation."""
     As = stored(A, transa).numpy()
     Bs = stored(B, transb).numpy()
     if rounded:
-        As, Bs = oracle_mod.round_tf32(As), oracle_mod.round_tf32(Bs)
+        As, Bs = oracle_mod.truncate_tf32(As), oracle_mod.truncate_tf32(Bs)
     c0 = C0.numpy() if C0 is not None else None
     ref, refabs = oracle_mod.gemm_ex(As, Bs, "f32", bool(transa), bool(transb), alpha, beta, c0)
     Cg = C.numpy()
@@ -87,7 +88,7 @@ def test_3xtf32_meets_the_fp32_bound(oracle_mod, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_tf32_is_the_product_of_rounded_inputs(oracle_mod, M, N, K):
+def test_tf32_is_the_product_of_truncated_inputs(oracle_mod, M, N, K):
     A, B = inputs.make(M, N, K, "f32", "normal", 1.0, seed=M + 5 * N + K)
     C = run_mode(TF32, A, B)
     check(oracle_mod, A, B, C, TOL["f32"], rounded=True)
