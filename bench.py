@@ -384,20 +384,25 @@ def run_ours(args, dist: Dist):
     # ---- end to end through the public API with host tensors
     e2e = None
     if not args.no_e2e:
+        # inputs and the result buffers in pinned host memory, allocated once
+        # (as a caller reusing its buffers would); every step sends A and B to
+        # the GPU and brings C back inside the timed region
         pinned = {n: (a.pin_memory(), b.pin_memory()) for n, (a, b) in host.items()}
+        outs = {p["name"]: torch.empty((p["w"].M, p["w"].N), dtype=torch.float32,
+                                       pin_memory=True) for p in parts}
         h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size()
                   for a, b in pinned.values())
         d2h = sum(p["w"].M * p["w"].N * 4 for p in parts)
         e2e_steps = max(1, min(K, 5))
         for _ in range(2):
             for n, (a, b) in pinned.items():
-                g14.gemm(a, b)
+                g14.gemm(a, b, out=outs[n])
         dist.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             for n, (a, b) in pinned.items():
-                g14.gemm(a, b)
+                g14.gemm(a, b, out=outs[n])
         torch.cuda.synchronize()
         t_e2e = dist.max(time.perf_counter() - t0)
         e2e = {"value": flops_step * e2e_steps * dist.world / t_e2e / 1e12, "unit": UNIT,

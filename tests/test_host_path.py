@@ -1,0 +1,74 @@
+"""GPU tests of the public tensor API's host path: CPU tensors in, the result
+in (pinned) host memory, with row panels pipelined over three streams."""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_14_gb300 as g14
+from dense_gemm_14_gb300 import inputs
+
+from gpu_util import TOL, oracle_check, oracle_check_ex
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("panels", [1, 2, 3, 4, 7])
+def test_panels_bf16_match_the_device_product(panels):
+    """The pair kernel sums every element in k order whatever rows a launch
+    covers: any panel split gives the device product's bits."""
+    M, N, K = 1000, 700, 300
+    A, B = inputs.make(M, N, K, "bf16", "normal", 0.1, seed=41)
+    want = g14.gemm(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    got = g14.gemm(A, B, panels=panels)
+    assert got.device.type == "cpu" and got.is_pinned()
+    assert torch.equal(got, want.cpu())
+
+
+@pytest.mark.parametrize("panels", [1, 4])
+def test_panels_f32_within_bound(oracle_mod, panels):
+    M, N, K = 1100, 600, 257
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=42)
+    out = torch.full((M, N), float("nan"), pin_memory=True)
+    got = g14.gemm(A, B, out=out, panels=panels)
+    assert got.data_ptr() == out.data_ptr()
+    oracle_check(oracle_mod, A, B, got)
+
+
+def test_default_panels_on_a_large_product(oracle_mod):
+    """2048 x 1024 x 1100 takes the pipelined path by default (2 panels)."""
+    M, N, K = 2048, 1024, 1100
+    assert g14.api.host_panels(M, N, K) == 2
+    A, B = inputs.make(M, N, K, "bf16", "normal", 0.03, seed=43)
+    got = g14.gemm(A, B)
+    rows = np.arange(0, M, 37)
+    oracle_check(oracle_mod, A, B, got, rows=rows)
+
+
+def test_host_alpha_beta_and_transposed_views(oracle_mod):
+    M, N, K = 1500, 400, 200
+    A, B = inputs.make(M, N, K, "f32", "normal", 0.3, seed=44)
+    C0 = torch.from_numpy(np.random.default_rng(45).standard_normal((M, N)).astype(np.float32))
+    out = C0.clone().pin_memory()
+    g14.gemm(A, B, out=out, alpha=-2.0, beta=0.5, panels=3)
+    oracle_check_ex(oracle_mod, A, B, out, 0, 0, -2.0, 0.5, C0)
+    # a transposed host view of A: one panel, the same product
+    At = A.t().contiguous()
+    got = g14.gemm(At.t(), B)
+    oracle_check(oracle_mod, A, B, got)
+
+
+def test_host_tf32_mode(oracle_mod):
+    M, N, K = 1200, 512, 320
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=46)
+    got = g14.gemm(A, B, fp32_mode="3xtf32", panels=2)
+    oracle_check(oracle_mod, A, B, got)
+
+
+def test_host_degenerate_sizes():
+    A = torch.zeros((0, 5))
+    B = torch.zeros((5, 3))
+    assert g14.gemm(A, B).shape == (0, 3)
+    A, B = torch.zeros((4, 0)), torch.zeros((0, 3))
+    got = g14.gemm(A, B)
+    assert torch.equal(got, torch.zeros((4, 3)))
