@@ -69,6 +69,8 @@ def parse_args():
     ap.add_argument("--table-tf32", action="store_true",
                     help="time fp32 inputs in every arithmetic (FFMA, TF32, 3xTF32) at 3072^3 "
                          "and 8192^3, one JSON line each")
+    ap.add_argument("--table-only", default=None, metavar="WORKLOAD",
+                    help="with --table: one named workload (for profiling)")
     ap.add_argument("--tf32-only", default=None, metavar="SHAPE:MODE",
                     help="with --table-tf32: one shape (f32_3072 or f32_8192) and one mode "
                          "(fp32, tf32 or 3xtf32), e.g. f32_3072:3xtf32 (for profiling)")
@@ -460,6 +462,8 @@ def run_table(args):
             "f16": g14.GEMM14_DTYPE_F16}
     stream = torch.cuda.current_stream()
     for name, w in inputs.WORKLOADS.items():
+        if args.table_only and name != args.table_only:
+            continue
         _, fl, ib = workload_info(name)
         A, B = inputs.make_workload(name)
         per_set = A.numel() * A.element_size() + B.numel() * B.element_size() + w.M * w.N * 4
