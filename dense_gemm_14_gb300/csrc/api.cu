@@ -184,9 +184,9 @@ int validate(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
 
 int hgemm_bn_for(int64_t N) { return N <= 64 ? 64 : N <= 128 ? 128 : 256; }
 
-// The fp32 kernel's TMA loader serves untransposed operands only; stored
-// transposes go through its cp.async loader. The 16-bit kernels' TMA loaders
-// serve every storage (a transposed operand is an MN-major A or a K-major B).
+// Every kernel's TMA loader serves every storage: a stored transpose is an
+// M-major A or a K-major B in shared memory (the fp32 kernel's thread mapping
+// follows the layout; the tensor-core kernels take either major-ness).
 void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K, const void* A,
               int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
               gemm14_plan* p) {
@@ -217,10 +217,7 @@ void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K
   if (dtype == GEMM14_DTYPE_F32) {
     using S = SgemmShape;
     p->kernel = 1;
-    p->loader = (!transa && !transb && aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 &&
-                 ldb % 4 == 0)
-                    ? 1
-                    : 2;
+    p->loader = (aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 && ldb % 4 == 0) ? 1 : 2;
     p->bm = S::BM;
     p->bn = S::BN;
     p->bk = S::BK;
@@ -402,13 +399,21 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
     schedule(plan, K, dev->sm_count, workspace, workspace_bytes, args, grid);
     if (plan.loader == 2)
       return finish(launch_sgemm_cpasync(args, grid, stream), "sgemm launch", stream);
+    // A stored M x K: box 32 k x 128 m, 128-byte swizzle; stored K x M: box
+    // 128 m x 32 k. B stored K x N: box 256 n x 32 k; stored N x K: box
+    // 32 k x 256 n, 128-byte swizzle.
     CUtensorMap ma, mb;
-    if ((st = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A, M, K, lda, SgemmShape::BK,
-                       SgemmShape::BM, CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
-      return st;
-    if ((st = make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, K, N, ldb, SgemmShape::BN,
-                       SgemmShape::BK, CU_TENSOR_MAP_SWIZZLE_NONE)) != GEMM14_OK)
-      return st;
+    const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    st = transa ? make_map(&ma, f32, 4, A, K, M, lda, SgemmShape::BM, SgemmShape::BK,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)
+                : make_map(&ma, f32, 4, A, M, K, lda, SgemmShape::BK, SgemmShape::BM,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != GEMM14_OK) return st;
+    st = transb ? make_map(&mb, f32, 4, B, N, K, ldb, SgemmShape::BK, SgemmShape::BN,
+                           CU_TENSOR_MAP_SWIZZLE_128B)
+                : make_map(&mb, f32, 4, B, K, N, ldb, SgemmShape::BN, SgemmShape::BK,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != GEMM14_OK) return st;
     return finish(launch_sgemm_tma(ma, mb, args, grid, stream), "sgemm launch", stream);
   }
 

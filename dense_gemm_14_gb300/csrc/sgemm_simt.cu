@@ -12,75 +12,35 @@
 //    Buffering", and of gpu-hpc-book ch.06 "高级 cuda 特性 —— 从矩阵乘法(gemm)说起",
 //    "调度优化" (batching loads along k, asynchronous copies), with a deeper ring.
 //  * Loads: thread 0 issues TMA boxes (A: 32 k x 128 m with the 128-byte
-//    swizzle; B: 256 n x 32 k). When an operand breaks TMA's 16-byte rules all
-//    256 threads fill the very same shared-memory layout with 4-byte cp.async
-//    copies instead. Either way out-of-range elements are zero-filled: the
+//    swizzle; B: 256 n x 32 k; stored transposes in their own layouts, see
+//    Lay below). When an operand breaks TMA's 16-byte rules all 256 threads
+//    fill the untransposed shared-memory layout with 4-byte cp.async copies
+//    instead. Either way out-of-range elements are zero-filled: the
 //    guarded zero-fill of the pages' tiled kernels ("矩阵乘法中的分块与数据复用",
 //    matmul_l1 and matmul_l1_reg).
 //  * Register tiling: each thread owns an 8 x 16 block of C and per k does
-//    8 x 16 FFMAs from 8 A values and 16 B values -- the outer product of the
-//    pages' matmul_l1_reg ("Register Tiling"), grown to a 128 x 256 block tile
-//    and an 8 x 16 microtile so that there are ~21 FFMAs per shared-memory
-//    load instruction.
+//    its 8 x 16 multiply-adds from 8 A values and 16 B values as 64 packed
+//    fp32x2 FMAs (fma.rn.f32x2: two IEEE fp32 FMAs per instruction, each
+//    accumulator summed over k in order, as scalar fmaf would) -- the outer
+//    product of the pages' matmul_l1_reg ("Register Tiling"), grown to a
+//    128 x 256 block tile and an 8 x 16 microtile. The k-block loop is fully
+//    unrolled so the next k group's shared loads overlap this one's FMAs.
 //  * Conflict-free shared memory: A rows are 128 bytes with the 16-byte chunk
 //    index XOR-ed by (row % 8); a warp's A loads touch rows r .. r+3 (distinct
 //    mod 8), so its four distinct 16-byte chunks land in distinct banks. B
 //    rows are read as 8 contiguous float4 per warp (128 bytes). This is the
 //    bank-conflict avoidance of "Kernel 优化指南", "Bank Conflict 避免", done by
-//    swizzling instead of padding.
+//    swizzling instead of padding. Stored transposes keep this property with
+//    their own thread mapping (Lay).
 //  * Epilogue: 16-byte stores when C permits ("向量化加载"), guarded scalar
 //    stores otherwise; each warp store covers 4 rows x 128 contiguous bytes.
 #include "kernels.h"
 #include "ptx.cuh"
 
-// Schedule parameters of the inner loop (defaults are the measured best):
-//   SGEMM_AK      k values per A-fragment load: 4 (float4) or 2 (float2)
-//   SGEMM_UNROLL  unroll factor of the loop over A fragments in a k-block
-//   SGEMM_B_OUTER 0: FFMAs ordered row-major over the 8 x 16 block (A value
-//                 reused across 16 FFMAs); 1: column-major (B value reused)
-#ifndef SGEMM_AK
-#define SGEMM_AK 4
-#endif
-#ifndef SGEMM_UNROLL
-#define SGEMM_UNROLL 8
-#endif
-#ifndef SGEMM_B_OUTER
-#define SGEMM_B_OUTER 0
-#endif
-//   SGEMM_FFMA2   1: packed fp32x2 FMAs (fma.rn.f32x2, two IEEE fp32 FMAs per
-//                 instruction, same rounding as fmaf); 0: scalar fmaf
-#ifndef SGEMM_FFMA2
-#define SGEMM_FFMA2 1
-#endif
-//   SGEMM_PACK_FIRST 1: duplicate all 8 A values of a k step into pairs
-//                 before its packed FMAs; 0: each just before its 8 FMAs
-#ifndef SGEMM_PACK_FIRST
-#define SGEMM_PACK_FIRST 0
-#endif
-#define GEMM14_PRAGMA(x) _Pragma(#x)
-#define GEMM14_UNROLL(n) GEMM14_PRAGMA(unroll n)
-
 namespace gemm14 {
 namespace {
 
 using S = SgemmShape;
-constexpr int kAK = SGEMM_AK;
-static_assert(kAK == 2 || kAK == 4, "A fragments are float2 or float4");
-
-template <int AK> struct AFrag;
-template <> struct AFrag<4> {
-  using T = float4;
-  static __device__ __forceinline__ float get(const float4& v, int kk) {
-    return kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w;
-  }
-};
-template <> struct AFrag<2> {
-  using T = float2;
-  static __device__ __forceinline__ float get(const float2& v, int kk) {
-    return kk == 0 ? v.x : v.y;
-  }
-};
-
 // Two fp32 values in one 64-bit register (low half = first value).
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
   uint64_t r;
@@ -130,7 +90,7 @@ struct TileGrid {
 };
 
 // Loads of flat iteration j (output tile `tile`, k-block kb) into stage j % STAGES.
-template <bool kTma, bool kGeneral>
+template <bool kTma, bool kGeneral, int kLay>
 __device__ __forceinline__ void issue_stage(uint32_t j, int tile, int kb, const TileGrid& grid,
                                             uint8_t* tiles, SgemmSmem& sm,
                                             const CUtensorMap* map_a, const CUtensorMap* map_b,
@@ -145,8 +105,11 @@ __device__ __forceinline__ void issue_stage(uint32_t j, int tile, int kb, const 
   if (kTma) {
     // called by thread 0 only
     mbar_arrive_expect_tx(&sm.full[s], S::STAGE_BYTES);
-    tma_load_2d(a_st, map_a, kb * S::BK, tm * S::BM, &sm.full[s]);
-    tma_load_2d(a_st + S::A_STAGE_BYTES, map_b, tn * S::BN, kb * S::BK, &sm.full[s]);
+    // A stored K x M: box 128 m x 32 k; B stored N x K: box 32 k x 256 n.
+    if (kLay & 1) tma_load_2d(a_st, map_a, tm * S::BM, kb * S::BK, &sm.full[s]);
+    else tma_load_2d(a_st, map_a, kb * S::BK, tm * S::BM, &sm.full[s]);
+    if (kLay & 2) tma_load_2d(a_st + S::A_STAGE_BYTES, map_b, kb * S::BK, tn * S::BN, &sm.full[s]);
+    else tma_load_2d(a_st + S::A_STAGE_BYTES, map_b, tn * S::BN, kb * S::BK, &sm.full[s]);
   } else {
     // called by all threads: 4096 A + 8192 B elements, 48 per thread
     const float* A = static_cast<const float*>(args.A);
@@ -201,15 +164,133 @@ __device__ __forceinline__ void issue_stage(uint32_t j, int tile, int kb, const 
   }
 }
 
+// Shared-memory layouts of the TMA loader for stored transposes. kLay bit 0:
+// A is M-major ([32 k][128 m], 512-byte rows, as TMA writes A stored K x M);
+// bit 1: B is K-major ([256 n][32 k], 128-byte rows with the 128-byte swizzle,
+// as TMA writes B stored N x K). The thread mapping follows the layout so
+// that shared loads stay 16 (or 8) bytes wide and conflict-free:
+//   rows    M-major A: warp_m*32 + tr*8 + i (8 contiguous rows per thread),
+//           else warp_m*32 + tr + 4i;
+//   columns K-major B: warp_n*128 + tc + 8j (16 columns 8 apart: the 8
+//           threads of a row group read 8 rows with distinct swizzled
+//           chunks), else warp_n*128 + 4tc + 32(j/4) + j%4.
+// Accumulator pair p of row i holds columns j = 2p and 2p + 1.
+template <int kLay>
+struct Lay {
+  static constexpr bool AM = (kLay & 1) != 0;
+  static constexpr bool BK = (kLay & 2) != 0;
+  static __device__ __forceinline__ int row(int warp_m, int tr, int i) {
+    return AM ? warp_m * 32 + tr * 8 + i : warp_m * 32 + tr + 4 * i;
+  }
+  static __device__ __forceinline__ int col(int warp_n, int tc, int j) {
+    return BK ? warp_n * 128 + tc + 8 * j : warp_n * 128 + tc * 4 + 32 * (j >> 2) + (j & 3);
+  }
+};
+
+__device__ __forceinline__ float2 lds64(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float comp4(const float4& v, int q) {
+  return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+}
+
+// Four k (group kg of a 32-deep k-block) of the 8 x 16 register tile from a
+// stage in layout kLay: per k, 8 A values (two 16-byte loads for M-major A,
+// else from 16-byte loads along k), 8 column pairs of B (four 16-byte loads
+// along n, or for K-major B sixteen 8-byte loads of two k per column, paired
+// per k), and 64 packed fp32x2 FMAs.
+template <int kLay>
+__device__ __forceinline__ void fma_kgroup(uint32_t a_base, uint32_t b_base, int kg, int warp_m,
+                                           int warp_n, int tr, int tc, uint64_t (&acc2)[8][8]) {
+  using LY = Lay<kLay>;
+  // M-major A: af[2kk + h] = rows 4h .. 4h+3 of this thread at k = 4kg + kk;
+  // else af[i] = row i at k = 4kg .. 4kg+3.
+  float4 af[8];
+  if (LY::AM) {
+    const uint32_t a0 = a_base + static_cast<uint32_t>((warp_m * 32 + tr * 8) * 4);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      af[2 * kk] = lds128(a0 + static_cast<uint32_t>((4 * kg + kk) * 512));
+      af[2 * kk + 1] = lds128(a0 + static_cast<uint32_t>((4 * kg + kk) * 512 + 16));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = LY::row(warp_m, tr, i);
+      af[i] = lds128(a_base + static_cast<uint32_t>(r * 128 + (((kg ^ r) & 7) << 4)));
+    }
+  }
+#pragma unroll
+  for (int kh = 0; kh < 2; ++kh) {
+    float2 bc[16];  // K-major B: column j's values at k = 4kg + 2kh + {0, 1}
+    if (LY::BK) {
+      const uint32_t b0 = b_base + static_cast<uint32_t>((warp_n * 128 + tc) * 128 +
+                                                         (((kg ^ tc) & 7) << 4) + kh * 8);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) bc[j] = lds64(b0 + static_cast<uint32_t>(j * 8 * 128));
+    }
+#pragma unroll
+    for (int kx = 0; kx < 2; ++kx) {
+      const int kk = 2 * kh + kx;
+      uint64_t bp[8];
+      if (LY::BK) {
+#pragma unroll
+        for (int p = 0; p < 8; ++p)
+          bp[p] = pack2(kx ? bc[2 * p].y : bc[2 * p].x, kx ? bc[2 * p + 1].y : bc[2 * p + 1].x);
+      } else {
+        const uint32_t b0 = b_base + static_cast<uint32_t>((4 * kg + kk) * (S::BN * 4) +
+                                                           (warp_n * 128 + tc * 4) * 4);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const float4 v = lds128(b0 + static_cast<uint32_t>(128 * jj));
+          bp[2 * jj] = pack2(v.x, v.y);
+          bp[2 * jj + 1] = pack2(v.z, v.w);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float av = LY::AM ? comp4(af[2 * kk + (i >> 2)], i & 3) : comp4(af[i], kk);
+        const uint64_t a2 = pack2(av, av);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) fma2(acc2[i][p], a2, bp[p]);
+      }
+    }
+  }
+}
+
+template <int kLay>
+__device__ __forceinline__ void fma_kblock(const uint8_t* stage, int warp_m, int warp_n, int tr,
+                                           int tc, uint64_t (&acc2)[8][8]) {
+  const uint32_t a_base = smem_u32(stage);
+  const uint32_t b_base = a_base + S::A_STAGE_BYTES;
+  if constexpr (Lay<kLay>::BK) {
+    // K-major B holds 32 fragment registers per k pair: unrolled, the k
+    // groups' live ranges overlap and it measured 20-25 % slower
+#pragma unroll 1
+    for (int kg = 0; kg < S::BK / 4; ++kg)
+      fma_kgroup<kLay>(a_base, b_base, kg, warp_m, warp_n, tr, tc, acc2);
+  } else {
+    // fully unrolled: the next k group's shared loads overlap this one's
+    // FMAs (5.7 % faster than unrolling by 2, no spills)
+#pragma unroll
+    for (int kg = 0; kg < S::BK / 4; ++kg)
+      fma_kgroup<kLay>(a_base, b_base, kg, warp_m, warp_n, tr, tc, acc2);
+  }
+}
+
 // kSK: the stream-K schedule (segments, workspace partials); without it the
 // schedule is plain data-parallel (tiles w, w+G, ... whole) and none of the
 // stream-K machinery is compiled in. kGeneral: stored transposes (cp.async
 // loader) and the alpha / beta epilogue are read from args; without it the
-// kernel is compiled for untransposed operands and a plain store of C.
-template <bool kTma, bool kSK, bool kGeneral>
+// kernel is compiled for untransposed operands and a plain store of C. kLay
+// (TMA loader only): the stored transposes' shared-memory layouts, above.
+template <bool kTma, bool kSK, bool kGeneral, int kLay>
 __global__ void __launch_bounds__(S::THREADS, 1)
     sgemm_simt_kernel(const __grid_constant__ CUtensorMap map_a,
                       const __grid_constant__ CUtensorMap map_b, const GemmArgs args) {
+  static_assert(kLay == 0 || kTma, "transposed layouts come from the TMA loader");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = align1024(smem_raw);
   SgemmSmem& sm = *reinterpret_cast<SgemmSmem*>(tiles + S::STAGES * S::STAGE_BYTES);
@@ -256,10 +337,10 @@ __global__ void __launch_bounds__(S::THREADS, 1)
   int dp_tile = w, dp_kb = 0;
   auto load = [&](uint32_t j) {
     if (kSK) {
-      issue_stage<kTma, kGeneral>(j, pcur.tile, pcur.kb, tgrid, tiles, sm, &map_a, &map_b, args);
+      issue_stage<kTma, kGeneral, kLay>(j, pcur.tile, pcur.kb, tgrid, tiles, sm, &map_a, &map_b, args);
       pcur.next<true>(sm.sched, G);
     } else {
-      issue_stage<kTma, kGeneral>(j, dp_tile, dp_kb, tgrid, tiles, sm, &map_a, &map_b, args);
+      issue_stage<kTma, kGeneral, kLay>(j, dp_tile, dp_kb, tgrid, tiles, sm, &map_a, &map_b, args);
       if (++dp_kb == L) {
         dp_kb = 0;
         dp_tile += G;
@@ -279,8 +360,6 @@ __global__ void __launch_bounds__(S::THREADS, 1)
   const int warp_n = warp >> 2; // 2 warps along n (128 columns each)
   const int tr = lane >> 3;     // 4 thread rows per warp
   const int tc = lane & 7;      // 8 thread columns per warp
-  const uint32_t a_thread = static_cast<uint32_t>((warp_m * 32 + tr) * 128);
-  const uint32_t b_thread = static_cast<uint32_t>((warp_n * 128 + tc * 4) * 4);
 
   uint32_t it = 0;
   bool ok = true;
@@ -295,116 +374,17 @@ __global__ void __launch_bounds__(S::THREADS, 1)
       kind = kSegFull;
     }
     tgrid.coords(tile, tm, tn);
-#if SGEMM_FFMA2
-    // acc2[i][2*jj + h] holds columns 4*jj + 2*h and 4*jj + 2*h + 1 of row i.
+    // acc2[i][p] holds columns j = 2p and 2p + 1 (Lay<kLay>::col) of row i.
     uint64_t acc2[8][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc2[i][j] = 0ull;
-#else
-    float acc[8][16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 16; ++j) acc[i][j] = 0.f;
-#endif
 
     for (int kb = kb0; kb < kb1; ++kb, ++it) {
       const uint32_t s = it % S::STAGES, ph = (it / S::STAGES) & 1;
       if (!mbar_wait(&sm.full[s], ph, wc)) { ok = false; break; }
-      const uint8_t* a_st = tiles + s * S::STAGE_BYTES + a_thread;
-      const uint8_t* b_st = tiles + s * S::STAGE_BYTES + S::A_STAGE_BYTES + b_thread;
-      GEMM14_UNROLL(SGEMM_UNROLL)
-      for (int kg = 0; kg < S::BK / kAK; ++kg) {
-        // A values for k = kAK*kg .. kAK*kg + kAK-1 of this thread's 8 rows:
-        // 16-byte chunk (kAK*kg)/4, XOR-swizzled by (row % 8) = tr + 4*(i % 2).
-        const int k0 = kg * kAK;
-        const uint32_t x0 = static_cast<uint32_t>((((k0 >> 2) ^ tr) << 4) + (k0 & 3) * 4);
-        const uint32_t x1 = x0 ^ 64u;  // rows with (row % 8) >= 4
-        typename AFrag<kAK>::T a[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          a[i] = *reinterpret_cast<const typename AFrag<kAK>::T*>(a_st + 512 * i +
-                                                                 ((i & 1) ? x1 : x0));
-#if SGEMM_FFMA2
-#pragma unroll
-        for (int kk = 0; kk < kAK; ++kk) {
-          ulonglong2 b[4];  // (cols 4jj, 4jj+1), (cols 4jj+2, 4jj+3)
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-            b[jj] = *reinterpret_cast<const ulonglong2*>(b_st + (k0 + kk) * (S::BN * 4) +
-                                                         128 * jj);
-#if SGEMM_PACK_FIRST || SGEMM_B_OUTER
-          uint64_t a2[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float av = AFrag<kAK>::get(a[i], kk);
-            a2[i] = pack2(av, av);
-          }
-#if SGEMM_B_OUTER
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int i = 0; i < 8; ++i) fma2(acc2[i][2 * jj + h], a2[i], h ? b[jj].y : b[jj].x);
-#else
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              fma2(acc2[i][2 * jj + 0], a2[i], b[jj].x);
-              fma2(acc2[i][2 * jj + 1], a2[i], b[jj].y);
-            }
-#endif
-#else
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float av = AFrag<kAK>::get(a[i], kk);
-            const uint64_t a2 = pack2(av, av);
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              fma2(acc2[i][2 * jj + 0], a2, b[jj].x);
-              fma2(acc2[i][2 * jj + 1], a2, b[jj].y);
-            }
-          }
-#endif
-        }
-#else
-#pragma unroll
-        for (int kk = 0; kk < kAK; ++kk) {
-          float4 b[4];
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-            b[jj] = *reinterpret_cast<const float4*>(b_st + (k0 + kk) * (S::BN * 4) + 128 * jj);
-#if SGEMM_B_OUTER
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float bv = q == 0 ? b[jj].x : q == 1 ? b[jj].y : q == 2 ? b[jj].z : b[jj].w;
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                acc[i][jj * 4 + q] = fmaf(AFrag<kAK>::get(a[i], kk), bv, acc[i][jj * 4 + q]);
-            }
-          }
-#else
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float av = AFrag<kAK>::get(a[i], kk);
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              acc[i][jj * 4 + 0] = fmaf(av, b[jj].x, acc[i][jj * 4 + 0]);
-              acc[i][jj * 4 + 1] = fmaf(av, b[jj].y, acc[i][jj * 4 + 1]);
-              acc[i][jj * 4 + 2] = fmaf(av, b[jj].z, acc[i][jj * 4 + 2]);
-              acc[i][jj * 4 + 3] = fmaf(av, b[jj].w, acc[i][jj * 4 + 3]);
-            }
-          }
-#endif
-        }
-#endif
-      }
+      fma_kblock<kLay>(tiles + s * S::STAGE_BYTES, warp_m, warp_n, tr, tc, acc2);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[s]);
 
@@ -435,26 +415,31 @@ __global__ void __launch_bounds__(S::THREADS, 1)
     // flag w. A HEAD waits for the later workers' flags and reduces the slots
     // w, w+1, ..., head_last in that order into C, a plain loop over the tile
     // with the accumulators no longer live.
-    const int r_loc = warp_m * 32 + tr;   // + 4 i
-    const int c_loc = warp_n * 128 + tc * 4;  // + 32 jj
     if (kSK && kind != kSegFull) {
       // PARTIAL -> slot w; HEAD -> slot G + w (a worker may hold both, and a
       // PARTIAL must survive until its owner has read it).
       float* slot = args.partials +
                     static_cast<size_t>(kind == kSegHead ? args.sk.G + w : w) * (S::BM * S::BN);
+      {
+        using LY = Lay<kLay>;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 8; ++i) {
+          float* srow = slot + LY::row(warp_m, tr, i) * S::BN;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          float4 v;
-#if SGEMM_FFMA2
-          const float2 lo = unpack2(acc2[i][2 * jj]), hi = unpack2(acc2[i][2 * jj + 1]);
-          v = make_float4(lo.x, lo.y, hi.x, hi.y);
-#else
-          v = make_float4(acc[i][jj * 4], acc[i][jj * 4 + 1], acc[i][jj * 4 + 2], acc[i][jj * 4 + 3]);
-#endif
-          __stcg(reinterpret_cast<float4*>(slot + (r_loc + 4 * i) * S::BN + c_loc + 32 * jj), v);
+          for (int p = 0; p < 8; p += 2) {
+            const float2 lo = unpack2(acc2[i][p]), hi = unpack2(acc2[i][p + 1]);
+            if (LY::BK) {
+              __stcg(srow + LY::col(warp_n, tc, 2 * p), lo.x);
+              __stcg(srow + LY::col(warp_n, tc, 2 * p + 1), lo.y);
+              __stcg(srow + LY::col(warp_n, tc, 2 * p + 2), hi.x);
+              __stcg(srow + LY::col(warp_n, tc, 2 * p + 3), hi.y);
+            } else {  // columns 2p .. 2p+3 are consecutive
+              __stcg(reinterpret_cast<float4*>(srow + LY::col(warp_n, tc, 2 * p)),
+                     make_float4(lo.x, lo.y, hi.x, hi.y));
+            }
+          }
         }
+      }
       if (kind == kSegPartial) {
         __syncthreads();
         if (threadIdx.x == 0) flag_publish(args.flags + w, args.epoch);
@@ -509,35 +494,39 @@ __global__ void __launch_bounds__(S::THREADS, 1)
     }
 
     // Epilogue: rows beyond M and columns beyond N are not written.
-    const int row0 = tm * S::BM + r_loc;
-    const int col0 = tn * S::BN + c_loc;
+    {
+      using LY = Lay<kLay>;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int row = row0 + 4 * i;
-      if (row >= M) continue;
-      float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
-#if SGEMM_FFMA2
-      float acc_row[16];
+      for (int i = 0; i < 8; ++i) {
+        const int row = tm * S::BM + LY::row(warp_m, tr, i);
+        if (row >= M) continue;
+        float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
+        float v[16];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float2 v = unpack2(acc2[i][j]);
-        acc_row[2 * j] = v.x;
-        acc_row[2 * j + 1] = v.y;
-      }
-#else
-      const float* acc_row = acc[i];
-#endif
+        for (int p = 0; p < 8; ++p) {
+          const float2 t = unpack2(acc2[i][p]);
+          v[2 * p] = t.x;
+          v[2 * p + 1] = t.y;
+        }
+        if (LY::BK) {
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int col = col0 + 32 * jj;
-        if (args.vec_store && col + 3 < N) {
-          epi_store4<kGeneral>(args, crow + col,
-                     make_float4(acc_row[jj * 4 + 0], acc_row[jj * 4 + 1], acc_row[jj * 4 + 2],
-                                 acc_row[jj * 4 + 3]));
+          for (int j = 0; j < 16; ++j) {
+            const int col = tn * S::BN + LY::col(warp_n, tc, j);
+            if (col < N) epi_store1<kGeneral>(args, crow + col, v[j]);
+          }
         } else {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (col + q < N) epi_store1<kGeneral>(args, crow + col + q, acc_row[jj * 4 + q]);
+          for (int jj = 0; jj < 4; ++jj) {
+            const int col = tn * S::BN + LY::col(warp_n, tc, 4 * jj);
+            if (args.vec_store && col + 3 < N) {
+              epi_store4<kGeneral>(args, crow + col,
+                                   make_float4(v[4 * jj], v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]));
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (col + q < N) epi_store1<kGeneral>(args, crow + col + q, v[4 * jj + q]);
+            }
+          }
         }
       }
     }
@@ -560,7 +549,7 @@ __global__ void __launch_bounds__(S::THREADS, 1)
   }
 }
 
-template <bool kTma, bool kSK, bool kGeneral>
+template <bool kTma, bool kSK, bool kGeneral, int kLay>
 cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
                            const GemmArgs& args, int grid, cudaStream_t stream) {
   static int configured[64] = {0};
@@ -568,13 +557,13 @@ cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(sgemm_simt_kernel<kTma, kSK, kGeneral>,
+    e = cudaFuncSetAttribute(sgemm_simt_kernel<kTma, kSK, kGeneral, kLay>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   CUtensorMap dummy{};
-  sgemm_simt_kernel<kTma, kSK, kGeneral><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(
+  sgemm_simt_kernel<kTma, kSK, kGeneral, kLay><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(
       map_a ? *map_a : dummy, map_b ? *map_b : dummy, args);
   return cudaGetLastError();
 }
@@ -582,9 +571,18 @@ cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
 template <bool kTma, bool kSK>
 cudaError_t launch_epi(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
                        int grid, cudaStream_t stream) {
+  if constexpr (kTma) {
+    if (args.transa || args.transb) {
+      // the TMA loader reads stored transposes in their own layouts
+      const int lay = (args.transa ? 1 : 0) | (args.transb ? 2 : 0);
+      if (lay == 1) return launch_variant<true, kSK, true, 1>(map_a, map_b, args, grid, stream);
+      if (lay == 2) return launch_variant<true, kSK, true, 2>(map_a, map_b, args, grid, stream);
+      return launch_variant<true, kSK, true, 3>(map_a, map_b, args, grid, stream);
+    }
+  }
   if (args.transa || args.transb || args.epi != kEpiStore)
-    return launch_variant<kTma, kSK, true>(map_a, map_b, args, grid, stream);
-  return launch_variant<kTma, kSK, false>(map_a, map_b, args, grid, stream);
+    return launch_variant<kTma, kSK, true, 0>(map_a, map_b, args, grid, stream);
+  return launch_variant<kTma, kSK, false, 0>(map_a, map_b, args, grid, stream);
 }
 
 template <bool kTma>

@@ -209,9 +209,9 @@ int gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int
  * beta == 0: C is not read (NaN or infinity in C does not propagate).
  * K == 0 or alpha == 0: A and B are not read; C becomes beta * C (beta == 1
  * launches nothing, beta == 0 zeroes C).
- * Loaders: 16-bit operands take TMA under the same alignment rules as
- * gemm_bf16_f32acc in either storage; fp32 operands take TMA only when
- * neither is transposed, and the equivalent cp.async loader otherwise.
+ * Loaders: operands take TMA under the same alignment rules as the plain
+ * entry points (16-byte aligned, pitches multiples of 16 bytes) in either
+ * storage, and the equivalent software loader otherwise.
  * workspace / workspace_bytes: as for the *_ws calls (NULL, 0 allowed); the
  * bytes needed do not depend on transa / transb, so
  * gemm14_workspace_bytes(dtype, M, N, K, ...) applies.

@@ -192,13 +192,15 @@ def test_ex_invalid_transpose_flags(lib, ta, tb):
 
 
 def test_ex_plan_loaders(lib):
-    """fp32: stored transposes take the cp.async loader (same tiles); 16-bit:
-    TMA in every storage, pairs included."""
+    """TMA in every storage for aligned operands (same tiles), the software
+    loader for unaligned ones; 16-bit transposes on pairs too."""
     st, nn = g14.plan_ex(F32, 0, 0, 512, 512, 512, P, 512, P, 512, P, 512, 152)
     assert st == 0 and nn.loader == 1
     for ta, tb in ((1, 0), (0, 1), (1, 1)):
         st, p = g14.plan_ex(F32, ta, tb, 512, 512, 512, P, 512, P, 512, P, 512, 152)
-        assert st == 0 and p.loader == 2 and p.tiles == nn.tiles and p.grid == nn.grid
+        assert st == 0 and p.loader == 1 and p.tiles == nn.tiles and p.grid == nn.grid
+        st, p = g14.plan_ex(F32, ta, tb, 512, 512, 512, P, 513, P, 512, P, 512, 152)
+        assert st == 0 and p.loader == 2
         st, p = g14.plan_ex(BF16, ta, tb, 512, 512, 512, P, 512, P, 512, P, 512, 152)
         assert st == 0 and p.loader == 1 and p.kernel == 3
         st, p = g14.plan_ex(F16, ta, tb, 100, 512, 512, P, 512, P, 512, P, 512, 152)
