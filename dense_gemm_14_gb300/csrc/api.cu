@@ -279,12 +279,43 @@ int finish(cudaError_t e, const char* what, cudaStream_t stream) {
 
 // Stream-K workspace the call would use with a workspace (0: it uses none).
 // Tile slots per worker: the fp32 kernel's HEAD keeps its own sums in a
-// second slot; the tensor-core kernel's HEAD adds straight from TMEM.
+// second slot; the tensor-core kernels' HEAD adds straight from TMEM. The
+// pair kernel's worker is a cluster of two SMs with a 256 x 256 tile: one
+// 128 x 256 slot (and flag) per CTA, i.e. per SM, like the one-SM kernels.
 int slots_per_worker(const gemm14_plan& plan) { return plan.kernel == 1 ? 2 : 1; }
 
-size_t workspace_need(const gemm14_plan& plan, int sm_count) {
+// The CTA-pair kernel's split, measured on GB300 against its unsplit run:
+// - between one and two waves of tiles with long k (>= 64 k-blocks a tile):
+//   2304x2560x8192 (1.18 waves) 86 -> 74 us;
+// - beyond two waves it gained nothing (8192^3, 16384x11008x4096: within
+//   1 %) or lost (4096x4096x16384: +21 %: ranges that start mid-tile no
+//   longer sweep k together, so clusters stop sharing A and B in L2);
+// - few tiles split over every cluster made the owner add up to ~19 partial
+//   sums one after another (512x512x16384: no gain): there the workers are
+//   capped at 4 per tile and at ranges of at least 32 k-blocks.
+// Returns the workers (clusters) to split over, or 0 to run unsplit.
+int pair_split_workers(int64_t tiles, int64_t L, int clusters) {
+  if (clusters <= 1 || tiles <= 0) return 0;
+  if (2 * tiles < clusters) {
+    int64_t g = clusters;
+    if (g > 4 * tiles) g = 4 * tiles;
+    if (g > tiles * L / 32) g = tiles * L / 32;
+    return g >= 2 * tiles ? static_cast<int>(g) : 0;
+  }
+  if (tiles > clusters && tiles < 2 * static_cast<int64_t>(clusters) && L >= 64)
+    return clusters;
+  return 0;
+}
+
+size_t workspace_need(const gemm14_plan& plan, int sm_count, int64_t K) {
+  if (plan.tiles > INT32_MAX) return 0;
+  if (plan.kernel == 3) {
+    const int64_t L = (K + PairShape::BK - 1) / PairShape::BK;
+    if (!pair_split_workers(plan.tiles, L, sm_count / 2)) return 0;
+    return streamk_workspace_bytes(sm_count, PairShape::BM / 2, PairShape::BN, 1);
+  }
   if (plan.kernel != 1 && plan.kernel != 2) return 0;
-  if (plan.tiles > INT32_MAX || !stream_k_pays(static_cast<int>(plan.tiles), sm_count)) return 0;
+  if (!stream_k_pays(static_cast<int>(plan.tiles), sm_count)) return 0;
   return streamk_workspace_bytes(sm_count, plan.bm, plan.bn, slots_per_worker(plan));
 }
 
@@ -294,7 +325,7 @@ void schedule(const gemm14_plan& plan, int64_t K, int sm_count, void* workspace,
               size_t workspace_bytes, GemmArgs& args, int& grid) {
   const int tiles = static_cast<int>(plan.tiles);
   const int L = static_cast<int>((K + plan.bk - 1) / plan.bk);
-  const size_t need = workspace_need(plan, sm_count);
+  const size_t need = workspace_need(plan, sm_count, K);
   const bool sk = workspace && need && workspace_bytes >= need;
   if (sk) {
     args.sk = make_stream_k(tiles, L, sm_count, true);
@@ -432,10 +463,33 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
     if ((st = make_maps_16(bf16, transa, transb, M, N, K, A, lda, B, ldb, 128, 128, &ma, &mb)) !=
         GEMM14_OK)
       return st;
-    const int64_t clusters = plan.tiles < pair_clusters ? plan.tiles : pair_clusters;
+    // Data-parallel over min(tiles, clusters) clusters, or with a large
+    // enough workspace stream-K over all co-resident clusters (workers).
+    int clusters = static_cast<int>(plan.tiles < pair_clusters ? plan.tiles : pair_clusters);
+    const int L = static_cast<int>((K + PairShape::BK - 1) / PairShape::BK);
+    const size_t need = workspace_need(plan, dev->sm_count, K);
+    const int workers = pair_split_workers(plan.tiles, L, pair_clusters);
+    if (workspace && need && workspace_bytes >= need && workers > 0) {
+      // every tile split (fewer than two waves): dp_tiles = 0
+      args.sk = StreamK{static_cast<int>(plan.tiles), L, workers, 0};
+      args.flags = static_cast<unsigned*>(workspace);
+      args.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                               streamk_flag_bytes(dev->sm_count));
+      args.epoch = next_epoch();
+      clusters = args.sk.G;
+    } else {
+      args.sk = make_stream_k(static_cast<int>(plan.tiles), L, clusters, false);
+    }
+    // C for the TMA-store epilogue (plain stores into a 16-byte-aligned C):
+    // box 32 columns x 32 rows of fp32 with the 128-byte swizzle.
+    CUtensorMap mc{};
+    if (epi == kEpiStore && !transa && !transb && plan.vec_store &&
+        (st = make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, ldc, 32, 32,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
+      return st;
     const uint32_t idesc2 =
         idesc_f16_f32acc(bf16, PairShape::BM, PairShape::BN, transa != 0, transb == 0);
-    return finish(launch_hgemm_tc_pair(ma, mb, args, idesc2, static_cast<int>(clusters), stream),
+    return finish(launch_hgemm_tc_pair(ma, mb, mc, args, idesc2, clusters, stream),
                   "hgemm pair launch", stream);
   }
   if (plan.kernel == 3)
@@ -536,7 +590,7 @@ size_t gemm14_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int sm
     return 0;
   gemm14_plan plan;
   plan_for(dtype, M, N, K, p, lda, p, ldb, p, ldb, sm_count, &plan);
-  return workspace_need(plan, sm_count);
+  return workspace_need(plan, sm_count, K);
 }
 
 const char* gemm14_status_string(int status) {
@@ -680,7 +734,9 @@ extern "C" int gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K, const v
   if ((st = current_device(&dev)) != GEMM14_OK) return st;
   gemm14_plan plan;
   plan_for(GEMM14_DTYPE_BF16, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
-  const size_t need = workspace_need(plan, dev->sm_count);
+  // The CTA-pair kernel's split (about 20 MB on 152 SMs) is not offered here:
+  // wide products run unsplit, as gemm_bf16_f32acc runs them.
+  const size_t need = plan.kernel == 3 ? 0 : workspace_need(plan, dev->sm_count, K);
   if (need > kNoAllocScratchBytes) {
     std::snprintf(t_last_error, sizeof t_last_error,
                   "gemm_bf16_f32acc_noalloc: this product needs %zu bytes of scratch, more than "

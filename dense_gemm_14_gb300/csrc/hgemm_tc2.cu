@@ -38,9 +38,13 @@ struct PairSmem {
   uint64_t acc_full[2];       // each CTA: accumulator b holds a finished tile
   uint64_t acc_empty[2];      // leader: all 8 epilogue warps drained accumulator b
   uint64_t drain;
+  uint64_t partial_stored;    // stream-K: this CTA's 4 epilogue warps stored its partial
+  uint64_t flags_ready;       // stream-K: the later workers' partials are published
   uint32_t tmem_base;
   int abort_flag;
+  SkTable sched;              // stream-K: this cluster's segments, decoded once
 };
+static_assert(sizeof(PairSmem) <= 256, "barrier block of the pair kernel");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -62,16 +66,23 @@ __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n
 // kGeneral: stored transposes and the alpha / beta epilogue are read from
 // args; without it the kernel is compiled for untransposed operands and a
 // plain store of C (the common case, with nothing decided at run time).
-template <bool kGeneral>
+// kSK: the stream-K schedule (streamk.cuh) with a cluster as the worker:
+// both CTAs of a cluster walk the same segments; each CTA stores the partial
+// sums of its 128 rows to its own workspace slot (worker w, rank r: slot
+// 2w + r, flag 2w + r), and the owner of a split tile adds, per CTA, the same
+// rank's partials of the later workers in worker order.
+template <bool kGeneral, bool kSK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
     hgemm_tc2_kernel(const __grid_constant__ CUtensorMap map_a,
-                     const __grid_constant__ CUtensorMap map_b, const GemmArgs args,
+                     const __grid_constant__ CUtensorMap map_b,
+                     const __grid_constant__ CUtensorMap map_c, const GemmArgs args,
                      const uint32_t idesc) {
   const int transa = kGeneral ? args.transa : 0;
   const int transb = kGeneral ? args.transb : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = align1024(smem_raw);
-  PairSmem& sm = *reinterpret_cast<PairSmem*>(tiles + P::STAGES * P::STAGE_BYTES + P::GUARD_BYTES);
+  uint8_t* out_stage = tiles + P::STAGES * P::STAGE_BYTES;  // epilogue staging for C
+  PairSmem& sm = *reinterpret_cast<PairSmem*>(out_stage + P::OUT_BYTES);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -99,10 +110,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
       mbar_init(&sm.acc_empty[b], 8);
     }
     mbar_init(&sm.drain, 1);
+    mbar_init(&sm.partial_stored, 4);
+    mbar_init(&sm.flags_ready, 1);
     sm.abort_flag = 0;
+    if (kSK) {
+      sm.sched.fill(args.sk, cid);
+      if (sm.sched.n_sk > kMaxSk) {  // cannot happen for schedules make_stream_k builds
+        atomicOr(args.err, kDevErrBadConfig);
+        sm.abort_flag = 1;
+      }
+    }
     fence_barrier_init();
     tma_prefetch_desc(&map_a);
     tma_prefetch_desc(&map_b);
+    if (!kGeneral && args.vec_store) tma_prefetch_desc(&map_c);
   }
   // Both CTAs' barriers exist before either CTA signals the other's.
   cluster_sync();
@@ -114,15 +135,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = sm.tmem_base;
+  // Both CTAs of a cluster decoded the same table: a pair that gave up at
+  // set-up (abort) runs no segment in either CTA.
+  const int n_seg = kSK ? (sm.abort_flag ? 0 : sm.sched.segments())
+                        : (cid < num_tiles ? (num_tiles - 1 - cid) / ncl + 1 : 0);
+  // Segment i: data-parallel tile cid + i * ncl whole, or the decoded table.
+  auto segment = [&](int i, int& tile, int& kb0, int& kb1, int& kind) {
+    if (kSK) {
+      sm.sched.get(i, tile, kb0, kb1, kind);
+    } else {
+      tile = cid + i * ncl;
+      kb0 = 0;
+      kb1 = kblocks;
+      kind = kSegFull;
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = true;
-      for (int t = cid; t < num_tiles && ok; t += ncl) {
-        int tm, tn;
+      for (int seg = 0; seg < n_seg && ok; ++seg) {
+        int t, kb0, kb1, kind, tm, tn;
+        segment(seg, t, kb0, kb1, kind);
         pair_tile_coords(t, tiles_m, tiles_n, tm, tn);
-        for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++prod_it) {
           const uint32_t s = prod_it % P::STAGES, ph = (prod_it / P::STAGES) & 1;
           if (!mbar_wait(&sm.empty[s], ph ^ 1, wc)) { ok = false; break; }
           // Failure-detection tests: the first stage is never loaded.
@@ -161,14 +198,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
       const OperandDesc b_op = operand_desc(transb != 0);
       bool ok = true;
       uint32_t it = 0;
-      int local = 0;
-      for (int t = cid; t < num_tiles && ok; t += ncl, ++local) {
-        const int b = local & 1;
-        const uint32_t aph = (local >> 1) & 1;
+      for (int seg = 0; seg < n_seg && ok; ++seg) {
+        int t, kb0, kb1, kind;
+        segment(seg, t, kb0, kb1, kind);
+        const int b = seg & 1;
+        const uint32_t aph = (seg >> 1) & 1;
         if (!mbar_wait_cluster(&sm.acc_empty[b], aph ^ 1, wc)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * P::BN);
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const uint32_t s = it % P::STAGES, ph = (it / P::STAGES) & 1;
           if (!mbar_wait(&sm.full[s], ph, wc)) { ok = false; break; }
           tc_fence_after_sync();
@@ -180,7 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
             // layout in both CTAs.
             const uint64_t a_desc = smem_desc_sw128(a_addr + kk * a_op.step, a_op.lbo, 1024);
             const uint64_t b_desc = smem_desc_sw128(b_addr + kk * b_op.step, b_op.lbo, 1024);
-            tc_mma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0);
+            tc_mma_f16_pair(d_tmem, a_desc, b_desc, idesc, kb > kb0 || kk != 0);
           }
           mma_issued = true;
           tc_commit_pair_multicast(&sm.empty[s], 0x3);
@@ -191,31 +229,113 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Thread = one row of the CTA's 128 (TMEM lane), 32 columns per chunk.
+    // The plain variant with a 16-byte-aligned C stages each warp's 32 x 32
+    // block in shared memory (128-byte swizzle: a row's 16-byte pieces spread
+    // over all banks) and writes it with one TMA store; two buffers per warp
+    // let the next chunk overlap the store. Otherwise each thread stores its
+    // row segment directly (the alpha / beta modes read C there).
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r_loc = q * 32 + lane;  // this thread's row within the CTA's 128
     const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&sm.acc_empty[0]), 0);
     const uint32_t acc_empty_leader1 = mapa_shared(smem_u32(&sm.acc_empty[1]), 0);
-    int local = 0;
-    for (int t = cid; t < num_tiles; t += ncl, ++local) {
-      int tm, tn;
+    const int w = cid;
+    const bool tma_c = !kGeneral && args.vec_store;
+    uint8_t* out_buf = out_stage + q * 2 * P::OUT_BUF_BYTES;
+    int ob = 0;
+    // Stream-K slot of worker c for this CTA (128 rows x 256 fp32), laid out
+    // chunk by chunk as [chunk][float4 v][row]: the 32 rows of a warp store
+    // (and load) 512 contiguous bytes per instruction.
+    auto slot4 = [&](int c, int chunk, int v) {
+      return reinterpret_cast<float4*>(args.partials) +
+             (static_cast<size_t>(2 * c + rank) * (P::BN / 32) + chunk) * 8 * 128 +
+             static_cast<size_t>(v) * 128 + r_loc;
+    };
+    for (int seg = 0; seg < n_seg; ++seg) {
+      int t, kb0, kb1, kind, tm, tn;
+      segment(seg, t, kb0, kb1, kind);
       pair_tile_coords(t, tiles_m, tiles_n, tm, tn);
-      const int b = local & 1;
-      const uint32_t aph = (local >> 1) & 1;
+      const int b = seg & 1;
+      const uint32_t aph = (seg >> 1) & 1;
       int got = 1;
       if (lane == 0) got = mbar_wait(&sm.acc_full[b], aph, wc) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
+      if (kSK && kind == kSegHead) {
+        // Wait for the later workers holding the rest of this tile (one lane
+        // of warp 2 polls their flags for this CTA's rank; the other warps
+        // wait on flags_ready). A worker has at most one HEAD segment.
+        if (warp == 2 && lane == 0) {
+          bool all = true;
+          for (int c = w + 1; c <= sm.sched.head_last && all; ++c)
+            all = flag_wait(args.flags + 2 * c + rank, args.epoch, wc);
+          if (all) mbar_arrive(&sm.flags_ready);
+        }
+        if (lane == 0) got = mbar_wait(&sm.flags_ready, 0, wc) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) break;
+      }
       tc_fence_after_sync();
-      const int row = tm * P::BM + static_cast<int>(rank) * 128 + q * 32 + lane;
+      const int row0 = tm * P::BM + static_cast<int>(rank) * 128 + q * 32;  // the warp's rows
+      const int row = row0 + lane;
       float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(b * P::BN);
 #pragma unroll 1
       for (int c = 0; c < P::BN / 32; ++c) {
+        // HEAD: fetch the first contributor's partial of this chunk before the
+        // TMEM read so that the two latencies overlap.
+        float4 pre[8];
+        if (kSK && kind == kSegHead && sm.sched.head_last > w) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v) pre[v] = __ldcg(slot4(w + 1, c, v));
+        }
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tc_wait_ld();
+        if (kSK && kind == kSegPartial) {
+          // Stream-K: this CTA's partial sums of the tile go to its slot.
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            __stcg(slot4(w, c, v),
+                   make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                               __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+          continue;
+        }
+        if (kSK && kind == kSegHead) {
+          // Add the later workers' partial sums, in worker order.
+          for (int cw = w + 1; cw <= sm.sched.head_last; ++cw) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const float4 p = cw == w + 1 ? pre[v] : __ldcg(slot4(cw, c, v));
+              r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + p.x);
+              r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + p.y);
+              r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + p.z);
+              r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + p.w);
+            }
+          }
+        }
         const int col0 = tn * P::BN + c * 32;
-        if (row < M) {
+        if (tma_c) {
+          // The buffer's store of two chunks ago has been read out.
+          uint8_t* buf = out_buf + ob * P::OUT_BUF_BYTES;
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          const uint32_t rb = smem_u32(buf) + static_cast<uint32_t>(lane * 128);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             rb + static_cast<uint32_t>(((v ^ lane) & 7) << 4)),
+                         "r"(r[4 * v + 0]), "r"(r[4 * v + 1]), "r"(r[4 * v + 2]), "r"(r[4 * v + 3])
+                         : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&map_c, buf, col0, row0);
+            bulk_commit();
+          }
+          ob ^= 1;
+        } else if (row < M) {
           if (args.vec_store && col0 + 32 <= N) {
 #pragma unroll
             for (int v = 0; v < 8; ++v)
@@ -232,7 +352,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(b ? acc_empty_leader1 : acc_empty_leader0);
+      if (kSK && kind == kSegPartial) {
+        // All four warps' partial stores precede the flag. A worker has at
+        // most one PARTIAL segment: the barrier's first phase.
+        if (lane == 0) mbar_arrive(&sm.partial_stored);
+        if (warp == 2 && lane == 0 && mbar_wait(&sm.partial_stored, 0, wc))
+          flag_publish(args.flags + 2 * w + rank, args.epoch);
+      }
     }
+    // The TMA stores have finished (their reads of the staging buffers, and
+    // their writes) before the CTA may exit.
+    if (tma_c && lane == 0) bulk_wait_all();
   }
 
   // Teardown. On abort, the leader lets its issued MMAs and both CTAs' loads
@@ -259,6 +389,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
   }
 }
 
+template <bool kGeneral, bool kSK>
+cudaError_t set_pair_smem() {
+  return cudaFuncSetAttribute(hgemm_tc2_kernel<kGeneral, kSK>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES);
+}
+
 }  // namespace
 
 int pair_max_clusters() {
@@ -267,31 +403,42 @@ int pair_max_clusters() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (have[dev]) return cached[dev];
-  if (cudaFuncSetAttribute(hgemm_tc2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           P::SMEM_BYTES) != cudaSuccess ||
-      cudaFuncSetAttribute(hgemm_tc2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           P::SMEM_BYTES) != cudaSuccess)
+  if (set_pair_smem<false, false>() != cudaSuccess || set_pair_smem<true, false>() != cudaSuccess ||
+      set_pair_smem<false, true>() != cudaSuccess || set_pair_smem<true, true>() != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(P::THREADS, 1, 1);
   cfg.dynamicSmemBytes = P::SMEM_BYTES;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2_kernel<false>, &cfg) != cudaSuccess) n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2_kernel<false, false>, &cfg) != cudaSuccess)
+    n = 0;
   cached[dev] = n;
   have[dev] = true;
   return n;
 }
 
 cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
-                                 const GemmArgs& args, uint32_t idesc, int clusters,
-                                 cudaStream_t stream) {
-  if (args.transa || args.transb || args.epi != kEpiStore)
-    hgemm_tc2_kernel<true><<<2 * clusters, P::THREADS, P::SMEM_BYTES, stream>>>(map_a, map_b,
-                                                                              args, idesc);
-  else
-    hgemm_tc2_kernel<false><<<2 * clusters, P::THREADS, P::SMEM_BYTES, stream>>>(map_a, map_b,
-                                                                               args, idesc);
+                                 const CUtensorMap& map_c, const GemmArgs& args, uint32_t idesc,
+                                 int clusters, cudaStream_t stream) {
+  const bool general = args.transa || args.transb || args.epi != kEpiStore;
+  const bool sk = args.sk.dp_tiles < args.sk.tiles;
+  const dim3 grid(2 * clusters), block(P::THREADS);
+  if (sk) {
+    if (general)
+      hgemm_tc2_kernel<true, true><<<grid, block, P::SMEM_BYTES, stream>>>(map_a, map_b, map_c,
+                                                                           args, idesc);
+    else
+      hgemm_tc2_kernel<false, true><<<grid, block, P::SMEM_BYTES, stream>>>(map_a, map_b, map_c,
+                                                                            args, idesc);
+  } else {
+    if (general)
+      hgemm_tc2_kernel<true, false><<<grid, block, P::SMEM_BYTES, stream>>>(map_a, map_b, map_c,
+                                                                            args, idesc);
+    else
+      hgemm_tc2_kernel<false, false><<<grid, block, P::SMEM_BYTES, stream>>>(map_a, map_b, map_c,
+                                                                             args, idesc);
+  }
   return cudaGetLastError();
 }
 

@@ -120,17 +120,23 @@ struct PairShape {
   static constexpr int A_BYTES = 128 * BK * 2;      // this CTA's 128 rows of A
   static constexpr int B_BYTES = BK * 128 * 2;      // this CTA's 128 columns of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int GUARD_BYTES = 16384;         // slack past the last stage
+  // epilogue staging for TMA stores of C: per epilogue warp two buffers of
+  // 32 rows x 32 fp32 columns (4 KB each)
+  static constexpr int OUT_BUF_BYTES = 32 * 32 * 4;
+  static constexpr int OUT_BYTES = 4 * 2 * OUT_BUF_BYTES;
   static constexpr int TMEM_COLS = 512;             // two 128-lane x 256-column accumulators
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + GUARD_BYTES + 256 + 1024;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 256 + 1024;
 };
 
 // Clusters of two that fit at once on the current device (0: the pair kernel
 // cannot run). The first call per device also sets the kernel's smem limit.
 int pair_max_clusters();
+// map_c: C as a 2-D fp32 tensor (box 32 columns x 32 rows, 128-byte swizzle)
+// for the TMA-store epilogue of the plain variant when C takes 16-byte stores
+// (args.vec_store); otherwise unused.
 cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
-                                 const GemmArgs& args, uint32_t idesc, int clusters,
-                                 cudaStream_t stream);
+                                 const CUtensorMap& map_c, const GemmArgs& args, uint32_t idesc,
+                                 int clusters, cudaStream_t stream);
 
 // Same kernel with the software loader (operands TMA cannot address).
 cudaError_t launch_hgemm_tc_soft(int bn, const GemmArgs& args, uint32_t idesc, int grid,

@@ -194,6 +194,8 @@ static __device__ __noinline__ bool flag_wait(const unsigned* flag, unsigned val
       if (globaltimer_ns() - t0 > w.limit_ns) {
         atomicOr(w.err, kDevErrTimeout);
         *w.abort_flag = 1;
+        if (w.peer_abort)
+          asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(w.peer_abort), "r"(1u) : "memory");
         return false;
       }
     }
@@ -228,6 +230,29 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr)
       : "memory");
+}
+
+// 2-D tiled TMA store of one box from shared memory to (x, y); out-of-range
+// parts of the box are not written. Bulk-group completion: commit, then wait
+// until at most N of this thread's groups still read shared memory (the
+// buffer may be rewritten) or, with wait_all, until every group is done.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src,
+                                             int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(smem_u32(smem_src))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- cp.async

@@ -141,8 +141,8 @@ int gemm_f32_3xtf32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda
  * tile's k-blocks in one run). With workspace == NULL, a smaller workspace, a
  * product whose tiles fill whole waves, or one with between half and all of
  * a wave of tiles (where splitting measured slower), the call is exactly the
- * plain entry point. The CTA-pair kernel (wide 16-bit products) does not use
- * a workspace.
+ * plain entry point. The CTA-pair kernel (wide 16-bit products) splits in the
+ * same way with a cluster of two SMs as the worker.
  * workspace: 16-byte aligned (else GEMM14_ERR_INVALID_ARG), zero-filled
  * before its first use. Its first bytes (one 4-byte word per SM, rounded up
  * to 256 bytes) hold publication flags that only ever contain zero or the
@@ -225,9 +225,8 @@ int gemm14_gemm_ex(int dtype, int transa, int transb, int64_t M, int64_t N, int6
 /*
  * Workspace bytes that let the *_ws call of this dtype and shape use the
  * stream-K schedule on a GPU with sm_count SMs (sm_count <= 0: the current
- * device's). 0 means the call would not split tiles (whole waves, between
- * half and one wave of tiles, or the CTA-pair kernel) or the arguments are
- * invalid. Assumes operands
+ * device's). 0 means the call would not split tiles (whole waves, or
+ * between half and one wave of tiles) or the arguments are invalid. Assumes operands
  * TMA can address (16-byte aligned, pitches multiple of 16 bytes).
  */
 size_t gemm14_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int sm_count);

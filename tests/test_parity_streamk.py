@@ -102,3 +102,55 @@ def test_workspace_reused_across_shapes(oracle_mod):
         A, B = inputs.make(M, N, K, dt, "uniform", 1.0, seed=40 + i)
         C = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), workspace=ws)
         oracle_check(oracle_mod, A, B, C)
+
+
+# ------------------------------------------------------------------ CTA pairs (cluster workers)
+
+PAIR_CASES = [(512, 512, 16384),    # 4 pair tiles: 4 workers per tile
+              (2304, 2560, 8192),   # 90 tiles, 1.2 waves: every tile split
+              (2304, 2560, 4100)]   # the same with a ragged last k-block
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", PAIR_CASES)
+def test_pair_streamk(oracle_mod, dt, M, N, K):
+    A, B = inputs.make(M, N, K, dt, "normal", 1.0 / K ** 0.5, seed=M + 2 * N + K)
+    st, plan = g14.plan(g14.GEMM14_DTYPE_BF16, M, N, K, 1 << 16, rup(K, 8), 1 << 16, rup(N, 8),
+                        1 << 16, N, 152)
+    assert plan.kernel == 3
+    ws = make_workspace(dt, M, N, K)
+    assert ws.numel() > 256, "this shape must take the stream-K schedule"
+    C1 = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), ldc=N, workspace=ws)
+    oracle_check(oracle_mod, A, B, C1, rows=np.arange(0, M, 7) if M * N * K > 3e9 else None)
+    C2 = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), ldc=N, workspace=ws)  # next epoch
+    assert torch.equal(C1, C2)
+
+
+def test_pair_streamk_integer_exact_and_ex_modes(oracle_mod):
+    """Integer inputs stay exact whatever the split; transposes and alpha /
+    beta apply once, where a tile is finished."""
+    from gpu_util import oracle_check_ex, run_ex
+    M, N, K = 512, 520, 16384
+    Ai, Bi = inputs.make_integer(M, N, K, 3, "bf16", seed=61)
+    want = (Ai.double() @ Bi.double()).float()
+    ws = make_workspace("bf16", M, N, K)
+    assert torch.equal(run_abi(Ai, Bi, lda=rup(K, 8), ldb=rup(N, 8), workspace=ws), want)
+    A, B = inputs.make(M, N, K, "bf16", "uniform", 0.05, seed=62)
+    C0 = torch.from_numpy(np.random.default_rng(63).standard_normal((M, N)).astype(np.float32))
+    for ta, tb in ((0, 0), (1, 0), (0, 1), (1, 1)):
+        C = run_ex(A, B, ta, tb, -0.5, 2.0, C0, lda=rup(K if not ta else M, 8),
+                   ldb=rup(N if not tb else K, 8), workspace=ws)
+        oracle_check_ex(oracle_mod, A, B, C, ta, tb, -0.5, 2.0, C0)
+
+
+def test_pair_streamk_expired_wait_reports_timeout(oracle_mod):
+    M, N, K = 512, 512, 8192
+    A, B = inputs.make(M, N, K, "bf16", "uniform", 1.0, seed=65)
+    ws = make_workspace("bf16", M, N, K)
+    s = torch.cuda.current_stream()
+    assert g14.check_device_error(s.cuda_stream) == 0
+    g14.debug_inject(1, 20_000_000)
+    run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), workspace=ws, check_err=False)
+    assert g14.check_device_error(s.cuda_stream) == _lib.GEMM14_ERR_TIMEOUT
+    C = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), workspace=ws)
+    oracle_check(oracle_mod, A, B, C)

@@ -32,8 +32,17 @@ def test_workspace_bytes():
     assert g14.workspace_bytes(BF16, 16384, 64, 4096, 152) == 0
     # few tiles (fewer than half a wave): split, one 128 x 64 slot per worker
     assert g14.workspace_bytes(BF16, 1024, 64, 4096, 152) == 768 + 152 * 128 * 64 * 4
-    # the CTA-pair kernel uses none; whole waves use none; invalid args -> 0
+    # the CTA-pair kernel (a cluster of two per worker): one 128 x 256 slot per
+    # SM when it splits -- between one and two waves with long k (90 tiles on
+    # 76 clusters), or few tiles with long k (4 tiles, 16 workers) ...
+    pair_ws = 768 + 152 * 128 * 256 * 4
+    assert g14.workspace_bytes(BF16, 2304, 2560, 8192, 152) == pair_ws
+    assert g14.workspace_bytes(BF16, 512, 512, 16384, 152) == pair_ws
+    # ... and not beyond two waves (8192^3: 13.47 waves), nor with short k
     assert g14.workspace_bytes(BF16, 8192, 8192, 8192, 152) == 0
+    assert g14.workspace_bytes(BF16, 2304, 2560, 2000, 152) == 0
+    assert g14.workspace_bytes(BF16, 1000, 776, 1000, 152) == 0
+    # whole waves use none; invalid args -> 0
     assert g14.workspace_bytes(F32, 128 * 152, 256, 64, 152) == 0
     assert g14.workspace_bytes(F32, -1, 4, 4, 152) == 0
 

@@ -55,9 +55,13 @@ def test_no_alloc_matches_allocating_entry_point(oracle_mod, M, N, K):
 
 
 def test_no_alloc_without_scratch_is_the_plain_product():
-    # a wide product runs on the CTA-pair kernel, which needs no scratch
+    # a wide product runs on the CTA-pair kernel; the no-alloc entry runs it
+    # unsplit (its split would need more than the built-in scratch), exactly
+    # as gemm_bf16_f32acc does
     A, B = inputs.make(512, 512, 512, "bf16", "normal", 0.05, seed=7)
-    assert g14.workspace_bytes(g14.GEMM14_DTYPE_BF16, 512, 512, 512, 0) == 0
+    st, plan = g14.plan(g14.GEMM14_DTYPE_BF16, 512, 512, 512, 1 << 16, 512, 1 << 16, 512,
+                        1 << 16, 512, 0 or 152)
+    assert st == 0 and plan.kernel == 3
     _, want = _run(g14.gemm_bf16_f32acc, A, B)
     st, got = _run(g14.gemm_bf16_f32acc_noalloc, A, B)
     assert st == 0 and torch.equal(got, want)
