@@ -307,6 +307,24 @@ int pair_split_workers(int64_t tiles, int64_t L, int clusters) {
   return 0;
 }
 
+// The one-SM kernels' split: the workers to spread the k-blocks over, or 0 to
+// run data-parallel. fp32 k-blocks are long (a 128 x 256 x 32 block is about
+// 2 MFLOP of FFMA work), so every SM takes a range. A 16-bit k-block streams
+// 24-48 KB in well under a microsecond, while each further worker adds a
+// partial sum that the tile's owner reads back; measured on GB300 (bf16,
+// N = 64 or 128, K = 4096-16384), the best split had about 4 workers per tile
+// and ranges of 16 or more k-blocks: 128x64x4096 25.0 us unsplit, 20.7 us on
+// 4 workers, 150 us on 64; 512x128x8192 45.2 us unsplit, 33.0 us on 16, 153 us
+// on 152.
+int one_sm_split_workers(int kernel, int64_t tiles, int64_t L, int G) {
+  if (tiles <= 0 || tiles > INT32_MAX || !stream_k_pays(static_cast<int>(tiles), G)) return 0;
+  if (kernel == 1 || 2 * tiles >= G) return G;
+  int64_t g = G;
+  if (g > 4 * tiles) g = 4 * tiles;
+  if (g > tiles * L / 16) g = tiles * L / 16;
+  return g >= 2 * tiles ? static_cast<int>(g) : 0;
+}
+
 size_t workspace_need(const gemm14_plan& plan, int sm_count, int64_t K) {
   if (plan.tiles > INT32_MAX) return 0;
   if (plan.kernel == 3) {
@@ -315,7 +333,8 @@ size_t workspace_need(const gemm14_plan& plan, int sm_count, int64_t K) {
     return streamk_workspace_bytes(sm_count, PairShape::BM / 2, PairShape::BN, 1);
   }
   if (plan.kernel != 1 && plan.kernel != 2) return 0;
-  if (!stream_k_pays(static_cast<int>(plan.tiles), sm_count)) return 0;
+  const int64_t L = (K + plan.bk - 1) / plan.bk;
+  if (!one_sm_split_workers(plan.kernel, plan.tiles, L, sm_count)) return 0;
   return streamk_workspace_bytes(sm_count, plan.bm, plan.bn, slots_per_worker(plan));
 }
 
@@ -328,7 +347,8 @@ void schedule(const gemm14_plan& plan, int64_t K, int sm_count, void* workspace,
   const size_t need = workspace_need(plan, sm_count, K);
   const bool sk = workspace && need && workspace_bytes >= need;
   if (sk) {
-    args.sk = make_stream_k(tiles, L, sm_count, true);
+    args.sk = make_stream_k(tiles, L, one_sm_split_workers(plan.kernel, tiles, L, sm_count),
+                            true);
     // Flags first (a fixed region), then the slots; sk.G <= sm_count.
     args.flags = static_cast<unsigned*>(workspace);
     args.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) +

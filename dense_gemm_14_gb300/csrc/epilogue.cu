@@ -4,6 +4,7 @@
 // A memory-bound pass: each C element is read and written once, with
 // 16-byte accesses in rows whose start and pitch allow them.
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace gemm14 {
 namespace {
@@ -11,6 +12,8 @@ namespace {
 // Grid-stride over rows; the threads of a block cover a row's columns.
 __global__ void __launch_bounds__(256) scale_c_kernel(float* C, int64_t ldc, int M, int N,
                                                       float beta, int vec) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
     float* c = C + row * ldc;
     if (vec) {
@@ -35,8 +38,7 @@ cudaError_t launch_scale_c(float* C, int64_t ldc, int M, int N, float beta, int 
   const int vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
   const int64_t cap = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 8;
   const int grid = static_cast<int>(M < cap ? M : cap);
-  scale_c_kernel<<<grid, 256, 0, stream>>>(C, ldc, M, N, beta, vec);
-  return cudaGetLastError();
+  return launch_kernel(scale_c_kernel, dim3(grid), dim3(256), 0, stream, C, ldc, M, N, beta, vec);
 }
 
 }  // namespace gemm14

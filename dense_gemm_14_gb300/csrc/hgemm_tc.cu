@@ -128,6 +128,43 @@ __device__ __forceinline__ void soft_load_stage(uint8_t* a_st, const GemmArgs& a
     soft_mnmajor<BN>(b_st, B, args.ldb, tn * BN, args.N, k0, args.K, lane);
 }
 
+// Stream-K fixup: a tile's owner reads the partial sums of its later workers
+// kPre at a time. Workspace slot cw holds worker cw's 128 x BN partial tile,
+// row-major; this thread's row is r_loc and its chunk the 32 columns from
+// 32 c. Loads of n (<= kPre) consecutive workers from cw0, all issued before
+// any is used.
+constexpr int kPre = 4;
+
+template <int BN>
+__device__ __forceinline__ void load_partials(float4 (&p)[kPre][8], const float* partials, int cw0,
+                                              int n, int r_loc, int c) {
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    if (j < n) {
+      const float* src =
+          partials + (static_cast<size_t>(cw0 + j) * H::BM + r_loc) * BN + c * 32;
+#pragma unroll
+      for (int v = 0; v < 8; ++v) p[j][v] = __ldcg(reinterpret_cast<const float4*>(src + 4 * v));
+    }
+  }
+}
+
+// r += p[0] + ... + p[n-1], one worker after another (a fixed order).
+__device__ __forceinline__ void add_partials(uint32_t (&r)[32], const float4 (&p)[kPre][8], int n) {
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    if (j < n) {
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + p[j][v].x);
+        r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + p[j][v].y);
+        r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + p[j][v].z);
+        r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + p[j][v].w);
+      }
+    }
+  }
+}
+
 // kSK: the stream-K schedule (segments, workspace partials); without it the
 // schedule is plain data-parallel and none of the stream-K code is compiled in.
 // kGeneral: stored transposes and the alpha / beta epilogue are read from
@@ -193,6 +230,12 @@ __global__ void __launch_bounds__(H::THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // Everything above touched only shared memory, TMEM and the kernel's
+  // parameters (and, on a bad schedule, OR-ed a bit into the error word, which
+  // commutes with an earlier grid's ORs); from here on global memory is read
+  // and written.
+  grid_dependency_wait();
+  grid_launch_dependents();
   const uint32_t tmem_base = sm.tmem_base;
   const int G = args.sk.G, L = args.sk.L;
   const int n_seg = kSK ? (sm.abort_flag ? 0 : sm.sched.segments()) : args.sk.dp_count(w);
@@ -336,14 +379,12 @@ __global__ void __launch_bounds__(H::THREADS, 1)
                              static_cast<uint32_t>(b * BN);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
-        // HEAD: fetch the first contributor's partial of this chunk before the
-        // TMEM read so that the two latencies overlap.
-        float4 pre[8];
-        if (kSK && kind == kSegHead && sm.sched.head_last > w) {
-          const float* src = args.partials + (static_cast<size_t>(w + 1) * H::BM + r_loc) * BN + c * 32;
-#pragma unroll
-          for (int v = 0; v < 8; ++v) pre[v] = __ldcg(reinterpret_cast<const float4*>(src + 4 * v));
-        }
+        // HEAD: fetch the first (up to) kPre contributors' partials of this
+        // chunk before the TMEM read, all loads in flight at once, so that
+        // their latencies overlap each other and the TMEM read's.
+        float4 pre[kPre][8];
+        const int n_pre = (kSK && kind == kSegHead) ? min(kPre, sm.sched.head_last - w) : 0;
+        if (kSK) load_partials<BN>(pre, args.partials, w + 1, n_pre, r_loc, c);
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tc_wait_ld();
@@ -357,18 +398,13 @@ __global__ void __launch_bounds__(H::THREADS, 1)
           continue;
         }
         if (kSK && kind == kSegHead) {
-          // Add the later workers' partial sums, in worker order.
-          for (int cw = w + 1; cw <= sm.sched.head_last; ++cw) {
-            const float* src = args.partials + (static_cast<size_t>(cw) * H::BM + r_loc) * BN + c * 32;
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const float4 p =
-                  cw == w + 1 ? pre[v] : __ldcg(reinterpret_cast<const float4*>(src + 4 * v));
-              r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + p.x);
-              r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + p.y);
-              r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + p.z);
-              r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + p.w);
-            }
+          // Add the later workers' partial sums, in worker order: the
+          // prefetched group, then further groups of kPre (loads first).
+          add_partials(r, pre, n_pre);
+          for (int cw0 = w + 1 + kPre; cw0 <= sm.sched.head_last; cw0 += kPre) {
+            const int n = min(kPre, sm.sched.head_last - cw0 + 1);
+            load_partials<BN>(pre, args.partials, cw0, n, r_loc, c);
+            add_partials(r, pre, n);
           }
         }
         const int col0 = tn * BN + c * 32;
@@ -436,9 +472,9 @@ cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
     configured[dev] = 1;
   }
   CUtensorMap dummy{};
-  hgemm_tc_kernel<BN, kTma, kSK, kGeneral><<<grid, H::THREADS, H::smem_bytes(BN), stream>>>(
-      map_a ? *map_a : dummy, map_b ? *map_b : dummy, args, idesc);
-  return cudaGetLastError();
+  return launch_kernel(hgemm_tc_kernel<BN, kTma, kSK, kGeneral>, dim3(grid), dim3(H::THREADS),
+                       H::smem_bytes(BN), stream, map_a ? *map_a : dummy,
+                       map_b ? *map_b : dummy, args, idesc);
 }
 
 template <int BN, bool kTma, bool kSK>

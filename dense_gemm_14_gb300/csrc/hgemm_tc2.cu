@@ -134,6 +134,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // Set-up touched only shared memory, TMEM and the parameters (and the error
+  // word's commuting OR); global memory is used from here on.
+  grid_dependency_wait();
+  grid_launch_dependents();
   const uint32_t tmem_base = sm.tmem_base;
   // Both CTAs of a cluster decoded the same table: a pair that gave up at
   // set-up (abort) runs no segment in either CTA.
@@ -424,22 +428,10 @@ cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& ma
   const bool general = args.transa || args.transb || args.epi != kEpiStore;
   const bool sk = args.sk.dp_tiles < args.sk.tiles;
   const dim3 grid(2 * clusters), block(P::THREADS);
-  if (sk) {
-    if (general)
-      hgemm_tc2_kernel<true, true><<<grid, block, P::SMEM_BYTES, stream>>>(map_a, map_b, map_c,
-                                                                           args, idesc);
-    else
-      hgemm_tc2_kernel<false, true><<<grid, block, P::SMEM_BYTES, stream>>>(map_a, map_b, map_c,
-                                                                            args, idesc);
-  } else {
-    if (general)
-      hgemm_tc2_kernel<true, false><<<grid, block, P::SMEM_BYTES, stream>>>(map_a, map_b, map_c,
-                                                                            args, idesc);
-    else
-      hgemm_tc2_kernel<false, false><<<grid, block, P::SMEM_BYTES, stream>>>(map_a, map_b, map_c,
-                                                                             args, idesc);
-  }
-  return cudaGetLastError();
+  auto kernel = sk ? (general ? hgemm_tc2_kernel<true, true> : hgemm_tc2_kernel<false, true>)
+                   : (general ? hgemm_tc2_kernel<true, false> : hgemm_tc2_kernel<false, false>);
+  return launch_kernel(kernel, grid, block, P::SMEM_BYTES, stream, map_a, map_b, map_c, args,
+                       idesc);
 }
 
 }  // namespace gemm14

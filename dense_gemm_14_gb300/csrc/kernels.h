@@ -6,9 +6,32 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "streamk.cuh"
 
 namespace gemm14 {
+
+// Launches kernel over grid x block threads with smem bytes of dynamic shared
+// memory on stream, with programmatic stream serialisation: the grid may be
+// launched while the previous grid on the stream still runs, and waits for it
+// inside (grid_dependency_wait) before touching global memory. This hides the
+// gap between back-to-back products (a few microseconds per launch).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // How the epilogue writes an output element from its sum s:
 //   kEpiStore  C = s                     (alpha = 1, beta = 0)

@@ -28,6 +28,21 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// The kernels are launched with programmatic stream serialisation, so a grid
+// may start while the grid before it on the stream is still running. Every
+// thread calls grid_dependency_wait() before its first access to global
+// memory: it returns once the earlier grid has completed and its writes are
+// visible (at once when there is no such grid). After it, the grid lets the
+// next one start its own launch and prologue (grid_launch_dependents); that
+// grid in turn waits in grid_dependency_wait() for this one to complete.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

@@ -325,6 +325,10 @@ __global__ void __launch_bounds__(S::THREADS, 1)
     }
   }
   __syncthreads();
+  // Set-up touched only shared memory and the parameters (and the error
+  // word's commuting OR); global memory is used from here on.
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int G = args.sk.G, L = args.sk.L;
   const int n_seg = kSK ? (sm.abort_flag ? 0 : sm.sched.segments()) : args.sk.dp_count(w);
 
@@ -563,9 +567,9 @@ cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
     configured[dev] = 1;
   }
   CUtensorMap dummy{};
-  sgemm_simt_kernel<kTma, kSK, kGeneral, kLay><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(
-      map_a ? *map_a : dummy, map_b ? *map_b : dummy, args);
-  return cudaGetLastError();
+  return launch_kernel(sgemm_simt_kernel<kTma, kSK, kGeneral, kLay>, dim3(grid), dim3(S::THREADS),
+                       S::SMEM_BYTES, stream, map_a ? *map_a : dummy, map_b ? *map_b : dummy,
+                       args);
 }
 
 template <bool kTma, bool kSK>

@@ -205,6 +205,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // Set-up touched only shared memory, TMEM and the parameters; global memory
+  // is used from here on.
+  grid_dependency_wait();
+  grid_launch_dependents();
   const uint32_t tmem_base = sm.tmem_base;
 
   if (warp == 0) {
@@ -403,19 +407,18 @@ cudaError_t set_smem() {
 }
 
 template <bool kTA, bool kTB, bool kGeneral>
-void launch_one(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
-                uint32_t idesc, int terms, int clusters, cudaStream_t stream) {
-  sgemm_tf32_pair_kernel<kTA, kTB, kGeneral>
-      <<<2 * clusters, T::THREADS, T::SMEM_BYTES, stream>>>(map_a, map_b, args, idesc, terms);
+cudaError_t launch_one(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
+                       uint32_t idesc, int terms, int clusters, cudaStream_t stream) {
+  return launch_kernel(sgemm_tf32_pair_kernel<kTA, kTB, kGeneral>, dim3(2 * clusters),
+                       dim3(T::THREADS), T::SMEM_BYTES, stream, map_a, map_b, args, idesc, terms);
 }
 
 template <bool kTA, bool kTB>
-void launch_epi(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
-                uint32_t idesc, int terms, int clusters, cudaStream_t stream) {
+cudaError_t launch_epi(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
+                       uint32_t idesc, int terms, int clusters, cudaStream_t stream) {
   if (args.epi != kEpiStore)
-    launch_one<kTA, kTB, true>(map_a, map_b, args, idesc, terms, clusters, stream);
-  else
-    launch_one<kTA, kTB, false>(map_a, map_b, args, idesc, terms, clusters, stream);
+    return launch_one<kTA, kTB, true>(map_a, map_b, args, idesc, terms, clusters, stream);
+  return launch_one<kTA, kTB, false>(map_a, map_b, args, idesc, terms, clusters, stream);
 }
 
 }  // namespace
@@ -449,13 +452,11 @@ cudaError_t launch_sgemm_tf32_pair(const CUtensorMap& map_a, const CUtensorMap& 
                                    cudaStream_t stream) {
   const uint32_t idesc = idesc_tf32_f32acc(T::BM, T::BN);
   if (args.transa) {
-    if (args.transb) launch_epi<true, true>(map_a, map_b, args, idesc, terms, clusters, stream);
-    else launch_epi<true, false>(map_a, map_b, args, idesc, terms, clusters, stream);
-  } else {
-    if (args.transb) launch_epi<false, true>(map_a, map_b, args, idesc, terms, clusters, stream);
-    else launch_epi<false, false>(map_a, map_b, args, idesc, terms, clusters, stream);
+    if (args.transb) return launch_epi<true, true>(map_a, map_b, args, idesc, terms, clusters, stream);
+    return launch_epi<true, false>(map_a, map_b, args, idesc, terms, clusters, stream);
   }
-  return cudaGetLastError();
+  if (args.transb) return launch_epi<false, true>(map_a, map_b, args, idesc, terms, clusters, stream);
+  return launch_epi<false, false>(map_a, map_b, args, idesc, terms, clusters, stream);
 }
 
 }  // namespace gemm14

@@ -38,8 +38,10 @@ def test_f32_streamk(oracle_mod, M, N, K, soft):
     assert torch.equal(C1, C2)
 
 
+# (2000, 128, 4000): 16 tiles of 63 k-blocks over 63 workers of 16 -- ranges
+# that start mid-tile, tiles with up to four contributors.
 TC_CASES = [(16384, 64, 4096), (300, 100, 5000), (2000, 128, 777), (129, 65, 3000),
-            (1, 8, 8), (500, 64, 64)]
+            (1, 8, 8), (500, 64, 64), (2000, 128, 4000)]
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f16"])

@@ -32,6 +32,13 @@ def test_workspace_bytes():
     assert g14.workspace_bytes(BF16, 16384, 64, 4096, 152) == 0
     # few tiles (fewer than half a wave): split, one 128 x 64 slot per worker
     assert g14.workspace_bytes(BF16, 1024, 64, 4096, 152) == 768 + 152 * 128 * 64 * 4
+    # ... but a 16-bit tile takes at most 4 workers, each with at least 16 of
+    # its k-blocks: one tile of 64 k-blocks splits 4 ways, one of 8 does not
+    assert g14.workspace_bytes(BF16, 128, 64, 4096, 152) == 768 + 152 * 128 * 64 * 4
+    assert g14.workspace_bytes(BF16, 128, 64, 512, 152) == 0
+    assert g14.workspace_bytes(BF16, 128, 64, 1024, 152) == 0
+    # fp32 k-blocks are long: two tiles of 8 k-blocks still spread over 16 SMs
+    assert g14.workspace_bytes(F32, 256, 256, 256, 152) == want
     # the CTA-pair kernel (a cluster of two per worker): one 128 x 256 slot per
     # SM when it splits -- between one and two waves with long k (90 tiles on
     # 76 clusters), or few tiles with long k (4 tiles, 16 workers) ...
