@@ -332,14 +332,22 @@ def run_ours(args, dist: Dist):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.2)
+    # The value: K steps back to back between one pair of events, nothing in
+    # between the kernels, so that each launch overlaps the end of the one
+    # before it (the kernels wait for their predecessor on the device).
     start.record(stream)
+    for step in range(K):
+        for p in parts:
+            launch(p, step)
+    end.record(stream)
+    # Each kernel's own duration (the roofline): the same K steps again with an
+    # event pair around every kernel (which keeps consecutive kernels apart).
     for step in range(K):
         for p in parts:
             s_ev, e_ev = ev[p["name"]]
             s_ev[step].record(stream)
             launch(p, step)
             e_ev[step].record(stream)
-    end.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
     clk = clocks.stop()
@@ -438,6 +446,9 @@ def run_ours(args, dist: Dist):
             "dominant_kernel": dominant["kernel"],
             "parts": part_out,
             "gpu_launches": len(parts) * K,
+            "timing": {"value": "K steps back to back between one event pair",
+                       "parts": "the same K steps again, an event pair around each kernel",
+                       "launches_timed_in_total": 2 * len(parts) * K},
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -506,6 +517,17 @@ def time_one(args, name, w, fl, ib, sets, nsets, stream, peaks, roofline, g14, s
     if g14.check_device_error(stream.cuda_stream):
         raise RuntimeError(f"device error in {name}")
     ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    # the same launches back to back between one event pair: consecutive
+    # products overlap launch and set-up with the end of the one before
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for i in range(reps):
+        launch(i)
+    b1.record(stream)
+    torch.cuda.synchronize()
+    if g14.check_device_error(stream.cuda_stream):
+        raise RuntimeError(f"device error in {name}")
+    ms_b2b = b0.elapsed_time(b1) / reps
     mean = statistics.mean(ms)
     tf = fl / (mean / 1e3) / 1e12
     if w.dtype == "f32":
@@ -517,7 +539,11 @@ def time_one(args, name, w, fl, ib, sets, nsets, stream, peaks, roofline, g14, s
                       "dtype": w.dtype, "ms_mean": mean, "ms_min": min(ms), "tflops": tf,
                       "bound": kind, "peak_tflops": peak, "frac_compute": tf / peak,
                       "algorithmic_bytes": ib, "gbs": gbs,
-                      "frac_hbm": gbs / peaks["hbm_gbs"]}), flush=True)
+                      "frac_hbm": gbs / peaks["hbm_gbs"],
+                      "back_to_back": {"ms": ms_b2b, "tflops": fl / (ms_b2b / 1e3) / 1e12,
+                                       "gbs": ib / (ms_b2b / 1e3) / 1e9,
+                                       "frac_hbm": ib / (ms_b2b / 1e3) / 1e9 / peaks["hbm_gbs"]}}),
+          flush=True)
 
 
 # (transa, transb, alpha, beta) variants of the extended call
