@@ -17,10 +17,10 @@ from ._lib import (GEMM14_DTYPE_BF16, GEMM14_DTYPE_F16, GEMM14_DTYPE_F32,
                    check_device_error, debug_inject, gemm_bf16_f32acc, gemm_bf16_f32acc_ws,
                    gemm_bf16_f32acc_noalloc, gemm_ex, gemm_f16_f32acc, gemm_f16_f32acc_ws, gemm_f32,
                    gemm_f32_3xtf32, gemm_f32_ws, gemm_tf32_f32acc, last_error_string, lib_path, load, plan, plan_ex, set_pair_kernel, status_string, version, workspace_bytes)
-from .api import gemm, gemm_into
+from .api import HostGemm, gemm, gemm_async, gemm_into
 
 __all__ = [
-    "gemm", "gemm_into", "gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "gemm_f32_ws",
+    "gemm", "gemm_async", "HostGemm", "gemm_into", "gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "gemm_f32_ws",
     "gemm_tf32_f32acc", "gemm_f32_3xtf32",
     "gemm_bf16_f32acc_ws", "gemm_f16_f32acc_ws", "gemm_bf16_f32acc_noalloc", "gemm_ex", "workspace_bytes",
     "last_error_string", "plan", "plan_ex", "Plan",

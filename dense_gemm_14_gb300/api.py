@@ -119,26 +119,65 @@ def host_panels(M: int, N: int, K: int) -> int:
     return min(8, M // 1024)
 
 
-def gemm(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
-         alpha: float = 1.0, beta: float = 0.0, fp32_mode: str | None = None,
-         panels: int | None = None) -> torch.Tensor:
-    """C = alpha * a @ b + beta * out with fp32 accumulation and output.
+class HostGemm:
+    """A product with host operands in flight (gemm_async): `out` is a pinned
+    host tensor that holds the result once wait() returns."""
 
-    CUDA inputs: computed on the current stream, returned on the GPU (as
-    gemm_into).
+    def __init__(self, out: torch.Tensor, done: torch.cuda.Event | None):
+        self.out = out
+        self._done = done
 
-    CPU inputs: the product runs on the current CUDA device and the result
-    lands in host memory (`out`, a pinned float32 (M, N) tensor, allocated if
-    not given); the call returns once it is there. Inputs that are not pinned
-    are pinned first. A row-major `a` is sent in row panels (host_panels, or
-    `panels`) so that copying panel i+1 in, computing panel i and copying panel
-    i-1 out overlap on three streams; b is sent once, first. With beta != 0 the
-    panels of `out` are sent in too.
-    """
+    def ready(self) -> bool:
+        return self._done is None or self._done.query()
+
+    def wait(self) -> torch.Tensor:
+        if self._done is not None:
+            self._done.synchronize()
+        return self.out
+
+
+# Host outputs of products still in flight, per device: (first byte, end byte,
+# event after the last copy out). A later product that reads host memory one
+# of them still writes (a result fed back as an operand) waits for it first;
+# every other order between products is kept by the copy streams themselves.
+_pending: dict = {}
+
+
+def _host_span(x: torch.Tensor) -> tuple[int, int]:
+    if x.numel() == 0:
+        return 0, 0
+    last = sum((n - 1) * st for n, st in zip(x.shape, x.stride()))
+    return x.data_ptr(), x.data_ptr() + (last + 1) * x.element_size()
+
+
+def _wait_for_writers(dev_index: int, s_in: torch.cuda.Stream, inputs) -> None:
+    live = [p for p in _pending.get(dev_index, []) if not p[2].query()]
+    _pending[dev_index] = live
+    for x in inputs:
+        lo, hi = _host_span(x)
+        for p_lo, p_hi, ev in live:
+            if lo < p_hi and p_lo < hi:
+                s_in.wait_event(ev)
+
+
+def gemm_async(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
+               alpha: float = 1.0, beta: float = 0.0, fp32_mode: str | None = None,
+               panels: int | None = None) -> HostGemm:
+    """C = alpha * a @ b + beta * out for host (CPU) operands, on the current
+    CUDA device, without waiting for the result: returns a HostGemm whose
+    wait() returns `out` (a pinned float32 (M, N) host tensor, allocated if not
+    given) once the result is there.
+
+    Inputs that are not pinned are pinned first. A row-major `a` is sent in row
+    panels (host_panels, or `panels`) so that copying panel i+1 in, computing
+    panel i and copying panel i-1 out overlap on three streams; b is sent once,
+    first; with beta != 0 the panels of `out` are sent in too. Products issued
+    one after another pipeline: the next one's operands go in while this one
+    computes and its result comes out. A product whose host operand is the
+    result of one still in flight waits for that result first. The caller
+    must not change the operands, nor read `out`, before wait()."""
     if a.is_cuda:
-        if out is None:
-            out = torch.empty((a.shape[0], b.shape[1]), dtype=torch.float32, device=a.device)
-        return gemm_into(a, b, out, alpha, beta, fp32_mode=fp32_mode)
+        raise ValueError("gemm_async takes host tensors; use gemm_into for CUDA tensors")
     M, K = a.shape
     N = b.shape[1]
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -158,10 +197,17 @@ def gemm(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
     compute = torch.cuda.current_stream(dev)
     s_in, s_out = _streams(dev)
     with torch.cuda.device(dev):
-        b_d = torch.empty_strided(b.shape, b.stride(), dtype=b.dtype, device=dev)
-        a_d = torch.empty_strided(a.shape, a.stride(), dtype=a.dtype, device=dev)
-        c_d = torch.empty((M, N), dtype=torch.float32, device=dev)
-        s_in.wait_stream(compute)  # the fresh buffers are free on the compute stream
+        _wait_for_writers(dev.index, s_in, [a, b] + ([out] if beta != 0.0 else []))
+        # Device buffers in the input stream's order; record_stream keeps each
+        # block from being handed out again before the other streams that use
+        # it are done with it, so no stream waits for earlier products here.
+        with torch.cuda.stream(s_in):
+            b_d = torch.empty_strided(b.shape, b.stride(), dtype=b.dtype, device=dev)
+            a_d = torch.empty_strided(a.shape, a.stride(), dtype=a.dtype, device=dev)
+            c_d = torch.empty((M, N), dtype=torch.float32, device=dev)
+        for t in (a_d, b_d, c_d):
+            t.record_stream(compute)
+        c_d.record_stream(s_out)
         bounds = [M * p // P for p in range(P + 1)]
         with torch.cuda.stream(s_in):
             b_d.copy_(b, non_blocking=True)
@@ -188,6 +234,26 @@ def gemm(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
             s_out.wait_event(e)
             with torch.cuda.stream(s_out):
                 out[r0:r1].copy_(c_d[r0:r1], non_blocking=True)
-        s_out.synchronize()
-        compute.synchronize()  # the device buffers go back to the caching allocator
-    return out
+        done = torch.cuda.Event()
+        done.record(s_out)
+    lo, hi = _host_span(out)
+    _pending.setdefault(dev.index, []).append((lo, hi, done))
+    return HostGemm(out, done)
+
+
+def gemm(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
+         alpha: float = 1.0, beta: float = 0.0, fp32_mode: str | None = None,
+         panels: int | None = None) -> torch.Tensor:
+    """C = alpha * a @ b + beta * out with fp32 accumulation and output.
+
+    CUDA inputs: computed on the current stream, returned on the GPU (as
+    gemm_into).
+
+    CPU inputs: gemm_async(...).wait(): the result lands in host memory
+    (`out`, a pinned float32 (M, N) tensor, allocated if not given) and the
+    call returns once it is there."""
+    if a.is_cuda:
+        if out is None:
+            out = torch.empty((a.shape[0], b.shape[1]), dtype=torch.float32, device=a.device)
+        return gemm_into(a, b, out, alpha, beta, fp32_mode=fp32_mode)
+    return gemm_async(a, b, out, alpha, beta, fp32_mode, panels).wait()

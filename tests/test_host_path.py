@@ -75,3 +75,50 @@ def test_host_degenerate_sizes():
     A, B = torch.zeros((4, 0)), torch.zeros((0, 3))
     got = g14.gemm(A, B)
     assert torch.equal(got, torch.zeros((4, 3)))
+
+
+def test_async_products_in_flight_match_the_blocking_call():
+    """Several products issued with gemm_async before any is waited for (their
+    copies and kernels overlap one another): each result has the bits of the
+    same product run through the blocking call."""
+    cases = [(3000, 520, 700, "bf16", 4), (1500, 1024, 512, "f32", 2), (300, 200, 100, "f16", 1),
+             (4096, 256, 1024, "bf16", 8), (2048, 300, 257, "f32", 3)]
+    ins = [inputs.make(M, N, K, dt, "normal", 0.1, seed=50 + i)
+           for i, (M, N, K, dt, _) in enumerate(cases)]
+    hs = [g14.gemm_async(A, B, panels=P) for (A, B), (_, _, _, _, P) in zip(ins, cases)]
+    got = [h.wait() for h in hs]
+    for (A, B), (_, _, _, _, P), C in zip(ins, cases, got):
+        assert torch.equal(C, g14.gemm(A, B, panels=P))
+
+
+def test_async_result_fed_back_as_an_operand():
+    """The second product reads the first one's host result before the caller
+    waited for it: the library orders the two (exact integer products)."""
+    M, N, K = 4096, 512, 1024
+    A, B = inputs.make_integer(M, N, K, 3, "f32", seed=61)
+    W = torch.from_numpy(np.random.default_rng(62).integers(-1, 2, (N, 64)).astype(np.float32))
+    out1 = torch.full((M, N), float("nan"), pin_memory=True)
+    h1 = g14.gemm_async(A, B, out=out1, panels=4)
+    h2 = g14.gemm_async(out1, W, panels=4)
+    C1 = A.double() @ B.double()
+    assert torch.equal(h2.wait().double(), C1 @ W.double())
+    assert torch.equal(h1.wait().double(), C1)
+
+
+def test_async_accumulations_into_one_out():
+    """Two products with beta = 1 into the same pinned out, both in flight:
+    the second sends out to the GPU only after the first's result is back."""
+    M, N, K = 2048, 512, 512
+    A1, B1 = inputs.make_integer(M, N, K, 2, "f32", seed=63)
+    A2, B2 = inputs.make_integer(M, N, K, 2, "f32", seed=64)
+    C0 = torch.from_numpy(np.random.default_rng(65).integers(-9, 10, (M, N)).astype(np.float32))
+    out = C0.clone().pin_memory()
+    g14.gemm_async(A1, B1, out=out, beta=1.0, panels=2)
+    g14.gemm_async(A2, B2, out=out, beta=1.0, panels=4).wait()
+    want = C0.double() + A1.double() @ B1.double() + A2.double() @ B2.double()
+    assert torch.equal(out.double(), want)
+
+
+def test_gemm_async_takes_host_tensors_only():
+    with pytest.raises(ValueError):
+        g14.gemm_async(torch.ones(4, 4, device="cuda"), torch.ones(4, 4, device="cuda"))
