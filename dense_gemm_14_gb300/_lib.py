@@ -56,6 +56,11 @@ SIGNATURES = {
                               _vp, _i64, ctypes.c_float, _vp, _i64, _vp, ctypes.c_size_t, _vp]),
     "gemm14_plan_gemm_ex": (_int, [_int, _int, _int, _i64, _i64, _i64, _vp, _i64, _vp, _i64,
                                    _vp, _i64, _int, ctypes.POINTER(_Plan)]),
+    "gemm14_gemm_host": (_int, [_int, _int, _int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64,
+                                _vp, _i64, ctypes.c_float, _vp, _i64, _int,
+                                ctypes.POINTER(ctypes.c_uint64)]),
+    "gemm14_host_wait": (_int, [ctypes.c_uint64]),
+    "gemm14_host_synchronize": (_int, []),
 }
 
 _lib = None
@@ -194,6 +199,36 @@ def gemm_ex(dtype: int, transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C,
                                    C, ldc, workspace, workspace_bytes, stream))
     if check and st:
         raise Gemm14Error(st, "gemm14_gemm_ex")
+    return st
+
+
+def gemm_host(dtype: int, transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+              panels: int = 0, check=True) -> int:
+    """C ABI gemm14_gemm_host on HOST pointers: enqueues the product and returns
+    its ticket (for host_wait). Raises Gemm14Error on a failed call when check."""
+    t = ctypes.c_uint64(0)
+    st = int(load().gemm14_gemm_host(dtype, transa, transb, M, N, K, alpha, A, lda, B, ldb, beta,
+                                     C, ldc, panels, ctypes.byref(t)))
+    if st:
+        if check:
+            raise Gemm14Error(st, "gemm14_gemm_host")
+        return -st
+    return t.value
+
+
+def host_wait(ticket: int, check=True) -> int:
+    """C ABI gemm14_host_wait: blocks until that product's C is in host memory."""
+    st = int(load().gemm14_host_wait(ticket))
+    if check and st:
+        raise Gemm14Error(st, "gemm14_host_wait")
+    return st
+
+
+def host_synchronize(check=True) -> int:
+    """C ABI gemm14_host_synchronize: waits for every host-buffer product in flight."""
+    st = int(load().gemm14_host_synchronize())
+    if check and st:
+        raise Gemm14Error(st, "gemm14_host_synchronize")
     return st
 
 

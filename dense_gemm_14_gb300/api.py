@@ -95,150 +95,79 @@ def gemm_into(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor, alpha: float 
     return out
 
 
-# Host-path streams per device: copies in, copies out (compute runs on the
-# caller's current stream).
-_copy_streams: dict = {}
-
-
-def _streams(dev: torch.device):
-    s = _copy_streams.get(dev.index)
-    if s is None:
-        s = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
-        _copy_streams[dev.index] = s
-    return s
-
-
-def host_panels(M: int, N: int, K: int) -> int:
-    """Row panels the host path splits a product into: one for small products
-    (transfers too short to pipeline), else one per 1024 rows, at most 8. On a
-    GB300 host link (about 200 GB/s each way) this measured 1.43 ms for fp32
-    3072^3 (3 panels; 1.66 ms unsplit) and 2.39 ms for bf16 8192^3 (8; 3.36
-    ms unsplit), near the bound set by sending all of B before the first panel."""
-    if M * N * K < (1 << 31) or M < 2048:
-        return 1
-    return min(8, M // 1024)
-
-
 class HostGemm:
-    """A product with host operands in flight (gemm_async): `out` is a pinned
-    host tensor that holds the result once wait() returns."""
+    """A product with host operands in flight (gemm_async): `out` is the host
+    tensor that holds the result once wait() returns. Keeps the operands (and
+    any pinned copies made of them) alive until then; a handle dropped unwaited
+    waits in its finaliser."""
 
-    def __init__(self, out: torch.Tensor, done: torch.cuda.Event | None):
+    def __init__(self, out: torch.Tensor, ticket: int, keep: tuple):
         self.out = out
-        self._done = done
-
-    def ready(self) -> bool:
-        return self._done is None or self._done.query()
+        self._ticket = ticket
+        self._keep = keep
 
     def wait(self) -> torch.Tensor:
-        if self._done is not None:
-            self._done.synchronize()
+        if self._ticket:
+            t, self._ticket = self._ticket, 0
+            _lib.host_wait(t)
+            self._keep = ()
         return self.out
 
-
-# Host outputs of products still in flight, per device: (first byte, end byte,
-# event after the last copy out). A later product that reads host memory one
-# of them still writes (a result fed back as an operand) waits for it first;
-# every other order between products is kept by the copy streams themselves.
-_pending: dict = {}
-
-
-def _host_span(x: torch.Tensor) -> tuple[int, int]:
-    if x.numel() == 0:
-        return 0, 0
-    last = sum((n - 1) * st for n, st in zip(x.shape, x.stride()))
-    return x.data_ptr(), x.data_ptr() + (last + 1) * x.element_size()
+    def __del__(self):
+        if getattr(self, "_ticket", 0):
+            try:
+                _lib.host_wait(self._ticket, check=False)
+            except Exception:  # interpreter shutdown
+                pass
 
 
-def _wait_for_writers(dev_index: int, s_in: torch.cuda.Stream, inputs) -> None:
-    live = [p for p in _pending.get(dev_index, []) if not p[2].query()]
-    _pending[dev_index] = live
-    for x in inputs:
-        lo, hi = _host_span(x)
-        for p_lo, p_hi, ev in live:
-            if lo < p_hi and p_lo < hi:
-                s_in.wait_event(ev)
+def _product_code(a: torch.Tensor, b: torch.Tensor, fp32_mode: str | None) -> int:
+    if a.dtype != b.dtype or a.dtype not in _CODE:
+        raise TypeError(f"unsupported dtypes {a.dtype}, {b.dtype}")
+    if fp32_mode not in _FP32_MODES or (fp32_mode not in (None, "fp32") and a.dtype != torch.float32):
+        raise ValueError(f"fp32_mode {fp32_mode!r} needs float32 inputs and one of {list(_FP32_MODES)}")
+    return _FP32_MODES[fp32_mode] if a.dtype == torch.float32 else _CODE[a.dtype]
 
 
 def gemm_async(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
                alpha: float = 1.0, beta: float = 0.0, fp32_mode: str | None = None,
                panels: int | None = None) -> HostGemm:
-    """C = alpha * a @ b + beta * out for host (CPU) operands, on the current
-    CUDA device, without waiting for the result: returns a HostGemm whose
-    wait() returns `out` (a pinned float32 (M, N) host tensor, allocated if not
-    given) once the result is there.
+    """C = alpha * a @ b + beta * out for host (CPU) tensors through the C ABI
+    gemm14_gemm_host, on the current CUDA device, without waiting: returns a
+    HostGemm whose wait() returns `out` (a float32 (M, N) row-major host
+    tensor, pinned and allocated if not given) once the result is there.
 
-    Inputs that are not pinned are pinned first. A row-major `a` is sent in row
-    panels (host_panels, or `panels`) so that copying panel i+1 in, computing
-    panel i and copying panel i-1 out overlap on three streams; b is sent once,
-    first; with beta != 0 the panels of `out` are sent in too. Products issued
-    one after another pipeline: the next one's operands go in while this one
-    computes and its result comes out. A product whose host operand is the
-    result of one still in flight waits for that result first. The caller
-    must not change the operands, nor read `out`, before wait()."""
-    if a.is_cuda:
+    a, b: as for gemm_into (row-major views or transposes of them). Operands
+    that are not pinned are pinned first (a copy kept until the wait). The
+    library sends a in row panels (`panels`, or its own choice) after b, and
+    overlaps copying panels in, computing and copying results out, within a
+    product and from one product to the next; a product whose operand is the
+    result of one still in flight waits for it. The caller must not change the
+    operands, nor read `out`, before wait()."""
+    if a.is_cuda or b.is_cuda:
         raise ValueError("gemm_async takes host tensors; use gemm_into for CUDA tensors")
+    code = _product_code(a, b, fp32_mode)
     M, K = a.shape
-    N = b.shape[1]
-    dev = torch.device("cuda", torch.cuda.current_device())
+    K2, N = b.shape
+    if K != K2:
+        raise ValueError(f"shape mismatch: {tuple(a.shape)} @ {tuple(b.shape)}")
     if not a.is_pinned():
         a = a.pin_memory()
     if not b.is_pinned():
         b = b.pin_memory()
+    ta, lda = _operand(a, "a")
+    tb, ldb = _operand(b, "b")
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
     elif out.is_cuda or out.dtype != torch.float32 or tuple(out.shape) != (M, N):
         raise ValueError("out must be a float32 (M, N) host tensor")
-    if beta != 0.0 and not out.is_pinned():
-        raise ValueError("beta != 0 needs a pinned out (its values are sent to the GPU)")
-    row_major_a = a.dim() == 2 and (K <= 1 or a.stride(1) == 1) and a.stride(0) == K
-    P = 1 if not row_major_a else (panels if panels else host_panels(M, N, K))
-    P = max(1, min(P, M)) if M else 1
-    compute = torch.cuda.current_stream(dev)
-    s_in, s_out = _streams(dev)
-    with torch.cuda.device(dev):
-        _wait_for_writers(dev.index, s_in, [a, b] + ([out] if beta != 0.0 else []))
-        # Device buffers in the input stream's order; record_stream keeps each
-        # block from being handed out again before the other streams that use
-        # it are done with it, so no stream waits for earlier products here.
-        with torch.cuda.stream(s_in):
-            b_d = torch.empty_strided(b.shape, b.stride(), dtype=b.dtype, device=dev)
-            a_d = torch.empty_strided(a.shape, a.stride(), dtype=a.dtype, device=dev)
-            c_d = torch.empty((M, N), dtype=torch.float32, device=dev)
-        for t in (a_d, b_d, c_d):
-            t.record_stream(compute)
-        c_d.record_stream(s_out)
-        bounds = [M * p // P for p in range(P + 1)]
-        with torch.cuda.stream(s_in):
-            b_d.copy_(b, non_blocking=True)
-        done_in = []
-        for p in range(P):
-            r0, r1 = bounds[p], bounds[p + 1]
-            with torch.cuda.stream(s_in):
-                if P == 1:
-                    a_d.copy_(a, non_blocking=True)
-                else:
-                    a_d[r0:r1].copy_(a[r0:r1], non_blocking=True)
-                if beta != 0.0:
-                    c_d[r0:r1].copy_(out[r0:r1], non_blocking=True)
-                e = torch.cuda.Event()
-                e.record(s_in)
-            done_in.append(e)
-        for p in range(P):
-            r0, r1 = bounds[p], bounds[p + 1]
-            compute.wait_event(done_in[p])
-            if r1 > r0:
-                gemm_into(a_d[r0:r1], b_d, c_d[r0:r1], alpha, beta, fp32_mode=fp32_mode)
-            e = torch.cuda.Event()
-            e.record(compute)
-            s_out.wait_event(e)
-            with torch.cuda.stream(s_out):
-                out[r0:r1].copy_(c_d[r0:r1], non_blocking=True)
-        done = torch.cuda.Event()
-        done.record(s_out)
-    lo, hi = _host_span(out)
-    _pending.setdefault(dev.index, []).append((lo, hi, done))
-    return HostGemm(out, done)
+    _check_matrix(out, "out")
+    ticket = _lib.gemm_host(code, ta, tb, M, N, K, float(alpha),
+                            a.data_ptr() if a.numel() else None, lda,
+                            b.data_ptr() if b.numel() else None, ldb, float(beta),
+                            out.data_ptr() if out.numel() else None, max(out.stride(0), N, 1),
+                            int(panels or 0))
+    return HostGemm(out, ticket, (a, b))
 
 
 def gemm(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
@@ -250,8 +179,8 @@ def gemm(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
     gemm_into).
 
     CPU inputs: gemm_async(...).wait(): the result lands in host memory
-    (`out`, a pinned float32 (M, N) tensor, allocated if not given) and the
-    call returns once it is there."""
+    (`out`, a float32 (M, N) tensor, pinned and allocated if not given) and
+    the call returns once it is there."""
     if a.is_cuda:
         if out is None:
             out = torch.empty((a.shape[0], b.shape[1]), dtype=torch.float32, device=a.device)

@@ -21,8 +21,9 @@ LIB_NAME = "libgemm14.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "sgemm_simt.cu", "hgemm_tc.cu", "hgemm_tc2.cu", "sgemm_tc3.cu", "epilogue.cu"]
-HEADERS = ["ptx.cuh", "kernels.h", "streamk.cuh"]
+SOURCES = ["api.cu", "sgemm_simt.cu", "hgemm_tc.cu", "hgemm_tc2.cu", "sgemm_tc3.cu", "epilogue.cu",
+           "host_path.cu"]
+HEADERS = ["ptx.cuh", "kernels.h", "streamk.cuh", "api_internal.h"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

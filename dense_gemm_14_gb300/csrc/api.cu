@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "../../include/gemm14.h"
+#include "api_internal.h"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -536,6 +537,81 @@ int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
 }
 
 }  // namespace
+
+// ---- the internal interface of api_internal.h (for the host-buffer runtime)
+int product_on_stream(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
+                      float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                      float beta, float* C, int64_t ldc, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream) {
+  return run_gemm(dtype, transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, workspace,
+                  workspace_bytes, stream);
+}
+
+int validate_product(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
+                     const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
+                     int64_t ldc) {
+  return validate(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc);
+}
+
+size_t product_workspace_bytes(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
+                               const void* A, int64_t lda, const void* B, int64_t ldb,
+                               const void* C, int64_t ldc) {
+  const DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != GEMM14_OK) return 0;
+  gemm14_plan plan;
+  plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+  return workspace_need(plan, dev->sm_count, K);
+}
+
+int operand_bytes(int dtype) { return elem_bytes_of(dtype); }
+
+double schedule_efficiency(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K) {
+  const DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != GEMM14_OK || M <= 0 || N <= 0 || K <= 0) return 1.0;
+  // Dense operands with 16-byte pitches at a 4 KB-aligned notional address:
+  // the plan of such device copies (only alignment and sizes enter it).
+  const int eb = elem_bytes_of(dtype);
+  const int64_t q = 16 / eb;
+  const int64_t lda = ((transa ? M : K) + q - 1) / q * q, ldb = ((transb ? K : N) + q - 1) / q * q;
+  const int64_t ldc = (N + 3) / 4 * 4;
+  const void* base = reinterpret_cast<const void*>(uintptr_t(1) << 12);
+  gemm14_plan plan;
+  plan_for(dtype, transa, transb, M, N, K, base, lda, base, ldb, base, ldc, dev->sm_count, &plan);
+  if (plan.tiles <= 0 || workspace_need(plan, dev->sm_count, K) > 0) return 1.0;
+  const int64_t slots = plan.kernel == 3 ? dev->sm_count / 2 : dev->sm_count;
+  if (slots <= 0) return 1.0;
+  const int64_t waves = (plan.tiles + slots - 1) / slots;
+  return static_cast<double>(plan.tiles) / static_cast<double>(waves * slots);
+}
+
+int current_device_index(int* device) {
+  const DeviceInfo* dev = nullptr;
+  const int st = current_device(&dev);
+  if (st != GEMM14_OK) return st;
+  cudaError_t e = cudaGetDevice(device);
+  if (e != cudaSuccess) {
+    set_cuda_error("cudaGetDevice", e);
+    return GEMM14_ERR_CUDA;
+  }
+  return GEMM14_OK;
+}
+
+int take_device_error() {
+  const DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GEMM14_OK) return st;
+  unsigned word = 0;
+  cudaError_t e;
+  if ((e = cudaMemcpy(&word, dev->err_word, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+      (e = cudaMemset(dev->err_word, 0, sizeof word)) != cudaSuccess) {
+    set_cuda_error("reading the device error word", e);
+    return GEMM14_ERR_CUDA;
+  }
+  return word ? GEMM14_ERR_TIMEOUT : GEMM14_OK;
+}
+
+void note_cuda_error(const char* what, cudaError_t e) { set_cuda_error(what, e); }
+
 }  // namespace gemm14
 
 using namespace gemm14;

@@ -244,6 +244,55 @@ const char* gemm14_last_error_string(void);
  */
 int gemm14_check_device_error(void* stream);
 
+/*
+ * Host-buffer product: C = alpha * op(A) op(B) + beta * C, as gemm14_gemm_ex,
+ * with A, B and C in HOST memory, computed on the current device. The library
+ * copies the operands in, runs the product and copies C back, on three
+ * streams of its own (copies in, kernels, copies out), with device buffers
+ * from a memory pool of its own. This call is the exception to the rules
+ * above on pointers, ownership and allocation.
+ *
+ * Pipelining: op(A) is sent in `panels` row panels (0: the library's choice;
+ * stored K x M A, transa = 1: one panel), after all of B; panel p is computed
+ * once it is in and copied out once computed, while panel p + 1 goes in.
+ * Consecutive calls pipeline in the same way: a call's operands go in while
+ * earlier calls compute and copy out.
+ *
+ * Asynchrony: the call enqueues the work and returns; *ticket (not NULL)
+ * names it for gemm14_host_wait. Until that wait returns, the caller must not
+ * change A, B or C, nor read C. Pinned host memory (cudaHostAlloc, or pinned
+ * torch tensors) gives asynchronous copies at the link's rate; pageable
+ * memory works but CUDA stages its copies through pinned buffers.
+ *
+ * Ordering: a call whose A, B (or C when beta != 0) overlaps the C of a call
+ * still in flight waits, on the device, for that call's C to be back in host
+ * memory. Calls are otherwise ordered only by their streams: products run in
+ * call order, and copies out finish in call order.
+ *
+ * Errors: invalid arguments (as gemm14_gemm_ex, with NULL host pointers where
+ * they are read) are reported before anything is enqueued, with *ticket
+ * untouched. Transfer or launch failures give GEMM14_ERR_CUDA. Degenerate
+ * sizes enqueue nothing (M == 0 or N == 0; beta == 1 with K == 0 or
+ * alpha == 0) and still return a ticket.
+ * Memory: the pool keeps its buffers for reuse for the life of the process.
+ */
+int gemm14_gemm_host(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
+                     float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                     float beta, float* C, int64_t ldc, int panels, uint64_t* ticket);
+
+/*
+ * Blocks until the call named by `ticket` has its C in host memory. Returns
+ * GEMM14_OK, GEMM14_ERR_TIMEOUT if a kernel of the device recorded an expired
+ * wait (the device error word, read and cleared as by
+ * gemm14_check_device_error), GEMM14_ERR_CUDA if the work failed, or
+ * GEMM14_ERR_INVALID_ARG for a ticket never issued. A ticket already waited
+ * for returns GEMM14_OK at once.
+ */
+int gemm14_host_wait(uint64_t ticket);
+
+/* Waits for every host-buffer call in flight (on every device), as gemm14_host_wait. */
+int gemm14_host_synchronize(void);
+
 /* Launch plan chosen for a call (host-side only; no CUDA call is made). */
 typedef struct gemm14_plan {
   int kernel;     /* 1 = fp32 SIMT (FFMA), 2 = tcgen05 on one SM per tile,

@@ -242,3 +242,27 @@ def test_tf32_entry_points_validate(lib):
         assert fn(4, 4, 8, P, 4, P, 4, P, 4, None, check=False) == _lib.GEMM14_ERR_INVALID_ARG
         assert fn(0, 4, 4, 0, 4, 0, 4, 0, 4, None, check=False) == 0
     assert _ex(5, 0, 0, 4, 4, 4, P, 4, P, 4, P, 4) == _lib.GEMM14_ERR_INVALID_ARG  # no dtype 5
+
+
+def test_host_entry_points_validate_before_any_cuda_call():
+    """gemm14_gemm_host / gemm14_host_wait reject bad arguments on the host."""
+    import ctypes
+    lib = g14.load()
+    F32 = g14.GEMM14_DTYPE_F32
+    P = 1 << 16
+    t = ctypes.c_uint64(0)
+    args = (0, 0, 8, 8, 8, 1.0, P, 8, P, 8, 0.0, P, 8)
+    assert lib.gemm14_gemm_host(F32, *args, 0, None) == _lib.GEMM14_ERR_INVALID_ARG
+    assert lib.gemm14_gemm_host(F32, *args, -1, ctypes.byref(t)) == _lib.GEMM14_ERR_INVALID_ARG
+    assert lib.gemm14_gemm_host(99, *args, 0, ctypes.byref(t)) == _lib.GEMM14_ERR_INVALID_ARG
+    # lda < K, NULL A with K > 0, transa = 2
+    bad = [(0, 0, 8, 8, 8, 1.0, P, 7, P, 8, 0.0, P, 8), (0, 0, 8, 8, 8, 1.0, 0, 8, P, 8, 0.0, P, 8),
+           (2, 0, 8, 8, 8, 1.0, P, 8, P, 8, 0.0, P, 8)]
+    for a in bad:
+        assert lib.gemm14_gemm_host(F32, *a, 0, ctypes.byref(t)) == _lib.GEMM14_ERR_INVALID_ARG
+    assert t.value == 0  # untouched by failed calls
+    # tickets never issued
+    assert g14.host_wait(0, check=False) == _lib.GEMM14_ERR_INVALID_ARG
+    assert g14.host_wait(1 << 60, check=False) == _lib.GEMM14_ERR_INVALID_ARG
+    # nothing in flight
+    assert g14.host_synchronize(check=False) == 0

@@ -39,9 +39,8 @@ def test_panels_f32_within_bound(oracle_mod, panels):
 
 
 def test_default_panels_on_a_large_product(oracle_mod):
-    """2048 x 1024 x 1100 takes the pipelined path by default (2 panels)."""
+    """2048 x 1024 x 1100 with the library's own panel split."""
     M, N, K = 2048, 1024, 1100
-    assert g14.api.host_panels(M, N, K) == 2
     A, B = inputs.make(M, N, K, "bf16", "normal", 0.03, seed=43)
     got = g14.gemm(A, B)
     rows = np.arange(0, M, 37)
@@ -122,3 +121,49 @@ def test_async_accumulations_into_one_out():
 def test_gemm_async_takes_host_tensors_only():
     with pytest.raises(ValueError):
         g14.gemm_async(torch.ones(4, 4, device="cuda"), torch.ones(4, 4, device="cuda"))
+
+
+def _padded_host(x: torch.Tensor, ld: int, fill: float = 0.0) -> tuple[torch.Tensor, torch.Tensor]:
+    rows, cols = x.shape
+    buf = torch.full((max(rows, 1) * ld + 8,), fill, dtype=x.dtype).pin_memory()
+    view = buf[:rows * ld].view(rows, ld)[:, :cols]
+    view.copy_(x)
+    return buf, view
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_c_abi_host_entry_pitched_and_transposed(oracle_mod, dt, ta, tb):
+    """gemm14_gemm_host on raw host pointers with padded pitches, stored
+    transposes and odd 16-bit row lengths (the device copies are re-pitched
+    to 16 bytes), against the oracle; then waited twice."""
+    M, N, K = 777, 301, 259
+    A, B = inputs.make(M, N, K, dt, "normal", 0.2, seed=70 + 2 * ta + tb)
+    As = A.t().contiguous() if ta else A
+    Bs = B.t().contiguous() if tb else B
+    abuf, a = _padded_host(As, As.shape[1] + 3)
+    bbuf, b = _padded_host(Bs, Bs.shape[1] + 5)
+    cbuf, c = _padded_host(torch.full((M, N), float("nan")), N + 7, fill=float("nan"))
+    code = {"f32": g14.GEMM14_DTYPE_F32, "bf16": g14.GEMM14_DTYPE_BF16}[dt]
+    t = g14.gemm_host(code, ta, tb, M, N, K, 1.0, a.data_ptr(), a.stride(0), b.data_ptr(),
+                      b.stride(0), 0.0, c.data_ptr(), c.stride(0), panels=3)
+    assert g14.host_wait(t) == 0
+    assert g14.host_wait(t) == 0
+    oracle_check(oracle_mod, A, B, c.clone())
+    # the padding of C is untouched
+    assert torch.isnan(cbuf[:M * (N + 7)].view(M, N + 7)[:, N:]).all()
+
+
+def test_c_abi_host_entry_degenerate_calls():
+    P = torch.zeros(64, pin_memory=True)
+    # M == 0: nothing to do, a ticket all the same
+    t = g14.gemm_host(g14.GEMM14_DTYPE_F32, 0, 0, 0, 4, 4, 1.0, P.data_ptr(), 4, P.data_ptr(), 4,
+                      0.0, P.data_ptr(), 4)
+    assert t > 0 and g14.host_wait(t) == 0
+    # K == 0: C = beta * C (beta 0.5), sent in and back
+    C = torch.arange(12, dtype=torch.float32).view(3, 4).pin_memory()
+    t = g14.gemm_host(g14.GEMM14_DTYPE_BF16, 0, 0, 3, 4, 0, 1.0, None, 1, None, 4, 0.5,
+                      C.data_ptr(), 4)
+    assert g14.host_wait(t) == 0
+    assert torch.equal(C, torch.arange(12, dtype=torch.float32).view(3, 4) * 0.5)
+    assert g14.host_synchronize() == 0
