@@ -494,7 +494,11 @@ def run_table(args):
         per_set = A.numel() * A.element_size() + B.numel() * B.element_size() + w.M * w.N * 4
         nsets = max(2, -(-2 * L2_BYTES // per_set))
         sets = [(A.cuda(), B.cuda(), torch.empty(w.M, w.N, device="cuda")) for _ in range(nsets)]
-        ws_bytes = g14.workspace_bytes(code[w.dtype], w.M, w.N, w.K, 0)
+        # the workspace for these operands: the stream-K region, and room to
+        # re-pitch operands TMA cannot read (same alignment in every set)
+        a0, b0, c0 = sets[0]
+        ws_bytes = g14.workspace_bytes_ex(code[w.dtype], 0, 0, w.M, w.N, w.K, a0.data_ptr(), w.K,
+                                          b0.data_ptr(), w.N, c0.data_ptr(), w.N)
         ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
         for schedule in ("data-parallel", "stream-K"):
             if schedule == "stream-K" and ws_bytes == 0:
@@ -554,6 +558,7 @@ def time_one(args, name, w, fl, ib, sets, nsets, stream, peaks, roofline, g14, s
                       "bound": kind, "peak_tflops": peak, "frac_compute": tf / peak,
                       "algorithmic_bytes": ib, "gbs": gbs,
                       "frac_hbm": gbs / peaks["hbm_gbs"],
+                      "workspace_bytes": ws_bytes if schedule == "stream-K" else 0,
                       "back_to_back": {"ms": ms_b2b, "tflops": fl / (ms_b2b / 1e3) / 1e12,
                                        "gbs": ib / (ms_b2b / 1e3) / 1e9,
                                        "frac_hbm": ib / (ms_b2b / 1e3) / 1e9 / peaks["hbm_gbs"]}}),

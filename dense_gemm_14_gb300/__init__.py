@@ -15,7 +15,7 @@ from __future__ import annotations
 from ._lib import (GEMM14_DTYPE_BF16, GEMM14_DTYPE_F16, GEMM14_DTYPE_F32,
                    GEMM14_DTYPE_F32_3XTF32, GEMM14_DTYPE_TF32, Gemm14Error, Plan,
                    check_device_error, debug_inject, gemm_bf16_f32acc, gemm_bf16_f32acc_ws,
-                   gemm_bf16_f32acc_noalloc, gemm_ex, gemm_host, host_synchronize, host_wait, gemm_f16_f32acc, gemm_f16_f32acc_ws, gemm_f32,
+                   gemm_bf16_f32acc_noalloc, gemm_ex, gemm_host, host_synchronize, host_wait, workspace_bytes_ex, gemm_f16_f32acc, gemm_f16_f32acc_ws, gemm_f32,
                    gemm_f32_3xtf32, gemm_f32_ws, gemm_tf32_f32acc, last_error_string, lib_path, load, plan, plan_ex, set_pair_kernel, status_string, version, workspace_bytes)
 from .api import HostGemm, gemm, gemm_async, gemm_into
 
@@ -23,7 +23,7 @@ __all__ = [
     "gemm", "gemm_async", "HostGemm", "gemm_into", "gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "gemm_f32_ws",
     "gemm_tf32_f32acc", "gemm_f32_3xtf32",
     "gemm_bf16_f32acc_ws", "gemm_f16_f32acc_ws", "gemm_bf16_f32acc_noalloc", "gemm_ex",
-    "gemm_host", "host_wait", "host_synchronize", "workspace_bytes",
+    "gemm_host", "host_wait", "host_synchronize", "workspace_bytes_ex", "workspace_bytes",
     "last_error_string", "plan", "plan_ex", "Plan",
     "check_device_error", "debug_inject", "set_pair_kernel", "status_string", "version", "load", "lib_path", "Gemm14Error",
     "GEMM14_DTYPE_F32", "GEMM14_DTYPE_BF16", "GEMM14_DTYPE_F16", "GEMM14_DTYPE_TF32",

@@ -60,6 +60,8 @@ SIGNATURES = {
                                 _vp, _i64, ctypes.c_float, _vp, _i64, _int,
                                 ctypes.POINTER(ctypes.c_uint64)]),
     "gemm14_host_wait": (_int, [ctypes.c_uint64]),
+    "gemm14_workspace_bytes_ex": (ctypes.c_size_t, [_int, _int, _int, _i64, _i64, _i64, _vp, _i64,
+                                                    _vp, _i64, _vp, _i64, _int]),
     "gemm14_host_synchronize": (_int, []),
 }
 
@@ -200,6 +202,14 @@ def gemm_ex(dtype: int, transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C,
     if check and st:
         raise Gemm14Error(st, "gemm14_gemm_ex")
     return st
+
+
+def workspace_bytes_ex(dtype: int, transa, transb, M, N, K, A, lda, B, ldb, C, ldc,
+                       sm_count: int = 0) -> int:
+    """C ABI gemm14_workspace_bytes_ex: workspace for these exact operands,
+    re-pitching of operands TMA cannot read included."""
+    return int(load().gemm14_workspace_bytes_ex(dtype, transa, transb, M, N, K, A, lda, B, ldb,
+                                                C, ldc, sm_count))
 
 
 def gemm_host(dtype: int, transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,

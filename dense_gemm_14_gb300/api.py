@@ -87,7 +87,9 @@ def gemm_into(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor, alpha: float 
         raise ValueError(f"fp32_mode {fp32_mode!r} needs float32 inputs and one of {list(_FP32_MODES)}")
     code = _FP32_MODES[fp32_mode] if a.dtype == torch.float32 else _CODE[a.dtype]
     with torch.cuda.device(a.device):
-        nbytes = _lib.workspace_bytes(code, M, N, K, 0) if M and N and K else 0
+        nbytes = _lib.workspace_bytes_ex(code, ta, tb, M, N, K, a.data_ptr(), lda, b.data_ptr(),
+                                         ldb, out.data_ptr(), max(out.stride(0), N, 1)) \
+            if M and N and K else 0
         ws = _workspace(a.device, int(stream or 0), nbytes) if nbytes else None
         _lib.gemm_ex(code, ta, tb, M, N, K, float(alpha), a.data_ptr(), lda,
                      b.data_ptr(), ldb, float(beta), out.data_ptr(), max(out.stride(0), N, 1),

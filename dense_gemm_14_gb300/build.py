@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["api.cu", "sgemm_simt.cu", "hgemm_tc.cu", "hgemm_tc2.cu", "sgemm_tc3.cu", "epilogue.cu",
-           "host_path.cu"]
+           "host_path.cu", "copy.cu"]
 HEADERS = ["ptx.cuh", "kernels.h", "streamk.cuh", "api_internal.h"]
 
 NVCC_FLAGS = [

@@ -365,6 +365,52 @@ void schedule(const gemm14_plan& plan, int64_t K, int sm_count, void* workspace,
   }
 }
 
+// Re-pitching into the caller's workspace. An operand whose base or row
+// pitch is not a multiple of 16 bytes cannot be read by TMA; with a large
+// enough workspace the call copies it there with a 16-byte pitch (a memory-
+// bound pass of one read and one write per element) and runs the TMA loaders
+// on the copy. Workspace layout: the stream-K region first (its flag words at
+// the start, where they always are), then the copy of A, then that of B.
+struct Repitch {
+  bool a = false, b = false;     // which operands are copied
+  int64_t lda = 0, ldb = 0;      // their pitches in the workspace
+  size_t sk_bytes = 0;           // the stream-K region (flags + slots)
+  size_t a_off = 0, b_off = 0;   // byte offsets of the copies
+  size_t total = 0;              // workspace bytes the call needs for all of it
+};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Fills *r for a call on `sms` SMs; r->a / r->b false when TMA can read the
+// operand as it is (then the call never copies it).
+void plan_repitch(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
+                  const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
+                  int64_t ldc, int sms, Repitch* r) {
+  *r = Repitch{};
+  if (M <= 0 || N <= 0 || K <= 0) return;
+  const int eb = elem_bytes_of(dtype);
+  const int64_t q = 16 / eb;
+  r->a = !(aligned(A, 16) && lda % q == 0);
+  r->b = !(aligned(B, 16) && ldb % q == 0);
+  if (!r->a && !r->b) return;
+  const int64_t rows_a = transa ? K : M, cols_a = transa ? M : K;
+  const int64_t rows_b = transb ? N : K, cols_b = transb ? K : N;
+  r->lda = r->a ? (cols_a + q - 1) / q * q : lda;
+  r->ldb = r->b ? (cols_b + q - 1) / q * q : ldb;
+  // The plan of the copies: only their alignment enters it.
+  const void* base = reinterpret_cast<const void*>(uintptr_t(1) << 12);
+  gemm14_plan plan;
+  plan_for(dtype, transa, transb, M, N, K, r->a ? base : A, r->lda, r->b ? base : B, r->ldb, C,
+           ldc, sms, &plan);
+  const size_t sk = workspace_need(plan, sms, K);
+  r->sk_bytes = sk;
+  const size_t flags = streamk_flag_bytes(sms);
+  r->a_off = round256(sk > flags ? sk : flags);
+  const size_t a_bytes = r->a ? static_cast<size_t>(rows_a * r->lda * eb) : 0;
+  r->b_off = round256(r->a_off + a_bytes);
+  r->total = r->b ? r->b_off + static_cast<size_t>(rows_b * r->ldb * eb) : r->a_off + a_bytes;
+}
+
 // Tensor maps of the 16-bit kernels for a tile of bm rows x bn columns:
 // A stored M x K: box 64 k x bm m; stored K x M: box 64 m x 64 k (bm / 64
 // loads per stage). B stored K x N: box 64 n x 64 k (bn / 64 loads); stored
@@ -409,6 +455,31 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
     return finish(launch_scale_c(C, ldc, static_cast<int>(M), static_cast<int>(N), beta,
                                  dev->sm_count, stream),
                   "scale launch", stream);
+  }
+
+  // Operands TMA cannot read: with room in the workspace, copy them there with
+  // 16-byte pitches first; the call then keeps the workspace's start (up to
+  // the copies) for the stream-K schedule.
+  if (workspace) {
+    Repitch rp;
+    plan_repitch(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &rp);
+    if ((rp.a || rp.b) && workspace_bytes >= rp.total) {
+      char* ws = static_cast<char*>(workspace);
+      RepitchJob ja{nullptr, 0, nullptr, 0, 0, 0}, jb{nullptr, 0, nullptr, 0, 0, 0};
+      if (rp.a) {
+        ja = RepitchJob{A, lda, ws + rp.a_off, rp.lda, transa ? K : M, transa ? M : K};
+        A = ws + rp.a_off;
+        lda = rp.lda;
+      }
+      if (rp.b) {
+        jb = RepitchJob{B, ldb, ws + rp.b_off, rp.ldb, transb ? N : K, transb ? K : N};
+        B = ws + rp.b_off;
+        ldb = rp.ldb;
+      }
+      const cudaError_t e = launch_repitch(ja, jb, elem_bytes_of(dtype), dev->sm_count, stream);
+      if (e != cudaSuccess) return finish(e, "re-pitch launch", stream);
+      workspace_bytes = rp.a_off;
+    }
   }
 
   gemm14_plan plan;
@@ -686,6 +757,24 @@ size_t gemm14_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int sm
     return 0;
   gemm14_plan plan;
   plan_for(dtype, M, N, K, p, lda, p, ldb, p, ldb, sm_count, &plan);
+  return workspace_need(plan, sm_count, K);
+}
+
+size_t gemm14_workspace_bytes_ex(int dtype, int transa, int transb, int64_t M, int64_t N,
+                                 int64_t K, const void* A, int64_t lda, const void* B,
+                                 int64_t ldb, const void* C, int64_t ldc, int sm_count) {
+  if (sm_count <= 0) {
+    const DeviceInfo* dev = nullptr;
+    if (current_device(&dev) != GEMM14_OK) return 0;
+    sm_count = dev->sm_count;
+  }
+  if (validate(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc) != GEMM14_OK) return 0;
+  if (M == 0 || N == 0 || K == 0) return 0;
+  Repitch rp;
+  plan_repitch(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, sm_count, &rp);
+  if (rp.a || rp.b) return rp.total;
+  gemm14_plan plan;
+  plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, sm_count, &plan);
   return workspace_need(plan, sm_count, K);
 }
 

@@ -1,0 +1,68 @@
+// copy.cu -- re-pitching an operand that TMA cannot address (a base or a
+// row pitch that is not a multiple of 16 bytes) into a caller workspace with a
+// 16-byte pitch, so that the product runs on the TMA loaders instead of the
+// element-wise ones. A memory-bound pass: each element is read and written
+// once. The work items are segments of kUnroll x 32 consecutive elements of a
+// row; a warp loads a whole segment (its lanes on consecutive elements, so
+// reads and writes are coalesced whatever the source alignment) before it
+// stores any of it, keeping kUnroll loads per lane in flight.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gemm14 {
+namespace {
+
+constexpr int kUnroll = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(256) repitch_kernel(const RepitchJob j0, const RepitchJob j1) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t seg = 32 * kUnroll;
+  const int64_t per_row0 = (j0.cols + seg - 1) / seg, per_row1 = (j1.cols + seg - 1) / seg;
+  const int64_t items0 = j0.rows * per_row0;
+  const int64_t items = items0 + j1.rows * per_row1;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t it = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       it < items; it += warps) {
+    const bool first = it < items0;
+    const RepitchJob& j = first ? j0 : j1;
+    const int64_t per_row = first ? per_row0 : per_row1;
+    const int64_t i = first ? it : it - items0;
+    const int64_t r = i / per_row;
+    const int64_t c0 = (i - r * per_row) * seg + lane;
+    const T* s = static_cast<const T*>(j.src) + r * j.ld_src;
+    T* d = static_cast<T*>(j.dst) + r * j.ld_dst;
+    T v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t c = c0 + 32 * u;
+      v[u] = c < j.cols ? s[c] : T(0);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t c = c0 + 32 * u;
+      if (c < j.cols) d[c] = v[u];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_repitch(const RepitchJob& j0, const RepitchJob& j1, int elem_bytes,
+                           int sm_count, cudaStream_t stream) {
+  // one segment per warp while there are fewer than 8 blocks an SM's worth
+  const int64_t seg = 32 * kUnroll;
+  const int64_t segments = (j0.cols > 0 ? j0.rows * ((j0.cols + seg - 1) / seg) : 0) +
+                           (j1.cols > 0 ? j1.rows * ((j1.cols + seg - 1) / seg) : 0);
+  if (segments <= 0) return cudaSuccess;
+  const int64_t blocks = (segments + 7) / 8;  // 8 warps a block
+  const int64_t cap = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 8;
+  const dim3 grid(static_cast<unsigned>(blocks < cap ? blocks : cap));
+  if (elem_bytes == 4)
+    return launch_kernel(repitch_kernel<uint32_t>, grid, dim3(256), 0, stream, j0, j1);
+  return launch_kernel(repitch_kernel<uint16_t>, grid, dim3(256), 0, stream, j0, j1);
+}
+
+}  // namespace gemm14

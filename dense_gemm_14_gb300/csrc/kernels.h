@@ -192,6 +192,19 @@ cudaError_t launch_sgemm_tf32_pair(const CUtensorMap& map_a, const CUtensorMap& 
                                    const GemmArgs& args, int terms, int clusters,
                                    cudaStream_t stream);
 
+// A rows x cols matrix to copy from row pitch ld_src to row pitch ld_dst
+// (rows = 0: nothing).
+struct RepitchJob {
+  const void* src;
+  int64_t ld_src;
+  void* dst;
+  int64_t ld_dst;
+  int64_t rows, cols;
+};
+// Both copies in one launch on `stream`, elements of elem_bytes (2 or 4) (copy.cu).
+cudaError_t launch_repitch(const RepitchJob& j0, const RepitchJob& j1, int elem_bytes,
+                           int sm_count, cudaStream_t stream);
+
 // ---- C = beta * C over an M x N block (epilogue.cu): the call when the
 // product term vanishes (K == 0 or alpha == 0) and beta is not 0 or 1.
 cudaError_t launch_scale_c(float* C, int64_t ldc, int M, int N, float beta, int sm_count,

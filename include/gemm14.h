@@ -134,7 +134,8 @@ int gemm_f32_3xtf32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda
  * kernels split the k-blocks of the last wave and a half of output tiles
  * evenly over all SMs instead of leaving SMs idle in a partial last wave, or,
  * for products of fewer tiles than half the SMs, spread all their k-blocks
- * over the SMs (the "stream-K" schedule): a tile shared by several SMs is finished by the
+ * over the SMs (16-bit tiles over at most 4 SMs each, with 16 or more
+ * k-blocks apiece) (the "stream-K" schedule): a tile shared by several SMs is finished by the
  * SM holding its first k-blocks, which adds the others' partial sums from the
  * workspace in a fixed order, so results are deterministic run to run (they
  * may differ in the last bits from the data-parallel schedule, which sums a
@@ -149,6 +150,13 @@ int gemm_f32_3xtf32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda
  * number of a finished call, so a workspace may be reused by any later call,
  * of any shape, without clearing; it must not be used by two calls that may
  * run at the same time.
+ * Re-pitching: an operand TMA cannot read (base or row pitch not a multiple
+ * of 16 bytes) is first copied into the workspace with a 16-byte pitch when
+ * the workspace has gemm14_workspace_bytes_ex(...) bytes for this call's
+ * operands; the product then runs on the TMA loaders (the same kernels, and
+ * the same bits, as for aligned operands). The copies lie after the stream-K
+ * region, never over the flag words. With less room the call reads such an
+ * operand as it is, with the element-wise loaders.
  */
 int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
                 int64_t ldb, float* C, int64_t ldc, void* workspace, size_t workspace_bytes,
@@ -212,9 +220,10 @@ int gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int
  * Loaders: operands take TMA under the same alignment rules as the plain
  * entry points (16-byte aligned, pitches multiples of 16 bytes) in either
  * storage, and the equivalent software loader otherwise.
- * workspace / workspace_bytes: as for the *_ws calls (NULL, 0 allowed); the
- * bytes needed do not depend on transa / transb, so
- * gemm14_workspace_bytes(dtype, M, N, K, ...) applies.
+ * workspace / workspace_bytes: as for the *_ws calls (NULL, 0 allowed),
+ * re-pitching included; gemm14_workspace_bytes_ex gives the bytes for these
+ * operands (for TMA-addressable ones it equals gemm14_workspace_bytes(dtype,
+ * M, N, K, ...), which does not depend on transa / transb).
  * Other rules (device pointers, stream, errors, degenerate sizes) as above.
  */
 int gemm14_gemm_ex(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
@@ -230,6 +239,18 @@ int gemm14_gemm_ex(int dtype, int transa, int transb, int64_t M, int64_t N, int6
  * TMA can address (16-byte aligned, pitches multiple of 16 bytes).
  */
 size_t gemm14_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int sm_count);
+
+/*
+ * Workspace bytes for a gemm14_gemm_ex (or *_ws) call on exactly these
+ * operands: the stream-K region as above, plus, for an operand TMA cannot
+ * read, room for its copy with a 16-byte pitch (so that the call re-pitches
+ * it). Pointers are only inspected for their alignment, never dereferenced;
+ * no CUDA call is made when sm_count > 0. 0: the call needs no workspace, or
+ * the arguments are invalid.
+ */
+size_t gemm14_workspace_bytes_ex(int dtype, int transa, int transb, int64_t M, int64_t N,
+                                 int64_t K, const void* A, int64_t lda, const void* B,
+                                 int64_t ldb, const void* C, int64_t ldc, int sm_count);
 
 /* Static text for a status code (never NULL). */
 const char* gemm14_status_string(int status);

@@ -66,3 +66,39 @@ def test_ws_entry_points_validate_workspace():
             _lib.GEMM14_ERR_INVALID_ARG
         # empty products need nothing
         assert fn(0, 8, 8, P, 8, P, 8, P, 8, 0, 0, None, check=False) == 0
+
+
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_workspace_bytes_ex_adds_room_to_repitch():
+    """Aligned operands need what gemm14_workspace_bytes gives; an operand TMA
+    cannot read adds its copy with a 16-byte pitch after the stream-K region
+    (which keeps the workspace's start), A's copy first."""
+    g14.load()
+    F32, BF16 = g14.GEMM14_DTYPE_F32, g14.GEMM14_DTYPE_BF16
+    P = 1 << 20
+    ex = g14.workspace_bytes_ex
+    # aligned: the same as the shape-only query, any storage
+    for dt, M, N, K in ((F32, 3072, 3072, 3072), (F32, 4097, 3001, 516), (BF16, 1024, 64, 4096),
+                        (BF16, 16384, 64, 4096), (BF16, 2304, 2560, 8192)):
+        lda, ldb = (K + 7) // 8 * 8, (N + 7) // 8 * 8
+        assert ex(dt, 0, 0, M, N, K, P, lda, P, ldb, P, ldb, 152) == \
+            g14.workspace_bytes(dt, M, N, K, 152)
+    # fp32 4097 x 3001 x 513 (pitches 2052 and 12004 bytes): both copied
+    M, N, K = 4097, 3001, 513
+    sk = 768 + 2 * 152 * 128 * 256 * 4          # 396 tiles: split, two fp32 slots per SM
+    a_off = _r256(sk)
+    b_off = _r256(a_off + M * 516 * 4)
+    assert ex(F32, 0, 0, M, N, K, P, K, P, N, P, N, 152) == b_off + K * 3004 * 4
+    # only B unaligned (bf16, ldb odd), 128 tiles (not split): the copy after the flags
+    M, N, K = 16384, 64, 4096
+    assert ex(BF16, 0, 0, M, N, K, P, K, P, 65, P, N, 152) == 768 + K * 64 * 2
+    # a misaligned base with an aligned pitch is copied too (A stored K x M)
+    M, N, K = 1000, 1000, 777
+    sk = g14.workspace_bytes(F32, M, N, K, 152)
+    assert ex(F32, 1, 0, M, N, K, P + 4, 1000, P, N, P, N, 152) == _r256(sk) + K * 1000 * 4
+    # nothing to compute, or invalid arguments: 0
+    assert ex(F32, 0, 0, 8, 8, 0, 0, 1, 0, 8, P, 8, 152) == 0
+    assert ex(F32, 0, 0, 8, 8, 8, P, 7, P, 8, P, 8, 152) == 0
