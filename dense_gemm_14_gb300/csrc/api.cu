@@ -199,6 +199,23 @@ void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K
     // anything else on the fp32 SIMT kernel (exact fp32 products, so at least
     // as accurate as either tensor-core mode).
     if (aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 && ldb % 4 == 0 && sm_count >= 2) {
+      if (dtype == GEMM14_DTYPE_TF32 && !transa && transb && g_pair_enabled.load()) {
+        // TF32 with both operands K-major as stored: the 16-bit pair kernel's
+        // mainloop with kind::tf32 MMAs (k-blocks of 32 fp32), no conversion
+        using P = PairShape;
+        p->kernel = 5;
+        p->loader = 1;
+        p->bm = P::BM;
+        p->bn = P::BN;
+        p->bk = 32;
+        p->stages = P::STAGES;
+        p->threads = P::THREADS;
+        p->smem_bytes = P::SMEM_BYTES;
+        p->tiles = ((M + P::BM - 1) / P::BM) * ((N + P::BN - 1) / P::BN);
+        const int64_t clusters = sm_count / 2;
+        p->grid = static_cast<int>(2 * (p->tiles < clusters ? p->tiles : clusters));
+        return;
+      }
       using T = Tf32Shape;
       p->kernel = 4;
       p->loader = 1;
@@ -328,8 +345,8 @@ int one_sm_split_workers(int kernel, int64_t tiles, int64_t L, int G) {
 
 size_t workspace_need(const gemm14_plan& plan, int sm_count, int64_t K) {
   if (plan.tiles > INT32_MAX) return 0;
-  if (plan.kernel == 3) {
-    const int64_t L = (K + PairShape::BK - 1) / PairShape::BK;
+  if (plan.kernel == 3 || plan.kernel == 5) {
+    const int64_t L = (K + plan.bk - 1) / plan.bk;
     if (!pair_split_workers(plan.tiles, L, sm_count / 2)) return 0;
     return streamk_workspace_bytes(sm_count, PairShape::BM / 2, PairShape::BN, 1);
   }
@@ -427,6 +444,41 @@ int make_maps_16(bool bf16, int transa, int transb, int64_t M, int64_t N, int64_
                 : make_map(mb, tt, 2, B, K, N, ldb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The CTA-pair kernel (plan kernels 3 and 5): data-parallel over
+// min(tiles, clusters) clusters, or, with a large enough workspace, stream-K
+// over all co-resident clusters (workers).
+int run_pair(const gemm14_plan& plan, GemmArgs& args, const CUtensorMap& ma,
+             const CUtensorMap& mb, int pair_clusters, bool tf32, uint32_t idesc, int64_t K,
+             int sm_count, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int clusters = static_cast<int>(plan.tiles < pair_clusters ? plan.tiles : pair_clusters);
+  const int L = static_cast<int>((K + plan.bk - 1) / plan.bk);
+  const size_t need = workspace_need(plan, sm_count, K);
+  const int workers = pair_split_workers(plan.tiles, L, pair_clusters);
+  if (workspace && need && workspace_bytes >= need && workers > 0) {
+    // every tile split (fewer than two waves): dp_tiles = 0
+    args.sk = StreamK{static_cast<int>(plan.tiles), L, workers, 0};
+    args.flags = static_cast<unsigned*>(workspace);
+    args.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             streamk_flag_bytes(sm_count));
+    args.epoch = next_epoch();
+    clusters = args.sk.G;
+  } else {
+    args.sk = make_stream_k(static_cast<int>(plan.tiles), L, clusters, false);
+  }
+  // C for the TMA-store epilogue of the plain variants (plain stores into a
+  // 16-byte-aligned C): box 32 columns x 32 rows of fp32, 128-byte swizzle.
+  // The variant is plain exactly when launch_hgemm_tc_pair picks it.
+  const bool general = (!tf32 && (args.transa || args.transb)) || args.epi != kEpiStore;
+  CUtensorMap mc{};
+  if (!general && plan.vec_store) {
+    const int st = make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, args.C, args.M, args.N,
+                            args.ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != GEMM14_OK) return st;
+  }
+  return finish(launch_hgemm_tc_pair(ma, mb, mc, args, idesc, clusters, tf32, stream),
+                "hgemm pair launch", stream);
+}
+
 int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K, float alpha,
              const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
              int64_t ldc, void* workspace, size_t workspace_bytes, void* stream_ptr) {
@@ -490,6 +542,27 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
                 dev->err_word, wait_limit_ns, fault, StreamK{}, nullptr, nullptr, 0u};
   int grid = plan.grid;
 
+  if (plan.kernel == 5) {
+    const int pair_clusters = pair_max_clusters();
+    if (pair_clusters > 0) {
+      // A stored M x K, B stored N x K: boxes of 32 k (128 bytes) x 128 rows
+      CUtensorMap ma, mb;
+      const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+      if ((st = make_map(&ma, f32, 4, A, M, K, lda, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+              GEMM14_OK ||
+          (st = make_map(&mb, f32, 4, B, N, K, ldb, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+              GEMM14_OK)
+        return st;
+      return run_pair(plan, args, ma, mb, pair_clusters, true,
+                      idesc_tf32_f32acc(PairShape::BM, PairShape::BN), K, dev->sm_count,
+                      workspace, workspace_bytes, stream);
+    }
+    // clusters of two do not fit: plan without the pair kernel
+    g_pair_enabled.store(0);
+    plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+    args.vec_store = plan.vec_store;
+    grid = plan.grid;
+  }
   if (plan.kernel == 4) {
     const int clusters_max = tf32_pair_max_clusters();
     if (clusters_max > 0) {
@@ -555,34 +628,9 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
     if ((st = make_maps_16(bf16, transa, transb, M, N, K, A, lda, B, ldb, 128, 128, &ma, &mb)) !=
         GEMM14_OK)
       return st;
-    // Data-parallel over min(tiles, clusters) clusters, or with a large
-    // enough workspace stream-K over all co-resident clusters (workers).
-    int clusters = static_cast<int>(plan.tiles < pair_clusters ? plan.tiles : pair_clusters);
-    const int L = static_cast<int>((K + PairShape::BK - 1) / PairShape::BK);
-    const size_t need = workspace_need(plan, dev->sm_count, K);
-    const int workers = pair_split_workers(plan.tiles, L, pair_clusters);
-    if (workspace && need && workspace_bytes >= need && workers > 0) {
-      // every tile split (fewer than two waves): dp_tiles = 0
-      args.sk = StreamK{static_cast<int>(plan.tiles), L, workers, 0};
-      args.flags = static_cast<unsigned*>(workspace);
-      args.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                               streamk_flag_bytes(dev->sm_count));
-      args.epoch = next_epoch();
-      clusters = args.sk.G;
-    } else {
-      args.sk = make_stream_k(static_cast<int>(plan.tiles), L, clusters, false);
-    }
-    // C for the TMA-store epilogue (plain stores into a 16-byte-aligned C):
-    // box 32 columns x 32 rows of fp32 with the 128-byte swizzle.
-    CUtensorMap mc{};
-    if (epi == kEpiStore && !transa && !transb && plan.vec_store &&
-        (st = make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, ldc, 32, 32,
-                       CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
-      return st;
-    const uint32_t idesc2 =
-        idesc_f16_f32acc(bf16, PairShape::BM, PairShape::BN, transa != 0, transb == 0);
-    return finish(launch_hgemm_tc_pair(ma, mb, mc, args, idesc2, clusters, stream),
-                  "hgemm pair launch", stream);
+    return run_pair(plan, args, ma, mb, pair_clusters, false,
+                    idesc_f16_f32acc(bf16, PairShape::BM, PairShape::BN, transa != 0, transb == 0),
+                    K, dev->sm_count, workspace, workspace_bytes, stream);
   }
   if (plan.kernel == 3)
     plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
@@ -649,7 +697,8 @@ double schedule_efficiency(int dtype, int transa, int transb, int64_t M, int64_t
   gemm14_plan plan;
   plan_for(dtype, transa, transb, M, N, K, base, lda, base, ldb, base, ldc, dev->sm_count, &plan);
   if (plan.tiles <= 0 || workspace_need(plan, dev->sm_count, K) > 0) return 1.0;
-  const int64_t slots = plan.kernel == 3 ? dev->sm_count / 2 : dev->sm_count;
+  const int64_t slots =
+      plan.kernel == 3 || plan.kernel == 5 ? dev->sm_count / 2 : dev->sm_count;
   if (slots <= 0) return 1.0;
   const int64_t waves = (plan.tiles + slots - 1) / slots;
   return static_cast<double>(plan.tiles) / static_cast<double>(waves * slots);

@@ -71,14 +71,19 @@ __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n
 // sums of its 128 rows to its own workspace slot (worker w, rank r: slot
 // 2w + r, flag 2w + r), and the owner of a split tile adds, per CTA, the same
 // rank's partials of the later workers in worker order.
-template <bool kGeneral, bool kSK>
+// kTf32: fp32 operands read as tf32 (tcgen05 kind::tf32, K = 8 per MMA), A
+// stored M x K and B stored N x K, i.e. both K-major as TMA writes them: the
+// same 128-byte rows, boxes and descriptors as 16-bit K-major operands, a
+// k-block being 32 fp32 instead of 64 16-bit elements.
+template <bool kGeneral, bool kSK, bool kTf32>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
     hgemm_tc2_kernel(const __grid_constant__ CUtensorMap map_a,
                      const __grid_constant__ CUtensorMap map_b,
                      const __grid_constant__ CUtensorMap map_c, const GemmArgs args,
                      const uint32_t idesc) {
-  const int transa = kGeneral ? args.transa : 0;
-  const int transb = kGeneral ? args.transb : 0;
+  const int transa = kTf32 ? 0 : kGeneral ? args.transa : 0;
+  const int transb = kTf32 ? 1 : kGeneral ? args.transb : 0;
+  constexpr int BK = kTf32 ? 32 : P::BK;  // elements of a 128-byte k-block row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = align1024(smem_raw);
   uint8_t* out_stage = tiles + P::STAGES * P::STAGE_BYTES;  // epilogue staging for C
@@ -94,7 +99,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
   const int tiles_m = (M + P::BM - 1) / P::BM;
   const int tiles_n = (N + P::BN - 1) / P::BN;
   const int num_tiles = tiles_m * tiles_n;
-  const int kblocks = (K + P::BK - 1) / P::BK;
+  const int kblocks = (K + BK - 1) / BK;
   const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns,
                    mapa_shared(smem_u32(&sm.abort_flag), rank ^ 1u)};
   uint32_t prod_it = 0;
@@ -176,7 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
           const int n0 = tn * P::BN + static_cast<int>(rank) * 128;
           // A: one box of 64 k x 128 m, or (stored K x M) two of 64 m x 64 k.
           if (!transa) {
-            tma_load_2d_pair(a_st, &map_a, kb * P::BK, m0, full_leader);
+            tma_load_2d_pair(a_st, &map_a, kb * BK, m0, full_leader);
           } else {
 #pragma unroll
             for (int c = 0; c < 2; ++c)
@@ -190,7 +195,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
               tma_load_2d_pair(b_st + c * (64 * P::BK * 2), &map_b, n0 + c * 64, kb * P::BK,
                                full_leader);
           } else {
-            tma_load_2d_pair(b_st, &map_b, kb * P::BK, n0, full_leader);
+            tma_load_2d_pair(b_st, &map_b, kb * BK, n0, full_leader);
           }
         }
       }
@@ -222,7 +227,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
             // layout in both CTAs.
             const uint64_t a_desc = smem_desc_sw128(a_addr + kk * a_op.step, a_op.lbo, 1024);
             const uint64_t b_desc = smem_desc_sw128(b_addr + kk * b_op.step, b_op.lbo, 1024);
-            tc_mma_f16_pair(d_tmem, a_desc, b_desc, idesc, kb > kb0 || kk != 0);
+            if (kTf32)
+              tc_mma_tf32_pair(d_tmem, a_desc, b_desc, idesc, kb > kb0 || kk != 0);
+            else
+              tc_mma_f16_pair(d_tmem, a_desc, b_desc, idesc, kb > kb0 || kk != 0);
           }
           mma_issued = true;
           tc_commit_pair_multicast(&sm.empty[s], 0x3);
@@ -393,10 +401,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
   }
 }
 
-template <bool kGeneral, bool kSK>
+template <bool kGeneral, bool kSK, bool kTf32>
 cudaError_t set_pair_smem() {
-  return cudaFuncSetAttribute(hgemm_tc2_kernel<kGeneral, kSK>,
+  return cudaFuncSetAttribute(hgemm_tc2_kernel<kGeneral, kSK, kTf32>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES);
+}
+
+template <bool kTf32>
+cudaError_t set_pair_smem_all() {
+  cudaError_t e;
+  if ((e = set_pair_smem<false, false, kTf32>()) != cudaSuccess ||
+      (e = set_pair_smem<true, false, kTf32>()) != cudaSuccess ||
+      (e = set_pair_smem<false, true, kTf32>()) != cudaSuccess)
+    return e;
+  return set_pair_smem<true, true, kTf32>();
 }
 
 }  // namespace
@@ -407,15 +425,15 @@ int pair_max_clusters() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (have[dev]) return cached[dev];
-  if (set_pair_smem<false, false>() != cudaSuccess || set_pair_smem<true, false>() != cudaSuccess ||
-      set_pair_smem<false, true>() != cudaSuccess || set_pair_smem<true, true>() != cudaSuccess)
+  if (set_pair_smem_all<false>() != cudaSuccess || set_pair_smem_all<true>() != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(P::THREADS, 1, 1);
   cfg.dynamicSmemBytes = P::SMEM_BYTES;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2_kernel<false, false>, &cfg) != cudaSuccess)
+  if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2_kernel<false, false, false>, &cfg) !=
+      cudaSuccess)
     n = 0;
   cached[dev] = n;
   have[dev] = true;
@@ -424,12 +442,21 @@ int pair_max_clusters() {
 
 cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
                                  const CUtensorMap& map_c, const GemmArgs& args, uint32_t idesc,
-                                 int clusters, cudaStream_t stream) {
-  const bool general = args.transa || args.transb || args.epi != kEpiStore;
+                                 int clusters, bool tf32, cudaStream_t stream) {
+  // tf32 operands are stored M x K and N x K, which the tf32 variants fix at
+  // compile time: only the epilogue mode makes them general
+  const bool general =
+      (!tf32 && (args.transa || args.transb)) || args.epi != kEpiStore;
   const bool sk = args.sk.dp_tiles < args.sk.tiles;
   const dim3 grid(2 * clusters), block(P::THREADS);
-  auto kernel = sk ? (general ? hgemm_tc2_kernel<true, true> : hgemm_tc2_kernel<false, true>)
-                   : (general ? hgemm_tc2_kernel<true, false> : hgemm_tc2_kernel<false, false>);
+  auto kernel =
+      tf32 ? (sk ? (general ? hgemm_tc2_kernel<true, true, true> : hgemm_tc2_kernel<false, true, true>)
+                 : (general ? hgemm_tc2_kernel<true, false, true>
+                            : hgemm_tc2_kernel<false, false, true>))
+           : (sk ? (general ? hgemm_tc2_kernel<true, true, false>
+                            : hgemm_tc2_kernel<false, true, false>)
+                 : (general ? hgemm_tc2_kernel<true, false, false>
+                            : hgemm_tc2_kernel<false, false, false>));
   return launch_kernel(kernel, grid, block, P::SMEM_BYTES, stream, map_a, map_b, map_c, args,
                        idesc);
 }

@@ -157,9 +157,11 @@ int pair_max_clusters();
 // map_c: C as a 2-D fp32 tensor (box 32 columns x 32 rows, 128-byte swizzle)
 // for the TMA-store epilogue of the plain variant when C takes 16-byte stores
 // (args.vec_store); otherwise unused.
+// tf32: fp32 operands stored M x K and N x K read as tf32 (kind::tf32, a
+// k-block of 32 elements; maps of fp32 boxes 32 k x 128 rows, 128-byte swizzle).
 cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
                                  const CUtensorMap& map_c, const GemmArgs& args, uint32_t idesc,
-                                 int clusters, cudaStream_t stream);
+                                 int clusters, bool tf32, cudaStream_t stream);
 
 // Same kernel with the software loader (operands TMA cannot address).
 cudaError_t launch_hgemm_tc_soft(int bn, const GemmArgs& args, uint32_t idesc, int grid,

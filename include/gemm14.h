@@ -318,7 +318,9 @@ int gemm14_host_synchronize(void);
 typedef struct gemm14_plan {
   int kernel;     /* 1 = fp32 SIMT (FFMA), 2 = tcgen05 on one SM per tile,
                      3 = tcgen05 on CTA pairs (two SMs per 256 x 256 tile),
-                     4 = tcgen05 kind::tf32 on CTA pairs (TF32 / 3xTF32), 0 = no launch */
+                     4 = tcgen05 kind::tf32 on CTA pairs (TF32 / 3xTF32),
+                     5 = kernel 3 with kind::tf32 MMAs (TF32, A stored M x K and B
+                         stored N x K: both read as stored), 0 = no launch */
   int loader;     /* 1 = TMA, 2 = software loader (cp.async for fp32), 0 = none */
   int bm, bn, bk; /* output tile rows x columns, k-block depth */
   int stages;     /* shared-memory ring depth */

@@ -229,7 +229,16 @@ def test_plan_tf32_pairs_and_fallback(lib, dtype):
     assert p.smem_bytes <= 227 * 1024
     for ta, tb in ((1, 0), (0, 1), (1, 1)):
         st, pt = g14.plan_ex(dtype, ta, tb, 3072, 3072, 3072, P, 3072, P, 3072, P, 3072, 152)
-        assert st == 0 and pt == p
+        if dtype == TF32 and (ta, tb) == (0, 1):
+            # both operands K-major as stored: the 16-bit pair kernel with
+            # kind::tf32 MMAs, k-blocks of 32 fp32, no converter warps
+            assert st == 0 and pt.kernel == 5 and (pt.bm, pt.bn, pt.bk) == (256, 256, 32)
+            assert pt.tiles == 144 and pt.grid == 152 and pt.threads == 192
+            # 144 tiles on 76 clusters, 96 k-blocks: split, one 128 x 256 slot an SM
+            assert g14.workspace_bytes_ex(dtype, 0, 1, 3072, 3072, 3072, P, 3072, P, 3072, P,
+                                          3072, 152) == 768 + 152 * 128 * 256 * 4
+        else:
+            assert st == 0 and pt == p
     # pitches TMA cannot take: the fp32 SIMT kernel (cp.async loader)
     st, p2 = g14.plan(dtype, 4097, 3001, 513, P, 513, P, 3001, P, 3001, 152)
     assert st == 0 and p2.kernel == 1 and p2.loader == 2

@@ -211,3 +211,41 @@ def test_3xtf32_full_size_3072_sampled(oracle_mod, ta, tb):
     ok, w3 = oracle_mod.within_bound(Cg[ri, ci], ref, refabs, TOL["f32"])
     assert ok, w3
     print(f"3xtf32 3072^3 ta={ta} tb={tb}: worst {max(w1, w2, w3):.3g}")
+
+
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (2.5, 0.0), (-1.0, 1.0)])
+def test_tf32_nt_on_the_pair_kernel_matches_the_converter_kernel(oracle_mod, alpha, beta):
+    """TF32 with A stored M x K and B stored N x K runs the 16-bit pair
+    kernel's mainloop with kind::tf32 MMAs (plan kernel 5): the same tf32
+    values in the same MMAs as the converter kernel on NN storage, so the same
+    bits, alpha and beta included."""
+    M, N, K = 300, 520, 200
+    A, B = inputs.make(M, N, K, "f32", "normal", 1.0, seed=31)
+    C0 = torch.from_numpy(np.random.default_rng(6).standard_normal((M, N)).astype(np.float32))
+    P = 1 << 16
+    st, plan = g14.plan_ex(TF32, 0, 1, M, N, K, P, K, P, K, P, N, 152)
+    assert st == 0 and plan.kernel == 5
+    c_nt = run_mode(TF32, A, B, 0, 1, alpha, beta, C0)
+    c_nn = run_mode(TF32, A, B, 0, 0, alpha, beta, C0)
+    assert torch.equal(c_nt, c_nn)
+    check(oracle_mod, A, B, c_nt, TOL["f32"], 0, 1, alpha, beta, C0, rounded=True)
+
+
+def test_tf32_nt_split_over_clusters(oracle_mod):
+    """Few tiles with long k on plan kernel 5 with a workspace: the stream-K
+    split over clusters (4 tiles, 256 k-blocks: 16 workers), within the fp32
+    bound of the product of the truncated inputs."""
+    M, N, K = 512, 512, 8192
+    A, B = inputs.make(M, N, K, "f32", "normal", 1.0, seed=32)
+    Bs = B.t().contiguous()
+    a, b = A.cuda(), Bs.cuda()
+    need = g14.workspace_bytes_ex(TF32, 0, 1, M, N, K, a.data_ptr(), K, b.data_ptr(), K,
+                                  a.data_ptr(), N)
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    c = torch.full((M, N), float("nan"), device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    g14.gemm_ex(TF32, 0, 1, M, N, K, 1.0, a.data_ptr(), K, b.data_ptr(), K, 0.0, c.data_ptr(), N,
+                ws.data_ptr(), need, s)
+    assert g14.check_device_error(s) == 0
+    check(oracle_mod, A, B, c.cpu(), TOL["f32"], rounded=True)
