@@ -390,6 +390,8 @@ void schedule(const gemm14_plan& plan, int64_t K, int sm_count, void* workspace,
 // the start, where they always are), then the copy of A, then that of B.
 struct Repitch {
   bool a = false, b = false;     // which operands are copied
+  bool a_t = false, b_t = false; // ... transposed (tf32: into K-major storage)
+  int transa = 0, transb = 0;    // the call's storage of op(A), op(B) after the copies
   int64_t lda = 0, ldb = 0;      // their pitches in the workspace
   size_t sk_bytes = 0;           // the stream-K region (flags + slots)
   size_t a_off = 0, b_off = 0;   // byte offsets of the copies
@@ -404,21 +406,36 @@ void plan_repitch(int dtype, int transa, int transb, int64_t M, int64_t N, int64
                   const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
                   int64_t ldc, int sms, Repitch* r) {
   *r = Repitch{};
+  r->transa = transa;
+  r->transb = transb;
   if (M <= 0 || N <= 0 || K <= 0) return;
   const int eb = elem_bytes_of(dtype);
   const int64_t q = 16 / eb;
   r->a = !(aligned(A, 16) && lda % q == 0);
   r->b = !(aligned(B, 16) && ldb % q == 0);
+  // TF32: the tensor cores read fp32 operands straight from TMA only K-major
+  // (A stored M x K, B stored N x K, plan kernel 5); other storages are
+  // transposed into that form (the converter kernel runs at about a quarter
+  // of the speed).
+  if (dtype == GEMM14_DTYPE_TF32 && g_pair_enabled.load() && sms >= 2) {
+    r->a_t = transa != 0;
+    r->b_t = transb == 0;
+    r->a = r->a || r->a_t;
+    r->b = r->b || r->b_t;
+    r->transa = 0;
+    r->transb = 1;
+  }
   if (!r->a && !r->b) return;
-  const int64_t rows_a = transa ? K : M, cols_a = transa ? M : K;
-  const int64_t rows_b = transb ? N : K, cols_b = transb ? K : N;
+  // Stored shape of each copy: as the source, or transposed.
+  const int64_t rows_a = r->transa ? K : M, cols_a = r->transa ? M : K;
+  const int64_t rows_b = r->transb ? N : K, cols_b = r->transb ? K : N;
   r->lda = r->a ? (cols_a + q - 1) / q * q : lda;
   r->ldb = r->b ? (cols_b + q - 1) / q * q : ldb;
-  // The plan of the copies: only their alignment enters it.
+  // The plan of the copies: only their alignment and storage enter it.
   const void* base = reinterpret_cast<const void*>(uintptr_t(1) << 12);
   gemm14_plan plan;
-  plan_for(dtype, transa, transb, M, N, K, r->a ? base : A, r->lda, r->b ? base : B, r->ldb, C,
-           ldc, sms, &plan);
+  plan_for(dtype, r->transa, r->transb, M, N, K, r->a ? base : A, r->lda, r->b ? base : B,
+           r->ldb, C, ldc, sms, &plan);
   const size_t sk = workspace_need(plan, sms, K);
   r->sk_bytes = sk;
   const size_t flags = streamk_flag_bytes(sms);
@@ -517,18 +534,25 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
     plan_repitch(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &rp);
     if ((rp.a || rp.b) && workspace_bytes >= rp.total) {
       char* ws = static_cast<char*>(workspace);
-      RepitchJob ja{nullptr, 0, nullptr, 0, 0, 0}, jb{nullptr, 0, nullptr, 0, 0, 0};
+      RepitchJob ja{nullptr, 0, nullptr, 0, 0, 0, 0}, jb{nullptr, 0, nullptr, 0, 0, 0, 0};
       if (rp.a) {
-        ja = RepitchJob{A, lda, ws + rp.a_off, rp.lda, transa ? K : M, transa ? M : K};
+        // source rows x cols as stored; the copy is that, or its transpose
+        ja = RepitchJob{A, lda, ws + rp.a_off, rp.lda, transa ? K : M, transa ? M : K,
+                        rp.a_t ? 1 : 0};
         A = ws + rp.a_off;
         lda = rp.lda;
       }
       if (rp.b) {
-        jb = RepitchJob{B, ldb, ws + rp.b_off, rp.ldb, transb ? N : K, transb ? K : N};
+        jb = RepitchJob{B, ldb, ws + rp.b_off, rp.ldb, transb ? N : K, transb ? K : N,
+                        rp.b_t ? 1 : 0};
         B = ws + rp.b_off;
         ldb = rp.ldb;
       }
-      const cudaError_t e = launch_repitch(ja, jb, elem_bytes_of(dtype), dev->sm_count, stream);
+      transa = rp.transa;
+      transb = rp.transb;
+      const cudaError_t e =
+          rp.a_t || rp.b_t ? launch_relayout(ja, jb, dev->sm_count, stream)
+                           : launch_repitch(ja, jb, elem_bytes_of(dtype), dev->sm_count, stream);
       if (e != cudaSuccess) return finish(e, "re-pitch launch", stream);
       workspace_bytes = rp.a_off;
     }

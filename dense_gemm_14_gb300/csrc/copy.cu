@@ -1,7 +1,8 @@
 // copy.cu -- re-pitching an operand that TMA cannot address (a base or a
 // row pitch that is not a multiple of 16 bytes) into a caller workspace with a
 // 16-byte pitch, so that the product runs on the TMA loaders instead of the
-// element-wise ones. A memory-bound pass: each element is read and written
+// element-wise ones; and, for tf32 products, transposing an fp32 operand into
+// the K-major storage the tensor cores read straight from TMA. A memory-bound pass: each element is read and written
 // once. The work items are segments of kUnroll x 32 consecutive elements of a
 // row; a warp loads a whole segment (its lanes on consecutive elements, so
 // reads and writes are coalesced whatever the source alignment) before it
@@ -48,7 +49,61 @@ __global__ void __launch_bounds__(256) repitch_kernel(const RepitchJob j0, const
   }
 }
 
+// Both jobs of a relayout: fp32 matrices copied, each transposed or not
+// (job.transpose), in 32 x 32 tiles through shared memory: a tile is read
+// along its source rows and written along its destination rows, so both
+// sides stay coalesced. Element (r, c) of a transposed job's source lands at
+// (c, r) of its destination.
+__global__ void __launch_bounds__(256) relayout_kernel(const RepitchJob j0, const RepitchJob j1) {
+  __shared__ float tile[32][33];
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  const int64_t tc0 = (j0.cols + 31) / 32, tc1 = (j1.cols + 31) / 32;
+  const int64_t tiles0 = ((j0.rows + 31) / 32) * tc0;
+  const int64_t tiles = tiles0 + ((j1.rows + 31) / 32) * tc1;
+  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    const bool first = t < tiles0;
+    const RepitchJob& j = first ? j0 : j1;
+    const int64_t tcols = first ? tc0 : tc1;
+    const int64_t i = first ? t : t - tiles0;
+    const int64_t r0 = (i / tcols) * 32, c0 = (i % tcols) * 32;
+    const float* src = static_cast<const float*>(j.src);
+    float* dst = static_cast<float*>(j.dst);
+#pragma unroll
+    for (int k = ty; k < 32; k += 8) {
+      const int64_t r = r0 + k, c = c0 + tx;
+      tile[k][tx] = r < j.rows && c < j.cols ? src[r * j.ld_src + c] : 0.0f;
+    }
+    __syncthreads();
+    if (j.transpose) {
+#pragma unroll
+      for (int k = ty; k < 32; k += 8) {
+        const int64_t c = c0 + k, r = r0 + tx;  // destination row c, column r
+        if (c < j.cols && r < j.rows) dst[c * j.ld_dst + r] = tile[tx][k];
+      }
+    } else {
+#pragma unroll
+      for (int k = ty; k < 32; k += 8) {
+        const int64_t r = r0 + k, c = c0 + tx;
+        if (r < j.rows && c < j.cols) dst[r * j.ld_dst + c] = tile[k][tx];
+      }
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_relayout(const RepitchJob& j0, const RepitchJob& j1, int sm_count,
+                            cudaStream_t stream) {
+  const int64_t tiles = ((j0.rows + 31) / 32) * ((j0.cols + 31) / 32) +
+                        ((j1.rows + 31) / 32) * ((j1.cols + 31) / 32);
+  if (tiles <= 0) return cudaSuccess;
+  const int64_t cap = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 8;
+  const dim3 grid(static_cast<unsigned>(tiles < cap ? tiles : cap));
+  return launch_kernel(relayout_kernel, grid, dim3(256), 0, stream, j0, j1);
+}
 
 cudaError_t launch_repitch(const RepitchJob& j0, const RepitchJob& j1, int elem_bytes,
                            int sm_count, cudaStream_t stream) {

@@ -202,10 +202,14 @@ struct RepitchJob {
   void* dst;
   int64_t ld_dst;
   int64_t rows, cols;
+  int transpose;  // relayout only: the destination is the cols x rows transpose
 };
 // Both copies in one launch on `stream`, elements of elem_bytes (2 or 4) (copy.cu).
 cudaError_t launch_repitch(const RepitchJob& j0, const RepitchJob& j1, int elem_bytes,
                            int sm_count, cudaStream_t stream);
+// Both fp32 copies in one launch, each transposed when job.transpose (copy.cu).
+cudaError_t launch_relayout(const RepitchJob& j0, const RepitchJob& j1, int sm_count,
+                            cudaStream_t stream);
 
 // ---- C = beta * C over an M x N block (epilogue.cu): the call when the
 // product term vanishes (K == 0 or alpha == 0) and beta is not 0 or 1.

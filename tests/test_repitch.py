@@ -139,3 +139,30 @@ def test_tensor_level_call_repitches():
     g14.gemm_into(a_pad[:, :K], B.cuda(), out2)
     torch.cuda.synchronize()
     assert torch.equal(out1, out2)
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (513, 700, 129), (1000, 777, 301)])
+def test_tf32_any_storage_runs_k_major_with_a_workspace(oracle_mod, ta, tb, M, N, K):
+    """TF32 with a workspace of workspace_bytes_ex bytes: MN-major operands are
+    transposed into K-major copies (odd pitches re-pitched on the way) and the
+    product runs on the pair kernel as for A stored M x K and B stored N x K,
+    with that storage's bits."""
+    A, B = inputs.make(M, N, K, "f32", "normal", 1.0, seed=M + 3 * N + 7 * K + ta + 2 * tb)
+    C, need = run("tf32", A, B, ta, tb)
+    assert need > 0
+    C_nt, _ = run("tf32", A, B, 0, 1)
+    assert torch.equal(C, C_nt)
+    As, Bs = oracle_mod.truncate_tf32(A.numpy()), oracle_mod.truncate_tf32(B.numpy())
+    ref, refabs = oracle_mod.gemm(As, Bs)
+    ok, worst = oracle_mod.within_bound(C.numpy(), ref, refabs, TOL["f32"])
+    assert ok, worst
+
+
+def test_tf32_transposed_copies_with_alpha_beta(oracle_mod):
+    M, N, K = 700, 530, 333
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=41)
+    C0 = torch.from_numpy(np.random.default_rng(42).standard_normal((M, N)).astype(np.float32))
+    C, need = run("tf32", A, B, 1, 0, a_off=1, alpha=-1.5, beta=0.5, C0=C0)
+    C_nt, _ = run("tf32", A, B, 0, 1, alpha=-1.5, beta=0.5, C0=C0)
+    assert need > 0 and torch.equal(C, C_nt)

@@ -102,3 +102,25 @@ def test_workspace_bytes_ex_adds_room_to_repitch():
     # nothing to compute, or invalid arguments: 0
     assert ex(F32, 0, 0, 8, 8, 0, 0, 1, 0, 8, P, 8, 152) == 0
     assert ex(F32, 0, 0, 8, 8, 8, P, 7, P, 8, P, 8, 152) == 0
+
+
+def test_workspace_bytes_ex_tf32_transposes_into_k_major():
+    """TF32 reads fp32 operands straight from TMA only K-major (A stored M x K,
+    B stored N x K): other storages get K-major copies in the workspace, after
+    the stream-K region of the pair kernel's split (plan kernel 5)."""
+    g14.load()
+    TF32, X3 = g14.GEMM14_DTYPE_TF32, g14.GEMM14_DTYPE_F32_3XTF32
+    P = 1 << 20
+    n = 3072
+    sk = 768 + 152 * 128 * 256 * 4        # 144 pair tiles, 96 k-blocks: split
+    ex = g14.workspace_bytes_ex
+    assert ex(TF32, 0, 1, n, n, n, P, n, P, n, P, n, 152) == sk            # NT: as stored
+    assert ex(TF32, 0, 0, n, n, n, P, n, P, n, P, n, 152) == sk + n * n * 4  # B^T
+    assert ex(TF32, 1, 1, n, n, n, P, n, P, n, P, n, 152) == sk + n * n * 4  # A^T
+    assert ex(TF32, 1, 0, n, n, n, P, n, P, n, P, n, 152) == sk + 2 * n * n * 4
+    # 3xTF32 needs its lo tiles in every storage: no transposed copies
+    assert ex(X3, 0, 0, n, n, n, P, n, P, n, P, n, 152) == 0
+    # a transposed copy has K rounded up to 4 floats: B (K x N) -> N x round4(K);
+    # 4 pair tiles of 32 k-blocks are not split, so the copy follows the flags
+    M, N, K = 512, 384, 1001
+    assert ex(TF32, 0, 0, M, N, K, P, 1004, P, N, P, N, 152) == 768 + N * 1004 * 4
