@@ -304,10 +304,14 @@ int slots_per_worker(const gemm14_plan& plan) { return plan.kernel == 1 ? 2 : 1;
 
 // The CTA-pair kernel's split, measured on GB300 against its unsplit run:
 // - between one and two waves of tiles with long k (>= 64 k-blocks a tile):
-//   2304x2560x8192 (1.18 waves) 86 -> 74 us;
-// - beyond two waves it gained nothing (8192^3, 16384x11008x4096: within
-//   1 %) or lost (4096x4096x16384: +21 %: ranges that start mid-tile no
-//   longer sweep k together, so clusters stop sharing A and B in L2);
+//   every tile split, 2304x2560x8192 (1.18 waves) 86 -> 74 us;
+// - beyond two waves, splitting every tile gained nothing (8192^3,
+//   16384x11008x4096: within 1 %) or lost (4096x4096x16384: +21 %: ranges
+//   that start mid-tile no longer sweep k together, so clusters stop sharing
+//   A and B in L2); splitting only the last one and a half waves (the rest
+//   data-parallel, as on the one-SM kernels) gains what the partial last wave
+//   wasted: bf16 8192^3 (13.47 waves) -1.6 %, 16384x11008x4096 -1.4 %, fp16
+//   8192^3 -2.5 %;
 // - few tiles split over every cluster made the owner add up to ~19 partial
 //   sums one after another (512x512x16384: no gain): there the workers are
 //   capped at 4 per tile and at ranges of at least 32 k-blocks.
@@ -322,6 +326,7 @@ int pair_split_workers(int64_t tiles, int64_t L, int clusters) {
   }
   if (tiles > clusters && tiles < 2 * static_cast<int64_t>(clusters) && L >= 64)
     return clusters;
+  if (tiles >= 2 * static_cast<int64_t>(clusters) && tiles % clusters != 0) return clusters;
   return 0;
 }
 
@@ -472,8 +477,11 @@ int run_pair(const gemm14_plan& plan, GemmArgs& args, const CUtensorMap& ma,
   const size_t need = workspace_need(plan, sm_count, K);
   const int workers = pair_split_workers(plan.tiles, L, pair_clusters);
   if (workspace && need && workspace_bytes >= need && workers > 0) {
-    // every tile split (fewer than two waves): dp_tiles = 0
-    args.sk = StreamK{static_cast<int>(plan.tiles), L, workers, 0};
+    if (plan.tiles >= 2 * static_cast<int64_t>(pair_clusters))
+      // whole waves data-parallel, the last one and a half split
+      args.sk = make_stream_k(static_cast<int>(plan.tiles), L, workers, true);
+    else  // fewer than two waves: every tile split (dp_tiles = 0)
+      args.sk = StreamK{static_cast<int>(plan.tiles), L, workers, 0};
     args.flags = static_cast<unsigned*>(workspace);
     args.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                              streamk_flag_bytes(sm_count));

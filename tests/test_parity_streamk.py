@@ -110,7 +110,9 @@ def test_workspace_reused_across_shapes(oracle_mod):
 
 PAIR_CASES = [(512, 512, 16384),    # 4 pair tiles: 4 workers per tile
               (2304, 2560, 8192),   # 90 tiles, 1.2 waves: every tile split
-              (2304, 2560, 4100)]   # the same with a ragged last k-block
+              (2304, 2560, 4100),   # the same with a ragged last k-block
+              (4096, 4096, 1024),   # 256 tiles, 3.4 waves: the last 1.4 split
+              (3000, 4100, 777)]    # 204 ragged tiles, 2.7 waves, ragged k
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f16"])
@@ -156,3 +158,17 @@ def test_pair_streamk_expired_wait_reports_timeout(oracle_mod):
     assert g14.check_device_error(s.cuda_stream) == _lib.GEMM14_ERR_TIMEOUT
     C = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), workspace=ws)
     oracle_check(oracle_mod, A, B, C)
+
+
+def test_pair_hybrid_split_integer_exact():
+    """More than two waves that are not whole: whole waves data-parallel, the
+    last one and a half split; integer inputs stay exact, and the result is
+    the bits of the next call (a new epoch on the same workspace)."""
+    M, N, K = 4096, 4096, 1024
+    Ai, Bi = inputs.make_integer(M, N, K, 4, "bf16", seed=66)
+    want = (Ai.double() @ Bi.double()).float()
+    ws = make_workspace("bf16", M, N, K)
+    assert ws.numel() > 256
+    C1 = run_abi(Ai, Bi, workspace=ws)
+    assert torch.equal(C1, want)
+    assert torch.equal(run_abi(Ai, Bi, workspace=ws), C1)

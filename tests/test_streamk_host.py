@@ -45,8 +45,11 @@ def test_workspace_bytes():
     pair_ws = 768 + 152 * 128 * 256 * 4
     assert g14.workspace_bytes(BF16, 2304, 2560, 8192, 152) == pair_ws
     assert g14.workspace_bytes(BF16, 512, 512, 16384, 152) == pair_ws
-    # ... and not beyond two waves (8192^3: 13.47 waves), nor with short k
-    assert g14.workspace_bytes(BF16, 8192, 8192, 8192, 152) == 0
+    # ... beyond two waves that are not whole, the last one and a half waves
+    # (8192^3: 1024 tiles = 13.47 waves on 76 clusters) ...
+    assert g14.workspace_bytes(BF16, 8192, 8192, 8192, 152) == pair_ws
+    # ... but not whole waves (152 tiles on 76 clusters), nor short k below two waves
+    assert g14.workspace_bytes(BF16, 2048, 4864, 8192, 152) == 0
     assert g14.workspace_bytes(BF16, 2304, 2560, 2000, 152) == 0
     assert g14.workspace_bytes(BF16, 1000, 776, 1000, 152) == 0
     # whole waves use none; invalid args -> 0
