@@ -167,3 +167,34 @@ def test_c_abi_host_entry_degenerate_calls():
     assert g14.host_wait(t) == 0
     assert torch.equal(C, torch.arange(12, dtype=torch.float32).view(3, 4) * 0.5)
     assert g14.host_synchronize() == 0
+
+
+def test_host_calls_from_several_threads():
+    """Four threads issue and wait for host-buffer products at the same time
+    (ctypes releases the GIL around each call): each result is the bits of
+    the same product issued alone."""
+    import threading
+    cases = [inputs.make(700 + 64 * t, 300 + 32 * t, 257, "f32", "normal", 0.2, seed=80 + t)
+             for t in range(4)]
+    want = [g14.gemm(A, B) for A, B in cases]
+    got = [[None] * 5 for _ in range(4)]
+    errors = []
+
+    def work(t):
+        try:
+            A, B = cases[t]
+            hs = [g14.gemm_async(A, B) for _ in range(5)]
+            for i, h in enumerate(hs):
+                got[t][i] = h.wait()
+        except Exception as e:  # reported by the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=work, args=(t,)) for t in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join(timeout=120)
+    assert not errors, errors
+    for t in range(4):
+        for i in range(5):
+            assert torch.equal(got[t][i], want[t]), (t, i)
