@@ -588,8 +588,6 @@ def run_table_ex(args):
     for name in ("f32_3072", "bf16_8192", "f16_8192"):
         w, fl, ib = workload_info(name)
         A, B = inputs.make_workload(name)
-        ws_bytes = g14.workspace_bytes(code[w.dtype], w.M, w.N, w.K, 0)
-        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
         for ta, tb, alpha, beta in EX_VARIANTS:
             As = (A.t().contiguous() if ta else A).cuda()
             Bs = (B.t().contiguous() if tb else B).cuda()
@@ -598,6 +596,12 @@ def run_table_ex(args):
             sets = [(As.clone(), Bs.clone(), torch.zeros(w.M, w.N, device="cuda"))
                     for _ in range(nsets)]
             lda, ldb = As.shape[1], Bs.shape[1]
+            # the workspace this call asks for (stream-K region, and copies of
+            # operands in a storage its kernel reads slowly)
+            ws_bytes = g14.workspace_bytes_ex(code[w.dtype], ta, tb, w.M, w.N, w.K,
+                                              sets[0][0].data_ptr(), lda, sets[0][1].data_ptr(),
+                                              ldb, sets[0][2].data_ptr(), w.N)
+            ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
 
             def launch(i):
                 a, b, c = sets[i % nsets]
@@ -668,9 +672,14 @@ def run_table_tf32(args):
         per_set = (M * K + K * N + M * N) * 4
         nsets = max(2, -(-2 * L2_BYTES // per_set))
         sets = [(A.cuda(), B.cuda(), torch.empty(M, N, device="cuda")) for _ in range(nsets)]
-        ws_bytes = g14.workspace_bytes(g14.GEMM14_DTYPE_F32, M, N, K, 0)
-        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
         for mode, code in modes:
+            # the workspace each mode asks for with these operands (TF32 on
+            # row-major B: room for its K-major copy)
+            a0, b0, c0 = sets[0]
+            ws_bytes = g14.workspace_bytes_ex(code, 0, 0, M, N, K, a0.data_ptr(), K, b0.data_ptr(),
+                                              N, c0.data_ptr(), N)
+            ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+
             def launch(i):
                 a, b, c = sets[i % nsets]
                 g14.gemm_ex(code, 0, 0, M, N, K, 1.0, a.data_ptr(), K, b.data_ptr(), N, 0.0,

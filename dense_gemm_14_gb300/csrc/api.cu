@@ -430,6 +430,15 @@ void plan_repitch(int dtype, int transa, int transb, int64_t M, int64_t N, int64
     r->transa = 0;
     r->transb = 1;
   }
+  // fp32 FFMA: B stored N x K (K-major in shared memory) needs per-k packing
+  // of its pairs and measured 42 % of the FFMA peak, against 76 % for B
+  // stored K x N (A stored K x M is the fastest storage of A, 80.5 %): B is
+  // transposed into K x N.
+  if (dtype == GEMM14_DTYPE_F32 && transb) {
+    r->b_t = true;
+    r->b = true;
+    r->transb = 0;
+  }
   if (!r->a && !r->b) return;
   // Stored shape of each copy: as the source, or transposed.
   const int64_t rows_a = r->transa ? K : M, cols_a = r->transa ? M : K;

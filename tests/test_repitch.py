@@ -166,3 +166,16 @@ def test_tf32_transposed_copies_with_alpha_beta(oracle_mod):
     C, need = run("tf32", A, B, 1, 0, a_off=1, alpha=-1.5, beta=0.5, C0=C0)
     C_nt, _ = run("tf32", A, B, 0, 1, alpha=-1.5, beta=0.5, C0=C0)
     assert need > 0 and torch.equal(C, C_nt)
+
+
+@pytest.mark.parametrize("ta", [0, 1])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (1000, 777, 301), (3072, 3072, 3072)])
+def test_fp32_b_stored_n_by_k_runs_k_by_n(oracle_mod, ta, M, N, K):
+    """fp32 with B stored N x K and a workspace: B is transposed into K x N and
+    the product has the bits of B stored K x N from the start."""
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=M + N + K + ta)
+    C, need = run("f32", A, B, ta, 1)
+    assert need > 0
+    C_kn, _ = run("f32", A, B, ta, 0)
+    assert torch.equal(C, C_kn)
+    oracle_check(oracle_mod, A, B, C, rows=np.arange(0, M, 17) if M * N * K > 1e9 else None)

@@ -127,3 +127,17 @@ def test_workspace_bytes_ex_tf32_transposes_into_k_major():
     # 4 pair tiles of 32 k-blocks are not split, so the copy follows the flags
     M, N, K = 512, 384, 1001
     assert ex(TF32, 0, 0, M, N, K, P, 1004, P, N, P, N, 152) == 768 + N * 1004 * 4
+
+
+def test_workspace_bytes_ex_fp32_b_stored_n_by_k():
+    """fp32 FFMA with B stored N x K gets a K x N copy of B (its fast storage)."""
+    g14.load()
+    F32 = g14.GEMM14_DTYPE_F32
+    P = 1 << 20
+    n = 3072
+    sk = g14.workspace_bytes(F32, n, n, n, 152)
+    ex = g14.workspace_bytes_ex
+    assert ex(F32, 0, 0, n, n, n, P, n, P, n, P, n, 152) == sk
+    assert ex(F32, 1, 0, n, n, n, P, n, P, n, P, n, 152) == sk
+    assert ex(F32, 0, 1, n, n, n, P, n, P, n, P, n, 152) == sk + n * n * 4
+    assert ex(F32, 1, 1, n, n, n, P, n, P, n, P, n, 152) == sk + n * n * 4
