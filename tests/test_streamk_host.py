@@ -83,17 +83,19 @@ def test_workspace_bytes_ex_adds_room_to_repitch():
     F32, BF16 = g14.GEMM14_DTYPE_F32, g14.GEMM14_DTYPE_BF16
     P = 1 << 20
     ex = g14.workspace_bytes_ex
-    # aligned: the same as the shape-only query, any storage
-    for dt, M, N, K in ((F32, 3072, 3072, 3072), (F32, 4097, 3001, 516), (BF16, 1024, 64, 4096),
-                        (BF16, 16384, 64, 4096), (BF16, 2304, 2560, 8192)):
+    # aligned: the same as the shape-only query (fp32 narrower than 2048
+    # columns: no transposed copy of A, below)
+    for dt, M, N, K in ((F32, 3072, 2000, 3072), (F32, 4097, 1001, 516), (BF16, 1024, 64, 4096),
+                        (BF16, 16384, 64, 4096), (BF16, 2304, 2560, 8192), (BF16, 3072, 3072, 3072)):
         lda, ldb = (K + 7) // 8 * 8, (N + 7) // 8 * 8
         assert ex(dt, 0, 0, M, N, K, P, lda, P, ldb, P, ldb, 152) == \
             g14.workspace_bytes(dt, M, N, K, 152)
-    # fp32 4097 x 3001 x 513 (pitches 2052 and 12004 bytes): both copied
+    # fp32 4097 x 3001 x 513 (pitches 2052 and 12004 bytes): both copied, A
+    # transposed into K x M (N >= 2048) with a pitch of 4100 floats
     M, N, K = 4097, 3001, 513
     sk = 768 + 2 * 152 * 128 * 256 * 4          # 396 tiles: split, two fp32 slots per SM
     a_off = _r256(sk)
-    b_off = _r256(a_off + M * 516 * 4)
+    b_off = _r256(a_off + K * 4100 * 4)
     assert ex(F32, 0, 0, M, N, K, P, K, P, N, P, N, 152) == b_off + K * 3004 * 4
     # only B unaligned (bf16, ldb odd), 128 tiles (not split): the copy after the flags
     M, N, K = 16384, 64, 4096
@@ -137,7 +139,11 @@ def test_workspace_bytes_ex_fp32_b_stored_n_by_k():
     n = 3072
     sk = g14.workspace_bytes(F32, n, n, n, 152)
     ex = g14.workspace_bytes_ex
-    assert ex(F32, 0, 0, n, n, n, P, n, P, n, P, n, 152) == sk
     assert ex(F32, 1, 0, n, n, n, P, n, P, n, P, n, 152) == sk
-    assert ex(F32, 0, 1, n, n, n, P, n, P, n, P, n, 152) == sk + n * n * 4
     assert ex(F32, 1, 1, n, n, n, P, n, P, n, P, n, 152) == sk + n * n * 4
+    # A stored M x K is transposed into K x M when N >= 2048 (5 % faster kernel)
+    assert ex(F32, 0, 0, n, n, n, P, n, P, n, P, n, 152) == sk + n * n * 4
+    assert ex(F32, 0, 1, n, n, n, P, n, P, n, P, n, 152) == sk + 2 * n * n * 4
+    # ... not for narrower products
+    assert ex(F32, 0, 0, n, 2047, n, P, n, P, 2048, P, 2048, 152) == \
+        g14.workspace_bytes(F32, n, 2047, n, 152)
