@@ -50,45 +50,56 @@ __global__ void __launch_bounds__(256) repitch_kernel(const RepitchJob j0, const
 }
 
 // Both jobs of a relayout: fp32 matrices copied, each transposed or not
-// (job.transpose), in 32 x 32 tiles through shared memory: a tile is read
+// (job.transpose), in 64 x 64 tiles through shared memory: a tile is read
 // along its source rows and written along its destination rows, so both
-// sides stay coalesced. Element (r, c) of a transposed job's source lands at
-// (c, r) of its destination.
+// sides stay coalesced, and each thread has its 16 loads in flight before
+// the barrier. Element (r, c) of a transposed job's source lands at (c, r) of
+// its destination. The tile's rows are padded to 65 floats, so the column
+// reads of the transposed store hit 32 different banks.
+constexpr int kRt = 64;
+
 __global__ void __launch_bounds__(256) relayout_kernel(const RepitchJob j0, const RepitchJob j1) {
-  __shared__ float tile[32][33];
+  __shared__ float tile[kRt][kRt + 1];
   grid_dependency_wait();
   grid_launch_dependents();
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
-  const int64_t tc0 = (j0.cols + 31) / 32, tc1 = (j1.cols + 31) / 32;
-  const int64_t tiles0 = ((j0.rows + 31) / 32) * tc0;
-  const int64_t tiles = tiles0 + ((j1.rows + 31) / 32) * tc1;
+  const int64_t tc0 = (j0.cols + kRt - 1) / kRt, tc1 = (j1.cols + kRt - 1) / kRt;
+  const int64_t tiles0 = ((j0.rows + kRt - 1) / kRt) * tc0;
+  const int64_t tiles = tiles0 + ((j1.rows + kRt - 1) / kRt) * tc1;
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
     const bool first = t < tiles0;
     const RepitchJob& j = first ? j0 : j1;
     const int64_t tcols = first ? tc0 : tc1;
     const int64_t i = first ? t : t - tiles0;
-    const int64_t r0 = (i / tcols) * 32, c0 = (i % tcols) * 32;
+    const int64_t r0 = (i / tcols) * kRt, c0 = (i % tcols) * kRt;
     const float* src = static_cast<const float*>(j.src);
     float* dst = static_cast<float*>(j.dst);
+    float v[kRt / 8][2];
 #pragma unroll
-    for (int k = ty; k < 32; k += 8) {
-      const int64_t r = r0 + k, c = c0 + tx;
-      tile[k][tx] = r < j.rows && c < j.cols ? src[r * j.ld_src + c] : 0.0f;
-    }
+    for (int k = 0; k < kRt / 8; ++k)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t r = r0 + ty + 8 * k, c = c0 + tx + 32 * h;
+        v[k][h] = r < j.rows && c < j.cols ? src[r * j.ld_src + c] : 0.0f;
+      }
+#pragma unroll
+    for (int k = 0; k < kRt / 8; ++k)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) tile[ty + 8 * k][tx + 32 * h] = v[k][h];
     __syncthreads();
-    if (j.transpose) {
 #pragma unroll
-      for (int k = ty; k < 32; k += 8) {
-        const int64_t c = c0 + k, r = r0 + tx;  // destination row c, column r
-        if (c < j.cols && r < j.rows) dst[c * j.ld_dst + r] = tile[tx][k];
-      }
-    } else {
+    for (int k = 0; k < kRt / 8; ++k)
 #pragma unroll
-      for (int k = ty; k < 32; k += 8) {
-        const int64_t r = r0 + k, c = c0 + tx;
-        if (r < j.rows && c < j.cols) dst[r * j.ld_dst + c] = tile[k][tx];
+      for (int h = 0; h < 2; ++h) {
+        if (j.transpose) {
+          // destination row c0 + ty + 8k, column r0 + tx + 32h
+          const int64_t c = c0 + ty + 8 * k, r = r0 + tx + 32 * h;
+          if (c < j.cols && r < j.rows) dst[c * j.ld_dst + r] = tile[tx + 32 * h][ty + 8 * k];
+        } else {
+          const int64_t r = r0 + ty + 8 * k, c = c0 + tx + 32 * h;
+          if (r < j.rows && c < j.cols) dst[r * j.ld_dst + c] = tile[ty + 8 * k][tx + 32 * h];
+        }
       }
-    }
     __syncthreads();
   }
 }
@@ -97,8 +108,8 @@ __global__ void __launch_bounds__(256) relayout_kernel(const RepitchJob j0, cons
 
 cudaError_t launch_relayout(const RepitchJob& j0, const RepitchJob& j1, int sm_count,
                             cudaStream_t stream) {
-  const int64_t tiles = ((j0.rows + 31) / 32) * ((j0.cols + 31) / 32) +
-                        ((j1.rows + 31) / 32) * ((j1.cols + 31) / 32);
+  const int64_t tiles = ((j0.rows + kRt - 1) / kRt) * ((j0.cols + kRt - 1) / kRt) +
+                        ((j1.rows + kRt - 1) / kRt) * ((j1.cols + kRt - 1) / kRt);
   if (tiles <= 0) return cudaSuccess;
   const int64_t cap = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 8;
   const dim3 grid(static_cast<unsigned>(tiles < cap ? tiles : cap));
