@@ -12,8 +12,8 @@
 //   warp 0      producer: TMA loads of A (128 m x 64 k, K-major, 128-byte
 //               swizzle) and B (BN/64 boxes of 64 n x 64 k, N-major, 128-byte
 //               swizzle) into an S-stage ring (full/empty mbarriers); for
-//               operands TMA cannot address, the whole warp fills the same
-//               layout with plain loads and stores;
+//               operands TMA cannot address, warp 0 and 7 more warps (6 ..)
+//               fill the same layout with plain loads and stores;
 //   warp 1      allocates 2*BN TMEM columns (two accumulators) and one lane
 //               issues 4 x tcgen05.mma (K = 16 each) per 64-deep k-block;
 //               tcgen05.commit frees the smem stage and, at the end of a
@@ -74,58 +74,82 @@ __device__ __forceinline__ uint32_t ld_pair(const uint16_t* base, int64_t row_of
   return lo | (hi << 16);
 }
 
-// A K-major operand tile of ROWS rows (matrix rows row0 ..) by 64 k (from
-// k0): 128-byte rows. Lane l holds k pair (2l, 2l+1) of a row; its 4-byte word
-// sits in 16-byte chunk (l / 4) XOR (row % 8), at byte 4 (l % 4) of the chunk.
+// The software loader runs on kSoftWarps warps (warp 0 and warps 6 ..), each
+// filling every kSoftWarps-th row of a stage, so that they have all their loads
+// of a stage in flight together (one warp alone is latency-bound: about 4 KB
+// in flight per SM).
+constexpr int kSoftWarps = 8;
+
+// Rows part, part + kSoftWarps, ... of a K-major operand tile of ROWS rows
+// (matrix rows row0 ..) by 64 k (from k0): 128-byte rows. Lane l holds k pair
+// (2l, 2l+1) of a row; its 4-byte word sits in 16-byte chunk (l / 4) XOR
+// (row % 8), at byte 4 (l % 4) of the chunk.
 template <int ROWS>
 __device__ __forceinline__ void soft_kmajor(uint8_t* dst, const uint16_t* src, int64_t ld,
-                                            int row0, int nrows, int k0, int K, int lane) {
+                                            int row0, int nrows, int k0, int K, int lane,
+                                            int part) {
+  constexpr int N = ROWS / kSoftWarps;
   const uint32_t word = static_cast<uint32_t>((lane & 3) << 2);
   const int k = k0 + 2 * lane;
-#pragma unroll 4
-  for (int r = 0; r < ROWS; ++r) {
-    const int m = row0 + r;
-    const uint32_t v = ld_pair(src, static_cast<int64_t>(m) * ld, k, K, m < nrows);
-    *reinterpret_cast<uint32_t*>(dst + r * 128 + ((((lane >> 2) ^ (r & 7)) & 7) << 4) + word) = v;
+  uint32_t v[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const int m = row0 + part + i * kSoftWarps;
+    v[i] = ld_pair(src, static_cast<int64_t>(m) * ld, k, K, m < nrows);
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const int r = part + i * kSoftWarps;
+    *reinterpret_cast<uint32_t*>(dst + r * 128 + ((((lane >> 2) ^ (r & 7)) & 7) << 4) + word) =
+        v[i];
   }
 }
 
-// An MN-major operand tile of COLS columns (matrix columns col0 ..) by 64 k:
-// COLS / 64 boxes of 64 columns x 64 k rows (8 KB each, 128-byte rows).
+// k-rows part, part + kSoftWarps, ... of an MN-major operand tile of COLS
+// columns (matrix columns col0 ..) by 64 k: COLS / 64 boxes of 64 columns x
+// 64 k rows (8 KB each, 128-byte rows).
 template <int COLS>
 __device__ __forceinline__ void soft_mnmajor(uint8_t* dst, const uint16_t* src, int64_t ld,
-                                             int col0, int ncols, int k0, int K, int lane) {
+                                             int col0, int ncols, int k0, int K, int lane,
+                                             int part) {
+  constexpr int N = H::BK / kSoftWarps;
   const uint32_t word = static_cast<uint32_t>((lane & 3) << 2);
 #pragma unroll 1
   for (int c = 0; c < COLS / 64; ++c) {
     const int n0 = col0 + c * 64 + 2 * lane;
-#pragma unroll 4
-    for (int kr = 0; kr < H::BK; ++kr) {
-      const int k = k0 + kr;
-      const uint32_t v = ld_pair(src, static_cast<int64_t>(k) * ld, n0, ncols, k < K);
+    uint32_t v[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const int k = k0 + part + i * kSoftWarps;
+      v[i] = ld_pair(src, static_cast<int64_t>(k) * ld, n0, ncols, k < K);
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const int kr = part + i * kSoftWarps;
       *reinterpret_cast<uint32_t*>(dst + c * (64 * H::BK * 2) + kr * 128 +
-                                   ((((lane >> 2) ^ (kr & 7)) & 7) << 4) + word) = v;
+                                   ((((lane >> 2) ^ (kr & 7)) & 7) << 4) + word) = v[i];
     }
   }
 }
 
-// One stage by the software loader. A stored M x K is K-major, stored K x M
-// (transa) MN-major; B stored K x N is MN-major, stored N x K (transb) K-major.
+// Loader warp `part`'s share of one stage. A stored M x K is K-major, stored
+// K x M (transa) MN-major; B stored K x N is MN-major, stored N x K (transb)
+// K-major.
 template <int BN>
 __device__ __forceinline__ void soft_load_stage(uint8_t* a_st, const GemmArgs& args, int tm,
-                                                int tn, int kb, int lane) {
+                                                int tn, int kb, int lane, int part) {
   const uint16_t* A = static_cast<const uint16_t*>(args.A);
   const uint16_t* B = static_cast<const uint16_t*>(args.B);
   uint8_t* b_st = a_st + H::BM * H::BK * 2;
   const int k0 = kb * H::BK;
   if (args.transa)
-    soft_mnmajor<H::BM>(a_st, A, args.lda, tm * H::BM, args.M, k0, args.K, lane);
+    soft_mnmajor<H::BM>(a_st, A, args.lda, tm * H::BM, args.M, k0, args.K, lane, part);
   else
-    soft_kmajor<H::BM>(a_st, A, args.lda, tm * H::BM, args.M, k0, args.K, lane);
+    soft_kmajor<H::BM>(a_st, A, args.lda, tm * H::BM, args.M, k0, args.K, lane, part);
   if (args.transb)
-    soft_kmajor<BN>(b_st, B, args.ldb, tn * BN, args.N, k0, args.K, lane);
+    soft_kmajor<BN>(b_st, B, args.ldb, tn * BN, args.N, k0, args.K, lane, part);
   else
-    soft_mnmajor<BN>(b_st, B, args.ldb, tn * BN, args.N, k0, args.K, lane);
+    soft_mnmajor<BN>(b_st, B, args.ldb, tn * BN, args.N, k0, args.K, lane, part);
 }
 
 // Stream-K fixup: a tile's owner reads the partial sums of its later workers
@@ -135,11 +159,11 @@ __device__ __forceinline__ void soft_load_stage(uint8_t* a_st, const GemmArgs& a
 // any is used.
 constexpr int kPre = 4;
 
-template <int BN>
-__device__ __forceinline__ void load_partials(float4 (&p)[kPre][8], const float* partials, int cw0,
+template <int BN, int NP>
+__device__ __forceinline__ void load_partials(float4 (&p)[NP][8], const float* partials, int cw0,
                                               int n, int r_loc, int c) {
 #pragma unroll
-  for (int j = 0; j < kPre; ++j) {
+  for (int j = 0; j < NP; ++j) {
     if (j < n) {
       const float* src =
           partials + (static_cast<size_t>(cw0 + j) * H::BM + r_loc) * BN + c * 32;
@@ -150,9 +174,10 @@ __device__ __forceinline__ void load_partials(float4 (&p)[kPre][8], const float*
 }
 
 // r += p[0] + ... + p[n-1], one worker after another (a fixed order).
-__device__ __forceinline__ void add_partials(uint32_t (&r)[32], const float4 (&p)[kPre][8], int n) {
+template <int NP>
+__device__ __forceinline__ void add_partials(uint32_t (&r)[32], const float4 (&p)[NP][8], int n) {
 #pragma unroll
-  for (int j = 0; j < kPre; ++j) {
+  for (int j = 0; j < NP; ++j) {
     if (j < n) {
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
@@ -170,8 +195,13 @@ __device__ __forceinline__ void add_partials(uint32_t (&r)[32], const float4 (&p
 // kGeneral: stored transposes and the alpha / beta epilogue are read from
 // args; without it the kernel is compiled for untransposed operands and a
 // plain store of C (the software-loader variants are always general).
+// Threads of a variant: the six warps of the roles, plus the software
+// loader's extra warps (6 ..) when operands are not read by TMA.
+template <bool kTma>
+constexpr int tc_threads() { return kTma ? H::THREADS : H::THREADS + 32 * (kSoftWarps - 1); }
+
 template <int BN, bool kTma, bool kSK, bool kGeneral>
-__global__ void __launch_bounds__(H::THREADS, 1)
+__global__ void __launch_bounds__(tc_threads<kTma>(), 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b, const GemmArgs args,
                     const uint32_t idesc) {
@@ -199,7 +229,7 @@ __global__ void __launch_bounds__(H::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sm.full[s], kTma ? 1 : 32);
+      mbar_init(&sm.full[s], kTma ? 1 : 32 * kSoftWarps);
       mbar_init(&sm.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -251,10 +281,12 @@ __global__ void __launch_bounds__(H::THREADS, 1)
     }
   };
 
-  if (warp == 0) {
+  if (warp == 0 || warp >= 6) {
     // ------------------------------------------------------------ producer
     // Segment by segment; a segment's tile coordinates are computed once.
+    // Software loader: warps 0 and 6 .. each fill their share of every stage.
     if (!kTma) {
+      const int part = warp == 0 ? 0 : warp - 5;
       bool ok = true;
       for (int seg = 0; seg < n_seg && ok; ++seg) {
         int tile, kb0, kb1, kind, tm, tn;
@@ -268,7 +300,7 @@ __global__ void __launch_bounds__(H::THREADS, 1)
           if (!got) { ok = false; break; }
           // Failure-detection tests: the first stage is never loaded.
           if (args.fault == kFaultSkipFirstStage && prod_it == 0) continue;
-          soft_load_stage<BN>(tiles + s * STAGE_BYTES, args, tm, tn, kb, lane);
+          soft_load_stage<BN>(tiles + s * STAGE_BYTES, args, tm, tn, kb, lane, part);
           fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
           mbar_arrive(&sm.full[s]);
         }
@@ -382,9 +414,12 @@ __global__ void __launch_bounds__(H::THREADS, 1)
         // HEAD: fetch the first (up to) kPre contributors' partials of this
         // chunk before the TMEM read, all loads in flight at once, so that
         // their latencies overlap each other and the TMEM read's.
-        float4 pre[kPre][8];
-        const int n_pre = (kSK && kind == kSegHead) ? min(kPre, sm.sched.head_last - w) : 0;
-        if (kSK) load_partials<BN>(pre, args.partials, w + 1, n_pre, r_loc, c);
+        // (the software-loader variants, whose 416 threads allow 157 registers
+        // each, prefetch one partial at a time)
+        constexpr int NP = kTma ? kPre : 1;
+        float4 pre[NP][8];
+        const int n_pre = (kSK && kind == kSegHead) ? min(NP, sm.sched.head_last - w) : 0;
+        if (kSK) load_partials<BN, NP>(pre, args.partials, w + 1, n_pre, r_loc, c);
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tc_wait_ld();
@@ -400,11 +435,11 @@ __global__ void __launch_bounds__(H::THREADS, 1)
         if (kSK && kind == kSegHead) {
           // Add the later workers' partial sums, in worker order: the
           // prefetched group, then further groups of kPre (loads first).
-          add_partials(r, pre, n_pre);
-          for (int cw0 = w + 1 + kPre; cw0 <= sm.sched.head_last; cw0 += kPre) {
-            const int n = min(kPre, sm.sched.head_last - cw0 + 1);
-            load_partials<BN>(pre, args.partials, cw0, n, r_loc, c);
-            add_partials(r, pre, n);
+          add_partials<NP>(r, pre, n_pre);
+          for (int cw0 = w + 1 + NP; cw0 <= sm.sched.head_last; cw0 += NP) {
+            const int n = min(NP, sm.sched.head_last - cw0 + 1);
+            load_partials<BN, NP>(pre, args.partials, cw0, n, r_loc, c);
+            add_partials<NP>(r, pre, n);
           }
         }
         const int col0 = tn * BN + c * 32;
@@ -472,7 +507,7 @@ cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
     configured[dev] = 1;
   }
   CUtensorMap dummy{};
-  return launch_kernel(hgemm_tc_kernel<BN, kTma, kSK, kGeneral>, dim3(grid), dim3(H::THREADS),
+  return launch_kernel(hgemm_tc_kernel<BN, kTma, kSK, kGeneral>, dim3(grid), dim3(tc_threads<kTma>()),
                        H::smem_bytes(BN), stream, map_a ? *map_a : dummy,
                        map_b ? *map_b : dummy, args, idesc);
 }
