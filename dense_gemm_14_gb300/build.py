@@ -22,8 +22,9 @@ LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["api.cu", "sgemm_simt.cu", "hgemm_tc.cu", "hgemm_tc2.cu", "sgemm_tc3.cu", "epilogue.cu",
-           "host_path.cu", "copy.cu"]
-HEADERS = ["ptx.cuh", "kernels.h", "streamk.cuh", "api_internal.h"]
+           "host_path.cu", "copy.cu", "plan.cu"]
+HEADERS = ["ptx.cuh", "kernels.h", "streamk.cuh", "api_internal.h", "plan.h",
+           "libgemm14.map"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -85,6 +86,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: s
     tmp = lib_path + f".tmp{os.getpid()}"
     objs = [o for _, o, _, _, _ in procs]
     subprocess.run([cc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a",
+                    "-Xlinker", "--version-script=" + os.path.join(CSRC, "libgemm14.map"),
                     "-o", tmp, *objs], check=True)
     os.replace(tmp, lib_path)
     return lib_path

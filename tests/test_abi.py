@@ -43,6 +43,17 @@ def test_every_declared_symbol_is_exported(lib):
         assert n in _lib.SIGNATURES, f"binding lacks {n}"
 
 
+def test_exports_are_exactly_the_header(lib):
+    """The library's dynamic symbol table holds the header's functions and
+    nothing else: the kernels' C++ internals and the statically linked CUDA
+    runtime stay local (a linker version script)."""
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", g14.lib_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = sorted({line.split()[-1] for line in out.splitlines() if line.strip()})
+    assert exported == declared_functions()
+
+
 def test_status_strings(lib):
     assert g14.status_string(0) == "ok"
     for s in range(1, 5):
