@@ -395,8 +395,10 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
         // A worker has at most one HEAD segment: the barrier's first phase.
         if (warp == 2 && lane == 0) {
           bool all = true;
-          for (int c = w + 1; c <= sm.sched.head_last && all; ++c)
+          for (int c = w + 1; c <= sm.sched.head_last && all; ++c) {
             all = flag_wait(args.flags + c, args.epoch, wc);
+            if (all) flag_clear(args.flags + c);
+          }
           if (all) mbar_arrive(&sm.flags_ready);
         }
         if (lane == 0) got = mbar_wait(&sm.flags_ready, 0, wc) ? 1 : 0;

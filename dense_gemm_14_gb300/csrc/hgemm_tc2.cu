@@ -279,8 +279,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
         // wait on flags_ready). A worker has at most one HEAD segment.
         if (warp == 2 && lane == 0) {
           bool all = true;
-          for (int c = w + 1; c <= sm.sched.head_last && all; ++c)
+          for (int c = w + 1; c <= sm.sched.head_last && all; ++c) {
             all = flag_wait(args.flags + 2 * c + rank, args.epoch, wc);
+            if (all) flag_clear(args.flags + 2 * c + rank);
+          }
           if (all) mbar_arrive(&sm.flags_ready);
         }
         if (lane == 0) got = mbar_wait(&sm.flags_ready, 0, wc) ? 1 : 0;

@@ -196,6 +196,14 @@ __device__ __forceinline__ void flag_publish(unsigned* flag, unsigned value) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(value) : "memory");
 }
 
+// Clears a flag that its one waiter has seen (GPU scope). The next call on
+// the stream starts after this grid completes and finds it 0, so a launch
+// replayed with the same epoch (a captured CUDA graph) never takes a previous
+// replay's publication for its own.
+__device__ __forceinline__ void flag_clear(unsigned* flag) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(0u) : "memory");
+}
+
 // Waits until *flag == value (acquire, GPU scope), bounded like mbar_wait.
 static __device__ __noinline__ bool flag_wait(const unsigned* flag, unsigned value,
                                               const WaitCtx& w) {

@@ -451,8 +451,10 @@ __global__ void __launch_bounds__(S::THREADS, 1)
       }
       const int last = sm.sched.head_last;
       if (threadIdx.x == 0)
-        for (int c = w + 1; c <= last; ++c)
+        for (int c = w + 1; c <= last; ++c) {
           if (!flag_wait(args.flags + c, args.epoch, wc)) break;  // raises abort on expiry
+          flag_clear(args.flags + c);
+        }
       __syncthreads();  // also orders this CTA's own slot stores before the reads
       if (sm.abort_flag) { ok = false; break; }
       // float4 q of the tile (q = thread + 256 u): row q / 64, columns

@@ -149,7 +149,9 @@ int gemm_f32_3xtf32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda
  * to 256 bytes) hold publication flags that only ever contain zero or the
  * number of a finished call, so a workspace may be reused by any later call,
  * of any shape, without clearing; it must not be used by two calls that may
- * run at the same time.
+ * run at the same time. Each flag is cleared by the one tile owner that waits
+ * for it, so a call captured in a CUDA graph (its number fixed at capture) may
+ * be replayed any number of times.
  * Re-pitching: an operand TMA cannot read (base or row pitch not a multiple
  * of 16 bytes) is first copied into the workspace with a 16-byte pitch when
  * the workspace has gemm14_workspace_bytes_ex(...) bytes for this call's
