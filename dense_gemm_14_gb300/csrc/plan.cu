@@ -122,8 +122,12 @@ void plan_for(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t
 int slots_per_worker(const gemm14_plan& plan) { return plan.kernel == 1 ? 2 : 1; }
 
 // The CTA-pair kernel's split, measured on GB300 against its unsplit run:
-// - between one and two waves of tiles with long k (>= 64 k-blocks a tile):
-//   every tile split, 2304x2560x8192 (1.18 waves) 86 -> 74 us;
+// - between one and one and a half waves of tiles with long k (>= 64
+//   k-blocks a tile): every tile split, 2304x2560x8192 (1.18 waves) 86 -> 74
+//   us, TF32 2304x2560x4096 81 -> 69 us; with the last wave more than half
+//   full the idle SMs are few and the split lost (bf16 3072x3072x8192, 1.89
+//   waves, 86.6 us unsplit against 103.5 split; TF32 3072^3 66.9 against
+//   79.4; 2816^2, 1.59 waves, 1.4-1.7 %);
 // - beyond two waves, splitting every tile gained nothing (8192^3,
 //   16384x11008x4096: within 1 %) or lost (4096x4096x16384: +21 %: ranges
 //   that start mid-tile no longer sweep k together, so clusters stop sharing
@@ -143,8 +147,7 @@ int pair_split_workers(int64_t tiles, int64_t L, int clusters) {
     if (g > tiles * L / 32) g = tiles * L / 32;
     return g >= 2 * tiles ? static_cast<int>(g) : 0;
   }
-  if (tiles > clusters && tiles < 2 * static_cast<int64_t>(clusters) && L >= 64)
-    return clusters;
+  if (tiles > clusters && 2 * (tiles - clusters) < clusters && L >= 64) return clusters;
   if (tiles >= 2 * static_cast<int64_t>(clusters) && tiles % clusters != 0) return clusters;
   return 0;
 }

@@ -245,9 +245,13 @@ def test_plan_tf32_pairs_and_fallback(lib, dtype):
             # kind::tf32 MMAs, k-blocks of 32 fp32, no converter warps
             assert st == 0 and pt.kernel == 5 and (pt.bm, pt.bn, pt.bk) == (256, 256, 32)
             assert pt.tiles == 144 and pt.grid == 152 and pt.threads == 192
-            # 144 tiles on 76 clusters, 96 k-blocks: split, one 128 x 256 slot an SM
+            # 144 tiles on 76 clusters (1.89 waves, the last more than half
+            # full): not split, no workspace
             assert g14.workspace_bytes_ex(dtype, 0, 1, 3072, 3072, 3072, P, 3072, P, 3072, P,
-                                          3072, 152) == 768 + 152 * 128 * 256 * 4
+                                          3072, 152) == 0
+            # 90 tiles (1.18 waves), 128 k-blocks: split, one 128 x 256 slot an SM
+            assert g14.workspace_bytes_ex(dtype, 0, 1, 2304, 2560, 4096, P, 4096, P, 4096, P,
+                                          2560, 152) == 768 + 152 * 128 * 256 * 4
         else:
             assert st == 0 and pt == p
     # pitches TMA cannot take: the fp32 SIMT kernel (cp.async loader)

@@ -48,7 +48,9 @@ def test_workspace_bytes():
     # ... beyond two waves that are not whole, the last one and a half waves
     # (8192^3: 1024 tiles = 13.47 waves on 76 clusters) ...
     assert g14.workspace_bytes(BF16, 8192, 8192, 8192, 152) == pair_ws
-    # ... but not whole waves (152 tiles on 76 clusters), nor short k below two waves
+    # ... but not a last wave more than half full below two waves (144 tiles =
+    # 1.89 waves), nor whole waves (152 tiles on 76 clusters), nor short k
+    assert g14.workspace_bytes(BF16, 3072, 3072, 8192, 152) == 0
     assert g14.workspace_bytes(BF16, 2048, 4864, 8192, 152) == 0
     assert g14.workspace_bytes(BF16, 2304, 2560, 2000, 152) == 0
     assert g14.workspace_bytes(BF16, 1000, 776, 1000, 152) == 0
@@ -117,12 +119,16 @@ def test_workspace_bytes_ex_tf32_transposes_into_k_major():
     TF32, X3 = g14.GEMM14_DTYPE_TF32, g14.GEMM14_DTYPE_F32_3XTF32
     P = 1 << 20
     n = 3072
-    sk = 768 + 152 * 128 * 256 * 4        # 144 pair tiles, 96 k-blocks: split
+    flags = 768                            # 144 pair tiles = 1.89 waves: not split
     ex = g14.workspace_bytes_ex
-    assert ex(TF32, 0, 1, n, n, n, P, n, P, n, P, n, 152) == sk            # NT: as stored
-    assert ex(TF32, 0, 0, n, n, n, P, n, P, n, P, n, 152) == sk + n * n * 4  # B^T
-    assert ex(TF32, 1, 1, n, n, n, P, n, P, n, P, n, 152) == sk + n * n * 4  # A^T
-    assert ex(TF32, 1, 0, n, n, n, P, n, P, n, P, n, 152) == sk + 2 * n * n * 4
+    assert ex(TF32, 0, 1, n, n, n, P, n, P, n, P, n, 152) == 0                   # NT: as stored
+    assert ex(TF32, 0, 0, n, n, n, P, n, P, n, P, n, 152) == flags + n * n * 4   # B^T
+    assert ex(TF32, 1, 1, n, n, n, P, n, P, n, P, n, 152) == flags + n * n * 4   # A^T
+    assert ex(TF32, 1, 0, n, n, n, P, n, P, n, P, n, 152) == flags + 2 * n * n * 4
+    # 2304 x 2560 (90 tiles, 1.18 waves, 128 k-blocks) is split: copies after the slots
+    M, N, K = 2304, 2560, 4096
+    sk = 768 + 152 * 128 * 256 * 4
+    assert ex(TF32, 0, 0, M, N, K, P, K, P, N, P, N, 152) == sk + N * K * 4
     # 3xTF32 needs its lo tiles in every storage: no transposed copies
     assert ex(X3, 0, 0, n, n, n, P, n, P, n, P, n, 152) == 0
     # a transposed copy has K rounded up to 4 floats: B (K x N) -> N x round4(K);
