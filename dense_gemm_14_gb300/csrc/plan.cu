@@ -160,9 +160,15 @@ int pair_split_workers(int64_t tiles, int64_t L, int clusters) {
 // N = 64 or 128, K = 4096-16384), the best split had about 4 workers per tile
 // and ranges of 16 or more k-blocks: 128x64x4096 25.0 us unsplit, 20.7 us on
 // 4 workers, 150 us on 64; 512x128x8192 45.2 us unsplit, 33.0 us on 16, 153 us
-// on 152.
+// on 152. Between one and two waves, a 16-bit product splits only when its
+// last wave is less than half full, as on the pair kernel: bf16 N = 64, K =
+// 4096: 1.18 waves 48.3 -> 39.8 us split, but 1.87 waves 52.8 us unsplit
+// against 56.7 split (N = 128, K = 2048: 33.7 against 39.7); fp32 gains at 1.89
+// waves (3072^3: 0.959 -> 0.944 ms).
 int one_sm_split_workers(int kernel, int64_t tiles, int64_t L, int G) {
   if (tiles <= 0 || tiles > INT32_MAX || !stream_k_pays(static_cast<int>(tiles), G)) return 0;
+  if (kernel != 1 && tiles >= G && tiles < 2 * static_cast<int64_t>(G) && 2 * (tiles - G) >= G)
+    return 0;
   if (kernel == 1 || 2 * tiles >= G) return G;
   int64_t g = G;
   if (g > 4 * tiles) g = 4 * tiles;

@@ -30,6 +30,12 @@ def test_workspace_bytes():
     assert g14.workspace_bytes(F32, 4097, 3001, 513, 152) == want
     # skinny bf16: 128 tiles of 128 x 64 -- between half and one wave: not split
     assert g14.workspace_bytes(BF16, 16384, 64, 4096, 152) == 0
+    # 16-bit one-SM tiles between one and two waves: split with the last wave
+    # under half full (180 tiles), not above (284 tiles); beyond two waves the
+    # last one and a half (320 tiles)
+    assert g14.workspace_bytes(BF16, 23040, 64, 4096, 152) == 768 + 152 * 128 * 64 * 4
+    assert g14.workspace_bytes(BF16, 36352, 64, 4096, 152) == 0
+    assert g14.workspace_bytes(BF16, 40960, 64, 4096, 152) == 768 + 152 * 128 * 64 * 4
     # few tiles (fewer than half a wave): split, one 128 x 64 slot per worker
     assert g14.workspace_bytes(BF16, 1024, 64, 4096, 152) == 768 + 152 * 128 * 64 * 4
     # ... but a 16-bit tile takes at most 4 workers, each with at least 16 of
