@@ -437,11 +437,18 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
   if (plan.loader == 2)
     return finish(launch_hgemm_tc_soft(plan.bn, args, idesc, grid, stream), "hgemm launch",
                   stream);
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mc{};
   if ((st = make_maps_16(bf16, transa, transb, M, N, K, A, lda, B, ldb, HgemmShape::BM, plan.bn,
                          &ma, &mb)) != GEMM14_OK)
     return st;
-  return finish(launch_hgemm_tc(plan.bn, ma, mb, args, idesc, grid, stream), "hgemm launch",
+  // C for the TMA-store epilogue of the plain variant (untransposed operands,
+  // plain store, 16-byte-aligned C), as for the pair kernel.
+  // The variant is plain exactly when launch_hgemm_tc picks it.
+  if (!args.transa && !args.transb && args.epi == kEpiStore && plan.vec_store &&
+      (st = make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, args.C, args.M, args.N, args.ldc,
+                     32, 32, CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
+    return st;
+  return finish(launch_hgemm_tc(plan.bn, ma, mb, mc, args, idesc, grid, stream), "hgemm launch",
                 stream);
 }
 

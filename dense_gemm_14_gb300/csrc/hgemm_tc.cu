@@ -203,7 +203,8 @@ constexpr int tc_threads() { return kTma ? H::THREADS : H::THREADS + 32 * (kSoft
 template <int BN, bool kTma, bool kSK, bool kGeneral>
 __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
-                    const __grid_constant__ CUtensorMap map_b, const GemmArgs args,
+                    const __grid_constant__ CUtensorMap map_b,
+                    const __grid_constant__ CUtensorMap map_c, const GemmArgs args,
                     const uint32_t idesc) {
   const int transa = kGeneral ? args.transa : 0;
   const int transb = kGeneral ? args.transb : 0;
@@ -213,9 +214,15 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr uint32_t TMEM_COLS = 2 * BN;
 
+  static_assert(sizeof(TcSmem<BN>) <= H::SMEM_RESERVE, "barrier block exceeds its reserve");
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = align1024(smem_raw);
-  TcSmem<BN>& sm = *reinterpret_cast<TcSmem<BN>*>(tiles + STAGES * STAGE_BYTES);
+  uint8_t* out_stage = tiles + STAGES * STAGE_BYTES;  // epilogue staging for C
+  TcSmem<BN>& sm = *reinterpret_cast<TcSmem<BN>*>(out_stage + H::OUT_BYTES);
+  // Plain variant with a 16-byte-aligned C: the epilogue writes C with TMA
+  // stores of 32 x 32 blocks staged in shared memory.
+  const bool tma_c = !kGeneral && args.vec_store;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -252,6 +259,7 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
       tma_prefetch_desc(&map_a);
       tma_prefetch_desc(&map_b);
     }
+    if (tma_c) tma_prefetch_desc(&map_c);
   }
   if (warp == 1) {
     tmem_alloc(&sm.tmem_base, TMEM_COLS);
@@ -378,6 +386,8 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r_loc = q * 32 + lane;  // this thread's row within the tile
+    uint8_t* out_buf = out_stage + q * 2 * H::OUT_BUF_BYTES;
+    int ob = 0;
     for (int seg = 0; seg < n_seg; ++seg) {
       int tile, kb0, kb1, kind, tm, tn;
       segment(seg, tile, kb0, kb1, kind);
@@ -445,7 +455,29 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
           }
         }
         const int col0 = tn * BN + c * 32;
-        if (row < M) {
+        if (tma_c) {
+          // Row i of the 32 x 32 block goes to staging row i with its eight
+          // 16-byte chunks permuted by i mod 8 (the 128-byte swizzle of
+          // map_c); the TMA store clips rows >= M and columns >= N. The
+          // buffer's store of two chunks ago has been read out first.
+          uint8_t* buf = out_buf + ob * H::OUT_BUF_BYTES;
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          const uint32_t rb = smem_u32(buf) + static_cast<uint32_t>(lane * 128);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             rb + static_cast<uint32_t>(((v ^ lane) & 7) << 4)),
+                         "r"(r[4 * v + 0]), "r"(r[4 * v + 1]), "r"(r[4 * v + 2]), "r"(r[4 * v + 3])
+                         : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&map_c, buf, col0, tm * H::BM + q * 32);
+            bulk_commit();
+          }
+          ob ^= 1;
+        } else if (row < M) {
           if (args.vec_store && col0 + 32 <= N) {
 #pragma unroll
             for (int v = 0; v < 8; ++v)
@@ -470,6 +502,9 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
           flag_publish(args.flags + w, args.epoch);
       }
     }
+    // The TMA stores have finished (their reads of the staging buffers, and
+    // their writes) before the CTA may exit.
+    if (tma_c && lane == 0) bulk_wait_all();
   }
 
   // On abort: let issued MMAs and TMA loads finish (bounded) before TMEM is
@@ -497,7 +532,8 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
 
 template <int BN, bool kTma, bool kSK, bool kGeneral>
 cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
-                           const GemmArgs& args, uint32_t idesc, int grid, cudaStream_t stream) {
+                           const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc,
+                           int grid, cudaStream_t stream) {
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -511,33 +547,36 @@ cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
   CUtensorMap dummy{};
   return launch_kernel(hgemm_tc_kernel<BN, kTma, kSK, kGeneral>, dim3(grid), dim3(tc_threads<kTma>()),
                        H::smem_bytes(BN), stream, map_a ? *map_a : dummy,
-                       map_b ? *map_b : dummy, args, idesc);
+                       map_b ? *map_b : dummy, map_c ? *map_c : dummy, args, idesc);
 }
 
 template <int BN, bool kTma, bool kSK>
-cudaError_t launch_epi(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
-                       uint32_t idesc, int grid, cudaStream_t stream) {
+cudaError_t launch_epi(const CUtensorMap* map_a, const CUtensorMap* map_b,
+                       const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc, int grid,
+                       cudaStream_t stream) {
   if (!kTma || args.transa || args.transb || args.epi != kEpiStore)
-    return launch_variant<BN, kTma, kSK, true>(map_a, map_b, args, idesc, grid, stream);
-  return launch_variant<BN, kTma, kSK, kTma ? false : true>(map_a, map_b, args, idesc, grid,
-                                                             stream);
+    return launch_variant<BN, kTma, kSK, true>(map_a, map_b, map_c, args, idesc, grid, stream);
+  return launch_variant<BN, kTma, kSK, kTma ? false : true>(map_a, map_b, map_c, args, idesc,
+                                                             grid, stream);
 }
 
 template <int BN, bool kTma>
-cudaError_t launch_bn(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& args,
-                      uint32_t idesc, int grid, cudaStream_t stream) {
+cudaError_t launch_bn(const CUtensorMap* map_a, const CUtensorMap* map_b,
+                      const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc, int grid,
+                      cudaStream_t stream) {
   if (args.sk.dp_tiles < args.sk.tiles)
-    return launch_epi<BN, kTma, true>(map_a, map_b, args, idesc, grid, stream);
-  return launch_epi<BN, kTma, false>(map_a, map_b, args, idesc, grid, stream);
+    return launch_epi<BN, kTma, true>(map_a, map_b, map_c, args, idesc, grid, stream);
+  return launch_epi<BN, kTma, false>(map_a, map_b, map_c, args, idesc, grid, stream);
 }
 
 template <bool kTma>
 cudaError_t launch_any(int bn, const CUtensorMap* map_a, const CUtensorMap* map_b,
-                       const GemmArgs& args, uint32_t idesc, int grid, cudaStream_t stream) {
+                       const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc, int grid,
+                       cudaStream_t stream) {
   switch (bn) {
-    case 64: return launch_bn<64, kTma>(map_a, map_b, args, idesc, grid, stream);
-    case 128: return launch_bn<128, kTma>(map_a, map_b, args, idesc, grid, stream);
-    case 256: return launch_bn<256, kTma>(map_a, map_b, args, idesc, grid, stream);
+    case 64: return launch_bn<64, kTma>(map_a, map_b, map_c, args, idesc, grid, stream);
+    case 128: return launch_bn<128, kTma>(map_a, map_b, map_c, args, idesc, grid, stream);
+    case 256: return launch_bn<256, kTma>(map_a, map_b, map_c, args, idesc, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -545,13 +584,14 @@ cudaError_t launch_any(int bn, const CUtensorMap* map_a, const CUtensorMap* map_
 }  // namespace
 
 cudaError_t launch_hgemm_tc(int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                            const GemmArgs& args, uint32_t idesc, int grid, cudaStream_t stream) {
-  return launch_any<true>(bn, &map_a, &map_b, args, idesc, grid, stream);
+                            const CUtensorMap& map_c, const GemmArgs& args, uint32_t idesc,
+                            int grid, cudaStream_t stream) {
+  return launch_any<true>(bn, &map_a, &map_b, &map_c, args, idesc, grid, stream);
 }
 
 cudaError_t launch_hgemm_tc_soft(int bn, const GemmArgs& args, uint32_t idesc, int grid,
                                  cudaStream_t stream) {
-  return launch_any<false>(bn, nullptr, nullptr, args, idesc, grid, stream);
+  return launch_any<false>(bn, nullptr, nullptr, nullptr, args, idesc, grid, stream);
 }
 
 }  // namespace gemm14

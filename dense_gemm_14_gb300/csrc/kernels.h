@@ -129,13 +129,23 @@ struct HgemmShape {
   static constexpr int THREADS = 6 * 32;  // producer, MMA, 4 epilogue warps
   static constexpr int stages(int bn) { return bn == 256 ? 4 : bn == 128 ? 6 : 8; }
   static constexpr int stage_bytes(int bn) { return BM * BK * 2 + BK * bn * 2; }
-  static constexpr int smem_bytes(int bn) { return stages(bn) * stage_bytes(bn) + 256 + 1024; }
+  // epilogue staging for TMA stores of C: per epilogue warp two buffers of
+  // 32 rows x 32 fp32 columns (4 KB each)
+  static constexpr int OUT_BUF_BYTES = 32 * 32 * 4;
+  static constexpr int OUT_BYTES = 4 * 2 * OUT_BUF_BYTES;
+  static constexpr int SMEM_RESERVE = 512;  // barriers and the stream-K table
+  static constexpr int smem_bytes(int bn) {
+    return stages(bn) * stage_bytes(bn) + OUT_BYTES + SMEM_RESERVE + 1024;
+  }
 };
 
 // bn in {64, 128, 256}; idesc is the tcgen05 instruction descriptor
-// (operand format and shape); map_b boxes are 64 (n) x 64 (k).
+// (operand format and shape); map_b boxes are 64 (n) x 64 (k). map_c: C as a
+// 2-D fp32 tensor (box 32 columns x 32 rows, 128-byte swizzle) for the
+// TMA-store epilogue of the plain variant when C takes 16-byte stores.
 cudaError_t launch_hgemm_tc(int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                            const GemmArgs& args, uint32_t idesc, int grid, cudaStream_t stream);
+                            const CUtensorMap& map_c, const GemmArgs& args, uint32_t idesc,
+                            int grid, cudaStream_t stream);
 // ---- bf16 / fp16 tcgen05 kernel on CTA pairs (hgemm_tc2.cu): 256 x 256 tiles
 struct PairShape {
   static constexpr int BM = 256, BN = 256, BK = 64, STAGES = 6;

@@ -9,7 +9,7 @@ import torch
 import dense_gemm_14_gb300 as g14
 from dense_gemm_14_gb300 import inputs
 
-from gpu_util import oracle_check, run_abi
+from gpu_util import oracle_check, run_abi, to_device_padded
 
 pytestmark = pytest.mark.gpu
 
@@ -56,6 +56,38 @@ def test_tensor_core_padded_pitches(oracle_mod, dt):
     A, B = inputs.make(300, 200, 150, dt, "uniform", 1.0, seed=3)
     C = run_abi(A, B, lda=160, ldb=264, ldc=203, a_off=8, b_off=16, c_off=3)
     oracle_check(oracle_mod, A, B, C)
+
+
+@pytest.mark.parametrize("pair,M,N,K", [(False, 300, 200, 150), (False, 129, 36, 64),
+                                        (False, 1000, 777, 130), (True, 300, 200, 150),
+                                        (True, 1000, 777, 130)])
+def test_tensor_core_tma_store_keeps_padding(oracle_mod, pair, M, N, K):
+    """The TMA-store epilogue writes 32 x 32 blocks clipped at M rows and N
+    columns: with a padded pitch the columns past N, and the memory past the
+    last row, keep the NaN they were filled with; C itself is within the bound."""
+    A, B = inputs.make(M, N, K, "bf16", "normal", 1.0 / K ** 0.5, seed=M + 3 * N + K)
+    lda, ldb, ldc = rup(K, 8), rup(N, 8), rup(N, 4) + 8
+    prev = g14.set_pair_kernel(pair)
+    try:
+        st, plan = g14.plan(g14.GEMM14_DTYPE_BF16, M, N, K, 1 << 16, lda, 1 << 16, ldb,
+                            1 << 16, ldc, 152)
+        assert st == 0 and plan.kernel == (3 if pair else 2) and plan.vec_store == 1
+        _abuf, a = to_device_padded(A, lda)
+        _bbuf, b = to_device_padded(B, ldb)
+        cbuf = torch.full((M * ldc + 4096,), float("nan"), device="cuda")
+        s = torch.cuda.current_stream().cuda_stream
+        g14.gemm_bf16_f32acc(M, N, K, a.data_ptr(), lda, b.data_ptr(), ldb, cbuf.data_ptr(),
+                             ldc, s)
+        assert g14.check_device_error(s) == 0
+        torch.cuda.synchronize()
+    finally:
+        g14.set_pair_kernel(prev)
+    full = cbuf.cpu()
+    rows = full[:M * ldc].view(M, ldc)
+    assert torch.isnan(rows[:, N:]).all()
+    assert torch.isnan(full[M * ldc:]).all()
+    assert not torch.isnan(rows[:, :N]).any()
+    oracle_check(oracle_mod, A, B, rows[:, :N].contiguous())
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f16"])
