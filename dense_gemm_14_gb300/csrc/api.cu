@@ -235,11 +235,13 @@ int make_maps_16(bool bf16, int transa, int transb, int64_t M, int64_t N, int64_
 // min(tiles, clusters) clusters, or, with a large enough workspace, stream-K
 // over all co-resident clusters (workers).
 int run_pair(const gemm14_plan& plan, GemmArgs& args, const CUtensorMap& ma,
-             const CUtensorMap& mb, int pair_clusters, bool tf32, uint32_t idesc, int64_t K,
-             int sm_count, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+             const CUtensorMap& mb, const CUtensorMap& ma_lo, const CUtensorMap& mb_lo,
+             int pair_clusters, bool tf32, uint32_t idesc, int64_t K, int sm_count,
+             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   int clusters = static_cast<int>(plan.tiles < pair_clusters ? plan.tiles : pair_clusters);
-  const int L = static_cast<int>((K + plan.bk - 1) / plan.bk);
-  const size_t need = workspace_need(plan, sm_count, K);
+  const int terms = args.k_terms == 3 ? 3 : 1;  // k-blocks of the split 3xTF32 sum
+  const int L = static_cast<int>((K + plan.bk - 1) / plan.bk) * terms;
+  const size_t need = workspace_need(plan, sm_count, K, terms);
   const int workers = pair_split_workers(plan.tiles, L, pair_clusters);
   if (workspace && need && workspace_bytes >= need && workers > 0) {
     if (plan.tiles >= 2 * static_cast<int64_t>(pair_clusters))
@@ -265,7 +267,8 @@ int run_pair(const gemm14_plan& plan, GemmArgs& args, const CUtensorMap& ma,
                             args.ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != GEMM14_OK) return st;
   }
-  return finish(launch_hgemm_tc_pair(ma, mb, mc, args, idesc, clusters, tf32, stream),
+  return finish(launch_hgemm_tc_pair(ma, mb, mc, ma_lo, mb_lo, args, idesc, clusters, tf32,
+                                     stream),
                 "hgemm pair launch", stream);
 }
 
@@ -301,33 +304,53 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
 
   // Operands TMA cannot read: with room in the workspace, copy them there with
   // 16-byte pitches first; the call then keeps the workspace's start (up to
-  // the copies) for the stream-K schedule.
+  // the copies) for the stream-K schedule. 3xTF32 on the pair kernel also
+  // writes lo(A) and lo(B) there (k_terms = 3; A and B are read as hi).
+  int k_terms = 1;
+  const void* A_lo = nullptr;
+  const void* B_lo = nullptr;
+  int64_t ld_lo = 0;
   if (workspace) {
     Repitch rp;
     plan_repitch(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &rp);
-    if ((rp.a || rp.b) && workspace_bytes >= rp.total) {
+    if ((rp.a || rp.b || rp.split) && workspace_bytes >= rp.total) {
       char* ws = static_cast<char*>(workspace);
-      RepitchJob ja{nullptr, 0, nullptr, 0, 0, 0, 0}, jb{nullptr, 0, nullptr, 0, 0, 0, 0};
-      if (rp.a) {
-        // source rows x cols as stored; the copy is that, or its transpose
-        ja = RepitchJob{A, lda, ws + rp.a_off, rp.lda, transa ? K : M, transa ? M : K,
-                        rp.a_t ? 1 : 0};
-        A = ws + rp.a_off;
-        lda = rp.lda;
+      RepitchJob ja{}, jb{};
+      // source rows x cols as stored; the copy (and lo part) is that, or its
+      // transpose. With the split a copy's pitch is ld_lo as well.
+      if (rp.a || rp.split) {
+        ja = RepitchJob{A, lda, rp.a ? ws + rp.a_off : nullptr, rp.split ? rp.ld_lo : rp.lda,
+                        transa ? K : M, transa ? M : K, rp.a_t ? 1 : 0,
+                        rp.split ? ws + rp.a_lo_off : nullptr};
+        if (rp.a) {
+          A = ws + rp.a_off;
+          lda = rp.lda;
+        }
       }
-      if (rp.b) {
-        jb = RepitchJob{B, ldb, ws + rp.b_off, rp.ldb, transb ? N : K, transb ? K : N,
-                        rp.b_t ? 1 : 0};
-        B = ws + rp.b_off;
-        ldb = rp.ldb;
+      if (rp.b || rp.split) {
+        jb = RepitchJob{B, ldb, rp.b ? ws + rp.b_off : nullptr, rp.split ? rp.ld_lo : rp.ldb,
+                        transb ? N : K, transb ? K : N, rp.b_t ? 1 : 0,
+                        rp.split ? ws + rp.b_lo_off : nullptr};
+        if (rp.b) {
+          B = ws + rp.b_off;
+          ldb = rp.ldb;
+        }
       }
       transa = rp.transa;
       transb = rp.transb;
       const cudaError_t e =
-          rp.a_t || rp.b_t ? launch_relayout(ja, jb, dev->sm_count, stream)
-                           : launch_repitch(ja, jb, elem_bytes_of(dtype), dev->sm_count, stream);
+          rp.a_t || rp.b_t || rp.split
+              ? launch_relayout(ja, jb, dev->sm_count, stream)
+              : launch_repitch(ja, jb, elem_bytes_of(dtype), dev->sm_count, stream);
       if (e != cudaSuccess) return finish(e, "re-pitch launch", stream);
       workspace_bytes = rp.a_off;
+      if (rp.split) {
+        k_terms = 3;
+        A_lo = ws + rp.a_lo_off;
+        B_lo = ws + rp.b_lo_off;
+        ld_lo = rp.ld_lo;
+        dtype = GEMM14_DTYPE_TF32;  // planned as TF32, run with 3 terms
+      }
     }
   }
 
@@ -336,26 +359,39 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
   const int epi = beta != 0.0f ? kEpiAccum : alpha != 1.0f ? kEpiScale : kEpiStore;
   GemmArgs args{static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                 A, lda, B, ldb, C, ldc, plan.vec_store, transa, transb, epi, alpha, beta,
-                dev->err_word, wait_limit_ns, fault, StreamK{}, nullptr, nullptr, 0u};
+                dev->err_word, wait_limit_ns, fault, StreamK{}, nullptr, nullptr, 0u, k_terms};
   int grid = plan.grid;
 
   if (plan.kernel == 5) {
     const int pair_clusters = pair_max_clusters();
     if (pair_clusters > 0) {
       // A stored M x K, B stored N x K: boxes of 32 k (128 bytes) x 128 rows
-      CUtensorMap ma, mb;
+      // (and so lo(A), lo(B) in the workspace)
+      CUtensorMap ma, mb, ma_lo{}, mb_lo{};
       const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
       if ((st = make_map(&ma, f32, 4, A, M, K, lda, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B)) !=
               GEMM14_OK ||
           (st = make_map(&mb, f32, 4, B, N, K, ldb, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B)) !=
               GEMM14_OK)
         return st;
-      return run_pair(plan, args, ma, mb, pair_clusters, true,
+      if (k_terms == 3 &&
+          ((st = make_map(&ma_lo, f32, 4, A_lo, M, K, ld_lo, 32, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK ||
+           (st = make_map(&mb_lo, f32, 4, B_lo, N, K, ld_lo, 32, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK))
+        return st;
+      return run_pair(plan, args, ma, mb, ma_lo, mb_lo, pair_clusters, true,
                       idesc_tf32_f32acc(PairShape::BM, PairShape::BN), K, dev->sm_count,
                       workspace, workspace_bytes, stream);
     }
-    // clusters of two do not fit: plan without the pair kernel
+    // clusters of two do not fit: plan without the pair kernel (the split
+    // operands' hi parts are A and B themselves: 3xTF32 on the converter kernel)
     g_pair_enabled.store(0);
+    if (k_terms == 3) {
+      dtype = GEMM14_DTYPE_F32_3XTF32;
+      k_terms = 1;
+      args.k_terms = 1;
+    }
     plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
     args.vec_store = plan.vec_store;
     grid = plan.grid;
@@ -420,12 +456,12 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
     }
   }
   if (plan.kernel == 3 && pair_clusters > 0) {
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, unused{};
     // each CTA of a pair loads 128 rows of A and 128 columns of B
     if ((st = make_maps_16(bf16, transa, transb, M, N, K, A, lda, B, ldb, 128, 128, &ma, &mb)) !=
         GEMM14_OK)
       return st;
-    return run_pair(plan, args, ma, mb, pair_clusters, false,
+    return run_pair(plan, args, ma, mb, unused, unused, pair_clusters, false,
                     idesc_f16_f32acc(bf16, PairShape::BM, PairShape::BN, transa != 0, transb == 0),
                     K, dev->sm_count, workspace, workspace_bytes, stream);
   }
@@ -625,7 +661,7 @@ size_t gemm14_workspace_bytes_ex(int dtype, int transa, int transb, int64_t M, i
   if (M == 0 || N == 0 || K == 0) return 0;
   Repitch rp;
   plan_repitch(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, sm_count, &rp);
-  if (rp.a || rp.b) return rp.total;
+  if (rp.a || rp.b || rp.split) return rp.total;
   gemm14_plan plan;
   plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, sm_count, &plan);
   return workspace_need(plan, sm_count, K);

@@ -2,8 +2,9 @@
 // row pitch that is not a multiple of 16 bytes) into a caller workspace with a
 // 16-byte pitch, so that the product runs on the TMA loaders instead of the
 // element-wise ones; and, for tf32 products, transposing an fp32 operand into
-// the K-major storage the tensor cores read straight from TMA. A memory-bound pass: each element is read and written
-// once. The work items are segments of kUnroll x 32 consecutive elements of a
+// the K-major storage the tensor cores read straight from TMA, and, for
+// split-precision 3xTF32 products, writing the lo part of each element. A
+// memory-bound pass: each element is read once and written once or twice. The work items are segments of kUnroll x 32 consecutive elements of a
 // row; a warp loads a whole segment (its lanes on consecutive elements, so
 // reads and writes are coalesced whatever the source alignment) before it
 // stores any of it, keeping kUnroll loads per lane in flight.
@@ -55,8 +56,19 @@ __global__ void __launch_bounds__(256) repitch_kernel(const RepitchJob j0, const
 // sides stay coalesced, and each thread has its 16 loads in flight before
 // the barrier. Element (r, c) of a transposed job's source lands at (c, r) of
 // its destination. The tile's rows are padded to 65 floats, so the column
-// reads of the transposed store hit 32 different banks.
+// reads of the transposed store hit 32 different banks. A job with dst_lo
+// also writes lo(x) there, at the same place as x in dst (dst may be null).
 constexpr int kRt = 64;
+
+// lo(x) = x - hi(x), hi(x) = x with its 13 low fraction bits cleared, as the
+// tensor cores read an fp32 operand of a kind::tf32 MMA. The subtraction is
+// exact: hi(x) and x share sign and exponent, so the difference is x's 13
+// low fraction bits, a value an fp32 holds exactly (also for subnormal x).
+// lo(inf) is NaN (inf - inf): as on the converter kernel, a product term with
+// an infinite input comes out NaN.
+__device__ __forceinline__ float tf32_lo(float x) {
+  return x - __uint_as_float(__float_as_uint(x) & 0xffffe000u);
+}
 
 __global__ void __launch_bounds__(256) relayout_kernel(const RepitchJob j0, const RepitchJob j1) {
   __shared__ float tile[kRt][kRt + 1];
@@ -74,6 +86,7 @@ __global__ void __launch_bounds__(256) relayout_kernel(const RepitchJob j0, cons
     const int64_t r0 = (i / tcols) * kRt, c0 = (i % tcols) * kRt;
     const float* src = static_cast<const float*>(j.src);
     float* dst = static_cast<float*>(j.dst);
+    float* dst_lo = static_cast<float*>(j.dst_lo);
     float v[kRt / 8][2];
 #pragma unroll
     for (int k = 0; k < kRt / 8; ++k)
@@ -94,10 +107,18 @@ __global__ void __launch_bounds__(256) relayout_kernel(const RepitchJob j0, cons
         if (j.transpose) {
           // destination row c0 + ty + 8k, column r0 + tx + 32h
           const int64_t c = c0 + ty + 8 * k, r = r0 + tx + 32 * h;
-          if (c < j.cols && r < j.rows) dst[c * j.ld_dst + r] = tile[tx + 32 * h][ty + 8 * k];
+          if (c < j.cols && r < j.rows) {
+            const float x = tile[tx + 32 * h][ty + 8 * k];
+            if (dst) dst[c * j.ld_dst + r] = x;
+            if (dst_lo) dst_lo[c * j.ld_dst + r] = tf32_lo(x);
+          }
         } else {
           const int64_t r = r0 + ty + 8 * k, c = c0 + tx + 32 * h;
-          if (r < j.rows && c < j.cols) dst[r * j.ld_dst + c] = tile[ty + 8 * k][tx + 32 * h];
+          if (r < j.rows && c < j.cols) {
+            const float x = tile[ty + 8 * k][tx + 32 * h];
+            if (dst) dst[r * j.ld_dst + c] = x;
+            if (dst_lo) dst_lo[r * j.ld_dst + c] = tf32_lo(x);
+          }
         }
       }
     __syncthreads();

@@ -455,11 +455,16 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
           }
         }
         const int col0 = tn * BN + c * 32;
-        if (tma_c) {
+        // A TMA store clips a row at 16-byte granularity, not per element: a
+        // chunk that runs past a column count N that is not a multiple of 4
+        // would write up to 3 floats past column N - 1 (into the pitch's
+        // padding), so that chunk takes the guarded direct stores.
+        if (tma_c && (col0 + 32 <= N || (N & 3) == 0)) {
           // Row i of the 32 x 32 block goes to staging row i with its eight
           // 16-byte chunks permuted by i mod 8 (the 128-byte swizzle of
-          // map_c); the TMA store clips rows >= M and columns >= N. The
-          // buffer's store of two chunks ago has been read out first.
+          // map_c); the TMA store leaves out rows >= M (and columns >= N,
+          // as above). The buffer's store of two chunks ago has been read
+          // out first.
           uint8_t* buf = out_buf + ob * H::OUT_BUF_BYTES;
           if (lane == 0) bulk_wait_read<1>();
           __syncwarp();

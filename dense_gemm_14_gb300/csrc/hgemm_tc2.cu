@@ -75,11 +75,21 @@ __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m, int tiles_n
 // stored M x K and B stored N x K, i.e. both K-major as TMA writes them: the
 // same 128-byte rows, boxes and descriptors as 16-bit K-major operands, a
 // k-block being 32 fp32 instead of 64 16-bit elements.
+// kTf32 with args.k_terms == 3: the split-precision 3xTF32 product (Ootomo and
+// Yokota, "Recovering single precision accuracy from Tensor Cores while
+// surpassing the FP32 theoretical peak performance", 2022) from lo(A) and
+// lo(B) written ahead of the call (map_a_lo, map_b_lo): the k sum runs over
+// three terms of L k-blocks each, lo(A) hi(B), then hi(A) lo(B), then
+// hi(A) hi(B) (small terms first), as if K were 3 K; only the producer's
+// choice of tensor map and k coordinate tells them apart, so stream-K splits
+// the 3 L k-blocks like any others.
 template <bool kGeneral, bool kSK, bool kTf32>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
     hgemm_tc2_kernel(const __grid_constant__ CUtensorMap map_a,
                      const __grid_constant__ CUtensorMap map_b,
-                     const __grid_constant__ CUtensorMap map_c, const GemmArgs args,
+                     const __grid_constant__ CUtensorMap map_c,
+                     const __grid_constant__ CUtensorMap map_a_lo,
+                     const __grid_constant__ CUtensorMap map_b_lo, const GemmArgs args,
                      const uint32_t idesc) {
   const int transa = kTf32 ? 0 : kGeneral ? args.transa : 0;
   const int transb = kTf32 ? 1 : kGeneral ? args.transb : 0;
@@ -99,7 +109,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
   const int tiles_m = (M + P::BM - 1) / P::BM;
   const int tiles_n = (N + P::BN - 1) / P::BN;
   const int num_tiles = tiles_m * tiles_n;
-  const int kblocks = (K + BK - 1) / BK;
+  const int kb_term = (K + BK - 1) / BK;  // k-blocks of one term of the sum
+  const bool split3 = kTf32 && args.k_terms == 3;
+  const int kblocks = split3 ? 3 * kb_term : kb_term;
   const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns,
                    mapa_shared(smem_u32(&sm.abort_flag), rank ^ 1u)};
   uint32_t prod_it = 0;
@@ -129,6 +141,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
     tma_prefetch_desc(&map_a);
     tma_prefetch_desc(&map_b);
     if (!kGeneral && args.vec_store) tma_prefetch_desc(&map_c);
+    if (split3) {
+      tma_prefetch_desc(&map_a_lo);
+      tma_prefetch_desc(&map_b_lo);
+    }
   }
   // Both CTAs' barriers exist before either CTA signals the other's.
   cluster_sync();
@@ -179,9 +195,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
           if (leader) mbar_arrive_expect_tx(&sm.full[s], 2 * P::STAGE_BYTES);
           const int m0 = tm * P::BM + static_cast<int>(rank) * 128;
           const int n0 = tn * P::BN + static_cast<int>(rank) * 128;
+          // 3xTF32: term t = kb / L reads lo(A) (t = 0) or lo(B) (t = 1) at
+          // k-block kb - t L; the plain product reads map_a and map_b at kb.
+          const CUtensorMap* ma = &map_a;
+          const CUtensorMap* mb = &map_b;
+          int kq = kb;
+          if (split3) {
+            const int t = kb / kb_term;
+            kq = kb - t * kb_term;
+            if (t == 0) ma = &map_a_lo;
+            if (t == 1) mb = &map_b_lo;
+          }
           // A: one box of 64 k x 128 m, or (stored K x M) two of 64 m x 64 k.
           if (!transa) {
-            tma_load_2d_pair(a_st, &map_a, kb * BK, m0, full_leader);
+            tma_load_2d_pair(a_st, ma, kq * BK, m0, full_leader);
           } else {
 #pragma unroll
             for (int c = 0; c < 2; ++c)
@@ -195,7 +222,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
               tma_load_2d_pair(b_st + c * (64 * P::BK * 2), &map_b, n0 + c * 64, kb * P::BK,
                                full_leader);
           } else {
-            tma_load_2d_pair(b_st, &map_b, kb * BK, n0, full_leader);
+            tma_load_2d_pair(b_st, mb, kq * BK, n0, full_leader);
           }
         }
       }
@@ -330,7 +357,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
           }
         }
         const int col0 = tn * P::BN + c * 32;
-        if (tma_c) {
+        // A TMA store clips a row at 16-byte granularity, not per element: a
+        // chunk that runs past a column count N that is not a multiple of 4
+        // would write up to 3 floats past column N - 1 (into the pitch's
+        // padding), so that chunk takes the guarded direct stores.
+        if (tma_c && (col0 + 32 <= N || (N & 3) == 0)) {
           // The buffer's store of two chunks ago has been read out.
           uint8_t* buf = out_buf + ob * P::OUT_BUF_BYTES;
           if (lane == 0) bulk_wait_read<1>();
@@ -443,8 +474,10 @@ int pair_max_clusters() {
 }
 
 cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
-                                 const CUtensorMap& map_c, const GemmArgs& args, uint32_t idesc,
-                                 int clusters, bool tf32, cudaStream_t stream) {
+                                 const CUtensorMap& map_c, const CUtensorMap& map_a_lo,
+                                 const CUtensorMap& map_b_lo, const GemmArgs& args,
+                                 uint32_t idesc, int clusters, bool tf32, cudaStream_t stream) {
+  if (args.k_terms == 3 && !tf32) return cudaErrorInvalidValue;
   // tf32 operands are stored M x K and N x K, which the tf32 variants fix at
   // compile time: only the epilogue mode makes them general
   const bool general =
@@ -459,8 +492,8 @@ cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& ma
                             : hgemm_tc2_kernel<false, true, false>)
                  : (general ? hgemm_tc2_kernel<true, false, false>
                             : hgemm_tc2_kernel<false, false, false>));
-  return launch_kernel(kernel, grid, block, P::SMEM_BYTES, stream, map_a, map_b, map_c, args,
-                       idesc);
+  return launch_kernel(kernel, grid, block, P::SMEM_BYTES, stream, map_a, map_b, map_c,
+                       map_a_lo, map_b_lo, args, idesc);
 }
 
 }  // namespace gemm14

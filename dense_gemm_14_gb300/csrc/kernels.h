@@ -64,6 +64,11 @@ struct GemmArgs {
   float* partials;     // stream-K: tile-sized fp32 slots (see streamk_workspace_bytes), or null
   unsigned* flags;     // stream-K: G publication flags (hold the call's epoch)
   unsigned epoch;      // this call's nonzero epoch
+  // Terms of the k sum (the pair kernel's tf32 variant): 0 or 1, the plain
+  // product; 3, the split-precision 3xTF32 product from operands split ahead
+  // of the call, lo(A) hi(B) + hi(A) lo(B) + hi(A) hi(B), run as 3 x the
+  // k-blocks of one term (see launch_hgemm_tc_pair).
+  int k_terms;
 };
 
 // The epilogue's update of one output element, and of four consecutive ones
@@ -169,9 +174,14 @@ int pair_max_clusters();
 // (args.vec_store); otherwise unused.
 // tf32: fp32 operands stored M x K and N x K read as tf32 (kind::tf32, a
 // k-block of 32 elements; maps of fp32 boxes 32 k x 128 rows, 128-byte swizzle).
+// With args.k_terms == 3 (tf32 only), map_a_lo and map_b_lo describe lo(A) and
+// lo(B) (x minus x with its 13 low fraction bits cleared) in the same storage
+// and boxes as map_a and map_b, which hold A and B themselves (the tensor
+// cores read them as hi(A) and hi(B)); otherwise both are unused.
 cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
-                                 const CUtensorMap& map_c, const GemmArgs& args, uint32_t idesc,
-                                 int clusters, bool tf32, cudaStream_t stream);
+                                 const CUtensorMap& map_c, const CUtensorMap& map_a_lo,
+                                 const CUtensorMap& map_b_lo, const GemmArgs& args,
+                                 uint32_t idesc, int clusters, bool tf32, cudaStream_t stream);
 
 // Same kernel with the software loader (operands TMA cannot address).
 cudaError_t launch_hgemm_tc_soft(int bn, const GemmArgs& args, uint32_t idesc, int grid,
@@ -213,11 +223,16 @@ struct RepitchJob {
   int64_t ld_dst;
   int64_t rows, cols;
   int transpose;  // relayout only: the destination is the cols x rows transpose
+  // relayout only: when set, lo(x) = x - (x with its 13 low fraction bits
+  // cleared) of each element goes here, placed and pitched as in dst (which
+  // may then be null: no copy of x itself)
+  void* dst_lo;
 };
 // Both copies in one launch on `stream`, elements of elem_bytes (2 or 4) (copy.cu).
 cudaError_t launch_repitch(const RepitchJob& j0, const RepitchJob& j1, int elem_bytes,
                            int sm_count, cudaStream_t stream);
-// Both fp32 copies in one launch, each transposed when job.transpose (copy.cu).
+// Both fp32 copies in one launch, each transposed when job.transpose, and each
+// also (or only) split into its lo part when job.dst_lo (copy.cu).
 cudaError_t launch_relayout(const RepitchJob& j0, const RepitchJob& j1, int sm_count,
                             cudaStream_t stream);
 

@@ -176,10 +176,10 @@ int one_sm_split_workers(int kernel, int64_t tiles, int64_t L, int G) {
   return g >= 2 * tiles ? static_cast<int>(g) : 0;
 }
 
-size_t workspace_need(const gemm14_plan& plan, int sm_count, int64_t K) {
+size_t workspace_need(const gemm14_plan& plan, int sm_count, int64_t K, int k_terms) {
   if (plan.tiles > INT32_MAX) return 0;
   if (plan.kernel == 3 || plan.kernel == 5) {
-    const int64_t L = (K + plan.bk - 1) / plan.bk;
+    const int64_t L = (K + plan.bk - 1) / plan.bk * (k_terms > 1 ? k_terms : 1);
     if (!pair_split_workers(plan.tiles, L, sm_count / 2)) return 0;
     return streamk_workspace_bytes(sm_count, PairShape::BM / 2, PairShape::BN, 1);
   }
@@ -208,13 +208,19 @@ void plan_repitch(int dtype, int transa, int transb, int64_t M, int64_t N, int64
   // (A stored M x K, B stored N x K, plan kernel 5); other storages are
   // transposed into that form (the converter kernel runs at about a quarter
   // of the speed).
-  if (dtype == GEMM14_DTYPE_TF32 && g_pair_enabled.load() && sms >= 2) {
+  // 3xTF32 the same way, with lo(A) and lo(B) written beside them: the pair
+  // kernel then runs 3 x the TF32 product's MMAs from K-major operands, while
+  // the converter kernel splits the raw tiles as they arrive and its ring's
+  // turnaround bounds it.
+  const bool split = dtype == GEMM14_DTYPE_F32_3XTF32 && g_pair_enabled.load() && sms >= 2;
+  if ((dtype == GEMM14_DTYPE_TF32 || split) && g_pair_enabled.load() && sms >= 2) {
     r->a_t = transa != 0;
     r->b_t = transb == 0;
     r->a = r->a || r->a_t;
     r->b = r->b || r->b_t;
     r->transa = 0;
     r->transb = 1;
+    r->split = split;
   }
   // fp32 FFMA: B stored N x K (K-major in shared memory) needs per-k packing
   // of its pairs and measured 42 % of the FFMA peak, against 76 % for B
@@ -234,7 +240,7 @@ void plan_repitch(int dtype, int transa, int transb, int64_t M, int64_t N, int64
     r->a = true;
     r->transa = 1;
   }
-  if (!r->a && !r->b) return;
+  if (!r->a && !r->b && !r->split) return;
   // Stored shape of each copy: as the source, or transposed.
   const int64_t rows_a = r->transa ? K : M, cols_a = r->transa ? M : K;
   const int64_t rows_b = r->transb ? N : K, cols_b = r->transb ? K : N;
@@ -243,15 +249,23 @@ void plan_repitch(int dtype, int transa, int transb, int64_t M, int64_t N, int64
   // The plan of the copies: only their alignment and storage enter it.
   const void* base = reinterpret_cast<const void*>(uintptr_t(1) << 12);
   gemm14_plan plan;
-  plan_for(dtype, r->transa, r->transb, M, N, K, r->a ? base : A, r->lda, r->b ? base : B,
-           r->ldb, C, ldc, sms, &plan);
-  const size_t sk = workspace_need(plan, sms, K);
+  plan_for(r->split ? GEMM14_DTYPE_TF32 : dtype, r->transa, r->transb, M, N, K,
+           r->a ? base : A, r->lda, r->b ? base : B, r->ldb, C, ldc, sms, &plan);
+  const size_t sk = workspace_need(plan, sms, K, r->split ? 3 : 1);
   r->sk_bytes = sk;
   const size_t flags = streamk_flag_bytes(sms);
   r->a_off = round256(sk > flags ? sk : flags);
   const size_t a_bytes = r->a ? static_cast<size_t>(rows_a * r->lda * eb) : 0;
   r->b_off = round256(r->a_off + a_bytes);
   r->total = r->b ? r->b_off + static_cast<size_t>(rows_b * r->ldb * eb) : r->a_off + a_bytes;
+  if (r->split) {
+    // lo(A) M x K and lo(B) N x K, K-major, rows of K rounded up to 4 floats
+    // (the pitch of A's and B's own copies, when they are copied)
+    r->ld_lo = (K + q - 1) / q * q;
+    r->a_lo_off = round256(r->total);
+    r->b_lo_off = round256(r->a_lo_off + static_cast<size_t>(M * r->ld_lo * eb));
+    r->total = r->b_lo_off + static_cast<size_t>(N * r->ld_lo * eb);
+  }
 }
 
 }  // namespace gemm14

@@ -35,14 +35,16 @@ void plan_for(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t
 int slots_per_worker(const gemm14_plan& plan);
 int pair_split_workers(int64_t tiles, int64_t L, int clusters);
 int one_sm_split_workers(int kernel, int64_t tiles, int64_t L, int G);
-size_t workspace_need(const gemm14_plan& plan, int sm_count, int64_t K);
+// k_terms: 3 for the pair kernel's split-precision 3xTF32 run (3 L k-blocks).
+size_t workspace_need(const gemm14_plan& plan, int sm_count, int64_t K, int k_terms = 1);
 
 // Re-pitching into the caller's workspace. An operand whose base or row
 // pitch is not a multiple of 16 bytes cannot be read by TMA; with a large
 // enough workspace the call copies it there with a 16-byte pitch (a memory-
 // bound pass of one read and one write per element) and runs the TMA loaders
 // on the copy. Workspace layout: the stream-K region first (its flag words at
-// the start, where they always are), then the copy of A, then that of B.
+// the start, where they always are), then the copy of A, then that of B, then
+// (3xTF32 split ahead of the call) lo(A) and lo(B).
 struct Repitch {
   bool a = false, b = false;     // which operands are copied
   bool a_t = false, b_t = false; // ... transposed (tf32: into K-major storage)
@@ -50,6 +52,12 @@ struct Repitch {
   int64_t lda = 0, ldb = 0;      // their pitches in the workspace
   size_t sk_bytes = 0;           // the stream-K region (flags + slots)
   size_t a_off = 0, b_off = 0;   // byte offsets of the copies
+  // 3xTF32 on the pair kernel: lo(A) (M x K) and lo(B) (N x K), K-major with
+  // pitch ld_lo, at a_lo_off and b_lo_off; A and B (copied or as stored) are
+  // then K-major too and the product runs 3 terms (GemmArgs::k_terms)
+  bool split = false;
+  int64_t ld_lo = 0;
+  size_t a_lo_off = 0, b_lo_off = 0;
   size_t total = 0;              // workspace bytes the call needs for all of it
 };
 

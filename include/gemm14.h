@@ -113,7 +113,12 @@ int gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  *   gemm_f32_3xtf32: each input x is split into hi = tf32(x) and lo = x - hi
  *     (exact), and C = hi(A) hi(B) + hi(A) lo(B) + lo(A) hi(B) summed in fp32
  *     (the split-precision scheme known as 3xTF32): within the fp32 bound,
- *     |C - A B| <= 1e-5 (|A||B|), at tensor-core speed.
+ *     |C - A B| <= 1e-5 (|A||B|), at tensor-core speed. Through
+ *     gemm14_gemm_ex with a workspace of gemm14_workspace_bytes_ex bytes, lo(A)
+ *     and lo(B) are first written into the workspace (with K-major copies of
+ *     operands stored otherwise) and the product runs as three k sums, lo(A)
+ *     hi(B), hi(A) lo(B), hi(A) hi(B), on CTA pairs: the same bound, other
+ *     bits (another order of the same terms).
  * Arguments, layout and rules as gemm_f32. A and B 16-byte aligned with lda,
  * ldb multiples of 4 run on CTA pairs of tensor-core SMs (256 x 256 tiles);
  * other operands run on gemm_f32's kernel, whose exact fp32 products meet both
@@ -214,8 +219,9 @@ int gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int
  *   GEMM14_ERR_INVALID_ARG.
  * Arithmetic: the sum over k is formed exactly as by gemm_f32 /
  * gemm_bf16_f32acc / gemm_f16_f32acc (bit-identical for alpha = 1,
- * beta = 0); then each element is written as alpha * sum (beta == 0) or as
- * fmaf(alpha, sum, beta * C) in fp32.
+ * beta = 0, with the same workspace; 3xTF32 with a workspace sums its terms
+ * in another order, see gemm_f32_3xtf32); then each element is written as
+ * alpha * sum (beta == 0) or as fmaf(alpha, sum, beta * C) in fp32.
  * beta == 0: C is not read (NaN or infinity in C does not propagate).
  * K == 0 or alpha == 0: A and B are not read; C becomes beta * C (beta == 1
  * launches nothing, beta == 0 zeroes C).
@@ -246,7 +252,8 @@ size_t gemm14_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int sm
  * Workspace bytes for a gemm14_gemm_ex (or *_ws) call on exactly these
  * operands: the stream-K region as above, plus, for an operand TMA cannot
  * read, room for its copy with a 16-byte pitch (so that the call re-pitches
- * it). Pointers are only inspected for their alignment, never dereferenced;
+ * it); for TF32 and 3xTF32, room for K-major copies of operands stored
+ * otherwise, and for 3xTF32 room for lo(A) and lo(B). Pointers are only inspected for their alignment, never dereferenced;
  * no CUDA call is made when sm_count > 0. 0: the call needs no workspace, or
  * the arguments are invalid.
  */

@@ -59,12 +59,14 @@ def test_tensor_core_padded_pitches(oracle_mod, dt):
 
 
 @pytest.mark.parametrize("pair,M,N,K", [(False, 300, 200, 150), (False, 129, 36, 64),
-                                        (False, 1000, 777, 130), (True, 300, 200, 150),
-                                        (True, 1000, 777, 130)])
+                                        (False, 1000, 777, 130), (False, 300, 201, 64),
+                                        (True, 300, 200, 150), (True, 1000, 777, 130),
+                                        (True, 1000, 779, 130)])
 def test_tensor_core_tma_store_keeps_padding(oracle_mod, pair, M, N, K):
-    """The TMA-store epilogue writes 32 x 32 blocks clipped at M rows and N
-    columns: with a padded pitch the columns past N, and the memory past the
-    last row, keep the NaN they were filled with; C itself is within the bound."""
+    """The TMA-store epilogue writes 32 x 32 blocks that the TMA unit clips at
+    M rows, but only at 16-byte granularity at N columns: with a padded pitch
+    the columns past N (N not a multiple of 4 included), and the memory past
+    the last row, keep the NaN they were filled with; C is within the bound."""
     A, B = inputs.make(M, N, K, "bf16", "normal", 1.0 / K ** 0.5, seed=M + 3 * N + K)
     lda, ldb, ldc = rup(K, 8), rup(N, 8), rup(N, 4) + 8
     prev = g14.set_pair_kernel(pair)

@@ -31,9 +31,11 @@ def rup(x, m):
 
 
 def run_mode(code, A, B, transa=0, transb=0, alpha=1.0, beta=0.0, C0=None, lda=None,
-             ldb=None, ldc=None, a_off=0, b_off=0, c_off=0):
+             ldb=None, ldc=None, a_off=0, b_off=0, c_off=0, workspace=False):
     """C = alpha op(A) op(B) + beta C0 through gemm14_gemm_ex with a tf32 mode;
-    pitches rounded to 4 floats by default (the tensor-core kernel)."""
+    pitches rounded to 4 floats by default (the tensor-core kernel). With
+    workspace, the call gets the workspace gemm14_workspace_bytes_ex asks for
+    (its K-major copies, lo parts and stream-K region), NaN-filled."""
     M, K = A.shape
     N = B.shape[1]
     As, Bs = stored(A, transa), stored(B, transb)
@@ -46,9 +48,16 @@ def run_mode(code, A, B, transa=0, transb=0, alpha=1.0, beta=0.0, C0=None, lda=N
     if C0 is not None:
         cbuf[c_off:c_off + M * ldc].view(M, ldc)[:, :N].copy_(C0.cuda())
     s = torch.cuda.current_stream()
+    ws, ws_bytes = None, 0
+    if workspace:
+        ws_bytes = g14.workspace_bytes_ex(code, transa, transb, M, N, K,
+                                          a.data_ptr() if As.numel() else 0, lda,
+                                          b.data_ptr() if Bs.numel() else 0, ldb,
+                                          cbuf.data_ptr() + 4 * c_off, ldc)
+        ws = torch.full((max(ws_bytes, 16) // 4 + 1,), float("nan"), device="cuda")
     g14.gemm_ex(code, transa, transb, M, N, K, alpha, a.data_ptr() if As.numel() else 0, lda,
                 b.data_ptr() if Bs.numel() else 0, ldb, beta, cbuf.data_ptr() + 4 * c_off, ldc,
-                None, 0, s.cuda_stream)
+                ws.data_ptr() if ws is not None else None, ws_bytes, s.cuda_stream)
     assert g14.check_device_error(s.cuda_stream) == 0
     torch.cuda.synchronize()
     return cbuf[c_off:c_off + M * ldc].view(M, ldc)[:, :N].cpu()
@@ -249,3 +258,141 @@ def test_tf32_nt_split_over_clusters(oracle_mod):
                 ws.data_ptr(), need, s)
     assert g14.check_device_error(s) == 0
     check(oracle_mod, A, B, c.cpu(), TOL["f32"], rounded=True)
+
+
+# ------------------------------------------------------------------ 3xTF32 split ahead of the call
+
+def split_bytes(code, M, N, K, ta=0, tb=0):
+    P = 1 << 16
+    As_cols = M if ta else K
+    Bs_cols = K if tb else N
+    return g14.workspace_bytes_ex(code, ta, tb, M, N, K, P, rup(As_cols, 4), P, rup(Bs_cols, 4),
+                                  P, N, 152)
+
+
+@pytest.mark.parametrize("ta,tb", TRANS)
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (5, 7, 3), (255, 257, 33), (300, 520, 200),
+                                   (513, 769, 1025), (64, 1000, 96)])
+def test_3xtf32_split_meets_the_fp32_bound(oracle_mod, ta, tb, M, N, K):
+    """With a workspace, 3xTF32 writes lo(A) and lo(B) (and K-major copies of
+    operands stored otherwise) ahead of the product, which runs on the pair
+    kernel as three k sums: within the fp32 bound in every storage, with the
+    same bits in every storage (the same values reach the same MMAs)."""
+    assert split_bytes(X3, M, N, K, ta, tb) >= (M + N) * rup(K, 4) * 4
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=M * 3 + N + 7 * K + 5 * ta + tb)
+    C = run_mode(X3, A, B, ta, tb, workspace=True)
+    worst = check(oracle_mod, A, B, C, TOL["f32"], ta, tb)
+    print(f"3xtf32 split {M}x{N}x{K} ta={ta} tb={tb}: worst {worst:.3g}")
+    if (ta, tb) != (0, 1):
+        assert torch.equal(C, run_mode(X3, A, B, 0, 1, workspace=True))
+
+
+def fractional(rows, cols, seed):
+    """i + j / 4096 with i, j in [-4, 4]: hi(x) + lo(x) = x with lo(x) a
+    multiple of 2^-12, nonzero for most entries (e.g. 4 + 3 / 4096 has hi 4,
+    lo 3 / 4096; 1 - 4 / 4096 is a tf32 value, lo 0)."""
+    g = torch.Generator().manual_seed(seed)
+    i = torch.randint(-4, 5, (rows, cols), generator=g)
+    j = torch.randint(-4, 5, (rows, cols), generator=g)
+    return (i.double() + j.double() / 4096).float()
+
+
+@pytest.mark.parametrize("which", ["lo(A) hi(B)", "hi(A) lo(B)"])
+def test_3xtf32_split_lo_terms_exact(which):
+    """One operand with 2^-12 steps below its tf32 part, the other integer
+    (lo = 0, so the dropped lo(A) lo(B) term is 0): every product and partial
+    sum is a multiple of 2^-12 below 2^10, exact in fp32, so the split product
+    must give A B bit for bit -- a missing or misplaced lo term (or one read
+    at the wrong k) shows at once."""
+    M, N, K = 300, 260, 64
+    g = torch.Generator().manual_seed(41)
+    if which == "lo(A) hi(B)":
+        A = fractional(M, K, 42)
+        B = torch.randint(-3, 4, (K, N), generator=g).float()
+    else:
+        A = torch.randint(-3, 4, (M, K), generator=g).float()
+        B = fractional(K, N, 43)
+    want = (A.double() @ B.double()).float()
+    assert torch.equal(want.double(), A.double() @ B.double())
+    for ta, tb in TRANS:
+        C = run_mode(X3, A, B, ta, tb, workspace=True)
+        assert torch.equal(C, want), (which, ta, tb)
+    # the tf32 product misses the lo parts
+    assert not torch.equal(run_mode(TF32, A, B, workspace=True), want)
+
+
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (2.5, 0.0), (-1.0, 1.0), (0.5, -2.0)])
+def test_3xtf32_split_alpha_beta(oracle_mod, alpha, beta):
+    M, N, K = 300, 260, 190
+    A, B = inputs.make(M, N, K, "f32", "normal", 0.1, seed=int(10 * alpha - 7 * beta) + 78)
+    C0 = torch.from_numpy(np.random.default_rng(5).standard_normal((M, N)).astype(np.float32))
+    for ldc in (N, N + 1):
+        C = run_mode(X3, A, B, 0, 0, alpha, beta, C0, ldc=ldc, workspace=True)
+        check(oracle_mod, A, B, C, TOL["f32"], 0, 0, alpha, beta, C0)
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 384, 1001), (512, 512, 8192), (2304, 2560, 1024)])
+def test_3xtf32_split_over_clusters(oracle_mod, M, N, K):
+    """Few tiles with 3 x L k-blocks: the stream-K split over clusters cuts
+    across the three terms (a range may start in one term and end in
+    another), within the fp32 bound; unaligned K pads each term's last k-block
+    with TMA's zero fill."""
+    P = 1 << 16
+    L3 = 3 * ((K + 31) // 32)
+    tiles = ((M + 255) // 256) * ((N + 255) // 256)
+    lo = (M + N) * rup(K, 4) * 4
+    # split: the stream-K slots (one 128 x 256 fp32 slot per SM) before the lo parts
+    assert split_bytes(X3, M, N, K, 0, 1) >= lo + 152 * 128 * 256 * 4
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=M + N + K)
+    C = run_mode(X3, A, B, 0, 1, workspace=True)
+    worst = check(oracle_mod, A, B, C, TOL["f32"], 0, 1)
+    print(f"3xtf32 split {M}x{N}x{K} ({tiles} tiles, {L3} k-blocks): worst {worst:.3g}")
+
+
+def test_3xtf32_split_full_size_3072_sampled(oracle_mod):
+    """The fp32 3072^3 workload in 3xTF32 with its workspace (B transposed,
+    lo parts): sampled rows and random entries against the oracle."""
+    A, B = inputs.make_workload("f32_3072")
+    C = run_mode(X3, A, B, workspace=True)
+    Cg = C.numpy()
+    assert not np.isnan(Cg).any()
+    Ah, Bh = A.numpy(), B.numpy()
+    g = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, 3071], g.integers(0, 3072, 14)]))
+    ref, refabs = oracle_mod.gemm(np.ascontiguousarray(Ah[rows]), Bh)
+    ok, w1 = oracle_mod.within_bound(Cg[rows], ref, refabs, TOL["f32"])
+    assert ok, w1
+    ri, ci = g.integers(0, 3072, 4096), g.integers(0, 3072, 4096)
+    ref, refabs = oracle_mod.gemm_entries(Ah, Bh, ri, ci)
+    ok, w2 = oracle_mod.within_bound(Cg[ri, ci], ref, refabs, TOL["f32"])
+    assert ok, w2
+    print(f"3xtf32 split 3072^3: worst {max(w1, w2):.3g}")
+
+
+@pytest.mark.parametrize("code", [TF32, X3])
+@pytest.mark.parametrize("M,N,K", [(1000, 777, 130), (300, 520, 64)])
+def test_pair_kernel_tf32_keeps_padding(oracle_mod, code, M, N, K):
+    """TF32 and split 3xTF32 on the pair kernel (A stored M x K, B N x K, a
+    workspace) write C through its TMA-store epilogue: with a padded pitch the
+    columns past N and the memory past the last row keep their NaN."""
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=M + N + K + code)
+    As, Bs = stored(A, 0), stored(B, 1)
+    lda = ldb = rup(K, 4)
+    ldc = rup(N, 4) + 8
+    _ab, a = to_device_padded(As, lda)
+    _bb, b = to_device_padded(Bs, ldb)
+    cbuf = torch.full((M * ldc + 4096,), float("nan"), device="cuda")
+    need = g14.workspace_bytes_ex(code, 0, 1, M, N, K, a.data_ptr(), lda, b.data_ptr(), ldb,
+                                  cbuf.data_ptr(), ldc)
+    ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    g14.gemm_ex(code, 0, 1, M, N, K, 1.0, a.data_ptr(), lda, b.data_ptr(), ldb, 0.0,
+                cbuf.data_ptr(), ldc, ws.data_ptr(), need, s)
+    assert g14.check_device_error(s) == 0
+    torch.cuda.synchronize()
+    full = cbuf.cpu()
+    rows = full[:M * ldc].view(M, ldc)
+    assert torch.isnan(rows[:, N:]).all()
+    assert torch.isnan(full[M * ldc:]).all()
+    check(oracle_mod, A, B, rows[:, :N].contiguous(), TOL["f32"], 0, 0,
+          rounded=code == TF32)

@@ -120,7 +120,8 @@ def test_workspace_bytes_ex_adds_room_to_repitch():
 def test_workspace_bytes_ex_tf32_transposes_into_k_major():
     """TF32 reads fp32 operands straight from TMA only K-major (A stored M x K,
     B stored N x K): other storages get K-major copies in the workspace, after
-    the stream-K region of the pair kernel's split (plan kernel 5)."""
+    the stream-K region of the pair kernel's split (plan kernel 5). 3xTF32 on
+    that kernel also needs lo(A) and lo(B), written after the copies."""
     g14.load()
     TF32, X3 = g14.GEMM14_DTYPE_TF32, g14.GEMM14_DTYPE_F32_3XTF32
     P = 1 << 20
@@ -135,8 +136,26 @@ def test_workspace_bytes_ex_tf32_transposes_into_k_major():
     M, N, K = 2304, 2560, 4096
     sk = 768 + 152 * 128 * 256 * 4
     assert ex(TF32, 0, 0, M, N, K, P, K, P, N, P, N, 152) == sk + N * K * 4
-    # 3xTF32 needs its lo tiles in every storage: no transposed copies
-    assert ex(X3, 0, 0, n, n, n, P, n, P, n, P, n, 152) == 0
+    # 3xTF32 takes the same K-major copies and lo(A), lo(B) after them (both
+    # K-major, pitch K rounded up to 4 floats), in every storage
+    lo = 2 * n * n * 4
+    assert ex(X3, 0, 1, n, n, n, P, n, P, n, P, n, 152) == flags + lo
+    assert ex(X3, 0, 0, n, n, n, P, n, P, n, P, n, 152) == flags + n * n * 4 + lo
+    assert ex(X3, 1, 0, n, n, n, P, n, P, n, P, n, 152) == flags + 2 * n * n * 4 + lo
+    # its 3 x 128 k-blocks at 1.18 waves are split like TF32's
+    M, N, K = 2304, 2560, 4096
+    assert ex(X3, 0, 1, M, N, K, P, K, P, K, P, N, 152) == sk + (M + N) * K * 4
+    # 4 pair tiles of 3 x 32 k-blocks: split over 12 clusters (3 terms make k
+    # long enough where TF32's 32 k-blocks stay unsplit); K rounded up to 1004
+    M, N, K = 512, 384, 1001
+    assert ex(X3, 0, 1, M, N, K, P, 1004, P, 1004, P, N, 152) == \
+        _r256(sk + M * 1004 * 4) + N * 1004 * 4
+    # without the pair kernel 3xTF32 runs on the converter kernel: no copies
+    prev = g14.set_pair_kernel(False)
+    try:
+        assert ex(X3, 0, 0, n, n, n, P, n, P, n, P, n, 152) == 0
+    finally:
+        g14.set_pair_kernel(prev)
     # a transposed copy has K rounded up to 4 floats: B (K x N) -> N x round4(K);
     # 4 pair tiles of 32 k-blocks are not split, so the copy follows the flags
     M, N, K = 512, 384, 1001
