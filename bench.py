@@ -208,9 +208,10 @@ def workload_info(name):
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def time_oracle_sample(name: str, target_s: float, A=None, B=None):
+def time_oracle_sample(name: str, target_s: float, A=None, B=None, want_rows=False):
     """Times the oracle on the first R rows of the named product, R sized so
-    the call takes about target_s seconds. Returns (flops, seconds, rows, threads)."""
+    the call takes about target_s seconds. Returns (flops, seconds, rows,
+    threads), and with want_rows also the oracle's R x N rows (float64)."""
     import oracle
     from dense_gemm_14_gb300 import inputs, roofline
     w = inputs.WORKLOADS[name]
@@ -218,15 +219,45 @@ def time_oracle_sample(name: str, target_s: float, A=None, B=None):
         A, B = inputs.make_workload(name)
     Ah, Bh = inputs.host_view(A), inputs.host_view(B)
     M, (K, N) = Ah.shape[0], Bh.shape
+    # two probes: 32 rows (whose time is mostly start-up), then about half a
+    # second's worth, from which the sample's rows are sized
     rows = min(M, 32)
+    for probe_s in (0.5, target_s):
+        t0 = time.perf_counter()
+        oracle.gemm(Ah[:rows], Bh, w.dtype, with_abs=False)
+        probe = time.perf_counter() - t0
+        rows = int(max(1, min(M, rows * min(probe_s, target_s) / max(probe, 1e-6))))
     t0 = time.perf_counter()
-    oracle.gemm(Ah[:rows], Bh, w.dtype, with_abs=False)
-    probe = time.perf_counter() - t0
-    rows = int(max(1, min(M, rows * target_s / max(probe, 1e-6))))
-    t0 = time.perf_counter()
-    oracle.gemm(Ah[:rows], Bh, w.dtype, with_abs=False)
+    ref, _ = oracle.gemm(Ah[:rows], Bh, w.dtype, with_abs=False)
     dt = time.perf_counter() - t0
-    return roofline.flops(rows, N, K), dt, rows, oracle.max_threads()
+    out = (roofline.flops(rows, N, K), dt, rows, oracle.max_threads())
+    return out + (ref,) if want_rows else out
+
+
+# The element-wise bounds the parity tests hold the products to:
+# |C - C_ref| <= bound * (|A| |B|) element by element.
+ELEMENT_BOUND = {"f32": 1e-5, "bf16": 4e-3}
+
+
+def accuracy_of(name, A, B, C_dev, ref_rows, abs_rows=16):
+    """The GPU product's first rows against the oracle: relative RMSE
+    ||C - C_ref||_2 / ||C_ref||_2 over the rows the oracle timing computed,
+    and the largest |C - C_ref| / (|A| |B|) over the first abs_rows rows
+    (its bound beside it)."""
+    import numpy as np
+
+    import oracle
+    from dense_gemm_14_gb300 import inputs
+    w = inputs.WORKLOADS[name]
+    r = ref_rows.shape[0]
+    got = C_dev[:r].double().cpu().numpy()
+    rmse = float(np.linalg.norm(got - ref_rows) / max(np.linalg.norm(ref_rows), 1e-300))
+    ra = min(abs_rows, r)
+    Ah, Bh = inputs.host_view(A), inputs.host_view(B)
+    ref, refabs = oracle.gemm(np.ascontiguousarray(Ah[:ra]), Bh, w.dtype, with_abs=True)
+    ok, worst = oracle.within_bound(got[:ra], ref, refabs, ELEMENT_BOUND[w.dtype])
+    return {"workload": name, "rows_rmse": r, "rel_rmse": rmse, "rows_bound": ra,
+            "max_err_over_abs": worst, "bound": ELEMENT_BOUND[w.dtype], "within": ok}
 
 
 def run_reference(args, dist: Dist, data=None):
@@ -443,15 +474,21 @@ def run_ours(args, dist: Dist):
 
     # ---- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
+    accuracy = None
     if dist.world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
         tf, tt, desc, threads = 0.0, 0.0, [], 1
+        accuracy = []
         for p in parts:
-            f, t, r, threads = time_oracle_sample(p["name"], args.cpu_seconds, *host[p["name"]])
+            f, t, r, threads, ref_rows = time_oracle_sample(p["name"], args.cpu_seconds,
+                                                            *host[p["name"]], want_rows=True)
             tf += f
             tt += t
             desc.append(f"first {r} rows of {p['name']}")
+            # the rows the oracle computed, against the GPU's C (every operand
+            # set holds the same A and B, so set 0's C is the product's)
+            accuracy.append(accuracy_of(p["name"], *host[p["name"]], p["sets"][0][2], ref_rows))
         cpu = {"value": tf / tt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": "; ".join(desc) + " (fp64 oracle, product only)", "seconds": tt}
 
@@ -475,6 +512,7 @@ def run_ours(args, dist: Dist):
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "accuracy": accuracy,
         }
         print(json.dumps(line), flush=True)
 

@@ -75,3 +75,21 @@ def test_source_hash_and_traffic_gate(tmp_path, monkeypatch):
     t = bench.traffic_for("sgemm_simt_kernel", "sgemm_simt.cu", "f32_3072")
     assert t is None or t > 0
     assert bench.traffic_for("sgemm_simt_kernel", "sgemm_simt.cu", "other_workload") is None
+
+
+def test_accuracy_of_reports_the_oracle_comparison():
+    """The bench's accuracy entry (computed in its oracle leg): a correctly
+    rounded product is within the bound with a tiny relative RMSE; one wrong
+    element in the sampled rows is reported."""
+    from dense_gemm_14_gb300 import inputs
+    A, B = inputs.make_workload("f32_256")
+    C = (A.double() @ B.double()).float()
+    _, _, rows, _, ref_rows = bench.time_oracle_sample("f32_256", 0.01, A, B, want_rows=True)
+    assert ref_rows.shape == (rows, 256)
+    acc = bench.accuracy_of("f32_256", A, B, C, ref_rows)
+    assert acc["within"] and acc["rel_rmse"] < 1e-7 and acc["bound"] == 1e-5
+    assert acc["max_err_over_abs"] < 1e-7 and acc["rows_bound"] == min(16, rows)
+    bad = C.clone()
+    bad[0, 3] += 1.0
+    acc = bench.accuracy_of("f32_256", A, B, bad, ref_rows)
+    assert not acc["within"] and acc["max_err_over_abs"] > 1e-5 and acc["rel_rmse"] > 1e-4
