@@ -15,6 +15,7 @@ GEMM14_ERR_INVALID_ARG = 1
 GEMM14_ERR_UNSUPPORTED_DEVICE = 2
 GEMM14_ERR_CUDA = 3
 GEMM14_ERR_TIMEOUT = 4
+GEMM14_ERR_DEVICE_CHECK = 5
 
 GEMM14_DTYPE_F32 = 0
 GEMM14_DTYPE_BF16 = 1

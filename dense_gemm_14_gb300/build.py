@@ -4,7 +4,11 @@ The translation units are compiled in parallel, then linked into one shared
 library with the CUDA runtime linked statically, so the library depends on
 nothing but the driver (libcuda, reached at run time) and libc/libstdc++.
 
-    python -m dense_gemm_14_gb300.build [--force] [--verbose]
+    python -m dense_gemm_14_gb300.build [--force] [--verbose] [--checked]
+
+--checked builds the variant with the device-side bounds checks
+(-DGEMM14_DEVICE_CHECKS, csrc/checks.h) into _build_checked/; select it at run
+time with GEMM14_LIB=<path of its libgemm14.so>.
 """
 from __future__ import annotations
 
@@ -17,13 +21,15 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
+CHECKED_BUILD_DIR = os.path.join(HERE, "_build_checked")
+CHECKED_FLAGS = ["-DGEMM14_DEVICE_CHECKS"]
 LIB_NAME = "libgemm14.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["api.cu", "sgemm_simt.cu", "hgemm_tc.cu", "hgemm_tc2.cu", "sgemm_tc3.cu", "epilogue.cu",
            "host_path.cu", "copy.cu", "plan.cu"]
-HEADERS = ["ptx.cuh", "kernels.h", "streamk.cuh", "api_internal.h", "plan.h",
+HEADERS = ["ptx.cuh", "kernels.h", "streamk.cuh", "api_internal.h", "plan.h", "checks.h",
            "libgemm14.map"]
 
 NVCC_FLAGS = [
@@ -49,19 +55,25 @@ def _stale(lib: str, inputs) -> bool:
     return any(os.path.getmtime(p) > t for p in inputs)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str | None = None) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str | None = None,
+          checked: bool = False) -> str:
     """Compiles every .cu and links libgemm14.so; returns its path.
 
     extra_flags (e.g. schedule macros such as -DSGEMM_UNROLL=2) and out_dir
     allow building variants side by side; the default build is the product.
+    checked: the variant with the device-side bounds checks, in its own folder
+    (rebuilt only when a source changed, like the product).
     """
+    if checked:
+        extra_flags = list(extra_flags) + CHECKED_FLAGS
+        out_dir = out_dir or CHECKED_BUILD_DIR
     build_dir = out_dir or BUILD_DIR
     lib_path = os.path.join(build_dir, LIB_NAME)
     os.makedirs(build_dir, exist_ok=True)
     inputs = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
     inputs.append(os.path.join(INCLUDE, "gemm14.h"))
     inputs.append(os.path.abspath(__file__))
-    if not force and not extra_flags and not _stale(lib_path, inputs):
+    if not force and (checked or not extra_flags) and not _stale(lib_path, inputs):
         return lib_path
     cc = nvcc()
     procs = []
@@ -96,8 +108,10 @@ def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
+    ap.add_argument("--checked", action="store_true",
+                    help="the variant with device-side bounds checks, in _build_checked/")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=a.verbose))
+    print(build(force=a.force, verbose=a.verbose, checked=a.checked))
 
 
 if __name__ == "__main__":

@@ -556,6 +556,13 @@ int current_device_index(int* device) {
   return GEMM14_OK;
 }
 
+// The status a device error word stands for: a failed bounds check (checked
+// builds) first, then any other recorded failure (an expired wait).
+int status_of_error_word(unsigned word) {
+  if (word & kDevErrBounds) return GEMM14_ERR_DEVICE_CHECK;
+  return word ? GEMM14_ERR_TIMEOUT : GEMM14_OK;
+}
+
 int take_device_error() {
   const DeviceInfo* dev = nullptr;
   int st = current_device(&dev);
@@ -567,7 +574,7 @@ int take_device_error() {
     set_cuda_error("reading the device error word", e);
     return GEMM14_ERR_CUDA;
   }
-  return word ? GEMM14_ERR_TIMEOUT : GEMM14_OK;
+  return status_of_error_word(word);
 }
 
 void note_cuda_error(const char* what, cudaError_t e) { set_cuda_error(what, e); }
@@ -674,6 +681,7 @@ const char* gemm14_status_string(int status) {
     case GEMM14_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
     case GEMM14_ERR_CUDA: return "CUDA error";
     case GEMM14_ERR_TIMEOUT: return "device-side wait timed out";
+    case GEMM14_ERR_DEVICE_CHECK: return "device-side bounds check failed (access skipped)";
     default: return "unknown status";
   }
 }
@@ -696,7 +704,7 @@ int gemm14_check_device_error(void* stream_ptr) {
     set_cuda_error("reading the device error word", e);
     return GEMM14_ERR_CUDA;
   }
-  return word ? GEMM14_ERR_TIMEOUT : GEMM14_OK;
+  return status_of_error_word(word);
 }
 
 int gemm14_plan_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,

@@ -159,16 +159,21 @@ __device__ __forceinline__ void soft_load_stage(uint8_t* a_st, const GemmArgs& a
 // any is used.
 constexpr int kPre = 4;
 
+// (Slot w holds worker w's 128 x BN partial sums; args.sk.G slots. A load the
+// bounds checks reject reads as zeros.)
 template <int BN, int NP>
-__device__ __forceinline__ void load_partials(float4 (&p)[NP][8], const float* partials, int cw0,
+__device__ __forceinline__ void load_partials(float4 (&p)[NP][8], const GemmArgs& args, int cw0,
                                               int n, int r_loc, int c) {
 #pragma unroll
   for (int j = 0; j < NP; ++j) {
     if (j < n) {
-      const float* src =
-          partials + (static_cast<size_t>(cw0 + j) * H::BM + r_loc) * BN + c * 32;
+      const int64_t off = (static_cast<int64_t>(cw0 + j) * H::BM + r_loc) * BN + c * 32;
+      const bool ok = dev_check(slot_span_ok(off, cw0 + j, H::BM * BN, args.sk.G, 32), args.err);
+      const float* src = args.partials + off;
 #pragma unroll
-      for (int v = 0; v < 8; ++v) p[j][v] = __ldcg(reinterpret_cast<const float4*>(src + 4 * v));
+      for (int v = 0; v < 8; ++v)
+        p[j][v] = ok ? __ldcg(reinterpret_cast<const float4*>(src + 4 * v))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
@@ -406,6 +411,7 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
         if (warp == 2 && lane == 0) {
           bool all = true;
           for (int c = w + 1; c <= sm.sched.head_last && all; ++c) {
+            if (!dev_check(index_ok(c, args.sk.G), args.err)) break;
             all = flag_wait(args.flags + c, args.epoch, wc);
             if (all) flag_clear(args.flags + c);
           }
@@ -431,12 +437,15 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
         constexpr int NP = kTma ? kPre : 1;
         float4 pre[NP][8];
         const int n_pre = (kSK && kind == kSegHead) ? min(NP, sm.sched.head_last - w) : 0;
-        if (kSK) load_partials<BN, NP>(pre, args.partials, w + 1, n_pre, r_loc, c);
+        if (kSK) load_partials<BN, NP>(pre, args, w + 1, n_pre, r_loc, c);
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tc_wait_ld();
         if (kSK && kind == kSegPartial) {
           // Stream-K: partial sums of this tile go to workspace slot w.
+          if (!dev_check(slot_span_ok(prow + c * 32 - args.partials, w, H::BM * BN, args.sk.G, 32),
+                         args.err))
+            continue;
 #pragma unroll
           for (int v = 0; v < 8; ++v)
             __stcg(reinterpret_cast<float4*>(prow + c * 32 + 4 * v),
@@ -450,7 +459,7 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
           add_partials<NP>(r, pre, n_pre);
           for (int cw0 = w + 1 + NP; cw0 <= sm.sched.head_last; cw0 += NP) {
             const int n = min(NP, sm.sched.head_last - cw0 + 1);
-            load_partials<BN, NP>(pre, args.partials, cw0, n, r_loc, c);
+            load_partials<BN, NP>(pre, args, cw0, n, r_loc, c);
             add_partials<NP>(r, pre, n);
           }
         }
@@ -503,7 +512,8 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
         // All four warps' partial stores precede the flag. A worker has at
         // most one PARTIAL segment: the barrier's first phase.
         if (lane == 0) mbar_arrive(&sm.partial_stored);
-        if (warp == 2 && lane == 0 && mbar_wait(&sm.partial_stored, 0, wc))
+        if (warp == 2 && lane == 0 && mbar_wait(&sm.partial_stored, 0, wc) &&
+            dev_check(index_ok(w, args.sk.G), args.err))
           flag_publish(args.flags + w, args.epoch);
       }
     }

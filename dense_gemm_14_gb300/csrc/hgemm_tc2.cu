@@ -290,6 +290,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
              (static_cast<size_t>(2 * c + rank) * (P::BN / 32) + chunk) * 8 * 128 +
              static_cast<size_t>(v) * 128 + r_loc;
     };
+    // the bounds checks of a slot access (2 args.sk.G slots of 8 x 8 x 128 float4)
+    auto slot_ok = [&](int c, int chunk, int v) {
+      const int64_t off = slot4(c, chunk, v) - reinterpret_cast<float4*>(args.partials);
+      return dev_check(slot_span_ok(off, 2 * c + static_cast<int>(rank), (P::BN / 32) * 8 * 128,
+                                    2 * static_cast<int64_t>(args.sk.G), 1),
+                       args.err);
+    };
+    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int seg = 0; seg < n_seg; ++seg) {
       int t, kb0, kb1, kind, tm, tn;
       segment(seg, t, kb0, kb1, kind);
@@ -307,6 +315,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
         if (warp == 2 && lane == 0) {
           bool all = true;
           for (int c = w + 1; c <= sm.sched.head_last && all; ++c) {
+            if (!dev_check(index_ok(2 * c + rank, 2 * static_cast<int64_t>(args.sk.G)),
+                           args.err))
+              break;
             all = flag_wait(args.flags + 2 * c + rank, args.epoch, wc);
             if (all) flag_clear(args.flags + 2 * c + rank);
           }
@@ -329,7 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
         float4 pre[8];
         if (kSK && kind == kSegHead && sm.sched.head_last > w) {
 #pragma unroll
-          for (int v = 0; v < 8; ++v) pre[v] = __ldcg(slot4(w + 1, c, v));
+          for (int v = 0; v < 8; ++v) pre[v] = slot_ok(w + 1, c, v) ? __ldcg(slot4(w + 1, c, v)) : zero4;
         }
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
@@ -338,7 +349,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
           // Stream-K: this CTA's partial sums of the tile go to its slot.
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            __stcg(slot4(w, c, v),
+            if (slot_ok(w, c, v))
+              __stcg(slot4(w, c, v),
                    make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
                                __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
           continue;
@@ -348,7 +360,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
           for (int cw = w + 1; cw <= sm.sched.head_last; ++cw) {
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
-              const float4 p = cw == w + 1 ? pre[v] : __ldcg(slot4(cw, c, v));
+              const float4 p = cw == w + 1 ? pre[v]
+                               : slot_ok(cw, c, v) ? __ldcg(slot4(cw, c, v)) : zero4;
               r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + p.x);
               r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + p.y);
               r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + p.z);
@@ -401,7 +414,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P::THREADS, 1)
         // All four warps' partial stores precede the flag. A worker has at
         // most one PARTIAL segment: the barrier's first phase.
         if (lane == 0) mbar_arrive(&sm.partial_stored);
-        if (warp == 2 && lane == 0 && mbar_wait(&sm.partial_stored, 0, wc))
+        if (warp == 2 && lane == 0 && mbar_wait(&sm.partial_stored, 0, wc) &&
+            dev_check(index_ok(2 * w + rank, 2 * static_cast<int64_t>(args.sk.G)), args.err))
           flag_publish(args.flags + 2 * w + rank, args.epoch);
       }
     }

@@ -8,6 +8,7 @@
 
 #include <utility>
 
+#include "checks.h"
 #include "streamk.cuh"
 
 namespace gemm14 {
@@ -75,14 +76,18 @@ struct GemmArgs {
 // (p 16-byte aligned). kEpiAccum reads C; the others do not. kGeneral false:
 // a plain store, with args.epi not consulted (kernels compiled for the
 // kEpiStore case only).
+// Both skip a store outside C's M x N block when the device-side bounds checks
+// are compiled in (checks.h).
 template <bool kGeneral>
 __device__ __forceinline__ void epi_store1(const GemmArgs& a, float* p, float s) {
+  if (!dev_check(c_span_ok(p - a.C, a.ldc, a.M, a.N, 1), a.err)) return;
   if (!kGeneral || a.epi == kEpiStore) *p = s;
   else if (a.epi == kEpiScale) *p = a.alpha * s;
   else *p = fmaf(a.alpha, s, a.beta * *p);
 }
 template <bool kGeneral>
 __device__ __forceinline__ void epi_store4(const GemmArgs& a, float* p, float4 v) {
+  if (!dev_check(c_span_ok(p - a.C, a.ldc, a.M, a.N, 4), a.err)) return;
   float4* q = reinterpret_cast<float4*>(p);
   if (!kGeneral || a.epi == kEpiStore) {
     *q = v;

@@ -11,9 +11,12 @@
 #include <cstdint>
 #include <cuda.h>  // CUtensorMap (type only; the driver is reached at run time)
 
+#include "checks.h"
+
 namespace gemm14 {
 
-// Bits OR-ed into the library's device error word.
+// Bits OR-ed into the library's device error word (and kDevErrBounds, the
+// device-side bounds checks' bit, in checks.h).
 enum : unsigned { kDevErrTimeout = 1u, kDevErrBadConfig = 2u };
 
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // default limit of one wait: 2 s

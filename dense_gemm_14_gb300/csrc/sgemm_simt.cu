@@ -424,6 +424,16 @@ __global__ void __launch_bounds__(S::THREADS, 1)
       // PARTIAL must survive until its owner has read it).
       float* slot = args.partials +
                     static_cast<size_t>(kind == kSegHead ? args.sk.G + w : w) * (S::BM * S::BN);
+#ifdef GEMM14_DEVICE_CHECKS
+      // the bounds checks of a slot access (2 args.sk.G slots of BM x BN); the
+      // product build compiles none of them (this kernel's registers are tight)
+      const int own = kind == kSegHead ? args.sk.G + w : w;
+      auto slot_ok = [&](const float* p, int s, int width) {
+        return dev_check(slot_span_ok(p - args.partials, s, S::BM * S::BN,
+                                      2 * static_cast<int64_t>(args.sk.G), width),
+                         args.err);
+      };
+#endif
       {
         using LY = Lay<kLay>;
 #pragma unroll
@@ -432,6 +442,11 @@ __global__ void __launch_bounds__(S::THREADS, 1)
 #pragma unroll
           for (int p = 0; p < 8; p += 2) {
             const float2 lo = unpack2(acc2[i][p]), hi = unpack2(acc2[i][p + 1]);
+#ifdef GEMM14_DEVICE_CHECKS
+            if (!slot_ok(srow + LY::col(warp_n, tc, 2 * p), own, 1) ||
+                !slot_ok(srow + LY::col(warp_n, tc, 2 * p + 3), own, 1))
+              continue;
+#endif
             if (LY::BK) {
               __stcg(srow + LY::col(warp_n, tc, 2 * p), lo.x);
               __stcg(srow + LY::col(warp_n, tc, 2 * p + 1), lo.y);
@@ -446,12 +461,14 @@ __global__ void __launch_bounds__(S::THREADS, 1)
       }
       if (kind == kSegPartial) {
         __syncthreads();
-        if (threadIdx.x == 0) flag_publish(args.flags + w, args.epoch);
+        if (threadIdx.x == 0 && dev_check(index_ok(w, args.sk.G), args.err))
+          flag_publish(args.flags + w, args.epoch);
         continue;
       }
       const int last = sm.sched.head_last;
       if (threadIdx.x == 0)
         for (int c = w + 1; c <= last; ++c) {
+          if (!dev_check(index_ok(c, args.sk.G), args.err)) break;
           if (!flag_wait(args.flags + c, args.epoch, wc)) break;  // raises abort on expiry
           flag_clear(args.flags + c);
         }
@@ -465,15 +482,31 @@ __global__ void __launch_bounds__(S::THREADS, 1)
       for (int u0 = 0; u0 < kPer; u0 += 8) {
         float4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
+        for (int u = 0; u < 8; ++u) {
+#ifdef GEMM14_DEVICE_CHECKS
+          if (!slot_ok(slot + 4 * (threadIdx.x + (u0 + u) * S::THREADS), own, 4)) {
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            continue;
+          }
+#endif
           v[u] = __ldcg(reinterpret_cast<const float4*>(slot) + threadIdx.x + (u0 + u) * S::THREADS);
+        }
 #pragma unroll 1
         for (int c = w + 1; c <= last; ++c) {
           const float4* src = reinterpret_cast<const float4*>(
               args.partials + static_cast<size_t>(c) * (S::BM * S::BN));
           float4 p[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) p[u] = __ldcg(src + threadIdx.x + (u0 + u) * S::THREADS);
+          for (int u = 0; u < 8; ++u) {
+#ifdef GEMM14_DEVICE_CHECKS
+            if (!slot_ok(reinterpret_cast<const float*>(src + threadIdx.x + (u0 + u) * S::THREADS),
+                         c, 4)) {
+              p[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+              continue;
+            }
+#endif
+            p[u] = __ldcg(src + threadIdx.x + (u0 + u) * S::THREADS);
+          }
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             v[u].x += p[u].x; v[u].y += p[u].y; v[u].z += p[u].z; v[u].w += p[u].w;

@@ -52,7 +52,10 @@ typedef enum gemm14_status {
   GEMM14_ERR_UNSUPPORTED_DEVICE = 2, /* no CUDA device, or it is not compute capability 10.3 */
   GEMM14_ERR_CUDA = 3,               /* a CUDA runtime/driver call failed; see
                                         gemm14_last_error_string() */
-  GEMM14_ERR_TIMEOUT = 4             /* a kernel's bounded wait expired (device-side) */
+  GEMM14_ERR_TIMEOUT = 4,            /* a kernel's bounded wait expired (device-side) */
+  GEMM14_ERR_DEVICE_CHECK = 5        /* a device-side bounds check failed and its access was
+                                        skipped (only a library built with
+                                        GEMM14_DEVICE_CHECKS runs these checks) */
 } gemm14_status;
 
 /*
@@ -269,8 +272,10 @@ const char* gemm14_last_error_string(void);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error
- * word. Returns GEMM14_ERR_TIMEOUT if a kernel recorded an expired wait since
- * the last check, GEMM14_ERR_CUDA if the synchronisation failed, else OK.
+ * word. Returns GEMM14_ERR_DEVICE_CHECK if a kernel of a checked build
+ * skipped an access its bounds checks rejected since the last check, else
+ * GEMM14_ERR_TIMEOUT if a kernel recorded an expired wait,
+ * GEMM14_ERR_CUDA if the synchronisation failed, else OK.
  */
 int gemm14_check_device_error(void* stream);
 

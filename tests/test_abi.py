@@ -56,7 +56,7 @@ def test_exports_are_exactly_the_header(lib):
 
 def test_status_strings(lib):
     assert g14.status_string(0) == "ok"
-    for s in range(1, 5):
+    for s in range(1, 6):
         assert g14.status_string(s) and g14.status_string(s) != "unknown status"
     assert g14.status_string(99) == "unknown status"
     assert g14.version() >= 100

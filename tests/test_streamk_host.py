@@ -178,3 +178,13 @@ def test_workspace_bytes_ex_fp32_b_stored_n_by_k():
     # ... not for narrower products
     assert ex(F32, 0, 0, n, 2047, n, P, n, P, 2048, P, 2048, 152) == \
         g14.workspace_bytes(F32, n, 2047, n, 152)
+
+
+def test_device_check_predicates(tmp_path):
+    """The predicates of the device-side bounds checks (csrc/checks.h), on
+    the host: in-bounds accesses pass, one element outside fails."""
+    exe = tmp_path / "checks_predicates"
+    subprocess.run(["g++", "-std=c++17", "-O1", "-I", CSRC, "-o", str(exe),
+                    os.path.join(ROOT, "tests", "checks_predicates.cpp")], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", out.stdout
