@@ -104,7 +104,7 @@ __device__ __forceinline__ void epi_store4(const GemmArgs& a, float* p, float4 v
 // per SM (a region whose place and size never depend on the product, so a
 // workspace reused for another shape never finds partial sums where a flag
 // is expected), then `spw` tile slots of bm x bn floats per worker (slot w: a
-// worker's PARTIAL; slot G + w, fp32 kernel only: its HEAD's own sums).
+// worker's PARTIAL).
 inline size_t streamk_flag_bytes(int sms) {
   return ((static_cast<size_t>(sms) * sizeof(unsigned) + 255) / 256) * 256;
 }

@@ -115,11 +115,12 @@ void plan_for(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t
 }
 
 // Stream-K workspace the call would use with a workspace (0: it uses none).
-// Tile slots per worker: the fp32 kernel's HEAD keeps its own sums in a
-// second slot; the tensor-core kernels' HEAD adds straight from TMEM. The
-// pair kernel's worker is a cluster of two SMs with a 256 x 256 tile: one
-// 128 x 256 slot (and flag) per CTA, i.e. per SM, like the one-SM kernels.
-int slots_per_worker(const gemm14_plan& plan) { return plan.kernel == 1 ? 2 : 1; }
+// One tile slot per worker, for its PARTIAL: a HEAD adds the later workers'
+// slots into its accumulators (registers on the fp32 kernel, TMEM on the
+// tensor-core kernels). The pair kernel's worker is a cluster of two SMs with
+// a 256 x 256 tile: one 128 x 256 slot (and flag) per CTA, i.e. per SM, like
+// the one-SM kernels.
+int slots_per_worker(const gemm14_plan&) { return 1; }
 
 // The CTA-pair kernel's split, measured on GB300 against its unsplit run:
 // - between one and one and a half waves of tiles with long k (>= 64

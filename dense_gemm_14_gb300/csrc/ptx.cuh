@@ -208,8 +208,11 @@ __device__ __forceinline__ void flag_clear(unsigned* flag) {
 }
 
 // Waits until *flag == value (acquire, GPU scope), bounded like mbar_wait.
-static __device__ __noinline__ bool flag_wait(const unsigned* flag, unsigned value,
-                                              const WaitCtx& w) {
+// flag_wait_inline is the loop itself, for a caller that holds many live
+// registers across the wait (a call would have to save them); flag_wait is
+// the same loop as a call.
+__device__ __forceinline__ bool flag_wait_inline(const unsigned* flag, unsigned value,
+                                                 const WaitCtx& w) {
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t i = 0;; ++i) {
     unsigned v;
@@ -227,6 +230,10 @@ static __device__ __noinline__ bool flag_wait(const unsigned* flag, unsigned val
     }
     __nanosleep(64);
   }
+}
+static __device__ __noinline__ bool flag_wait(const unsigned* flag, unsigned value,
+                                              const WaitCtx& w) {
+  return flag_wait_inline(flag, value, w);
 }
 
 // ---------------------------------------------------------------- TMA

@@ -414,23 +414,22 @@ __global__ void __launch_bounds__(S::THREADS, 1)
     }
     if (!ok) break;
 
-    // Stream-K: PARTIAL and HEAD segments leave their sums in workspace slot
-    // w (tile-local element (r, c) at r * BN + c). A PARTIAL then publishes
-    // flag w. A HEAD waits for the later workers' flags and reduces the slots
-    // w, w+1, ..., head_last in that order into C, a plain loop over the tile
-    // with the accumulators no longer live.
-    if (kSK && kind != kSegFull) {
-      // PARTIAL -> slot w; HEAD -> slot G + w (a worker may hold both, and a
-      // PARTIAL must survive until its owner has read it).
-      float* slot = args.partials +
-                    static_cast<size_t>(kind == kSegHead ? args.sk.G + w : w) * (S::BM * S::BN);
+    // Stream-K. A PARTIAL stores its sums to workspace slot w (tile-local
+    // element (r, c) at r * BN + c) and publishes flag w. A HEAD waits for the
+    // later workers' flags and adds their slots w+1, ..., head_last, in that
+    // order, into its own accumulators, then stores the tile like a FULL one.
+    // Every worker runs the same thread mapping (Lay), so the element a thread
+    // holds sits at the same place in each slot: the adds read the slots in
+    // the accumulators' layout, and the sum is own + p(w+1) + p(w+2) + ...
+    // as before, without a slot of the owner's own.
+    if (kSK && kind == kSegPartial) {
+      float* slot = args.partials + static_cast<size_t>(w) * (S::BM * S::BN);
 #ifdef GEMM14_DEVICE_CHECKS
-      // the bounds checks of a slot access (2 args.sk.G slots of BM x BN); the
+      // the bounds checks of a slot access (args.sk.G slots of BM x BN); the
       // product build compiles none of them (this kernel's registers are tight)
-      const int own = kind == kSegHead ? args.sk.G + w : w;
       auto slot_ok = [&](const float* p, int s, int width) {
         return dev_check(slot_span_ok(p - args.partials, s, S::BM * S::BN,
-                                      2 * static_cast<int64_t>(args.sk.G), width),
+                                      static_cast<int64_t>(args.sk.G), width),
                          args.err);
       };
 #endif
@@ -443,8 +442,8 @@ __global__ void __launch_bounds__(S::THREADS, 1)
           for (int p = 0; p < 8; p += 2) {
             const float2 lo = unpack2(acc2[i][p]), hi = unpack2(acc2[i][p + 1]);
 #ifdef GEMM14_DEVICE_CHECKS
-            if (!slot_ok(srow + LY::col(warp_n, tc, 2 * p), own, 1) ||
-                !slot_ok(srow + LY::col(warp_n, tc, 2 * p + 3), own, 1))
+            if (!slot_ok(srow + LY::col(warp_n, tc, 2 * p), w, 1) ||
+                !slot_ok(srow + LY::col(warp_n, tc, 2 * p + 3), w, 1))
               continue;
 #endif
             if (LY::BK) {
@@ -459,79 +458,81 @@ __global__ void __launch_bounds__(S::THREADS, 1)
           }
         }
       }
-      if (kind == kSegPartial) {
-        __syncthreads();
-        if (threadIdx.x == 0 && dev_check(index_ok(w, args.sk.G), args.err))
-          flag_publish(args.flags + w, args.epoch);
-        continue;
-      }
+      __syncthreads();
+      if (threadIdx.x == 0 && dev_check(index_ok(w, args.sk.G), args.err))
+        flag_publish(args.flags + w, args.epoch);
+      continue;
+    }
+    if (kSK && kind == kSegHead) {
       const int last = sm.sched.head_last;
       if (threadIdx.x == 0)
         for (int c = w + 1; c <= last; ++c) {
           if (!dev_check(index_ok(c, args.sk.G), args.err)) break;
-          if (!flag_wait(args.flags + c, args.epoch, wc)) break;  // raises abort on expiry
+          // (inline: the accumulators are live across the wait)
+          if (!flag_wait_inline(args.flags + c, args.epoch, wc)) break;  // raises abort on expiry
           flag_clear(args.flags + c);
         }
-      __syncthreads();  // also orders this CTA's own slot stores before the reads
+      __syncthreads();  // the flags were seen before any thread reads a slot
       if (sm.abort_flag) { ok = false; break; }
-      // float4 q of the tile (q = thread + 256 u): row q / 64, columns
-      // 4 (q % 64) .. +3 -- a warp covers 512 contiguous bytes of a row.
-      // Eight float4 per thread are in flight per slot to hide L2 latency.
-      constexpr int kPer = S::BM * S::BN / 4 / S::THREADS;  // 32
+      using LY = Lay<kLay>;
 #pragma unroll 1
-      for (int u0 = 0; u0 < kPer; u0 += 8) {
-        float4 v[8];
+      for (int c = w + 1; c <= last; ++c) {
+        const float* slot = args.partials + static_cast<size_t>(c) * (S::BM * S::BN);
+        // two rows of the thread's 8 x 16 block per round: their 8 (or 32)
+        // loads in flight together
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int i0 = 0; i0 < 8; i0 += 2) {
+          float v[2][16];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float* srow = slot + LY::row(warp_m, tr, i0 + h) * S::BN;
+            if (LY::BK) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
 #ifdef GEMM14_DEVICE_CHECKS
-          if (!slot_ok(slot + 4 * (threadIdx.x + (u0 + u) * S::THREADS), own, 4)) {
-            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            continue;
-          }
+                if (!dev_check(slot_span_ok(srow + LY::col(warp_n, tc, j) - args.partials, c,
+                                            S::BM * S::BN, args.sk.G, 1),
+                               args.err)) {
+                  v[h][j] = 0.f;
+                  continue;
+                }
 #endif
-          v[u] = __ldcg(reinterpret_cast<const float4*>(slot) + threadIdx.x + (u0 + u) * S::THREADS);
-        }
-#pragma unroll 1
-        for (int c = w + 1; c <= last; ++c) {
-          const float4* src = reinterpret_cast<const float4*>(
-              args.partials + static_cast<size_t>(c) * (S::BM * S::BN));
-          float4 p[8];
+                v[h][j] = __ldcg(srow + LY::col(warp_n, tc, j));
+              }
+            } else {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
+              for (int jj = 0; jj < 4; ++jj) {
+                const float* q = srow + LY::col(warp_n, tc, 4 * jj);
 #ifdef GEMM14_DEVICE_CHECKS
-            if (!slot_ok(reinterpret_cast<const float*>(src + threadIdx.x + (u0 + u) * S::THREADS),
-                         c, 4)) {
-              p[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-              continue;
+                if (!dev_check(slot_span_ok(q - args.partials, c, S::BM * S::BN, args.sk.G, 4),
+                               args.err)) {
+                  v[h][4 * jj] = v[h][4 * jj + 1] = v[h][4 * jj + 2] = v[h][4 * jj + 3] = 0.f;
+                  continue;
+                }
+#endif
+                const float4 t = __ldcg(reinterpret_cast<const float4*>(q));
+                v[h][4 * jj] = t.x;
+                v[h][4 * jj + 1] = t.y;
+                v[h][4 * jj + 2] = t.z;
+                v[h][4 * jj + 3] = t.w;
+              }
             }
-#endif
-            p[u] = __ldcg(src + threadIdx.x + (u0 + u) * S::THREADS);
           }
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            v[u].x += p[u].x; v[u].y += p[u].y; v[u].z += p[u].z; v[u].w += p[u].w;
-          }
-        }
+          for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int q = threadIdx.x + (u0 + u) * S::THREADS;
-          const int r = q / (S::BN / 4), c4 = (q % (S::BN / 4)) * 4;
-          const int row = tm * S::BM + r, col = tn * S::BN + c4;
-          if (row >= M) continue;
-          float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
-          if (args.vec_store && col + 3 < N) {
-            epi_store4<kGeneral>(args, crow + col, v[u]);
-          } else {
-            if (col < N) epi_store1<kGeneral>(args, crow + col, v[u].x);
-            if (col + 1 < N) epi_store1<kGeneral>(args, crow + col + 1, v[u].y);
-            if (col + 2 < N) epi_store1<kGeneral>(args, crow + col + 2, v[u].z);
-            if (col + 3 < N) epi_store1<kGeneral>(args, crow + col + 3, v[u].w);
-          }
+            for (int p = 0; p < 8; ++p) {
+              const float2 a = unpack2(acc2[i0 + h][p]);
+              acc2[i0 + h][p] = pack2(a.x + v[h][2 * p], a.y + v[h][2 * p + 1]);
+            }
+          // the next rounds' loads stay behind this one's adds (a compiler
+          // barrier: without it all 32 loads are hoisted, and their registers
+          // on top of the accumulators spill)
+          asm volatile("" ::: "memory");
         }
       }
-      continue;
+      // the HEAD's tile goes to C below, as a FULL tile's
     }
-
     // Epilogue: rows beyond M and columns beyond N are not written.
     {
       using LY = Lay<kLay>;

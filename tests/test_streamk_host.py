@@ -23,9 +23,9 @@ def test_schedule_covers_every_k_block_once(tmp_path):
 def test_workspace_bytes():
     g14.load()
     F32, BF16 = g14.GEMM14_DTYPE_F32, g14.GEMM14_DTYPE_BF16
-    # fp32: the flags (one word per SM, 256-byte aligned), then two 128 x 256
-    # slots per worker (PARTIAL and HEAD)
-    want = 768 + 2 * 152 * 128 * 256 * 4
+    # fp32: the flags (one word per SM, 256-byte aligned), then one 128 x 256
+    # slot per worker (for its PARTIAL; a HEAD adds into its accumulators)
+    want = 768 + 152 * 128 * 256 * 4
     assert g14.workspace_bytes(F32, 3072, 3072, 3072, 152) == want
     assert g14.workspace_bytes(F32, 4097, 3001, 513, 152) == want
     # skinny bf16: 128 tiles of 128 x 64 -- between half and one wave: not split
@@ -101,7 +101,7 @@ def test_workspace_bytes_ex_adds_room_to_repitch():
     # fp32 4097 x 3001 x 513 (pitches 2052 and 12004 bytes): both copied, A
     # transposed into K x M (N >= 2048) with a pitch of 4100 floats
     M, N, K = 4097, 3001, 513
-    sk = 768 + 2 * 152 * 128 * 256 * 4          # 396 tiles: split, two fp32 slots per SM
+    sk = 768 + 152 * 128 * 256 * 4              # 396 tiles: split, one fp32 slot per SM
     a_off = _r256(sk)
     b_off = _r256(a_off + K * 4100 * 4)
     assert ex(F32, 0, 0, M, N, K, P, K, P, N, P, N, 152) == b_off + K * 3004 * 4
