@@ -59,7 +59,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target oracle seconds per part for cpu_baseline")
     ap.add_argument("--only", choices=[p[0] for p in PARTS], default=None,
                     help="time one part only (for profiling; not a bench line)")
