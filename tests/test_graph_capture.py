@@ -2,7 +2,8 @@
 publication flags must not let a replay's tile owner take a partial sum that
 the replay has not yet written (the call's epoch is fixed at capture). Each
 replay runs on new inputs and is checked against the oracle; the capture holds
-split products of all three split kernels and a re-pitched one."""
+split products of all three split kernels, a re-pitched one, and a 3xTF32 one
+whose lo parts the replay writes afresh."""
 import numpy as np
 import pytest
 import torch
@@ -14,21 +15,24 @@ from gpu_util import oracle_check
 
 pytestmark = pytest.mark.gpu
 
-F32, BF16 = g14.GEMM14_DTYPE_F32, g14.GEMM14_DTYPE_BF16
+F32, BF16, X3 = g14.GEMM14_DTYPE_F32, g14.GEMM14_DTYPE_BF16, g14.GEMM14_DTYPE_F32_3XTF32
+CODE = {"f32": F32, "bf16": BF16, "x3": X3}
 
 # (dtype, M, N, K, ldb): fp32 few tiles (every SM shares them), the one-SM
 # tensor kernel with 4 workers a tile, the pair kernel between one and two
-# waves, and fp32 with an odd B pitch (re-pitched, then split)
+# waves, fp32 with an odd B pitch (re-pitched, then split), and 3xTF32 split
+# ahead (B transposed, lo parts) on the pair kernel over 12 clusters
 CASES = [("f32", 1000, 1000, 777, 1000), ("bf16", 300, 100, 5000, 104),
-         ("bf16", 2304, 2560, 8192, 2560), ("f32", 129, 257, 4000, 257)]
+         ("bf16", 2304, 2560, 8192, 2560), ("f32", 129, 257, 4000, 257),
+         ("x3", 512, 384, 1001, 384)]
 
 
 def test_split_products_replayed_from_a_graph(oracle_mod):
     s = torch.cuda.Stream()
     bufs = []
     for i, (dt, M, N, K, ldb) in enumerate(CASES):
-        code = F32 if dt == "f32" else BF16
-        td = torch.float32 if dt == "f32" else torch.bfloat16
+        code = CODE[dt]
+        td = torch.bfloat16 if dt == "bf16" else torch.float32
         a = torch.zeros(M, K, dtype=td, device="cuda")
         b = torch.zeros(K, ldb, dtype=td, device="cuda")
         c = torch.zeros(M, N, device="cuda")
@@ -53,7 +57,8 @@ def test_split_products_replayed_from_a_graph(oracle_mod):
     for rep in range(4):
         host = []
         for i, (code, dt, M, N, K, ldb, a, b, c, ws, need) in enumerate(bufs):
-            A, B = inputs.make(M, N, K, dt, "normal", 1.0 / K ** 0.5, seed=100 * rep + i)
+            A, B = inputs.make(M, N, K, "bf16" if dt == "bf16" else "f32", "normal",
+                               1.0 / K ** 0.5, seed=100 * rep + i)
             a.copy_(A.cuda())
             b[:, :N].copy_(B.cuda())
             c.fill_(float("nan"))
