@@ -517,6 +517,14 @@ size_t product_workspace_bytes(int dtype, int transa, int transb, int64_t M, int
                                const void* C, int64_t ldc) {
   const DeviceInfo* dev = nullptr;
   if (current_device(&dev) != GEMM14_OK) return 0;
+  // TF32 and 3xTF32 also get room for their K-major copies and lo parts (the
+  // pair kernel runs them several times faster than the converter kernel);
+  // the other products take the stream-K region only
+  if (is_tf32_mode(dtype)) {
+    Repitch rp;
+    plan_repitch(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &rp);
+    if (rp.a || rp.b || rp.split) return rp.total;
+  }
   gemm14_plan plan;
   plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
   return workspace_need(plan, dev->sm_count, K);

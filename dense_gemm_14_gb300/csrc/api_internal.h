@@ -20,7 +20,8 @@ int validate_product(int dtype, int transa, int transb, int64_t M, int64_t N, in
                      int64_t ldc);
 
 // Workspace bytes with which such a call on these device operands would use
-// the stream-K schedule on the current device (0: it would not split).
+// the stream-K schedule on the current device (0: it would not split); for
+// TF32 and 3xTF32 also the room for their K-major copies and lo parts.
 size_t product_workspace_bytes(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
                                const void* A, int64_t lda, const void* B, int64_t ldb,
                                const void* C, int64_t ldc);

@@ -60,11 +60,29 @@ def test_host_alpha_beta_and_transposed_views(oracle_mod):
     oracle_check(oracle_mod, A, B, got)
 
 
-def test_host_tf32_mode(oracle_mod):
+@pytest.mark.parametrize("mode", ["3xtf32", "tf32"])
+@pytest.mark.parametrize("panels", [1, 2, 3])
+def test_host_tf32_mode(oracle_mod, mode, panels):
+    """The host-buffer path gives the TF32 modes the room for their K-major
+    copies and lo parts, so each panel runs on the pair kernel: 3xTF32 within
+    the fp32 bound, TF32 within 4e-3 of the fp32 inputs' product."""
     M, N, K = 1200, 512, 320
     A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=46)
-    got = g14.gemm(A, B, fp32_mode="3xtf32", panels=2)
-    oracle_check(oracle_mod, A, B, got)
+    got = g14.gemm(A, B, fp32_mode=mode, panels=panels)
+    if mode == "3xtf32":
+        oracle_check(oracle_mod, A, B, got)
+    else:
+        ref, refabs = oracle_mod.gemm(A.numpy(), B.numpy())
+        ok, worst = oracle_mod.within_bound(got.numpy(), ref, refabs, 4e-3)
+        assert ok, worst
+    # a stored transpose of B (N x K), read through a strided view
+    Bt = B.t().contiguous().t()
+    got_t = g14.gemm(A, Bt, fp32_mode=mode, panels=panels)
+    if mode == "3xtf32":
+        oracle_check(oracle_mod, A, B, got_t)
+    else:
+        ok, worst = oracle_mod.within_bound(got_t.numpy(), ref, refabs, 4e-3)
+        assert ok, worst
 
 
 def test_host_degenerate_sizes():
