@@ -240,3 +240,38 @@ def test_pair_kernel_matches_single_sm_kernel(oracle_mod, dt, M, N, K):
         g14.set_pair_kernel(prev)
     oracle_check(oracle_mod, A, B, C_pair)
     assert torch.equal(C_pair, C_one)
+
+
+@pytest.mark.parametrize("pair,M,N,K", [(True, 2304, 2557, 8192), (False, 512, 125, 8192)])
+def test_split_products_keep_padding(oracle_mod, pair, M, N, K):
+    """Stream-K variants of both 16-bit kernels (the tile owners store through
+    the TMA-store epilogue) with N not a multiple of 4 and a padded pitch:
+    the columns past N and the memory past the last row keep their NaN; C is
+    within the bound on sampled rows."""
+    A, B = inputs.make(M, N, K, "bf16", "normal", 1.0 / K ** 0.5, seed=M + N + K)
+    lda, ldb, ldc = rup(K, 8), rup(N, 8), rup(N, 4) + 8
+    prev = g14.set_pair_kernel(pair)
+    try:
+        st, plan = g14.plan(g14.GEMM14_DTYPE_BF16, M, N, K, 1 << 16, lda, 1 << 16, ldb,
+                            1 << 16, ldc, 152)
+        assert st == 0 and plan.kernel == (3 if pair else 2) and plan.vec_store == 1
+        need = g14.workspace_bytes(g14.GEMM14_DTYPE_BF16, M, N, K, 0)
+        assert need > 0  # split
+        _abuf, a = to_device_padded(A, lda)
+        _bbuf, b = to_device_padded(B, ldb)
+        cbuf = torch.full((M * ldc + 4096,), float("nan"), device="cuda")
+        ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+        s = torch.cuda.current_stream().cuda_stream
+        g14.gemm_bf16_f32acc_ws(M, N, K, a.data_ptr(), lda, b.data_ptr(), ldb, cbuf.data_ptr(),
+                                ldc, ws.data_ptr(), need, s)
+        assert g14.check_device_error(s) == 0
+        torch.cuda.synchronize()
+    finally:
+        g14.set_pair_kernel(prev)
+    full = cbuf.cpu()
+    rows = full[:M * ldc].view(M, ldc)
+    assert torch.isnan(rows[:, N:]).all()
+    assert torch.isnan(full[M * ldc:]).all()
+    assert not torch.isnan(rows[:, :N]).any()
+    sample = np.unique(np.concatenate([[0, M - 1], np.arange(1, M, 97)]))
+    oracle_check(oracle_mod, A, B, rows[:, :N].contiguous(), rows=sample)
