@@ -13,7 +13,9 @@ GPU and the result is copied back (the end-to-end path).
 from __future__ import annotations
 
 from ._lib import (GEMM14_DTYPE_BF16, GEMM14_DTYPE_F16, GEMM14_DTYPE_F32,
-                   GEMM14_DTYPE_F32_3XTF32, GEMM14_DTYPE_TF32, Gemm14Error, Plan,
+                   GEMM14_DTYPE_F32_3XTF32, GEMM14_DTYPE_TF32, GEMM14_ERR_CUDA,
+                   GEMM14_ERR_DEVICE_CHECK, GEMM14_ERR_INVALID_ARG, GEMM14_ERR_TIMEOUT,
+                   GEMM14_ERR_UNSUPPORTED_DEVICE, GEMM14_OK, Gemm14Error, Plan,
                    check_device_error, debug_inject, gemm_bf16_f32acc, gemm_bf16_f32acc_ws,
                    gemm_bf16_f32acc_noalloc, gemm_ex, gemm_host, host_synchronize, host_wait, workspace_bytes_ex, gemm_f16_f32acc, gemm_f16_f32acc_ws, gemm_f32,
                    gemm_f32_3xtf32, gemm_f32_ws, gemm_tf32_f32acc, last_error_string, lib_path, load, plan, plan_ex, set_pair_kernel, status_string, version, workspace_bytes)
@@ -28,4 +30,6 @@ __all__ = [
     "check_device_error", "debug_inject", "set_pair_kernel", "status_string", "version", "load", "lib_path", "Gemm14Error",
     "GEMM14_DTYPE_F32", "GEMM14_DTYPE_BF16", "GEMM14_DTYPE_F16", "GEMM14_DTYPE_TF32",
     "GEMM14_DTYPE_F32_3XTF32",
+    "GEMM14_OK", "GEMM14_ERR_INVALID_ARG", "GEMM14_ERR_UNSUPPORTED_DEVICE", "GEMM14_ERR_CUDA",
+    "GEMM14_ERR_TIMEOUT", "GEMM14_ERR_DEVICE_CHECK",
 ]

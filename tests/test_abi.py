@@ -290,3 +290,17 @@ def test_host_entry_points_validate_before_any_cuda_call():
     assert g14.host_wait(1 << 60, check=False) == _lib.GEMM14_ERR_INVALID_ARG
     # nothing in flight
     assert g14.host_synchronize(check=False) == 0
+
+
+def test_status_constants_match_the_header():
+    """The binding's status constants are the header's enum values."""
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "include", "gemm14.h")).read()
+    enum = dict((m.group(1), int(m.group(2)))
+                for m in re.finditer(r"\b(GEMM14_(?:OK|ERR_[A-Z_]+))\s*=\s*(\d+)", hdr))
+    assert set(enum) == {"GEMM14_OK", "GEMM14_ERR_INVALID_ARG", "GEMM14_ERR_UNSUPPORTED_DEVICE",
+                         "GEMM14_ERR_CUDA", "GEMM14_ERR_TIMEOUT", "GEMM14_ERR_DEVICE_CHECK"}
+    for name, value in enum.items():
+        assert getattr(g14, name) == value, name
