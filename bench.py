@@ -59,6 +59,12 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustained-s", type=float, default=1.5,
+                    help="seconds of the sustained leg (back-to-back steps with their own "
+                         "clock record; 0: skip)")
+    ap.add_argument("--cpu-1t-seconds", type=float, default=3.0,
+                    help="target single-thread oracle seconds per fp32 config (1-3) "
+                         "in cpu_baseline (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target oracle seconds per part for cpu_baseline")
     ap.add_argument("--only", choices=[p[0] for p in PARTS], default=None,
@@ -119,24 +125,88 @@ class Dist:
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi sampled every 100 ms in a child process during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, power and clock-event reasons of one GPU, sampled in a thread
+    every `period_s` while a timed region runs (start() just before its first
+    launch, stop() just after its last event), read through NVML (the driver's
+    libnvidia-ml, read-only queries). Where NVML cannot be loaded, nvidia-smi
+    is sampled at its fastest period instead."""
 
-    def __init__(self, device_index: int):
+    # clock-event reason bits of NVML's public header
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
         self.dev = device_index
-        self.proc = None
-        self.out = None
+        self.period = period_s
+        self.samples = []  # (sm_mhz, power_w, reason bits)
+        self.sm_max = None
+        self.source = None
+        self._nvml = None
+        self._handle = None
+        self._thread = None
+        self._stop = None
+        self._proc = None
+        self._open_nvml()
+
+    def _open_nvml(self):
+        import ctypes
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            uuid = None
+            try:
+                import torch
+                uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            except Exception:
+                uuid = None
+            ok = False
+            if uuid:
+                ok = nv.nvmlDeviceGetHandleByUUID(f"GPU-{uuid}".encode(), ctypes.byref(h)) == 0
+            if not ok and nv.nvmlDeviceGetHandleByIndex_v2(self.dev, ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint(0)
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1: SM clock
+                self.sm_max = float(mx.value)
+            # the reasons query under its current name, else its older one
+            self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self._nvml, self._handle = nv, h
+            self.source = "nvml"
+        except (OSError, AttributeError):
+            self._nvml = None
+
+    def _sample_nvml(self):
+        import ctypes
+        nv, h = self._nvml, self._handle
+        mhz, mw, why = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
+                nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+                self._reasons_fn(h, ctypes.byref(why))
+                self.samples.append((float(mhz.value), mw.value / 1e3, int(why.value)))
+            self._stop.wait(self.period)
 
     def start(self):
+        import threading
+        self.samples = []
+        if self._nvml is not None:
+            self._stop = threading.Event()
+            self._thread = threading.Thread(target=self._sample_nvml, daemon=True)
+            self._thread.start()
+            return
         try:
-            self.out = open(self._path(), "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(self.dev)], stdout=self.out, stderr=subprocess.DEVNULL)
+            self._out = open(self._path(), "w")
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "10", "-i", str(self.dev)], stdout=self._out, stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi"
         except (OSError, FileNotFoundError):
-            self.proc = None
+            self._proc = None
 
     def _path(self):
         d = os.path.join(ROOT, "gpurun_out")
@@ -144,34 +214,46 @@ class ClockSampler:
         return os.path.join(d, f"clocks_rank{self.dev}.csv")
 
     def stop(self) -> dict:
-        if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.out.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self._path()) as f:
-            for line in f:
-                cols = [c.strip() for c in line.split(",")]
-                if len(cols) < 9:
-                    continue
-                try:
-                    sm.append(float(cols[1]))
-                    smax.append(float(cols[2]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, cols[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            self._thread = None
+        elif self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+            self._out.close()
+            self._proc = None
+            names = {5: 0x8, 6: 0x40, 7: 0x20, 8: 0x4}
+            with open(self._path()) as f:
+                for line in f:
+                    cols = [c.strip() for c in line.split(",")]
+                    if len(cols) < 9:
+                        continue
+                    try:
+                        sm, smax = float(cols[1]), float(cols[2])
+                        pw = float(cols[3]) if cols[3].replace(".", "", 1).isdigit() else 0.0
+                    except ValueError:
+                        continue
+                    bits = sum(b for i, b in names.items() if cols[i].lower().startswith("active"))
+                    self.samples.append((sm, pw, bits))
+                    self.sm_max = max(self.sm_max or 0.0, smax)
+        return self.summary()
+
+    def summary(self) -> dict:
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.sm_max, "reasons": ["no samples"],
+                    "samples": 0, "source": self.source}
+        sm = [x[0] for x in self.samples]
+        counts = {name: sum(1 for x in self.samples if x[2] & bit)
+                  for bit, name in self.REASONS.items()}
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": self.sm_max,
+                "reasons": sorted(n for n, c in counts.items() if c),
+                "reason_samples": {n: c for n, c in counts.items() if c},
+                "power_w_max": max(x[1] for x in self.samples),
+                "samples": len(sm), "period_ms": self.period * 1e3, "source": self.source}
 
 
 # ------------------------------------------------------------------ helpers
@@ -208,10 +290,12 @@ def workload_info(name):
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def time_oracle_sample(name: str, target_s: float, A=None, B=None, want_rows=False):
+def time_oracle_sample(name: str, target_s: float, A=None, B=None, want_rows=False,
+                       threads: int = 0):
     """Times the oracle on the first R rows of the named product, R sized so
-    the call takes about target_s seconds. Returns (flops, seconds, rows,
-    threads), and with want_rows also the oracle's R x N rows (float64)."""
+    the call takes about target_s seconds, on `threads` threads (0: all the
+    host's). Returns (flops, seconds, rows, threads), and with want_rows also
+    the oracle's R x N rows (float64)."""
     import oracle
     from dense_gemm_14_gb300 import inputs, roofline
     w = inputs.WORKLOADS[name]
@@ -224,13 +308,13 @@ def time_oracle_sample(name: str, target_s: float, A=None, B=None, want_rows=Fal
     rows = min(M, 32)
     for probe_s in (0.5, target_s):
         t0 = time.perf_counter()
-        oracle.gemm(Ah[:rows], Bh, w.dtype, with_abs=False)
+        oracle.gemm(Ah[:rows], Bh, w.dtype, threads=threads, with_abs=False)
         probe = time.perf_counter() - t0
         rows = int(max(1, min(M, rows * min(probe_s, target_s) / max(probe, 1e-6))))
     t0 = time.perf_counter()
-    ref, _ = oracle.gemm(Ah[:rows], Bh, w.dtype, with_abs=False)
+    ref, _ = oracle.gemm(Ah[:rows], Bh, w.dtype, threads=threads, with_abs=False)
     dt = time.perf_counter() - t0
-    out = (roofline.flops(rows, N, K), dt, rows, oracle.max_threads())
+    out = (roofline.flops(rows, N, K), dt, rows, threads or oracle.max_threads())
     return out + (ref,) if want_rows else out
 
 
@@ -369,18 +453,24 @@ def run_ours(args, dist: Dist):
     clocks = ClockSampler(dev.index)
     dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.2)
     # The value: K steps back to back between one pair of events, nothing in
     # between the kernels, so that each launch overlaps the end of the one
-    # before it (the kernels wait for their predecessor on the device).
+    # before it (the kernels wait for their predecessor on the device). The
+    # clocks are sampled from just before the first launch to just after the
+    # last event (every 2 ms).
+    clocks.start()
     start.record(stream)
     for step in range(K):
         for p in parts:
             launch(p, step)
     end.record(stream)
+    end.synchronize()
+    clk = clocks.stop()
     # Each kernel's own duration (the roofline): the same K steps again with an
-    # event pair around every kernel (which keeps consecutive kernels apart).
+    # event pair around every kernel (which keeps consecutive kernels apart),
+    # with a clock record of its own.
+    clocks_parts = ClockSampler(dev.index)
+    clocks_parts.start()
     for step in range(K):
         for p in parts:
             s_ev, e_ev = ev[p["name"]]
@@ -388,8 +478,8 @@ def run_ours(args, dist: Dist):
             launch(p, step)
             e_ev[step].record(stream)
     torch.cuda.synchronize()
+    clk_parts = clocks_parts.stop()
     dist.barrier()
-    clk = clocks.stop()
     st = g14.check_device_error(stream.cuda_stream)
     if st:
         raise RuntimeError(f"device error in the timed region: {g14.status_string(st)}")
@@ -398,12 +488,39 @@ def run_ours(args, dist: Dist):
     flops_step = sum(p["flops"] for p in parts)
     value = flops_step * K * dist.world / elapsed_max / 1e12
 
+    # A sustained leg: the same step back to back for about args.sustained_s
+    # seconds (the clock settles under the power cap), one event pair, its own
+    # clock record. Reported beside the value, not in it.
+    sustained = None
+    if args.sustained_s > 0:
+        n_sus = max(1, int(args.sustained_s / max(elapsed_s / K, 1e-6)))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clocks_sus = ClockSampler(dev.index, period_s=0.005)
+        torch.cuda.synchronize()
+        clocks_sus.start()
+        s0.record(stream)
+        for step in range(n_sus):
+            for p in parts:
+                launch(p, step)
+        s1.record(stream)
+        s1.synchronize()
+        clk_sus = clocks_sus.stop()
+        st = g14.check_device_error(stream.cuda_stream)
+        if st:
+            raise RuntimeError(f"device error in the sustained leg: {g14.status_string(st)}")
+        sus_s = dist.max(s0.elapsed_time(s1) / 1e3)
+        sustained = {"steps": n_sus, "seconds": sus_s, "ms_per_step": sus_s / n_sus * 1e3,
+                     "value": flops_step * n_sus * dist.world / sus_s / 1e12, "unit": UNIT,
+                     "clocks": clk_sus}
+
     part_out = []
     for p in parts:
         s_ev, e_ev = ev[p["name"]]
         ms = [s_ev[i].elapsed_time(e_ev[i]) for i in range(K)]
         avg_s = statistics.mean(ms) / 1e3
         tflops = p["flops"] / avg_s / 1e12
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = clk_parts.get("sm_mhz")
         if p["bound"] == "tensor":
             # a short back-to-back region runs at burst clocks; seconds of
             # load settle at the power-capped sustained rate
@@ -413,16 +530,26 @@ def run_ours(args, dist: Dist):
             else:
                 peak = peaks["bf16_tflops"]
                 peak_note = f"bf16 dense, burst ({peaks['source']}; timed region < 1 s)"
+            # dense bf16: 8192 FLOP (4096 multiply-adds) per SM per clock, at
+            # the clock sampled while the parts ran
+            per_clock = 8192
         else:
             peak = roofline.fp32_alu_peak_tflops()
             peak_note = "FFMA: 152 SMs x 128 lanes x 2 FLOP x 2070 MHz (unit counts)"
+            per_clock = 256
+        at_clock = None
+        if mhz:
+            pk = sms * per_clock * mhz * 1e6 / 1e12
+            at_clock = {"sm_mhz_median": mhz, "peak_tflops": pk, "frac": tflops / pk,
+                        "note": f"{sms} SMs x {per_clock} FLOP/clock x the median SM clock "
+                                "sampled while the parts were timed"}
         part_out.append({
             "workload": p["name"], "kernel": p["kernel"], "entry": p["entry"],
             "launches_per_call": p["launches"],
             "schedule": "stream-K" if p["ws_bytes"] else "data-parallel",
             "workspace_bytes": p["ws_bytes"], "M": p["w"].M, "N": p["w"].N,
-            "K": p["w"].K, "ms_mean": statistics.mean(ms), "ms_min": min(ms),
-            "tflops": tflops,
+            "K": p["w"].K, "ms_mean": statistics.mean(ms), "ms_median": statistics.median(ms),
+            "ms_min": min(ms), "tflops": tflops, "at_sampled_clock": at_clock,
             "roofline": {"bound": p["bound"], "achieved": tflops, "peak": peak, "unit": UNIT,
                          "frac": tflops / peak, "peak_kind": peak_note,
                          "traffic": traffic_for(p["kernel"], p["src"], p["name"]),
@@ -491,6 +618,16 @@ def run_ours(args, dist: Dist):
             accuracy.append(accuracy_of(p["name"], *host[p["name"]], p["sets"][0][2], ref_rows))
         cpu = {"value": tf / tt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": "; ".join(desc) + " (fp64 oracle, product only)", "seconds": tt}
+        # the oracle on one thread, on the three fp32 configs (a bounded
+        # sample of rows each, the whole product when it fits the time)
+        if args.cpu_1t_seconds > 0:
+            one = []
+            for name in ("f32_256", "f32_3072", "f32_ragged"):
+                f1, t1, r1, _ = time_oracle_sample(name, args.cpu_1t_seconds, threads=1)
+                w1 = inputs.WORKLOADS[name]
+                one.append({"workload": name, "rows": r1, "of_rows": w1.M, "seconds": t1,
+                            "gflops": f1 / t1 / 1e9})
+            cpu["one_thread"] = one
 
     if dist.rank == 0:
         line = {
@@ -510,6 +647,8 @@ def run_ours(args, dist: Dist):
                        "parts": "the same K steps again, an event pair around each kernel",
                        "launches_timed_in_total": 2 * sum(p["launches"] for p in parts) * K},
             "clocks": clk,
+            "clocks_parts": clk_parts,
+            "sustained": sustained,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "accuracy": accuracy,
@@ -601,7 +740,7 @@ def time_one(args, name, w, fl, ib, sets, nsets, stream, peaks, roofline, g14, s
         peak, kind = peaks["bf16_tflops"], "tensor"  # each workload is timed alone: burst
     gbs = ib / (mean / 1e3) / 1e9
     print(json.dumps({"workload": name, "schedule": schedule, "M": w.M, "N": w.N, "K": w.K,
-                      "dtype": w.dtype, "ms_mean": mean, "ms_min": min(ms), "tflops": tf,
+                      "dtype": w.dtype, "ms_mean": mean, "ms_median": statistics.median(ms), "ms_min": min(ms), "tflops": tf,
                       "bound": kind, "peak_tflops": peak, "frac_compute": tf / peak,
                       "algorithmic_bytes": ib, "gbs": gbs,
                       "frac_hbm": gbs / peaks["hbm_gbs"],
@@ -678,7 +817,7 @@ def run_table_ex(args):
             nbytes = ib + (w.M * w.N * 4 if beta != 0.0 else 0)
             gbs = nbytes / (mean / 1e3) / 1e9
             print(json.dumps({"workload": name, "transa": ta, "transb": tb, "alpha": alpha,
-                              "beta": beta, "ms_mean": mean, "ms_min": min(ms), "tflops": tf,
+                              "beta": beta, "ms_mean": mean, "ms_median": statistics.median(ms), "ms_min": min(ms), "tflops": tf,
                               "bound": kind, "peak_tflops": peak, "frac_compute": tf / peak,
                               "algorithmic_bytes": nbytes, "gbs": gbs,
                               "frac_hbm": gbs / peaks["hbm_gbs"]}), flush=True)
@@ -755,7 +894,7 @@ def run_table_tf32(args):
                 # tf32 / bf16 ratio (1.1 / 2.25 PFLOP/s)
                 peak, kind = peaks["bf16_tflops"] * 1.1 / 2.25, "tensor (tf32)"
             print(json.dumps({"workload": name, "mode": mode, "M": M, "N": N, "K": K,
-                              "ms_mean": mean, "ms_min": min(ms), "tflops": tf,
+                              "ms_mean": mean, "ms_median": statistics.median(ms), "ms_min": min(ms), "tflops": tf,
                               "mma_tflops": mma_flops / (mean / 1e3) / 1e12, "bound": kind,
                               "peak_tflops": peak,
                               "frac_compute": mma_flops / (mean / 1e3) / 1e12 / peak,

@@ -767,10 +767,11 @@ int gemm14_version(void) { return 200; }
 namespace gemm14 {
 namespace {
 
-// Capacity of the built-in scratch: enough for every product the one-SM
-// tensor-core kernel splits with tiles up to 128 columns wide on this GPU
-// (flags + one 128 x 128 fp32 slot per SM: about 10 MB on 152 SMs).
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+// Capacity of the built-in scratch: the largest split either 16-bit kernel
+// makes (flags + one 128 x 256 fp32 slot per SM: 19.9 MB on 152 SMs) fits on
+// any GPU with up to 159 SMs. Operand copies (re-pitching) also land here
+// when they fit beside the split's region.
+constexpr size_t kNoAllocScratchBytes = size_t(20) << 20;  // 20 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -824,13 +825,12 @@ extern "C" int gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K, const v
   if ((st = current_device(&dev)) != GEMM14_OK) return st;
   gemm14_plan plan;
   plan_for(GEMM14_DTYPE_BF16, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
-  // The CTA-pair kernel's split (about 20 MB on 152 SMs) is not offered here:
-  // wide products run unsplit, as gemm_bf16_f32acc runs them.
-  const size_t need = plan.kernel == 3 ? 0 : workspace_need(plan, dev->sm_count, K);
+  const size_t need = workspace_need(plan, dev->sm_count, K);
   if (need > kNoAllocScratchBytes) {
     std::snprintf(t_last_error, sizeof t_last_error,
-                  "gemm_bf16_f32acc_noalloc: this product needs %zu bytes of scratch, more than "
-                  "the %zu bytes built into the library; use gemm_bf16_f32acc_ws",
+                  "gemm_bf16_f32acc_noalloc: this product's split needs %zu bytes of scratch, "
+                  "more than the %zu bytes built into the library; gemm_bf16_f32acc computes it "
+                  "unsplit without scratch, gemm_bf16_f32acc_ws with a caller workspace",
                   need, kNoAllocScratchBytes);
     return GEMM14_ERR_INVALID_ARG;
   }

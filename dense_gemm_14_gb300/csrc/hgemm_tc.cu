@@ -549,16 +549,10 @@ template <int BN, bool kTma, bool kSK, bool kGeneral>
 cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
                            const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc,
                            int grid, cudaStream_t stream) {
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static DeviceOnce configured;
+  const cudaError_t e = set_smem_once(configured, hgemm_tc_kernel<BN, kTma, kSK, kGeneral>,
+                                      H::smem_bytes(BN));
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(hgemm_tc_kernel<BN, kTma, kSK, kGeneral>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, H::smem_bytes(BN));
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
   CUtensorMap dummy{};
   return launch_kernel(hgemm_tc_kernel<BN, kTma, kSK, kGeneral>, dim3(grid), dim3(tc_threads<kTma>()),
                        H::smem_bytes(BN), stream, map_a ? *map_a : dummy,

@@ -467,24 +467,27 @@ cudaError_t set_pair_smem_all() {
 }  // namespace
 
 int pair_max_clusters() {
-  static int cached[64];
-  static bool have[64];
+  static DeviceOnce cached;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (have[dev]) return cached[dev];
-  if (set_pair_smem_all<false>() != cudaSuccess || set_pair_smem_all<true>() != cudaSuccess)
-    return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(P::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = P::SMEM_BYTES;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2_kernel<false, false, false>, &cfg) !=
-      cudaSuccess)
-    n = 0;
-  cached[dev] = n;
-  have[dev] = true;
-  return n;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= DeviceOnce::kDevices) return 0;
+  // -1: the kernels' attributes could not be set (not kept: tried again)
+  const int n = cached.get(
+      dev,
+      [] {
+        if (set_pair_smem_all<false>() != cudaSuccess || set_pair_smem_all<true>() != cudaSuccess)
+          return -1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(P::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = P::SMEM_BYTES;
+        int k = 0;
+        if (cudaOccupancyMaxActiveClusters(&k, hgemm_tc2_kernel<false, false, false>, &cfg) !=
+            cudaSuccess)
+          k = 0;
+        return k;
+      },
+      [](int v) { return v >= 0; });
+  return n > 0 ? n : 0;
 }
 
 cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,

@@ -6,6 +6,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <climits>
+#include <mutex>
 #include <utility>
 
 #include "checks.h"
@@ -32,6 +35,53 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// A value worked out once per device (a kernel's shared-memory attribute set,
+// an occupancy query) and reused by later calls on that device. First calls
+// from several host threads at once are serialised by the lock: one runs
+// set_up(), the others then read its result. A result for which keep(v) is
+// false (a failed set-up) is returned but not stored, so the next call on the
+// device tries again.
+class DeviceOnce {
+ public:
+  static constexpr int kDevices = 64;
+  DeviceOnce() {
+    for (auto& v : value_) v.store(kUnset, std::memory_order_relaxed);
+  }
+  template <typename SetUp, typename Keep>
+  int get(int dev, SetUp&& set_up, Keep&& keep) {
+    if (dev < 0 || dev >= kDevices) return set_up();
+    int v = value_[dev].load(std::memory_order_acquire);
+    if (v != kUnset) return v;
+    std::lock_guard<std::mutex> lock(mutex_);
+    v = value_[dev].load(std::memory_order_relaxed);
+    if (v != kUnset) return v;
+    v = set_up();
+    if (keep(v)) value_[dev].store(v, std::memory_order_release);
+    return v;
+  }
+
+ private:
+  static constexpr int kUnset = INT_MIN;
+  std::atomic<int> value_[kDevices];
+  std::mutex mutex_;
+};
+
+// Sets `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device (see DeviceOnce; `once` is the kernel's own).
+template <typename Kernel>
+cudaError_t set_smem_once(DeviceOnce& once, Kernel kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return static_cast<cudaError_t>(once.get(
+      dev,
+      [&] {
+        return static_cast<int>(
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+      },
+      [](int r) { return r == static_cast<int>(cudaSuccess); }));
 }
 
 // How the epilogue writes an output element from its sum s:

@@ -592,16 +592,10 @@ __global__ void __launch_bounds__(S::THREADS, 1)
 template <bool kTma, bool kSK, bool kGeneral, int kLay>
 cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
                            const GemmArgs& args, int grid, cudaStream_t stream) {
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static DeviceOnce configured;
+  const cudaError_t e = set_smem_once(configured, sgemm_simt_kernel<kTma, kSK, kGeneral, kLay>,
+                                      S::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(sgemm_simt_kernel<kTma, kSK, kGeneral, kLay>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
   CUtensorMap dummy{};
   return launch_kernel(sgemm_simt_kernel<kTma, kSK, kGeneral, kLay>, dim3(grid), dim3(S::THREADS),
                        S::SMEM_BYTES, stream, map_a ? *map_a : dummy, map_b ? *map_b : dummy,

@@ -187,13 +187,18 @@ int gemm_f16_f32acc_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t l
  * the implicit device synchronisation of cudaMalloc / cudaFree. The caller
  * passes A, B and C exactly as for gemm_bf16_f32acc; the stream-K scratch
  * that gemm_bf16_f32acc_ws would take from the caller comes instead from a
- * 16 MiB array built into the library, which every GPU that loads the library
- * holds until the process exits. It calls no cudaMalloc, cudaFree or other
- * allocating routine.
- * Limit: products whose split needs more than the 16 MiB (on this GPU, those
- * the one-SM kernel computes in 256-column tiles, e.g. M <= 128 with wide N)
- * return GEMM14_ERR_INVALID_ARG and gemm14_last_error_string() says how many
- * bytes were needed; products that need no scratch run as gemm_bf16_f32acc.
+ * 20 MiB array built into the library, which every GPU that loads the library
+ * holds until the process exits. Operands that TMA cannot read are re-pitched
+ * into the same array when they fit beside the split's region, as the
+ * workspace entry points do with theirs. It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ * Limit: a product whose split needs more than the 20 MiB returns
+ * GEMM14_ERR_INVALID_ARG, and gemm14_last_error_string() says how many bytes
+ * were needed (gemm_bf16_f32acc then computes it unsplit, with no scratch).
+ * The largest split is one 128 x 256 fp32 slot per SM plus a flag word each,
+ * so this happens only on GPUs with more than 159 SMs; on 152 SMs every
+ * product runs, split exactly as gemm_bf16_f32acc_ws would split it.
+ * Products that need no scratch run as gemm_bf16_f32acc.
  * Set-up: the first call on each device looks up the array's device address
  * and clears its flag words on the caller's stream; make that first call
  * before any stream capture. Every call shares the one array, which keeps the

@@ -71,8 +71,6 @@ def _load():
                                            ctypes.c_double, vp, i64, vp, i64, ctypes.c_double,
                                            vp, i64, dp, dp, i64, ctypes.c_int]
             lib.oracle_gemm_ex.restype = ctypes.c_int
-            lib.oracle_round_tf32.argtypes = [vp, i64]
-            lib.oracle_round_tf32.restype = ctypes.c_int
             lib.oracle_truncate_tf32.argtypes = [vp, i64]
             lib.oracle_truncate_tf32.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
@@ -183,16 +181,6 @@ def gemm_entries(A: np.ndarray, B: np.ndarray, rows, cols, dtype: str = "f32",
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_entries failed with code {rc}")
     return out, outabs
-
-
-def round_tf32(X: np.ndarray) -> np.ndarray:
-    """A float32 copy of X with every value rounded to the nearest tf32 value
-    (10 fraction bits, ties away from zero; inf and NaN unchanged)."""
-    out = np.array(X, dtype=np.float32, copy=True, order="C")
-    rc = _load().oracle_round_tf32(_ptr(out) if out.size else 0, out.size)
-    if rc != 0:
-        raise RuntimeError(f"oracle_round_tf32 failed with code {rc}")
-    return out
 
 
 def truncate_tf32(X: np.ndarray) -> np.ndarray:

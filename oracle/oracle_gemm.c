@@ -228,29 +228,6 @@ int oracle_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, int transa, int t
 }
 
 /*
- * TF32, the pages' tensor-core format for fp32 data (gpu-hpc-book ch.06
- * "Tensor Cores": fp32's sign and 8 exponent bits with 10 fraction bits): each
- * fp32 value x of the n-element array is replaced by the nearest value with 10
- * fraction bits, ties away from zero (the rounding of the kernels' conversion).
- * On the binary32 pattern that is: add half a unit of the 13 dropped bits to
- * the magnitude bits, then clear them; a carry moves into the exponent, and
- * one out of the largest binade gives infinity. Infinities and NaN stay as
- * they are.
- */
-int oracle_round_tf32(float *x, int64_t n) {
-  if (n < 0 || (n > 0 && !x)) return -1;
-  for (int64_t i = 0; i < n; ++i) {
-    uint32_t w;
-    memcpy(&w, &x[i], sizeof w);
-    const uint32_t sign = w & 0x80000000u, mag = w & 0x7fffffffu;
-    if (mag >= 0x7f800000u) continue; /* inf or NaN */
-    const uint32_t r = ((mag + 0x1000u) & ~0x1fffu) | sign;
-    memcpy(&x[i], &r, sizeof r);
-  }
-  return 0;
-}
-
-/*
  * The tf32 value the tensor cores take from an fp32 input: the binary32
  * pattern with its 13 low fraction bits cleared (truncation toward zero to 10
  * fraction bits, every exponent kept). The pages fix the format, not the

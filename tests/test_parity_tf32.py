@@ -4,12 +4,20 @@ pairs) against the oracle:
 - gemm_f32_3xtf32 (split hi/lo tf32 arithmetic): within the fp32 bound
   1e-5 (|A||B|) of the exact product of the fp32 inputs;
 - gemm_tf32_f32acc (inputs read as tf32 by the tensor cores, i.e. with their
-  13 low fraction bits dropped): within the fp32 bound of the exact product of
-  the oracle-truncated inputs, and within 4e-3 (|A||B|) of the exact product
-  of the fp32 ones (two truncations of under 2^-10 per product, doubled).
+  13 low fraction bits dropped), two checks of different standing:
+  * within 4e-3 (|A||B|) of the exact product of the fp32 inputs. This is the
+    pin the page fixes: its format (fp32's exponent, 10 fraction bits) bounds
+    each operand's change by 2^-10 relative, so each product by about
+    2 * 2^-10, whatever the conversion's rounding;
+  * within the fp32 bound of the exact product of the oracle-truncated
+    inputs. The truncation is the hardware's reading of an fp32 operand, taken
+    from a check on the GPU rather than from the page, so this tighter check
+    is self-consistency: it shows the kernel applies the same reading
+    everywhere (no term dropped, no operand swapped), not that the reading is
+    the page's.
 
 TF32 is the pages' tensor-core format for fp32 data (gpu-hpc-book ch.06,
-"Tensor Cores")."""
+"Tensor Cores" -> "TF32 (TensorFloat-32) 精度")."""
 import numpy as np
 import pytest
 import torch
