@@ -713,11 +713,15 @@ def time_one(args, name, w, fl, ib, sets, nsets, stream, peaks, roofline, g14, s
     reps = max(args.steps, 5)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(reps)]
+    clocks = ClockSampler(torch.cuda.current_device(), period_s=0.001)
+    torch.cuda.synchronize()
+    clocks.start()
     for i, (e0, e1) in enumerate(evs):
         e0.record(stream)
         launch(i)
         e1.record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop()
     if g14.check_device_error(stream.cuda_stream):
         raise RuntimeError(f"device error in {name}")
     ms = [e0.elapsed_time(e1) for e0, e1 in evs]
@@ -745,6 +749,7 @@ def time_one(args, name, w, fl, ib, sets, nsets, stream, peaks, roofline, g14, s
                       "algorithmic_bytes": ib, "gbs": gbs,
                       "frac_hbm": gbs / peaks["hbm_gbs"],
                       "workspace_bytes": ws_bytes if schedule == "stream-K" else 0,
+                      "clocks": clk,
                       "back_to_back": {"ms": ms_b2b, "tflops": fl / (ms_b2b / 1e3) / 1e12,
                                        "gbs": ib / (ms_b2b / 1e3) / 1e9,
                                        "frac_hbm": ib / (ms_b2b / 1e3) / 1e9 / peaks["hbm_gbs"]}}),

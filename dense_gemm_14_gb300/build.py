@@ -27,8 +27,8 @@ LIB_NAME = "libgemm14.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "sgemm_simt.cu", "hgemm_tc.cu", "hgemm_tc2.cu", "sgemm_tc3.cu", "epilogue.cu",
-           "host_path.cu", "copy.cu", "plan.cu"]
+SOURCES = ["api.cu", "sgemm_simt.cu", "sgemm_small.cu", "hgemm_tc.cu", "hgemm_tc2.cu",
+           "sgemm_tc3.cu", "epilogue.cu", "host_path.cu", "copy.cu", "plan.cu"]
 HEADERS = ["ptx.cuh", "kernels.h", "streamk.cuh", "api_internal.h", "plan.h", "checks.h",
            "libgemm14.map"]
 

@@ -354,8 +354,16 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
     }
   }
 
+  // With a workspace, plan for a split; if the split that plan counts on
+  // does not fit the workspace left (an fp32 product of few tiles), plan as
+  // the call without a workspace.
+  bool split_ok = workspace != nullptr;
   gemm14_plan plan;
-  plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+  plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan, split_ok);
+  if (split_ok && plan.kernel == 1 && workspace_bytes < workspace_need(plan, dev->sm_count, K)) {
+    split_ok = false;
+    plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+  }
   const int epi = beta != 0.0f ? kEpiAccum : alpha != 1.0f ? kEpiScale : kEpiStore;
   GemmArgs args{static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                 A, lda, B, ldb, C, ldc, plan.vec_store, transa, transb, epi, alpha, beta,
@@ -392,7 +400,8 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
       k_terms = 1;
       args.k_terms = 1;
     }
-    plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+    plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan,
+             split_ok);
     args.vec_store = plan.vec_store;
     grid = plan.grid;
   }
@@ -418,12 +427,19 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
     }
     // clusters of the tf32 kernel do not fit: the fp32 SIMT kernel
     dtype = GEMM14_DTYPE_F32;
-    plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+    plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan,
+             split_ok);
     args.vec_store = plan.vec_store;
     grid = plan.grid;
   }
   if (is_tf32_mode(dtype)) dtype = GEMM14_DTYPE_F32;  // planned on the SIMT kernel
 
+  if (dtype == GEMM14_DTYPE_F32 && plan.kernel == 6) {
+    // few tiles: 64 x 64 tiles, k split over clusters (no workspace)
+    const int tiles = static_cast<int>(plan.tiles);
+    return finish(launch_sgemm_small(args, plan.loader == 1, plan.grid / tiles, tiles, stream),
+                  "sgemm small launch", stream);
+  }
   if (dtype == GEMM14_DTYPE_F32) {
     schedule(plan, K, dev->sm_count, workspace, workspace_bytes, args, grid);
     if (plan.loader == 2)
@@ -468,24 +484,24 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
   if (plan.kernel == 3)
     plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
   schedule(plan, K, dev->sm_count, workspace, workspace_bytes, args, grid);
-  const uint32_t idesc =
-      idesc_f16_f32acc(bf16, HgemmShape::BM, plan.bn, transa != 0, transb == 0);
+  const uint32_t idesc = idesc_f16_f32acc(bf16, plan.bm, plan.bn, transa != 0, transb == 0);
   if (plan.loader == 2)
-    return finish(launch_hgemm_tc_soft(plan.bn, args, idesc, grid, stream), "hgemm launch",
-                  stream);
+    return finish(launch_hgemm_tc_soft(plan.bm, plan.bn, args, idesc, grid, stream),
+                  "hgemm launch", stream);
   CUtensorMap ma, mb, mc{};
-  if ((st = make_maps_16(bf16, transa, transb, M, N, K, A, lda, B, ldb, HgemmShape::BM, plan.bn,
-                         &ma, &mb)) != GEMM14_OK)
+  if ((st = make_maps_16(bf16, transa, transb, M, N, K, A, lda, B, ldb, plan.bm, plan.bn, &ma,
+                         &mb)) != GEMM14_OK)
     return st;
   // C for the TMA-store epilogue of the plain variant (untransposed operands,
-  // plain store, 16-byte-aligned C), as for the pair kernel.
+  // plain store, 16-byte-aligned C), as for the pair kernel: boxes of 32
+  // columns x the rows one epilogue warp holds (bm / 4).
   // The variant is plain exactly when launch_hgemm_tc picks it.
   if (!args.transa && !args.transb && args.epi == kEpiStore && plan.vec_store &&
       (st = make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, args.C, args.M, args.N, args.ldc,
-                     32, 32, CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
+                     32, plan.bm / 4, CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM14_OK)
     return st;
-  return finish(launch_hgemm_tc(plan.bn, ma, mb, mc, args, idesc, grid, stream), "hgemm launch",
-                stream);
+  return finish(launch_hgemm_tc(plan.bm, plan.bn, ma, mb, mc, args, idesc, grid, stream),
+                "hgemm launch", stream);
 }
 
 int run_gemm(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
@@ -526,7 +542,7 @@ size_t product_workspace_bytes(int dtype, int transa, int transb, int64_t M, int
     if (rp.a || rp.b || rp.split) return rp.total;
   }
   gemm14_plan plan;
-  plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
+  plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan, true);
   return workspace_need(plan, dev->sm_count, K);
 }
 
@@ -543,7 +559,8 @@ double schedule_efficiency(int dtype, int transa, int transb, int64_t M, int64_t
   const int64_t ldc = (N + 3) / 4 * 4;
   const void* base = reinterpret_cast<const void*>(uintptr_t(1) << 12);
   gemm14_plan plan;
-  plan_for(dtype, transa, transb, M, N, K, base, lda, base, ldb, base, ldc, dev->sm_count, &plan);
+  plan_for(dtype, transa, transb, M, N, K, base, lda, base, ldb, base, ldc, dev->sm_count, &plan,
+           true);
   if (plan.tiles <= 0 || workspace_need(plan, dev->sm_count, K) > 0) return 1.0;
   const int64_t slots =
       plan.kernel == 3 || plan.kernel == 5 ? dev->sm_count / 2 : dev->sm_count;
@@ -660,7 +677,7 @@ size_t gemm14_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int sm
                N > 0 ? ldb : 1) != GEMM14_OK)
     return 0;
   gemm14_plan plan;
-  plan_for(dtype, M, N, K, p, lda, p, ldb, p, ldb, sm_count, &plan);
+  plan_for(dtype, M, N, K, p, lda, p, ldb, p, ldb, sm_count, &plan, true);
   return workspace_need(plan, sm_count, K);
 }
 
@@ -678,7 +695,7 @@ size_t gemm14_workspace_bytes_ex(int dtype, int transa, int transb, int64_t M, i
   plan_repitch(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, sm_count, &rp);
   if (rp.a || rp.b || rp.split) return rp.total;
   gemm14_plan plan;
-  plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, sm_count, &plan);
+  plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, sm_count, &plan, true);
   return workspace_need(plan, sm_count, K);
 }
 

@@ -8,8 +8,9 @@
 // memory fed by TMA) are the prior art; on sm_103a the same product is one
 // tcgen05.mma issued by a single thread with the accumulator in tensor memory.
 //
-// Structure (one CTA per SM, persistent over output tiles of 128 x BN):
-//   warp 0      producer: TMA loads of A (128 m x 64 k, K-major, 128-byte
+// Structure (one CTA per SM, persistent over output tiles of BM x BN, BM =
+// 128, or 64 for products whose 128-row tiles leave SMs idle):
+//   warp 0      producer: TMA loads of A (BM m x 64 k, K-major, 128-byte
 //               swizzle) and B (BN/64 boxes of 64 n x 64 k, N-major, 128-byte
 //               swizzle) into an S-stage ring (full/empty mbarriers); for
 //               operands TMA cannot address, warp 0 and 7 more warps (6 ..)
@@ -21,6 +22,10 @@
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, fp32
 //               stores to C (16-byte vectors when C allows, guarded edges);
 //               while they drain accumulator b the MMA warp fills 1-b.
+//               An M = 128 accumulator holds row r in TMEM lane r; an M = 64
+//               one holds row r in lane 32 (r / 16) + r % 16, so each
+//               epilogue warp finds its 16 rows in the first 16 lanes of its
+//               quarter (the other 16 hold nothing of the product).
 // Tiles are visited in groups of 16 row-tiles so that the CTAs running at the
 // same time share A and B panels in L2.
 #include "kernels.h"
@@ -32,9 +37,9 @@ namespace {
 using H = HgemmShape;
 constexpr int kGroupM = 16;
 
-template <int BN>
+template <int BM, int BN>
 struct TcSmem {
-  static constexpr int STAGES = H::stages(BN);
+  static constexpr int STAGES = H::stages(BN, BM);
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t acc_full[2];
@@ -135,17 +140,17 @@ __device__ __forceinline__ void soft_mnmajor(uint8_t* dst, const uint16_t* src, 
 // Loader warp `part`'s share of one stage. A stored M x K is K-major, stored
 // K x M (transa) MN-major; B stored K x N is MN-major, stored N x K (transb)
 // K-major.
-template <int BN>
+template <int BM, int BN>
 __device__ __forceinline__ void soft_load_stage(uint8_t* a_st, const GemmArgs& args, int tm,
                                                 int tn, int kb, int lane, int part) {
   const uint16_t* A = static_cast<const uint16_t*>(args.A);
   const uint16_t* B = static_cast<const uint16_t*>(args.B);
-  uint8_t* b_st = a_st + H::BM * H::BK * 2;
+  uint8_t* b_st = a_st + BM * H::BK * 2;
   const int k0 = kb * H::BK;
   if (args.transa)
-    soft_mnmajor<H::BM>(a_st, A, args.lda, tm * H::BM, args.M, k0, args.K, lane, part);
+    soft_mnmajor<BM>(a_st, A, args.lda, tm * BM, args.M, k0, args.K, lane, part);
   else
-    soft_kmajor<H::BM>(a_st, A, args.lda, tm * H::BM, args.M, k0, args.K, lane, part);
+    soft_kmajor<BM>(a_st, A, args.lda, tm * BM, args.M, k0, args.K, lane, part);
   if (args.transb)
     soft_kmajor<BN>(b_st, B, args.ldb, tn * BN, args.N, k0, args.K, lane, part);
   else
@@ -153,22 +158,22 @@ __device__ __forceinline__ void soft_load_stage(uint8_t* a_st, const GemmArgs& a
 }
 
 // Stream-K fixup: a tile's owner reads the partial sums of its later workers
-// kPre at a time. Workspace slot cw holds worker cw's 128 x BN partial tile,
+// kPre at a time. Workspace slot cw holds worker cw's BM x BN partial tile,
 // row-major; this thread's row is r_loc and its chunk the 32 columns from
 // 32 c. Loads of n (<= kPre) consecutive workers from cw0, all issued before
 // any is used.
 constexpr int kPre = 4;
 
-// (Slot w holds worker w's 128 x BN partial sums; args.sk.G slots. A load the
+// (Slot w holds worker w's BM x BN partial sums; args.sk.G slots. A load the
 // bounds checks reject reads as zeros.)
-template <int BN, int NP>
+template <int BM, int BN, int NP>
 __device__ __forceinline__ void load_partials(float4 (&p)[NP][8], const GemmArgs& args, int cw0,
                                               int n, int r_loc, int c) {
 #pragma unroll
   for (int j = 0; j < NP; ++j) {
     if (j < n) {
-      const int64_t off = (static_cast<int64_t>(cw0 + j) * H::BM + r_loc) * BN + c * 32;
-      const bool ok = dev_check(slot_span_ok(off, cw0 + j, H::BM * BN, args.sk.G, 32), args.err);
+      const int64_t off = (static_cast<int64_t>(cw0 + j) * BM + r_loc) * BN + c * 32;
+      const bool ok = dev_check(slot_span_ok(off, cw0 + j, BM * BN, args.sk.G, 32), args.err);
       const float* src = args.partials + off;
 #pragma unroll
       for (int v = 0; v < 8; ++v)
@@ -205,7 +210,7 @@ __device__ __forceinline__ void add_partials(uint32_t (&r)[32], const float4 (&p
 template <bool kTma>
 constexpr int tc_threads() { return kTma ? H::THREADS : H::THREADS + 32 * (kSoftWarps - 1); }
 
-template <int BN, bool kTma, bool kSK, bool kGeneral>
+template <int BM, int BN, bool kTma, bool kSK, bool kGeneral>
 __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b,
@@ -213,18 +218,21 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
                     const uint32_t idesc) {
   const int transa = kGeneral ? args.transa : 0;
   const int transb = kGeneral ? args.transb : 0;
-  constexpr int STAGES = H::stages(BN);
-  constexpr int A_BYTES = H::BM * H::BK * 2;   // 16 KB
+  static_assert(BM == 64 || BM == 128, "tile rows");
+  constexpr int STAGES = H::stages(BN, BM);
+  constexpr int A_BYTES = BM * H::BK * 2;      // 16 KB (BM 128) or 8 KB (BM 64)
   constexpr int B_BYTES = H::BK * BN * 2;      // BN/64 boxes of 8 KB
+  constexpr int OUT_BUF_BYTES = H::out_buf_bytes(BM);
+  constexpr int ROWS_PER_WARP = BM / 4;        // rows each epilogue warp stores
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr uint32_t TMEM_COLS = 2 * BN;
 
-  static_assert(sizeof(TcSmem<BN>) <= H::SMEM_RESERVE, "barrier block exceeds its reserve");
+  static_assert(sizeof(TcSmem<BM, BN>) <= H::SMEM_RESERVE, "barrier block exceeds its reserve");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = align1024(smem_raw);
   uint8_t* out_stage = tiles + STAGES * STAGE_BYTES;  // epilogue staging for C
-  TcSmem<BN>& sm = *reinterpret_cast<TcSmem<BN>*>(out_stage + H::OUT_BYTES);
+  TcSmem<BM, BN>& sm = *reinterpret_cast<TcSmem<BM, BN>*>(out_stage + H::out_bytes(BM));
   // Plain variant with a 16-byte-aligned C: the epilogue writes C with TMA
   // stores of 32 x 32 blocks staged in shared memory.
   const bool tma_c = !kGeneral && args.vec_store;
@@ -232,7 +240,7 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int M = args.M, N = args.N;
-  const int tiles_m = (M + H::BM - 1) / H::BM;
+  const int tiles_m = (M + BM - 1) / BM;
   const int tiles_n = (N + BN - 1) / BN;
   const int w = blockIdx.x;  // this CTA's worker index in the schedule
   const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns, 0u};
@@ -313,7 +321,7 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
           if (!got) { ok = false; break; }
           // Failure-detection tests: the first stage is never loaded.
           if (args.fault == kFaultSkipFirstStage && prod_it == 0) continue;
-          soft_load_stage<BN>(tiles + s * STAGE_BYTES, args, tm, tn, kb, lane, part);
+          soft_load_stage<BM, BN>(tiles + s * STAGE_BYTES, args, tm, tn, kb, lane, part);
           fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
           mbar_arrive(&sm.full[s]);
         }
@@ -332,13 +340,13 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
           uint8_t* a_st = tiles + s * STAGE_BYTES;
           uint8_t* b_st = a_st + A_BYTES;
           mbar_arrive_expect_tx(&sm.full[s], STAGE_BYTES);
-          // A: one box of 64 k x 128 m, or (stored K x M) two boxes of 64 m x 64 k.
+          // A: one box of 64 k x BM m, or (stored K x M) BM / 64 boxes of 64 m x 64 k.
           if (!transa) {
-            tma_load_2d(a_st, &map_a, kb * H::BK, tm * H::BM, &sm.full[s]);
+            tma_load_2d(a_st, &map_a, kb * H::BK, tm * BM, &sm.full[s]);
           } else {
 #pragma unroll
-            for (int c = 0; c < H::BM / 64; ++c)
-              tma_load_2d(a_st + c * (64 * H::BK * 2), &map_a, tm * H::BM + c * 64, kb * H::BK,
+            for (int c = 0; c < BM / 64; ++c)
+              tma_load_2d(a_st + c * (64 * H::BK * 2), &map_a, tm * BM + c * 64, kb * H::BK,
                           &sm.full[s]);
           }
           // B: BN / 64 boxes of 64 n x 64 k, or (stored N x K) one box of 64 k x BN n.
@@ -390,8 +398,13 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int r_loc = q * 32 + lane;  // this thread's row within the tile
-    uint8_t* out_buf = out_stage + q * 2 * H::OUT_BUF_BYTES;
+    // This thread's row within the tile: lane l of the quarter for BM 128;
+    // for BM 64 lanes 0..15 hold rows 16 q + l and lanes 16..31 no row (they
+    // take part in the warp-wide TMEM loads and the staging, but load and
+    // store no data of their own).
+    const bool has_row = BM == 128 || lane < 16;
+    const int r_loc = q * ROWS_PER_WARP + (BM == 128 ? lane : (lane & 15));
+    uint8_t* out_buf = out_stage + q * 2 * OUT_BUF_BYTES;
     int ob = 0;
     for (int seg = 0; seg < n_seg; ++seg) {
       int tile, kb0, kb1, kind, tm, tn;
@@ -422,9 +435,9 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
         if (!got) break;
       }
       tc_fence_after_sync();
-      const int row = tm * H::BM + r_loc;
+      const int row = tm * BM + r_loc;
       float* crow = args.C + static_cast<int64_t>(row) * args.ldc;
-      float* prow = args.partials + (static_cast<size_t>(w) * H::BM + r_loc) * BN;
+      float* prow = args.partials + (static_cast<size_t>(w) * BM + r_loc) * BN;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(b * BN);
 #pragma unroll 1
@@ -436,14 +449,16 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
         // each, prefetch one partial at a time)
         constexpr int NP = kTma ? kPre : 1;
         float4 pre[NP][8];
-        const int n_pre = (kSK && kind == kSegHead) ? min(NP, sm.sched.head_last - w) : 0;
-        if (kSK) load_partials<BN, NP>(pre, args, w + 1, n_pre, r_loc, c);
+        const int n_pre =
+            (kSK && kind == kSegHead && has_row) ? min(NP, sm.sched.head_last - w) : 0;
+        if (kSK) load_partials<BM, BN, NP>(pre, args, w + 1, n_pre, r_loc, c);
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tc_wait_ld();
         if (kSK && kind == kSegPartial) {
           // Stream-K: partial sums of this tile go to workspace slot w.
-          if (!dev_check(slot_span_ok(prow + c * 32 - args.partials, w, H::BM * BN, args.sk.G, 32),
+          if (!has_row ||
+              !dev_check(slot_span_ok(prow + c * 32 - args.partials, w, BM * BN, args.sk.G, 32),
                          args.err))
             continue;
 #pragma unroll
@@ -457,9 +472,9 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
           // Add the later workers' partial sums, in worker order: the
           // prefetched group, then further groups of kPre (loads first).
           add_partials<NP>(r, pre, n_pre);
-          for (int cw0 = w + 1 + NP; cw0 <= sm.sched.head_last; cw0 += NP) {
+          for (int cw0 = w + 1 + NP; has_row && cw0 <= sm.sched.head_last; cw0 += NP) {
             const int n = min(NP, sm.sched.head_last - cw0 + 1);
-            load_partials<BN, NP>(pre, args, cw0, n, r_loc, c);
+            load_partials<BM, BN, NP>(pre, args, cw0, n, r_loc, c);
             add_partials<NP>(r, pre, n);
           }
         }
@@ -474,24 +489,27 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
           // map_c); the TMA store leaves out rows >= M (and columns >= N,
           // as above). The buffer's store of two chunks ago has been read
           // out first.
-          uint8_t* buf = out_buf + ob * H::OUT_BUF_BYTES;
+          uint8_t* buf = out_buf + ob * OUT_BUF_BYTES;
           if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
           const uint32_t rb = smem_u32(buf) + static_cast<uint32_t>(lane * 128);
+          if (has_row) {
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                             rb + static_cast<uint32_t>(((v ^ lane) & 7) << 4)),
-                         "r"(r[4 * v + 0]), "r"(r[4 * v + 1]), "r"(r[4 * v + 2]), "r"(r[4 * v + 3])
-                         : "memory");
+            for (int v = 0; v < 8; ++v)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                               rb + static_cast<uint32_t>(((v ^ lane) & 7) << 4)),
+                           "r"(r[4 * v + 0]), "r"(r[4 * v + 1]), "r"(r[4 * v + 2]),
+                           "r"(r[4 * v + 3])
+                           : "memory");
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&map_c, buf, col0, tm * H::BM + q * 32);
+            tma_store_2d(&map_c, buf, col0, tm * BM + q * ROWS_PER_WARP);
             bulk_commit();
           }
           ob ^= 1;
-        } else if (row < M) {
+        } else if (has_row && row < M) {
           if (args.vec_store && col0 + 32 <= N) {
 #pragma unroll
             for (int v = 0; v < 8; ++v)
@@ -545,62 +563,75 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
   }
 }
 
-template <int BN, bool kTma, bool kSK, bool kGeneral>
+template <int BM, int BN, bool kTma, bool kSK, bool kGeneral>
 cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
                            const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc,
                            int grid, cudaStream_t stream) {
   static DeviceOnce configured;
-  const cudaError_t e = set_smem_once(configured, hgemm_tc_kernel<BN, kTma, kSK, kGeneral>,
-                                      H::smem_bytes(BN));
+  const cudaError_t e = set_smem_once(configured, hgemm_tc_kernel<BM, BN, kTma, kSK, kGeneral>,
+                                      H::smem_bytes(BN, BM));
   if (e != cudaSuccess) return e;
   CUtensorMap dummy{};
-  return launch_kernel(hgemm_tc_kernel<BN, kTma, kSK, kGeneral>, dim3(grid), dim3(tc_threads<kTma>()),
-                       H::smem_bytes(BN), stream, map_a ? *map_a : dummy,
-                       map_b ? *map_b : dummy, map_c ? *map_c : dummy, args, idesc);
+  return launch_kernel(hgemm_tc_kernel<BM, BN, kTma, kSK, kGeneral>, dim3(grid),
+                       dim3(tc_threads<kTma>()), H::smem_bytes(BN, BM), stream,
+                       map_a ? *map_a : dummy, map_b ? *map_b : dummy, map_c ? *map_c : dummy,
+                       args, idesc);
 }
 
-template <int BN, bool kTma, bool kSK>
+template <int BM, int BN, bool kTma, bool kSK>
 cudaError_t launch_epi(const CUtensorMap* map_a, const CUtensorMap* map_b,
                        const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc, int grid,
                        cudaStream_t stream) {
   if (!kTma || args.transa || args.transb || args.epi != kEpiStore)
-    return launch_variant<BN, kTma, kSK, true>(map_a, map_b, map_c, args, idesc, grid, stream);
-  return launch_variant<BN, kTma, kSK, kTma ? false : true>(map_a, map_b, map_c, args, idesc,
-                                                             grid, stream);
+    return launch_variant<BM, BN, kTma, kSK, true>(map_a, map_b, map_c, args, idesc, grid,
+                                                   stream);
+  return launch_variant<BM, BN, kTma, kSK, kTma ? false : true>(map_a, map_b, map_c, args, idesc,
+                                                                 grid, stream);
 }
 
-template <int BN, bool kTma>
+template <int BM, int BN, bool kTma>
 cudaError_t launch_bn(const CUtensorMap* map_a, const CUtensorMap* map_b,
                       const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc, int grid,
                       cudaStream_t stream) {
   if (args.sk.dp_tiles < args.sk.tiles)
-    return launch_epi<BN, kTma, true>(map_a, map_b, map_c, args, idesc, grid, stream);
-  return launch_epi<BN, kTma, false>(map_a, map_b, map_c, args, idesc, grid, stream);
+    return launch_epi<BM, BN, kTma, true>(map_a, map_b, map_c, args, idesc, grid, stream);
+  return launch_epi<BM, BN, kTma, false>(map_a, map_b, map_c, args, idesc, grid, stream);
+}
+
+template <int BM, bool kTma>
+cudaError_t launch_bm(int bn, const CUtensorMap* map_a, const CUtensorMap* map_b,
+                      const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc, int grid,
+                      cudaStream_t stream) {
+  switch (bn) {
+    case 64: return launch_bn<BM, 64, kTma>(map_a, map_b, map_c, args, idesc, grid, stream);
+    case 128: return launch_bn<BM, 128, kTma>(map_a, map_b, map_c, args, idesc, grid, stream);
+    case 256: return launch_bn<BM, 256, kTma>(map_a, map_b, map_c, args, idesc, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <bool kTma>
-cudaError_t launch_any(int bn, const CUtensorMap* map_a, const CUtensorMap* map_b,
+cudaError_t launch_any(int bm, int bn, const CUtensorMap* map_a, const CUtensorMap* map_b,
                        const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc, int grid,
                        cudaStream_t stream) {
-  switch (bn) {
-    case 64: return launch_bn<64, kTma>(map_a, map_b, map_c, args, idesc, grid, stream);
-    case 128: return launch_bn<128, kTma>(map_a, map_b, map_c, args, idesc, grid, stream);
-    case 256: return launch_bn<256, kTma>(map_a, map_b, map_c, args, idesc, grid, stream);
+  switch (bm) {
+    case 64: return launch_bm<64, kTma>(bn, map_a, map_b, map_c, args, idesc, grid, stream);
+    case 128: return launch_bm<128, kTma>(bn, map_a, map_b, map_c, args, idesc, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_hgemm_tc(int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_hgemm_tc(int bm, int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
                             const CUtensorMap& map_c, const GemmArgs& args, uint32_t idesc,
                             int grid, cudaStream_t stream) {
-  return launch_any<true>(bn, &map_a, &map_b, &map_c, args, idesc, grid, stream);
+  return launch_any<true>(bm, bn, &map_a, &map_b, &map_c, args, idesc, grid, stream);
 }
 
-cudaError_t launch_hgemm_tc_soft(int bn, const GemmArgs& args, uint32_t idesc, int grid,
+cudaError_t launch_hgemm_tc_soft(int bm, int bn, const GemmArgs& args, uint32_t idesc, int grid,
                                  cudaStream_t stream) {
-  return launch_any<false>(bn, nullptr, nullptr, nullptr, args, idesc, grid, stream);
+  return launch_any<false>(bm, bn, nullptr, nullptr, nullptr, args, idesc, grid, stream);
 }
 
 }  // namespace gemm14

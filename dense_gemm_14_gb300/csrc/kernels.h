@@ -183,27 +183,47 @@ cudaError_t launch_sgemm_tma(const CUtensorMap& map_a, const CUtensorMap& map_b,
                              const GemmArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_sgemm_cpasync(const GemmArgs& args, int grid, cudaStream_t stream);
 
-// ---- bf16 / fp16 tcgen05 kernel (hgemm_tc.cu)
+// ---- fp32 products with few 128 x 256 tiles (sgemm_small.cu): 64 x 64 tiles,
+// the k range of each split over a cluster of `split` CTAs (1, 2, 4 or 8)
+// whose partial tiles are added through distributed shared memory.
+struct SmallShape {
+  static constexpr int BM = 64, BN = 64, BK = 32, STAGES = 3, THREADS = 256;
+  // 3 stages of A [64][36] + B [32][68] floats
+  static constexpr int SMEM_BYTES = STAGES * (BM * (BK + 4) + BK * (BN + 4)) * 4;
+};
+// vec_loads: A stored M x K and B stored K x N, 16-byte aligned, pitches
+// multiples of 4 floats (16-byte copies); else 4-byte copies (any storage,
+// pitch or alignment). tiles: 64 x 64 output tiles; the grid is split x tiles.
+cudaError_t launch_sgemm_small(const GemmArgs& args, bool vec_loads, int split, int tiles,
+                               cudaStream_t stream);
+
+// ---- bf16 / fp16 tcgen05 kernel (hgemm_tc.cu): tiles of bm x bn on one SM,
+// bm = 128 (M = 128 MMAs) or 64 (M = 64 MMAs, for products whose 128-row
+// tiles would leave SMs idle).
 struct HgemmShape {
   static constexpr int BM = 128, BK = 64;
   static constexpr int THREADS = 6 * 32;  // producer, MMA, 4 epilogue warps
-  static constexpr int stages(int bn) { return bn == 256 ? 4 : bn == 128 ? 6 : 8; }
-  static constexpr int stage_bytes(int bn) { return BM * BK * 2 + BK * bn * 2; }
+  static constexpr int stages(int bn, int bm = 128) {
+    return bm == 128 ? (bn == 256 ? 4 : bn == 128 ? 6 : 8) : (bn == 256 ? 4 : bn == 128 ? 8 : 12);
+  }
+  static constexpr int stage_bytes(int bn, int bm = 128) { return bm * BK * 2 + BK * bn * 2; }
   // epilogue staging for TMA stores of C: per epilogue warp two buffers of
-  // 32 rows x 32 fp32 columns (4 KB each)
-  static constexpr int OUT_BUF_BYTES = 32 * 32 * 4;
-  static constexpr int OUT_BYTES = 4 * 2 * OUT_BUF_BYTES;
+  // bm / 4 rows x 32 fp32 columns (4 KB each for bm = 128)
+  static constexpr int out_buf_bytes(int bm = 128) { return (bm / 4) * 32 * 4; }
+  static constexpr int out_bytes(int bm = 128) { return 4 * 2 * out_buf_bytes(bm); }
   static constexpr int SMEM_RESERVE = 512;  // barriers and the stream-K table
-  static constexpr int smem_bytes(int bn) {
-    return stages(bn) * stage_bytes(bn) + OUT_BYTES + SMEM_RESERVE + 1024;
+  static constexpr int smem_bytes(int bn, int bm = 128) {
+    return stages(bn, bm) * stage_bytes(bn, bm) + out_bytes(bm) + SMEM_RESERVE + 1024;
   }
 };
 
-// bn in {64, 128, 256}; idesc is the tcgen05 instruction descriptor
-// (operand format and shape); map_b boxes are 64 (n) x 64 (k). map_c: C as a
-// 2-D fp32 tensor (box 32 columns x 32 rows, 128-byte swizzle) for the
-// TMA-store epilogue of the plain variant when C takes 16-byte stores.
-cudaError_t launch_hgemm_tc(int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
+// bm in {64, 128}, bn in {64, 128, 256}; idesc is the tcgen05 instruction
+// descriptor (operand format and shape M = bm, N = bn); map_a boxes are 64 k x
+// bm rows (A stored M x K) or 64 m x 64 k (stored K x M); map_b boxes are 64
+// (n) x 64 (k). map_c: C as a 2-D fp32 tensor (box 32 columns x bm / 4 rows,
+// 128-byte swizzle) for the TMA-store epilogue of the plain variant when C
+// takes 16-byte stores.
+cudaError_t launch_hgemm_tc(int bm, int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
                             const CUtensorMap& map_c, const GemmArgs& args, uint32_t idesc,
                             int grid, cudaStream_t stream);
 // ---- bf16 / fp16 tcgen05 kernel on CTA pairs (hgemm_tc2.cu): 256 x 256 tiles
@@ -239,7 +259,7 @@ cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& ma
                                  uint32_t idesc, int clusters, bool tf32, cudaStream_t stream);
 
 // Same kernel with the software loader (operands TMA cannot address).
-cudaError_t launch_hgemm_tc_soft(int bn, const GemmArgs& args, uint32_t idesc, int grid,
+cudaError_t launch_hgemm_tc_soft(int bm, int bn, const GemmArgs& args, uint32_t idesc, int grid,
                                  cudaStream_t stream);
 
 // ---- fp32 inputs on the tensor cores (sgemm_tc3.cu): tcgen05 kind::tf32 on

@@ -24,9 +24,16 @@ int hgemm_bn_for(int64_t N) { return N <= 64 ? 64 : N <= 128 ? 128 : 256; }
 // Every kernel's TMA loader serves every storage: a stored transpose is an
 // M-major A or a K-major B in shared memory (the fp32 kernel's thread mapping
 // follows the layout; the tensor-core kernels take either major-ness).
+// fp32 products above this many FLOP (2MNK) whose call has a workspace stay
+// on the large kernel even with few tiles: its stream-K split over every SM
+// beat the small-product kernel from about 1 GFLOP on GB300 (1024^3: 55.9
+// against 67.8 us; 2048 x 1024 x 1024: 86.8 against 121.1 us; 512^3: 38.8
+// against 16.3 us; 256 x 4096 x 256: 31.3 against 22.5 us).
+constexpr double kSmallSplitFlops = 1073741824.0;
+
 void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K, const void* A,
               int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
-              gemm14_plan* p) {
+              gemm14_plan* p, bool split_ok) {
   std::memset(p, 0, sizeof *p);
   if (M == 0 || N == 0 || K == 0) return;  // nothing launched (K == 0: a memset)
   p->vec_store = aligned(C, 16) && (ldc % 4 == 0);
@@ -70,6 +77,32 @@ void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K
   }
   if (dtype == GEMM14_DTYPE_F32) {
     using S = SgemmShape;
+    const int64_t big_tiles = ((M + S::BM - 1) / S::BM) * ((N + S::BN - 1) / S::BN);
+    const double flops = 2.0 * static_cast<double>(M) * static_cast<double>(N) *
+                         static_cast<double>(K);
+    if (2 * big_tiles <= sm_count && !(split_ok && flops > kSmallSplitFlops)) {
+      // Fewer 128 x 256 tiles than half the SMs: 64 x 64 tiles, the k range of
+      // each split over a cluster of up to 8 CTAs while the grid stays within
+      // two CTAs per SM (and each CTA keeps at least one k-block).
+      using Q = SmallShape;
+      p->kernel = 6;
+      p->loader = (!transa && !transb && aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 &&
+                   ldb % 4 == 0) ? 1 : 2;
+      p->bm = Q::BM;
+      p->bn = Q::BN;
+      p->bk = Q::BK;
+      p->stages = Q::STAGES;
+      p->threads = Q::THREADS;
+      p->smem_bytes = Q::SMEM_BYTES;
+      p->tiles = ((M + Q::BM - 1) / Q::BM) * ((N + Q::BN - 1) / Q::BN);
+      const int64_t L = (K + Q::BK - 1) / Q::BK;
+      int64_t split = 1;
+      while (split < 8 && p->tiles * split * 2 <= 2 * static_cast<int64_t>(sm_count) &&
+             split * 2 <= L)
+        split *= 2;
+      p->grid = static_cast<int>(split * p->tiles);
+      return;
+    }
     p->kernel = 1;
     p->loader = (aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 && ldb % 4 == 0) ? 1 : 2;
     p->bm = S::BM;
@@ -96,13 +129,24 @@ void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K
       p->grid = static_cast<int>(2 * (p->tiles < clusters ? p->tiles : clusters));
       return;
     }
+    // One SM per tile: 128-row tiles, or 64-row tiles (M = 64 MMAs) when even
+    // the 64-row tiles fit in one wave (the 128-row ones fill at most half the
+    // SMs). Measured on GB300 (bf16, K = 4096): a tile's k-blocks stream at
+    // about the same rate per CTA whatever the tile's rows, so the plain call
+    // gains nothing from the smaller tiles (1024 to 8192 x 64: 21.7-22.6 us
+    // back to back either way) and loses when they spill past one wave
+    // (16384 x 64: 256 tiles, 41.3 against 26.9 us); the split call gains
+    // from the finer work (128 x 2048: 52.8 -> 27.6 us; 1024 x 64: 20.1 ->
+    // 16.6 us).
+    const int64_t tiles128 = ((M + 127) / 128) * ((N + bn - 1) / bn);
+    const int bm = 2 * tiles128 <= sm_count ? 64 : 128;
     p->kernel = 2;
-    p->bm = HgemmShape::BM;
+    p->bm = bm;
     p->bn = bn;
     p->bk = HgemmShape::BK;
-    p->stages = HgemmShape::stages(bn);
+    p->stages = HgemmShape::stages(bn, bm);
     p->threads = HgemmShape::THREADS;
-    p->smem_bytes = HgemmShape::smem_bytes(bn);
+    p->smem_bytes = HgemmShape::smem_bytes(bn, bm);
   }
   p->tiles = ((M + p->bm - 1) / p->bm) * ((N + p->bn - 1) / p->bn);
   const int64_t sms = sm_count > 0 ? sm_count : 1;
@@ -110,8 +154,8 @@ void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K
 }
 void plan_for(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
               const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
-              gemm14_plan* p) {
-  plan_for(dtype, 0, 0, M, N, K, A, lda, B, ldb, C, ldc, sm_count, p);
+              gemm14_plan* p, bool split_ok) {
+  plan_for(dtype, 0, 0, M, N, K, A, lda, B, ldb, C, ldc, sm_count, p, split_ok);
 }
 
 // Stream-K workspace the call would use with a workspace (0: it uses none).
@@ -179,6 +223,7 @@ int one_sm_split_workers(int kernel, int64_t tiles, int64_t L, int G) {
 
 size_t workspace_need(const gemm14_plan& plan, int sm_count, int64_t K, int k_terms) {
   if (plan.tiles > INT32_MAX) return 0;
+  if (plan.kernel == 6) return 0;  // its split is added up in shared memory
   if (plan.kernel == 3 || plan.kernel == 5) {
     const int64_t L = (K + plan.bk - 1) / plan.bk * (k_terms > 1 ? k_terms : 1);
     if (!pair_split_workers(plan.tiles, L, sm_count / 2)) return 0;
@@ -227,6 +272,18 @@ void plan_repitch(int dtype, int transa, int transb, int64_t M, int64_t N, int64
   // of its pairs and measured 42 % of the FFMA peak, against 76 % for B
   // stored K x N (A stored K x M is the fastest storage of A, 80.5 %): B is
   // transposed into K x N.
+  // The small-product kernel reads any storage and pitch as it is: nothing
+  // is copied for it.
+  if (dtype == GEMM14_DTYPE_F32 || (is_tf32_mode(dtype) && !r->split &&
+                                    !(dtype == GEMM14_DTYPE_TF32 && g_pair_enabled.load() &&
+                                      sms >= 2))) {
+    gemm14_plan as_stored;
+    plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, sms, &as_stored, true);
+    if (as_stored.kernel == 6) {
+      r->a = r->b = false;
+      return;
+    }
+  }
   if (dtype == GEMM14_DTYPE_F32 && transb) {
     r->b_t = true;
     r->b = true;
@@ -251,7 +308,7 @@ void plan_repitch(int dtype, int transa, int transb, int64_t M, int64_t N, int64
   const void* base = reinterpret_cast<const void*>(uintptr_t(1) << 12);
   gemm14_plan plan;
   plan_for(r->split ? GEMM14_DTYPE_TF32 : dtype, r->transa, r->transb, M, N, K,
-           r->a ? base : A, r->lda, r->b ? base : B, r->ldb, C, ldc, sms, &plan);
+           r->a ? base : A, r->lda, r->b ? base : B, r->ldb, C, ldc, sms, &plan, true);
   const size_t sk = workspace_need(plan, sms, K, r->split ? 3 : 1);
   r->sk_bytes = sk;
   const size_t flags = streamk_flag_bytes(sms);

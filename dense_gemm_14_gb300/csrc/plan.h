@@ -22,13 +22,16 @@ int hgemm_bn_for(int64_t N);   // one-SM tensor-core tile width for N columns
 
 // The plan (kernel, loader, tile, ring, grid) of a product on operands with
 // these addresses and pitches on a GPU with sm_count SMs (no launch when M, N
-// or K is 0). The pointers only enter through their alignment.
+// or K is 0). The pointers only enter through their alignment. split_ok: the
+// call has a workspace for a stream-K split (an fp32 product of over 2^30
+// FLOP then stays on the large kernel's tiles, which split over every SM,
+// rather than taking the small-product kernel).
 void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K, const void* A,
               int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
-              gemm14_plan* p);
+              gemm14_plan* p, bool split_ok = false);
 void plan_for(int dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
               const void* B, int64_t ldb, const void* C, int64_t ldc, int sm_count,
-              gemm14_plan* p);
+              gemm14_plan* p, bool split_ok = false);
 
 // Stream-K policy: the workers a plan's tiles are split over (0: unsplit),
 // the tile slots each worker keeps, and the workspace bytes that takes.

@@ -80,6 +80,11 @@ enum {
  * 16-byte aligned and lda, ldb are multiples of 4; otherwise an equivalent
  * cp.async loader is used (same results). 16-byte stores are used for C when
  * C is 16-byte aligned and ldc is a multiple of 4.
+ * A product whose 128 x 256 output tiles would fill at most half the SMs runs
+ * on 64 x 64 tiles instead, the k range of each tile split over a cluster of
+ * up to 8 CTAs and added up in a fixed order on chip (no workspace): its last
+ * bits may differ from the large tiles' (another summation order), within the
+ * same bound, and are the same with or without a workspace.
  * Follows the register-tiled, shared-memory-tiled kernels of gpu-hpc-book
  * ch.06, "矩阵乘法中的分块与数据复用" (Shared Memory Tiling, Register Tiling).
  */
@@ -339,8 +344,13 @@ typedef struct gemm14_plan {
                      3 = tcgen05 on CTA pairs (two SMs per 256 x 256 tile),
                      4 = tcgen05 kind::tf32 on CTA pairs (TF32 / 3xTF32),
                      5 = kernel 3 with kind::tf32 MMAs (TF32, A stored M x K and B
-                         stored N x K: both read as stored), 0 = no launch */
-  int loader;     /* 1 = TMA, 2 = software loader (cp.async for fp32), 0 = none */
+                         stored N x K: both read as stored),
+                     6 = fp32 FFMA on 64 x 64 tiles, the k range of each tile split
+                         over a cluster of grid / tiles CTAs (products whose
+                         128 x 256 tiles would fill at most half the SMs),
+                     0 = no launch */
+  int loader;     /* 1 = TMA (kernel 6: 16-byte cp.async), 2 = software loader
+                     (cp.async for fp32; kernel 6: 4-byte cp.async), 0 = none */
   int bm, bn, bk; /* output tile rows x columns, k-block depth */
   int stages;     /* shared-memory ring depth */
   int threads;    /* threads per CTA */
@@ -348,7 +358,8 @@ typedef struct gemm14_plan {
   int vec_store;  /* 1 if C takes 16-byte stores */
   int64_t tiles;  /* output tiles */
   int grid;       /* CTAs launched (persistent: min(tiles, sm_count); for kernel 3,
-                     2 x min(tiles, sm_count / 2)) */
+                     2 x min(tiles, sm_count / 2); for kernel 6, tiles x the
+                     cluster size) */
 } gemm14_plan;
 
 /*
@@ -369,8 +380,9 @@ int gemm14_plan_gemm_ex(int dtype, int transa, int transb, int64_t M, int64_t N,
 /*
  * The 16-bit entry points compute 256 x 256 output tiles on pairs of SMs
  * (a cluster of two CTAs sharing each tile's B operand) when the operands are
- * TMA-addressable and M, N > 128; otherwise 128-row tiles on one SM. Both
- * kernels accumulate in the same order and give bit-identical results.
+ * TMA-addressable and M, N > 128; otherwise tiles on one SM, of 128 rows, or
+ * of 64 rows when the 128-row tiles would be fewer than the SMs. The kernels
+ * accumulate in the same order and give bit-identical results.
  * gemm14_set_pair_kernel(0) restricts all later calls in the process to the
  * one-SM kernel, (1) allows pairs again (the default); returns the previous
  * setting. If pairs cannot be launched on the device the library falls back
@@ -388,6 +400,9 @@ int gemm14_set_pair_kernel(int enable);
  *   wait_limit_ns = 0 keeps the default limit (2 s).
  * No fault makes the GPU fault, trap or hang: waits are bounded, the context
  * stays usable, and gemm14_check_device_error reports the timeout.
+ * The fp32 small-product kernel (plan kernel 6) synchronises only through
+ * block and cluster barriers, with no mbarrier wait to expire: a call that
+ * runs on it consumes the request and computes C as usual.
  * Returns GEMM14_ERR_INVALID_ARG for an unknown mode.
  */
 int gemm14_debug_inject(int fault, uint64_t wait_limit_ns);

@@ -1,10 +1,11 @@
 """Runs a fixed set of products through gemm14_gemm_ex on whichever library
 GEMM14_LIB names, covering every kernel, loader and schedule: the fp32 FFMA
 kernel (TMA and cp.async loaders, data-parallel and stream-K, the A transpose
-copy), the one-SM and CTA-pair tensor-core kernels (data-parallel, stream-K,
-the hybrid split, the software loader, the TMA-store epilogue with a ragged
-N), TF32 on both tf32 kernels and split 3xTF32, the alpha/beta epilogue and
-stored transposes.
+copy), the fp32 small-product kernel (cluster split, both loaders), the
+one-SM tensor-core kernel with 64- and 128-row tiles and the CTA-pair one
+(data-parallel, stream-K, the hybrid split, the software loader, the
+TMA-store epilogue with a ragged N), TF32 on both tf32 kernels and split
+3xTF32, the alpha/beta epilogue and stored transposes.
 
     python device_checks_worker.py OUT.npz
 
@@ -31,13 +32,18 @@ DT = {F32: "f32", BF16: "bf16", F16: "f16", TF32: "f32", X3: "f32"}
 
 # name, dtype, transa, transb, M, N, K, alpha, beta, workspace, pitch pad (elements), offset
 CASES = [
-    ("f32 dp", F32, 0, 0, 300, 520, 200, 1.0, 0.0, False, 0, 0),
-    ("f32 stream-K", F32, 0, 0, 1000, 777, 513, 1.0, 0.0, True, 0, 0),
-    ("f32 A transposed copy", F32, 0, 0, 512, 2048, 256, 1.0, 0.0, True, 0, 0),
-    ("f32 cp.async", F32, 0, 0, 257, 300, 129, 1.0, 0.0, False, 1, 1),
-    ("f32 transposes alpha beta", F32, 1, 1, 300, 260, 190, -1.5, 0.5, True, 0, 0),
-    ("bf16 one-SM dp", BF16, 0, 0, 4096, 64, 512, 1.0, 0.0, False, 0, 0),
-    ("bf16 one-SM stream-K", BF16, 0, 0, 512, 128, 8192, 1.0, 0.0, True, 0, 0),
+    ("f32 dp", F32, 0, 0, 2048, 2048, 200, 1.0, 0.0, False, 0, 0),
+    ("f32 stream-K", F32, 0, 0, 2560, 2048, 513, 1.0, 0.0, True, 0, 0),
+    ("f32 A transposed copy", F32, 0, 0, 2048, 2048, 256, 1.0, 0.0, True, 0, 0),
+    ("f32 cp.async", F32, 0, 0, 2049, 2047, 129, 1.0, 0.0, False, 1, 1),
+    ("f32 transposes alpha beta", F32, 1, 1, 2048, 1536, 190, -1.5, 0.5, True, 0, 0),
+    ("f32 small split 8", F32, 0, 0, 256, 256, 256, 1.0, 0.0, False, 0, 0),
+    ("f32 small 4-byte loader", F32, 0, 0, 257, 300, 129, 1.0, 0.0, False, 1, 1),
+    ("f32 small transposes alpha beta", F32, 1, 1, 300, 260, 190, -1.5, 0.5, True, 0, 0),
+    ("bf16 one-SM 64-row dp", BF16, 0, 0, 4096, 64, 512, 1.0, 0.0, False, 0, 0),
+    ("bf16 one-SM 128-row dp", BF16, 0, 0, 32768, 64, 512, 1.0, 0.0, False, 0, 0),
+    ("bf16 one-SM 64-row stream-K", BF16, 0, 0, 512, 128, 8192, 1.0, 0.0, True, 0, 0),
+    ("bf16 one-SM 128-row stream-K", BF16, 0, 0, 23040, 64, 1024, 1.0, 0.0, True, 0, 0),
     ("bf16 pair dp ragged N", BF16, 0, 0, 1000, 777, 130, 1.0, 0.0, False, 0, 0),
     ("bf16 pair stream-K", BF16, 0, 0, 2304, 2560, 1024, 1.0, 0.0, True, 0, 0),
     ("bf16 pair hybrid", BF16, 0, 0, 4096, 5120, 256, 1.0, 0.0, True, 0, 0),

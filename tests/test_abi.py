@@ -115,17 +115,65 @@ def test_plan_fp32_tma_and_fallback(lib):
     st, p = g14.plan(F32, 4097, 3001, 513, P, 513, P, 3001, P, 3001, 152)
     assert st == 0 and p.loader == 2 and p.vec_store == 0
     assert p.tiles == 33 * 12
-    # few tiles -> grid = tiles
-    st, p = g14.plan(F32, 256, 256, 256, P, 256, P, 256, P, 256, 152)
-    assert p.tiles == 2 and p.grid == 2
+    # just over half the SMs' worth of 128 x 256 tiles: still the large kernel
+    st, p = g14.plan(F32, 1280, 2048, 256, P, 256, P, 2048, P, 2048, 152)
+    assert (p.kernel, p.tiles, p.grid) == (1, 80, 80)
 
 
-@pytest.mark.parametrize("N,bn", [(1, 64), (64, 64), (65, 128), (128, 128)])
-def test_plan_tensor_core_tile_width(lib, N, bn):
-    st, p = g14.plan(BF16, 16384, N, 4096, P, 4096, P, ((N + 7) // 8) * 8, P, N, 152)
-    assert st == 0 and p.kernel == 2 and p.bn == bn and p.bm == 128 and p.bk == 64
+# fp32 products whose 128 x 256 tiles would fill at most half the SMs: 64 x 64
+# tiles, k split over a cluster of 2-8 CTAs while the grid stays within two
+# CTAs per SM and each CTA has a k-block.
+@pytest.mark.parametrize("M,N,K,tiles,split", [
+    (256, 256, 256, 16, 8),      # the 256^3 workload: 8 k-blocks, one per CTA
+    (512, 512, 512, 64, 4),      # 4 x 64 CTAs <= 2 x 152
+    (1024, 1024, 1024, 256, 1),  # 256 tiles already fill the grid
+    (256, 256, 64, 16, 2),       # 2 k-blocks: split 2
+    (1, 1, 1, 1, 1),
+    (64, 64, 65536, 1, 8),       # a cluster is at most 8 CTAs
+    (1280, 1024, 256, 320, 1),   # 40 large tiles <= 76
+])
+def test_plan_fp32_small_products(lib, M, N, K, tiles, split):
+    st, p = g14.plan(F32, M, N, K, P, K, P, N, P, N, 152)
+    assert st == 0 and p.kernel == 6 and (p.bm, p.bn, p.bk) == (64, 64, 32)
+    assert p.tiles == tiles and p.grid == split * tiles
+    assert p.threads == 256 and p.smem_bytes <= 227 * 1024
+    assert p.loader == (1 if K % 4 == 0 and N % 4 == 0 else 2)
+    # no stream-K workspace and no operand copies: the split is added up on
+    # chip; but a call with a workspace runs products above 2^30 FLOP on the
+    # large kernel, split over every SM
+    if 2 * M * N * K <= 1 << 30:
+        assert g14.workspace_bytes(F32, M, N, K, 152) == 0
+        assert g14.workspace_bytes_ex(F32, 0, 1, M, N, K, P, K, P, K, P, N, 152) == 0
+    else:
+        assert g14.workspace_bytes(F32, M, N, K, 152) == 768 + 152 * 128 * 256 * 4
+
+
+def test_plan_fp32_small_product_loaders(lib):
+    # 16-byte copies need A stored M x K, B stored K x N, aligned, pitches % 4 == 0
+    st, p = g14.plan(F32, 256, 256, 256, P + 4, 256, P, 256, P, 256, 152)
+    assert p.kernel == 6 and p.loader == 2
+    st, p = g14.plan(F32, 256, 256, 256, P, 257, P, 256, P, 256, 152)
+    assert p.kernel == 6 and p.loader == 2
+    for ta, tb in ((1, 0), (0, 1), (1, 1)):
+        st, p = g14.plan_ex(F32, ta, tb, 256, 256, 256, P, 256, P, 256, P, 256, 152)
+        assert st == 0 and p.kernel == 6 and p.loader == 2
+
+
+def _bm_for(M, N, bn, sms=152):
+    """One-SM tile rows: 64 when the 64-row tiles fit in one wave."""
+    return 64 if 2 * ((M + 127) // 128) * ((N + bn - 1) // bn) <= sms else 128
+
+
+@pytest.mark.parametrize("M,N,bn", [(16384, 1, 64), (16384, 64, 64), (16384, 65, 128),
+                                    (16384, 128, 128), (32768, 64, 64), (19457, 64, 64),
+                                    (64, 64, 64), (100, 128, 128)])
+def test_plan_tensor_core_tile_width(lib, M, N, bn):
+    st, p = g14.plan(BF16, M, N, 4096, P, 4096, P, ((N + 7) // 8) * 8, P, N, 152)
+    bm = _bm_for(M, N, bn)
+    assert st == 0 and p.kernel == 2 and p.bn == bn and p.bm == bm and p.bk == 64
     assert p.smem_bytes <= 227 * 1024
-    assert p.tiles == 128 * ((N + bn - 1) // bn)
+    assert p.tiles == ((M + bm - 1) // bm) * ((N + bn - 1) // bn)
+    assert p.grid == min(p.tiles, 152)
 
 
 @pytest.mark.parametrize("M,N", [(16384, 129), (16384, 11008), (8192, 8192), (129, 300)])
@@ -139,7 +187,7 @@ def test_plan_pair_kernel_for_wide_products(lib, M, N):
     prev = g14.set_pair_kernel(False)
     try:
         st, p1 = g14.plan(BF16, M, N, 4096, P, 4096, P, ldb, P, N, 152)
-        assert p1.kernel == 2 and p1.bm == 128
+        assert p1.kernel == 2 and p1.bm == _bm_for(M, N, 256)
     finally:
         g14.set_pair_kernel(prev)
     # operands TMA cannot address stay on the one-SM kernel with the software loader
@@ -205,12 +253,12 @@ def test_ex_invalid_transpose_flags(lib, ta, tb):
 def test_ex_plan_loaders(lib):
     """TMA in every storage for aligned operands (same tiles), the software
     loader for unaligned ones; 16-bit transposes on pairs too."""
-    st, nn = g14.plan_ex(F32, 0, 0, 512, 512, 512, P, 512, P, 512, P, 512, 152)
-    assert st == 0 and nn.loader == 1
+    st, nn = g14.plan_ex(F32, 0, 0, 2048, 2048, 512, P, 2048, P, 2048, P, 2048, 152)
+    assert st == 0 and nn.loader == 1 and nn.kernel == 1
     for ta, tb in ((1, 0), (0, 1), (1, 1)):
-        st, p = g14.plan_ex(F32, ta, tb, 512, 512, 512, P, 512, P, 512, P, 512, 152)
+        st, p = g14.plan_ex(F32, ta, tb, 2048, 2048, 512, P, 2048, P, 2048, P, 2048, 152)
         assert st == 0 and p.loader == 1 and p.tiles == nn.tiles and p.grid == nn.grid
-        st, p = g14.plan_ex(F32, ta, tb, 512, 512, 512, P, 513, P, 512, P, 512, 152)
+        st, p = g14.plan_ex(F32, ta, tb, 2048, 2048, 512, P, 2049, P, 2048, P, 2048, 152)
         assert st == 0 and p.loader == 2
         st, p = g14.plan_ex(BF16, ta, tb, 512, 512, 512, P, 512, P, 512, P, 512, 152)
         assert st == 0 and p.loader == 1 and p.kernel == 3

@@ -36,7 +36,9 @@ def test_injection_is_consumed_by_the_next_call_even_if_invalid():
 @pytest.mark.parametrize("dt,soft", [("f32", False), ("f32", True), ("bf16", False),
                                      ("bf16", True), ("f16", False)])
 def test_expired_wait_reports_timeout_and_context_survives(oracle_mod, dt, soft):
-    M, N, K = 300, 520, 200
+    # fp32: enough 128 x 256 tiles for the large kernel (the small-product
+    # kernel has no mbarrier wait to expire, below)
+    M, N, K = (2048, 2048, 200) if dt == "f32" else (300, 520, 200)
     A, B = inputs.make(M, N, K, dt, "uniform", 1.0, seed=31)
     lda = K + 1 if soft else (K + 7) // 8 * 8
     ldb = N + 1 if soft else (N + 7) // 8 * 8
@@ -52,4 +54,22 @@ def test_expired_wait_reports_timeout_and_context_survives(oracle_mod, dt, soft)
     # the error word was read and cleared; the context still computes correctly
     assert g14.check_device_error(s.cuda_stream) == 0
     C = run_abi(A, B, lda=lda, ldb=ldb)
+    oracle_check(oracle_mod, A, B, C)
+
+
+@pytest.mark.gpu
+def test_small_product_kernel_consumes_the_request(oracle_mod):
+    """The fp32 small-product kernel synchronises through hardware barriers
+    (block and cluster), with no mbarrier wait that a skipped stage could
+    leave open: an injected fault is consumed by its call, which computes
+    the product as usual, and the next call is unaffected."""
+    M, N, K = 300, 520, 200
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=32)
+    st, plan = g14.plan(g14.GEMM14_DTYPE_F32, M, N, K, 1 << 16, K, 1 << 16, N, 1 << 16, N,
+                        torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan.kernel == 6
+    s = torch.cuda.current_stream()
+    assert g14.debug_inject(1, 20_000_000) == 0
+    C = run_abi(A, B)
+    assert g14.check_device_error(s.cuda_stream) == 0
     oracle_check(oracle_mod, A, B, C)

@@ -18,12 +18,13 @@ pytestmark = pytest.mark.gpu
 F32, BF16, X3 = g14.GEMM14_DTYPE_F32, g14.GEMM14_DTYPE_BF16, g14.GEMM14_DTYPE_F32_3XTF32
 CODE = {"f32": F32, "bf16": BF16, "x3": X3}
 
-# (dtype, M, N, K, ldb): fp32 few tiles (every SM shares them), the one-SM
-# tensor kernel with 4 workers a tile, the pair kernel between one and two
-# waves, fp32 with an odd B pitch (re-pitched, then split), and 3xTF32 split
-# ahead (B transposed, lo parts) on the pair kernel over 12 clusters
-CASES = [("f32", 1000, 1000, 777, 1000), ("bf16", 300, 100, 5000, 104),
-         ("bf16", 2304, 2560, 8192, 2560), ("f32", 129, 257, 4000, 257),
+# (dtype, M, N, K, ldb): fp32 just over one wave of tiles (the last ones
+# shared by every SM, A transposed first), the one-SM tensor kernel with 4
+# workers a 64-row tile, the pair kernel between one and two waves, fp32 with
+# an odd B pitch (re-pitched, then split), and 3xTF32 split ahead (B
+# transposed, lo parts) on the pair kernel over 12 clusters
+CASES = [("f32", 2560, 2048, 256, 2048), ("bf16", 300, 100, 5000, 104),
+         ("bf16", 2304, 2560, 8192, 2560), ("f32", 2560, 2047, 129, 2049),
          ("x3", 512, 384, 1001, 384)]
 
 

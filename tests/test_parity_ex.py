@@ -36,7 +36,9 @@ def odd_pitch(cols):
 
 # ------------------------------------------------------------------ fp32
 
-F32_SHAPES = [(3, 5, 7), (129, 257, 33), (300, 520, 200), (1000, 70, 513)]
+# small products (64 x 64 tiles) and one with 17 x 7 tiles of 128 x 256 (the
+# large kernel's stored-transpose layouts)
+F32_SHAPES = [(3, 5, 7), (129, 257, 33), (300, 520, 200), (1000, 70, 513), (2049, 1537, 97)]
 
 
 @pytest.mark.parametrize("ta,tb", TRANS)
@@ -147,7 +149,7 @@ def test_alpha_beta(oracle_mod, dt, alpha, beta, vec):
 def test_alpha_beta_stream_k(oracle_mod, dt, ta, tb):
     """alpha, beta applied once, after the stream-K fixup (tiles split over
     many SMs), with transposed storage; repeatable bit for bit."""
-    M, N, K = (129, 257, 4000) if dt == "f32" else (300, 100, 5000)
+    M, N, K = (2560, 2048, 256) if dt == "f32" else (300, 100, 5000)
     A, B = inputs.make(M, N, K, dt, "uniform", 1.0 / K ** 0.5, seed=9 + ta + 2 * tb)
     C0 = torch.from_numpy(np.random.default_rng(6).uniform(-1, 1, (M, N)).astype(np.float32))
     ws = make_workspace(dt, M, N, K)

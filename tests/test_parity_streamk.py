@@ -18,9 +18,10 @@ def rup(x, m):
     return (x + m - 1) // m * m
 
 
-# (M, N, K): few tiles over all SMs (a tile shared by many SMs), about two
-# waves (each tile split in two), a ragged tail, and tiny products.
-F32_CASES = [(1000, 1000, 777), (3072, 3072, 3072), (4097, 3001, 513), (129, 257, 4000),
+# (M, N, K): just over one wave (the last tiles shared by every SM), about
+# two waves (each tile split in two), a ragged tail; and products of few
+# tiles, which take the small-tile kernel and no workspace.
+F32_CASES = [(2560, 2048, 256), (3072, 3072, 3072), (4097, 3001, 513), (129, 257, 4000),
              (256, 256, 256), (1, 1, 1), (7, 300, 35)]
 
 
@@ -59,28 +60,35 @@ def test_tensor_core_streamk(oracle_mod, dt, M, N, K):
     assert torch.equal(C1, C3)
 
 
+# fp32 products split over a workspace need a wave of 128 x 256 tiles or
+# more (fewer take the small-tile kernel): 160 tiles here
+F32_SPLIT = (2560, 2048, 256)
+
+
 def test_streamk_vs_data_parallel_within_bound(oracle_mod):
-    A, B = inputs.make(1000, 1000, 777, "f32", "normal", 1.0, seed=5)
-    ws = make_workspace("f32", 1000, 1000, 777)
+    M, N, K = F32_SPLIT
+    A, B = inputs.make(M, N, K, "f32", "normal", 1.0, seed=5)
+    ws = make_workspace("f32", M, N, K)
+    assert ws.numel() > 256
     C_sk = run_abi(A, B, workspace=ws)
     C_dp = run_abi(A, B)
     oracle_check(oracle_mod, A, B, C_sk)
     oracle_check(oracle_mod, A, B, C_dp)
     # exact on integer inputs, whatever the split
-    Ai, Bi = inputs.make_integer(1000, 1000, 777, 3, "f32", seed=6)
+    Ai, Bi = inputs.make_integer(M, N, K, 3, "f32", seed=6)
     want = (Ai.double() @ Bi.double()).float()
     assert torch.equal(run_abi(Ai, Bi, workspace=ws), want)
 
 
 def test_small_workspace_falls_back_to_data_parallel():
-    A, B = inputs.make(1000, 1000, 777, "f32", "normal", 1.0, seed=7)
+    A, B = inputs.make(*F32_SPLIT, "f32", "normal", 1.0, seed=7)
     small = torch.zeros(1024, dtype=torch.uint8, device="cuda")
     assert torch.equal(run_abi(A, B, workspace=small), run_abi(A, B))
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_streamk_expired_wait_reports_timeout(oracle_mod, dt):
-    M, N, K = (1000, 1000, 777) if dt == "f32" else (300, 100, 5000)
+    M, N, K = F32_SPLIT if dt == "f32" else (300, 100, 5000)
     A, B = inputs.make(M, N, K, dt, "uniform", 1.0, seed=8)
     ws = make_workspace(dt, M, N, K)
     s = torch.cuda.current_stream()
@@ -95,11 +103,11 @@ def test_streamk_expired_wait_reports_timeout(oracle_mod, dt):
 def test_workspace_reused_across_shapes(oracle_mod):
     """One workspace, products of different shapes and dtypes in turn: the
     flag words sit at a fixed place, so stale partial sums never pose as flags."""
-    need = max(g14.workspace_bytes(g14.GEMM14_DTYPE_F32, 1000, 1000, 777, 0),
+    need = max(g14.workspace_bytes(g14.GEMM14_DTYPE_F32, 2560, 2048, 256, 0),
                g14.workspace_bytes(g14.GEMM14_DTYPE_BF16, 300, 100, 5000, 0))
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
-    cases = [("f32", 1000, 1000, 777), ("bf16", 300, 100, 5000), ("f32", 256, 256, 256),
-             ("bf16", 500, 64, 64), ("f32", 1000, 1000, 777)]
+    cases = [("f32", 2560, 2048, 256), ("bf16", 300, 100, 5000), ("f32", 256, 256, 256),
+             ("bf16", 500, 64, 64), ("f32", 2560, 2048, 256)]
     for i, (dt, M, N, K) in enumerate(cases):
         A, B = inputs.make(M, N, K, dt, "uniform", 1.0, seed=40 + i)
         C = run_abi(A, B, lda=rup(K, 8), ldb=rup(N, 8), workspace=ws)

@@ -50,7 +50,7 @@ def run(mode, A, B, ta=0, tb=0, lda=None, ldb=None, a_off=0, workspace=True, alp
     return c.cpu(), need
 
 
-@pytest.mark.parametrize("mode,M,N,K", [("f32", 4097, 3001, 513), ("f32", 1000, 777, 301),
+@pytest.mark.parametrize("mode,M,N,K", [("f32", 4097, 3001, 513), ("f32", 2049, 2047, 301),
                                         ("bf16", 1000, 777, 1000), ("f16", 300, 1001, 259),
                                         ("3xtf32", 1000, 777, 301), ("tf32", 513, 700, 129)])
 def test_unaligned_pitches_give_the_aligned_bits(oracle_mod, mode, M, N, K):
@@ -74,7 +74,7 @@ def test_unaligned_pitches_give_the_aligned_bits(oracle_mod, mode, M, N, K):
 def test_stored_transposes_and_misaligned_bases(oracle_mod, ta, tb):
     """Stored transposes with odd pitches and A's base 4 bytes off: the same
     bits as 16-byte-aligned storage, alpha and beta included."""
-    M, N, K = 700, 530, 333
+    M, N, K = 2049, 1537, 333  # 17 x 7 tiles of 128 x 256: the large kernel
     A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=11 * ta + tb)
     C0 = torch.from_numpy(np.random.default_rng(3).standard_normal((M, N)).astype(np.float32))
     C1, need = run("f32", A, B, ta, tb, a_off=1, alpha=-1.5, beta=0.5, C0=C0)
@@ -89,7 +89,7 @@ def test_stored_transposes_and_misaligned_bases(oracle_mod, ta, tb):
 def test_too_small_a_workspace_reads_operands_as_they_are(oracle_mod):
     """One byte short of workspace_bytes_ex: no copy; the stream-K schedule on
     the element-wise loader, the bits of a workspace of the shape-only size."""
-    M, N, K = 300, 200, 150
+    M, N, K = 2560, 2048, 150  # 160 tiles: split over every SM
     A, B = inputs.make(M, N, K, "f32", "normal", 1.0, seed=5)
     _, need = run("f32", A, B)
     sk = g14.workspace_bytes(CODE["f32"], M, N, K, 0)
@@ -104,8 +104,8 @@ def test_one_workspace_for_split_and_repitched_products(oracle_mod):
     """A workspace reused by stream-K products and re-pitched ones in turn:
     the copies never land on the flag words (integer data: exact)."""
     g14.load()
-    cases = [(1000, 1000, 777, 1000, 1000), (4097, 3001, 513, 513, 3001),
-             (1000, 1000, 777, 1000, 1000), (129, 257, 4001, 4001, 257)]
+    cases = [(2560, 2048, 256, 256, 2048), (4097, 3001, 513, 513, 3001),
+             (2560, 2048, 256, 256, 2048), (2049, 2047, 301, 301, 2047)]
     need = 0
     for M, N, K, lda, ldb in cases:
         need = max(need, g14.workspace_bytes_ex(CODE["f32"], 0, 0, M, N, K, 1 << 20, lda, 1 << 20,
@@ -169,7 +169,7 @@ def test_tf32_transposed_copies_with_alpha_beta(oracle_mod):
 
 
 @pytest.mark.parametrize("ta", [0, 1])
-@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (1000, 777, 301), (3072, 3072, 3072)])
+@pytest.mark.parametrize("M,N,K", [(2048, 1536, 200), (2049, 2047, 301), (3072, 3072, 3072)])
 def test_fp32_b_stored_n_by_k_runs_k_by_n(oracle_mod, ta, M, N, K):
     """fp32 with B stored N x K and a workspace: B is transposed into K x N and
     the product has the bits of B stored K x N from the start."""

@@ -28,7 +28,8 @@ def test_workspace_bytes():
     want = 768 + 152 * 128 * 256 * 4
     assert g14.workspace_bytes(F32, 3072, 3072, 3072, 152) == want
     assert g14.workspace_bytes(F32, 4097, 3001, 513, 152) == want
-    # skinny bf16: 128 tiles of 128 x 64 -- between half and one wave: not split
+    # skinny bf16: 128 tiles of 128 x 64 (64-row tiles would spill past one
+    # wave) -- between half and one wave: not split
     assert g14.workspace_bytes(BF16, 16384, 64, 4096, 152) == 0
     # 16-bit one-SM tiles between one and two waves: split with the last wave
     # under half full (180 tiles), not above (284 tiles); beyond two waves the
@@ -36,15 +37,22 @@ def test_workspace_bytes():
     assert g14.workspace_bytes(BF16, 23040, 64, 4096, 152) == 768 + 152 * 128 * 64 * 4
     assert g14.workspace_bytes(BF16, 36352, 64, 4096, 152) == 0
     assert g14.workspace_bytes(BF16, 40960, 64, 4096, 152) == 768 + 152 * 128 * 64 * 4
-    # few tiles (fewer than half a wave): split, one 128 x 64 slot per worker
-    assert g14.workspace_bytes(BF16, 1024, 64, 4096, 152) == 768 + 152 * 128 * 64 * 4
+    # few tiles (fewer than half a wave; 64-row tiles since those fit in one
+    # wave): split, one 64 x 64 slot per worker
+    assert g14.workspace_bytes(BF16, 1024, 64, 4096, 152) == 768 + 152 * 64 * 64 * 4
     # ... but a 16-bit tile takes at most 4 workers, each with at least 16 of
-    # its k-blocks: one tile of 64 k-blocks splits 4 ways, one of 8 does not
-    assert g14.workspace_bytes(BF16, 128, 64, 4096, 152) == 768 + 152 * 128 * 64 * 4
+    # its k-blocks: two tiles of 64 k-blocks split 4 ways each, of 8 or 16 not
+    assert g14.workspace_bytes(BF16, 128, 64, 4096, 152) == 768 + 152 * 64 * 64 * 4
     assert g14.workspace_bytes(BF16, 128, 64, 512, 152) == 0
     assert g14.workspace_bytes(BF16, 128, 64, 1024, 152) == 0
-    # fp32 k-blocks are long: two tiles of 8 k-blocks still spread over 16 SMs
-    assert g14.workspace_bytes(F32, 256, 256, 256, 152) == want
+    # fp32 products of few 128 x 256 tiles run 64 x 64 tiles split over
+    # clusters, added up in shared memory: no workspace
+    assert g14.workspace_bytes(F32, 256, 256, 256, 152) == 0
+    # ... from more than half the SMs' worth of tiles the large kernel, whose
+    # long k-blocks spread over every SM past a whole wave (160 tiles of 8
+    # k-blocks), not within one (80 tiles)
+    assert g14.workspace_bytes(F32, 2560, 2048, 256, 152) == want
+    assert g14.workspace_bytes(F32, 1280, 2048, 256, 152) == 0
     # the CTA-pair kernel (a cluster of two per worker): one 128 x 256 slot per
     # SM when it splits -- between one and two waves with long k (90 tiles on
     # 76 clusters), or few tiles with long k (4 tiles, 16 workers) ...
@@ -109,9 +117,19 @@ def test_workspace_bytes_ex_adds_room_to_repitch():
     M, N, K = 16384, 64, 4096
     assert ex(BF16, 0, 0, M, N, K, P, K, P, 65, P, N, 152) == 768 + K * 64 * 2
     # a misaligned base with an aligned pitch is copied too (A stored K x M)
-    M, N, K = 1000, 1000, 777
+    M, N, K = 2000, 2000, 777
     sk = g14.workspace_bytes(F32, M, N, K, 152)
-    assert ex(F32, 1, 0, M, N, K, P + 4, 1000, P, N, P, N, 152) == _r256(sk) + K * 1000 * 4
+    assert ex(F32, 1, 0, M, N, K, P + 4, 2000, P, N, P, N, 152) == _r256(max(sk, 768)) + K * 2000 * 4
+    # ... but not for the small-product kernel (18 tiles of 128 x 256, under
+    # 2^30 FLOP), which reads any base, pitch and storage as it is
+    M, N, K = 700, 530, 333
+    assert ex(F32, 1, 0, M, N, K, P + 4, 700, P, N, P, N, 152) == 0
+    assert ex(F32, 0, 1, M, N, K, P, 333, P + 4, 333, P, N, 152) == 0
+    # ... which a call with a workspace leaves above 2^30 FLOP (1000 x 1000 x
+    # 777: 1.55 GFLOP): the large kernel, A copied, split over every SM
+    M, N, K = 1000, 1000, 777
+    assert ex(F32, 1, 0, M, N, K, P + 4, 1000, P, N, P, N, 152) == \
+        _r256(768 + 152 * 128 * 256 * 4) + K * 1000 * 4
     # nothing to compute, or invalid arguments: 0
     assert ex(F32, 0, 0, 8, 8, 0, 0, 1, 0, 8, P, 8, 152) == 0
     assert ex(F32, 0, 0, 8, 8, 8, P, 7, P, 8, P, 8, 152) == 0
