@@ -80,6 +80,9 @@ def parse_args():
     ap.add_argument("--tf32-only", default=None, metavar="SHAPE:MODE",
                     help="with --table-tf32: one shape (f32_3072 or f32_8192) and one mode "
                          "(fp32, tf32 or 3xtf32), e.g. f32_3072:3xtf32 (for profiling)")
+    ap.add_argument("--fma-ceiling", action="store_true",
+                    help="measure the FFMA throughput a register-only loop reaches "
+                         "(packed and scalar), one JSON line each (not the bench line)")
     ap.add_argument("--table-ex", action="store_true",
                     help="time the extended call (stored transposes, alpha/beta) on the fp32 "
                          "3072^3 and 16-bit 8192^3 workloads, one JSON line per variant")
@@ -488,6 +491,43 @@ def run_ours(args, dist: Dist):
     flops_step = sum(p["flops"] for p in parts)
     value = flops_step * K * dist.world / elapsed_max / 1e12
 
+    # The SM clock the tensor-core part actually runs at. NVML reports the
+    # clock the GPU targets, which under a dense tensor load can sit above
+    # the one the SMs run at. A one-thread kernel that spins for a fixed
+    # number of SM cycles (torch.cuda._sleep) is started on a second stream
+    # together with each product; it shares an SM with the product's CTAs
+    # (they leave room for it), so cycles / event time is the clock while the
+    # product runs. Kept only when the spin ended before the product did.
+    effective = {}
+    for p in parts:
+        if p["bound"] != "tensor":
+            continue
+        side = torch.cuda.Stream(dev)
+        cycles = 200_000
+        mhz = []
+        for step in range(10):
+            pre = torch.cuda.Event()
+            pre.record(stream)
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            launch(p, step)
+            g1.record(stream)
+            side.wait_event(pre)
+            with torch.cuda.stream(side):
+                s0.record(side)
+                torch.cuda._sleep(cycles)
+                s1.record(side)
+            torch.cuda.synchronize()
+            spin_ms = s0.elapsed_time(s1)
+            # the spin lies inside the product's run: it started after the
+            # product's start event and ended before its end event
+            if g0.elapsed_time(s0) >= 0 and s1.elapsed_time(g1) >= 0 and spin_ms > 0:
+                mhz.append(cycles / (spin_ms * 1e3))
+        effective[p["name"]] = {"sm_mhz_median": statistics.median(mhz) if mhz else None,
+                                "samples": len(mhz), "method": "spin of 200000 SM cycles on a "
+                                "second stream inside the product's run, 10 tries"}
+
     # A sustained leg: the same step back to back for about args.sustained_s
     # seconds (the clock settles under the power cap), one event pair, its own
     # clock record. Reported beside the value, not in it.
@@ -542,7 +582,11 @@ def run_ours(args, dist: Dist):
             pk = sms * per_clock * mhz * 1e6 / 1e12
             at_clock = {"sm_mhz_median": mhz, "peak_tflops": pk, "frac": tflops / pk,
                         "note": f"{sms} SMs x {per_clock} FLOP/clock x the median SM clock "
-                                "sampled while the parts were timed"}
+                                "NVML reported while the parts were timed"}
+        eff = effective.get(p["name"])
+        if eff and eff["sm_mhz_median"]:
+            pk = sms * per_clock * eff["sm_mhz_median"] * 1e6 / 1e12
+            eff = dict(eff, peak_tflops=pk, frac=tflops / pk)
         part_out.append({
             "workload": p["name"], "kernel": p["kernel"], "entry": p["entry"],
             "launches_per_call": p["launches"],
@@ -550,6 +594,7 @@ def run_ours(args, dist: Dist):
             "workspace_bytes": p["ws_bytes"], "M": p["w"].M, "N": p["w"].N,
             "K": p["w"].K, "ms_mean": statistics.mean(ms), "ms_median": statistics.median(ms),
             "ms_min": min(ms), "tflops": tflops, "at_sampled_clock": at_clock,
+            "at_effective_clock": eff,
             "roofline": {"bound": p["bound"], "achieved": tflops, "peak": peak, "unit": UNIT,
                          "frac": tflops / peak, "peak_kind": peak_note,
                          "traffic": traffic_for(p["kernel"], p["src"], p["name"]),
@@ -909,8 +954,99 @@ def run_table_tf32(args):
         torch.cuda.empty_cache()
 
 
+FMA_CEILING_SRC = r"""
+#include <cstdint>
+// Each thread runs 32 independent accumulator chains of fused multiply-adds
+// on register operands only: packed fma.rn.f32x2 (MODE 0) or scalar
+// fma.rn.f32 (MODE 1). No memory traffic but one store per thread at the end.
+template <int MODE>
+__global__ void fma_loop(float* out, int iters, float a0, float b0) {
+  constexpr int NCH = 32;
+  uint64_t acc2[NCH], a2, b2;
+  float acc1[NCH];
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a2) : "f"(a0), "f"(a0 + 1.0f));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(b2) : "f"(b0), "f"(b0 - 1.0f));
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    asm("mov.b64 %0, {%1, %2};" : "=l"(acc2[i]) : "f"((float)i), "f"((float)(i + threadIdx.x)));
+    acc1[i] = (float)(3 * i + threadIdx.x);
+  }
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      if (MODE == 0) asm volatile("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[i]) : "l"(a2), "l"(b2));
+      else asm volatile("fma.rn.f32 %0, %1, %2, %0;" : "+f"(acc1[i]) : "f"(a0), "f"(b0));
+    }
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    float x, y;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(acc2[i]));
+    s += x + y + acc1[i];
+  }
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+// out: blocks x threads floats on the device; launches on the default stream.
+extern "C" int fma_ceiling_run(float* out, int mode, int blocks, int threads, int iters) {
+  if (mode == 0) fma_loop<0><<<blocks, threads>>>(out, iters, 1.0001f, 0.9999f);
+  else fma_loop<1><<<blocks, threads>>>(out, iters, 1.0001f, 0.9999f);
+  return (int)cudaGetLastError();
+}
+"""
+
+
+def run_fma_ceiling(args):
+    """The FFMA throughput a register-only loop reaches on this GPU, packed
+    (fma.rn.f32x2, what the fp32 kernel issues) and scalar, against the
+    unit-count peak (SMs x 128 lanes x 2 FLOP x clock). The loop is compiled
+    here with nvcc into a scratch folder; one JSON line per mode."""
+    import ctypes
+    import tempfile
+
+    import torch
+
+    from dense_gemm_14_gb300 import build, roofline
+    tmp = tempfile.mkdtemp(prefix="fma_ceiling_")
+    src, lib = os.path.join(tmp, "fma.cu"), os.path.join(tmp, "libfma.so")
+    with open(src, "w") as f:
+        f.write(FMA_CEILING_SRC)
+    subprocess.run([build.nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
+                    "-Xcompiler", "-fPIC", "-shared", "-o", lib, src], check=True)
+    so = ctypes.CDLL(lib)
+    so.fma_ceiling_run.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 4
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    threads, iters = 256, 20000
+    for mode, name in ((0, "packed fma.rn.f32x2"), (1, "scalar fma.rn.f32")):
+        blocks = 2 * sms
+        out = torch.empty(blocks * threads, device="cuda")
+        torch.cuda.synchronize()
+        assert so.fma_ceiling_run(out.data_ptr(), mode, blocks, threads, 100) == 0
+        clocks = ClockSampler(torch.cuda.current_device(), period_s=0.001)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        clocks.start()
+        e0.record(torch.cuda.default_stream())
+        so.fma_ceiling_run(out.data_ptr(), mode, blocks, threads, iters)
+        e1.record(torch.cuda.default_stream())
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+        ms = e0.elapsed_time(e1)
+        fmas = float(iters) * 32 * (2 if mode == 0 else 1) * blocks * threads
+        tflops = 2 * fmas / (ms * 1e-3) / 1e12
+        peak = roofline.fp32_alu_peak_tflops()
+        print(json.dumps({"fma_ceiling": name, "ms": ms, "tflops": tflops,
+                          "unit_count_peak_tflops": peak, "frac_of_unit_count_peak": tflops / peak,
+                          "fma_per_clock_per_sm_at_2070": fmas / (ms * 1e-3) / sms / 2.07e9,
+                          "grid": f"{blocks} x {threads} threads, 32 chains each",
+                          "clocks": clk}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.fma_ceiling:
+        run_fma_ceiling(args)
+        return
     if args.table_tf32:
         run_table_tf32(args)
         return
