@@ -717,6 +717,28 @@ def run_table(args):
     code = {"f32": g14.GEMM14_DTYPE_F32, "bf16": g14.GEMM14_DTYPE_BF16,
             "f16": g14.GEMM14_DTYPE_F16}
     stream = torch.cuda.current_stream()
+    if not args.table_only:
+        # the floor of a launch timed this way: a one-thread kernel that spins for
+        # 100 SM cycles, timed alone and back to back like the products below
+        for i in range(5):
+            torch.cuda._sleep(100)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(50)]
+        for e0, e1 in evs:
+            e0.record(stream)
+            torch.cuda._sleep(100)
+            e1.record(stream)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(50):
+            torch.cuda._sleep(100)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        alone = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+        print(json.dumps({"launch_floor": {"kernel": "one thread, 100 SM cycles",
+                                           "us_alone_median": alone * 1e3,
+                                           "us_back_to_back": b0.elapsed_time(b1) / 50 * 1e3}}),
+              flush=True)
     for name, w in inputs.WORKLOADS.items():
         if args.table_only and name != args.table_only:
             continue
