@@ -187,7 +187,7 @@ cudaError_t launch_sgemm_cpasync(const GemmArgs& args, int grid, cudaStream_t st
 // the k range of each split over a cluster of `split` CTAs (1, 2, 4 or 8)
 // whose partial tiles are added through distributed shared memory.
 struct SmallShape {
-  static constexpr int BM = 64, BN = 64, BK = 32, STAGES = 3, THREADS = 256;
+  static constexpr int BM = 64, BN = 64, BK = 32, STAGES = 3, THREADS = 128;
   // 3 stages of A [64][36] + B [32][68] floats
   static constexpr int SMEM_BYTES = STAGES * (BM * (BK + 4) + BK * (BN + 4)) * 4;
 };

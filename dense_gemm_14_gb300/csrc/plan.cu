@@ -83,7 +83,7 @@ void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K
     if (2 * big_tiles <= sm_count && !(split_ok && flops > kSmallSplitFlops)) {
       // Fewer 128 x 256 tiles than half the SMs: 64 x 64 tiles, the k range of
       // each split over a cluster of up to 8 CTAs while the grid stays within
-      // two CTAs per SM (and each CTA keeps at least one k-block).
+      // four CTAs per SM (and each CTA keeps at least one k-block).
       using Q = SmallShape;
       p->kernel = 6;
       p->loader = (!transa && !transb && aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 &&
@@ -97,7 +97,7 @@ void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K
       p->tiles = ((M + Q::BM - 1) / Q::BM) * ((N + Q::BN - 1) / Q::BN);
       const int64_t L = (K + Q::BK - 1) / Q::BK;
       int64_t split = 1;
-      while (split < 8 && p->tiles * split * 2 <= 2 * static_cast<int64_t>(sm_count) &&
+      while (split < 8 && p->tiles * split * 2 <= 4 * static_cast<int64_t>(sm_count) &&
              split * 2 <= L)
         split *= 2;
       p->grid = static_cast<int>(split * p->tiles);

@@ -12,9 +12,11 @@
 // is thus formed in a fixed order (deterministic run to run) without any
 // workspace, atomics or second launch.
 //
-// Within a CTA: 256 threads, each with a 4 x 4 block of the tile; a 3-stage
-// cp.async ring of 32-deep k-blocks (A tile 64 x 32, B tile 32 x 64, zero
-// filled outside the matrices). This is the shared-memory tiling and
+// Within a CTA: 128 threads, each with a 4 x 8 block of the tile summed with
+// packed fp32x2 FMAs (fma.rn.f32x2: two IEEE fp32 FMAs per instruction, each
+// accumulator summed over k in order); a 3-stage cp.async ring of 32-deep
+// k-blocks (A tile 64 x 32, B tile 32 x 64, zero filled outside the
+// matrices). This is the shared-memory tiling and
 // register blocking of gpu-hpc-book ch.06 "高级 cuda 特性 —— 从矩阵乘法(gemm)
 // 说起" ("矩阵乘法中的分块与数据复用", matmul_l1 and matmul_l1_reg) and the
 // double buffering of "Kernel 优化指南" ("Level 3: Double Buffering"), sized for
@@ -67,7 +69,7 @@ __device__ __forceinline__ void load_stage(float* st, const GemmArgs& a, int m0,
   if (kVec) {
     // A: 64 rows x 8 chunks of 4 k; B: 32 rows x 16 chunks of 4 n
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 512 / Q::THREADS; ++i) {
       const int c = t + i * Q::THREADS;
       const int m = c >> 3, kc = (c & 7) * 4;
       const int gm = m0 + m, gk = k0 + kc;
@@ -77,7 +79,7 @@ __device__ __forceinline__ void load_stage(float* st, const GemmArgs& a, int m0,
                   bytes);
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 512 / Q::THREADS; ++i) {
       const int c = t + i * Q::THREADS;
       const int k = c >> 4, nc = (c & 15) * 4;
       const int gk = k0 + k, gn = n0 + nc;
@@ -89,15 +91,16 @@ __device__ __forceinline__ void load_stage(float* st, const GemmArgs& a, int m0,
   } else {
     // one element per copy; consecutive threads read consecutive addresses
     // of the stored matrix
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    constexpr int R32 = Q::THREADS / 32, R64 = Q::THREADS / 64;  // rows per pass
+#pragma unroll 4
+    for (int i = 0; i < 2048 / Q::THREADS; ++i) {
       int m, k;
       if (!a.transa) {  // A[m * lda + k]: k fastest
         k = t & 31;
-        m = (t >> 5) + 8 * i;
+        m = (t >> 5) + R32 * i;
       } else {          // A[k * lda + m]: m fastest
         m = t & 63;
-        k = (t >> 6) + 4 * i;
+        k = (t >> 6) + R64 * i;
       }
       const int gm = m0 + m, gk = k0 + k;
       const bool in = gm < a.M && gk < k_end;
@@ -105,15 +108,15 @@ __device__ __forceinline__ void load_stage(float* st, const GemmArgs& a, int m0,
                                    : static_cast<int64_t>(gm) * a.lda + gk;
       cp_async_4(smem_u32(As + m * A_LD + k), in ? A + off : A, in ? 4u : 0u);
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
+#pragma unroll 4
+    for (int i = 0; i < 2048 / Q::THREADS; ++i) {
       int k, n;
       if (!a.transb) {  // B[k * ldb + n]: n fastest
         n = t & 63;
-        k = (t >> 6) + 4 * i;
+        k = (t >> 6) + R64 * i;
       } else {          // B[n * ldb + k]: k fastest
         k = t & 31;
-        n = (t >> 5) + 8 * i;
+        n = (t >> 5) + R32 * i;
       }
       const int gk = k0 + k, gn = n0 + n;
       const bool in = gn < a.N && gk < k_end;
@@ -124,27 +127,53 @@ __device__ __forceinline__ void load_stage(float* st, const GemmArgs& a, int m0,
   }
 }
 
-// The 4 x 4 block of thread (tm, tn) over one k-block: rows 4 tm .. 4 tm + 3,
-// columns 4 tn .. 4 tn + 3, k in order.
-__device__ __forceinline__ void fma_block(const float* st, int tm, int tn, float (&acc)[4][4]) {
-  const uint32_t a0 = smem_u32(st + (4 * tm) * A_LD);
-  const uint32_t b0 = smem_u32(st + A_STAGE + 4 * tn);
+// Two fp32 values in one 64-bit register (low half = first value).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+// d = a * b + d on both halves, each an IEEE fp32 fma (round to nearest).
+__device__ __forceinline__ void fma2(uint64_t& d, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+// Thread t of the CTA: warp w = t / 32 holds rows 16 w .. 16 w + 15; lane l
+// holds rows 16 w + (l / 8) + 4 i (i < 4) and columns 4 (l % 8) + q and
+// 32 + 4 (l % 8) + q (q < 4). acc2[i][p]: row i, columns pair p (p < 2: the
+// first four columns, p >= 2: the second four).
+__device__ __forceinline__ int small_row(int t, int i) {
+  return 16 * (t >> 5) + ((t & 31) >> 3) + 4 * i;
+}
+__device__ __forceinline__ int small_col(int t, int h) { return 32 * h + 4 * (t & 7); }
+
+// The thread's 4 x 8 block over one k-block, k in order: per 4 k, four
+// 16-byte loads of A (4 k of each row) and two of B per k.
+__device__ __forceinline__ void fma_block(const float* st, int t, uint64_t (&acc2)[4][4]) {
+  const uint32_t a0 = smem_u32(st + small_row(t, 0) * A_LD);
+  const uint32_t b0 = smem_u32(st + A_STAGE + small_col(t, 0));
 #pragma unroll
   for (int k4 = 0; k4 < Q::BK; k4 += 4) {
-    float4 a[4], b[4];
+    float4 a[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = lds128(a0 + static_cast<uint32_t>((i * A_LD + k4) * 4));
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) b[kk] = lds128(b0 + static_cast<uint32_t>((k4 + kk) * B_LD * 4));
+    for (int i = 0; i < 4; ++i) a[i] = lds128(a0 + static_cast<uint32_t>((4 * i * A_LD + k4) * 4));
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
+      const uint32_t bk = b0 + static_cast<uint32_t>((k4 + kk) * B_LD * 4);
+      const float4 v0 = lds128(bk), v1 = lds128(bk + 128);
+      const uint64_t bp[4] = {pack2(v0.x, v0.y), pack2(v0.z, v0.w), pack2(v1.x, v1.y),
+                              pack2(v1.z, v1.w)};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-        acc[i][0] = fmaf(av, b[kk].x, acc[i][0]);
-        acc[i][1] = fmaf(av, b[kk].y, acc[i][1]);
-        acc[i][2] = fmaf(av, b[kk].z, acc[i][2]);
-        acc[i][3] = fmaf(av, b[kk].w, acc[i][3]);
+        const uint64_t a2 = pack2(av, av);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) fma2(acc2[i][p], a2, bp[p]);
       }
     }
   }
@@ -189,12 +218,11 @@ __global__ void __launch_bounds__(Q::THREADS)
   const int kb_begin = rank * kb_per;
   const int k_end = min(args.K, (kb_begin + kb_per) * Q::BK);
   const int nkb = max(0, min(kb_per, (args.K + Q::BK - 1) / Q::BK - kb_begin));
-  const int tm = t >> 4, tn = t & 15;
-  float acc[4][4];
+  uint64_t acc2[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 4; ++j) acc2[i][j] = 0ull;
 
   // Global memory is touched only after the previous grid on the stream is
   // complete (programmatic dependent launch).
@@ -217,15 +245,20 @@ __global__ void __launch_bounds__(Q::THREADS)
       load_stage<kVec>(smem + (nx % Q::STAGES) * (A_STAGE + B_STAGE), args, m0, n0,
                        (kb_begin + nx) * Q::BK, k_end);
     cp_async_commit();
-    fma_block(smem + (i % Q::STAGES) * (A_STAGE + B_STAGE), tm, tn, acc);
+    fma_block(smem + (i % Q::STAGES) * (A_STAGE + B_STAGE), t, acc2);
   }
   cp_async_wait<0>();
 
+  // the thread's row i, columns 32 h + 4 (t % 8) .. + 3
+  auto quad = [&](int i, int h) {
+    const float2 lo = unpack2(acc2[i][2 * h]), hi = unpack2(acc2[i][2 * h + 1]);
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+  };
   if (split == 1) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      store4(args, m0 + 4 * tm + i, n0 + 4 * tn,
-             make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) store4(args, m0 + small_row(t, i), n0 + small_col(t, h), quad(i, h));
     return;
   }
   // Partial tile into this CTA's shared memory (the ring is no longer read).
@@ -233,8 +266,9 @@ __global__ void __launch_bounds__(Q::THREADS)
   float* P = smem;
 #pragma unroll
   for (int i = 0; i < 4; ++i)
-    *reinterpret_cast<float4*>(P + (4 * tm + i) * P_LD + 4 * tn) =
-        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      *reinterpret_cast<float4*>(P + small_row(t, i) * P_LD + small_col(t, h)) = quad(i, h);
   cluster_sync();  // every partial tile of the cluster is written and visible
   // Rank r adds up rows [r * rows, (r + 1) * rows) of the tile: one float4
   // of 4 columns per thread and step, ranks in order 0, 1, ...

@@ -347,7 +347,8 @@ typedef struct gemm14_plan {
                          stored N x K: both read as stored),
                      6 = fp32 FFMA on 64 x 64 tiles, the k range of each tile split
                          over a cluster of grid / tiles CTAs (products whose
-                         128 x 256 tiles would fill at most half the SMs),
+                         128 x 256 tiles would fill at most half the SMs; with a
+                         workspace, only those of at most 2^30 FLOP),
                      0 = no launch */
   int loader;     /* 1 = TMA (kernel 6: 16-byte cp.async), 2 = software loader
                      (cp.async for fp32; kernel 6: 4-byte cp.async), 0 = none */

@@ -121,12 +121,12 @@ def test_plan_fp32_tma_and_fallback(lib):
 
 
 # fp32 products whose 128 x 256 tiles would fill at most half the SMs: 64 x 64
-# tiles, k split over a cluster of 2-8 CTAs while the grid stays within two
+# tiles, k split over a cluster of 2-8 CTAs while the grid stays within four
 # CTAs per SM and each CTA has a k-block.
 @pytest.mark.parametrize("M,N,K,tiles,split", [
     (256, 256, 256, 16, 8),      # the 256^3 workload: 8 k-blocks, one per CTA
-    (512, 512, 512, 64, 4),      # 4 x 64 CTAs <= 2 x 152
-    (1024, 1024, 1024, 256, 1),  # 256 tiles already fill the grid
+    (512, 512, 512, 64, 8),      # 8 x 64 CTAs <= 4 x 152
+    (1024, 1024, 1024, 256, 2),  # 4 x 256 would pass four CTAs per SM
     (256, 256, 64, 16, 2),       # 2 k-blocks: split 2
     (1, 1, 1, 1, 1),
     (64, 64, 65536, 1, 8),       # a cluster is at most 8 CTAs
@@ -136,7 +136,7 @@ def test_plan_fp32_small_products(lib, M, N, K, tiles, split):
     st, p = g14.plan(F32, M, N, K, P, K, P, N, P, N, 152)
     assert st == 0 and p.kernel == 6 and (p.bm, p.bn, p.bk) == (64, 64, 32)
     assert p.tiles == tiles and p.grid == split * tiles
-    assert p.threads == 256 and p.smem_bytes <= 227 * 1024
+    assert p.threads == 128 and p.smem_bytes <= 227 * 1024
     assert p.loader == (1 if K % 4 == 0 and N % 4 == 0 else 2)
     # no stream-K workspace and no operand copies: the split is added up on
     # chip; but a call with a workspace runs products above 2^30 FLOP on the
