@@ -212,9 +212,8 @@ class ClockSampler:
             self._proc = None
 
     def _path(self):
-        d = os.path.join(ROOT, "gpurun_out")
-        os.makedirs(d, exist_ok=True)
-        return os.path.join(d, f"clocks_rank{self.dev}.csv")
+        import tempfile
+        return os.path.join(tempfile.gettempdir(), f"gemm14_clocks_{os.getpid()}_{self.dev}.csv")
 
     def stop(self) -> dict:
         if self._thread is not None:

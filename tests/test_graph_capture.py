@@ -71,3 +71,42 @@ def test_split_products_replayed_from_a_graph(oracle_mod):
         for (A, B, c), (code, dt, M, N, K, *_rest) in zip(host, bufs):
             oracle_check(oracle_mod, A, B, c.cpu(),
                          rows=np.arange(0, M, 13) if M * N * K > 1e9 else None)
+
+
+def test_small_tile_products_replayed_from_a_graph(oracle_mod):
+    """The fp32 small-tile kernel's cluster launches (the k split summed
+    through distributed shared memory) captured in a graph with a 64-row
+    tensor-core product between them, replayed on new inputs."""
+    cases = [("f32", 256, 256, 256), ("bf16", 1000, 64, 1000), ("f32", 300, 260, 190)]
+    s = torch.cuda.Stream()
+    bufs = []
+    for dt, M, N, K in cases:
+        td = torch.bfloat16 if dt == "bf16" else torch.float32
+        bufs.append((dt, M, N, K, torch.zeros(M, K, dtype=td, device="cuda"),
+                     torch.zeros(K, N, dtype=td, device="cuda"), torch.zeros(M, N, device="cuda")))
+    entry = {"f32": g14.gemm_f32, "bf16": g14.gemm_bf16_f32acc}
+
+    def issue():
+        for dt, M, N, K, a, b, c in bufs:
+            entry[dt](M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, s.cuda_stream)
+
+    with torch.cuda.stream(s):
+        issue()  # warm-up outside the capture (kernel attributes)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        issue()
+    for rep in range(3):
+        host = []
+        for i, (dt, M, N, K, a, b, c) in enumerate(bufs):
+            A, B = inputs.make(M, N, K, dt, "normal", 1.0 / K ** 0.5, seed=300 + 10 * rep + i)
+            a.copy_(A.cuda())
+            b.copy_(B.cuda())
+            c.fill_(float("nan"))
+            host.append((A, B, c))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert g14.check_device_error(torch.cuda.current_stream().cuda_stream) == 0
+        for A, B, c in host:
+            oracle_check(oracle_mod, A, B, c.cpu())
