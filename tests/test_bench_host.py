@@ -93,3 +93,27 @@ def test_accuracy_of_reports_the_oracle_comparison():
     bad[0, 3] += 1.0
     acc = bench.accuracy_of("f32_256", A, B, bad, ref_rows)
     assert not acc["within"] and acc["max_err_over_abs"] > 1e-5 and acc["rel_rmse"] > 1e-4
+
+
+def test_clock_summary_counts_reasons_per_sample():
+    """The clock record's summary: median and range of the SM clock, the
+    highest power, and how many samples carried each clock-event reason
+    (bits of NVML's public header: 0x4 sw_power_cap, 0x8 hw_slowdown, 0x20
+    sw_thermal_slowdown, 0x40 hw_thermal_slowdown)."""
+    c = bench.ClockSampler(0, period_s=0.002)
+    assert c.summary()["samples"] == 0 and c.summary()["reasons"] == ["no samples"]
+    c.samples = [(2070.0, 900.0, 0x0), (1900.0, 1390.0, 0x4), (1700.0, 1400.0, 0x4 | 0x8),
+                 (2070.0, 700.0, 0x1)]
+    s = c.summary()
+    assert s["samples"] == 4 and s["sm_mhz"] == 1985.0 and s["sm_min_mhz"] == 1700.0
+    assert s["power_w_max"] == 1400.0
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert s["reason_samples"] == {"sw_power_cap": 2, "hw_slowdown": 1}
+    assert s["period_ms"] == 2.0
+
+
+def test_one_thread_oracle_sample():
+    """The cpu_baseline's one-thread leg: the oracle on one thread, a bounded
+    number of rows, the whole product when it fits."""
+    f, t, rows, threads = bench.time_oracle_sample("f32_256", 0.5, threads=1)
+    assert threads == 1 and rows == 256 and f == 2 * 256 ** 3 and t > 0
