@@ -86,6 +86,12 @@ def parse_args():
     ap.add_argument("--table-ex", action="store_true",
                     help="time the extended call (stored transposes, alpha/beta) on the fp32 "
                          "3072^3 and 16-bit 8192^3 workloads, one JSON line per variant")
+    ap.add_argument("--table-soft", action="store_true",
+                    help="time bf16 products whose operands TMA cannot read (odd pitches, "
+                         "2-byte offsets) through the plain call, against the same kernel "
+                         "on 16-byte pitches, one JSON line per shape")
+    ap.add_argument("--soft-only", default=None, metavar="SHAPE",
+                    help="with --table-soft: one shape, unaligned call only (for profiling)")
     return ap.parse_args()
 
 
@@ -896,6 +902,106 @@ def run_table_ex(args):
             torch.cuda.empty_cache()
 
 
+# bf16 products with operands TMA cannot read: (name, M, N, K, transa, transb,
+# extra pitch of A, extra pitch of B, element offset of A and B), the stored
+# rows' pitches being their lengths plus the extra.
+SOFT_SHAPES = [
+    ("8192x8192x8191_lda_odd", 8192, 8192, 8191, 0, 0, 0, 0, 0),
+    ("4096_nn_odd", 4096, 4096, 4096, 0, 0, 1, 1, 0),
+    ("4096_tt_odd", 4096, 4096, 4096, 1, 1, 1, 1, 0),
+    ("4096_nn_pitch+2_offset1", 4096, 4096, 4096, 0, 0, 2, 2, 1),
+    ("1000x777x1000_ldb_odd", 1000, 777, 1000, 0, 0, 0, 1, 0),
+    ("16384x64x4096_odd", 16384, 64, 4096, 0, 0, 1, 1, 0),
+]
+
+
+def run_table_soft(args):
+    """The 16-bit software loader: bf16 products through the plain call (no
+    workspace, so no re-pitching) with operands that TMA cannot read, against
+    the same one-SM kernel on copies with 16-byte pitches (CTA pairs off for
+    both). Operand copies rotate over > 2x L2; the two results must agree bit
+    for bit."""
+    import torch
+
+    import dense_gemm_14_gb300 as g14
+    from dense_gemm_14_gb300 import roofline
+
+    g14.load()
+    peaks = roofline.measured_peaks()
+    stream = torch.cuda.current_stream()
+    prev = g14.set_pair_kernel(False)
+    try:
+        for name, M, N, K, ta, tb, xa, xb, off in SOFT_SHAPES:
+            if args.soft_only and name != args.soft_only:
+                continue
+            ar, ac = (K, M) if ta else (M, K)
+            br, bc = (N, K) if tb else (K, N)
+            g = torch.Generator(device="cuda").manual_seed(14100)
+            variants = {"unaligned": (ac + xa, bc + xb, off)}
+            if not args.soft_only:
+                variants["tma"] = (-(-ac // 8) * 8, -(-bc // 8) * 8, 0)
+            res, outs = {}, {}
+            for v, (lda, ldb, o) in variants.items():
+                per_set = (ar * lda + br * ldb) * 2 + M * N * 4
+                nsets = max(2, -(-2 * L2_BYTES // per_set))
+                sets = []
+                for _ in range(nsets):
+                    a = torch.zeros(o + ar * lda, dtype=torch.bfloat16, device="cuda")
+                    b = torch.zeros(o + br * ldb, dtype=torch.bfloat16, device="cuda")
+                    a[o:].view(ar, lda)[:, :ac] = (torch.randn(ar, ac, device="cuda", generator=g)
+                                                    * 0.05).to(torch.bfloat16)
+                    b[o:].view(br, ldb)[:, :bc] = (torch.randn(br, bc, device="cuda", generator=g)
+                                                    * 0.05).to(torch.bfloat16)
+                    sets.append((a, b, torch.zeros(M, N, device="cuda")))
+                if v == "tma":  # the same operand values as the unaligned sets
+                    for (a, b, _), (ua, ub, _) in zip(sets, outs["sets"]):
+                        ula, ulb, uo = variants["unaligned"]
+                        a.view(ar, lda)[:, :ac] = ua[uo:].view(ar, ula)[:, :ac]
+                        b.view(br, ldb)[:, :bc] = ub[uo:].view(br, ulb)[:, :bc]
+
+                def launch(i):
+                    a, b, c = sets[i % nsets]
+                    g14.gemm_ex(g14.GEMM14_DTYPE_BF16, ta, tb, M, N, K, 1.0,
+                                a.data_ptr() + 2 * o, lda, b.data_ptr() + 2 * o, ldb, 0.0,
+                                c.data_ptr(), N, None, 0, stream.cuda_stream)
+
+                for i in range(args.warmup):
+                    launch(i)
+                reps = max(args.steps, 5)
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(reps)]
+                for i, (e0, e1) in enumerate(evs):
+                    e0.record(stream)
+                    launch(i)
+                    e1.record(stream)
+                torch.cuda.synchronize()
+                if g14.check_device_error(stream.cuda_stream):
+                    raise RuntimeError(f"device error in {name} ({v})")
+                ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+                res[v] = {"lda": lda, "ldb": ldb, "offset": o, "ms_median": statistics.median(ms),
+                          "ms_min": min(ms)}
+                launch(0)
+                torch.cuda.synchronize()
+                outs[v] = sets[0][2].clone()
+                if v == "unaligned":
+                    outs["sets"] = sets
+                else:
+                    del sets
+            fl = roofline.flops(M, N, K)
+            line = {"shape": name, "M": M, "N": N, "K": K, "transa": ta, "transb": tb}
+            for v, r in res.items():
+                tf = fl / (r["ms_median"] / 1e3) / 1e12
+                line[v] = dict(r, tflops=tf, frac_of_bf16_peak=tf / peaks["bf16_tflops"])
+            if "tma" in outs:
+                line["bit_identical"] = bool(torch.equal(outs["unaligned"], outs["tma"]))
+                line["unaligned_over_tma"] = res["unaligned"]["ms_median"] / res["tma"]["ms_median"]
+            print(json.dumps(line), flush=True)
+            outs.clear()
+            torch.cuda.empty_cache()
+    finally:
+        g14.set_pair_kernel(prev)
+
+
 def run_table_tf32(args):
     """fp32 inputs timed alone in each arithmetic: gemm_f32 (FFMA, workspace
     entry), gemm_tf32_f32acc and gemm_f32_3xtf32 (tensor cores), at the 3072^3
@@ -1076,6 +1182,9 @@ def main():
         return
     if args.table_ex:
         run_table_ex(args)
+        return
+    if args.table_soft:
+        run_table_soft(args)
         return
     dist = Dist(args.gpus)
     try:

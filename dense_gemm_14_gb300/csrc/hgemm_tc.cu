@@ -68,94 +68,290 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
 }
 
 // Software loader for operands that break TMA's 16-byte rules (any 2-byte
-// aligned base and pitch): the producer warp reads element pairs with 2-byte
-// loads (zero outside the matrix) and writes them into the same 128-byte
-// swizzled layout TMA would produce, then fences them into the async proxy.
-__device__ __forceinline__ uint32_t ld_pair(const uint16_t* base, int64_t row_off, int col,
-                                            int ncols, bool row_ok) {
-  uint32_t lo = 0, hi = 0;
-  if (row_ok && col < ncols) lo = __ldg(base + row_off + col);
-  if (row_ok && col + 1 < ncols) hi = __ldg(base + row_off + col + 1);
-  return lo | (hi << 16);
+// aligned base and pitch). A row segment is the 64 elements of one 128-byte
+// row of the 128-byte swizzled layout TMA would produce. Loader warps copy
+// the 16-byte-aligned global chunks that cover a segment straight into shared
+// memory with cp.async.cg (no register holds data in flight, L1 is bypassed,
+// and several stages are in flight at once), zero-filling bytes past the
+// row's last element. When the segment starts sh bytes past a 16-byte
+// boundary, it spans nine chunks: the first eight land in the row's eight
+// swizzled slots, the ninth in a side buffer, and once they have landed the
+// warp shifts the row left by sh bytes in place. sh is the same for every
+// segment a loader warp handles (its rows are 8 apart and its k or column
+// blocks 64 elements apart). No byte past a row's last element is read; bytes
+// before a segment's first element are read only inside the operand (the
+// chunk that holds the operand's first element, when that sits past a
+// 16-byte boundary, is read element by element).
+constexpr int kSoftWarps = 8;  // warps 6 .. 13, two per scheduler; each fills every 8-th row
+
+__device__ __align__(16) uint32_t g_zero_chunk[4];  // source of zero-byte copies
+
+__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* src,
+                                            uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128u(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts128u(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
-// The software loader runs on kSoftWarps warps (warp 0 and warps 6 ..), each
-// filling every kSoftWarps-th row of a stage, so that they have all their loads
-// of a stage in flight together (one warp alone is latency-bound: about 4 KB
-// in flight per SM).
-constexpr int kSoftWarps = 8;
+// A bounded wait like mbar_wait whose polls let the thread sleep until the
+// phase completes (or about kSleepHintNs pass): for the roles of the
+// software-loader variants that wait long (the epilogue for a tile's whole
+// main loop, the MMA warp for the loader warps), so that their polling takes
+// no issue slots from the loader warps on the same schedulers.
+constexpr uint32_t kSleepHintNs = 20000;
 
-// Rows part, part + kSoftWarps, ... of a K-major operand tile of ROWS rows
-// (matrix rows row0 ..) by 64 k (from k0): 128-byte rows. Lane l holds k pair
-// (2l, 2l+1) of a row; its 4-byte word sits in 16-byte chunk (l / 4) XOR
-// (row % 8), at byte 4 (l % 4) of the chunk.
-template <int ROWS>
-__device__ __forceinline__ void soft_kmajor(uint8_t* dst, const uint16_t* src, int64_t ld,
-                                            int row0, int nrows, int k0, int K, int lane,
-                                            int part) {
-  constexpr int N = ROWS / kSoftWarps;
-  const uint32_t word = static_cast<uint32_t>((lane & 3) << 2);
-  const int k = k0 + 2 * lane;
-  uint32_t v[N];
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    const int m = row0 + part + i * kSoftWarps;
-    v[i] = ld_pair(src, static_cast<int64_t>(m) * ld, k, K, m < nrows);
-  }
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    const int r = part + i * kSoftWarps;
-    *reinterpret_cast<uint32_t*>(dst + r * 128 + ((((lane >> 2) ^ (r & 7)) & 7) << 4) + word) =
-        v[i];
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSleepHintNs)
+      : "memory");
+  return done != 0;
+}
+
+static __device__ __noinline__ bool mbar_wait_sleep_slow(uint64_t* bar, uint32_t parity,
+                                                         const WaitCtx& w) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (*w.abort_flag) return false;
+    if (globaltimer_ns() - t0 > w.limit_ns) {
+      atomicOr(w.err, kDevErrTimeout);
+      *w.abort_flag = 1;
+      return false;
+    }
   }
 }
 
-// k-rows part, part + kSoftWarps, ... of an MN-major operand tile of COLS
-// columns (matrix columns col0 ..) by 64 k: COLS / 64 boxes of 64 columns x
-// 64 k rows (8 KB each, 128-byte rows).
-template <int COLS>
-__device__ __forceinline__ void soft_mnmajor(uint8_t* dst, const uint16_t* src, int64_t ld,
-                                             int col0, int ncols, int k0, int K, int lane,
-                                             int part) {
-  constexpr int N = H::BK / kSoftWarps;
-  const uint32_t word = static_cast<uint32_t>((lane & 3) << 2);
+// mbar_wait for the TMA variants, the sleeping wait for the others.
+template <bool kSleep>
+__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return kSleep ? mbar_wait_sleep_slow(bar, parity, w) : mbar_wait_slow<false>(bar, parity, w);
+}
+
+// Copy of one 16-byte chunk at global byte address cs into shared memory at
+// d: the bytes below the row end re (zeros above). Bytes below the operand's
+// base are not read (their slots are shifted out later).
+__device__ __forceinline__ void copy_chunk(uint32_t d, uintptr_t cs, uintptr_t base,
+                                           uintptr_t re, bool row_ok) {
+  if (row_ok && cs < base) {
 #pragma unroll 1
-  for (int c = 0; c < COLS / 64; ++c) {
-    const int n0 = col0 + c * 64 + 2 * lane;
-    uint32_t v[N];
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-      const int k = k0 + part + i * kSoftWarps;
-      v[i] = ld_pair(src, static_cast<int64_t>(k) * ld, n0, ncols, k < K);
+    for (int p = 0; p < 16; p += 2) {
+      const uintptr_t a = cs + p;
+      sts16(d + p, a >= base && a < re ? __ldg(reinterpret_cast<const uint16_t*>(a))
+                                       : static_cast<uint16_t>(0));
     }
+    return;
+  }
+  const uint32_t bytes =
+      !row_ok || cs >= re ? 0u : re - cs >= 16 ? 16u : static_cast<uint32_t>(re - cs);
+  cp_async_16(d, bytes ? reinterpret_cast<const void*>(cs) : g_zero_chunk, bytes);
+}
+
+// Bytes sh .. sh + 15 of the 32 bytes X, Y, sh = 4 Q + fs / 8 (fs 0 or 16).
+template <int Q>
+__device__ __forceinline__ uint4 shift_chunk(const uint4& X, const uint4& Y, uint32_t fs) {
+  const uint32_t w[8] = {X.x, X.y, X.z, X.w, Y.x, Y.y, Y.z, Y.w};
+  return make_uint4(__funnelshift_r(w[Q], w[Q + 1], fs), __funnelshift_r(w[Q + 1], w[Q + 2], fs),
+                    __funnelshift_r(w[Q + 2], w[Q + 3], fs),
+                    __funnelshift_r(w[Q + 3], w[Q + 4], fs));
+}
+
+// One operand's share of a stage for loader warp `part`. K-major (KMAJ): E
+// tile rows from r0 (matrix rows r0 + part + 8 s) by 64 k from c0, segment s
+// in smem row part + 8 s. MN-major: E / 64 boxes of 64 columns by 64 k rows
+// (8 KB each); segment s is k row r0 + part + 8 (s % 8) of box s / 8,
+// columns c0 + 64 (s / 8) ...
+// Lane l copies chunk j = l % 8 of segments 4 t + l / 8, t = 0 .. NSEG / 4 - 1:
+// relative to the lane's first segment, iteration t is rows_t(t) matrix rows,
+// cols_t(t) elements and smem_t(t) shared bytes further on.
+template <bool KMAJ, int E>
+struct SoftOperand {
+  static constexpr int NSEG = E / kSoftWarps;
+  static constexpr int T = NSEG / 4;
+  static constexpr int COLS = KMAJ ? 64 : E;  // elements of a stage's row span
+  __device__ __forceinline__ static constexpr int rows_t(int t) { return KMAJ ? 32 * t : 32 * (t & 1); }
+  __device__ __forceinline__ static constexpr int cols_t(int t) { return KMAJ ? 0 : 64 * (t >> 1); }
+  __device__ __forceinline__ static constexpr uint32_t smem_t(int t) {
+    return KMAJ ? 4096u * t : 4096u * (t & 1) + 8192u * (t >> 1);
+  }
+  // segment s of the side chunks: rows and columns past the warp's first
+  __device__ __forceinline__ static int rows_s(int s) { return KMAJ ? 8 * s : 8 * (s & 7); }
+  __device__ __forceinline__ static int cols_s(int s) { return KMAJ ? 0 : 64 * (s >> 3); }
+
+  const uint16_t* src;
+  int64_t ld;
+  int r0, c0, nrows, ncols, part;
+  uint32_t dst;  // shared address of the operand tile
+
+  // Global byte address of the warp's first segment's first element.
+  __device__ __forceinline__ uintptr_t first() const {
+    return reinterpret_cast<uintptr_t>(src) +
+           2 * static_cast<uintptr_t>(static_cast<int64_t>(r0 + part) * ld + c0);
+  }
+  __device__ __forceinline__ int shift() const { return static_cast<int>(first() & 15); }
+
+  // Every row of the warp's segments is in the matrix, every chunk they need
+  // lies in its row, and none starts below the operand's base.
+  __device__ __forceinline__ bool interior(int sh) const {
+    const int last_row = r0 + part + (KMAJ ? 8 * (NSEG - 1) : 56);
+    return last_row < nrows && 2 * (c0 + COLS) - sh + (sh ? 16 : 0) <= 2 * ncols &&
+           first() - sh >= reinterpret_cast<uintptr_t>(src);
+  }
+
+  __device__ __forceinline__ void issue(uint32_t side, int lane) const {
+    const int sh = shift();
+    const int j = lane & 7, s4 = lane >> 3;
+    const uint32_t d = dst + (part + kSoftWarps * s4) * 128 + ((j ^ part) << 4);
+    const uintptr_t rstep = 2 * static_cast<uintptr_t>(ld);
+    if (interior(sh)) {
+      // Whole 16-byte chunks, no bounds to check.
+      const uintptr_t p = first() - sh + 16 * j + (kSoftWarps * s4) * rstep;
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-      const int kr = part + i * kSoftWarps;
-      *reinterpret_cast<uint32_t*>(dst + c * (64 * H::BK * 2) + kr * 128 +
-                                   ((((lane >> 2) ^ (kr & 7)) & 7) << 4) + word) = v[i];
+      for (int t = 0; t < T; ++t)
+        cp_async_16(d + smem_t(t),
+                    reinterpret_cast<const void*>(p + rows_t(t) * rstep + 2 * cols_t(t)), 16);
+      if (sh) {
+#pragma unroll
+        for (int u = 0; u < (NSEG + 31) / 32; ++u) {
+          const int s = 32 * u + lane;
+          if (s < NSEG)
+            cp_async_16(side + 128 * s,
+                        reinterpret_cast<const void*>(first() - sh + 128 + rows_s(s) * rstep +
+                                                      2 * cols_s(s)),
+                        16);
+        }
+      }
+      return;
+    }
+    // Edge of the matrix: chunk by chunk, bounded by the row's end.
+    const uintptr_t base = reinterpret_cast<uintptr_t>(src);
+    const int row1 = r0 + part + kSoftWarps * s4;
+    const uintptr_t rs1 = base + 2 * static_cast<uintptr_t>(static_cast<int64_t>(row1) * ld);
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      const int row = row1 + rows_t(t);
+      const uintptr_t rs = rs1 + rows_t(t) * rstep;
+      const uintptr_t cs = ((rs + 2 * static_cast<uintptr_t>(c0 + cols_t(t))) & ~uintptr_t(15)) + 16 * j;
+      copy_chunk(d + smem_t(t), cs, base, rs + 2 * static_cast<uintptr_t>(ncols), row < nrows);
+    }
+    if (sh) {
+#pragma unroll
+      for (int u = 0; u < (NSEG + 31) / 32; ++u) {
+        const int s = 32 * u + lane;
+        if (s < NSEG) {
+          const int row = r0 + part + rows_s(s);
+          const uintptr_t rs = base + 2 * static_cast<uintptr_t>(static_cast<int64_t>(row) * ld);
+          const uintptr_t cs = ((rs + 2 * static_cast<uintptr_t>(c0 + cols_s(s))) & ~uintptr_t(15)) + 128;
+          copy_chunk(side + 128 * s, cs, base, rs + 2 * static_cast<uintptr_t>(ncols), row < nrows);
+        }
+      }
     }
   }
-}
+
+  // Chunks of RB iterations are read before any is rewritten, so that their
+  // shared-memory latencies overlap.
+  template <int Q>
+  __device__ __forceinline__ void realign_q(uint32_t side, int lane, uint32_t fs) const {
+    constexpr int RB = T < 8 ? T : 8;
+    const int j = lane & 7, s4 = lane >> 3;
+    const uint32_t rowb = dst + (part + kSoftWarps * s4) * 128;
+    const uint32_t dx = rowb + ((j ^ part) << 4);
+    const uint32_t dy = rowb + (((j + 1) ^ part) << 4);
+    const uint32_t ds = side + 128 * s4;
+#pragma unroll
+    for (int t0 = 0; t0 < T; t0 += RB) {
+      uint4 X[RB], Y[RB];
+#pragma unroll
+      for (int u = 0; u < RB; ++u) {
+        X[u] = lds128u(dx + smem_t(t0 + u));
+        Y[u] = lds128u(j < 7 ? dy + smem_t(t0 + u) : ds + 512 * (t0 + u));
+      }
+      __syncwarp();  // every lane has read its chunks before any is overwritten
+#pragma unroll
+      for (int u = 0; u < RB; ++u) sts128u(dx + smem_t(t0 + u), shift_chunk<Q>(X[u], Y[u], fs));
+    }
+  }
+
+  // After every lane's copies of the stage have landed (and a __syncwarp).
+  __device__ __forceinline__ void realign(uint32_t side, int lane) const {
+    const int sh = shift();
+    const uint32_t fs = 8u * static_cast<uint32_t>(sh & 3);
+    switch (sh >> 2) {
+      case 0: if (sh) realign_q<0>(side, lane, fs); break;
+      case 1: realign_q<1>(side, lane, fs); break;
+      case 2: realign_q<2>(side, lane, fs); break;
+      default: realign_q<3>(side, lane, fs); break;
+    }
+  }
+};
 
 // Loader warp `part`'s share of one stage. A stored M x K is K-major, stored
 // K x M (transa) MN-major; B stored K x N is MN-major, stored N x K (transb)
-// K-major.
+// K-major. side: the stage's side buffer, one 128-byte row per segment index
+// ((BM + BN) / 8 rows: A's segments, then B's), in which warp `part` owns the
+// 16 bytes at 16 part; so a segment's ninth chunk sits in the one bank group
+// the other seven lanes of its quarter-warp do not read in the realignment.
 template <int BM, int BN>
-__device__ __forceinline__ void soft_load_stage(uint8_t* a_st, const GemmArgs& args, int tm,
-                                                int tn, int kb, int lane, int part) {
-  const uint16_t* A = static_cast<const uint16_t*>(args.A);
-  const uint16_t* B = static_cast<const uint16_t*>(args.B);
-  uint8_t* b_st = a_st + BM * H::BK * 2;
-  const int k0 = kb * H::BK;
-  if (args.transa)
-    soft_mnmajor<BM>(a_st, A, args.lda, tm * BM, args.M, k0, args.K, lane, part);
-  else
-    soft_kmajor<BM>(a_st, A, args.lda, tm * BM, args.M, k0, args.K, lane, part);
-  if (args.transb)
-    soft_kmajor<BN>(b_st, B, args.ldb, tn * BN, args.N, k0, args.K, lane, part);
-  else
-    soft_mnmajor<BN>(b_st, B, args.ldb, tn * BN, args.N, k0, args.K, lane, part);
-}
+struct SoftStage {
+  static constexpr int A_BYTES = BM * H::BK * 2;
+  static constexpr int SIDE_BYTES = (BM + BN) / kSoftWarps * 128;  // one stage, all warps
+  template <class F>
+  __device__ __forceinline__ static void each(const GemmArgs& args, uint32_t a_st, int tm, int tn,
+                                              int kb, int part, uint32_t side, F&& f) {
+    const uint16_t* A = static_cast<const uint16_t*>(args.A);
+    const uint16_t* B = static_cast<const uint16_t*>(args.B);
+    const uint32_t b_st = a_st + A_BYTES;
+    const uint32_t side_b = side + BM / kSoftWarps * 128;
+    const int k0 = kb * H::BK;
+    if (args.transa)
+      f(SoftOperand<false, BM>{A, args.lda, k0, tm * BM, args.K, args.M, part, a_st}, side);
+    else
+      f(SoftOperand<true, BM>{A, args.lda, tm * BM, k0, args.M, args.K, part, a_st}, side);
+    if (args.transb)
+      f(SoftOperand<true, BN>{B, args.ldb, tn * BN, k0, args.N, args.K, part, b_st}, side_b);
+    else
+      f(SoftOperand<false, BN>{B, args.ldb, k0, tn * BN, args.K, args.N, part, b_st}, side_b);
+  }
+  __device__ __forceinline__ static void issue(const GemmArgs& args, uint32_t a_st, int tm, int tn,
+                                               int kb, int lane, int part, uint32_t side) {
+    each(args, a_st, tm, tn, kb, part, side,
+         [&](const auto& op, uint32_t sd) { op.issue(sd, lane); });
+  }
+  __device__ __forceinline__ static void realign(const GemmArgs& args, uint32_t a_st, int tm,
+                                                 int tn, int kb, int lane, int part,
+                                                 uint32_t side) {
+    each(args, a_st, tm, tn, kb, part, side,
+         [&](const auto& op, uint32_t sd) { op.realign(sd, lane); });
+  }
+};
 
 // Stream-K fixup: a tile's owner reads the partial sums of its later workers
 // kPre at a time. Workspace slot cw holds worker cw's BM x BN partial tile,
@@ -206,9 +402,10 @@ __device__ __forceinline__ void add_partials(uint32_t (&r)[32], const float4 (&p
 // args; without it the kernel is compiled for untransposed operands and a
 // plain store of C (the software-loader variants are always general).
 // Threads of a variant: the six warps of the roles, plus the software
-// loader's extra warps (6 ..) when operands are not read by TMA.
+// loader's eight warps (6 .. 13) when operands are not read by TMA (warp 0,
+// TMA's producer, then has no role).
 template <bool kTma>
-constexpr int tc_threads() { return kTma ? H::THREADS : H::THREADS + 32 * (kSoftWarps - 1); }
+constexpr int tc_threads() { return kTma ? H::THREADS : H::THREADS + 32 * kSoftWarps; }
 
 template <int BM, int BN, bool kTma, bool kSK, bool kGeneral>
 __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
@@ -219,6 +416,7 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
   const int transa = kGeneral ? args.transa : 0;
   const int transb = kGeneral ? args.transb : 0;
   static_assert(BM == 64 || BM == 128, "tile rows");
+  static_assert(kTma || kGeneral, "software-loader variants are general");
   constexpr int STAGES = H::stages(BN, BM);
   constexpr int A_BYTES = BM * H::BK * 2;      // 16 KB (BM 128) or 8 KB (BM 64)
   constexpr int B_BYTES = H::BK * BN * 2;      // BN/64 boxes of 8 KB
@@ -302,12 +500,50 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
     }
   };
 
-  if (warp == 0 || warp >= 6) {
+  if (kTma ? warp == 0 : warp >= 6) {
     // ------------------------------------------------------------ producer
     // Segment by segment; a segment's tile coordinates are computed once.
-    // Software loader: warps 0 and 6 .. each fill their share of every stage.
+    // Software loader: warps 6 .. 13 each fill their share of every stage,
+    // DEPTH stages in flight (warp 0 has no role in these variants).
     if (!kTma) {
-      const int part = warp == 0 ? 0 : warp - 5;
+      using SS = SoftStage<BM, BN>;
+      // Stages a loader warp keeps in flight: all but the one the MMA reads,
+      // as far as the side buffers fit in the epilogue staging they reuse.
+      constexpr int DEPTH = (STAGES - 1) * SS::SIDE_BYTES <= H::out_bytes(BM)
+                                ? STAGES - 1
+                                : H::out_bytes(BM) / SS::SIDE_BYTES;
+      static_assert(DEPTH >= 2, "software loader depth");
+      const int part = warp - 6;
+      const uint32_t tiles_u = smem_u32(tiles);
+      // The software-loader variants are general (no TMA-store epilogue): the
+      // epilogue staging holds the side chunks of the stages in flight.
+      const uint32_t side_u = smem_u32(out_stage) + 16 * part;
+      constexpr uint32_t SIDE_STAGE = SS::SIDE_BYTES;
+      // Stages in flight, oldest first: tile (tm, tn) and k block (< 0: the
+      // stage is not loaded and not announced).
+      int q_tm[DEPTH] = {}, q_tn[DEPTH] = {}, q_kb[DEPTH] = {};
+      int q_n = 0;
+      uint32_t done_it = 0;
+      // The oldest stage's copies have landed (every lane waited, then the
+      // warp synchronised): realign, fence the generic-proxy writes for
+      // tcgen05.mma, announce.
+      auto complete_oldest = [&]() {
+        const uint32_t s = done_it % STAGES;
+        if (q_kb[0] >= 0) {
+          SS::realign(args, tiles_u + s * STAGE_BYTES, q_tm[0], q_tn[0], q_kb[0], lane, part,
+                      side_u + (done_it % DEPTH) * SIDE_STAGE);
+          fence_proxy_async_smem();
+          mbar_arrive(&sm.full[s]);
+        }
+#pragma unroll
+        for (int j = 0; j + 1 < DEPTH; ++j) {
+          q_tm[j] = q_tm[j + 1];
+          q_tn[j] = q_tn[j + 1];
+          q_kb[j] = q_kb[j + 1];
+        }
+        --q_n;
+        ++done_it;
+      };
       bool ok = true;
       for (int seg = 0; seg < n_seg && ok; ++seg) {
         int tile, kb0, kb1, kind, tm, tn;
@@ -320,12 +556,29 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
           got = __shfl_sync(0xffffffffu, got, 0);
           if (!got) { ok = false; break; }
           // Failure-detection tests: the first stage is never loaded.
-          if (args.fault == kFaultSkipFirstStage && prod_it == 0) continue;
-          soft_load_stage<BM, BN>(tiles + s * STAGE_BYTES, args, tm, tn, kb, lane, part);
-          fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
-          mbar_arrive(&sm.full[s]);
+          const bool skip = args.fault == kFaultSkipFirstStage && prod_it == 0;
+          if (!skip)
+            SS::issue(args, tiles_u + s * STAGE_BYTES, tm, tn, kb, lane, part,
+                      side_u + (prod_it % DEPTH) * SIDE_STAGE);
+          cp_async_commit();
+#pragma unroll
+          for (int j = 0; j < DEPTH; ++j) {
+            if (j == q_n) {
+              q_tm[j] = tm;
+              q_tn[j] = tn;
+              q_kb[j] = skip ? -1 : kb;
+            }
+          }
+          if (++q_n == DEPTH) {
+            cp_async_wait<DEPTH - 1>();
+            __syncwarp();
+            complete_oldest();
+          }
         }
       }
+      cp_async_wait<0>();
+      __syncwarp();
+      while (q_n > 0) complete_oldest();
     } else if (lane == 0) {
       bool ok = true;
       for (int seg = 0; seg < n_seg && ok; ++seg) {
@@ -373,12 +626,12 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
         segment(seg, tile, kb0, kb1, kind);
         const int b = seg & 1;
         const uint32_t aph = (seg >> 1) & 1;
-        if (!mbar_wait(&sm.acc_empty[b], aph ^ 1, wc)) break;
+        if (!role_wait<!kTma>(&sm.acc_empty[b], aph ^ 1, wc)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-          if (!mbar_wait(&sm.full[s], ph, wc)) { ok = false; break; }
+          if (!role_wait<!kTma>(&sm.full[s], ph, wc)) { ok = false; break; }
           tc_fence_after_sync();
           const uint32_t a_addr = smem_u32(tiles + s * STAGE_BYTES);
           const uint32_t b_addr = a_addr + A_BYTES;
@@ -395,7 +648,7 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
         tc_commit(&sm.acc_full[b]);
       }
     }
-  } else {
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     // This thread's row within the tile: lane l of the quarter for BM 128;
@@ -414,7 +667,7 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
       const uint32_t aph = (seg >> 1) & 1;
       // One lane waits; the warp then proceeds converged (tcgen05.ld is .sync.aligned).
       int got = 1;
-      if (lane == 0) got = mbar_wait(&sm.acc_full[b], aph, wc) ? 1 : 0;
+      if (lane == 0) got = role_wait<!kTma>(&sm.acc_full[b], aph, wc) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
       if (kSK && kind == kSegHead) {
@@ -445,7 +698,7 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
         // HEAD: fetch the first (up to) kPre contributors' partials of this
         // chunk before the TMEM read, all loads in flight at once, so that
         // their latencies overlap each other and the TMEM read's.
-        // (the software-loader variants, whose 416 threads allow 157 registers
+        // (the software-loader variants, whose 448 threads allow 146 registers
         // each, prefetch one partial at a time)
         constexpr int NP = kTma ? kPre : 1;
         float4 pre[NP][8];

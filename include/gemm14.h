@@ -14,6 +14,10 @@
  * dimensions are counted in elements: lda >= K, ldb >= N, ldc >= N (each at
  * least 1). C is overwritten (alpha, beta and stored transposes: see
  * gemm14_gemm_ex); A and B are only read. C must not overlap A or B.
+ * Reads of A and B stay inside each one's storage span, from its first
+ * element to the last element of its last row; the 16-bit software loader
+ * (operands TMA cannot address) may read padding elements between rows inside
+ * that span, whose values it does not use.
  *
  * Pointers are DEVICE pointers in the current CUDA device's address space
  * (e.g. torch CUDA tensors' data_ptr()). `stream` is a cudaStream_t (NULL =

@@ -117,3 +117,14 @@ def test_one_thread_oracle_sample():
     number of rows, the whole product when it fits."""
     f, t, rows, threads = bench.time_oracle_sample("f32_256", 0.5, threads=1)
     assert threads == 1 and rows == 256 and f == 2 * 256 ** 3 and t > 0
+
+
+def test_software_loader_table_shapes_break_tma_rules():
+    """Every shape of the software-loader table gives at least one operand a
+    pitch that is not a multiple of 8 elements or a base off 16 bytes, so the
+    plain call cannot use TMA; the reference run rounds both pitches up to 8."""
+    for name, M, N, K, ta, tb, xa, xb, off in bench.SOFT_SHAPES:
+        ac = M if ta else K
+        bc = K if tb else N
+        assert (ac + xa) % 8 or (bc + xb) % 8 or (2 * off) % 16, name
+        assert min(M, N, K) > 0
