@@ -175,6 +175,14 @@ struct SgemmShape {
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
   // + barriers, schedule table and the loaders' cursors (20 B per thread) + align slack
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 512 + 20 * THREADS + 1024;
+  // B stored N x K read by TMA (layout bit 1): each stage's B tile is
+  // transposed in shared memory into one of two [k][n] buffers, and the ring
+  // has one stage fewer to make room for them.
+  static constexpr int BT_BYTES = BK * BN * 4;
+  static constexpr int stages(int lay) { return (lay & 2) ? STAGES - 1 : STAGES; }
+  static constexpr int smem_bytes(int lay) {
+    return stages(lay) * STAGE_BYTES + ((lay & 2) ? 2 * BT_BYTES : 0) + 512 + 20 * THREADS + 1024;
+  }
 };
 
 // Loader: TMA tensor maps (A box 32 x 128 with 128-byte swizzle, B box

@@ -60,6 +60,7 @@ __device__ __forceinline__ void fma2(uint64_t& d, uint64_t a, uint64_t b) {
 struct SgemmSmem {
   uint64_t full[S::STAGES];
   uint64_t empty[S::STAGES];
+  uint64_t bt_ready[2];  // B stored N x K: transposed buffer b holds the current stage
   int abort_flag;
   SkTable sched;  // this CTA's segments, decoded once
   // The loaders' position in the schedule (touched once per k-block, kept out
@@ -100,7 +101,7 @@ __device__ __forceinline__ void issue_stage(uint32_t j, int tile, int kb, const 
   if (args.fault == kFaultSkipFirstStage && j == 0) return;
   int tm, tn;
   grid.coords(tile, tm, tn);
-  const uint32_t s = j % S::STAGES;
+  const uint32_t s = j % S::stages(kLay);
   uint8_t* a_st = tiles + s * S::STAGE_BYTES;
   if (kTma) {
     // called by thread 0 only
@@ -166,32 +167,26 @@ __device__ __forceinline__ void issue_stage(uint32_t j, int tile, int kb, const 
 
 // Shared-memory layouts of the TMA loader for stored transposes. kLay bit 0:
 // A is M-major ([32 k][128 m], 512-byte rows, as TMA writes A stored K x M);
-// bit 1: B is K-major ([256 n][32 k], 128-byte rows with the 128-byte swizzle,
-// as TMA writes B stored N x K). The thread mapping follows the layout so
-// that shared loads stay 16 (or 8) bytes wide and conflict-free:
+// bit 1: B arrives K-major ([256 n][32 k], 128-byte rows with the 128-byte
+// swizzle, as TMA writes B stored N x K) and is transposed in shared memory
+// into the [k][n] layout of B stored K x N before the FMAs read it. The
+// thread mapping follows A's layout so that shared loads stay 16 bytes wide
+// and conflict-free:
 //   rows    M-major A: warp_m*32 + tr*8 + i (8 contiguous rows per thread),
 //           else warp_m*32 + tr + 4i;
-//   columns K-major B: warp_n*128 + tc + 8j (16 columns 8 apart: the 8
-//           threads of a row group read 8 rows with distinct swizzled
-//           chunks), else warp_n*128 + 4tc + 32(j/4) + j%4.
+//   columns warp_n*128 + 4tc + 32(j/4) + j%4.
 // Accumulator pair p of row i holds columns j = 2p and 2p + 1.
 template <int kLay>
 struct Lay {
   static constexpr bool AM = (kLay & 1) != 0;
-  static constexpr bool BK = (kLay & 2) != 0;
   static __device__ __forceinline__ int row(int warp_m, int tr, int i) {
     return AM ? warp_m * 32 + tr * 8 + i : warp_m * 32 + tr + 4 * i;
   }
   static __device__ __forceinline__ int col(int warp_n, int tc, int j) {
-    return BK ? warp_n * 128 + tc + 8 * j : warp_n * 128 + tc * 4 + 32 * (j >> 2) + (j & 3);
+    return warp_n * 128 + tc * 4 + 32 * (j >> 2) + (j & 3);
   }
 };
 
-__device__ __forceinline__ float2 lds64(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ float comp4(const float4& v, int q) {
   return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
@@ -199,8 +194,7 @@ __device__ __forceinline__ float comp4(const float4& v, int q) {
 // Four k (group kg of a 32-deep k-block) of the 8 x 16 register tile from a
 // stage in layout kLay: per k, 8 A values (two 16-byte loads for M-major A,
 // else from 16-byte loads along k), 8 column pairs of B (four 16-byte loads
-// along n, or for K-major B sixteen 8-byte loads of two k per column, paired
-// per k), and 64 packed fp32x2 FMAs.
+// along n), and 64 packed fp32x2 FMAs.
 template <int kLay>
 __device__ __forceinline__ void fma_kgroup(uint32_t a_base, uint32_t b_base, int kg, int warp_m,
                                            int warp_n, int tr, int tc, uint64_t (&acc2)[8][8]) {
@@ -223,60 +217,61 @@ __device__ __forceinline__ void fma_kgroup(uint32_t a_base, uint32_t b_base, int
     }
   }
 #pragma unroll
-  for (int kh = 0; kh < 2; ++kh) {
-    float2 bc[16];  // K-major B: column j's values at k = 4kg + 2kh + {0, 1}
-    if (LY::BK) {
-      const uint32_t b0 = b_base + static_cast<uint32_t>((warp_n * 128 + tc) * 128 +
-                                                         (((kg ^ tc) & 7) << 4) + kh * 8);
+  for (int kk = 0; kk < 4; ++kk) {
+    uint64_t bp[8];
+    const uint32_t b0 = b_base + static_cast<uint32_t>((4 * kg + kk) * (S::BN * 4) +
+                                                       (warp_n * 128 + tc * 4) * 4);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) bc[j] = lds64(b0 + static_cast<uint32_t>(j * 8 * 128));
+    for (int jj = 0; jj < 4; ++jj) {
+      const float4 v = lds128(b0 + static_cast<uint32_t>(128 * jj));
+      bp[2 * jj] = pack2(v.x, v.y);
+      bp[2 * jj + 1] = pack2(v.z, v.w);
     }
 #pragma unroll
-    for (int kx = 0; kx < 2; ++kx) {
-      const int kk = 2 * kh + kx;
-      uint64_t bp[8];
-      if (LY::BK) {
+    for (int i = 0; i < 8; ++i) {
+      const float av = LY::AM ? comp4(af[2 * kk + (i >> 2)], i & 3) : comp4(af[i], kk);
+      const uint64_t a2 = pack2(av, av);
 #pragma unroll
-        for (int p = 0; p < 8; ++p)
-          bp[p] = pack2(kx ? bc[2 * p].y : bc[2 * p].x, kx ? bc[2 * p + 1].y : bc[2 * p + 1].x);
-      } else {
-        const uint32_t b0 = b_base + static_cast<uint32_t>((4 * kg + kk) * (S::BN * 4) +
-                                                           (warp_n * 128 + tc * 4) * 4);
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const float4 v = lds128(b0 + static_cast<uint32_t>(128 * jj));
-          bp[2 * jj] = pack2(v.x, v.y);
-          bp[2 * jj + 1] = pack2(v.z, v.w);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float av = LY::AM ? comp4(af[2 * kk + (i >> 2)], i & 3) : comp4(af[i], kk);
-        const uint64_t a2 = pack2(av, av);
-#pragma unroll
-        for (int p = 0; p < 8; ++p) fma2(acc2[i][p], a2, bp[p]);
-      }
+      for (int p = 0; p < 8; ++p) fma2(acc2[i][p], a2, bp[p]);
     }
   }
 }
 
+// One k-block: A from the stage, B ([k][n], 1 KB rows) at b_base.
 template <int kLay>
-__device__ __forceinline__ void fma_kblock(const uint8_t* stage, int warp_m, int warp_n, int tr,
-                                           int tc, uint64_t (&acc2)[8][8]) {
+__device__ __forceinline__ void fma_kblock(const uint8_t* stage, uint32_t b_base, int warp_m,
+                                           int warp_n, int tr, int tc, uint64_t (&acc2)[8][8]) {
   const uint32_t a_base = smem_u32(stage);
-  const uint32_t b_base = a_base + S::A_STAGE_BYTES;
-  if constexpr (Lay<kLay>::BK) {
-    // K-major B holds 32 fragment registers per k pair: unrolled, the k
-    // groups' live ranges overlap and it measured 20-25 % slower
-#pragma unroll 1
-    for (int kg = 0; kg < S::BK / 4; ++kg)
-      fma_kgroup<kLay>(a_base, b_base, kg, warp_m, warp_n, tr, tc, acc2);
-  } else {
-    // fully unrolled: the next k group's shared loads overlap this one's
-    // FMAs (5.7 % faster than unrolling by 2, no spills)
+  // fully unrolled: the next k group's shared loads overlap this one's FMAs
+  // (5.7 % faster than unrolling by 2, no spills)
 #pragma unroll
-    for (int kg = 0; kg < S::BK / 4; ++kg)
-      fma_kgroup<kLay>(a_base, b_base, kg, warp_m, warp_n, tr, tc, acc2);
+  for (int kg = 0; kg < S::BK / 4; ++kg)
+    fma_kgroup<kLay>(a_base, b_base, kg, warp_m, warp_n, tr, tc, acc2);
+}
+
+// B stored N x K as TMA lands it ([256 n][32 k], 128-byte rows, 16-byte chunk
+// c of row n at chunk c XOR (n % 8)) into bt as [32 k][256 n], the layout of
+// B stored K x N. Thread t moves row n = t: eight 16-byte loads (a quarter
+// warp reads 8 rows' distinct chunks) and 32 4-byte stores (a warp writes
+// 128 contiguous bytes of a k row).
+__device__ __forceinline__ void transpose_b(uint32_t b_st, uint32_t bt) {
+  const int n = threadIdx.x;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float4 v[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      v[c] = lds128(b_st + static_cast<uint32_t>(n * 128 + ((((4 * h + c) ^ n) & 7) << 4)));
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int k = 4 * (4 * h + c) + q;
+        const float x = comp4(v[c], q);
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(bt + static_cast<uint32_t>((k * S::BN + n) * 4)),
+                     "f"(x)
+                     : "memory");
+      }
   }
 }
 
@@ -291,9 +286,13 @@ __global__ void __launch_bounds__(S::THREADS, 1)
     sgemm_simt_kernel(const __grid_constant__ CUtensorMap map_a,
                       const __grid_constant__ CUtensorMap map_b, const GemmArgs args) {
   static_assert(kLay == 0 || kTma, "transposed layouts come from the TMA loader");
+  constexpr int STG = S::stages(kLay);        // ring stages
+  constexpr bool kBT = (kLay & 2) != 0;      // B transposed in shared memory
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = align1024(smem_raw);
-  SgemmSmem& sm = *reinterpret_cast<SgemmSmem*>(tiles + S::STAGES * S::STAGE_BYTES);
+  const uint32_t bt_base = smem_u32(tiles + STG * S::STAGE_BYTES);  // two [k][n] buffers (kBT)
+  SgemmSmem& sm = *reinterpret_cast<SgemmSmem*>(tiles + STG * S::STAGE_BYTES +
+                                                (kBT ? 2 * S::BT_BYTES : 0));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -306,10 +305,11 @@ __global__ void __launch_bounds__(S::THREADS, 1)
   uint32_t issued = 0;  // iterations whose loads this thread has issued
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S::STAGES; ++s) {
+    for (int s = 0; s < STG; ++s) {
       mbar_init(&sm.full[s], kTma ? 1 : S::THREADS);
       mbar_init(&sm.empty[s], S::WARPS);
     }
+    for (int b = 0; b < 2; ++b) mbar_init(&sm.bt_ready[b], S::THREADS);
     sm.abort_flag = 0;
     if (kSK) {
       sm.sched.fill(args.sk, w);
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(S::THREADS, 1)
   // Prologue: fill the ring (fresh stages need no empty-wait).
   if (producer && n_seg > 0) {
     if (kSK) pcur.start<true>(sm.sched, w, n_seg, L);
-    for (; issued < n_iter && issued < static_cast<uint32_t>(S::STAGES); ++issued) load(issued);
+    for (; issued < n_iter && issued < static_cast<uint32_t>(STG); ++issued) load(issued);
   }
 
   // This thread's rows: warp_m*32 + tr + 4*i (i < 8); columns:
@@ -386,18 +386,32 @@ __global__ void __launch_bounds__(S::THREADS, 1)
       for (int j = 0; j < 8; ++j) acc2[i][j] = 0ull;
 
     for (int kb = kb0; kb < kb1; ++kb, ++it) {
-      const uint32_t s = it % S::STAGES, ph = (it / S::STAGES) & 1;
+      const uint32_t s = it % STG, ph = (it / STG) & 1;
       if (!mbar_wait(&sm.full[s], ph, wc)) { ok = false; break; }
-      fma_kblock<kLay>(tiles + s * S::STAGE_BYTES, warp_m, warp_n, tr, tc, acc2);
+      uint8_t* stage = tiles + s * S::STAGE_BYTES;
+      uint32_t b_base = smem_u32(stage) + S::A_STAGE_BYTES;
+      if (kBT) {
+        // Transpose this stage's B into buffer it % 2; every thread's part
+        // is in before any thread reads it (a bounded wait, not a CTA
+        // barrier: a thread that gave up on a wait leaves the loop). The
+        // buffer's previous contents (iteration it - 2) were read before
+        // each thread arrived here for iteration it - 1.
+        const uint32_t bt = bt_base + (it & 1) * S::BT_BYTES;
+        transpose_b(b_base, bt);
+        mbar_arrive(&sm.bt_ready[it & 1]);
+        if (!mbar_wait(&sm.bt_ready[it & 1], (it >> 1) & 1, wc)) { ok = false; break; }
+        b_base = bt;
+      }
+      fma_kblock<kLay>(stage, b_base, warp_m, warp_n, tr, tc, acc2);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[s]);
 
       // Refill: once every warp is done with iteration it-1, its stage takes
-      // iteration it-1+STAGES (one iteration of slack keeps warp 0 from
-      // waiting on the slowest warp of the current iteration).
-      if (producer && it >= 1 && issued < n_iter && issued == it - 1 + S::STAGES) {
+      // iteration it-1+STG (one iteration of slack keeps warp 0 from waiting
+      // on the slowest warp of the current iteration).
+      if (producer && it >= 1 && issued < n_iter && issued == it - 1 + STG) {
         const uint32_t j = it - 1;
-        if (!mbar_wait(&sm.empty[j % S::STAGES], (j / S::STAGES) & 1, wc)) {
+        if (!mbar_wait(&sm.empty[j % STG], (j / STG) & 1, wc)) {
           ok = false;
           break;
         }
@@ -446,15 +460,9 @@ __global__ void __launch_bounds__(S::THREADS, 1)
                 !slot_ok(srow + LY::col(warp_n, tc, 2 * p + 3), w, 1))
               continue;
 #endif
-            if (LY::BK) {
-              __stcg(srow + LY::col(warp_n, tc, 2 * p), lo.x);
-              __stcg(srow + LY::col(warp_n, tc, 2 * p + 1), lo.y);
-              __stcg(srow + LY::col(warp_n, tc, 2 * p + 2), hi.x);
-              __stcg(srow + LY::col(warp_n, tc, 2 * p + 3), hi.y);
-            } else {  // columns 2p .. 2p+3 are consecutive
-              __stcg(reinterpret_cast<float4*>(srow + LY::col(warp_n, tc, 2 * p)),
-                     make_float4(lo.x, lo.y, hi.x, hi.y));
-            }
+            // columns 2p .. 2p+3 are consecutive
+            __stcg(reinterpret_cast<float4*>(srow + LY::col(warp_n, tc, 2 * p)),
+                   make_float4(lo.x, lo.y, hi.x, hi.y));
           }
         }
       }
@@ -486,36 +494,21 @@ __global__ void __launch_bounds__(S::THREADS, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const float* srow = slot + LY::row(warp_m, tr, i0 + h) * S::BN;
-            if (LY::BK) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
+            for (int jj = 0; jj < 4; ++jj) {
+              const float* q = srow + LY::col(warp_n, tc, 4 * jj);
 #ifdef GEMM14_DEVICE_CHECKS
-                if (!dev_check(slot_span_ok(srow + LY::col(warp_n, tc, j) - args.partials, c,
-                                            S::BM * S::BN, args.sk.G, 1),
-                               args.err)) {
-                  v[h][j] = 0.f;
-                  continue;
-                }
-#endif
-                v[h][j] = __ldcg(srow + LY::col(warp_n, tc, j));
+              if (!dev_check(slot_span_ok(q - args.partials, c, S::BM * S::BN, args.sk.G, 4),
+                             args.err)) {
+                v[h][4 * jj] = v[h][4 * jj + 1] = v[h][4 * jj + 2] = v[h][4 * jj + 3] = 0.f;
+                continue;
               }
-            } else {
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-                const float* q = srow + LY::col(warp_n, tc, 4 * jj);
-#ifdef GEMM14_DEVICE_CHECKS
-                if (!dev_check(slot_span_ok(q - args.partials, c, S::BM * S::BN, args.sk.G, 4),
-                               args.err)) {
-                  v[h][4 * jj] = v[h][4 * jj + 1] = v[h][4 * jj + 2] = v[h][4 * jj + 3] = 0.f;
-                  continue;
-                }
 #endif
-                const float4 t = __ldcg(reinterpret_cast<const float4*>(q));
-                v[h][4 * jj] = t.x;
-                v[h][4 * jj + 1] = t.y;
-                v[h][4 * jj + 2] = t.z;
-                v[h][4 * jj + 3] = t.w;
-              }
+              const float4 t = __ldcg(reinterpret_cast<const float4*>(q));
+              v[h][4 * jj] = t.x;
+              v[h][4 * jj + 1] = t.y;
+              v[h][4 * jj + 2] = t.z;
+              v[h][4 * jj + 3] = t.w;
             }
           }
 #pragma unroll
@@ -548,13 +541,7 @@ __global__ void __launch_bounds__(S::THREADS, 1)
           v[2 * p] = t.x;
           v[2 * p + 1] = t.y;
         }
-        if (LY::BK) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = tn * S::BN + LY::col(warp_n, tc, j);
-            if (col < N) epi_store1<kGeneral>(args, crow + col, v[j]);
-          }
-        } else {
+        {
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const int col = tn * S::BN + LY::col(warp_n, tc, 4 * jj);
@@ -578,10 +565,10 @@ __global__ void __launch_bounds__(S::THREADS, 1)
   if (sm.abort_flag) {
     if (kTma) {
       if (threadIdx.x == 0) {
-        const uint32_t first = issued > S::STAGES ? issued - S::STAGES : 0;
+        const uint32_t first = issued > STG ? issued - STG : 0;
         for (uint32_t j = first; j < issued; ++j)
           if (!(args.fault == kFaultSkipFirstStage && j == 0))
-            mbar_wait_timed(&sm.full[j % S::STAGES], (j / S::STAGES) & 1, 100000000ull);
+            mbar_wait_timed(&sm.full[j % STG], (j / STG) & 1, 100000000ull);
       }
     } else {
       asm volatile("cp.async.wait_all;" ::: "memory");
@@ -594,12 +581,12 @@ cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
                            const GemmArgs& args, int grid, cudaStream_t stream) {
   static DeviceOnce configured;
   const cudaError_t e = set_smem_once(configured, sgemm_simt_kernel<kTma, kSK, kGeneral, kLay>,
-                                      S::SMEM_BYTES);
+                                      S::smem_bytes(kLay));
   if (e != cudaSuccess) return e;
   CUtensorMap dummy{};
   return launch_kernel(sgemm_simt_kernel<kTma, kSK, kGeneral, kLay>, dim3(grid), dim3(S::THREADS),
-                       S::SMEM_BYTES, stream, map_a ? *map_a : dummy, map_b ? *map_b : dummy,
-                       args);
+                       S::smem_bytes(kLay), stream, map_a ? *map_a : dummy,
+                       map_b ? *map_b : dummy, args);
 }
 
 template <bool kTma, bool kSK>

@@ -258,6 +258,10 @@ def test_ex_plan_loaders(lib):
     for ta, tb in ((1, 0), (0, 1), (1, 1)):
         st, p = g14.plan_ex(F32, ta, tb, 2048, 2048, 512, P, 2048, P, 2048, P, 2048, 152)
         assert st == 0 and p.loader == 1 and p.tiles == nn.tiles and p.grid == nn.grid
+        # B stored N x K is transposed in shared memory: two 32 KB buffers take
+        # one ring stage's place
+        assert p.stages == (3 if tb else nn.stages) and p.smem_bytes <= 227 * 1024
+        assert p.smem_bytes == nn.smem_bytes + (32768 * 2 - 49152 if tb else 0)
         st, p = g14.plan_ex(F32, ta, tb, 2048, 2048, 512, P, 2049, P, 2048, P, 2048, 152)
         assert st == 0 and p.loader == 2
         st, p = g14.plan_ex(BF16, ta, tb, 512, 512, 512, P, 512, P, 512, P, 512, 152)

@@ -58,6 +58,23 @@ def test_f32_transposes(oracle_mod, M, N, K, ta, tb):
     assert torch.equal(C2, C_nn)
 
 
+@pytest.mark.parametrize("ta", [0, 1])
+def test_f32_b_stored_nk_transposed_in_shared_memory(oracle_mod, ta):
+    """B stored N x K reaches the 128 x 256 kernel through TMA as K-major tiles,
+    which the CTA transposes in shared memory stage by stage into two
+    alternating buffers. Several tiles per CTA, a ragged k tail (K = 333) and
+    ragged edges; the FMAs then run in the order of B stored K x N, so the
+    product has that call's very bits. Rows sampled against the oracle."""
+    M, N, K = 4100, 2600, 333
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=91 + ta)
+    lda, ldb = pitches(M, N, K, ta, 1, 4)
+    C = run_ex(A, B, ta, 1, lda=lda, ldb=ldb, ldc=rup(N, 4))
+    C_nn = run_ex(A, B, 0, 0, lda=rup(K, 4), ldb=rup(N, 4), ldc=rup(N, 4))
+    assert torch.equal(C, C_nn)
+    rows = torch.arange(0, M, 41)
+    oracle_check_ex(oracle_mod, A[rows].contiguous(), B, C[rows].contiguous())
+
+
 # ------------------------------------------------------------------ bf16 / fp16
 
 TC_SHAPES = [(5, 7, 3), (128, 64, 64), (129, 65, 130), (200, 300, 100), (257, 129, 1000),
