@@ -1124,10 +1124,11 @@ extern "C" int fma_ceiling_run(float* out, int mode, int blocks, int threads, in
 
 
 def run_fma_ceiling(args):
-    """The FFMA throughput a register-only loop reaches on this GPU, packed
-    (fma.rn.f32x2, what the fp32 kernel issues) and scalar, against the
-    unit-count peak (SMs x 128 lanes x 2 FLOP x clock). The loop is compiled
-    here with nvcc into a scratch folder; one JSON line per mode."""
+    """The FFMA throughput register-only loops reach on this GPU against the
+    unit-count peak (SMs x 128 lanes x 2 FLOP x clock): 32 independent chains
+    a thread, packed (fma.rn.f32x2, what the fp32 kernel issues) and scalar,
+    at 16 warps per SM and at the fp32 kernel's 8. Compiled here with nvcc
+    into a scratch folder; one JSON line per case."""
     import ctypes
     import tempfile
 
@@ -1143,9 +1144,11 @@ def run_fma_ceiling(args):
     so = ctypes.CDLL(lib)
     so.fma_ceiling_run.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 4
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    threads, iters = 256, 20000
-    for mode, name in ((0, "packed fma.rn.f32x2"), (1, "scalar fma.rn.f32")):
-        blocks = 2 * sms
+    threads = 256
+    cases = ((0, "packed fma.rn.f32x2", 2, 20000, 32), (1, "scalar fma.rn.f32", 2, 20000, 32),
+             (0, "packed fma.rn.f32x2", 1, 20000, 32), (1, "scalar fma.rn.f32", 1, 20000, 32))
+    for mode, name, per_sm, iters, fma_per_iter in cases:
+        blocks = per_sm * sms
         out = torch.empty(blocks * threads, device="cuda")
         torch.cuda.synchronize()
         assert so.fma_ceiling_run(out.data_ptr(), mode, blocks, threads, 100) == 0
@@ -1159,13 +1162,14 @@ def run_fma_ceiling(args):
         torch.cuda.synchronize()
         clk = clocks.stop()
         ms = e0.elapsed_time(e1)
-        fmas = float(iters) * 32 * (2 if mode == 0 else 1) * blocks * threads
+        fmas = float(iters) * fma_per_iter * (1 if mode == 1 else 2) * blocks * threads
         tflops = 2 * fmas / (ms * 1e-3) / 1e12
         peak = roofline.fp32_alu_peak_tflops()
         print(json.dumps({"fma_ceiling": name, "ms": ms, "tflops": tflops,
                           "unit_count_peak_tflops": peak, "frac_of_unit_count_peak": tflops / peak,
                           "fma_per_clock_per_sm_at_2070": fmas / (ms * 1e-3) / sms / 2.07e9,
-                          "grid": f"{blocks} x {threads} threads, 32 chains each",
+                          "grid": f"{blocks} x {threads} threads ({8 * per_sm} warps per SM), "
+                                  f"{fma_per_iter} chains each",
                           "clocks": clk}), flush=True)
 
 
