@@ -219,14 +219,17 @@ void schedule(const gemm14_plan& plan, int64_t K, int sm_count, void* workspace,
 // A stored M x K: box 64 k x bm m; stored K x M: box 64 m x 64 k (bm / 64
 // loads per stage). B stored K x N: box 64 n x 64 k (bn / 64 loads); stored
 // N x K: box 64 k x bn n. All with the 128-byte swizzle.
+// ma / mb may be null: that operand gets no map (the software loader reads it).
 int make_maps_16(bool bf16, int transa, int transb, int64_t M, int64_t N, int64_t K,
                  const void* A, int64_t lda, const void* B, int64_t ldb, int bm, int bn,
                  CUtensorMap* ma, CUtensorMap* mb) {
   const CUtensorMapDataType tt =
       bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  int st = transa ? make_map(ma, tt, 2, A, K, M, lda, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
-                  : make_map(ma, tt, 2, A, M, K, lda, 64, bm, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st != GEMM14_OK) return st;
+  int st = GEMM14_OK;
+  if (ma)
+    st = transa ? make_map(ma, tt, 2, A, K, M, lda, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
+                : make_map(ma, tt, 2, A, M, K, lda, 64, bm, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != GEMM14_OK || !mb) return st;
   return transb ? make_map(mb, tt, 2, B, N, K, ldb, 64, bn, CU_TENSOR_MAP_SWIZZLE_128B)
                 : make_map(mb, tt, 2, B, K, N, ldb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -485,9 +488,18 @@ int run_gemm(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K,
     plan_for(dtype, transa, transb, M, N, K, A, lda, B, ldb, C, ldc, dev->sm_count, &plan);
   schedule(plan, K, dev->sm_count, workspace, workspace_bytes, args, grid);
   const uint32_t idesc = idesc_f16_f32acc(bf16, plan.bm, plan.bn, transa != 0, transb == 0);
-  if (plan.loader == 2)
-    return finish(launch_hgemm_tc_soft(plan.bm, plan.bn, args, idesc, grid, stream),
+  if (plan.loader != 1) {
+    // software loader for A (loader 3), B (4) or both (2); TMA for the other
+    const int soft = plan.loader == 3 ? 1 : plan.loader == 4 ? 2 : 3;
+    CUtensorMap ma{}, mb{};
+    if (soft != 3 &&
+        (st = make_maps_16(bf16, transa, transb, M, N, K, A, lda, B, ldb, plan.bm, plan.bn,
+                           soft == 1 ? nullptr : &ma, soft == 2 ? nullptr : &mb)) != GEMM14_OK)
+      return st;
+    return finish(launch_hgemm_tc_soft(plan.bm, plan.bn, soft, &ma, &mb, args, idesc, grid,
+                                       stream),
                   "hgemm launch", stream);
+  }
   CUtensorMap ma, mb, mc{};
   if ((st = make_maps_16(bf16, transa, transb, M, N, K, A, lda, B, ldb, plan.bm, plan.bn, &ma,
                          &mb)) != GEMM14_OK)

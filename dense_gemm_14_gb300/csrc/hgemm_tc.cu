@@ -313,13 +313,14 @@ struct SoftOperand {
   }
 };
 
-// Loader warp `part`'s share of one stage. A stored M x K is K-major, stored
-// K x M (transa) MN-major; B stored K x N is MN-major, stored N x K (transb)
+// Loader warp `part`'s share of one stage: the operands of kSoft (bit 0: A,
+// bit 1: B; TMA loads the other). A stored M x K is K-major, stored K x M
+// (transa) MN-major; B stored K x N is MN-major, stored N x K (transb)
 // K-major. side: the stage's side buffer, one 128-byte row per segment index
 // ((BM + BN) / 8 rows: A's segments, then B's), in which warp `part` owns the
 // 16 bytes at 16 part; so a segment's ninth chunk sits in the one bank group
 // the other seven lanes of its quarter-warp do not read in the realignment.
-template <int BM, int BN>
+template <int BM, int BN, int kSoft>
 struct SoftStage {
   static constexpr int A_BYTES = BM * H::BK * 2;
   static constexpr int SIDE_BYTES = (BM + BN) / kSoftWarps * 128;  // one stage, all warps
@@ -331,14 +332,18 @@ struct SoftStage {
     const uint32_t b_st = a_st + A_BYTES;
     const uint32_t side_b = side + BM / kSoftWarps * 128;
     const int k0 = kb * H::BK;
-    if (args.transa)
-      f(SoftOperand<false, BM>{A, args.lda, k0, tm * BM, args.K, args.M, part, a_st}, side);
-    else
-      f(SoftOperand<true, BM>{A, args.lda, tm * BM, k0, args.M, args.K, part, a_st}, side);
-    if (args.transb)
-      f(SoftOperand<true, BN>{B, args.ldb, tn * BN, k0, args.N, args.K, part, b_st}, side_b);
-    else
-      f(SoftOperand<false, BN>{B, args.ldb, k0, tn * BN, args.K, args.N, part, b_st}, side_b);
+    if (kSoft & 1) {
+      if (args.transa)
+        f(SoftOperand<false, BM>{A, args.lda, k0, tm * BM, args.K, args.M, part, a_st}, side);
+      else
+        f(SoftOperand<true, BM>{A, args.lda, tm * BM, k0, args.M, args.K, part, a_st}, side);
+    }
+    if (kSoft & 2) {
+      if (args.transb)
+        f(SoftOperand<true, BN>{B, args.ldb, tn * BN, k0, args.N, args.K, part, b_st}, side_b);
+      else
+        f(SoftOperand<false, BN>{B, args.ldb, k0, tn * BN, args.K, args.N, part, b_st}, side_b);
+    }
   }
   __device__ __forceinline__ static void issue(const GemmArgs& args, uint32_t a_st, int tm, int tn,
                                                int kb, int lane, int part, uint32_t side) {
@@ -401,14 +406,15 @@ __device__ __forceinline__ void add_partials(uint32_t (&r)[32], const float4 (&p
 // kGeneral: stored transposes and the alpha / beta epilogue are read from
 // args; without it the kernel is compiled for untransposed operands and a
 // plain store of C (the software-loader variants are always general).
-// Threads of a variant: the six warps of the roles, plus the software
-// loader's eight warps (6 .. 13) when operands are not read by TMA (warp 0,
-// TMA's producer, then has no role).
-template <bool kTma>
-constexpr int tc_threads() { return kTma ? H::THREADS : H::THREADS + 32 * kSoftWarps; }
+// kSoft: the operands the software loader copies (bit 0: A, bit 1: B); TMA
+// loads the others. Threads of a variant: the six warps of the roles, plus the
+// software loader's eight warps (6 .. 13) when kSoft is not 0 (warp 0, TMA's
+// producer, then loads only the operands TMA can read, or idles).
+template <int kSoft>
+constexpr int tc_threads() { return kSoft == 0 ? H::THREADS : H::THREADS + 32 * kSoftWarps; }
 
-template <int BM, int BN, bool kTma, bool kSK, bool kGeneral>
-__global__ void __launch_bounds__(tc_threads<kTma>(), 1)
+template <int BM, int BN, int kSoft, bool kSK, bool kGeneral>
+__global__ void __launch_bounds__(tc_threads<kSoft>(), 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b,
                     const __grid_constant__ CUtensorMap map_c, const GemmArgs args,
@@ -416,7 +422,12 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
   const int transa = kGeneral ? args.transa : 0;
   const int transb = kGeneral ? args.transb : 0;
   static_assert(BM == 64 || BM == 128, "tile rows");
-  static_assert(kTma || kGeneral, "software-loader variants are general");
+  static_assert(kSoft == 0 || kGeneral, "software-loader variants are general");
+  constexpr bool kTma = kSoft == 0;             // every operand by TMA
+  constexpr bool kTmaPart = kSoft != 3;         // warp 0 issues TMA loads
+  // bytes a stage's TMA loads bring (the operands the software loader leaves)
+  constexpr uint32_t TMA_BYTES = ((kSoft & 1) ? 0u : uint32_t(BM * H::BK * 2)) +
+                                 ((kSoft & 2) ? 0u : uint32_t(H::BK * BN * 2));
   constexpr int STAGES = H::stages(BN, BM);
   constexpr int A_BYTES = BM * H::BK * 2;      // 16 KB (BM 128) or 8 KB (BM 64)
   constexpr int B_BYTES = H::BK * BN * 2;      // BN/64 boxes of 8 KB
@@ -447,7 +458,8 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sm.full[s], kTma ? 1 : 32 * kSoftWarps);
+      // one TMA arrival (with the stage's bytes) and/or every loader thread's
+      mbar_init(&sm.full[s], (kTmaPart ? 1 : 0) + (kSoft ? 32 * kSoftWarps : 0));
       mbar_init(&sm.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -466,10 +478,8 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
       }
     }
     fence_barrier_init();
-    if (kTma) {
-      tma_prefetch_desc(&map_a);
-      tma_prefetch_desc(&map_b);
-    }
+    if (!(kSoft & 1)) tma_prefetch_desc(&map_a);
+    if (!(kSoft & 2)) tma_prefetch_desc(&map_b);
     if (tma_c) tma_prefetch_desc(&map_c);
   }
   if (warp == 1) {
@@ -500,13 +510,14 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
     }
   };
 
-  if (kTma ? warp == 0 : warp >= 6) {
+  if ((kTmaPart && warp == 0) || (kSoft && warp >= 6)) {
     // ------------------------------------------------------------ producer
     // Segment by segment; a segment's tile coordinates are computed once.
-    // Software loader: warps 6 .. 13 each fill their share of every stage,
-    // DEPTH stages in flight (warp 0 has no role in these variants).
-    if (!kTma) {
-      using SS = SoftStage<BM, BN>;
+    // Software loader: warps 6 .. 13 each fill their share of every stage's
+    // kSoft operands, DEPTH stages in flight; warp 0 loads the others by TMA
+    // (or idles when kSoft covers both).
+    if (kSoft && warp >= 6) {
+      using SS = SoftStage<BM, BN, kSoft>;
       // Stages a loader warp keeps in flight: all but the one the MMA reads,
       // as far as the side buffers fit in the epilogue staging they reuse.
       constexpr int DEPTH = (STAGES - 1) * SS::SIDE_BYTES <= H::out_bytes(BM)
@@ -592,9 +603,11 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
           if (args.fault == kFaultSkipFirstStage && prod_it == 0) continue;
           uint8_t* a_st = tiles + s * STAGE_BYTES;
           uint8_t* b_st = a_st + A_BYTES;
-          mbar_arrive_expect_tx(&sm.full[s], STAGE_BYTES);
+          mbar_arrive_expect_tx(&sm.full[s], TMA_BYTES);
           // A: one box of 64 k x BM m, or (stored K x M) BM / 64 boxes of 64 m x 64 k.
-          if (!transa) {
+          if (kSoft & 1) {
+            // the software loader's
+          } else if (!transa) {
             tma_load_2d(a_st, &map_a, kb * H::BK, tm * BM, &sm.full[s]);
           } else {
 #pragma unroll
@@ -603,7 +616,9 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
                           &sm.full[s]);
           }
           // B: BN / 64 boxes of 64 n x 64 k, or (stored N x K) one box of 64 k x BN n.
-          if (!transb) {
+          if (kSoft & 2) {
+            // the software loader's
+          } else if (!transb) {
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
               tma_load_2d(b_st + c * (64 * H::BK * 2), &map_b, tn * BN + c * 64, kb * H::BK,
@@ -626,12 +641,12 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
         segment(seg, tile, kb0, kb1, kind);
         const int b = seg & 1;
         const uint32_t aph = (seg >> 1) & 1;
-        if (!role_wait<!kTma>(&sm.acc_empty[b], aph ^ 1, wc)) break;
+        if (!role_wait<kSoft != 0>(&sm.acc_empty[b], aph ^ 1, wc)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-          if (!role_wait<!kTma>(&sm.full[s], ph, wc)) { ok = false; break; }
+          if (!role_wait<kSoft != 0>(&sm.full[s], ph, wc)) { ok = false; break; }
           tc_fence_after_sync();
           const uint32_t a_addr = smem_u32(tiles + s * STAGE_BYTES);
           const uint32_t b_addr = a_addr + A_BYTES;
@@ -667,7 +682,7 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
       const uint32_t aph = (seg >> 1) & 1;
       // One lane waits; the warp then proceeds converged (tcgen05.ld is .sync.aligned).
       int got = 1;
-      if (lane == 0) got = role_wait<!kTma>(&sm.acc_full[b], aph, wc) ? 1 : 0;
+      if (lane == 0) got = role_wait<kSoft != 0>(&sm.acc_full[b], aph, wc) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
       if (kSK && kind == kSegHead) {
@@ -801,7 +816,7 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
       tc_commit(&sm.drain);
       mbar_wait_timed(&sm.drain, 0, 100000000ull);
     }
-    if (kTma && warp == 0 && lane == 0) {
+    if (kTmaPart && warp == 0 && lane == 0) {
       const uint32_t first = prod_it > STAGES ? prod_it - STAGES : 0;
       for (uint32_t j = first; j < prod_it; ++j)
         if (!(args.fault == kFaultSkipFirstStage && j == 0))
@@ -816,60 +831,64 @@ __global__ void __launch_bounds__(tc_threads<kTma>(), 1)
   }
 }
 
-template <int BM, int BN, bool kTma, bool kSK, bool kGeneral>
+template <int BM, int BN, int kSoft, bool kSK, bool kGeneral>
 cudaError_t launch_variant(const CUtensorMap* map_a, const CUtensorMap* map_b,
                            const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc,
                            int grid, cudaStream_t stream) {
   static DeviceOnce configured;
-  const cudaError_t e = set_smem_once(configured, hgemm_tc_kernel<BM, BN, kTma, kSK, kGeneral>,
+  const cudaError_t e = set_smem_once(configured, hgemm_tc_kernel<BM, BN, kSoft, kSK, kGeneral>,
                                       H::smem_bytes(BN, BM));
   if (e != cudaSuccess) return e;
   CUtensorMap dummy{};
-  return launch_kernel(hgemm_tc_kernel<BM, BN, kTma, kSK, kGeneral>, dim3(grid),
-                       dim3(tc_threads<kTma>()), H::smem_bytes(BN, BM), stream,
+  return launch_kernel(hgemm_tc_kernel<BM, BN, kSoft, kSK, kGeneral>, dim3(grid),
+                       dim3(tc_threads<kSoft>()), H::smem_bytes(BN, BM), stream,
                        map_a ? *map_a : dummy, map_b ? *map_b : dummy, map_c ? *map_c : dummy,
                        args, idesc);
 }
 
-template <int BM, int BN, bool kTma, bool kSK>
+template <int BM, int BN, int kSoft, bool kSK>
 cudaError_t launch_epi(const CUtensorMap* map_a, const CUtensorMap* map_b,
                        const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc, int grid,
                        cudaStream_t stream) {
-  if (!kTma || args.transa || args.transb || args.epi != kEpiStore)
-    return launch_variant<BM, BN, kTma, kSK, true>(map_a, map_b, map_c, args, idesc, grid,
-                                                   stream);
-  return launch_variant<BM, BN, kTma, kSK, kTma ? false : true>(map_a, map_b, map_c, args, idesc,
-                                                                 grid, stream);
+  if (kSoft || args.transa || args.transb || args.epi != kEpiStore)
+    return launch_variant<BM, BN, kSoft, kSK, true>(map_a, map_b, map_c, args, idesc, grid,
+                                                    stream);
+  return launch_variant<BM, BN, kSoft, kSK, kSoft != 0>(map_a, map_b, map_c, args, idesc, grid,
+                                                        stream);
 }
 
-template <int BM, int BN, bool kTma>
+// One operand by software and the other by TMA is compiled for the
+// data-parallel schedule only: a split product whose operand TMA cannot read
+// (its workspace too small to re-pitch it) loads both by software.
+template <int BM, int BN, int kSoft>
 cudaError_t launch_bn(const CUtensorMap* map_a, const CUtensorMap* map_b,
                       const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc, int grid,
                       cudaStream_t stream) {
   if (args.sk.dp_tiles < args.sk.tiles)
-    return launch_epi<BM, BN, kTma, true>(map_a, map_b, map_c, args, idesc, grid, stream);
-  return launch_epi<BM, BN, kTma, false>(map_a, map_b, map_c, args, idesc, grid, stream);
+    return launch_epi<BM, BN, kSoft == 0 ? 0 : 3, true>(map_a, map_b, map_c, args, idesc, grid,
+                                                        stream);
+  return launch_epi<BM, BN, kSoft, false>(map_a, map_b, map_c, args, idesc, grid, stream);
 }
 
-template <int BM, bool kTma>
+template <int BM, int kSoft>
 cudaError_t launch_bm(int bn, const CUtensorMap* map_a, const CUtensorMap* map_b,
                       const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc, int grid,
                       cudaStream_t stream) {
   switch (bn) {
-    case 64: return launch_bn<BM, 64, kTma>(map_a, map_b, map_c, args, idesc, grid, stream);
-    case 128: return launch_bn<BM, 128, kTma>(map_a, map_b, map_c, args, idesc, grid, stream);
-    case 256: return launch_bn<BM, 256, kTma>(map_a, map_b, map_c, args, idesc, grid, stream);
+    case 64: return launch_bn<BM, 64, kSoft>(map_a, map_b, map_c, args, idesc, grid, stream);
+    case 128: return launch_bn<BM, 128, kSoft>(map_a, map_b, map_c, args, idesc, grid, stream);
+    case 256: return launch_bn<BM, 256, kSoft>(map_a, map_b, map_c, args, idesc, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <bool kTma>
+template <int kSoft>
 cudaError_t launch_any(int bm, int bn, const CUtensorMap* map_a, const CUtensorMap* map_b,
                        const CUtensorMap* map_c, const GemmArgs& args, uint32_t idesc, int grid,
                        cudaStream_t stream) {
   switch (bm) {
-    case 64: return launch_bm<64, kTma>(bn, map_a, map_b, map_c, args, idesc, grid, stream);
-    case 128: return launch_bm<128, kTma>(bn, map_a, map_b, map_c, args, idesc, grid, stream);
+    case 64: return launch_bm<64, kSoft>(bn, map_a, map_b, map_c, args, idesc, grid, stream);
+    case 128: return launch_bm<128, kSoft>(bn, map_a, map_b, map_c, args, idesc, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -879,12 +898,18 @@ cudaError_t launch_any(int bm, int bn, const CUtensorMap* map_a, const CUtensorM
 cudaError_t launch_hgemm_tc(int bm, int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
                             const CUtensorMap& map_c, const GemmArgs& args, uint32_t idesc,
                             int grid, cudaStream_t stream) {
-  return launch_any<true>(bm, bn, &map_a, &map_b, &map_c, args, idesc, grid, stream);
+  return launch_any<0>(bm, bn, &map_a, &map_b, &map_c, args, idesc, grid, stream);
 }
 
-cudaError_t launch_hgemm_tc_soft(int bm, int bn, const GemmArgs& args, uint32_t idesc, int grid,
-                                 cudaStream_t stream) {
-  return launch_any<false>(bm, bn, nullptr, nullptr, nullptr, args, idesc, grid, stream);
+cudaError_t launch_hgemm_tc_soft(int bm, int bn, int soft, const CUtensorMap* map_a,
+                                 const CUtensorMap* map_b, const GemmArgs& args, uint32_t idesc,
+                                 int grid, cudaStream_t stream) {
+  switch (soft) {
+    case 1: return launch_any<1>(bm, bn, nullptr, map_b, nullptr, args, idesc, grid, stream);
+    case 2: return launch_any<2>(bm, bn, map_a, nullptr, nullptr, args, idesc, grid, stream);
+    case 3: return launch_any<3>(bm, bn, nullptr, nullptr, nullptr, args, idesc, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace gemm14

@@ -266,9 +266,12 @@ cudaError_t launch_hgemm_tc_pair(const CUtensorMap& map_a, const CUtensorMap& ma
                                  const CUtensorMap& map_b_lo, const GemmArgs& args,
                                  uint32_t idesc, int clusters, bool tf32, cudaStream_t stream);
 
-// Same kernel with the software loader (operands TMA cannot address).
-cudaError_t launch_hgemm_tc_soft(int bm, int bn, const GemmArgs& args, uint32_t idesc, int grid,
-                                 cudaStream_t stream);
+// Same kernel with the software loader for the operands TMA cannot address:
+// soft bit 0 = A, bit 1 = B; the other operand (if any) comes by TMA through
+// its map (map_a / map_b; the software operand's may be null).
+cudaError_t launch_hgemm_tc_soft(int bm, int bn, int soft, const CUtensorMap* map_a,
+                                 const CUtensorMap* map_b, const GemmArgs& args, uint32_t idesc,
+                                 int grid, cudaStream_t stream);
 
 // ---- fp32 inputs on the tensor cores (sgemm_tc3.cu): tcgen05 kind::tf32 on
 // CTA pairs, 256 x 256 tiles. The tensor cores read an fp32 operand as tf32 by

@@ -117,7 +117,10 @@ void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K
     p->smem_bytes = S::smem_bytes(lay);
   } else {
     const int bn = hgemm_bn_for(N);
-    p->loader = (aligned(A, 16) && aligned(B, 16) && lda % 8 == 0 && ldb % 8 == 0) ? 1 : 2;
+    // TMA for each operand it can read; the software loader for the others
+    // (3: A only, 4: B only, 2: both)
+    const bool a_tma = aligned(A, 16) && lda % 8 == 0, b_tma = aligned(B, 16) && ldb % 8 == 0;
+    p->loader = a_tma && b_tma ? 1 : !a_tma && !b_tma ? 2 : !a_tma ? 3 : 4;
     if (p->loader == 1 && M > 128 && N > 128 && g_pair_enabled.load() && sm_count >= 2) {
       // 256 x 256 tiles on CTA pairs; grid = 2 x clusters
       using P = PairShape;

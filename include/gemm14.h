@@ -98,9 +98,10 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const
 /*
  * bf16 inputs (raw bfloat16 bit patterns), fp32 accumulation on the tensor
  * cores (tcgen05), fp32 output. Inputs are rounded to bf16 by the caller.
- * A, B: 2-byte aligned; C: 4-byte aligned. The fast loader (TMA) is used when
- * A and B are 16-byte aligned and lda, ldb are multiples of 8; otherwise a
- * software loader fills the same shared-memory tiles (same results, slower).
+ * A, B: 2-byte aligned; C: 4-byte aligned. The fast loader (TMA) reads each
+ * operand that is 16-byte aligned with a leading dimension that is a multiple
+ * of 8; a software loader fills the same shared-memory tiles for the other
+ * operand(s) (same results, slower).
  * The tensor-core path of "Kernel 优化指南", "Level 4: Tensor Cores (WMMA)"
  * (half-precision inputs, float accumulator), and of gpu-hpc-book ch.06,
  * "Tensor Cores".
@@ -355,7 +356,9 @@ typedef struct gemm14_plan {
                          workspace, only those of at most 2^30 FLOP),
                      0 = no launch */
   int loader;     /* 1 = TMA (kernel 6: 16-byte cp.async), 2 = software loader
-                     (cp.async for fp32; kernel 6: 4-byte cp.async), 0 = none */
+                     (cp.async for fp32; kernel 6: 4-byte cp.async); kernel 2
+                     only: 3 = software loader for A and TMA for B, 4 = TMA for
+                     A and software loader for B; 0 = none */
   int bm, bn, bk; /* output tile rows x columns, k-block depth */
   int stages;     /* shared-memory ring depth */
   int threads;    /* threads per CTA */

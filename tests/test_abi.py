@@ -87,9 +87,14 @@ def test_loader_choice_follows_tma_rules(lib):
     # 16-bit operands: TMA needs 16-byte bases and pitches (multiples of 8 elements)
     st, p = g14.plan(BF16, 4, 8, 4, P, 8, P, 8, P, 8, 152)
     assert st == 0 and p.loader == 1
+    # each operand on its own: 3 = software A and TMA B, 4 = the reverse, 2 = both
     st, p = g14.plan(BF16, 4, 8, 4, P, 12, P, 8, P, 8, 152)
-    assert st == 0 and p.loader == 2
+    assert st == 0 and p.loader == 3
     st, p = g14.plan(F16, 4, 8, 4, P + 8, 8, P, 8, P, 8, 152)
+    assert st == 0 and p.loader == 3
+    st, p = g14.plan(BF16, 4, 8, 4, P, 8, P + 2, 8, P, 8, 152)
+    assert st == 0 and p.loader == 4
+    st, p = g14.plan(BF16, 4, 8, 4, P, 12, P, 9, P, 8, 152)
     assert st == 0 and p.loader == 2
     # an odd byte address is not an element address
     assert g14.gemm_bf16_f32acc(4, 8, 4, P + 1, 8, P, 8, P, 8, None, check=False) == 1
@@ -192,7 +197,7 @@ def test_plan_pair_kernel_for_wide_products(lib, M, N):
         g14.set_pair_kernel(prev)
     # operands TMA cannot address stay on the one-SM kernel with the software loader
     st, p2 = g14.plan(BF16, M, N, 4096, P, 4097, P, ldb, P, N, 152)
-    assert p2.kernel == 2 and p2.loader == 2
+    assert p2.kernel == 2 and p2.loader == (3 if ldb % 8 == 0 else 2)
 
 
 def test_plan_k_zero_launches_nothing(lib):

@@ -4,8 +4,9 @@ shared memory by loader warps in the same swizzled layout the TMA boxes give,
 so the one-SM kernel must return the TMA path's very bits. The cases mix row
 segments that start on either half of a 4-byte word (odd pitches alternate
 them row by row; a 2-byte offset with an even pitch makes them all start on
-the upper half), ragged k and column edges, both tile heights and every
-stored transpose. The tensor-core MMA of the pages' "Tensor Cores" section
+the upper half), ragged k and column edges, both tile heights, every stored
+transpose, and calls where only one operand breaks TMA's rules (TMA loads the
+other in the same stages). The tensor-core MMA of the pages' "Tensor Cores" section
 reads its operand tiles from shared memory in a fixed layout; how the tiles
 get there must not change the product.
 """
@@ -26,8 +27,11 @@ TRANS = [(0, 0), (1, 0), (0, 1), (1, 1)]
 # more tiles than SMs (264 tiles of 128 x 256: CTAs run two tiles in turn)
 SHAPES = [(300, 520, 700), (2100, 1300, 300), (200, 64, 333), (4100, 2100, 200)]
 
-# (extra pitch of A, offset of A, extra pitch of B, offset of B), in elements
-PITCHES = [(1, 0, 3, 0), (2, 1, 1, 1), (3, 1, 2, 0), (6, 0, 5, 1)]
+# (extra pitch of A, offset of A, extra pitch of B, offset of B), in elements;
+# None: that operand on a 16-byte pitch (TMA reads it, the software loader the
+# other one)
+PITCHES = [(1, 0, 3, 0), (2, 1, 1, 1), (3, 1, 2, 0), (6, 0, 5, 1),
+           (None, None, 1, 0), (1, 0, None, None), (None, None, 2, 1), (3, 1, None, None)]
 
 
 def rup(x, m):
@@ -50,8 +54,10 @@ def test_software_loader_gives_the_tma_bits(oracle_mod, M, N, K, ta, tb):
     a_cols, b_cols = (M if ta else K), (K if tb else N)
     C_tma = run_ex(A, B, ta, tb, lda=rup(a_cols, 8), ldb=rup(b_cols, 8))
     for i, (da, oa, db, ob) in enumerate(PITCHES):
-        C = run_ex(A, B, ta, tb, lda=a_cols + da, ldb=b_cols + db, ldc=N + 1, a_off=oa,
-                   b_off=ob, c_off=1)
+        lda = rup(a_cols, 8) if da is None else a_cols + da
+        ldb = rup(b_cols, 8) if db is None else b_cols + db
+        C = run_ex(A, B, ta, tb, lda=lda, ldb=ldb, ldc=N + 1, a_off=oa or 0, b_off=ob or 0,
+                   c_off=1)
         if i == 0:
             oracle_check_ex(oracle_mod, A, B, C, ta, tb)
         assert torch.equal(C, C_tma), (da, oa, db, ob)
