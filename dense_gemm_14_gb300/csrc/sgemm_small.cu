@@ -179,6 +179,8 @@ __device__ __forceinline__ void fma_block(const float* st, int t, uint64_t (&acc
   }
 }
 
+constexpr int kMaxClusterSplit = 8;  // the plan splits a tile over at most 8 CTAs
+
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t cluster_addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -278,17 +280,28 @@ __global__ void __launch_bounds__(Q::THREADS)
     const int r = rank * rows + e / (Q::BN / 4);
     const int c = (e % (Q::BN / 4)) * 4;
     const uint32_t off = static_cast<uint32_t>((r * P_LD + c) * 4);
+    // every rank's value is loaded before the first add, so that the remote
+    // loads' latencies overlap; the sum still runs over ranks 0, 1, ...
+    float4 v[kMaxClusterSplit];
+#pragma unroll
+    for (int q = 0; q < kMaxClusterSplit; ++q)
+      if (q < split) v[q] = ld_dsmem_f4(mapa_shared(p_local + off, static_cast<uint32_t>(q)));
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = 0; q < split; ++q) {
-      const float4 v = ld_dsmem_f4(mapa_shared(p_local + off, static_cast<uint32_t>(q)));
-      s.x += v.x;
-      s.y += v.y;
-      s.z += v.z;
-      s.w += v.w;
+#pragma unroll
+    for (int q = 0; q < kMaxClusterSplit; ++q) {
+      if (q < split) {
+        s.x += v[q].x;
+        s.y += v[q].y;
+        s.z += v[q].z;
+        s.w += v[q].w;
+      }
     }
     store4(args, m0 + r, n0 + c, s);
   }
-  cluster_sync();  // no CTA leaves while another still reads its partial tile
+  // No CTA leaves while another still reads its partial tile. The values read
+  // were all consumed above, so the arrival needs no release ordering.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" :::
+                   "memory");
 }
 
 template <bool kVec>
