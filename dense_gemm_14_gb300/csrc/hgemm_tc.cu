@@ -82,7 +82,7 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
 // before a segment's first element are read only inside the operand (the
 // chunk that holds the operand's first element, when that sits past a
 // 16-byte boundary, is read element by element).
-constexpr int kSoftWarps = 8;  // warps 6 .. 13, two per scheduler; each fills every 8-th row
+constexpr int kSoftWarps = H::SOFT_WARPS;  // warps 6 .. 13, two per scheduler; each fills every 8-th row
 
 __device__ __align__(16) uint32_t g_zero_chunk[4];  // source of zero-byte copies
 
@@ -411,7 +411,7 @@ __device__ __forceinline__ void add_partials(uint32_t (&r)[32], const float4 (&p
 // software loader's eight warps (6 .. 13) when kSoft is not 0 (warp 0, TMA's
 // producer, then loads only the operands TMA can read, or idles).
 template <int kSoft>
-constexpr int tc_threads() { return kSoft == 0 ? H::THREADS : H::THREADS + 32 * kSoftWarps; }
+constexpr int tc_threads() { return kSoft == 0 ? H::THREADS : H::SOFT_THREADS; }
 
 template <int BM, int BN, int kSoft, bool kSK, bool kGeneral>
 __global__ void __launch_bounds__(tc_threads<kSoft>(), 1)

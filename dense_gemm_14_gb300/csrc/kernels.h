@@ -211,6 +211,9 @@ cudaError_t launch_sgemm_small(const GemmArgs& args, bool vec_loads, int split, 
 struct HgemmShape {
   static constexpr int BM = 128, BK = 64;
   static constexpr int THREADS = 6 * 32;  // producer, MMA, 4 epilogue warps
+  // + the software loader's warps when an operand breaks TMA's rules
+  static constexpr int SOFT_WARPS = 8;
+  static constexpr int SOFT_THREADS = THREADS + 32 * SOFT_WARPS;
   static constexpr int stages(int bn, int bm = 128) {
     return bm == 128 ? (bn == 256 ? 4 : bn == 128 ? 6 : 8) : (bn == 256 ? 4 : bn == 128 ? 8 : 12);
   }

@@ -152,7 +152,7 @@ void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K
     p->bn = bn;
     p->bk = HgemmShape::BK;
     p->stages = HgemmShape::stages(bn, bm);
-    p->threads = HgemmShape::THREADS;
+    p->threads = p->loader == 1 ? HgemmShape::THREADS : HgemmShape::SOFT_THREADS;
     p->smem_bytes = HgemmShape::smem_bytes(bn, bm);
   }
   p->tiles = ((M + p->bm - 1) / p->bm) * ((N + p->bn - 1) / p->bn);
