@@ -112,35 +112,44 @@ __device__ __forceinline__ void issue_stage(uint32_t j, int tile, int kb, const 
     if (kLay & 2) tma_load_2d(a_st + S::A_STAGE_BYTES, map_b, kb * S::BK, tn * S::BN, &sm.full[s]);
     else tma_load_2d(a_st + S::A_STAGE_BYTES, map_b, tn * S::BN, kb * S::BK, &sm.full[s]);
   } else {
-    // called by all threads: 4096 A + 8192 B elements, 48 per thread
+    // called by all threads: 4096 A + 8192 B elements, 48 per thread. Each
+    // thread's copies step through memory by a fixed stride and through
+    // shared memory by a fixed offset, so the addresses are kept incrementally
+    // (a few instructions a copy).
     const float* A = static_cast<const float*>(args.A);
     const float* B = static_cast<const float*>(args.B);
     const uint32_t a_sm = smem_u32(a_st);
     const uint32_t b_sm = a_sm + S::A_STAGE_BYTES;
     const int t = threadIdx.x;
     if (!(kGeneral && args.transa)) {
-      const int kl = t & 31;           // k within the block: a warp reads 128 contiguous bytes
+      // k = the thread's lane within the block: a warp reads 128 contiguous
+      // bytes of a row; rows r0, r0 + 8, ... (same swizzle: r % 8 is fixed)
+      const int kl = t & 31, r0 = t >> 5;
       const int k = kb * S::BK + kl;
-      const bool k_ok = k < args.K;
-#pragma unroll 4
-      for (int r = t >> 5; r < S::BM; r += S::THREADS / 32) {
-        const int m = tm * S::BM + r;
-        const bool in = k_ok && m < args.M;
-        cp_async_4(a_sm + a_tile_offset(r, kl),
-                   in ? A + static_cast<int64_t>(m) * args.lda + k : A, in ? 4u : 0u);
+      const int m = tm * S::BM + r0;
+      const int rows_in = k < args.K ? args.M - m : 0;  // copies i with 8 i < rows_in
+      const int64_t step = static_cast<int64_t>(S::THREADS / 32) * args.lda;
+      int64_t off = static_cast<int64_t>(m) * args.lda + k;
+      const uint32_t d0 = a_sm + a_tile_offset(r0, kl);
+#pragma unroll
+      for (int i = 0; i < S::BM / (S::THREADS / 32); ++i, off += step) {
+        const bool in = (S::THREADS / 32) * i < rows_in;
+        cp_async_4(d0 + i * (S::THREADS / 32) * 128, in ? A + off : A, in ? 4u : 0u);
       }
     } else {
       // A stored K x M: 128 threads read 512 contiguous bytes (128 m) of a k
       // row; the swizzle spreads their 4-byte stores over 8 banks.
-      const int ml = t & (S::BM - 1);
+      const int ml = t & (S::BM - 1), kr0 = t / S::BM;
       const int m = tm * S::BM + ml;
-      const bool m_ok = m < args.M;
-#pragma unroll 4
-      for (int kr = t / S::BM; kr < S::BK; kr += S::THREADS / S::BM) {
-        const int k = kb * S::BK + kr;
-        const bool in = m_ok && k < args.K;
-        cp_async_4(a_sm + a_tile_offset(ml, kr),
-                   in ? A + static_cast<int64_t>(k) * args.lda + m : A, in ? 4u : 0u);
+      const int k = kb * S::BK + kr0;
+      const int k_in = m < args.M ? args.K - k : 0;  // copies i with 2 i < k_in
+      constexpr int KSTEP = S::THREADS / S::BM;
+      const int64_t step = static_cast<int64_t>(KSTEP) * args.lda;
+      int64_t off = static_cast<int64_t>(k) * args.lda + m;
+#pragma unroll
+      for (int i = 0; i < S::BK / KSTEP; ++i, off += step) {
+        const bool in = KSTEP * i < k_in;
+        cp_async_4(a_sm + a_tile_offset(ml, kr0 + KSTEP * i), in ? A + off : A, in ? 4u : 0u);
       }
     }
     {
@@ -149,16 +158,16 @@ __device__ __forceinline__ void issue_stage(uint32_t j, int tile, int kb, const 
       // across the loop); the shared-memory stores stay conflict-free.
       const int nl = t;
       const int n = tn * S::BN + nl;
-      const bool n_ok = n < args.N;
       const bool tb = kGeneral && args.transb;
       const int64_t k_stride = tb ? 1 : args.ldb;
-      const float* b_col = B + (tb ? static_cast<int64_t>(n) * args.ldb : n);
-#pragma unroll 4
-      for (int kr = 0; kr < S::BK; ++kr) {
-        const int k = kb * S::BK + kr;
-        const bool in = n_ok && k < args.K;
-        cp_async_4(b_sm + static_cast<uint32_t>(kr * S::BN + nl) * 4,
-                   in ? b_col + static_cast<int64_t>(k) * k_stride : B, in ? 4u : 0u);
+      const int k0 = kb * S::BK;
+      const int k_in = n < args.N ? args.K - k0 : 0;  // copies kr < k_in
+      int64_t off = (tb ? static_cast<int64_t>(n) * args.ldb : n) + k0 * k_stride;
+#pragma unroll
+      for (int kr = 0; kr < S::BK; ++kr, off += k_stride) {
+        const bool in = kr < k_in;
+        cp_async_4(b_sm + static_cast<uint32_t>(kr * S::BN + nl) * 4, in ? B + off : B,
+                   in ? 4u : 0u);
       }
     }
     cp_async_mbar_arrive_noinc(&sm.full[s]);
