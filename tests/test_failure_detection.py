@@ -14,7 +14,7 @@ import torch
 import dense_gemm_14_gb300 as g14
 from dense_gemm_14_gb300 import _lib, inputs
 
-from gpu_util import oracle_check, run_abi
+from gpu_util import oracle_check, oracle_check_ex, run_abi, run_ex
 
 
 def test_inject_rejects_unknown_modes():
@@ -55,6 +55,38 @@ def test_expired_wait_reports_timeout_and_context_survives(oracle_mod, dt, soft)
     assert g14.check_device_error(s.cuda_stream) == 0
     C = run_abi(A, B, lda=lda, ldb=ldb)
     oracle_check(oracle_mod, A, B, C)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dt,ta,tb,soft_a,soft_b", [
+    ("f32", 0, 1, False, False),   # B stored N x K: tiles transposed in shared memory
+    ("f32", 1, 1, False, False),
+    ("bf16", 0, 0, True, False),   # A by the software loader, B by TMA in the same stages
+    ("bf16", 0, 1, False, True),   # the reverse, B stored N x K
+])
+def test_expired_wait_with_transposes_and_mixed_loaders(oracle_mod, dt, ta, tb, soft_a, soft_b):
+    """The same expired wait in the variants with their own stage bookkeeping:
+    the fp32 kernel's three-stage ring with transposed B buffers (a bounded
+    hand-over barrier per buffer), and the one-SM tensor-core kernel with one
+    operand by TMA and the other by the software loader (two producers per
+    stage, warp 0's TMA loads drained on abort)."""
+    M, N, K = (2048, 2048, 200) if dt == "f32" else (300, 520, 200)
+    A, B = inputs.make(M, N, K, dt, "uniform", 1.0, seed=33 + 2 * ta + tb)
+    q = 4 if dt == "f32" else 8
+    a_cols, b_cols = (M if ta else K), (K if tb else N)
+    lda = a_cols + 1 if soft_a else -(-a_cols // q) * q
+    ldb = b_cols + 1 if soft_b else -(-b_cols // q) * q
+    s = torch.cuda.current_stream()
+    assert g14.check_device_error(s.cuda_stream) == 0
+    assert g14.debug_inject(1, 20_000_000) == 0
+    t0 = time.perf_counter()
+    run_ex(A, B, ta, tb, lda=lda, ldb=ldb, check_err=False)
+    st = g14.check_device_error(s.cuda_stream)
+    assert st == _lib.GEMM14_ERR_TIMEOUT, g14.status_string(st)
+    assert time.perf_counter() - t0 < 10.0
+    assert g14.check_device_error(s.cuda_stream) == 0
+    C = run_ex(A, B, ta, tb, lda=lda, ldb=ldb)
+    oracle_check_ex(oracle_mod, A, B, C, ta, tb)
 
 
 @pytest.mark.gpu
