@@ -83,3 +83,38 @@ def test_fuzz_against_oracle(oracle_mod, seed):
     rows = torch.tensor(sorted(random.Random(seed).sample(range(M), min(M, 24))))
     oracle_check_ex(oracle_mod, A[rows].contiguous(), B, C[rows].contiguous(), c["ta"], c["tb"],
                     c["alpha"], c["beta"], C0[rows].contiguous() if C0 is not None else None)
+
+
+def draw_large(seed):
+    """Output shapes of one to a few waves of the large tiles (the fp32 128 x 256
+    kernel, the 16-bit one-SM and pair kernels), moderate k: stream-K splits,
+    re-pitch copies and stored transposes on the large kernels."""
+    rng = random.Random(seed)
+    c = draw(seed)
+    c["dt"] = rng.choice(["f32", "bf16", "f32", "f16"])
+    c["M"], c["N"] = rng.randint(1500, 5000), rng.randint(1500, 5000)
+    c["K"] = rng.choice([rng.randint(1, 96), rng.randint(96, 1500)])
+    q = 4 if c["dt"] == "f32" else 8
+    a_cols, b_cols = (c["M"] if c["ta"] else c["K"]), (c["K"] if c["tb"] else c["N"])
+    c["lda"] = -(-a_cols // q) * q if rng.random() < 0.5 else a_cols + rng.randint(1, 9)
+    c["ldb"] = -(-b_cols // q) * q if rng.random() < 0.5 else b_cols + rng.randint(1, 9)
+    c["a_off"] = 0 if rng.random() < 0.6 else rng.randint(1, q - 1)
+    c["b_off"] = 0 if rng.random() < 0.6 else rng.randint(1, q - 1)
+    c["ldc"] = c["N"] + rng.choice([0, 1, 4])
+    c["ws_mode"] = rng.choice(["none", "exact", "split", "split"])
+    return c
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_fuzz_large_tiles_against_oracle(oracle_mod, seed):
+    c = draw_large(50000 + seed)
+    M, N, K = c["M"], c["N"], c["K"]
+    A, B = inputs.make(M, N, K, c["dt"], "uniform", 1.0, seed=60000 + seed)
+    C0 = (torch.rand(M, N, generator=torch.Generator().manual_seed(seed)) * 2 - 1
+          if c["beta"] != 0.0 else None)
+    ws = workspace_for(c)
+    C = run_ex(A, B, c["ta"], c["tb"], c["alpha"], c["beta"], C0, lda=c["lda"], ldb=c["ldb"],
+               ldc=c["ldc"], a_off=c["a_off"], b_off=c["b_off"], c_off=1, workspace=ws)
+    rows = torch.tensor(sorted(random.Random(seed).sample(range(M), 24)))
+    oracle_check_ex(oracle_mod, A[rows].contiguous(), B, C[rows].contiguous(), c["ta"], c["tb"],
+                    c["alpha"], c["beta"], C0[rows].contiguous() if C0 is not None else None)
