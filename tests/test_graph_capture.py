@@ -110,3 +110,55 @@ def test_small_tile_products_replayed_from_a_graph(oracle_mod):
         assert g14.check_device_error(torch.cuda.current_stream().cuda_stream) == 0
         for A, B, c in host:
             oracle_check(oracle_mod, A, B, c.cpu())
+
+
+def test_plain_loader_variants_replayed_from_a_graph(oracle_mod):
+    """Plain calls (no workspace) of the loader variants captured in one graph:
+    fp32 with B stored N x K (tiles transposed in shared memory), fp32 with
+    odd pitches (the cp.async loader), bf16 with only A by the software loader
+    (B by TMA in the same stages), and bf16 with both by software; replayed on
+    new inputs against the oracle."""
+    from gpu_util import oracle_check_ex, stored
+    # (dt, tb, M, N, K, extra pitch of A, extra pitch of B)
+    cases = [("f32", 1, 2100, 2048, 300, 0, 0), ("f32", 0, 2100, 2047, 129, 1, 1),
+             ("bf16", 0, 700, 520, 333, 1, 0), ("bf16", 0, 300, 130, 257, 1, 3)]
+    s = torch.cuda.Stream()
+    bufs = []
+    for dt, tb, M, N, K, xa, xb in cases:
+        td = torch.bfloat16 if dt == "bf16" else torch.float32
+        q = 8 if dt == "bf16" else 4
+        b_cols = K if tb else N
+        lda = (-(-K // q) * q) if xa == 0 else K + xa
+        ldb = (-(-b_cols // q) * q) if xb == 0 else b_cols + xb
+        a = torch.zeros(M, lda, dtype=td, device="cuda")
+        b = torch.zeros(N if tb else K, ldb, dtype=td, device="cuda")
+        c = torch.zeros(M, N, device="cuda")
+        bufs.append((dt, tb, M, N, K, lda, ldb, a, b, c))
+
+    def issue():
+        for dt, tb, M, N, K, lda, ldb, a, b, c in bufs:
+            g14.gemm_ex(CODE[dt], 0, tb, M, N, K, 1.0, a.data_ptr(), lda, b.data_ptr(), ldb, 0.0,
+                        c.data_ptr(), N, None, 0, s.cuda_stream)
+
+    with torch.cuda.stream(s):
+        issue()  # warm-up outside the capture (kernel attributes)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        issue()
+    for rep in range(3):
+        host = []
+        for i, (dt, tb, M, N, K, lda, ldb, a, b, c) in enumerate(bufs):
+            A, B = inputs.make(M, N, K, dt, "normal", 1.0 / K ** 0.5, seed=500 + 10 * rep + i)
+            Bs = stored(B, tb)
+            a[:, :K].copy_(A.cuda())
+            b[:, :Bs.shape[1]].copy_(Bs.cuda())
+            c.fill_(float("nan"))
+            host.append((A, B, c))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert g14.check_device_error(torch.cuda.current_stream().cuda_stream) == 0
+        for (A, B, c), (dt, tb, M, *_rest) in zip(host, bufs):
+            rows = torch.arange(0, M, 17)
+            oracle_check_ex(oracle_mod, A[rows].contiguous(), B, c.cpu()[rows].contiguous(), 0, tb)
