@@ -283,9 +283,14 @@ cudaError_t launch_hgemm_tc_soft(int bm, int bn, int soft, const CUtensorMap* ma
 // written by converter warps ("3xTF32").
 struct Tf32Shape {
   static constexpr int BM = 256, BN = 256, BK = 32;  // k-block: 32 fp32 = one 128-byte row
-  static constexpr int OP_STAGES = 2;
+  static constexpr int OP_STAGES = 2;       // 3xTF32
+  static constexpr int OP_STAGES_TF32 = 4;  // TF32: compact stages (copies only)
   static constexpr int MAX_RAW_STAGES = 5;
-  static constexpr int THREADS = 10 * 32;  // producer, MMA, 4 epilogue, 4 converter warps
+  // producer, MMA, 4 epilogue, 4 converter warps; TF32 adds two announcer
+  // warps (each forwards every other k-block's operand stage)
+  static constexpr int THREADS = 12 * 32;
+  static constexpr int threads(bool three) { return three ? 10 * 32 : THREADS; }
+  static constexpr int op_stages(bool three) { return three ? OP_STAGES : OP_STAGES_TF32; }
   static constexpr int TILE = 128 * BK * 4;       // one CTA's 128 rows x 32 k of fp32: 16 KB
   static constexpr int RAW_STAGE = 2 * TILE;      // A, B as loaded
   static constexpr int RING_BYTES = 224 * 1024;   // raw + operand rings

@@ -66,8 +66,8 @@ void plan_for(int dtype, int transa, int transb, int64_t M, int64_t N, int64_t K
       p->bm = T::BM;
       p->bn = T::BN;
       p->bk = T::BK;
-      p->stages = T::OP_STAGES;
-      p->threads = T::THREADS;
+      p->stages = T::op_stages(dtype == GEMM14_DTYPE_F32_3XTF32);
+      p->threads = T::threads(dtype == GEMM14_DTYPE_F32_3XTF32);
       p->smem_bytes = T::SMEM_BYTES;
       p->tiles = ((M + T::BM - 1) / T::BM) * ((N + T::BN - 1) / T::BN);
       const int64_t clusters = sm_count / 2;

@@ -15,17 +15,25 @@
 // dropping lo(A) lo(B) and the tensor cores' truncation of the lo parts (each
 // below 2^-20 relative): at most 3 * 2^-20 |A||B| in all.
 //
-// Roles per CTA (320 threads, cluster of two, persistent over 256 x 256 pair
-// tiles; each CTA holds 128 rows of A and 128 columns of B):
+// Roles per CTA (cluster of two, persistent over 256 x 256 pair tiles; each
+// CTA holds 128 rows of A and 128 columns of B; 384 threads for TF32, 320 for
+// 3xTF32, which has no announcers):
 //   warp 0      producer: TMA of this CTA's fp32 A and B tiles of a 32-deep
 //               k-block, in the storage's own layout, into a raw ring;
 //   warp 1      TMEM (2 x 256 columns per CTA); in the leader one lane issues
 //               per k-block 4 slices x (1 or 3) pair MMAs M 256, N 256, K 8;
 //   warps 2..5  epilogue: each CTA's 128 accumulator rows from TMEM to C;
 //   warps 6..9  converters: write what the MMAs need beyond the raw tiles into
-//               a 2-stage operand ring: the lo tiles (3xTF32), and a K-major
-//               copy of an operand stored MN-major; both CTAs' converters count
-//               on the leader's barrier before its MMAs read the stage.
+//               an operand ring: the lo tiles (3xTF32), and a K-major copy of
+//               an operand stored MN-major; 2 stages for 3xTF32, 4 smaller
+//               ones for TF32 (copies only, in the same bytes); they release
+//               each stage to their CTA's announcer;
+//   warps 10,11 announcers (TF32), each taking every other k-block: forward
+//               each completed stage to the leader's barrier (one cluster-scope
+//               release arrival per CTA and stage, about 0.6 us, kept off the
+//               converters' path); the leader's MMAs read the stage once both
+//               CTAs' arrived. For 3xTF32, whose MMAs outlast the arrival,
+//               the converter warps arrive on the leader's barrier themselves.
 // Every MMA operand is K-major with the 128-byte swizzle, the one layout every
 // tcgen05 kind takes. A raw tile that TMA already wrote K-major (A stored
 // M x K, B stored N x K) is an MMA operand as it stands; its raw stage is then
@@ -53,6 +61,12 @@ struct Tf32Plan {
   static constexpr int B_HI = A_LO + T::TILE;
   static constexpr int B_LO = B_HI + (B_RAW ? 0 : 1) * T::TILE;
   static constexpr int OP_STAGE = B_LO + T::TILE;
+  // TF32 (one term) needs only the K-major copies: stages of OP1_STAGE
+  // bytes, A's copy (A stored K x M) first, then B's (B stored K x N); four of
+  // them fit where the two 3xTF32 stages lie.
+  static constexpr int B1_HI = A_RAW ? 0 : T::TILE;
+  static constexpr int OP1_STAGE = ((A_RAW ? 0 : 1) + (B_RAW ? 0 : 1)) * T::TILE;
+  static_assert(T::OP_STAGES_TF32 * OP1_STAGE <= T::OP_STAGES * OP_STAGE, "TF32 operand ring");
   static constexpr int RAW_STAGES_FIT = (T::RING_BYTES - T::OP_STAGES * OP_STAGE) / T::RAW_STAGE;
   static constexpr int RAW_STAGES =
       RAW_STAGES_FIT < T::MAX_RAW_STAGES ? RAW_STAGES_FIT : T::MAX_RAW_STAGES;
@@ -63,8 +77,10 @@ struct Tf32Plan {
 struct Tf32Smem {
   uint64_t raw_full[T::MAX_RAW_STAGES];   // each CTA: its TMA bytes of a raw stage landed
   uint64_t raw_empty[T::MAX_RAW_STAGES];  // each CTA: converters (and MMAs) are done with it
-  uint64_t op_full[T::OP_STAGES];         // leader: both CTAs' converters wrote an operand stage
-  uint64_t op_empty[T::OP_STAGES];        // each CTA: the pair MMAs finished reading it
+  // operand stages: T::OP_STAGES for 3xTF32, T::OP_STAGES_TF32 for TF32
+  uint64_t op_full[T::OP_STAGES_TF32];    // leader: both CTAs forwarded an operand stage
+  uint64_t conv_done[T::OP_STAGES_TF32];  // each CTA: its 4 converter warps wrote an operand stage
+  uint64_t op_empty[T::OP_STAGES_TF32];   // each CTA: the pair MMAs finished reading it
   uint64_t acc_full[2];                   // each CTA: accumulator b holds a finished tile
   uint64_t acc_empty[2];                  // leader: all 8 epilogue warps drained accumulator b
   uint64_t drain;
@@ -172,6 +188,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
   const int num_tiles = tiles_m * tiles_n;
   const int kblocks = (K + T::BK - 1) / T::BK;
   const bool three = terms == 3;
+  // operand ring: 2 stages of the 3xTF32 layout, or 4 compact TF32 stages
+  const uint32_t op_log = three ? 1u : 2u;
+  const uint32_t op_mask = (1u << op_log) - 1u;
+  const uint32_t op_bytes = three ? L::OP_STAGE : L::OP1_STAGE;
+  const uint32_t b_hi_off = three ? L::B_HI : L::B1_HI;
   const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns,
                    mapa_shared(smem_u32(&sm.abort_flag), rank ^ 1u)};
   uint32_t prod_it = 0;
@@ -182,8 +203,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
       mbar_init(&sm.raw_full[s], 1);
       mbar_init(&sm.raw_empty[s], kMmaReadsRaw ? 5 : 4);
     }
-    for (int s = 0; s < T::OP_STAGES; ++s) {
-      mbar_init(&sm.op_full[s], 8);
+    for (int s = 0; s <= static_cast<int>(op_mask); ++s) {
+      // 3xTF32: the 8 converter warps of both CTAs arrive themselves; TF32:
+      // the two CTAs' announcers
+      mbar_init(&sm.op_full[s], three ? 8 : 2);
+      mbar_init(&sm.conv_done[s], 128);
       mbar_init(&sm.op_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -249,15 +273,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * T::BN);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const uint32_t s = it % RS;
-          const uint32_t o = it % T::OP_STAGES, oph = (it / T::OP_STAGES) & 1;
+          const uint32_t o = it & op_mask, oph = (it >> op_log) & 1;
           // Both CTAs' converters have seen raw stage s full and written
           // operand stage o.
           if (!mbar_wait_cluster(&sm.op_full[o], oph, wc)) { ok = false; break; }
           tc_fence_after_sync();
           const uint32_t raw = smem_u32(raw_ring + s * T::RAW_STAGE);
-          const uint32_t op = smem_u32(op_ring + o * L::OP_STAGE);
+          const uint32_t op = smem_u32(op_ring + o * op_bytes);
           const uint32_t a_hi = L::A_RAW ? raw : op + L::A_HI;
-          const uint32_t b_hi = L::B_RAW ? raw + T::TILE : op + L::B_HI;
+          const uint32_t b_hi = L::B_RAW ? raw + T::TILE : op + b_hi_off;
 #pragma unroll
           for (int kk = 0; kk < T::BK / 8; ++kk) {
             // K-major, 128-byte rows, 8-row groups 1024 B apart; a K = 8 slice
@@ -326,7 +350,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(b ? acc_empty_leader1 : acc_empty_leader0);
     }
-  } else {
+  } else if (warp < 10) {
     // ------------------------------------------------------------ converters
     // Thread r handles row r of A and row r of B^T. A raw stage is released
     // only after the values loaded from it are stored: the stores consume
@@ -341,7 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
     for (int t = cid; t < num_tiles && ok; t += ncl) {
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
         const uint32_t s = it % RS, ph = (it / RS) & 1;
-        const uint32_t o = it % T::OP_STAGES, oph = (it / T::OP_STAGES) & 1;
+        const uint32_t o = it & op_mask, oph = (it >> op_log) & 1;
         int got = 1;
         if (lane == 0) got = mbar_wait(&sm.raw_full[s], ph, wc) ? 1 : 0;
         got = __shfl_sync(0xffffffffu, got, 0);
@@ -360,18 +384,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
         if (lane == 0) got = mbar_wait(&sm.op_empty[o], oph ^ 1, wc) ? 1 : 0;
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) { ok = false; break; }
-        const uint32_t op = smem_u32(op_ring + o * L::OP_STAGE);
+        const uint32_t op = smem_u32(op_ring + o * op_bytes);
         if (!L::A_RAW) store_row(op + L::A_HI, r, va);
         if (three) store_lo_row(op + L::A_LO, r, va);
-        if (!L::B_RAW) store_row(op + L::B_HI, r, vb);
+        if (!L::B_RAW) store_row(op + b_hi_off, r, vb);
         if (three) store_lo_row(op + L::B_LO, r, vb);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.raw_empty[s]);
-        // This thread's operand writes -> visible to the MMAs (async proxy);
-        // the warp's writes are ordered before lane 0's release arrival.
+        // This thread's operand writes -> visible to the MMAs (async proxy).
         fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm.op_full[o]), 0));
+        if (three) {
+          // the warp's writes are ordered before lane 0's release arrival on
+          // the leader's barrier (the 3xTF32 MMAs take longer than the
+          // arrival, which stays on this path)
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm.op_full[o]), 0));
+        } else {
+          // released to this CTA's announcer (CTA scope), which forwards the
+          // stage to the leader at cluster scope off this warp's path
+          mbar_arrive(&sm.conv_done[o]);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ announcer
+    // Acquires each operand stage from this CTA's converters and releases it
+    // to the leader's op_full barrier at cluster scope: the converters' writes
+    // reach the leader's MMAs through this chain of release and acquire.
+    // Warp 10 + a handles the k-blocks it with it % 2 == a (TF32; for 3xTF32
+    // the converters arrive themselves).
+    const uint32_t a = static_cast<uint32_t>(warp - 10);
+    if (lane == 0 && !three) {
+      const uint32_t uses = static_cast<uint32_t>((num_tiles - cid + ncl - 1) / ncl) *
+                            static_cast<uint32_t>(kblocks);  // this CTA's k-blocks
+      for (uint32_t it = a; it < uses; it += 2) {
+        const uint32_t o = it & op_mask;
+        if (!mbar_wait(&sm.conv_done[o], (it >> op_log) & 1, wc)) break;
+        mbar_arrive_cluster(mapa_shared(smem_u32(&sm.op_full[o]), 0));
       }
     }
   }
@@ -409,8 +458,11 @@ cudaError_t set_smem() {
 template <bool kTA, bool kTB, bool kGeneral>
 cudaError_t launch_one(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
                        uint32_t idesc, int terms, int clusters, cudaStream_t stream) {
+  // 3xTF32 runs without the announcer warps (its converters arrive on the
+  // leader's barrier themselves)
+  const int threads = T::threads(terms == 3);
   return launch_kernel(sgemm_tf32_pair_kernel<kTA, kTB, kGeneral>, dim3(2 * clusters),
-                       dim3(T::THREADS), T::SMEM_BYTES, stream, map_a, map_b, args, idesc, terms);
+                       dim3(threads), T::SMEM_BYTES, stream, map_a, map_b, args, idesc, terms);
 }
 
 template <bool kTA, bool kTB>

@@ -293,7 +293,10 @@ TF32, X3 = g14.GEMM14_DTYPE_TF32, g14.GEMM14_DTYPE_F32_3XTF32
 def test_plan_tf32_pairs_and_fallback(lib, dtype):
     st, p = g14.plan(dtype, 3072, 3072, 3072, P, 3072, P, 3072, P, 3072, 152)
     assert st == 0 and p.kernel == 4 and (p.bm, p.bn, p.bk) == (256, 256, 32)
-    assert p.tiles == 144 and p.grid == 152 and p.threads == 320
+    assert p.tiles == 144 and p.grid == 152
+    # TF32: 12 warps (two announcers), 4 compact operand stages; 3xTF32: 10
+    # warps, 2 operand stages (copies and lo tiles)
+    assert (p.threads, p.stages) == ((384, 4) if dtype == TF32 else (320, 2))
     assert p.smem_bytes <= 227 * 1024
     for ta, tb in ((1, 0), (0, 1), (1, 1)):
         st, pt = g14.plan_ex(dtype, ta, tb, 3072, 3072, 3072, P, 3072, P, 3072, P, 3072, 152)
