@@ -24,10 +24,11 @@
 //               per k-block 4 slices x (1 or 3) pair MMAs M 256, N 256, K 8;
 //   warps 2..5  epilogue: each CTA's 128 accumulator rows from TMEM to C;
 //   warps 6..9  converters: write what the MMAs need beyond the raw tiles into
-//               an operand ring: the lo tiles (3xTF32), and a K-major copy of
-//               an operand stored MN-major; 2 stages for 3xTF32, 4 smaller
-//               ones for TF32 (copies only, in the same bytes); they release
-//               each stage to their CTA's announcer;
+//               an operand ring. 3xTF32: 2 stages of the lo tiles and a
+//               K-major copy of an operand stored MN-major. TF32: 4 stages of
+//               K-major copies of both operands wherever one of them needs a
+//               copy, so that no raw stage waits for the MMAs; 3 raw stages.
+//               They release each stage to their CTA's announcer;
 //   warps 10,11 announcers (TF32), each taking every other k-block: forward
 //               each completed stage to the leader's barrier (one cluster-scope
 //               release arrival per CTA and stage, about 0.6 us, kept off the
@@ -36,8 +37,9 @@
 //               the converter warps arrive on the leader's barrier themselves.
 // Every MMA operand is K-major with the 128-byte swizzle, the one layout every
 // tcgen05 kind takes. A raw tile that TMA already wrote K-major (A stored
-// M x K, B stored N x K) is an MMA operand as it stands; its raw stage is then
-// freed by the MMAs' commit as well as by the converters.
+// M x K, B stored N x K) is an MMA operand as it stands (3xTF32, and TF32 with
+// both operands stored so); its raw stage is then freed by the MMAs' commit
+// as well as by the converters.
 // Every wait is bounded, a CTA that gives up raises its peer's abort flag,
 // and both CTAs meet at a cluster barrier before TMEM is freed.
 #include "kernels.h"
@@ -61,12 +63,16 @@ struct Tf32Plan {
   static constexpr int B_HI = A_LO + T::TILE;
   static constexpr int B_LO = B_HI + (B_RAW ? 0 : 1) * T::TILE;
   static constexpr int OP_STAGE = B_LO + T::TILE;
-  // TF32 (one term) needs only the K-major copies: stages of OP1_STAGE
-  // bytes, A's copy (A stored K x M) first, then B's (B stored K x N); four of
-  // them fit where the two 3xTF32 stages lie.
-  static constexpr int B1_HI = A_RAW ? 0 : T::TILE;
-  static constexpr int OP1_STAGE = ((A_RAW ? 0 : 1) + (B_RAW ? 0 : 1)) * T::TILE;
-  static_assert(T::OP_STAGES_TF32 * OP1_STAGE <= T::OP_STAGES * OP_STAGE, "TF32 operand ring");
+  // TF32 (one term) needs only K-major copies. Where one operand needs a
+  // copy, both are copied (A at 0, B at TILE): the converters then free every
+  // raw stage without waiting for the MMAs, and four operand stages cover the
+  // MMAs' latency. The TF32 rings: 3 raw stages and 4 operand stages (both
+  // operands as stored K-major: no copies, the 3xTF32 raw ring).
+  static constexpr bool COPY_TF32 = !(A_RAW && B_RAW);
+  static constexpr int OP1_STAGE = COPY_TF32 ? 2 * T::TILE : 0;
+  static constexpr int RAW_STAGES_TF32 = COPY_TF32 ? 3 : 0;  // 0: RAW_STAGES
+  static_assert(RAW_STAGES_TF32 * T::RAW_STAGE + T::OP_STAGES_TF32 * OP1_STAGE <= T::RING_BYTES,
+                "TF32 rings");
   static constexpr int RAW_STAGES_FIT = (T::RING_BYTES - T::OP_STAGES * OP_STAGE) / T::RAW_STAGE;
   static constexpr int RAW_STAGES =
       RAW_STAGES_FIT < T::MAX_RAW_STAGES ? RAW_STAGES_FIT : T::MAX_RAW_STAGES;
@@ -168,12 +174,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
                            const __grid_constant__ CUtensorMap map_b, const GemmArgs args,
                            const uint32_t idesc, const int terms) {
   using L = Tf32Plan<kTA, kTB>;
-  constexpr int RS = L::RAW_STAGES;
-  constexpr bool kMmaReadsRaw = L::A_RAW || L::B_RAW;
+  const bool three = terms == 3;
+  // The MMAs read an operand's hi part from the raw stage where TMA wrote it
+  // K-major (TF32: unless the other operand needs a copy); the raw stage is
+  // then freed by their commit as well as by the converters.
+  const bool a_raw = L::A_RAW && (three || !L::COPY_TF32);
+  const bool b_raw = L::B_RAW && (three || !L::COPY_TF32);
+  const bool mma_reads_raw = a_raw || b_raw;
+  const uint32_t rs = (three || !L::COPY_TF32) ? L::RAW_STAGES : L::RAW_STAGES_TF32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint8_t* raw_ring = base;
-  uint8_t* op_ring = base + RS * T::RAW_STAGE;
+  uint8_t* op_ring = base + rs * T::RAW_STAGE;
   Tf32Smem& sm = *reinterpret_cast<Tf32Smem*>(base + T::RING_BYTES);
 
   const int warp = threadIdx.x >> 5;
@@ -187,21 +199,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
   const int tiles_n = (N + T::BN - 1) / T::BN;
   const int num_tiles = tiles_m * tiles_n;
   const int kblocks = (K + T::BK - 1) / T::BK;
-  const bool three = terms == 3;
-  // operand ring: 2 stages of the 3xTF32 layout, or 4 compact TF32 stages
+  // operand ring: 2 stages of the 3xTF32 layout, or 4 TF32 stages of copies
   const uint32_t op_log = three ? 1u : 2u;
   const uint32_t op_mask = (1u << op_log) - 1u;
   const uint32_t op_bytes = three ? L::OP_STAGE : L::OP1_STAGE;
-  const uint32_t b_hi_off = three ? L::B_HI : L::B1_HI;
+  const uint32_t b_hi_off = three ? L::B_HI : T::TILE;
   const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns,
                    mapa_shared(smem_u32(&sm.abort_flag), rank ^ 1u)};
   uint32_t prod_it = 0;
   bool mma_issued = false;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < RS; ++s) {
+    for (int s = 0; s < static_cast<int>(rs); ++s) {
       mbar_init(&sm.raw_full[s], 1);
-      mbar_init(&sm.raw_empty[s], kMmaReadsRaw ? 5 : 4);
+      mbar_init(&sm.raw_empty[s], mma_reads_raw ? 5 : 4);
     }
     for (int s = 0; s <= static_cast<int>(op_mask); ++s) {
       // 3xTF32: the 8 converter warps of both CTAs arrive themselves; TF32:
@@ -239,14 +250,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = true;
+      uint32_t next_s = 0, next_ph = 0;  // raw stage and phase of prod_it
       for (int t = cid; t < num_tiles && ok; t += ncl) {
         int tm, tn;
         pair_tile_coords(t, tiles_m, tiles_n, tm, tn);
         const int m0 = tm * T::BM + static_cast<int>(rank) * 128;
         const int n0 = tn * T::BN + static_cast<int>(rank) * 128;
         for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
-          const uint32_t s = prod_it % RS, ph = (prod_it / RS) & 1;
+          const uint32_t s = next_s, ph = next_ph;
           if (!mbar_wait(&sm.raw_empty[s], ph ^ 1, wc)) { ok = false; break; }
+          if (++next_s == rs) { next_s = 0; next_ph ^= 1; }
           // Failure-detection tests: the first stage is never loaded.
           if (args.fault == kFaultSkipFirstStage && prod_it == 0) continue;
           uint8_t* ra = raw_ring + s * T::RAW_STAGE;
@@ -263,7 +276,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer (leader)
     if (leader && lane == 0) {
       bool ok = true;
-      uint32_t it = 0;
+      uint32_t it = 0, s = 0;  // s: raw stage of it
       int local = 0;
       for (int t = cid; t < num_tiles && ok; t += ncl, ++local) {
         const int b = local & 1;
@@ -271,8 +284,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
         if (!mbar_wait_cluster(&sm.acc_empty[b], aph ^ 1, wc)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * T::BN);
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const uint32_t s = it % RS;
+        for (int kb = 0; kb < kblocks; ++kb, ++it, s = s + 1 == rs ? 0 : s + 1) {
           const uint32_t o = it & op_mask, oph = (it >> op_log) & 1;
           // Both CTAs' converters have seen raw stage s full and written
           // operand stage o.
@@ -280,8 +292,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
           tc_fence_after_sync();
           const uint32_t raw = smem_u32(raw_ring + s * T::RAW_STAGE);
           const uint32_t op = smem_u32(op_ring + o * op_bytes);
-          const uint32_t a_hi = L::A_RAW ? raw : op + L::A_HI;
-          const uint32_t b_hi = L::B_RAW ? raw + T::TILE : op + b_hi_off;
+          const uint32_t a_hi = a_raw ? raw : op + L::A_HI;
+          const uint32_t b_hi = b_raw ? raw + T::TILE : op + b_hi_off;
 #pragma unroll
           for (int kk = 0; kk < T::BK / 8; ++kk) {
             // K-major, 128-byte rows, 8-row groups 1024 B apart; a K = 8 slice
@@ -299,7 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
           }
           mma_issued = true;
           tc_commit_pair_multicast(&sm.op_empty[o], 0x3);
-          if (kMmaReadsRaw) tc_commit_pair_multicast(&sm.raw_empty[s], 0x3);
+          if (mma_reads_raw) tc_commit_pair_multicast(&sm.raw_empty[s], 0x3);
         }
         if (!ok) break;
         tc_commit_pair_multicast(&sm.acc_full[b], 0x3);
@@ -358,13 +370,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
     // refill it (released straight after the loads, it was refilled under
     // them).
     const int r = threadIdx.x - 6 * 32;
-    const bool need_a = !L::A_RAW || three;  // a K-major copy of A, or lo(A)
-    const bool need_b = !L::B_RAW || three;
-    uint32_t it = 0;
+    const bool need_a = !a_raw || three;  // a K-major copy of A, or lo(A)
+    const bool need_b = !b_raw || three;
+    uint32_t it = 0, s = 0, ph = 0;  // s, ph: raw stage and phase of it
     bool ok = true;
     for (int t = cid; t < num_tiles && ok; t += ncl) {
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
-        const uint32_t s = it % RS, ph = (it / RS) & 1;
         const uint32_t o = it & op_mask, oph = (it >> op_log) & 1;
         int got = 1;
         if (lane == 0) got = mbar_wait(&sm.raw_full[s], ph, wc) ? 1 : 0;
@@ -385,9 +396,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) { ok = false; break; }
         const uint32_t op = smem_u32(op_ring + o * op_bytes);
-        if (!L::A_RAW) store_row(op + L::A_HI, r, va);
+        if (!a_raw) store_row(op + L::A_HI, r, va);
         if (three) store_lo_row(op + L::A_LO, r, va);
-        if (!L::B_RAW) store_row(op + b_hi_off, r, vb);
+        if (!b_raw) store_row(op + b_hi_off, r, vb);
         if (three) store_lo_row(op + L::B_LO, r, vb);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.raw_empty[s]);
@@ -404,6 +415,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
           // stage to the leader at cluster scope off this warp's path
           mbar_arrive(&sm.conv_done[o]);
         }
+        if (++s == rs) { s = 0; ph ^= 1; }
       }
     }
   } else {
@@ -434,10 +446,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
       mbar_wait_timed(&sm.drain, 0, 100000000ull);
     }
     if (warp == 0 && lane == 0) {
-      const uint32_t first = prod_it > RS ? prod_it - RS : 0;
+      const uint32_t first = prod_it > rs ? prod_it - rs : 0;
       for (uint32_t j = first; j < prod_it; ++j)
         if (!(args.fault == kFaultSkipFirstStage && j == 0))
-          mbar_wait_timed(&sm.raw_full[j % RS], (j / RS) & 1, 100000000ull);
+          mbar_wait_timed(&sm.raw_full[j % rs], (j / rs) & 1, 100000000ull);
     }
   }
   // Neither CTA frees TMEM or exits while the pair may still use it.
