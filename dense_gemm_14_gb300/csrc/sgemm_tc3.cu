@@ -80,6 +80,23 @@ struct Tf32Plan {
   static_assert(RAW_STAGES * T::RAW_STAGE + T::OP_STAGES * OP_STAGE <= T::RING_BYTES, "rings");
 };
 
+// The ring geometry of one mode (kThree: 3xTF32), fixed at compile time in
+// the roles' loops; the kernel picks the mode once per role.
+template <class L, bool kThree>
+struct Tf32Mode {
+  static constexpr bool THREE = kThree;
+  // the MMAs read hi(A) / hi(B) from the raw stage where TMA wrote it K-major
+  static constexpr bool A_RAW = L::A_RAW && (kThree || !L::COPY_TF32);
+  static constexpr bool B_RAW = L::B_RAW && (kThree || !L::COPY_TF32);
+  static constexpr bool MMA_READS_RAW = A_RAW || B_RAW;
+  static constexpr uint32_t RS =
+      (kThree || !L::COPY_TF32) ? L::RAW_STAGES : L::RAW_STAGES_TF32;
+  static constexpr uint32_t OP_LOG = kThree ? 1u : 2u;  // operand stages: 2 or 4
+  static constexpr uint32_t OP_MASK = (1u << OP_LOG) - 1u;
+  static constexpr uint32_t OP_BYTES = kThree ? L::OP_STAGE : L::OP1_STAGE;
+  static constexpr uint32_t B_HI = kThree ? L::B_HI : T::TILE;
+};
+
 struct Tf32Smem {
   uint64_t raw_full[T::MAX_RAW_STAGES];   // each CTA: its TMA bytes of a raw stage landed
   uint64_t raw_empty[T::MAX_RAW_STAGES];  // each CTA: converters (and MMAs) are done with it
@@ -174,18 +191,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
                            const __grid_constant__ CUtensorMap map_b, const GemmArgs args,
                            const uint32_t idesc, const int terms) {
   using L = Tf32Plan<kTA, kTB>;
+  using Three = Tf32Mode<L, true>;
+  using One = Tf32Mode<L, false>;
   const bool three = terms == 3;
-  // The MMAs read an operand's hi part from the raw stage where TMA wrote it
-  // K-major (TF32: unless the other operand needs a copy); the raw stage is
-  // then freed by their commit as well as by the converters.
-  const bool a_raw = L::A_RAW && (three || !L::COPY_TF32);
-  const bool b_raw = L::B_RAW && (three || !L::COPY_TF32);
-  const bool mma_reads_raw = a_raw || b_raw;
-  const uint32_t rs = (three || !L::COPY_TF32) ? L::RAW_STAGES : L::RAW_STAGES_TF32;
+  // ring geometry of the mode, for set-up and teardown (the roles' loops
+  // take it from Tf32Mode at compile time)
+  const bool mma_reads_raw = three ? Three::MMA_READS_RAW : One::MMA_READS_RAW;
+  const uint32_t rs = three ? Three::RS : One::RS;
+  const uint32_t op_stages = three ? T::OP_STAGES : T::OP_STAGES_TF32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint8_t* raw_ring = base;
-  uint8_t* op_ring = base + rs * T::RAW_STAGE;
   Tf32Smem& sm = *reinterpret_cast<Tf32Smem*>(base + T::RING_BYTES);
 
   const int warp = threadIdx.x >> 5;
@@ -199,11 +215,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
   const int tiles_n = (N + T::BN - 1) / T::BN;
   const int num_tiles = tiles_m * tiles_n;
   const int kblocks = (K + T::BK - 1) / T::BK;
-  // operand ring: 2 stages of the 3xTF32 layout, or 4 TF32 stages of copies
-  const uint32_t op_log = three ? 1u : 2u;
-  const uint32_t op_mask = (1u << op_log) - 1u;
-  const uint32_t op_bytes = three ? L::OP_STAGE : L::OP1_STAGE;
-  const uint32_t b_hi_off = three ? L::B_HI : T::TILE;
   const WaitCtx wc{args.err, &sm.abort_flag, args.wait_limit_ns,
                    mapa_shared(smem_u32(&sm.abort_flag), rank ^ 1u)};
   uint32_t prod_it = 0;
@@ -214,7 +225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
       mbar_init(&sm.raw_full[s], 1);
       mbar_init(&sm.raw_empty[s], mma_reads_raw ? 5 : 4);
     }
-    for (int s = 0; s <= static_cast<int>(op_mask); ++s) {
+    for (int s = 0; s < static_cast<int>(op_stages); ++s) {
       // 3xTF32: the 8 converter warps of both CTAs arrive themselves; TF32:
       // the two CTAs' announcers
       mbar_init(&sm.op_full[s], three ? 8 : 2);
@@ -248,75 +259,86 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      bool ok = true;
-      uint32_t next_s = 0, next_ph = 0;  // raw stage and phase of prod_it
-      for (int t = cid; t < num_tiles && ok; t += ncl) {
-        int tm, tn;
-        pair_tile_coords(t, tiles_m, tiles_n, tm, tn);
-        const int m0 = tm * T::BM + static_cast<int>(rank) * 128;
-        const int n0 = tn * T::BN + static_cast<int>(rank) * 128;
-        for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
-          const uint32_t s = next_s, ph = next_ph;
-          if (!mbar_wait(&sm.raw_empty[s], ph ^ 1, wc)) { ok = false; break; }
-          if (++next_s == rs) { next_s = 0; next_ph ^= 1; }
-          // Failure-detection tests: the first stage is never loaded.
-          if (args.fault == kFaultSkipFirstStage && prod_it == 0) continue;
-          uint8_t* ra = raw_ring + s * T::RAW_STAGE;
-          uint8_t* rb = ra + T::TILE;
-          mbar_arrive_expect_tx(&sm.raw_full[s], T::RAW_STAGE);
-          if (kTA) tma_load_2d(ra, &map_a, m0, kb * T::BK, &sm.raw_full[s]);
-          else tma_load_2d(ra, &map_a, kb * T::BK, m0, &sm.raw_full[s]);
-          if (kTB) tma_load_2d(rb, &map_b, kb * T::BK, n0, &sm.raw_full[s]);
-          else tma_load_2d(rb, &map_b, n0, kb * T::BK, &sm.raw_full[s]);
+    auto run = [&](auto mode) {
+      using Md = decltype(mode);
+      if (lane == 0) {
+        bool ok = true;
+        uint32_t next_s = 0, next_ph = 0;  // raw stage and phase of prod_it
+        for (int t = cid; t < num_tiles && ok; t += ncl) {
+          int tm, tn;
+          pair_tile_coords(t, tiles_m, tiles_n, tm, tn);
+          const int m0 = tm * T::BM + static_cast<int>(rank) * 128;
+          const int n0 = tn * T::BN + static_cast<int>(rank) * 128;
+          for (int kb = 0; kb < kblocks; ++kb, ++prod_it) {
+            const uint32_t s = next_s, ph = next_ph;
+            if (!mbar_wait(&sm.raw_empty[s], ph ^ 1, wc)) { ok = false; break; }
+            if (++next_s == Md::RS) { next_s = 0; next_ph ^= 1; }
+            // Failure-detection tests: the first stage is never loaded.
+            if (args.fault == kFaultSkipFirstStage && prod_it == 0) continue;
+            uint8_t* ra = raw_ring + s * T::RAW_STAGE;
+            uint8_t* rb = ra + T::TILE;
+            mbar_arrive_expect_tx(&sm.raw_full[s], T::RAW_STAGE);
+            if (kTA) tma_load_2d(ra, &map_a, m0, kb * T::BK, &sm.raw_full[s]);
+            else tma_load_2d(ra, &map_a, kb * T::BK, m0, &sm.raw_full[s]);
+            if (kTB) tma_load_2d(rb, &map_b, kb * T::BK, n0, &sm.raw_full[s]);
+            else tma_load_2d(rb, &map_b, n0, kb * T::BK, &sm.raw_full[s]);
+          }
         }
       }
-    }
+    };
+    if (three) run(Three{});
+    else run(One{});
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader)
-    if (leader && lane == 0) {
-      bool ok = true;
-      uint32_t it = 0, s = 0;  // s: raw stage of it
-      int local = 0;
-      for (int t = cid; t < num_tiles && ok; t += ncl, ++local) {
-        const int b = local & 1;
-        const uint32_t aph = (local >> 1) & 1;
-        if (!mbar_wait_cluster(&sm.acc_empty[b], aph ^ 1, wc)) break;
-        tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * T::BN);
-        for (int kb = 0; kb < kblocks; ++kb, ++it, s = s + 1 == rs ? 0 : s + 1) {
-          const uint32_t o = it & op_mask, oph = (it >> op_log) & 1;
-          // Both CTAs' converters have seen raw stage s full and written
-          // operand stage o.
-          if (!mbar_wait_cluster(&sm.op_full[o], oph, wc)) { ok = false; break; }
+    auto run = [&](auto mode) {
+      using Md = decltype(mode);
+      uint8_t* const op_ring_md = base + Md::RS * T::RAW_STAGE;
+      if (leader && lane == 0) {
+        bool ok = true;
+        uint32_t it = 0, s = 0;  // s: raw stage of it
+        int local = 0;
+        for (int t = cid; t < num_tiles && ok; t += ncl, ++local) {
+          const int b = local & 1;
+          const uint32_t aph = (local >> 1) & 1;
+          if (!mbar_wait_cluster(&sm.acc_empty[b], aph ^ 1, wc)) break;
           tc_fence_after_sync();
-          const uint32_t raw = smem_u32(raw_ring + s * T::RAW_STAGE);
-          const uint32_t op = smem_u32(op_ring + o * op_bytes);
-          const uint32_t a_hi = a_raw ? raw : op + L::A_HI;
-          const uint32_t b_hi = b_raw ? raw + T::TILE : op + b_hi_off;
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * T::BN);
+          for (int kb = 0; kb < kblocks; ++kb, ++it, s = s + 1 == Md::RS ? 0 : s + 1) {
+            const uint32_t o = it & Md::OP_MASK, oph = (it >> Md::OP_LOG) & 1;
+            // Both CTAs' converters have seen raw stage s full and written
+            // operand stage o.
+            if (!mbar_wait_cluster(&sm.op_full[o], oph, wc)) { ok = false; break; }
+            tc_fence_after_sync();
+            const uint32_t raw = smem_u32(raw_ring + s * T::RAW_STAGE);
+            const uint32_t op = smem_u32(op_ring_md + o * Md::OP_BYTES);
+            const uint32_t a_hi = Md::A_RAW ? raw : op + L::A_HI;
+            const uint32_t b_hi = Md::B_RAW ? raw + T::TILE : op + Md::B_HI;
 #pragma unroll
-          for (int kk = 0; kk < T::BK / 8; ++kk) {
-            // K-major, 128-byte rows, 8-row groups 1024 B apart; a K = 8 slice
-            // of tf32 is 32 bytes further along the rows.
-            const uint32_t off = static_cast<uint32_t>(kk * 32);
-            const uint64_t ah = smem_desc_sw128(a_hi + off, 16, 1024);
-            const uint64_t bh = smem_desc_sw128(b_hi + off, 16, 1024);
-            tc_mma_tf32_pair(d_tmem, ah, bh, idesc, (kb | kk) != 0);
-            if (three) {
-              tc_mma_tf32_pair(d_tmem, ah, smem_desc_sw128(op + L::B_LO + off, 16, 1024), idesc,
-                               true);
-              tc_mma_tf32_pair(d_tmem, smem_desc_sw128(op + L::A_LO + off, 16, 1024), bh, idesc,
-                               true);
+            for (int kk = 0; kk < T::BK / 8; ++kk) {
+              // K-major, 128-byte rows, 8-row groups 1024 B apart; a K = 8 slice
+              // of tf32 is 32 bytes further along the rows.
+              const uint32_t off = static_cast<uint32_t>(kk * 32);
+              const uint64_t ah = smem_desc_sw128(a_hi + off, 16, 1024);
+              const uint64_t bh = smem_desc_sw128(b_hi + off, 16, 1024);
+              tc_mma_tf32_pair(d_tmem, ah, bh, idesc, (kb | kk) != 0);
+              if (Md::THREE) {
+                tc_mma_tf32_pair(d_tmem, ah, smem_desc_sw128(op + L::B_LO + off, 16, 1024), idesc,
+                                 true);
+                tc_mma_tf32_pair(d_tmem, smem_desc_sw128(op + L::A_LO + off, 16, 1024), bh, idesc,
+                                 true);
+              }
             }
+            mma_issued = true;
+            tc_commit_pair_multicast(&sm.op_empty[o], 0x3);
+            if (Md::MMA_READS_RAW) tc_commit_pair_multicast(&sm.raw_empty[s], 0x3);
           }
-          mma_issued = true;
-          tc_commit_pair_multicast(&sm.op_empty[o], 0x3);
-          if (mma_reads_raw) tc_commit_pair_multicast(&sm.raw_empty[s], 0x3);
+          if (!ok) break;
+          tc_commit_pair_multicast(&sm.acc_full[b], 0x3);
         }
-        if (!ok) break;
-        tc_commit_pair_multicast(&sm.acc_full[b], 0x3);
       }
-    }
+    };
+    if (three) run(Three{});
+    else run(One{});
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -364,60 +386,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
     }
   } else if (warp < 10) {
     // ------------------------------------------------------------ converters
-    // Thread r handles row r of A and row r of B^T. A raw stage is released
-    // only after the values loaded from it are stored: the stores consume
-    // the loaded registers, so the loads have read the stage before TMA may
-    // refill it (released straight after the loads, it was refilled under
-    // them).
-    const int r = threadIdx.x - 6 * 32;
-    const bool need_a = !a_raw || three;  // a K-major copy of A, or lo(A)
-    const bool need_b = !b_raw || three;
-    uint32_t it = 0, s = 0, ph = 0;  // s, ph: raw stage and phase of it
-    bool ok = true;
-    for (int t = cid; t < num_tiles && ok; t += ncl) {
-      for (int kb = 0; kb < kblocks; ++kb, ++it) {
-        const uint32_t o = it & op_mask, oph = (it >> op_log) & 1;
-        int got = 1;
-        if (lane == 0) got = mbar_wait(&sm.raw_full[s], ph, wc) ? 1 : 0;
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) { ok = false; break; }
-        const uint32_t ra = smem_u32(raw_ring + s * T::RAW_STAGE);
-        const uint32_t rb = ra + T::TILE;
-        float4 va[8], vb[8];
-        if (need_a) {
-          if (kTA) load_mnmajor(ra, r, va);
-          else load_kmajor(ra, r, va);
-        }
-        if (need_b) {
-          if (kTB) load_kmajor(rb, r, vb);
-          else load_mnmajor(rb, r, vb);
-        }
-        if (lane == 0) got = mbar_wait(&sm.op_empty[o], oph ^ 1, wc) ? 1 : 0;
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) { ok = false; break; }
-        const uint32_t op = smem_u32(op_ring + o * op_bytes);
-        if (!a_raw) store_row(op + L::A_HI, r, va);
-        if (three) store_lo_row(op + L::A_LO, r, va);
-        if (!b_raw) store_row(op + b_hi_off, r, vb);
-        if (three) store_lo_row(op + L::B_LO, r, vb);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.raw_empty[s]);
-        // This thread's operand writes -> visible to the MMAs (async proxy).
-        fence_proxy_async_smem();
-        if (three) {
-          // the warp's writes are ordered before lane 0's release arrival on
-          // the leader's barrier (the 3xTF32 MMAs take longer than the
-          // arrival, which stays on this path)
+    auto run = [&](auto mode) {
+      using Md = decltype(mode);
+      uint8_t* const op_ring_md = base + Md::RS * T::RAW_STAGE;
+      // Thread r handles row r of A and row r of B^T. A raw stage is released
+      // only after the values loaded from it are stored: the stores consume
+      // the loaded registers, so the loads have read the stage before TMA may
+      // refill it (released straight after the loads, it was refilled under
+      // them).
+      const int r = threadIdx.x - 6 * 32;
+      constexpr bool need_a = !Md::A_RAW || Md::THREE;  // a K-major copy of A, or lo(A)
+      constexpr bool need_b = !Md::B_RAW || Md::THREE;
+      uint32_t it = 0, s = 0, ph = 0;  // s, ph: raw stage and phase of it
+      bool ok = true;
+      for (int t = cid; t < num_tiles && ok; t += ncl) {
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const uint32_t o = it & Md::OP_MASK, oph = (it >> Md::OP_LOG) & 1;
+          int got = 1;
+          if (lane == 0) got = mbar_wait(&sm.raw_full[s], ph, wc) ? 1 : 0;
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) { ok = false; break; }
+          const uint32_t ra = smem_u32(raw_ring + s * T::RAW_STAGE);
+          const uint32_t rb = ra + T::TILE;
+          float4 va[8], vb[8];
+          if (need_a) {
+            if (kTA) load_mnmajor(ra, r, va);
+            else load_kmajor(ra, r, va);
+          }
+          if (need_b) {
+            if (kTB) load_kmajor(rb, r, vb);
+            else load_mnmajor(rb, r, vb);
+          }
+          if (lane == 0) got = mbar_wait(&sm.op_empty[o], oph ^ 1, wc) ? 1 : 0;
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) { ok = false; break; }
+          const uint32_t op = smem_u32(op_ring_md + o * Md::OP_BYTES);
+          if (!Md::A_RAW) store_row(op + L::A_HI, r, va);
+          if (Md::THREE) store_lo_row(op + L::A_LO, r, va);
+          if (!Md::B_RAW) store_row(op + Md::B_HI, r, vb);
+          if (Md::THREE) store_lo_row(op + L::B_LO, r, vb);
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm.op_full[o]), 0));
-        } else {
-          // released to this CTA's announcer (CTA scope), which forwards the
-          // stage to the leader at cluster scope off this warp's path
-          mbar_arrive(&sm.conv_done[o]);
+          if (lane == 0) mbar_arrive(&sm.raw_empty[s]);
+          // This thread's operand writes -> visible to the MMAs (async proxy).
+          fence_proxy_async_smem();
+          if (Md::THREE) {
+            // the warp's writes are ordered before lane 0's release arrival on
+            // the leader's barrier (the 3xTF32 MMAs take longer than the
+            // arrival, which stays on this path)
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm.op_full[o]), 0));
+          } else {
+            // released to this CTA's announcer (CTA scope), which forwards the
+            // stage to the leader at cluster scope off this warp's path
+            mbar_arrive(&sm.conv_done[o]);
+          }
+          if (++s == Md::RS) { s = 0; ph ^= 1; }
         }
-        if (++s == rs) { s = 0; ph ^= 1; }
       }
-    }
+    };
+    if (three) run(Three{});
+    else run(One{});
   } else {
     // ------------------------------------------------------------ announcer
     // Acquires each operand stage from this CTA's converters and releases it
@@ -430,8 +458,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(T::THREADS, 1)
       const uint32_t uses = static_cast<uint32_t>((num_tiles - cid + ncl - 1) / ncl) *
                             static_cast<uint32_t>(kblocks);  // this CTA's k-blocks
       for (uint32_t it = a; it < uses; it += 2) {
-        const uint32_t o = it & op_mask;
-        if (!mbar_wait(&sm.conv_done[o], (it >> op_log) & 1, wc)) break;
+        const uint32_t o = it & One::OP_MASK;
+        if (!mbar_wait(&sm.conv_done[o], (it >> One::OP_LOG) & 1, wc)) break;
         mbar_arrive_cluster(mapa_shared(smem_u32(&sm.op_full[o]), 0));
       }
     }
