@@ -126,6 +126,25 @@ def test_transposes(oracle_mod, code, ta, tb, M, N, K):
     assert torch.equal(C, run_mode(code, A, B))
 
 
+@pytest.mark.parametrize("code", [TF32, X3])
+def test_more_pair_tiles_than_clusters_every_storage(oracle_mod, code):
+    """90 pair tiles of 256 x 256 (ragged at both edges) on 76 clusters of a
+    152-SM GB300: 14 clusters run a second tile through the rings (TF32: 3 raw
+    and 4 copy stages; 3xTF32: its own layout), each over 11 k-blocks, the last
+    a quarter full. Every storage gives NN's bits; NN's sampled rows are
+    checked against the oracle."""
+    M, N, K = 2500, 2250, 328
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=2718 + code)
+    C = run_mode(code, A, B)
+    g = np.random.default_rng(code)
+    rows = torch.tensor(sorted(set([0, 255, 256, 2303, 2304, M - 1]) |
+                               set(g.integers(0, M, 26).tolist())))
+    check(oracle_mod, A[rows].contiguous(), B, C[rows].contiguous(), TOL["f32"],
+          rounded=code == TF32)
+    for ta, tb in TRANS[1:]:
+        assert torch.equal(run_mode(code, A, B, ta, tb), C), (ta, tb)
+
+
 @pytest.mark.parametrize("code", [X3, TF32])
 @pytest.mark.parametrize("alpha,beta", [(2.5, 0.0), (-1.0, 1.0), (0.5, -2.0)])
 def test_alpha_beta(oracle_mod, code, alpha, beta):
