@@ -80,6 +80,9 @@ def parse_args():
     ap.add_argument("--tf32-only", default=None, metavar="SHAPE:MODE",
                     help="with --table-tf32: one shape (f32_3072 or f32_8192) and one mode "
                          "(fp32, tf32 or 3xtf32), e.g. f32_3072:3xtf32 (for profiling)")
+    ap.add_argument("--tf32-plain", action="store_true",
+                    help="with --table-tf32: call without a workspace (the plain entry "
+                         "points: the fp32 kernel's own loader, the tf32 converter kernel)")
     ap.add_argument("--fma-ceiling", action="store_true",
                     help="measure the FFMA throughput a register-only loop reaches "
                          "(packed and scalar), one JSON line each (not the bench line)")
@@ -1003,10 +1006,11 @@ def run_table_soft(args):
 
 
 def run_table_tf32(args):
-    """fp32 inputs timed alone in each arithmetic: gemm_f32 (FFMA, workspace
-    entry), gemm_tf32_f32acc and gemm_f32_3xtf32 (tensor cores), at the 3072^3
-    workload and at an 8192^3 product of the same distribution (U[-1,1), seed
-    14007). Operand copies rotate over > 2x L2."""
+    """fp32 inputs timed alone in each arithmetic: gemm_f32 (FFMA), gemm_tf32_f32acc
+    and gemm_f32_3xtf32 (tensor cores), at the 3072^3 workload and at an 8192^3
+    product of the same distribution (U[-1,1), seed 14007), each with the
+    workspace it asks for (with --tf32-plain: none). Operand copies rotate over
+    > 2x L2."""
     import torch
 
     import dense_gemm_14_gb300 as g14
@@ -1039,14 +1043,16 @@ def run_table_tf32(args):
             # the workspace each mode asks for with these operands (TF32 on
             # row-major B: room for its K-major copy)
             a0, b0, c0 = sets[0]
-            ws_bytes = g14.workspace_bytes_ex(code, 0, 0, M, N, K, a0.data_ptr(), K, b0.data_ptr(),
-                                              N, c0.data_ptr(), N)
-            ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+            ws_bytes = 0 if args.tf32_plain else g14.workspace_bytes_ex(
+                code, 0, 0, M, N, K, a0.data_ptr(), K, b0.data_ptr(), N, c0.data_ptr(), N)
+            ws = (None if args.tf32_plain else
+                  torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda"))
 
             def launch(i):
                 a, b, c = sets[i % nsets]
                 g14.gemm_ex(code, 0, 0, M, N, K, 1.0, a.data_ptr(), K, b.data_ptr(), N, 0.0,
-                            c.data_ptr(), N, ws.data_ptr(), ws_bytes, stream.cuda_stream)
+                            c.data_ptr(), N, ws.data_ptr() if ws is not None else None,
+                            ws_bytes, stream.cuda_stream)
 
             for i in range(args.warmup):
                 launch(i)
@@ -1071,7 +1077,7 @@ def run_table_tf32(args):
                 # tf32 / bf16 ratio (1.1 / 2.25 PFLOP/s)
                 peak, kind = peaks["bf16_tflops"] * 1.1 / 2.25, "tensor (tf32)"
             print(json.dumps({"workload": name, "mode": mode, "M": M, "N": N, "K": K,
-                              "ms_mean": mean, "ms_median": statistics.median(ms), "ms_min": min(ms), "tflops": tf,
+                              "workspace_bytes": ws_bytes, "ms_mean": mean, "ms_median": statistics.median(ms), "ms_min": min(ms), "tflops": tf,
                               "mma_tflops": mma_flops / (mean / 1e3) / 1e12, "bound": kind,
                               "peak_tflops": peak,
                               "frac_compute": mma_flops / (mean / 1e3) / 1e12 / peak,
