@@ -128,3 +128,15 @@ def test_software_loader_table_shapes_break_tma_rules():
         bc = K if tb else N
         assert (ac + xa) % 8 or (bc + xb) % 8 or (2 * off) % 16, name
         assert min(M, N, K) > 0
+
+
+def test_tf32_table_options_parse(monkeypatch):
+    """--table-tf32 with one shape and mode, without a workspace (the plain
+    entry points), is the command the converter kernel's profile names."""
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--table-tf32", "--tf32-only", "f32_3072:tf32",
+                                      "--tf32-plain", "--steps", "5", "--warmup", "1"])
+    a = bench.parse_args()
+    assert a.table_tf32 and a.tf32_plain and a.tf32_only == "f32_3072:tf32"
+    assert (a.steps, a.warmup) == (5, 1)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--table-tf32"])
+    assert not bench.parse_args().tf32_plain
