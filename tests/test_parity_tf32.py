@@ -18,6 +18,8 @@ pairs) against the oracle:
 
 TF32 is the pages' tensor-core format for fp32 data (gpu-hpc-book ch.06,
 "Tensor Cores" -> "TF32 (TensorFloat-32) 精度")."""
+import random
+
 import numpy as np
 import pytest
 import torch
@@ -423,3 +425,47 @@ def test_pair_kernel_tf32_keeps_padding(oracle_mod, code, M, N, K):
     assert torch.isnan(full[M * ldc:]).all()
     check(oracle_mod, A, B, rows[:, :N].contiguous(), TOL["f32"], 0, 0,
           rounded=code == TF32)
+
+
+TF32_EDGES = [1, 7, 31, 32, 33, 127, 128, 129, 255, 256, 257, 511, 513]
+
+
+def draw_tf32(seed):
+    """One random call of a tf32 mode: sizes near tile and k-block edges or
+    anywhere up to 3000, a stored transpose of either operand, alpha / beta,
+    and a workspace or none (the split-ahead pair kernel or the converter
+    kernel)."""
+    rng = random.Random(seed)
+
+    def dim():
+        r = rng.random()
+        if r < 0.35:
+            return rng.choice(TF32_EDGES)
+        return rng.randint(1, 1500) if r < 0.9 else rng.randint(1500, 3000)
+
+    return dict(code=rng.choice([TF32, X3]), M=dim(), N=dim(), K=dim(), ta=rng.randint(0, 1),
+                tb=rng.randint(0, 1),
+                ab=rng.choice([(1.0, 0.0), (1.0, 0.0), (0.5, 0.0), (1.0, 1.0), (-2.0, 0.25)]),
+                workspace=rng.random() < 0.5)
+
+
+def run_tf32_case(oracle_mod, seed):
+    c = draw_tf32(seed)
+    M, N, K, code = c["M"], c["N"], c["K"], c["code"]
+    alpha, beta = c["ab"]
+    A, B = inputs.make(M, N, K, "f32", "uniform", 1.0, seed=seed)
+    C0 = (torch.rand(M, N, generator=torch.Generator().manual_seed(seed)) * 2 - 1
+          if beta != 0.0 else None)
+    C = run_mode(code, A, B, c["ta"], c["tb"], alpha, beta, C0, workspace=c["workspace"])
+    rows = torch.tensor(sorted(random.Random(seed).sample(range(M), min(M, 24))))
+    check(oracle_mod, A[rows].contiguous(), B, C[rows].contiguous(), TOL["f32"], c["ta"],
+          c["tb"], alpha, beta, C0[rows].contiguous() if C0 is not None else None,
+          rounded=code == TF32)
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_tf32_modes_fuzz_against_oracle(oracle_mod, seed):
+    """48 seeded random calls of the tf32 modes, each on sampled rows against
+    the oracle: 3xTF32 within the fp32 bound of the exact product, TF32 within
+    it of the product of the truncated inputs."""
+    run_tf32_case(oracle_mod, 70000 + seed)
