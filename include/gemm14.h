@@ -360,7 +360,8 @@ typedef struct gemm14_plan {
                      only: 3 = software loader for A and TMA for B, 4 = TMA for
                      A and software loader for B; 0 = none */
   int bm, bn, bk; /* output tile rows x columns, k-block depth */
-  int stages;     /* shared-memory ring depth */
+  int stages;     /* shared-memory ring depth (kernel 4: operand stages the converter
+                     warps fill, 4 for TF32 and 2 for 3xTF32) */
   int threads;    /* threads per CTA */
   int smem_bytes; /* dynamic shared memory per CTA */
   int vec_store;  /* 1 if C takes 16-byte stores */
