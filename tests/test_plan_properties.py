@@ -70,6 +70,10 @@ def test_plan_invariants(dtype, ta, tb, M, N, K, a_al, b_al, xa, xb, oa, ob, xc,
             assert M > 128 and N > 128 and p.threads == 192
         if p.kernel == 5:
             assert dtype == TF32 and not ta and tb
+        if p.kernel == 4:
+            # TF32: two announcer warps, 4 operand stages of copies; 3xTF32:
+            # its converters announce themselves, 2 operand stages
+            assert (p.threads, p.stages) == ((384, 4) if dtype == TF32 else (320, 2))
     else:  # kernel 2: one SM per tile, each operand by TMA where it can be
         assert p.bm in (64, 128) and p.bn in (64, 128, 256) and p.bk == 64
         assert p.grid == min(p.tiles, sms)
