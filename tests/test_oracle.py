@@ -371,3 +371,57 @@ def test_truncate_tf32_matches_exact_rational_truncation(oracle_mod):
     # a quiet NaN stays NaN; truncation never moves a value away from zero
     assert np.isnan(oracle_mod.truncate_tf32(np.array([[np.nan]], np.float32))[0, 0])
     assert (np.abs(got) <= np.abs(x[0])).all()
+
+
+# 3xTF32 (reading R14: the split of Ootomo and Yokota, 2022): x = hi + lo with
+# hi = tf32(x) and lo = x - hi, and A B ~ hi(A) hi(B) + hi(A) lo(B) + lo(A) hi(B).
+# The bound the kernels are held to rests on the split being exact, lo being
+# below 2^-10 |x|, and the dropped and truncated terms each staying below
+# 2^-20 |a||b| per product; these pins check those facts on the oracle's
+# truncation and its products.
+
+def _split(oracle_mod, X):
+    hi = oracle_mod.truncate_tf32(X)
+    return hi, (X - hi).astype(np.float32)
+
+
+def test_tf32_split_is_exact_and_lo_is_small(oracle_mod):
+    g = np.random.default_rng(62)
+    x = (g.standard_normal(20000) * np.exp2(g.integers(-60, 61, 20000))).astype(np.float32)
+    x = x.reshape(1, -1)
+    hi, lo = _split(oracle_mod, x)
+    # the fp32 subtraction is exact: hi + lo is x, compared in float64
+    assert np.array_equal(hi.astype(np.float64) + lo.astype(np.float64), x.astype(np.float64))
+    # lo is below 2^-10 |x| (normal x: 10 fraction bits kept), with x's sign or zero
+    assert (np.abs(lo) < np.abs(x) * 2.0 ** -10).all()
+    assert ((lo == 0) | (np.sign(lo) == np.sign(x))).all()
+    # truncation is idempotent and hi is already a tf32 value
+    assert np.array_equal(oracle_mod.truncate_tf32(hi), hi)
+
+
+def test_3xtf32_terms_against_the_exact_product(oracle_mod):
+    """The three-term sum misses the exact product of the fp32 inputs by the
+    dropped lo(A) lo(B) term alone, below 2^-20 (|A||B|); reading each lo part
+    as tf32 too (the tensor cores' reading) stays below 3 * 2^-20 (|A||B|),
+    the bound the fp32 tolerance 1e-5 covers."""
+    g = np.random.default_rng(63)
+    A = (g.random((48, 96)) * 2 - 1).astype(np.float32)
+    B = (g.random((96, 40)) * 2 - 1).astype(np.float32)
+    hA, lA = _split(oracle_mod, A)
+    hB, lB = _split(oracle_mod, B)
+    exact, absAB = oracle_mod.gemm(A, B)
+    hh, _ = oracle_mod.gemm(hA, hB)
+    hl, _ = oracle_mod.gemm(hA, lB)
+    lh, _ = oracle_mod.gemm(lA, hB)
+    ll, _ = oracle_mod.gemm(lA, lB)
+    slack = 1e-12 * absAB  # the oracle's own float64 sums
+    # exact split: the four terms give the product
+    assert (np.abs(hh + hl + lh + ll - exact) <= slack).all()
+    err3 = np.abs(hh + hl + lh - exact)
+    assert (err3 <= 2.0 ** -20 * absAB + slack).all()
+    assert err3.max() > 0  # the dropped term is not always zero
+    tl, _ = oracle_mod.gemm(hA, oracle_mod.truncate_tf32(lB))
+    lt, _ = oracle_mod.gemm(oracle_mod.truncate_tf32(lA), hB)
+    assert (np.abs(hh + tl + lt - exact) <= 3 * 2.0 ** -20 * absAB + slack).all()
+    # and a single tf32 product is far outside that bound somewhere
+    assert (np.abs(hh - exact) > 3 * 2.0 ** -20 * absAB).any()
